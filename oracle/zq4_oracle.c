@@ -1,0 +1,356 @@
+/*
+ * zq4_oracle.c -- plain, slow, fp64 CPU oracle for the q4f16_1 fused
+ * dequantize + NT matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load this file's library. The product path
+ * (the CUDA library) never calls it, and the two share no code.
+ *
+ * Every function follows one passage of the pages it was written from:
+ *
+ *  [DOC-Q4]  "Zero TVM Documentation", section "Q4F16 quantization format":
+ *            8 unsigned 4-bit codes per uint32, element i of a word is
+ *            (word >> 4i) & 0xF, one f16 scale per 32 weights,
+ *            value = (code - 7) * scale.
+ *  [DOC-MM]  "Zero TVM Documentation", section "WGSL Kernel Roles", card 5
+ *            "int4 Matmul": output row n is the dot product of the input
+ *            vector with dequantized row n; K_groups = K/8 words per row,
+ *            scale_stride = K/32 scales per row.
+ *  [DOC-FFN] same page, card 6 "Fused FFN": gate and up projections share one
+ *            2*I-row matrix, followed by SiLU and an elementwise multiply.
+ *  [RES-TVM] "RESEARCH.md" (Zero-TVM), section "TVM Already Fuses Elementwise
+ *            Operations" (fused_dequantize + NT_matmul; split + SiLU +
+ *            multiply) and "Matmul Shader Analysis" (one output element is a
+ *            dot product over all K of input * (code - 7) * group scale).
+ *  [BENCH-MOE] "Zero-TVM benchmarks" (BENCH.md), section "MoE chunked
+ *            prefill": per (token, slot) the expert index comes from the
+ *            routing ids, experts never mix tokens, and a combine sums the
+ *            slots of one token weighted by the router scores.
+ *
+ * Readings where the pages are silent (the same list is kept with the design
+ * notes): SiLU(z) = z / (1 + e^-z); gate/up "interleaved" layout puts gate row
+ * j at row 2j and up row j at row 2j+1, "concatenated" puts gate rows first;
+ * an expert id outside [0, E) contributes nothing and is counted.
+ *
+ * Arithmetic is IEEE fp64 throughout. The dequantized weight (q-7)*s is exact
+ * in fp64 (4-bit integer times an 11-bit significand). Sums are taken in
+ * plain ascending k order; S = sum |x*w| is returned beside every dot product
+ * because the parity tolerance is |y - y_ref| <= 2^-10 |y_ref| + 1e-4 S.
+ *
+ * Parallelism: when built with OpenMP, independent output elements are
+ * spread over threads; no sum is split or reordered.
+ *
+ * Mutants: building with -DZO_MUTANT=<n> plants one deliberate mistake so
+ * that the tests can show their pins catch it. The normal build has none.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ZO_MUTANT
+#define ZO_MUTANT 0
+#endif
+
+/* Upper bound of the k loops of the dot products (mutant 4 drops the last term). */
+#if ZO_MUTANT == 4
+#define ZO_KEND(K) ((K) - 1)
+#else
+#define ZO_KEND(K) (K)
+#endif
+
+/* ---------------------------------------------------------------------- */
+/* IEEE 754 binary16 <-> binary64, written from the format's definition:   */
+/* 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 is   */
+/* zero/subnormal (value = frac * 2^-24), exponent 31 is inf/NaN.           */
+/* ---------------------------------------------------------------------- */
+
+double zo_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* Round half to even of a non-negative double to an integer-valued double. */
+static double zo_round_half_even(double r)
+{
+    double fl = floor(r);
+    double diff = r - fl;
+    if (diff > 0.5) return fl + 1.0;
+    if (diff < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+uint16_t zo_f64_to_f16_rn(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return 0x7E00;
+    if (isinf(a)) return sign | 0x7C00;
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);            /* a = m * 2^E, m in [0.5, 1) */
+    int e = E - 1;           /* a in [2^e, 2^(e+1)) */
+    if (e < -14) {           /* subnormal range: quantum 2^-24 */
+        double n = zo_round_half_even(ldexp(a, 24));
+        return sign | (uint16_t)n;      /* n == 1024 encodes 2^-14 exactly */
+    }
+    double n = zo_round_half_even(ldexp(a, 10 - e));   /* in [1024, 2048] */
+    if (n == 2048.0) { n = 1024.0; e += 1; }
+    if (e + 15 >= 31) return sign | 0x7C00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)n - 1024));
+}
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-Q4] code of element k of row n: word k/8 of the row, nibble k%8,    */
+/* least significant nibble first.                                         */
+/* ---------------------------------------------------------------------- */
+int zo_code(const uint32_t *wq, int64_t K, int64_t n, int64_t k)
+{
+    uint32_t word = wq[n * (K / 8) + k / 8];
+#if ZO_MUTANT == 1
+    int i = 7 - (int)(k % 8);          /* mutant: most significant nibble first */
+#else
+    int i = (int)(k % 8);
+#endif
+    return (int)((word >> (4 * i)) & 0xFu);
+}
+
+/* [DOC-Q4] w[n,k] = (q[n,k] - 7) * s[n, k/32], exact in fp64. */
+double zo_weight(const uint32_t *wq, const uint16_t *scales, int64_t K, int64_t n, int64_t k)
+{
+    int q = zo_code(wq, K, n, k);
+    int64_t g = k / 32;
+#if ZO_MUTANT == 3
+    g = (g + 1) % (K / 32);            /* mutant: scale index off by one group */
+#endif
+    double s = zo_f16_to_f64(scales[n * (K / 32) + g]);
+#if ZO_MUTANT == 2
+    return (double)(q - 8) * s;        /* mutant: zero point 8 */
+#else
+    return (double)(q - 7) * s;
+#endif
+}
+
+/* Dequantized row n into w[0..K). */
+static void zo_dequant_row(const uint32_t *wq, const uint16_t *scales, int64_t K, int64_t n, double *w)
+{
+    for (int64_t k = 0; k < K; ++k) w[k] = zo_weight(wq, scales, K, n, k);
+}
+
+/* [DOC-Q4] whole matrix, w[n*K + k]. */
+void zo_dequant(const uint32_t *wq, const uint16_t *scales, int64_t N, int64_t K, double *w)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) zo_dequant_row(wq, scales, K, n, w + n * K);
+}
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-MM], [RES-TVM]: y[m,n] = sum_k x[m,k] * w[n,k] (NT matmul: both     */
+/* operands are stored with K innermost). Also S[m,n] = sum_k |x*w|.        */
+/* rows == NULL computes every n; otherwise only the n listed in rows[0..R) */
+/* (outputs are then [M, R]).                                               */
+/* ---------------------------------------------------------------------- */
+void zo_gemv_rows(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                  int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t R,
+                  double *y, double *S)
+{
+    int64_t count = rows ? R : N;
+    #pragma omp parallel
+    {
+        double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < count; ++i) {
+            int64_t n = rows ? rows[i] : i;
+            zo_dequant_row(wq, scales, K, n, w);
+            for (int64_t m = 0; m < M; ++m) {
+                double acc = 0.0, sabs = 0.0;
+                for (int64_t k = 0; k < ZO_KEND(K); ++k) {
+                    double p = zo_f16_to_f64(x[m * K + k]) * w[k];
+                    acc += p;
+                    sabs += fabs(p);
+                }
+                y[m * count + i] = acc;
+                S[m * count + i] = sabs;
+            }
+        }
+        free(w);
+    }
+}
+
+void zo_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+             int64_t M, int64_t N, int64_t K, double *y, double *S)
+{
+    zo_gemv_rows(wq, scales, x, M, N, K, NULL, 0, y, S);
+}
+
+/* ---------------------------------------------------------------------- */
+/* SiLU, the activation of the gated FFN ([DOC-FFN]; the pages name it but  */
+/* do not define it): silu(z) = z * sigmoid(z) = z / (1 + e^-z).            */
+/* ---------------------------------------------------------------------- */
+double zo_silu(double z)
+{
+#if ZO_MUTANT == 5
+    return z / (1.0 + exp(z));         /* mutant: sign error in the sigmoid */
+#else
+    return z / (1.0 + exp(-z));
+#endif
+}
+
+/* d silu / dz = sigmoid(z) * (1 + z * (1 - sigmoid(z))), used only for the
+ * first-order error propagation of the gate_up tolerance. */
+double zo_silu_deriv(double z)
+{
+    double sg = 1.0 / (1.0 + exp(-z));
+    return sg * (1.0 + z * (1.0 - sg));
+}
+
+/* Row of gate j and of up j under the two layouts of a 2*I-row matrix. */
+static int64_t zo_gate_row(int64_t j, int64_t I, int interleaved) { return interleaved ? 2 * j : j; }
+static int64_t zo_up_row(int64_t j, int64_t I, int interleaved) { return interleaved ? 2 * j + 1 : I + j; }
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-FFN], [RES-TVM]: h[m,j] = silu(g[m,j]) * u[m,j] where g and u are   */
+/* the GEMV outputs of gate row j and up row j of the shared N2 = 2I-row    */
+/* matrix. Also returns g, u, S_g, S_u and the propagated tolerance scale   */
+/* Sh = |silu'(g) u| S_g + |silu(g)| S_u.                                   */
+/* Any of the optional outputs may be NULL.                                 */
+/* ---------------------------------------------------------------------- */
+void zo_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                     int64_t M, int64_t N2, int64_t K, int interleaved,
+                     double *h, double *Sh, double *g_out, double *u_out,
+                     double *Sg_out, double *Su_out)
+{
+    int64_t I = N2 / 2;
+    #pragma omp parallel
+    {
+        double *wg = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        double *wu = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t j = 0; j < I; ++j) {
+            zo_dequant_row(wq, scales, K, zo_gate_row(j, I, interleaved), wg);
+            zo_dequant_row(wq, scales, K, zo_up_row(j, I, interleaved), wu);
+            for (int64_t m = 0; m < M; ++m) {
+                double g = 0, u = 0, sg = 0, su = 0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double xv = zo_f16_to_f64(x[m * K + k]);
+                    double pg = xv * wg[k], pu = xv * wu[k];
+                    g += pg; u += pu; sg += fabs(pg); su += fabs(pu);
+                }
+                int64_t o = m * I + j;
+                double a = zo_silu(g);
+                h[o] = a * u;
+                if (Sh) Sh[o] = fabs(zo_silu_deriv(g) * u) * sg + fabs(a) * su;
+                if (g_out) g_out[o] = g;
+                if (u_out) u_out[o] = u;
+                if (Sg_out) Sg_out[o] = sg;
+                if (Su_out) Su_out[o] = su;
+            }
+        }
+        free(wg);
+        free(wu);
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* [BENCH-MOE] expert gate_up stage. Expert e's matrix starts at word        */
+/* e * N2 * K/8 and scale e * N2 * K/32. For token t and slot j the expert  */
+/* is ids[t*top_k + j]; h[(t*top_k + j)*I + i] = silu(g) * u of that expert */
+/* on x[t]. An id outside [0, E) gives h = 0, Sh = 0 and is counted in the  */
+/* return value.                                                            */
+/* ---------------------------------------------------------------------- */
+int64_t zo_moe_gate_up(const uint32_t *wq_bank, const uint16_t *sc_bank, int64_t E,
+                       const uint16_t *x, int64_t T, int64_t N2, int64_t K,
+                       const int32_t *ids, int64_t top_k, int interleaved,
+                       double *h, double *Sh)
+{
+    int64_t I = N2 / 2, bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            double *ho = h + (t * top_k + j) * I;
+            double *so = Sh ? Sh + (t * top_k + j) * I : NULL;
+            if (e < 0 || e >= E) {
+                ++bad;
+                for (int64_t i = 0; i < I; ++i) { ho[i] = 0.0; if (so) so[i] = 0.0; }
+                continue;
+            }
+            zo_gate_up_silu(wq_bank + e * N2 * (K / 8), sc_bank + e * N2 * (K / 32),
+                            x + t * K, 1, N2, K, interleaved, ho, so, NULL, NULL, NULL, NULL);
+        }
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------- */
+/* [BENCH-MOE] expert down stage + combine: for token t,                    */
+/*   y[t,n] = sum_j r[t,j] * z[t,j,n],  z[t,j,n] = sum_k h[t,j,k] w_e[n,k]  */
+/* with e = ids[t,j]; S[t,n] = sum_j |r[t,j]| * sum_k |h w|. h is f16 [T,   */
+/* top_k, K]; r is float32 [T, top_k]. Invalid ids contribute nothing and   */
+/* are counted in the return value.                                         */
+/* ---------------------------------------------------------------------- */
+int64_t zo_moe_down_combine(const uint32_t *wq_bank, const uint16_t *sc_bank, int64_t E,
+                            const uint16_t *h, const float *r, int64_t T, int64_t N, int64_t K,
+                            const int32_t *ids, int64_t top_k, double *y, double *S)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            if (e < 0 || e >= E) ++bad;
+        }
+    #pragma omp parallel
+    {
+        double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t t = 0; t < T; ++t) {
+                double acc = 0.0, sabs = 0.0;
+                for (int64_t j = 0; j < top_k; ++j) {
+                    int64_t e = ids[t * top_k + j];
+                    if (e < 0 || e >= E) continue;
+                    zo_dequant_row(wq_bank + e * N * (K / 8), sc_bank + e * N * (K / 32), K, n, w);
+                    const uint16_t *hv = h + (t * top_k + j) * K;
+                    double z = 0.0, sz = 0.0;
+                    for (int64_t k = 0; k < K; ++k) {
+                        double p = zo_f16_to_f64(hv[k]) * w[k];
+                        z += p;
+                        sz += fabs(p);
+                    }
+                    double rj = (double)r[t * top_k + j];
+                    acc += rj * z;
+                    sabs += fabs(rj) * sz;
+                }
+                y[t * N + n] = acc;
+                S[t * N + n] = sabs;
+            }
+        }
+        free(w);
+    }
+    return bad;
+}
+
+/* Threads the OpenMP regions above use (1 without OpenMP). */
+int zo_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int zo_mutant(void) { return ZO_MUTANT; }

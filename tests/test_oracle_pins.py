@@ -1,0 +1,348 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+Each pin is chosen so that a plausible mistake in the oracle (nibble order,
+zero point, scale index, a transposed operand, a dropped term, a sign) fails
+at least one of them; ``test_mutants_are_caught`` plants such mistakes in the
+oracle (compile-time mutants, CPU only) and checks that they are caught.
+"""
+from fractions import Fraction
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as oracle_mod
+from int4_weight_only_q4f16_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                out.append(line.split())
+    return out
+
+
+def pack_codes(codes: np.ndarray) -> np.ndarray:
+    """Pack codes [N, K] (0..15) into words [N, K/8], element i of a word in
+    bits 4i..4i+3 (the packing the docs page's extraction rule inverts)."""
+    N, K = codes.shape
+    c = codes.reshape(N, K // 8, 8).astype(np.uint64)
+    words = np.zeros((N, K // 8), dtype=np.uint64)
+    for i in range(8):
+        words |= c[:, :, i] << np.uint64(4 * i)
+    return words.astype(np.uint32)
+
+
+def codes_by_hex(word: int):
+    """Independent route to a word's codes: its 8-digit hex string read from
+    the right (element 0 is the last hex digit)."""
+    s = "%08x" % (word & 0xFFFFFFFF)
+    return [int(s[7 - i], 16) for i in range(8)]
+
+
+# --------------------------------------------------------------------------
+# binary16 conversions against numpy's (a library routine)
+# --------------------------------------------------------------------------
+def test_f16_decode_all_patterns(oracle):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, oracle.f16_to_f64(0x8000)) == -1.0
+
+
+def test_f16_encode_round_to_nearest_even(oracle):
+    rng = np.random.default_rng(7)
+    vals = np.concatenate([
+        rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 5, 4000),
+        # exact ties between adjacent f16 values, normal and subnormal
+        (np.arange(1024, 1100) + 0.5) * 2.0 ** -10,
+        (np.arange(0, 60) + 0.5) * 2.0 ** -24,
+        [65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -25, 2.0 ** -26, -2.0 ** -25,
+         3 * 2.0 ** -26, 0.0, -0.0, 6.1e-5, 2.0 ** -14 - 2.0 ** -25],
+    ])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16)
+    got = oracle.round_f16(vals)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+
+
+# --------------------------------------------------------------------------
+# the format, from the golden fixtures
+# --------------------------------------------------------------------------
+def test_nibble_order_golden(oracle):
+    for row in _rows("nibble_order.txt"):
+        word = int(row[0], 16)
+        want = [int(v) for v in row[1:]]
+        wq = np.array([[word]], dtype=np.uint32)
+        got = [oracle.code(wq, 8, 0, k) for k in range(8)]
+        assert got == want, hex(word)
+        assert codes_by_hex(word) == want
+
+
+def test_dequant_golden(oracle):
+    for code, sbits, sdec, want in _rows("dequant_values.txt"):
+        code, sbits = int(code), int(sbits, 16)
+        assert oracle.f16_to_f64(sbits) == float(sdec)
+        K = 32
+        wq = pack_codes(np.full((1, K), code, dtype=np.int64))
+        sc = np.array([[sbits]], dtype=np.uint16).view(np.float16)
+        w = oracle.dequant(wq, sc, 1, K)
+        assert np.all(w == float(want)), (code, hex(sbits))
+
+
+def test_pack_unpack_round_trip(oracle):
+    rng = np.random.default_rng(1)
+    N, K = 5, 96
+    codes = rng.integers(0, 16, (N, K))
+    wq = pack_codes(codes)
+    for n in range(N):
+        for k in range(K):
+            assert oracle.code(wq, K, n, k) == codes[n, k]
+    # and the independent hex-digit route agrees with the packing
+    for n in range(N):
+        flat = sum((codes_by_hex(int(w)) for w in wq[n]), [])
+        assert flat == list(codes[n])
+
+
+# --------------------------------------------------------------------------
+# GEMV: one-hot columns, closed form, brute force, linearity
+# --------------------------------------------------------------------------
+def _patterned(N, K, seed=3):
+    """codes q[n,k] = (n + 3k) mod 16 and distinct scales per (n, group)."""
+    n = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    codes = (n + 3 * k) % 16
+    rng = np.random.default_rng(seed)
+    sc = (rng.random((N, K // 32)) * 0.9 + 0.05).astype(np.float16)
+    return codes, pack_codes(codes), sc
+
+
+def test_one_hot_columns_exact(oracle):
+    """x = e_k must return exactly column k of the dequantized matrix; N != K
+    so that a transposed operand cannot pass."""
+    N, K = 12, 96
+    codes, wq, sc = _patterned(N, K)
+    for k in range(K):
+        x = np.zeros((1, K), dtype=np.float16)
+        x[0, k] = 1.0
+        y, S = oracle.gemv(wq, sc, x, N, K)
+        want = (codes[:, k] - 7) * sc[:, k // 32].astype(np.float64)
+        assert np.array_equal(y[0], want), k
+        assert np.array_equal(S[0], np.abs(want))
+
+
+def test_closed_form_constant_codes(oracle):
+    """All codes c and all scales s: y = (c - 7) * s * sum_k x_k."""
+    rng = np.random.default_rng(11)
+    N, K = 4, 256
+    x = synth.activations(rng, 3, K)
+    xs = x.astype(np.float64).sum(axis=1)
+    for c in range(16):
+        wq = np.full((N, K // 8), c * 0x11111111, dtype=np.uint32)
+        for s in (0.5, 0.0137, 6.0e-8, 0.0):
+            sc = np.full((N, K // 32), s, dtype=np.float16)
+            sv = float(sc[0, 0])
+            y, S = oracle.gemv(wq, sc, x, N, K)
+            want = (c - 7) * sv * xs
+            assert np.allclose(y, want[:, None], rtol=0, atol=1e-12 * max(1.0, np.abs(S).max()))
+            if c == 7 or sv == 0.0:
+                assert np.all(y == 0.0)
+
+
+def test_brute_force_exact_rationals(oracle):
+    """2 x 64 activations against 4 x 64 weights in exact rational arithmetic,
+    codes read through the hex-digit route, values through Fraction(float)."""
+    rng = np.random.default_rng(5)
+    M, N, K = 2, 4, 64
+    wq = synth.packed_codes(rng, N, K)
+    sc = synth.group_scales(rng, N, K)
+    x = synth.activations(rng, M, K)
+    y, S = oracle.gemv(wq, sc, x, N, K)
+    for n in range(N):
+        codes = sum((codes_by_hex(int(w)) for w in wq[n]), [])
+        wrow = [(codes[k] - 7) * Fraction(float(sc[n, k // 32])) for k in range(K)]
+        for m in range(M):
+            exact = sum(Fraction(float(x[m, k])) * wrow[k] for k in range(K))
+            sabs = sum(abs(Fraction(float(x[m, k])) * wrow[k]) for k in range(K))
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(1, 10 ** 12) * sabs
+            assert abs(Fraction(S[m, n]) - sabs) <= Fraction(1, 10 ** 12) * sabs
+
+
+def test_linearity_power_of_two(oracle):
+    rng = np.random.default_rng(9)
+    N, K = 16, 128
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x = synth.activations(rng, 2, K)
+    y1, _ = oracle.gemv(wq, sc, x, N, K)
+    y2, _ = oracle.gemv(wq, sc, (x.astype(np.float32) * 2).astype(np.float16), N, K)
+    assert np.array_equal(y2, 2 * y1)
+
+
+def test_row_subset_matches_full(oracle):
+    rng = np.random.default_rng(2)
+    N, K = 40, 160
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x = synth.activations(rng, 3, K)
+    y, S = oracle.gemv(wq, sc, x, N, K)
+    rows = np.array([0, 39, 7, 7, 21])
+    ys, Ss = oracle.gemv(wq, sc, x, N, K, rows=rows)
+    assert np.array_equal(ys, y[:, rows]) and np.array_equal(Ss, S[:, rows])
+
+
+# --------------------------------------------------------------------------
+# SiLU and the gate_up epilogue
+# --------------------------------------------------------------------------
+def test_silu_values(oracle):
+    assert oracle.silu(0.0) == 0.0
+    # sigmoid(1) = 1 / (1 + 1/e)
+    assert abs(oracle.silu(1.0) - 0.7310585786300049) < 1e-15
+    for z in (0.3, 1.7, 5.0, 20.0):
+        # silu(z) - silu(-z) = z (sigma(z) + sigma(-z) = 1)
+        assert abs(oracle.silu(z) - oracle.silu(-z) - z) < 1e-12 * max(1.0, z)
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12
+    assert abs(oracle.silu(-40.0)) < 1e-15
+    lib = oracle.lib
+    for z in (-3.0, -0.5, 0.0, 0.8, 4.0):
+        fd = (oracle.silu(z + 1e-6) - oracle.silu(z - 1e-6)) / 2e-6
+        assert abs(lib.zo_silu_deriv(z) - fd) < 1e-8
+
+
+def test_gate_up_equals_two_gemvs(oracle):
+    rng = np.random.default_rng(4)
+    I, K, M = 24, 96, 3
+    wq, sc = synth.packed_codes(rng, 2 * I, K), synth.group_scales(rng, 2 * I, K)
+    x = synth.activations(rng, M, K)
+    h, Sh, g, u, Sg, Su = oracle.gate_up_silu(wq, sc, x, 2 * I, K, True, parts=True)
+    gy, gS = oracle.gemv(wq[0::2], sc[0::2], x, I, K)
+    uy, uS = oracle.gemv(wq[1::2], sc[1::2], x, I, K)
+    assert np.array_equal(g, gy) and np.array_equal(u, uy)
+    assert np.array_equal(Sg, gS) and np.array_equal(Su, uS)
+    want = np.vectorize(oracle.silu)(gy) * uy
+    assert np.array_equal(h, want)
+    # concatenated layout [gate; up] computes the same thing
+    wq_c = np.concatenate([wq[0::2], wq[1::2]])
+    sc_c = np.concatenate([sc[0::2], sc[1::2]])
+    hc, Shc = oracle.gate_up_silu(wq_c, sc_c, x, 2 * I, K, False)
+    assert np.array_equal(hc, h) and np.array_equal(Shc, Sh)
+
+
+def test_gate_up_brute_force(oracle):
+    """gate_up on one row pair in exact rationals (SiLU through math.exp)."""
+    rng = np.random.default_rng(12)
+    K = 64
+    wq, sc = synth.packed_codes(rng, 2, K), synth.group_scales(rng, 2, K)
+    x = synth.activations(rng, 1, K)
+    h, _ = oracle.gate_up_silu(wq, sc, x, 2, K, True)
+    vals = []
+    for n in range(2):
+        codes = sum((codes_by_hex(int(w)) for w in wq[n]), [])
+        vals.append(sum(Fraction(float(x[0, k])) * (codes[k] - 7) * Fraction(float(sc[n, k // 32]))
+                        for k in range(K)))
+    g, u = float(vals[0]), float(vals[1])
+    want = g / (1 + math.exp(-g)) * u
+    assert abs(h[0, 0] - want) <= 1e-13 * max(1.0, abs(want))
+
+
+# --------------------------------------------------------------------------
+# MoE
+# --------------------------------------------------------------------------
+def _bank(rng, E, N, K):
+    return synth.packed_codes(rng, E * N, K), synth.group_scales(rng, E * N, K)
+
+
+def test_moe_single_slot_is_plain_gemv(oracle):
+    rng = np.random.default_rng(21)
+    E, I, K, N = 6, 32, 64, 40
+    gq, gs = _bank(rng, E, 2 * I, K)
+    dq, ds = _bank(rng, E, N, I)
+    T = 3
+    x = synth.activations(rng, T, K)
+    ids = np.array([[4], [0], [5]], dtype=np.int32)
+    h, Sh, bad = oracle.moe_gate_up(gq, gs, E, x, 2 * I, K, ids)
+    assert bad == 0
+    for t in range(T):
+        e = ids[t, 0]
+        hr, Shr = oracle.gate_up_silu(gq[e * 2 * I:(e + 1) * 2 * I], gs[e * 2 * I:(e + 1) * 2 * I],
+                                      x[t:t + 1], 2 * I, K, True)
+        assert np.array_equal(h[t, 0], hr[0]) and np.array_equal(Sh[t, 0], Shr[0])
+    hf = h.astype(np.float16)
+    r = np.ones((T, 1), dtype=np.float32)
+    y, S, bad = oracle.moe_down_combine(dq, ds, E, hf, r, N, I, ids)
+    assert bad == 0
+    for t in range(T):
+        e = ids[t, 0]
+        yr, Sr = oracle.gemv(dq[e * N:(e + 1) * N], ds[e * N:(e + 1) * N], hf[t, 0][None], N, I)
+        assert np.array_equal(y[t], yr[0]) and np.array_equal(S[t], Sr[0])
+
+
+def test_moe_combine_weighted_sum_and_slot_permutation(oracle):
+    rng = np.random.default_rng(22)
+    E, N, K, T, top_k = 10, 24, 64, 4, 3
+    dq, ds = _bank(rng, E, N, K)
+    h = synth.activations(rng, T * top_k, K).reshape(T, top_k, K)
+    ids, r = synth.routing(rng, T, E, top_k)
+    y, S, bad = oracle.moe_down_combine(dq, ds, E, h, r, N, K, ids)
+    assert bad == 0
+    for t in range(T):
+        acc = np.zeros(N)
+        for j in range(top_k):
+            e = ids[t, j]
+            z, _ = oracle.gemv(dq[e * N:(e + 1) * N], ds[e * N:(e + 1) * N], h[t, j][None], N, K)
+            acc += float(r[t, j]) * z[0]
+        assert np.allclose(y[t], acc, rtol=0, atol=1e-13 * S[t].max())
+    perm = np.array([2, 0, 1])
+    y2, S2, _ = oracle.moe_down_combine(dq, ds, E, h[:, perm], r[:, perm], N, K, ids[:, perm])
+    assert np.allclose(y2, y, rtol=0, atol=1e-13 * S.max())
+
+
+def test_moe_invalid_ids_contribute_nothing(oracle):
+    rng = np.random.default_rng(23)
+    E, N, K, T = 4, 8, 32, 2
+    dq, ds = _bank(rng, E, N, K)
+    h = synth.activations(rng, T * 2, K).reshape(T, 2, K)
+    ids = np.array([[1, 7], [-1, 2]], dtype=np.int32)
+    r = np.full((T, 2), 0.5, dtype=np.float32)
+    y, S, bad = oracle.moe_down_combine(dq, ds, E, h, r, N, K, ids)
+    assert bad == 2
+    ids_ok = np.array([[1, 1], [2, 2]], dtype=np.int32)
+    r_ok = np.array([[0.5, 0.0], [0.0, 0.5]], dtype=np.float32)
+    y2, _, _ = oracle.moe_down_combine(dq, ds, E, h, r_ok, N, K, ids_ok)
+    assert np.array_equal(y, y2)
+
+
+# --------------------------------------------------------------------------
+# the pins must be able to fail: mutants planted in the oracle (CPU only)
+# --------------------------------------------------------------------------
+def _pins_pass(o) -> bool:
+    try:
+        test_nibble_order_golden(o)
+        test_one_hot_columns_exact(o)
+        test_brute_force_exact_rationals(o)
+        test_closed_form_constant_codes(o)
+        test_silu_values(o)
+        test_gate_up_brute_force(o)
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_mutants_are_caught(mutant):
+    o = oracle_mod.Oracle(mutant)
+    assert o.lib.zo_mutant() == mutant
+    assert not _pins_pass(o)
+
+
+def test_real_oracle_passes_mutant_harness(oracle):
+    assert oracle.lib.zo_mutant() == 0
+    assert _pins_pass(oracle)

@@ -1,0 +1,60 @@
+"""The workload shapes and byte counts the benchmark uses, pinned to the
+Phi-3-mini weight table of the Zero TVM docs page (CPU only)."""
+import os
+
+import numpy as np
+
+from int4_weight_only_q4f16_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _table():
+    rows, extra = {}, {}
+    with open(os.path.join(GOLDEN, "phi3_weight_shapes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) == 5:
+                rows[line[0]] = tuple(int(v) for v in line[1:])
+            elif len(line) == 2:
+                extra[line[0]] = float(line[1])
+    return rows, extra
+
+
+def test_phi3_shapes_match_weight_table():
+    rows, extra = _table()
+    for name, N, K in synth.PHI3_LAYER + (synth.PHI3_LM_HEAD,):
+        n, words, scales, per_layer = rows[name]
+        assert (N, K // 8, K // 32) == (n, words, scales)
+        assert per_layer == (0 if name == "lm_head" else 1)
+    assert synth.PHI3_LAYERS == int(extra["layers"])
+
+
+def test_phi3_bytes_per_token_about_2_09_gb():
+    rows, extra = _table()
+    total = 0
+    for name, (n, words, scales, per_layer) in rows.items():
+        b = n * (4 * words + 2 * scales)
+        total += b * (int(extra["layers"]) if per_layer else 1)
+    assert total == 2_093_838_336
+    assert abs(total / 1e9 - extra["approx_total_gb"]) < 0.005
+
+
+def test_generator_shapes_and_ranges():
+    rng = synth.rng_for("t", 1)
+    wq = synth.packed_codes(rng, 7, 96)
+    sc = synth.group_scales(rng, 7, 96)
+    x = synth.activations(rng, 3, 96)
+    assert wq.shape == (7, 12) and wq.dtype == np.uint32
+    assert sc.shape == (7, 3) and sc.dtype == np.float16 and np.all(sc >= 0)
+    assert x.shape == (3, 96) and x.dtype == np.float16
+    ids, r = synth.routing(rng, 5, 128, 8)
+    assert ids.shape == (5, 8) and r.shape == (5, 8)
+    for t in range(5):
+        assert len(set(ids[t])) == 8 and ids[t].min() >= 0 and ids[t].max() < 128
+    assert np.allclose(r.sum(axis=1), 1.0, atol=1e-6) and np.all(r > 0)
+    # streams are reproducible and independent of each other
+    a = synth.packed_codes(synth.rng_for("w", 3), 4, 64)
+    b = synth.packed_codes(synth.rng_for("w", 3), 4, 64)
+    c = synth.packed_codes(synth.rng_for("w", 4), 4, 64)
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
