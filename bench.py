@@ -1,0 +1,578 @@
+#!/usr/bin/env python
+"""Benchmark of the q4f16_1 dequant-GEMV decode path on GB300.
+
+Default workload: the Phi-3-mini-shaped decode layer stack at M = 1
+(32 layers x {QKV 9216x3072, O 3072x3072, gate_up 16384x3072 -> SiLU*mul
+8192, down 3072x8192} + LM head 32064x3072, every matrix distinct, seeded
+synthetic weights; 2.09 GB of packed weights per token). One step = one
+decode token through the whole stack = 129 kernel launches, replayed from a
+CUDA graph. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zq4|reference]
+                  [--workload phi3|gemv3072|qwen3|moe] [--m M] [--t T]
+
+--impl reference times the CPU oracle (fp64, host cores) on a bounded
+sample of the same workload and prints the same line with "impl":
+"reference". Multi-GPU runs (torchrun) are independent replicas: every rank
+runs its own stack; value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "W4A16 dequant-GEMV achieved HBM GB/s (% of peak); Phi-3-shape decode tok/s"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
+    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe"])
+    ap.add_argument("--m", type=int, default=1, help="tokens per step (qwen3 workload)")
+    ap.add_argument("--t", type=int, default=16, help="tokens per step (moe workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU time budget of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and max-of-times, no data path)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 10:
+                continue
+            if self.uuid and f[1] != self.uuid:
+                continue
+            rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2])]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(num(r[3]) or 0 for r in rows),
+                "power_w_max": max(num(r[4]) or 0 for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_weight_only_q4f16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    or None when the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (test infrastructure; timed, never used for results)
+# ---------------------------------------------------------------------------
+def oracle_sample_rate(projs, budget_s: float, M: int = 1):
+    """Run the fp64 oracle over row blocks of the given projections
+    ((name, N, K, layer) in step order) until budget_s seconds of wall time;
+    return (weight bytes covered per second, threads, description)."""
+    import oracle
+    from int4_weight_only_q4f16_gb300 import synth
+    o = oracle.get()
+    covered = 0
+    spent = 0.0
+    done = []
+    for name, N, K, layer in projs:
+        wq, sc = synth.weight(name, N, K, layer)
+        x = synth.activations(synth.rng_for("cpu_x", layer), M, K)
+        rows_per_call = max(1, min(N, 256))
+        for r0 in range(0, N, rows_per_call):
+            rows = np.arange(r0, min(N, r0 + rows_per_call))
+            t0 = time.perf_counter()
+            o.gemv(wq, sc, x, N, K, rows=rows)
+            spent += time.perf_counter() - t0
+            covered += rows.size * (K // 8 * 4 + K // 32 * 2)
+            if spent >= budget_s:
+                done.append(f"{name}[layer {layer}] rows 0..{rows[-1]}")
+                desc = "; ".join(done)
+                return covered / spent, o.num_threads(), desc
+        done.append(f"{name}[layer {layer}]")
+    return covered / max(spent, 1e-9), o.num_threads(), "; ".join(done)
+
+
+def phi3_projs():
+    from int4_weight_only_q4f16_gb300 import synth
+    out = []
+    for l in range(synth.PHI3_LAYERS):
+        for name, N, K in synth.PHI3_LAYER:
+            out.append((name, N, K, l))
+        if l == 0:
+            out.append((synth.PHI3_LM_HEAD[0],) + synth.PHI3_LM_HEAD[1:] + (0,))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+def time_replays(torch, fn, steps, stream):
+    """Seconds for `steps` calls of fn issued on `stream`, CUDA events on
+    that stream, synchronised on both sides."""
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / 1e3
+
+
+def replay_on(torch, g, stream, n):
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            g.replay()
+    torch.cuda.synchronize()
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def run_phi3(args, torch, dist, peaks, peak_kind):
+    from int4_weight_only_q4f16_gb300 import stack as stack_mod, synth, zq4
+    dev = torch.device("cuda", dist.local)
+    st = stack_mod.phi3_stack(M=1, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        st.launch_step(stream)                         # eager step: sets kernel attributes
+    torch.cuda.synchronize()
+    head = st.y[("head",)].float()
+    assert torch.isfinite(head).all() and head.abs().sum() > 0, "stack output is zero/non-finite"
+    g = st.capture(stream)
+    replay_on(torch, g, stream, args.warmup)
+
+    sampler = ClockSampler(gpu_uuid(torch, dev) if dist.rank == 0 else None)
+    if dist.rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    dist.barrier()
+    elapsed = time_replays(torch, g.replay, args.steps, stream)
+    dist.barrier()
+    clocks = sampler.stop() if dist.rank == 0 else None
+    elapsed = dist.max(elapsed)
+    step_s = elapsed / args.steps
+    bytes_step = st.bytes_per_step()
+    tok_s = dist.world * st.M / step_s
+
+    # dominant kernel: gate_up + SiLU*mul over the stack's 32 distinct matrices
+    gu = [st.layers[l]["gate_up"] for l in range(st.n_layers)]
+
+    def gate_up_chain():
+        for l, p in enumerate(gu):
+            zq4.gate_up_silu(p.wq, p.sc, st.x[(l, "gate_up")], p.N, p.K, h=st.y[(l, "gate_up")],
+                             stream=stream)
+    gg = capture(torch, gate_up_chain, stream)
+    replay_on(torch, gg, stream, 3)
+    reps = max(10, min(200, args.steps // 10))
+    gu_s = time_replays(torch, gg.replay, reps, stream) / (reps * len(gu))
+    p0 = gu[0]
+    gu_bytes = p0.nbytes + st.M * p0.K * 2 + st.M * (p0.N // 2) * 2
+    achieved = gu_bytes / gu_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "k_dense<1,32,2> (gate_up + SiLU*mul, 16384x3072)",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                "traffic": profiled_traffic("gate_up_phi3_M1"),
+                "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_s * 1e6, 3),
+                "launches_timed": reps * len(gu)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = phi3_e2e(args, torch, st, stream, dist)
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        rate, threads, desc = oracle_sample_rate(phi3_projs(), args.cpu_seconds)
+        cpu = {"value": round(rate / st.weight_bytes(), 4), "unit": "tok/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"fp64 oracle GEMV over {desc} (~{args.cpu_seconds:.0f} s), scaled by "
+                         f"weight bytes to one 2.09 GB token"}
+
+    launches = st.launches_per_step() * args.steps
+    line = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "hbm_gbs": round(bytes_step / step_s / 1e9, 1),
+        "hbm_frac_of_measured": round(bytes_step / step_s / 1e9 / peaks["hbm_gbs"], 4),
+        "hbm_frac_of_8tbs": round(bytes_step / step_s / 8e12, 4),
+        "config": {"workload": "phi3-mini decode layer stack, M=1 (32 layers + LM head)",
+                   "M": 1, "layers": 32, "launches_per_step": st.launches_per_step(),
+                   "bytes_per_step": bytes_step, "weight_bytes_per_step": st.weight_bytes(),
+                   "l2": f"inputs larger than L2: {st.weight_bytes() / 1e9:.2f} GB of distinct "
+                         f"weights per step vs {L2_BYTES >> 20} MiB L2",
+                   "parallelism": f"replicas x{dist.world}", "graph": "one CUDA graph per step",
+                   "arith": "int4 codes -> exact f16 (q-7); f16*f16 products, fp32 accumulate; "
+                            "f16 out"},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def phi3_e2e(args, torch, st, stream, dist):
+    """Same metric through the public API with host buffers: per step, copy
+    every fresh activation from pinned host memory, replay, read the logits
+    back to pinned host memory."""
+    keys = [k for k in st.x]
+    sizes = [st.x[k].numel() for k in keys]
+    host_in = torch.empty(sum(sizes), dtype=torch.float16, pin_memory=True)
+    off = 0
+    for k, n in zip(keys, sizes):
+        host_in[off:off + n].copy_(st.x[k].flatten().cpu())
+        off += n
+    dev_in = torch.empty_like(host_in, device=st.device)
+    views, off = [], 0
+    for k, n in zip(keys, sizes):
+        views.append((st.x[k], dev_in[off:off + n].view_as(st.x[k])))
+        off += n
+    out = st.y[("head",)]
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    # the step's inputs are read from dev_in: rebind the stack's inputs to it
+    saved = dict(st.x)
+    for (k, _), (_, v) in zip(zip(keys, sizes), views):
+        st.x[k] = v
+    g = st.capture(stream)
+    steps = max(3, min(args.steps, 500))
+
+    def one():
+        with torch.cuda.stream(stream):
+            dev_in.copy_(host_in, non_blocking=True)
+            g.replay()
+            host_out.copy_(out, non_blocking=True)
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = dist.max(time.perf_counter() - t0)
+    st.x.update(saved)
+    return {"value": round(dist.world * st.M * steps / el, 2), "unit": "tok/s",
+            "h2d_bytes_per_step": int(host_in.numel() * 2),
+            "d2h_bytes_per_step": int(host_out.numel() * 2), "steps": steps,
+            "timer": "host wall clock around copies + replay, synchronised"}
+
+
+def run_gemv3072(args, torch, dist, peaks, peak_kind):
+    """Single 3072x3072 GEMV, M=1, rotating over distinct weight copies that
+    together exceed 4x L2 (so every call reads HBM)."""
+    from int4_weight_only_q4f16_gb300 import synth, zq4
+    N = K = 3072
+    copies = 128
+    wq, sc = synth.weight("cfg0", N, K, 0)
+    W = torch.from_numpy(wq.view(np.int32)).cuda().repeat(copies, 1).view(copies, N, K // 8)
+    S = torch.from_numpy(sc).cuda().repeat(copies, 1).view(copies, N, K // 32)
+    x = torch.from_numpy(synth.activations(synth.rng_for("cfg0x"), 1, K)).cuda()
+    y = torch.empty((copies, 1, N), dtype=torch.float16, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def chain():
+        for c in range(copies):
+            zq4.gemv(W[c], S[c], x, N, K, y=y[c], stream=stream)
+    with torch.cuda.stream(stream):
+        chain()
+    g = capture(torch, chain, stream)
+    replay_on(torch, g, stream, max(3, args.warmup))
+    reps = max(5, min(args.steps // copies, 100))
+    el = time_replays(torch, g.replay, reps, stream)
+    per = el / (reps * copies)
+    b = N * (K // 8) * 4 + N * (K // 32) * 2 + K * 2 + N * 2
+    gbs = b / per / 1e9
+    return {"metric": "single GEMV 3072x3072 M=1 achieved HBM GB/s", "value": round(gbs, 1),
+            "unit": "GB/s", "us_per_call": round(per * 1e6, 3), "bytes_per_call": b,
+            "frac_of_measured": round(gbs / peaks["hbm_gbs"], 4),
+            "config": {"workload": "gemv 3072x3072 M=1", "copies": copies,
+                       "l2": f"{copies} distinct copies ({copies * b / 1e6:.0f} MB) > 4x L2"}}
+
+
+def run_qwen3(args, torch, dist, peaks, peak_kind):
+    from int4_weight_only_q4f16_gb300 import stack as stack_mod
+    st = stack_mod.qwen3_4b_stack(M=args.m)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        st.launch_step(stream)
+    g = st.capture(stream)
+    replay_on(torch, g, stream, max(3, args.warmup))
+    steps = max(5, min(args.steps, 1000))
+    el = time_replays(torch, g.replay, steps, stream)
+    step = el / steps
+    b = st.bytes_per_step()
+    return {"metric": "Qwen3-4B-shape projection stack tokens/s", "value": round(st.M / step, 1),
+            "unit": "tok/s", "M": st.M, "ms_per_step": round(step * 1e3, 4),
+            "hbm_gbs": round(b / step / 1e9, 1), "frac_of_measured": round(b / step / 1e9 / peaks["hbm_gbs"], 4),
+            "launches_per_step": st.launches_per_step(),
+            "config": {"workload": f"qwen3-4b 36-layer projection stack, M={st.M}",
+                       "bytes_per_step": b}}
+
+
+def run_moe(args, torch, dist, peaks, peak_kind):
+    """MoE expert GEMV (gate_up+SiLU, down+combine), 128 experts, top-8,
+    rotating over 4 distinct banks (> 4x L2 in total)."""
+    from int4_weight_only_q4f16_gb300 import synth, zq4
+    E, top_k, T = synth.MOE_EXPERTS, synth.MOE_TOP_K, args.t
+    (N2, D), (Dn, I) = synth.MOE_GATE_UP, synth.MOE_DOWN
+    banks = 4
+    gq, gs, dq, ds, xs, ids, rs, hs, ys = [], [], [], [], [], [], [], [], []
+    uniq_bytes = []
+    for b in range(banks):
+        a, s = synth.weight("moe_gu", E * N2, D, b)
+        gq.append(torch.from_numpy(a.view(np.int32)).cuda())
+        gs.append(torch.from_numpy(s).cuda())
+        a, s = synth.weight("moe_dn", E * Dn, I, b)
+        dq.append(torch.from_numpy(a.view(np.int32)).cuda())
+        ds.append(torch.from_numpy(s).cuda())
+        rng = synth.rng_for("moe_route", b, T)
+        i_, r_ = synth.routing(rng, T, E, top_k)
+        xs.append(torch.from_numpy(synth.activations(rng, T, D)).cuda())
+        ids.append(torch.from_numpy(i_).cuda())
+        rs.append(torch.from_numpy(r_).cuda())
+        hs.append(torch.empty((T, top_k, N2 // 2), dtype=torch.float16, device="cuda"))
+        ys.append(torch.empty((T, Dn), dtype=torch.float16, device="cuda"))
+        nu = len(np.unique(i_))
+        uniq_bytes.append(nu * (N2 * (D // 8) * 4 + N2 * (D // 32) * 2 + Dn * (I // 8) * 4 + Dn * (I // 32) * 2))
+    stream = torch.cuda.Stream()
+
+    def chain():
+        for b in range(banks):
+            zq4.moe_gemv(gq[b], gs[b], E, xs[b], N2, D, ids[b], zq4.MOE_GATE_UP_SILU, y=hs[b],
+                         stream=stream)
+            zq4.moe_gemv(dq[b], ds[b], E, hs[b], Dn, I, ids[b], zq4.MOE_DOWN_COMBINE,
+                         route_w=rs[b], y=ys[b], stream=stream)
+    with torch.cuda.stream(stream):
+        chain()
+    g = capture(torch, chain, stream)
+    replay_on(torch, g, stream, max(3, args.warmup))
+    reps = max(5, min(args.steps, 500))
+    el = time_replays(torch, g.replay, reps, stream)
+    per = el / (reps * banks)
+    ub = sum(uniq_bytes) / banks
+    return {"metric": "MoE expert GEMV block (gate_up+SiLU, down+combine) GB/s over unique experts",
+            "value": round(ub / per / 1e9, 1), "unit": "GB/s", "T": T, "us_per_block": round(per * 1e6, 3),
+            "unique_expert_bytes": ub, "frac_of_measured": round(ub / per / 1e9 / peaks["hbm_gbs"], 4),
+            "config": {"workload": f"MoE 128 experts top-8, T={T}", "banks": banks}}
+
+
+def run_reference(args, dist):
+    """The CPU oracle on the host cores, timed on a bounded sample of the
+    Phi-3 stack; each step covers the same row sample."""
+    if dist.rank != 0:
+        return None
+    import oracle
+    from int4_weight_only_q4f16_gb300 import synth
+    o = oracle.get()
+    # sample: 256 rows of each projection of layer 0 and of the LM head
+    projs = [(n, N, K) for n, N, K in synth.PHI3_LAYER] + [synth.PHI3_LM_HEAD]
+    data = []
+    rows = 256
+    for name, N, K in projs:
+        wq, sc = synth.weight(name, N, K, 0)
+        x = synth.activations(synth.rng_for("ref_x"), 1, K)
+        data.append((wq, sc, x, N, K, np.arange(rows)))
+    sample_bytes = sum(rows * (K // 8 * 4 + K // 32 * 2) for _, _, _, _, K, _ in data)
+    token_bytes = sum(N * (K // 8 * 4 + K // 32 * 2) for _, N, K in synth.PHI3_LAYER) * synth.PHI3_LAYERS + \
+        synth.PHI3_LM_HEAD[1] * (synth.PHI3_LM_HEAD[2] // 8 * 4 + synth.PHI3_LM_HEAD[2] // 32 * 2)
+
+    def step():
+        for wq, sc, x, N, K, r in data:
+            o.gemv(wq, sc, x, N, K, rows=r)
+    t0 = time.perf_counter()
+    step()
+    one = time.perf_counter() - t0
+    budget = 150.0
+    steps = args.steps
+    scale = 1
+    if one * (steps + args.warmup) > budget:       # keep the whole run within a few minutes
+        steps = max(1, int(budget / one) - args.warmup)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t0
+    per_step = el / steps
+    tok_s = sample_bytes / per_step / token_bytes
+    desc = (f"256 rows of each layer-0 projection (QKV, O, gate_up, down) and of the LM head "
+            f"({sample_bytes / 1e6:.2f} MB of packed weights per step), scaled by weight bytes "
+            f"to one {token_bytes / 1e9:.2f} GB token")
+    return {"impl": "reference", "metric": METRIC, "value": round(tok_s, 5), "unit": "tok/s",
+            "n_gpus": dist.world, "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "phi3-mini decode layer stack, M=1 (32 layers + LM head)",
+                       "M": 1, "layers": 32},
+            "cpu_baseline": {"value": round(tok_s, 5), "unit": "tok/s", "cores": o.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(tok_s, 5), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        line = run_reference(args, dist)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        dist.close()
+        return 0
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(dist.local)
+    peaks, kind = measured_peaks()
+    fn = {"phi3": run_phi3, "gemv3072": run_gemv3072, "qwen3": run_qwen3, "moe": run_moe}[args.workload]
+    line = fn(args, torch, dist, peaks, kind)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

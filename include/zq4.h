@@ -1,0 +1,202 @@
+/*
+ * zq4.h -- C ABI of the q4f16_1 fused dequantize + NT matmul library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The format ("Zero TVM Documentation", section "Q4F16 quantization
+ * format"): a weight matrix W of N rows and K columns (K along the reduction)
+ * is stored as
+ *   wq     uint32 [N, K/8]   8 unsigned 4-bit codes per word; element i of a
+ *                            word (i = 0..7, least significant nibble first)
+ *                            is column 8*word_index + i;
+ *   scales f16    [N, K/32]  one scale per 32 consecutive columns;
+ * and the weight value is w[n,k] = (q[n,k] - 7) * scales[n, k/32].
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer to memory the caller allocated
+ *     and owns; the library allocates nothing and keeps no pointer after the
+ *     call returns. f16 data is passed as uint16_t (IEEE binary16 bits).
+ *   - Row-major, densely packed: row r of a [R, C] array starts at element
+ *     r*C. No strides.
+ *   - K must be a positive multiple of 32 (the group size). wq, scales and
+ *     the activation input must start on a 16-byte boundary.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous and stream-ordered; none synchronises the host.
+ *     Outputs are valid once the stream reaches the call.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns a negative zq4_status and launches nothing. A failed
+ *     launch returns ZQ4_ERR_CUDA (zq4_last_cuda_error() gives the CUDA
+ *     error code of that failure on the calling thread).
+ *   - Accumulation is fp32; the output is rounded to f16 (nearest even).
+ *   - Kernels are launched with programmatic dependent launch allowed: a
+ *     kernel may start while the previous kernel of the stream finishes and
+ *     read its WEIGHTS early, but it reads its activation input and writes
+ *     its output only after that previous kernel has completed.
+ */
+#ifndef ZQ4_H
+#define ZQ4_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZQ4_API __attribute__((visibility("default")))
+#else
+#define ZQ4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zq4_status {
+    ZQ4_OK = 0,
+    ZQ4_ERR_NULL = -1,        /* a required pointer is NULL */
+    ZQ4_ERR_SHAPE = -2,       /* M, N, K, T, top_k or num_experts out of range */
+    ZQ4_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+    ZQ4_ERR_FLAGS = -4,       /* unknown mode or flags */
+    ZQ4_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+    ZQ4_ERR_UNSUPPORTED = -6, /* valid arguments this build does not handle */
+    ZQ4_ERR_OVERLAP = -7      /* input and output buffers overlap */
+} zq4_status;
+
+/* Human-readable name of a status (static string, never NULL). */
+ZQ4_API const char *zq4_status_string(int status);
+
+/* CUDA error code (cudaError_t as int) behind the last ZQ4_ERR_CUDA returned
+ * on the calling thread; 0 if none. */
+ZQ4_API int zq4_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+ZQ4_API int zq4_version(void);
+
+/*
+ * zq4_gemv -- y = x * W^T, the fused dequantize + NT matmul.
+ * Source: "Zero TVM Documentation", section "WGSL Kernel Roles", card 5
+ * "int4 Matmul" (one output per weight row; K_groups = K/8,
+ * scale_stride = K/32), and "RESEARCH.md" (Zero-TVM), section "Matmul
+ * Shader Analysis" (TVM's fused_dequantize*_NT_matmul: dot product of the
+ * input with (code - 7) * group scale).
+ *
+ *   wq     [N, K/8]  uint32, device        scales [N, K/32] f16, device
+ *   x      [M, K]    f16, device           y      [M, N]    f16, device
+ *   y[m,n] = f16( sum_k x[m,k] * w[n,k] )  (fp32 accumulation)
+ *
+ * M >= 1 (1..16 run the decode GEMV kernels; M >= 64 the tensor-core GEMM
+ * that dequantizes tiles into shared memory; 17..63 the decode kernels in
+ * blocks of 16 rows), N >= 1, K a multiple of 32. y must not overlap wq,
+ * scales or x. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
+ * ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                    uint16_t *y, int M, int N, int K, void *stream);
+
+/*
+ * zq4_gate_up_silu -- h = silu(x * Wg^T) * (x * Wu^T) in one pass over the
+ * shared gate/up matrix.
+ * Source: "Zero TVM Documentation", section "WGSL Kernel Roles", card 6
+ * "Fused FFN" (gate and up share one 2*I-row matrix; SiLU and the
+ * multiply follow in the same dispatch) and "RESEARCH.md" (Zero-TVM),
+ * section "TVM Already Fuses Elementwise Operations" (split + SiLU +
+ * multiply).
+ *
+ *   wq     [N2, K/8]  uint32, rows INTERLEAVED: row 2j is gate j, row 2j+1
+ *                     is up j (zq4_prepare_weight converts the concatenated
+ *                     [gate; up] layout)
+ *   scales [N2, K/32] f16          x [M, K] f16          h [M, N2/2] f16
+ *   h[m,j] = f16( silu(g) * u ),  g = sum_k x[m,k] w[2j,k],
+ *   u = sum_k x[m,k] w[2j+1,k],  silu(z) = z / (1 + exp(-z)), all fp32.
+ *
+ * N2 must be even and >= 2; M >= 1 (M >= 64 uses the tensor-core GEMM).
+ * Errors as zq4_gemv.
+ */
+ZQ4_API zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                            uint16_t *h, int M, int N2, int K, void *stream);
+
+/* Modes of zq4_moe_gemv. */
+#define ZQ4_MOE_GATE_UP_SILU 1
+#define ZQ4_MOE_DOWN_COMBINE 2
+
+/* Bits of the device status word of zq4_moe_gemv. */
+#define ZQ4_DEV_BAD_EXPERT_ID 1u
+
+/*
+ * zq4_moe_gemv -- expert-gather q4f16_1 GEMV of a mixture-of-experts block.
+ * Source: "Zero-TVM benchmarks" (BENCH.md), section "MoE chunked prefill"
+ * (routing ids and scores of shape [tokens, slots]; the expert matmul takes
+ * the token in one grid dimension and the slot in another; experts never mix
+ * tokens; a combine sums the slots of each token) and "Zero TVM
+ * Documentation", section "Qwen3.6-35B-A3B MoE" (expert index in the grid).
+ *
+ * The bank holds num_experts matrices of identical shape [N, K] back to
+ * back: expert e's codes start at wq_bank + e*N*(K/8) and its scales at
+ * scales_bank + e*N*(K/32).
+ *   expert_ids [T, top_k] int32, device; route_w [T, top_k] float32, device.
+ *
+ * mode ZQ4_MOE_GATE_UP_SILU: the bank holds interleaved gate/up matrices
+ *   (N = 2I rows, as zq4_gate_up_silu); x is [T, K]; y is [T, top_k, I]:
+ *   y[t,j,:] = silu/mul epilogue of expert expert_ids[t,j] applied to x[t].
+ *   route_w is not read (may be NULL).
+ * mode ZQ4_MOE_DOWN_COMBINE: x is [T, top_k, K] (one input per slot, e.g.
+ *   the previous stage's y); y is [T, N]:
+ *   y[t,n] = f16( sum_j route_w[t,j] * sum_k x[t,j,k] w_e[n,k] ),
+ *   e = expert_ids[t,j], fp32 throughout; route_w is required.
+ *
+ * An expert id outside [0, num_experts) is detected on the device: that
+ * slot contributes nothing (GATE_UP: its y rows are written as zero) and
+ * ZQ4_DEV_BAD_EXPERT_ID is OR-ed into *dev_status (a device int32 the
+ * caller clears; may be NULL). 1 <= top_k <= 32, T >= 1. Errors as
+ * zq4_gemv, plus ZQ4_ERR_FLAGS for an unknown mode.
+ */
+ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, int num_experts,
+                        const uint16_t *x, uint16_t *y, int T, int N, int K,
+                        const int32_t *expert_ids, const float *route_w, int top_k, int mode,
+                        int32_t *dev_status, void *stream);
+
+/* Flags of zq4_prepare_weight. */
+#define ZQ4_PREP_COPY 0                  /* plain copy of the canonical layout */
+#define ZQ4_PREP_CONCAT_TO_INTERLEAVED 1 /* [gate; up] rows -> g0,u0,g1,u1,... */
+
+/*
+ * zq4_prepare_weight -- rewrite a q4f16_1 matrix into the layout the kernels
+ * take. The row order is the only thing that changes; each row's words and
+ * scales are copied bit for bit, so dequantized values are identical.
+ * Source: "Zero-TVM benchmarks" (BENCH.md), section "Qwen3.5 hybrid perf
+ * round" (q4f16_1 matrices are concatenated row-wise by concatenating their
+ * bytes) and "Zero TVM Documentation", card 6 "Fused FFN" (the gate_up
+ * matrix holds all gate rows, then all up rows).
+ *
+ *   wq_src/scales_src [N, K/8] / [N, K/32]  ->  wq_dst/scales_dst (same shapes)
+ * N even for ZQ4_PREP_CONCAT_TO_INTERLEAVED. Source and destination must
+ * not overlap. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_FLAGS,
+ * ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src,
+                              uint32_t *wq_dst, uint16_t *scales_dst, int N, int K, int flags,
+                              void *stream);
+
+/*
+ * zq4_dequant_f32 -- w[n,k] = (q - 7) * s as float32, exact (a 4-bit integer
+ * times an f16 is representable in fp32). This is the value every decode
+ * kernel multiplies with. Source: "Zero TVM Documentation", section "Q4F16
+ * quantization format".
+ *   w [N, K] float32, device. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE,
+ *   ZQ4_ERR_ALIGN, ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
+                           void *stream);
+
+/*
+ * zq4_dequant_f16 -- w[n,k] = f16((q - 7) * s), rounded once to nearest even:
+ * the f16 product the docs page's dequantization formula computes (f16 of
+ * (code - 7) times the f16 scale), and the operand the tensor-core GEMM
+ * (M >= 64) feeds to the tensor cores. Source: "Zero TVM Documentation",
+ * section "Q4F16 quantization format".
+ *   w [N, K] f16, device. Errors as zq4_dequant_f32.
+ */
+ZQ4_API zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N, int K,
+                           void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZQ4_H */

@@ -1,0 +1,214 @@
+// zq4_api.cu -- the extern "C" entry points declared in include/zq4.h:
+// host-side argument checks, then stream-ordered launches.
+#include <atomic>
+
+#include "zq4_common.cuh"
+#include "zq4_internal.h"
+
+namespace zq4 {
+
+static thread_local int t_last_cuda_error = 0;
+
+void set_last_cuda_error(cudaError_t e) { t_last_cuda_error = int(e); }
+
+zq4_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return ZQ4_OK;
+    set_last_cuda_error(e);
+    return ZQ4_ERR_CUDA;
+}
+
+int sm_count()
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        v = 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+cudaError_t ensure_smem(const void *kernel, size_t bytes, int *cache_by_device)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        auto *slot = reinterpret_cast<std::atomic<int> *>(&cache_by_device[dev]);
+        if (size_t(slot->load(std::memory_order_relaxed)) >= bytes) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+        if (e == cudaSuccess) {
+            int cur = slot->load(std::memory_order_relaxed);
+            while (size_t(cur) < bytes && !slot->compare_exchange_weak(cur, int(bytes))) {
+            }
+        }
+        return e;
+    }
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+}  // namespace zq4
+
+using namespace zq4;
+
+namespace {
+
+// Shape checks shared by the GEMV-family calls.
+zq4_status check_matrix(const void *wq, const void *scales, int N, int K)
+{
+    if (!wq || !scales) return ZQ4_ERR_NULL;
+    if (N <= 0 || K <= 0 || (K % 32) != 0) return ZQ4_ERR_SHAPE;
+    if (!aligned16(wq) || !aligned16(scales)) return ZQ4_ERR_ALIGN;
+    return ZQ4_OK;
+}
+
+size_t wq_bytes(size_t N, size_t K) { return N * (K / 8) * 4; }
+size_t sc_bytes(size_t N, size_t K) { return N * (K / 32) * 2; }
+
+}  // namespace
+
+extern "C" {
+
+const char *zq4_status_string(int status)
+{
+    switch (status) {
+    case ZQ4_OK: return "ZQ4_OK";
+    case ZQ4_ERR_NULL: return "ZQ4_ERR_NULL: a required pointer is NULL";
+    case ZQ4_ERR_SHAPE: return "ZQ4_ERR_SHAPE: a size is out of range";
+    case ZQ4_ERR_ALIGN: return "ZQ4_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case ZQ4_ERR_FLAGS: return "ZQ4_ERR_FLAGS: unknown mode or flags";
+    case ZQ4_ERR_CUDA: return "ZQ4_ERR_CUDA: a CUDA call or launch failed";
+    case ZQ4_ERR_UNSUPPORTED: return "ZQ4_ERR_UNSUPPORTED: not handled by this build";
+    case ZQ4_ERR_OVERLAP: return "ZQ4_ERR_OVERLAP: input and output buffers overlap";
+    default: return "ZQ4: unknown status";
+    }
+}
+
+int zq4_last_cuda_error(void) { return t_last_cuda_error; }
+
+int zq4_version(void) { return 100; }
+
+zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
+                    int M, int N, int K, void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !y) return ZQ4_ERR_NULL;
+    if (M <= 0) return ZQ4_ERR_SHAPE;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 1)) return ZQ4_ERR_ALIGN;
+    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    size_t ybytes = size_t(M) * N * 2;
+    if (overlap(y, ybytes, wq, wq_bytes(N, K)) || overlap(y, ybytes, scales, sc_bytes(N, K)) ||
+        overlap(y, ybytes, x, size_t(M) * K * 2))
+        return ZQ4_ERR_OVERLAP;
+    return cuda_status(launch_decode(wq, scales, x, y, M, N, K, false,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                            uint16_t *h, int M, int N2, int K, void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N2, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !h) return ZQ4_ERR_NULL;
+    if (M <= 0 || (N2 & 1)) return ZQ4_ERR_SHAPE;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(h) & 1)) return ZQ4_ERR_ALIGN;
+    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    size_t hbytes = size_t(M) * (N2 / 2) * 2;
+    if (overlap(h, hbytes, wq, wq_bytes(N2, K)) || overlap(h, hbytes, scales, sc_bytes(N2, K)) ||
+        overlap(h, hbytes, x, size_t(M) * K * 2))
+        return ZQ4_ERR_OVERLAP;
+    return cuda_status(launch_decode(wq, scales, x, h, M, N2, K, true,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, int num_experts,
+                        const uint16_t *x, uint16_t *y, int T, int N, int K,
+                        const int32_t *expert_ids, const float *route_w, int top_k, int mode,
+                        int32_t *dev_status, void *stream)
+{
+    if (mode != ZQ4_MOE_GATE_UP_SILU && mode != ZQ4_MOE_DOWN_COMBINE) return ZQ4_ERR_FLAGS;
+    zq4_status st = check_matrix(wq_bank, scales_bank, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !y || !expert_ids) return ZQ4_ERR_NULL;
+    if (mode == ZQ4_MOE_DOWN_COMBINE && !route_w) return ZQ4_ERR_NULL;
+    if (num_experts <= 0 || T <= 0 || top_k <= 0 || top_k > 32) return ZQ4_ERR_SHAPE;
+    if (mode == ZQ4_MOE_GATE_UP_SILU && (N & 1)) return ZQ4_ERR_SHAPE;
+    if (T > 65535 || (mode == ZQ4_MOE_GATE_UP_SILU && size_t(T) * top_k > 65535))
+        return ZQ4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 1) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3) || (reinterpret_cast<uintptr_t>(route_w) & 3) ||
+        (reinterpret_cast<uintptr_t>(dev_status) & 3))
+        return ZQ4_ERR_ALIGN;
+    const size_t xrows = mode == ZQ4_MOE_GATE_UP_SILU ? size_t(T) : size_t(T) * top_k;
+    const size_t staged_rows = mode == ZQ4_MOE_GATE_UP_SILU ? 1 : size_t(top_k);
+    if (staged_rows * K * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    const size_t ybytes = mode == ZQ4_MOE_GATE_UP_SILU ? size_t(T) * top_k * (N / 2) * 2
+                                                       : size_t(T) * N * 2;
+    const size_t E = size_t(num_experts);
+    if (overlap(y, ybytes, wq_bank, E * wq_bytes(N, K)) ||
+        overlap(y, ybytes, scales_bank, E * sc_bytes(N, K)) ||
+        overlap(y, ybytes, x, xrows * K * 2) ||
+        overlap(y, ybytes, expert_ids, size_t(T) * top_k * 4))
+        return ZQ4_ERR_OVERLAP;
+    MoeArgs a = {};
+    a.wq = wq_bank;
+    a.scales = scales_bank;
+    a.x = x;
+    a.y = y;
+    a.ids = expert_ids;
+    a.route_w = route_w;
+    a.dev_status = dev_status;
+    a.num_experts = num_experts;
+    a.T = T;
+    a.N = N;
+    a.K = K;
+    a.top_k = top_k;
+    return cuda_status(launch_moe(a, mode, static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src,
+                              uint32_t *wq_dst, uint16_t *scales_dst, int N, int K, int flags,
+                              void *stream)
+{
+    if (flags != ZQ4_PREP_COPY && flags != ZQ4_PREP_CONCAT_TO_INTERLEAVED) return ZQ4_ERR_FLAGS;
+    zq4_status st = check_matrix(wq_src, scales_src, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!wq_dst || !scales_dst) return ZQ4_ERR_NULL;
+    if (!aligned16(wq_dst) || !aligned16(scales_dst)) return ZQ4_ERR_ALIGN;
+    if (flags == ZQ4_PREP_CONCAT_TO_INTERLEAVED && (N & 1)) return ZQ4_ERR_SHAPE;
+    const size_t wb = wq_bytes(N, K), sb = sc_bytes(N, K);
+    if (overlap(wq_dst, wb, wq_src, wb) || overlap(wq_dst, wb, scales_src, sb) ||
+        overlap(scales_dst, sb, wq_src, wb) || overlap(scales_dst, sb, scales_src, sb) ||
+        overlap(wq_dst, wb, scales_dst, sb))
+        return ZQ4_ERR_OVERLAP;
+    return cuda_status(launch_prepare(wq_src, scales_src, wq_dst, scales_dst, N, K,
+                                      flags == ZQ4_PREP_CONCAT_TO_INTERLEAVED,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
+                           void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!w) return ZQ4_ERR_NULL;
+    if (!aligned16(w)) return ZQ4_ERR_ALIGN;
+    return cuda_status(launch_dequant_f32(wq, scales, w, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N, int K,
+                           void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!w) return ZQ4_ERR_NULL;
+    if (!aligned16(w)) return ZQ4_ERR_ALIGN;
+    return cuda_status(launch_dequant_f16(wq, scales, w, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

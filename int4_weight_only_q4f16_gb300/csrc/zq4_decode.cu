@@ -1,0 +1,533 @@
+// zq4_decode.cu -- memory-bound q4f16_1 GEMV kernels for small M (decode),
+// the gate_up + SiLU*mul epilogue, the MoE expert-gather variants, and the
+// dequantize / layout helpers.
+//
+// What they compute: "Zero TVM Documentation", section "WGSL Kernel Roles",
+// cards 5 ("int4 Matmul") and 6 ("Fused FFN"); "RESEARCH.md" (Zero-TVM),
+// section "Matmul Shader Analysis"; "Zero-TVM benchmarks" (BENCH.md), section
+// "MoE chunked prefill". How they compute it is a GB300 design of its own:
+//
+//  * one 16-byte load = the 4 words of one 32-weight scale group, so a warp
+//    reads 512 contiguous bytes of a row per load instruction, never
+//    allocating in L1;
+//  * the activations x are staged once per CTA in shared memory, with each
+//    word's 8 values stored as the pairs (0,4),(1,5),(2,6),(3,7) that the
+//    unpack produces, and the four 16-byte chunks of a group rotated by
+//    (group/2) mod 4 so that a quarter-warp's 16-byte reads hit 8 distinct
+//    bank groups;
+//  * codes become exact f16 (q - 7) with one LOP3 and one f16x2 op per two
+//    weights; products are f16 x f16 -> fp32 fused multiply-adds, and each
+//    group's sum is scaled once by its fp32 scale;
+//  * lanes of a row (8, 16 or 32) reduce with warp shuffles;
+//  * before waiting on the previous kernel (programmatic dependent launch)
+//    each CTA asks L2 to prefetch the weight rows it owns: weights never
+//    depend on the previous kernel, so the stream of weights continues
+//    across kernel boundaries.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "zq4_common.cuh"
+#include "zq4_internal.h"
+
+namespace zq4 {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;          // groups in flight per lane
+constexpr int kMoeSlotChunk = 8;    // expert slots loaded together in DOWN_COMBINE
+
+// ---------------------------------------------------------------------------
+// Activation staging
+// ---------------------------------------------------------------------------
+
+// Shared-memory byte offset of chunk c (word c of the group, 0..3) of group g.
+__device__ __forceinline__ uint32_t xs_offset(int g, int c)
+{
+    return uint32_t(g) * 64u + 16u * uint32_t(c ^ ((g >> 1) & 3));
+}
+
+// Stage rows [0, rows) of src (row stride K elements) into xs (row stride
+// 2K bytes) in the paired/rotated layout; rows [rows, rows_alloc) are zeroed.
+__device__ __forceinline__ void stage_rows(uint8_t *xs, const uint16_t *src, int rows,
+                                           int rows_alloc, int K)
+{
+    const int words = K >> 3;                 // 8 values per chunk
+    const int total = rows_alloc * words;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        int r = i / words, cw = i - r * words;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < rows) v = *reinterpret_cast<const uint4 *>(src + size_t(r) * K + size_t(cw) * 8);
+        uint4 o;
+        o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
+        o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
+        o.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
+        o.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
+        int g = cw >> 2, c = cw & 3;
+        *reinterpret_cast<uint4 *>(xs + size_t(r) * K * 2 + xs_offset(g, c)) = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One 32-weight group of one row against MT staged activation rows.
+// part[m] += s * sum_{k in group} x[m,k] * (q[k] - 7)
+// ---------------------------------------------------------------------------
+template <int MT>
+__device__ __forceinline__ void group_dot(const uint4 wv, float s, uint32_t xs_base, int g,
+                                          uint32_t row_bytes, float (&part)[MT])
+{
+    uint32_t p[4][4];
+    unpack_word_f16x2(wv.x, p[0]);
+    unpack_word_f16x2(wv.y, p[1]);
+    unpack_word_f16x2(wv.z, p[2]);
+    unpack_word_f16x2(wv.w, p[3]);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 xv = lds_v4(xs_base + uint32_t(m) * row_bytes + xs_offset(g, c));
+            fma2_f16_f32(p[c][0], xv.x, a0, a1);
+            fma2_f16_f32(p[c][1], xv.y, a0, a1);
+            fma2_f16_f32(p[c][2], xv.z, a0, a1);
+            fma2_f16_f32(p[c][3], xv.w, a0, a1);
+        }
+        part[m] = fmaf(s, a0 + a1, part[m]);
+    }
+}
+
+// Sum of v over the LPR lanes of a row segment (all lanes end with the sum).
+template <int LPR>
+__device__ __forceinline__ float segment_sum(float v, unsigned mask)
+{
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(mask, v, o, LPR);
+    return v;
+}
+
+template <int LPR>
+__device__ __forceinline__ unsigned segment_mask()
+{
+    if (LPR == 32) return 0xFFFFFFFFu;
+    unsigned lane = threadIdx.x & 31;
+    return ((1u << (LPR & 31)) - 1u) << (lane & ~unsigned(LPR - 1));
+}
+
+// Accumulate RU consecutive rows (starting at row0) of a matrix against MT
+// staged activation rows: part[r][m] holds this lane's partial sums.
+template <int MT, int LPR, int RU>
+__device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *scales, int K,
+                                         int row0, uint32_t xs_base, int lane,
+                                         float (&part)[RU][MT])
+{
+    const int G = K >> 5, KW = K >> 3;
+    const uint32_t row_bytes = uint32_t(K) * 2;
+    const uint32_t *wrow[RU];
+    const uint16_t *srow[RU];
+#pragma unroll
+    for (int r = 0; r < RU; ++r) {
+        wrow[r] = wq + size_t(row0 + r) * KW;
+        srow[r] = scales + size_t(row0 + r) * G;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[r][m] = 0.f;
+    }
+    for (int g0 = lane; g0 < G; g0 += kUnroll * LPR) {
+        uint4 wv[RU][kUnroll];
+        uint16_t sv[RU][kUnroll];
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) {
+            int g = g0 + i * LPR;
+#pragma unroll
+            for (int r = 0; r < RU; ++r) {
+                if (g < G) {
+                    wv[r][i] = ldg_stream_v4(wrow[r] + 4 * g);
+                    sv[r][i] = ldg_u16(srow[r] + g);
+                } else {
+                    wv[r][i] = make_uint4(0, 0, 0, 0);
+                    sv[r][i] = 0;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) {
+            int g = g0 + i * LPR;
+            if (g < G) {
+#pragma unroll
+                for (int r = 0; r < RU; ++r)
+                    group_dot<MT>(wv[r][i], f16_bits_to_float(sv[r][i]), xs_base, g, row_bytes,
+                                  part[r]);
+            }
+        }
+    }
+}
+
+// L2 prefetch of rows [row_lo, row_hi) of a q4f16_1 matrix by warp 0.
+__device__ __forceinline__ void prefetch_rows(const uint32_t *wq, const uint16_t *scales, int K,
+                                              size_t row_lo, size_t row_hi)
+{
+    if (threadIdx.x < 32) {
+        const size_t KW = size_t(K) >> 3, G = size_t(K) >> 5;
+        prefetch_l2_range(wq + row_lo * KW, wq + row_hi * KW, threadIdx.x, 32);
+        prefetch_l2_range(scales + row_lo * G, scales + row_hi * G, threadIdx.x, 32);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dense GEMV (RU = 1) and gate_up + SiLU*mul (RU = 2, interleaved rows).
+// A "unit" is RU consecutive rows; CTA b owns units [b*upc, (b+1)*upc).
+// ---------------------------------------------------------------------------
+template <int MT, int LPR, int RU>
+__global__ void __launch_bounds__(kThreads) k_dense(DenseArgs a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];
+    const int u0 = blockIdx.x * a.units_per_cta;
+    const int u1 = min(u0 + a.units_per_cta, a.units);
+    prefetch_rows(a.wq, a.scales, a.K, size_t(u0) * RU, size_t(u1) * RU);
+    griddep_wait();
+    stage_rows(xs, a.x, a.M, MT, a.K);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
+    const unsigned mask = segment_mask<LPR>();
+    const uint32_t xs_base = smem_addr(xs);
+    for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
+        float part[RU][MT];
+        rows_dot<MT, LPR, RU>(a.wq, a.scales, a.K, u * RU, xs_base, lane, part);
+#pragma unroll
+        for (int r = 0; r < RU; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) part[r][m] = segment_sum<LPR>(part[r][m], mask);
+        if (lane == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < a.M) {
+                    float v = (RU == 1) ? part[0][m] : silu_f32(part[0][m]) * part[RU - 1][m];
+                    a.y[size_t(m) * a.y_stride + u] = float_to_f16_bits(v);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MoE, mode GATE_UP_SILU: blockIdx.y = slot (t*top_k + j); the slot's expert
+// is read after the wait (the ids may come from the previous kernel).
+// ---------------------------------------------------------------------------
+template <int LPR>
+__global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];
+    const int slot = blockIdx.y, t = slot / a.top_k;
+    const int units = a.N >> 1;
+    const int u0 = blockIdx.x * a.units_per_cta;
+    const int u1 = min(u0 + a.units_per_cta, units);
+    griddep_wait();
+    const int e = a.ids[slot];
+    const bool valid = e >= 0 && e < a.num_experts;
+    uint16_t *yo = a.y + size_t(slot) * units;
+    if (!valid) {
+        if (blockIdx.x == 0 && threadIdx.x == 0 && a.dev_status)
+            atomicOr(reinterpret_cast<unsigned *>(a.dev_status), ZQ4_DEV_BAD_EXPERT_ID);
+        for (int u = u0 + threadIdx.x; u < u1; u += blockDim.x) yo[u] = 0;
+        griddep_launch_dependents();
+        return;
+    }
+    const uint32_t *wq = a.wq + size_t(e) * a.N * (a.K >> 3);
+    const uint16_t *sc = a.scales + size_t(e) * a.N * (a.K >> 5);
+    stage_rows(xs, a.x + size_t(t) * a.K, 1, 1, a.K);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
+    const unsigned mask = segment_mask<LPR>();
+    const uint32_t xs_base = smem_addr(xs);
+    for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
+        float part[2][1];
+        rows_dot<1, LPR, 2>(wq, sc, a.K, 2 * u, xs_base, lane, part);
+        float g = segment_sum<LPR>(part[0][0], mask);
+        float v = segment_sum<LPR>(part[1][0], mask);
+        if (lane == 0) yo[u] = float_to_f16_bits(silu_f32(g) * v);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MoE, mode DOWN_COMBINE: blockIdx.y = token t; each unit is one output row
+// n; y[t,n] = sum_j r[t,j] * (x[t,j,:] . w_{e_j}[n,:]).
+// ---------------------------------------------------------------------------
+template <int LPR>
+__global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];
+    __shared__ int s_ids[32];
+    __shared__ float s_r[32];
+    const int t = blockIdx.y;
+    const int u0 = blockIdx.x * a.units_per_cta;
+    const int u1 = min(u0 + a.units_per_cta, a.N);
+    griddep_wait();
+    if (threadIdx.x < a.top_k) {
+        int e = a.ids[t * a.top_k + threadIdx.x];
+        bool valid = e >= 0 && e < a.num_experts;
+        if (!valid && blockIdx.x == 0 && a.dev_status)
+            atomicOr(reinterpret_cast<unsigned *>(a.dev_status), ZQ4_DEV_BAD_EXPERT_ID);
+        s_ids[threadIdx.x] = valid ? e : -1;
+        s_r[threadIdx.x] = a.route_w[t * a.top_k + threadIdx.x];
+    }
+    stage_rows(xs, a.x + size_t(t) * a.top_k * a.K, a.top_k, a.top_k, a.K);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const int G = a.K >> 5, KW = a.K >> 3;
+    const uint32_t row_bytes = uint32_t(a.K) * 2;
+    const size_t expert_words = size_t(a.N) * KW, expert_scales = size_t(a.N) * G;
+    const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
+    const unsigned mask = segment_mask<LPR>();
+    const uint32_t xs_base = smem_addr(xs);
+    for (int n = u0 + sub; n < u1; n += kThreads / LPR) {
+        float acc = 0.f;
+        for (int g = lane; g < G; g += LPR) {
+            for (int j0 = 0; j0 < a.top_k; j0 += kMoeSlotChunk) {
+                uint4 wv[kMoeSlotChunk];
+                uint16_t sv[kMoeSlotChunk];
+#pragma unroll
+                for (int i = 0; i < kMoeSlotChunk; ++i) {
+                    int j = j0 + i, e = j < a.top_k ? s_ids[j] : -1;
+                    if (e >= 0) {
+                        wv[i] = ldg_stream_v4(a.wq + size_t(e) * expert_words + size_t(n) * KW + 4 * g);
+                        sv[i] = ldg_u16(a.scales + size_t(e) * expert_scales + size_t(n) * G + g);
+                    } else {
+                        wv[i] = make_uint4(0, 0, 0, 0);
+                        sv[i] = 0;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kMoeSlotChunk; ++i) {
+                    int j = j0 + i;
+                    if (j < a.top_k && s_ids[j] >= 0) {
+                        float part[1] = {0.f};
+                        group_dot<1>(wv[i], f16_bits_to_float(sv[i]), xs_base + uint32_t(j) * row_bytes,
+                                     g, row_bytes, part);
+                        acc = fmaf(s_r[j], part[0], acc);
+                    }
+                }
+            }
+        }
+        acc = segment_sum<LPR>(acc, mask);
+        if (lane == 0) a.y[size_t(t) * a.N + n] = float_to_f16_bits(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantize (one thread per packed word) and row-order rewrite.
+// ---------------------------------------------------------------------------
+__global__ void k_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K)
+{
+    const size_t words = size_t(N) * (K >> 3);
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += size_t(gridDim.x) * blockDim.x) {
+        uint32_t v = wq[i];
+        size_t n = i / (K >> 3), kw = i - n * (K >> 3);
+        float s = f16_bits_to_float(scales[n * (K >> 5) + (kw >> 2)]);
+        float *o = w + n * K + kw * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = float(int((v >> (4 * e)) & 0xF) - 7) * s;
+    }
+}
+
+// f16((q - 7) * s): the exact f16 (q - 7) pairs times the f16 scale pair,
+// rounded once to nearest even; the same operation the tensor-core GEMM
+// applies when it dequantizes tiles.
+__global__ void k_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N, int K)
+{
+    const size_t words = size_t(N) * (K >> 3);
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += size_t(gridDim.x) * blockDim.x) {
+        size_t n = i / (K >> 3), kw = i - n * (K >> 3);
+        uint32_t s = scales[n * (K >> 5) + (kw >> 2)];
+        uint32_t s2 = s | (s << 16);
+        uint32_t p[4];
+        unpack_word_f16x2(wq[i], p);
+        uint16_t *o = w + n * K + kw * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t d = hmul2(p[j], s2);     // elements j (low) and j + 4 (high)
+            o[j] = uint16_t(d & 0xFFFF);
+            o[j + 4] = uint16_t(d >> 16);
+        }
+    }
+}
+
+// dst row 2j <- src row j, dst row 2j+1 <- src row N/2 + j (or a plain copy).
+__global__ void k_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32_t *wq_dst,
+                          uint16_t *sc_dst, int N, int K, int interleave)
+{
+    const int KW = K >> 3, G = K >> 5, half = N >> 1;
+    const int dst_row = blockIdx.x;
+    const int src_row = interleave ? ((dst_row & 1) ? half + (dst_row >> 1) : (dst_row >> 1)) : dst_row;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(wq_src + size_t(src_row) * KW);
+    uint4 *d4 = reinterpret_cast<uint4 *>(wq_dst + size_t(dst_row) * KW);
+    for (int i = threadIdx.x; i < KW / 4; i += blockDim.x) d4[i] = s4[i];
+    for (int i = threadIdx.x; i < G; i += blockDim.x)
+        sc_dst[size_t(dst_row) * G + i] = sc_src[size_t(src_row) * G + i];
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+namespace {
+
+int pick_lpr(int K)
+{
+    int G = K >> 5;
+    return G >= 32 ? 32 : (G >= 16 ? 16 : 8);
+}
+
+// Units per CTA: one unit per row segment of the CTA, doubled while the grid
+// would still cover every SM twice (fewer, fuller CTAs stage x less often).
+int units_per_cta(int units, int lpr)
+{
+    int subs = kThreads / lpr;
+    int upc = subs;
+    int sms = sm_count();
+    while (units / (2 * upc) >= 2 * sms && upc < 8 * subs) upc *= 2;
+    return upc;
+}
+
+template <int MT, int LPR, int RU>
+cudaError_t launch_dense_t(const DenseArgs &a, cudaStream_t s)
+{
+    static int smem_set[kMaxDevices] = {};
+    auto kern = k_dense<MT, LPR, RU>;
+    size_t smem = size_t(MT) * a.K * 2;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
+    if (e != cudaSuccess) return e;
+    int grid = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+template <int MT, int RU>
+cudaError_t launch_dense_lpr(const DenseArgs &a, cudaStream_t s)
+{
+    switch (pick_lpr(a.K)) {
+    case 32: return launch_dense_t<MT, 32, RU>(a, s);
+    case 16: return launch_dense_t<MT, 16, RU>(a, s);
+    default: return launch_dense_t<MT, 8, RU>(a, s);
+    }
+}
+
+template <int RU>
+cudaError_t launch_dense_mt(int MT, const DenseArgs &a, cudaStream_t s)
+{
+    switch (MT) {
+    case 8: return launch_dense_lpr<8, RU>(a, s);
+    case 4: return launch_dense_lpr<4, RU>(a, s);
+    case 2: return launch_dense_lpr<2, RU>(a, s);
+    default: return launch_dense_lpr<1, RU>(a, s);
+    }
+}
+
+}  // namespace
+
+size_t decode_max_smem() { return 227 * 1024; }
+
+int decode_tokens_per_launch(int M, int K)
+{
+    int mt = 8;
+    while (mt > 1 && (mt > M || size_t(mt) * K * 2 > decode_max_smem())) mt >>= 1;
+    return mt;
+}
+
+cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                          uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s)
+{
+    const int RU = gate_up ? 2 : 1;
+    const int out_cols = N / RU;
+    DenseArgs a;
+    a.wq = wq;
+    a.scales = scales;
+    a.K = K;
+    a.units = out_cols;
+    a.units_per_cta = units_per_cta(a.units, pick_lpr(K));
+    a.y_stride = out_cols;
+    for (int m0 = 0; m0 < M;) {
+        int mt = decode_tokens_per_launch(M - m0, K);
+        a.x = x + size_t(m0) * K;
+        a.y = y + size_t(m0) * out_cols;
+        a.M = std::min(mt, M - m0);
+        cudaError_t e = gate_up ? launch_dense_mt<2>(mt, a, s) : launch_dense_mt<1>(mt, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += a.M;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_moe(const MoeArgs &a0, int mode, cudaStream_t s)
+{
+    MoeArgs a = a0;
+    const int lpr = pick_lpr(a.K);
+    if (mode == ZQ4_MOE_GATE_UP_SILU) {
+        a.units_per_cta = units_per_cta(a.N >> 1, lpr);
+        int gx = ((a.N >> 1) + a.units_per_cta - 1) / a.units_per_cta;
+        dim3 grid(gx, a.T * a.top_k);
+        size_t smem = size_t(a.K) * 2;
+        static int set32[kMaxDevices] = {}, set16[kMaxDevices] = {}, set8[kMaxDevices] = {};
+        cudaError_t e;
+        switch (lpr) {
+        case 32:
+            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<32>), smem, set32);
+            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<32>, grid, dim3(kThreads), smem, s, a);
+        case 16:
+            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<16>), smem, set16);
+            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<16>, grid, dim3(kThreads), smem, s, a);
+        default:
+            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<8>), smem, set8);
+            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<8>, grid, dim3(kThreads), smem, s, a);
+        }
+    }
+    a.units_per_cta = units_per_cta(a.N, lpr);
+    int gx = (a.N + a.units_per_cta - 1) / a.units_per_cta;
+    dim3 grid(gx, a.T);
+    size_t smem = size_t(a.top_k) * a.K * 2;
+    static int set32[kMaxDevices] = {}, set16[kMaxDevices] = {}, set8[kMaxDevices] = {};
+    cudaError_t e;
+    switch (lpr) {
+    case 32:
+        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<32>), smem, set32);
+        return e != cudaSuccess ? e : launch_pdl(k_moe_down<32>, grid, dim3(kThreads), smem, s, a);
+    case 16:
+        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<16>), smem, set16);
+        return e != cudaSuccess ? e : launch_pdl(k_moe_down<16>, grid, dim3(kThreads), smem, s, a);
+    default:
+        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<8>), smem, set8);
+        return e != cudaSuccess ? e : launch_pdl(k_moe_down<8>, grid, dim3(kThreads), smem, s, a);
+    }
+}
+
+static int elementwise_grid(size_t items)
+{
+    size_t blocks = (items + 255) / 256;
+    size_t cap = size_t(sm_count()) * 8;
+    return int(std::max<size_t>(1, std::min(blocks, cap)));
+}
+
+cudaError_t launch_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
+                               cudaStream_t s)
+{
+    k_dequant_f32<<<elementwise_grid(size_t(N) * (K >> 3)), 256, 0, s>>>(wq, scales, w, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N,
+                               int K, cudaStream_t s)
+{
+    k_dequant_f16<<<elementwise_grid(size_t(N) * (K >> 3)), 256, 0, s>>>(wq, scales, w, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32_t *wq_dst,
+                           uint16_t *sc_dst, int N, int K, int interleave, cudaStream_t s)
+{
+    k_prepare<<<N, 128, 0, s>>>(wq_src, sc_src, wq_dst, sc_dst, N, K, interleave);
+    return cudaGetLastError();
+}
+
+}  // namespace zq4

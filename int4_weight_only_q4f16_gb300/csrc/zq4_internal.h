@@ -1,0 +1,50 @@
+// zq4_internal.h -- declarations shared by the zq4 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace zq4 {
+
+constexpr int kMaxDevices = 64;
+
+struct DenseArgs {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;
+    uint16_t *y;
+    int M;              // activation rows in this launch (<= the kernel's MT)
+    int K;
+    int units;          // output columns: N (GEMV) or N/2 (gate_up)
+    int units_per_cta;
+    int y_stride;       // elements between output rows
+};
+
+struct MoeArgs {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;
+    uint16_t *y;
+    const int32_t *ids;
+    const float *route_w;
+    int32_t *dev_status;
+    int num_experts;
+    int T, N, K, top_k;
+    int units_per_cta;
+};
+
+// zq4_decode.cu
+int decode_tokens_per_launch(int M, int K);
+size_t decode_max_smem();
+cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                          uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
+cudaError_t launch_moe(const MoeArgs &a, int mode, cudaStream_t s);
+cudaError_t launch_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
+                               cudaStream_t s);
+cudaError_t launch_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N,
+                               int K, cudaStream_t s);
+cudaError_t launch_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32_t *wq_dst,
+                           uint16_t *sc_dst, int N, int K, int interleave, cudaStream_t s);
+
+}  // namespace zq4

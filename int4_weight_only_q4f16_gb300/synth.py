@@ -54,9 +54,9 @@ def packed_codes(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
     """Uniform random packed words, shape [N, K/8] uint32 (8 codes per word)."""
     if K % 32:
         raise ValueError("K must be a multiple of 32")
-    n = N * (K // 8)
-    words = np.frombuffer(rng.bytes(4 * n), dtype="<u4") if n else np.zeros(0, np.uint32)
-    return words.astype(np.uint32, copy=False).reshape(N, K // 8)
+    n = N * (K // 8)                      # even: K/8 is a multiple of 4
+    raw = rng.bit_generator.random_raw(n // 2)
+    return raw.astype("<u8", copy=False).view("<u4").astype(np.uint32, copy=False).reshape(N, K // 8)
 
 
 def group_scales(rng: np.random.Generator, N: int, K: int, sigma: float = 0.02) -> np.ndarray:

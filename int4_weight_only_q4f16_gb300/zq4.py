@@ -1,0 +1,188 @@
+"""Python binding of the zq4 C ABI (include/zq4.h).
+
+Argument marshalling only: every function checks that the torch tensors it
+is given are CUDA, contiguous and large enough, then calls the C entry point
+of the same name with their device pointers and the current CUDA stream.
+All arithmetic runs in the CUDA library. There is no fallback: if the
+library is not built, importing this module raises.
+
+Packed codes may be any 4-byte integer dtype (torch.int32 holding the uint32
+bits, or torch.uint32); f16 data is torch.float16; expert ids torch.int32;
+router weights torch.float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+ZQ4_OK = 0
+ZQ4_ERR_NULL = -1
+ZQ4_ERR_SHAPE = -2
+ZQ4_ERR_ALIGN = -3
+ZQ4_ERR_FLAGS = -4
+ZQ4_ERR_CUDA = -5
+ZQ4_ERR_UNSUPPORTED = -6
+ZQ4_ERR_OVERLAP = -7
+
+MOE_GATE_UP_SILU = 1
+MOE_DOWN_COMBINE = 2
+DEV_BAD_EXPERT_ID = 1
+PREP_COPY = 0
+PREP_CONCAT_TO_INTERLEAVED = 1
+
+EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_gemv",
+           "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
+           "zq4_dequant_f16")
+
+
+class Zq4Error(RuntimeError):
+    def __init__(self, fn: str, status: int, lib):
+        self.status = status
+        msg = lib.zq4_status_string(status).decode()
+        if status == ZQ4_ERR_CUDA:
+            msg += f" (cudaError {lib.zq4_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg}")
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"zq4 CUDA library not built ({path} missing): run "
+            "`python -m int4_weight_only_q4f16_gb300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.zq4_status_string.argtypes = [I]
+    lib.zq4_status_string.restype = ctypes.c_char_p
+    lib.zq4_last_cuda_error.restype = I
+    lib.zq4_version.restype = I
+    sig = {
+        "zq4_gemv": [P, P, P, P, I, I, I, P],
+        "zq4_gate_up_silu": [P, P, P, P, I, I, I, P],
+        "zq4_moe_gemv": [P, P, I, P, P, I, I, I, P, P, I, I, P, P],
+        "zq4_prepare_weight": [P, P, P, P, I, I, I, P],
+        "zq4_dequant_f32": [P, P, P, I, I, P],
+        "zq4_dequant_f16": [P, P, P, I, I, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = I
+    return lib
+
+
+lib = _load()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t, name, nbytes, elem=None):
+    """Device pointer of t after checking it can hold nbytes."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+    if elem is not None and t.element_size() != elem:
+        raise TypeError(f"{name}: expected {elem}-byte elements, got {t.dtype}")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name}: holds {t.numel() * t.element_size()} bytes, needs {nbytes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, status):
+    if status != ZQ4_OK:
+        raise Zq4Error(fn, status, lib)
+
+
+def _mat(wq, scales, N, K):
+    return (_ptr(wq, "wq", N * (K // 8) * 4, 4), _ptr(scales, "scales", N * (K // 32) * 2, 2))
+
+
+def gemv(wq, scales, x, N, K, y=None, stream=None):
+    """y[M, N] = x[M, K] @ dequant(wq, scales)^T (f16 out)."""
+    M = x.numel() // K
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    w, s = _mat(wq, scales, N, K)
+    _check("zq4_gemv", lib.zq4_gemv(w, s, _ptr(x, "x", M * K * 2, 2), _ptr(y, "y", M * N * 2, 2),
+                                    M, N, K, _stream(stream)))
+    return y
+
+
+def gate_up_silu(wq, scales, x, N2, K, h=None, stream=None):
+    """h[M, N2/2] = silu(g) * u over interleaved gate/up rows."""
+    M = x.numel() // K
+    if h is None:
+        h = torch.empty((M, N2 // 2), dtype=torch.float16, device=x.device)
+    w, s = _mat(wq, scales, N2, K)
+    _check("zq4_gate_up_silu",
+           lib.zq4_gate_up_silu(w, s, _ptr(x, "x", M * K * 2, 2),
+                                _ptr(h, "h", M * (N2 // 2) * 2, 2), M, N2, K, _stream(stream)))
+    return h
+
+
+def moe_gemv(wq_bank, scales_bank, num_experts, x, N, K, expert_ids, mode, route_w=None,
+             y=None, dev_status=None, stream=None):
+    """Expert-gather GEMV; see zq4_moe_gemv in include/zq4.h for the modes."""
+    T, top_k = expert_ids.shape
+    if mode == MOE_GATE_UP_SILU:
+        xrows, yshape = T, (T, top_k, N // 2)
+    else:
+        xrows, yshape = T * top_k, (T, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float16, device=x.device)
+    ybytes = 2
+    for d in yshape:
+        ybytes *= d
+    w = _ptr(wq_bank, "wq_bank", num_experts * N * (K // 8) * 4, 4)
+    s = _ptr(scales_bank, "scales_bank", num_experts * N * (K // 32) * 2, 2)
+    _check("zq4_moe_gemv", lib.zq4_moe_gemv(
+        w, s, num_experts, _ptr(x, "x", xrows * K * 2, 2), _ptr(y, "y", ybytes, 2), T, N, K,
+        _ptr(expert_ids, "expert_ids", T * top_k * 4, 4),
+        _ptr(route_w, "route_w", T * top_k * 4, 4), top_k, mode,
+        _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
+    return y
+
+
+def prepare_weight(wq_src, scales_src, N, K, flags=PREP_CONCAT_TO_INTERLEAVED, wq_dst=None,
+                   scales_dst=None, stream=None):
+    if wq_dst is None:
+        wq_dst = torch.empty_like(wq_src)
+    if scales_dst is None:
+        scales_dst = torch.empty_like(scales_src)
+    w, s = _mat(wq_src, scales_src, N, K)
+    wd, sd = _mat(wq_dst, scales_dst, N, K)
+    _check("zq4_prepare_weight", lib.zq4_prepare_weight(w, s, wd, sd, N, K, flags, _stream(stream)))
+    return wq_dst, scales_dst
+
+
+def dequant_f32(wq, scales, N, K, out=None, stream=None):
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=wq.device)
+    w, s = _mat(wq, scales, N, K)
+    _check("zq4_dequant_f32", lib.zq4_dequant_f32(w, s, _ptr(out, "w", N * K * 4, 4), N, K,
+                                                  _stream(stream)))
+    return out
+
+
+def dequant_f16(wq, scales, N, K, out=None, stream=None):
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=wq.device)
+    w, s = _mat(wq, scales, N, K)
+    _check("zq4_dequant_f16", lib.zq4_dequant_f16(w, s, _ptr(out, "w", N * K * 2, 2), N, K,
+                                                  _stream(stream)))
+    return out
+
+
+def status_string(status: int) -> str:
+    return lib.zq4_status_string(status).decode()

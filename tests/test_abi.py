@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads and exports every symbol include/zq4.h
+declares; host-side argument checks reject bad calls before any launch.
+CPU only: no call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "zq4.h")).read()
+    return sorted(set(re.findall(r"ZQ4_API\s+[\w\s\*]*?\b(zq4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_weight_only_q4f16_gb300 import build
+    build.build()
+    from int4_weight_only_q4f16_gb300 import zq4
+    return zq4
+
+
+def test_header_declares_the_api():
+    syms = declared_symbols()
+    for s in ("zq4_gemv", "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight",
+              "zq4_dequant_f32", "zq4_dequant_f16", "zq4_status_string"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib._build.LIB)
+    for s in declared_symbols():
+        assert hasattr(raw, s), s
+    assert set(lib.EXPORTS) == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "ZQ4_OK"
+    for st in range(-7, 0):
+        assert lib.status_string(st).startswith("ZQ4_ERR")
+    assert "unknown" in lib.status_string(-99)
+    assert lib.lib.zq4_version() >= 100
+
+
+def _call_gemv(lib, wq, sc, x, y, M, N, K):
+    P = ctypes.c_void_p
+    return lib.lib.zq4_gemv(P(wq), P(sc), P(x), P(y), M, N, K, P(0))
+
+
+def test_host_checks_reject_before_launch(lib):
+    A = 0x7F0000000000          # fake, 16-byte aligned, never dereferenced
+    B, X, Y = A + (1 << 30), A + (2 << 30), A + (3 << 30)
+    assert _call_gemv(lib, 0, B, X, Y, 1, 64, 64) == lib.ZQ4_ERR_NULL
+    assert _call_gemv(lib, A, B, X, 0, 1, 64, 64) == lib.ZQ4_ERR_NULL
+    assert _call_gemv(lib, A, B, X, Y, 1, 64, 48) == lib.ZQ4_ERR_SHAPE
+    assert _call_gemv(lib, A, B, X, Y, 0, 64, 64) == lib.ZQ4_ERR_SHAPE
+    assert _call_gemv(lib, A, B, X, Y, 1, 0, 64) == lib.ZQ4_ERR_SHAPE
+    assert _call_gemv(lib, A + 4, B, X, Y, 1, 64, 64) == lib.ZQ4_ERR_ALIGN
+    assert _call_gemv(lib, A, B, X + 2, Y, 1, 64, 64) == lib.ZQ4_ERR_ALIGN
+    assert _call_gemv(lib, A, B, X, X, 1, 64, 64) == lib.ZQ4_ERR_OVERLAP
+    assert _call_gemv(lib, A, B, X, A + 100, 1, 64, 64) == lib.ZQ4_ERR_OVERLAP
+    P = ctypes.c_void_p
+    # gate_up needs an even row count
+    assert lib.lib.zq4_gate_up_silu(P(A), P(B), P(X), P(Y), 1, 63, 64, P(0)) == lib.ZQ4_ERR_SHAPE
+    # MoE: unknown mode, missing router weights, top_k range
+    ids, r = A + (4 << 30), A + (5 << 30)
+    moe = lib.lib.zq4_moe_gemv
+    assert moe(P(A), P(B), 4, P(X), P(Y), 1, 64, 64, P(ids), P(r), 2, 9, P(0), P(0)) == lib.ZQ4_ERR_FLAGS
+    assert moe(P(A), P(B), 4, P(X), P(Y), 1, 64, 64, P(ids), P(0), 2, lib.MOE_DOWN_COMBINE,
+               P(0), P(0)) == lib.ZQ4_ERR_NULL
+    assert moe(P(A), P(B), 4, P(X), P(Y), 1, 64, 64, P(ids), P(r), 33, lib.MOE_DOWN_COMBINE,
+               P(0), P(0)) == lib.ZQ4_ERR_SHAPE
+    assert moe(P(A), P(B), 0, P(X), P(Y), 1, 64, 64, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
+               P(0), P(0)) == lib.ZQ4_ERR_SHAPE
+    # prepare: odd N for interleave, unknown flag, overlap
+    prep = lib.lib.zq4_prepare_weight
+    assert prep(P(A), P(B), P(X), P(Y), 63, 64, 1, P(0)) == lib.ZQ4_ERR_SHAPE
+    assert prep(P(A), P(B), P(X), P(Y), 64, 64, 7, P(0)) == lib.ZQ4_ERR_FLAGS
+    assert prep(P(A), P(B), P(A), P(Y), 64, 64, 1, P(0)) == lib.ZQ4_ERR_OVERLAP
+    # dequant
+    assert lib.lib.zq4_dequant_f32(P(A), P(B), P(0), 4, 64, P(0)) == lib.ZQ4_ERR_NULL
+    assert lib.lib.zq4_dequant_f16(P(A), P(B), P(Y), 4, 40, P(0)) == lib.ZQ4_ERR_SHAPE
