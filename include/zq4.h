@@ -68,6 +68,18 @@ ZQ4_API int zq4_last_cuda_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 ZQ4_API int zq4_version(void);
 
+/* Bits of the library's device error word. */
+#define ZQ4_DEVERR_WAIT_TIMEOUT 1u   /* a kernel gave up an internal wait (2 s) */
+
+/*
+ * zq4_device_errors -- read (and with clear != 0, reset) the device error
+ * word of the current device. Kernels never trap: an internal wait that runs
+ * out sets a bit here, the kernel drains its own in-flight copies and
+ * returns (its output is then undefined). SYNCHRONOUS: waits for all work
+ * on the device. Errors: ZQ4_ERR_NULL, ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_device_errors(uint32_t *flags, int clear);
+
 /*
  * zq4_gemv -- y = x * W^T, the fused dequantize + NT matmul.
  * Source: "Zero TVM Documentation", section "WGSL Kernel Roles", card 5

@@ -31,6 +31,20 @@ int sm_count()
     return v;
 }
 
+size_t smem_per_sm()
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 228 * 1024;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return size_t(v);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        v <= 0)
+        v = 228 * 1024;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return size_t(v);
+}
+
 cudaError_t ensure_smem(const void *kernel, size_t bytes, int *cache_by_device)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
@@ -105,6 +119,9 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
     if (overlap(y, ybytes, wq, wq_bytes(N, K)) || overlap(y, ybytes, scales, sc_bytes(N, K)) ||
         overlap(y, ybytes, x, size_t(M) * K * 2))
         return ZQ4_ERR_OVERLAP;
+    if (decode_tc_supported(M, K))
+        return cuda_status(launch_decode_tc(wq, scales, x, y, M, N, K, false,
+                                            static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_decode(wq, scales, x, y, M, N, K, false,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -122,6 +139,9 @@ zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const ui
     if (overlap(h, hbytes, wq, wq_bytes(N2, K)) || overlap(h, hbytes, scales, sc_bytes(N2, K)) ||
         overlap(h, hbytes, x, size_t(M) * K * 2))
         return ZQ4_ERR_OVERLAP;
+    if (decode_tc_supported(M, K))
+        return cuda_status(launch_decode_tc(wq, scales, x, h, M, N2, K, true,
+                                            static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_decode(wq, scales, x, h, M, N2, K, true,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -169,6 +189,15 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
     a.K = K;
     a.top_k = top_k;
     return cuda_status(launch_moe(a, mode, static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_device_errors(uint32_t *flags, int clear)
+{
+    if (!flags) return ZQ4_ERR_NULL;
+    unsigned v = 0;
+    zq4_status st = cuda_status(read_device_error(&v, clear != 0));
+    *flags = v;
+    return st;
 }
 
 zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src,

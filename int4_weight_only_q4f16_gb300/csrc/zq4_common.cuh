@@ -163,6 +163,38 @@ __device__ __forceinline__ void unpack_word_f16x2(uint32_t w, uint32_t p[4])
     p[3] = hfma2((w8 & 0x00F000F0u) | kMagic, kSixteenth, kNeg71);   // elements 3, 7
 }
 
+// Codes of the low 16 bits / high 16 bits of v (each byte holding one code
+// in bits 0..3) to an f16x2 of (code / 8): read as e2m3 (sign 0, exponent
+// bit = code bit 3, 3 mantissa bits), code c is c/8 exactly for c in 0..15
+// (c < 8 are the subnormals c/8, c >= 8 the normals 1 + (c-8)/8). Byte 0
+// of the half goes to the low f16.
+__device__ __forceinline__ uint32_t e2m3x2_lo(uint32_t v)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e2m3x2 %0, l;\n\t}" : "=r"(d) : "r"(v));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e2m3x2_hi(uint32_t v)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e2m3x2 %0, h;\n\t}" : "=r"(d) : "r"(v));
+    return d;
+}
+
+// Unpack one packed word into four f16x2 values holding q/8 exactly, as the
+// element pairs (0,2), (1,3), (4,6), (5,7) (low half first): one shift and
+// two masks put every code alone in a byte, four conversions do the rest.
+__device__ __forceinline__ void unpack_word_q8_f16x2(uint32_t w, uint32_t p[4])
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+    p[0] = e2m3x2_lo(lo);                         // elements 0, 2
+    p[1] = e2m3x2_lo(hi);                         // elements 1, 3
+    p[2] = e2m3x2_hi(lo);                         // elements 4, 6
+    p[3] = e2m3x2_hi(hi);                         // elements 5, 7
+}
+
 // acc_lo += lo(a) * lo(b), acc_hi += hi(a) * hi(b): f16 operands, exact
 // products, fp32 accumulation (one rounding per add).
 __device__ __forceinline__ void fma2_f16_f32(uint32_t a, uint32_t b, float &acc_lo, float &acc_hi)

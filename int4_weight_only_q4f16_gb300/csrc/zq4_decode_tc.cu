@@ -1,0 +1,487 @@
+// zq4_decode_tc.cu -- the decode GEMV for M = 1..16 on GB300: weight tiles
+// streamed by TMA into shared memory, multiply-accumulate on the tensor
+// cores.
+//
+// What it computes: y = x * W^T with W in q4f16_1 ("Zero TVM Documentation",
+// section "Q4F16 quantization format" and card 5 "int4 Matmul"), or the fused
+// gate_up + SiLU*mul epilogue (card 6 "Fused FFN") when rows are interleaved
+// gate/up pairs.
+//
+// How:
+//  * CTA = 8 compute warps + 1 producer warp; the CTA owns 16-row tiles of W
+//    (grid-stride). The producer streams a tile in stages of 16 rows x 1024
+//    columns through a 4-stage shared-memory ring: four 2D tensor-map TMA
+//    boxes of [16 rows x 128 B] of codes (128-byte swizzle) and one box of
+//    [16 rows x 32] scales per stage, completion on an mbarrier. Rows past N
+//    and columns past K are zero-filled by the TMA unit. The producer starts
+//    before griddepcontrol.wait: weights never depend on the previous kernel,
+//    so the next kernel's weight stream overlaps this one's tail.
+//  * Each compute warp takes an eighth of a stage's 32-column groups. Per
+//    group, lane (r, t) (r = lane/4, t = lane%4) unpacks word t of rows r and
+//    r+8 into f16 pairs of q/8 (exact; elements (0,2),(1,3),(4,6),(5,7) of
+//    the word) with one shift, two masks and four e2m3->f16x2 conversions:
+//    these are the A fragments of two chained m16n8k16 MMAs. The B fragment
+//    is the matching pair-permuted x chunk of token r (x staged once per CTA
+//    in shared memory). The k order inside a group is permuted identically on
+//    both operands, which leaves the dot product unchanged.
+//  * The MMA pair gives D = sum_k (q_k/8) x_k. The zero-point term
+//    E = sum_k (7/8) x_k comes from the same MMA chain on the same B
+//    registers with every A element 7/8 (a constant register, no unpack), so
+//    for a row whose codes are all 7 the two are bit-identical and the row
+//    contributes exactly 0. The running fp32 accumulator takes
+//    (8 s) * (D - E) = s * sum_k (q_k - 7) x_k per group.
+//    (Unpacking to (q - 7) directly costs 9 instead of 7 half-rate integer /
+//    f16x2 instructions per word, and that pipe bounds this loop.)
+//  * Tiles are reduced across the 8 warps through shared memory; the epilogue
+//    writes f16 y (or silu(g)*u for interleaved gate/up rows).
+//  * Every mbarrier wait is bounded in time; on expiry the kernel records
+//    ZQ4_DEVERR_WAIT_TIMEOUT, drains the copies it issued, and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "zq4_common.cuh"
+#include "zq4_internal.h"
+
+namespace zq4 {
+
+__device__ unsigned g_device_error = 0;
+
+namespace tc {
+
+// Tile parameters (compile-time; the defaults are the tuned values).
+#ifndef ZQ4_TC_WARPS
+#define ZQ4_TC_WARPS 8
+#endif
+#ifndef ZQ4_TC_STAGES
+#define ZQ4_TC_STAGES 4
+#endif
+#ifndef ZQ4_TC_OCC
+#define ZQ4_TC_OCC 2
+#endif
+#ifndef ZQ4_TC_UNROLL
+#define ZQ4_TC_UNROLL 4
+#endif
+
+constexpr int kWarps = ZQ4_TC_WARPS;              // compute warps
+constexpr int kThreads = (kWarps + 1) * 32;       // + producer warp
+constexpr int kKC = 1024;                         // columns per stage
+constexpr int kSegs = kKC / 256;                  // 128-byte code segments per row per stage
+constexpr int kSegBytes = 16 * 128;               // one swizzled [16 rows x 128 B] box
+constexpr int kScaleBytes = 16 * (kKC / 32) * 2;  // [16 rows x 32 scales]
+constexpr int kStageBytes = kSegs * kSegBytes + kScaleBytes;   // 9 KB, a multiple of 1 KB
+constexpr int kStages = ZQ4_TC_STAGES;
+constexpr int kUnrollG = ZQ4_TC_UNROLL;           // groups unrolled per loop trip
+constexpr int kGpw = (kKC / 32 + kWarps - 1) / kWarps;   // groups of a stage per warp
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kSevenEighths = 0x3B003B00u;   // f16x2 (7/8, 7/8)
+
+static_assert(kStageBytes % 1024 == 0, "stages must keep the 1 KB swizzle alignment");
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t addr, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
+                 : "memory");
+}
+
+// Wait for the phase of the given parity to complete; false once the wait
+// has lasted longer than the time limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
+{
+    const unsigned long long t0 = globaltimer();
+    for (unsigned i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 2D tensor-map TMA load of one box at (x, y) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_compute()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+
+// D = A * B + C, m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                         const float (&c)[4])
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory layout (offsets from a 1 KB aligned base)
+// ---------------------------------------------------------------------------
+__host__ __device__ inline size_t xs_row_bytes(int K) { return size_t(K) * 2 + 64; }
+constexpr size_t kRingBytes = size_t(kStages) * kStageBytes;
+constexpr size_t kMbarBytes = 128;
+template <int NB>
+__host__ __device__ inline size_t red_bytes() { return size_t(kWarps) * NB * 16 * 8 * 4; }
+__host__ __device__ inline size_t scale_bytes() { return size_t(kWarps) * kGpw * 8 * 8; }
+template <int NB>
+__host__ __device__ inline size_t smem_bytes(int M, int K)
+{
+    return 1024 /* alignment slack */ + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes() +
+           size_t(M) * xs_row_bytes(K);
+}
+
+template <int NB, int RU>
+__global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ CUtensorMap tm_codes,
+                                                        const __grid_constant__ CUtensorMap tm_scales,
+                                                        TcArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t full0 = ring + uint32_t(kRingBytes), empty0 = full0 + 8 * kStages;
+    float *red = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes);
+    float2 *sscr = reinterpret_cast<float2 *>(smem + kRingBytes + kMbarBytes + red_bytes<NB>());
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K, N = a.N;
+    uint8_t *xs = smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes();
+    const int chunks = (K + kKC - 1) / kKC;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ---------------- producer warp ----------------
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
+            for (int c = 0; c < chunks; ++c, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                // The first kStages fills need no wait and run before the
+                // previous grid completes; from then on the consumers must be
+                // past their own wait on the previous grid for a stage to free.
+                if (it == kStages) griddep_wait();
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int k0 = c * kKC, nseg = min(kKC, K - k0) / 256;
+                    const uint32_t full = full0 + 8 * s, st = ring + s * kStageBytes;
+                    mbar_arrive_expect_tx(full, uint32_t(nseg * kSegBytes + kScaleBytes));
+                    for (int g = 0; g < nseg; ++g)
+                        tma_load_2d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, tile * 16, full);
+                    tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) atomicOr(&g_device_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+        // Drain: never leave the CTA with copies in flight into its smem.
+        for (int j = max(0, it - kStages); j < it; ++j) {
+            if (!mbar_wait(full0 + 8 * (j % kStages), (j / kStages) & 1)) {
+                if (lane == 0) atomicOr(&g_device_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps ----------------
+    griddep_wait();
+    const uint32_t xrow = uint32_t(xs_row_bytes(K));
+    {
+        // Stage x[0..M): the 8 values of word chunk cw of token m are stored
+        // as the pairs (x0,x2),(x1,x3),(x4,x6),(x5,x7) the unpack produces.
+        // Loads are issued kBatch at a time so their latencies overlap.
+        constexpr int kBatch = 8;
+        const int words = K >> 3, total = a.M * words;
+        for (int i0 = threadIdx.x; i0 < total; i0 += kBatch * kWarps * 32) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = i0 + b * kWarps * 32;
+                if (i < total) {
+                    const int m = i / words, cw = i - m * words;
+                    v[b] = *reinterpret_cast<const uint4 *>(a.x + size_t(m) * K + size_t(cw) * 8);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = i0 + b * kWarps * 32;
+                if (i < total) {
+                    const int m = i / words, cw = i - m * words;
+                    uint4 o;
+                    o.x = __byte_perm(v[b].x, v[b].y, 0x5410);
+                    o.y = __byte_perm(v[b].x, v[b].y, 0x7632);
+                    o.z = __byte_perm(v[b].z, v[b].w, 0x5410);
+                    o.w = __byte_perm(v[b].z, v[b].w, 0x7632);
+                    *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
+                }
+            }
+        }
+    }
+    named_barrier_compute();
+    griddep_launch_dependents();
+    const int r = lane >> 2, t = lane & 3;
+    const uint32_t a7[4] = {kSevenEighths, kSevenEighths, kSevenEighths, kSevenEighths};
+
+    float2 *sp = sscr + warp * kGpw * 8;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        float acc[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[nb][j] = 0.f;
+        for (int c = 0; c < chunks; ++c, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (ok && !mbar_wait(full0 + 8 * s, ph)) ok = false;
+            if (ok) {
+                const int k0 = c * kKC, gc = min(kKC, K - k0) >> 5;
+                const int gpw = (gc + kWarps - 1) / kWarps;
+                const int g_lo = warp * gpw, ng = min(gc, g_lo + gpw) - g_lo;
+                const uint8_t *st = smem + s * kStageBytes;
+                // this warp's scales of the stage, as fp32 pairs 8*(s[r], s[r+8])
+                const uint16_t *scl = reinterpret_cast<const uint16_t *>(st + kSegs * kSegBytes);
+                for (int i = lane; i < ng * 8; i += 32) {
+                    const int gi = i >> 3, rp = i & 7;
+                    const float s0 = f16_bits_to_float(scl[rp * 32 + g_lo + gi]);
+                    const float s1 = f16_bits_to_float(scl[(rp + 8) * 32 + g_lo + gi]);
+                    sp[gi * 8 + rp] = make_float2(8.f * s0, 8.f * s1);
+                }
+                __syncwarp();
+                const int kg0 = (k0 >> 5) + g_lo;           // global index of the warp's first group
+                const uint8_t *xg = xs + size_t(kg0) * 64 + 16 * t;
+                const uint8_t *rowr = st + r * 128 + 4 * t;  // row r; row r+8 is 1 KB further
+#pragma unroll(kUnrollG)
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int gl = g_lo + gi;                // group within the stage
+                    const uint8_t *p = rowr + (gl >> 3) * kSegBytes + (((gl & 7) ^ r) << 4);
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(p);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p + 8 * 128);
+                    const float2 sc = sp[gi * 8 + r];
+                    uint32_t pa[4], pb[4];
+                    unpack_word_q8_f16x2(w0, pa);
+                    unpack_word_q8_f16x2(w1, pb);
+                    const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+                    const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        const int m = r + 8 * nb;
+                        uint4 xv = make_uint4(0, 0, 0, 0);
+                        if (m < a.M) xv = *reinterpret_cast<const uint4 *>(xg + size_t(m) * xrow + 64 * gi);
+                        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                        float d[4], e[4];
+                        mma16816(d, a0, xv.x, xv.y, z);
+                        mma16816(d, a1, xv.z, xv.w, d);
+                        mma16816(e, a7, xv.x, xv.y, z);     // zero-point term, same chain
+                        mma16816(e, a7, xv.z, xv.w, e);
+                        acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
+                        acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
+                        acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
+                        acc[nb][3] = fmaf(sc.y, d[3] - e[3], acc[nb][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // cross-warp reduction of the tile: red[w][nb][row][col]
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            float *rw = red + ((warp * NB + nb) * 16) * 8;
+            rw[r * 8 + 2 * t] = acc[nb][0];
+            rw[r * 8 + 2 * t + 1] = acc[nb][1];
+            rw[(r + 8) * 8 + 2 * t] = acc[nb][2];
+            rw[(r + 8) * 8 + 2 * t + 1] = acc[nb][3];
+        }
+        named_barrier_compute();
+        const int row0 = tile * 16;
+        if (RU == 1) {
+            for (int o = threadIdx.x; o < 16 * a.M; o += kWarps * 32) {
+                const int m = o >> 4, i = o & 15;
+                if (row0 + i < N) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) v += red[((w * NB + (m >> 3)) * 16 + i) * 8 + (m & 7)];
+                    a.y[size_t(m) * a.y_stride + row0 + i] = float_to_f16_bits(v);
+                }
+            }
+        } else {
+            for (int o = threadIdx.x; o < 8 * a.M; o += kWarps * 32) {
+                const int m = o >> 3, j = o & 7;
+                if (row0 + 2 * j + 1 < N) {
+                    float gv = 0.f, uv = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        const float *rw = red + ((w * NB + (m >> 3)) * 16) * 8 + (m & 7);
+                        gv += rw[(2 * j) * 8];
+                        uv += rw[(2 * j + 1) * 8];
+                    }
+                    a.y[size_t(m) * a.y_stride + (row0 >> 1) + j] = float_to_f16_bits(silu_f32(gv) * uv);
+                }
+            }
+        }
+        named_barrier_compute();
+    }
+    if (!ok && lane == 0) atomicOr(&g_device_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// Tensor maps of one q4f16_1 matrix: codes as uint32 [N][K/8] read in boxes
+// of [16 rows x 32 words] with the 128-byte swizzle, scales as uint16
+// [N][K/32] in boxes of [16 rows x 32].
+cudaError_t make_maps(const uint32_t *wq, const uint16_t *scales, int N, int K, CUtensorMap *codes,
+                      CUtensorMap *sc)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    {
+        const cuuint64_t dim[2] = {cuuint64_t(K / 8), cuuint64_t(N)};
+        const cuuint64_t stride[1] = {cuuint64_t(K / 2)};
+        const cuuint32_t box[2] = {32, 16};
+        if (enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(wq), dim, stride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dim[2] = {cuuint64_t(K / 32), cuuint64_t(N)};
+        const cuuint64_t stride[1] = {cuuint64_t(K / 16)};
+        const cuuint32_t box[2] = {32, 16};
+        if (enc(sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(scales), dim, stride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+template <int NB, int RU>
+cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgs &a, cudaStream_t s)
+{
+    static int smem_set[kMaxDevices] = {};
+    auto kern = k_decode_tc<NB, RU>;
+    const size_t smem = smem_bytes<NB>(a.M, a.K);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
+    if (e != cudaSuccess) return e;
+    // CTAs per SM by shared memory (1 KB per CTA is reserved), at most ZQ4_TC_OCC.
+    const int occ = std::max(1, std::min(ZQ4_TC_OCC, int(smem_per_sm() / (smem + 1024))));
+    const int grid = std::max(1, std::min(a.tiles, occ * sm_count()));
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, mc, ms, a);
+}
+
+}  // namespace tc
+
+bool decode_tc_supported(int M, int K)
+{
+    // Scale rows must be 16-byte multiples for the tensor map (K % 256 == 0);
+    // activations are staged whole, in blocks of up to 8 rows.
+    return K % 256 == 0 && tc::smem_bytes<1>(std::min(M, 8), K) <= 220 * 1024 && tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
+                             int M, int N, int K, bool gate_up, cudaStream_t s)
+{
+    CUtensorMap mc, ms;
+    cudaError_t e = tc::make_maps(wq, scales, N, K, &mc, &ms);
+    if (e != cudaSuccess) return e;
+    const int out_cols = gate_up ? N / 2 : N;
+    TcArgs a;
+    a.wq = wq;
+    a.scales = scales;
+    a.N = N;
+    a.K = K;
+    a.tiles = (N + 15) / 16;
+    a.y_stride = out_cols;
+    const bool fit16 = tc::smem_bytes<2>(16, K) <= 220 * 1024;
+    for (int m0 = 0; m0 < M;) {
+        const int rem = M - m0;
+        const int nb = (rem > 8 && fit16) ? 2 : 1;
+        const int mt = std::min(rem, 8 * nb);
+        a.x = x + size_t(m0) * K;
+        a.y = y + size_t(m0) * out_cols;
+        a.M = mt;
+        if (nb == 2)
+            e = gate_up ? tc::launch_t<2, 2>(mc, ms, a, s) : tc::launch_t<2, 1>(mc, ms, a, s);
+        else
+            e = gate_up ? tc::launch_t<1, 2>(mc, ms, a, s) : tc::launch_t<1, 1>(mc, ms, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t read_device_error(unsigned *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace zq4

@@ -34,6 +34,24 @@ struct MoeArgs {
     int units_per_cta;
 };
 
+struct TcArgs {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;
+    uint16_t *y;
+    int M, N, K;
+    int tiles;          // 16-row tiles of W
+    int y_stride;       // elements between output rows
+};
+
+size_t smem_per_sm();      // shared memory per SM of the current device (cached)
+
+// zq4_decode_tc.cu
+bool decode_tc_supported(int M, int K);
+cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                             uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
+cudaError_t read_device_error(unsigned *flags, bool clear);
+
 // zq4_decode.cu
 int decode_tokens_per_launch(int M, int K);
 size_t decode_max_smem();

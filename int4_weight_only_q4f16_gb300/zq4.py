@@ -34,7 +34,7 @@ DEV_BAD_EXPERT_ID = 1
 PREP_COPY = 0
 PREP_CONCAT_TO_INTERLEAVED = 1
 
-EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_gemv",
+EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
            "zq4_dequant_f16")
 
@@ -60,6 +60,8 @@ def _load():
     lib.zq4_status_string.restype = ctypes.c_char_p
     lib.zq4_last_cuda_error.restype = I
     lib.zq4_version.restype = I
+    lib.zq4_device_errors.argtypes = [P, I]
+    lib.zq4_device_errors.restype = I
     sig = {
         "zq4_gemv": [P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu": [P, P, P, P, I, I, I, P],
@@ -182,6 +184,13 @@ def dequant_f16(wq, scales, N, K, out=None, stream=None):
     _check("zq4_dequant_f16", lib.zq4_dequant_f16(w, s, _ptr(out, "w", N * K * 2, 2), N, K,
                                                   _stream(stream)))
     return out
+
+
+def device_errors(clear: bool = True) -> int:
+    """Device error word (ZQ4_DEVERR_* bits); synchronises the device."""
+    v = ctypes.c_uint32(0)
+    _check("zq4_device_errors", lib.zq4_device_errors(ctypes.byref(v), int(clear)))
+    return int(v.value)
 
 
 def status_string(status: int) -> str:

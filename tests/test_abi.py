@@ -83,3 +83,4 @@ def test_host_checks_reject_before_launch(lib):
     # dequant
     assert lib.lib.zq4_dequant_f32(P(A), P(B), P(0), 4, 64, P(0)) == lib.ZQ4_ERR_NULL
     assert lib.lib.zq4_dequant_f16(P(A), P(B), P(Y), 4, 40, P(0)) == lib.ZQ4_ERR_SHAPE
+    assert lib.lib.zq4_device_errors(P(0), 1) == lib.ZQ4_ERR_NULL

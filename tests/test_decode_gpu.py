@@ -68,6 +68,21 @@ def test_gemv_constant_codes_closed_form(zq4, oracle):
             assert np.all(y == 0)
 
 
+@pytest.mark.parametrize("K", [256, 3072, 8192])
+def test_all_zero_point_codes_give_exact_zero(zq4, K):
+    """Codes all 7 make every weight exactly 0: S = 0, so the output must be
+    exactly 0 even for large activations (no bias-cancellation residue)."""
+    N, M = 48, 3
+    rng = synth.rng_for("zp7", K)
+    x = (rng.standard_normal((M, K)) * 300).astype(np.float16)
+    wq = np.full((N, K // 8), 0x77777777, np.uint32)
+    sc = synth.group_scales(rng, N, K)
+    y = host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K))
+    assert np.all(y == 0)
+    h = host_f16(zq4.gate_up_silu(dev(wq), dev(sc), dev(x), N, K))
+    assert np.all(h == 0)
+
+
 def test_gemv_reproducible_and_linear(zq4):
     M, N, K = 3, 257, 3072
     wq, sc, x = _case("repro", M, N, K)
@@ -158,3 +173,8 @@ def test_subnormal_and_zero_scales(zq4, oracle):
     y = zq4.gemv(dev(wq), dev(sc), dev(x), N, K)
     y_ref, S = oracle.gemv(wq, sc, x, N, K)
     assert_within(host_f16(y), y_ref, S, "subnormal scales")
+
+
+def test_no_device_errors_recorded(zq4):
+    """No kernel run so far gave up an internal wait."""
+    assert zq4.device_errors(clear=True) == 0

@@ -24,7 +24,7 @@ def _bank(tag, E, N, K):
 
 
 @pytest.mark.parametrize("E,T,top_k,I,D", [(8, 1, 2, 32, 64), (16, 4, 8, 64, 128),
-                                           (128, 3, 8, 96, 64), (5, 6, 5, 48, 96),
+                                           (128, 3, 8, 96, 64), (5, 6, 5, 96, 96),
                                            (4, 2, 1, 32, 32)])
 def test_moe_two_stage_parity(zq4, oracle, E, T, top_k, I, D):
     gq, gs = _bank("moe_gu", E, 2 * I, D)     # gate_up: [2I, D] per expert
