@@ -41,7 +41,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
-    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe"])
+    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel"])
+    ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
+    ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
+    ap.add_argument("--gate-up", action="store_true", help="kernel workload: fused gate_up + SiLU*mul")
+    ap.add_argument("--copies", type=int, default=8, help="distinct weight copies (kernel workload)")
+    ap.add_argument("--eager", action="store_true", help="kernel workload: plain launches, no graph")
     ap.add_argument("--m", type=int, default=1, help="tokens per step (qwen3 workload)")
     ap.add_argument("--t", type=int, default=16, help="tokens per step (moe workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -497,6 +502,46 @@ def run_moe(args, torch, dist, peaks, peak_kind):
             "config": {"workload": f"MoE 128 experts top-8, T={T}", "banks": banks}}
 
 
+def run_kernel(args, torch, dist, peaks, peak_kind):
+    """One projection shape: `copies` distinct matrices called in turn (a CUDA
+    graph of them, or plain launches with --eager, e.g. under a profiler)."""
+    from int4_weight_only_q4f16_gb300 import synth, zq4
+    N, K, M, C = args.n, args.k, args.m, args.copies
+    wq, sc = synth.weight("kernel", N, K, 0)
+    W = torch.from_numpy(wq.view(np.int32)).cuda().repeat(C, 1).view(C, N, K // 8)
+    S = torch.from_numpy(sc).cuda().repeat(C, 1).view(C, N, K // 32)
+    x = torch.from_numpy(synth.activations(synth.rng_for("kernel_x"), M, K)).cuda()
+    cols = N // 2 if args.gate_up else N
+    y = torch.empty((C, M, cols), dtype=torch.float16, device="cuda")
+    f = zq4.gate_up_silu if args.gate_up else zq4.gemv
+    stream = torch.cuda.Stream()
+
+    def chain():
+        for c in range(C):
+            f(W[c], S[c], x, N, K, y[c], stream=stream)
+    reps = max(1, args.steps // C)
+    if args.eager:
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                chain()
+        el = time_replays(torch, chain, reps, stream)
+    else:
+        with torch.cuda.stream(stream):
+            chain()
+        g = capture(torch, chain, stream)
+        replay_on(torch, g, stream, max(3, args.warmup))
+        el = time_replays(torch, g.replay, reps, stream)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all() and (y != 0).any(), "kernel output zero/non-finite"
+    per = el / (reps * C)
+    b = N * (K // 8) * 4 + N * (K // 32) * 2 + M * K * 2 + M * cols * 2
+    return {"metric": f"{'gate_up+SiLU' if args.gate_up else 'GEMV'} {N}x{K} M={M} achieved HBM GB/s",
+            "value": round(b / per / 1e9, 1), "unit": "GB/s", "us_per_call": round(per * 1e6, 3),
+            "bytes_per_call": b, "frac_of_measured": round(b / per / 1e9 / peaks["hbm_gbs"], 4),
+            "config": {"workload": f"kernel {N}x{K} M={M}", "copies": C, "graph": not args.eager,
+                       "l2": f"{C} distinct copies, {C * b / 1e6:.0f} MB"}}
+
+
 def run_reference(args, dist):
     """The CPU oracle on the host cores, timed on a bounded sample of the
     Phi-3 stack; each step covers the same row sample."""
@@ -566,7 +611,8 @@ def main():
         return 1
     torch.cuda.set_device(dist.local)
     peaks, kind = measured_peaks()
-    fn = {"phi3": run_phi3, "gemv3072": run_gemv3072, "qwen3": run_qwen3, "moe": run_moe}[args.workload]
+    fn = {"phi3": run_phi3, "gemv3072": run_gemv3072, "qwen3": run_qwen3, "moe": run_moe,
+          "kernel": run_kernel}[args.workload]
     line = fn(args, torch, dist, peaks, kind)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
