@@ -189,7 +189,10 @@ def profiled_traffic(kernel_tag: str):
     for line in open(path):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`"):
+                v = v[1:].split("`", 1)[0]
+            vals[k.strip()] = v
     if vals.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:

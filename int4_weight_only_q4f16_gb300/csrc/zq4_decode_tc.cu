@@ -15,23 +15,28 @@
 //    [16 rows x 32] scales per stage, completion on an mbarrier. Rows past N
 //    and columns past K are zero-filled by the TMA unit. The producer starts
 //    before griddepcontrol.wait: weights never depend on the previous kernel,
-//    so the next kernel's weight stream overlaps this one's tail.
+//    so the next kernel's weight stream overlaps this one's tail. Beyond the
+//    ring it keeps a window of 16 stages requested into L2 with tensor-map
+//    prefetches (loaded DRAM latency on GB300 is ~3 us; ring refills then hit
+//    L2).
 //  * Each compute warp takes an eighth of a stage's 32-column groups. Per
 //    group, lane (r, t) (r = lane/4, t = lane%4) unpacks word t of rows r and
-//    r+8 into f16 pairs of q/8 (exact; elements (0,2),(1,3),(4,6),(5,7) of
-//    the word) with one shift, two masks and four e2m3->f16x2 conversions:
-//    these are the A fragments of two chained m16n8k16 MMAs. The B fragment
-//    is the matching pair-permuted x chunk of token r (x staged once per CTA
-//    in shared memory). The k order inside a group is permuted identically on
-//    both operands, which leaves the dot product unchanged.
-//  * The MMA pair gives D = sum_k (q_k/8) x_k. The zero-point term
-//    E = sum_k (7/8) x_k comes from the same MMA chain on the same B
-//    registers with every A element 7/8 (a constant register, no unpack), so
-//    for a row whose codes are all 7 the two are bit-identical and the row
-//    contributes exactly 0. The running fp32 accumulator takes
-//    (8 s) * (D - E) = s * sum_k (q_k - 7) x_k per group.
-//    (Unpacking to (q - 7) directly costs 9 instead of 7 half-rate integer /
-//    f16x2 instructions per word, and that pipe bounds this loop.)
+//    r+8 into four f16 pairs that are the A fragments of two chained
+//    m16n8k16 MMAs; the B fragment is the matching pair-permuted x chunk of
+//    token r (x staged once per CTA in shared memory). The k order inside a
+//    group is permuted identically on both operands, which leaves the dot
+//    product unchanged. The group's fp32 MMA result is scaled by the fp32
+//    group scale into a running fp32 accumulator.
+//  * Unpack forms (ZQ4_TC_UNPACK): 0 (default) gives exact (q - 7) pairs
+//    (0,4),(1,5),(2,6),(3,7) with one shift, four LOP3 and four f16x2 ops per
+//    word. 1 and 2 give exact q/8 pairs (0,2),(1,3),(4,6),(5,7) with one
+//    shift, two masks and four e2m3->f16x2 conversions (a code alone in a
+//    byte read as e2m3 is q/8), two fewer half-rate instructions per word;
+//    the zero-point term sum (7/8) x then comes from the same MMA chain with
+//    every A element 7/8 (inline in form 1, once per CTA in form 2), so a row
+//    of all-7 codes still gives exactly 0. The exact form is the default: in
+//    the latency-bound regime measured here the zero-point work costs more
+//    than the saved instructions.
 //  * Tiles are reduced across the 8 warps through shared memory; the epilogue
 //    writes f16 y (or silu(g)*u for interleaved gate/up rows).
 //  * Every mbarrier wait is bounded in time; on expiry the kernel records
@@ -65,19 +70,35 @@ namespace tc {
 #ifndef ZQ4_TC_UNROLL
 #define ZQ4_TC_UNROLL 4
 #endif
+// Unpack form: 0 = exact (q - 7) (no zero-point term), 1 = q/8 via e2m3 with
+// the zero-point MMA chain inline, 2 = q/8 via e2m3 with the zero-point term
+// computed once per CTA.
+#ifndef ZQ4_TC_UNPACK
+#define ZQ4_TC_UNPACK 0
+#endif
+#ifndef ZQ4_TC_KC
+#define ZQ4_TC_KC 1024
+#endif
+// Stages of L2 look-ahead beyond the shared-memory ring.
+#ifndef ZQ4_TC_PREFETCH
+#define ZQ4_TC_PREFETCH 16
+#endif
 
 constexpr int kWarps = ZQ4_TC_WARPS;              // compute warps
 constexpr int kThreads = (kWarps + 1) * 32;       // + producer warp
-constexpr int kKC = 1024;                         // columns per stage
+constexpr int kKC = ZQ4_TC_KC;                    // columns per stage
 constexpr int kSegs = kKC / 256;                  // 128-byte code segments per row per stage
 constexpr int kSegBytes = 16 * 128;               // one swizzled [16 rows x 128 B] box
-constexpr int kScaleBytes = 16 * (kKC / 32) * 2;  // [16 rows x 32 scales]
+constexpr int kScaleCols = kKC / 32;              // scales per row per stage
+constexpr int kScaleBytes = 16 * kScaleCols * 2;  // [16 rows x kScaleCols scales]
 constexpr int kStageBytes = kSegs * kSegBytes + kScaleBytes;   // 9 KB, a multiple of 1 KB
 constexpr int kStages = ZQ4_TC_STAGES;
 constexpr int kUnrollG = ZQ4_TC_UNROLL;           // groups unrolled per loop trip
 constexpr int kGpw = (kKC / 32 + kWarps - 1) / kWarps;   // groups of a stage per warp
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint32_t kSevenEighths = 0x3B003B00u;   // f16x2 (7/8, 7/8)
+constexpr int kUnpack = ZQ4_TC_UNPACK;
+constexpr int kPrefetch = ZQ4_TC_PREFETCH;
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1 KB swizzle alignment");
 
@@ -123,6 +144,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
     }
 }
 
+// Bring the box at (x, y) of a tensor map into L2 (no shared memory).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2D tensor-map TMA load of one box at (x, y) into shared memory.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t mbar)
@@ -159,11 +189,15 @@ constexpr size_t kMbarBytes = 128;
 template <int NB>
 __host__ __device__ inline size_t red_bytes() { return size_t(kWarps) * NB * 16 * 8 * 4; }
 __host__ __device__ inline size_t scale_bytes() { return size_t(kWarps) * kGpw * 8 * 8; }
+// zero-point term of every (group, token): E[g][m] = sum_k in g (7/8) x[m,k]
+template <int NB>
+__host__ __device__ inline size_t zp_bytes(int K) { return kUnpack == 2 ? size_t(K / 32) * 8 * NB * 4 : 0; }
+
 template <int NB>
 __host__ __device__ inline size_t smem_bytes(int M, int K)
 {
     return 1024 /* alignment slack */ + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes() +
-           size_t(M) * xs_row_bytes(K);
+           zp_bytes<NB>(K) + size_t(M) * xs_row_bytes(K);
 }
 
 template <int NB, int RU>
@@ -179,7 +213,8 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     float2 *sscr = reinterpret_cast<float2 *>(smem + kRingBytes + kMbarBytes + red_bytes<NB>());
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = a.K, N = a.N;
-    uint8_t *xs = smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes();
+    float *zp = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes());
+    uint8_t *xs = smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes() + zp_bytes<NB>(K);
     const int chunks = (K + kKC - 1) / kKC;
 
     if (threadIdx.x == 0) {
@@ -193,6 +228,20 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
 
     if (warp == kWarps) {
         // ---------------- producer warp ----------------
+        // Stage j of this CTA is chunk j % chunks of tile blockIdx + (j / chunks) * grid.
+        const int nstage = ((a.tiles - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x)) * chunks;
+        auto prefetch_stage = [&](int j) {
+            if (j >= nstage) return;
+            const int tile = blockIdx.x + (j / chunks) * gridDim.x, k0 = (j % chunks) * kKC;
+            const int nseg = min(kKC, K - k0) / 256;
+            for (int g = 0; g < nseg; ++g) tma_prefetch_2d(&tm_codes, (k0 >> 3) + 32 * g, tile * 16);
+            tma_prefetch_2d(&tm_scales, k0 >> 5, tile * 16);
+        };
+        // L2 look-ahead: the stages after the ring's first fill are requested
+        // from DRAM now (before the grid-dependency wait), so ring refills
+        // later hit L2 instead of paying the DRAM latency.
+        if (lane == 0)
+            for (int j = kStages; j < kStages + kPrefetch; ++j) prefetch_stage(j);
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
@@ -214,6 +263,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     for (int g = 0; g < nseg; ++g)
                         tma_load_2d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, tile * 16, full);
                     tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                    if (it >= kStages) prefetch_stage(it + kPrefetch);   // keep the window moving
                 }
                 __syncwarp();
             }
@@ -240,6 +290,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
         const int words = K >> 3, total = a.M * words;
         for (int i0 = threadIdx.x; i0 < total; i0 += kBatch * kWarps * 32) {
             uint4 v[kBatch];
+            // exact unpack pairs elements (i, i+4); the e2m3 unpack (0,2),(1,3),(4,6),(5,7)
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
                 const int i = i0 + b * kWarps * 32;
@@ -254,10 +305,17 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 if (i < total) {
                     const int m = i / words, cw = i - m * words;
                     uint4 o;
-                    o.x = __byte_perm(v[b].x, v[b].y, 0x5410);
-                    o.y = __byte_perm(v[b].x, v[b].y, 0x7632);
-                    o.z = __byte_perm(v[b].z, v[b].w, 0x5410);
-                    o.w = __byte_perm(v[b].z, v[b].w, 0x7632);
+                    if (kUnpack == 0) {
+                        o.x = __byte_perm(v[b].x, v[b].z, 0x5410);
+                        o.y = __byte_perm(v[b].x, v[b].z, 0x7632);
+                        o.z = __byte_perm(v[b].y, v[b].w, 0x5410);
+                        o.w = __byte_perm(v[b].y, v[b].w, 0x7632);
+                    } else {
+                        o.x = __byte_perm(v[b].x, v[b].y, 0x5410);
+                        o.y = __byte_perm(v[b].x, v[b].y, 0x7632);
+                        o.z = __byte_perm(v[b].z, v[b].w, 0x5410);
+                        o.w = __byte_perm(v[b].z, v[b].w, 0x7632);
+                    }
                     *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
                 }
             }
@@ -266,6 +324,35 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     named_barrier_compute();
     griddep_launch_dependents();
     const int r = lane >> 2, t = lane & 3;
+    {
+        // Zero-point term of every (group, token): the main loop's MMA chain
+        // on the same B fragments with every A element 7/8, so that a row of
+        // all-7 codes gives bit-identical D and E. Four groups are kept in
+        // flight per warp; lanes of row 0 store.
+        const uint32_t a7[4] = {kSevenEighths, kSevenEighths, kSevenEighths, kSevenEighths};
+        const int G = kUnpack == 2 ? K >> 5 : 0;
+        for (int g0 = warp; g0 < G; g0 += 4 * kWarps) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = g0 + u * kWarps;
+                if (g < G) {
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        const int m = r + 8 * nb;
+                        uint4 xv = make_uint4(0, 0, 0, 0);
+                        if (m < a.M)
+                            xv = *reinterpret_cast<const uint4 *>(xs + size_t(m) * xrow + size_t(g) * 64 + 16 * t);
+                        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                        float e[4];
+                        mma16816(e, a7, xv.x, xv.y, z);
+                        mma16816(e, a7, xv.z, xv.w, e);
+                        if (r == 0) *reinterpret_cast<float2 *>(zp + (g * NB + nb) * 8 + 2 * t) = make_float2(e[0], e[1]);
+                    }
+                }
+            }
+        }
+    }
+    if (kUnpack == 2) named_barrier_compute();
     const uint32_t a7[4] = {kSevenEighths, kSevenEighths, kSevenEighths, kSevenEighths};
 
     float2 *sp = sscr + warp * kGpw * 8;
@@ -290,13 +377,15 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 const uint16_t *scl = reinterpret_cast<const uint16_t *>(st + kSegs * kSegBytes);
                 for (int i = lane; i < ng * 8; i += 32) {
                     const int gi = i >> 3, rp = i & 7;
-                    const float s0 = f16_bits_to_float(scl[rp * 32 + g_lo + gi]);
-                    const float s1 = f16_bits_to_float(scl[(rp + 8) * 32 + g_lo + gi]);
-                    sp[gi * 8 + rp] = make_float2(8.f * s0, 8.f * s1);
+                    const float s0 = f16_bits_to_float(scl[rp * kScaleCols + g_lo + gi]);
+                    const float s1 = f16_bits_to_float(scl[(rp + 8) * kScaleCols + g_lo + gi]);
+                    const float f = kUnpack == 0 ? 1.f : 8.f;
+                    sp[gi * 8 + rp] = make_float2(f * s0, f * s1);
                 }
                 __syncwarp();
                 const int kg0 = (k0 >> 5) + g_lo;           // global index of the warp's first group
                 const uint8_t *xg = xs + size_t(kg0) * 64 + 16 * t;
+                const float *zg = zp + size_t(kg0) * NB * 8 + 2 * t;
                 const uint8_t *rowr = st + r * 128 + 4 * t;  // row r; row r+8 is 1 KB further
 #pragma unroll(kUnrollG)
                 for (int gi = 0; gi < ng; ++gi) {
@@ -306,8 +395,13 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p + 8 * 128);
                     const float2 sc = sp[gi * 8 + r];
                     uint32_t pa[4], pb[4];
-                    unpack_word_q8_f16x2(w0, pa);
-                    unpack_word_q8_f16x2(w1, pb);
+                    if (kUnpack == 0) {
+                        unpack_word_f16x2(w0, pa);
+                        unpack_word_f16x2(w1, pb);
+                    } else {
+                        unpack_word_q8_f16x2(w0, pa);
+                        unpack_word_q8_f16x2(w1, pb);
+                    }
                     const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
                     const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
@@ -316,11 +410,18 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                         uint4 xv = make_uint4(0, 0, 0, 0);
                         if (m < a.M) xv = *reinterpret_cast<const uint4 *>(xg + size_t(m) * xrow + 64 * gi);
                         const float z[4] = {0.f, 0.f, 0.f, 0.f};
-                        float d[4], e[4];
+                        float d[4];
                         mma16816(d, a0, xv.x, xv.y, z);
                         mma16816(d, a1, xv.z, xv.w, d);
-                        mma16816(e, a7, xv.x, xv.y, z);     // zero-point term, same chain
-                        mma16816(e, a7, xv.z, xv.w, e);
+                        float e[4] = {0.f, 0.f, 0.f, 0.f};
+                        if (kUnpack == 1) {
+                            mma16816(e, a7, xv.x, xv.y, z);
+                            mma16816(e, a7, xv.z, xv.w, e);
+                        } else if (kUnpack == 2) {
+                            const float2 ev = *reinterpret_cast<const float2 *>(zg + (gi * NB + nb) * 8);
+                            e[0] = e[2] = ev.x;
+                            e[1] = e[3] = ev.y;
+                        }
                         acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
                         acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
                         acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
@@ -393,7 +494,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // Tensor maps of one q4f16_1 matrix: codes as uint32 [N][K/8] read in boxes
 // of [16 rows x 32 words] with the 128-byte swizzle, scales as uint16
-// [N][K/32] in boxes of [16 rows x 32].
+// [N][K/32] in boxes of [16 rows x kScaleCols].
 cudaError_t make_maps(const uint32_t *wq, const uint16_t *scales, int N, int K, CUtensorMap *codes,
                       CUtensorMap *sc)
 {
@@ -412,7 +513,7 @@ cudaError_t make_maps(const uint32_t *wq, const uint16_t *scales, int N, int K, 
     {
         const cuuint64_t dim[2] = {cuuint64_t(K / 32), cuuint64_t(N)};
         const cuuint64_t stride[1] = {cuuint64_t(K / 16)};
-        const cuuint32_t box[2] = {32, 16};
+        const cuuint32_t box[2] = {cuuint32_t(kScaleCols), 16};
         if (enc(sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(scales), dim, stride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
