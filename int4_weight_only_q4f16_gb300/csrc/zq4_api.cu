@@ -114,11 +114,14 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
     if (!x || !y) return ZQ4_ERR_NULL;
     if (M <= 0) return ZQ4_ERR_SHAPE;
     if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 1)) return ZQ4_ERR_ALIGN;
-    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    if (!prefill_supported(M, K) && size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
     size_t ybytes = size_t(M) * N * 2;
     if (overlap(y, ybytes, wq, wq_bytes(N, K)) || overlap(y, ybytes, scales, sc_bytes(N, K)) ||
         overlap(y, ybytes, x, size_t(M) * K * 2))
         return ZQ4_ERR_OVERLAP;
+    if (prefill_supported(M, K))
+        return cuda_status(launch_prefill(wq, scales, x, y, M, N, K, false,
+                                          static_cast<cudaStream_t>(stream)));
     if (decode_tc_supported(M, K))
         return cuda_status(launch_decode_tc(wq, scales, x, y, M, N, K, false,
                                             static_cast<cudaStream_t>(stream)));
@@ -134,11 +137,14 @@ zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const ui
     if (!x || !h) return ZQ4_ERR_NULL;
     if (M <= 0 || (N2 & 1)) return ZQ4_ERR_SHAPE;
     if (!aligned16(x) || (reinterpret_cast<uintptr_t>(h) & 1)) return ZQ4_ERR_ALIGN;
-    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    if (!prefill_supported(M, K) && size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
     size_t hbytes = size_t(M) * (N2 / 2) * 2;
     if (overlap(h, hbytes, wq, wq_bytes(N2, K)) || overlap(h, hbytes, scales, sc_bytes(N2, K)) ||
         overlap(h, hbytes, x, size_t(M) * K * 2))
         return ZQ4_ERR_OVERLAP;
+    if (prefill_supported(M, K))
+        return cuda_status(launch_prefill(wq, scales, x, h, M, N2, K, true,
+                                          static_cast<cudaStream_t>(stream)));
     if (decode_tc_supported(M, K))
         return cuda_status(launch_decode_tc(wq, scales, x, h, M, N2, K, true,
                                             static_cast<cudaStream_t>(stream)));
@@ -194,9 +200,10 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
 zq4_status zq4_device_errors(uint32_t *flags, int clear)
 {
     if (!flags) return ZQ4_ERR_NULL;
-    unsigned v = 0;
+    unsigned v = 0, vp = 0;
     zq4_status st = cuda_status(read_device_error(&v, clear != 0));
-    *flags = v;
+    if (st == ZQ4_OK) st = cuda_status(read_prefill_error(&vp, clear != 0));
+    *flags = v | vp;
     return st;
 }
 

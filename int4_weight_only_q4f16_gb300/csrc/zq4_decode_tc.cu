@@ -577,6 +577,8 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
     return cudaSuccess;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return tc::encode_fn(); }
+
 cudaError_t read_device_error(unsigned *flags, bool clear)
 {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error, sizeof(unsigned));

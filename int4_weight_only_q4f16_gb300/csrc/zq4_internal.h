@@ -52,6 +52,14 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
                              uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t read_device_error(unsigned *flags, bool clear);
 
+// zq4_prefill_tc.cu: the tensor-core GEMM for chunks of kPrefillMinRows or
+// more activation rows
+constexpr int kPrefillMinRows = 64;
+bool prefill_supported(int M, int K);
+cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
+                           int M, int N, int K, bool gate_up, cudaStream_t s);
+cudaError_t read_prefill_error(unsigned *flags, bool clear);
+
 // zq4_decode.cu
 int decode_tokens_per_launch(int M, int K);
 size_t decode_max_smem();

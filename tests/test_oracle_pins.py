@@ -76,6 +76,21 @@ def test_f16_encode_round_to_nearest_even(oracle):
     assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
 
 
+def test_tolerance_admits_correctly_rounded_f16_outputs():
+    """The outputs are f16, so the parity bar must admit f16_rn(y_ref) for
+    every y_ref in f16 range, normal or subnormal, even with S = 0 (numpy's
+    f16 conversion as the rounding)."""
+    rng = np.random.default_rng(11)
+    y = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-12, 4, 20000),
+                        (np.arange(0, 200) + 0.5) * 2.0 ** -24, [0.0, 2.0 ** -25, 6.5e4]])
+    err = np.abs(y.astype(np.float16).astype(np.float64) - y)
+    assert np.all(err <= oracle_mod.tolerance(y, np.zeros_like(y)))
+    # and the absolute term is no larger than it must be: half the f16
+    # subnormal spacing, attained at an exact tie
+    t = 2.0 ** -25
+    assert oracle_mod.tolerance(0.0, 0.0) == t
+
+
 # --------------------------------------------------------------------------
 # the format, from the golden fixtures
 # --------------------------------------------------------------------------

@@ -1,0 +1,184 @@
+"""GPU parity of the prefill-chunk path (M >= 64: the tensor-core GEMM that
+dequantizes weight tiles into shared memory) against the CPU oracle.
+
+Two bars:
+  * a tight bar against the pages' own arithmetic for this path, where each
+    weight is dequantized to f16 with one rounding of (q - 7) * s and the
+    products are summed in fp32: |y - y16| <= 2^-10 |y16| + 2^-16 sum|x*w16|,
+    with y16 = sum x * f16(w) in fp64 (f16 output rounding plus fp32
+    accumulation; a wrong index, group or scale misses it by far). Every case.
+  * the stated tolerance against the oracle's exact fp64 result,
+    |y - y_ref| <= 2^-10 |y_ref| + 1e-4 sum|x*w|, for K >= 256. The f16
+    rounding of each weight (relative error up to 2^-11) averages out over a
+    long dot product, but not over a handful of groups: evaluated on the
+    oracle alone, f16-dequantized weights put 23 of 12,800 outputs outside
+    this bar at K = 32 and 1 at K = 96, none at K >= 256 (worst 0.28 of the
+    bar at K = 3072). All the workloads' K are 2048 or more.
+"""
+import numpy as np
+import pytest
+import torch
+
+from int4_weight_only_q4f16_gb300 import synth
+from helpers import assert_within, dev, host_f16
+
+pytestmark = pytest.mark.gpu
+
+STATED_BAR_MIN_K = 256
+
+
+@pytest.fixture(scope="module")
+def zq4():
+    from int4_weight_only_q4f16_gb300 import zq4 as m
+    return m
+
+
+def _case(tag, M, N, K):
+    rng = synth.rng_for(tag, M, N, K)
+    return synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K), synth.activations(rng, M, K)
+
+
+def _y16(oracle, wq, sc, x, N, K, rows=None):
+    """sum_k x * f16_rn((q-7) s) in fp64, and the matching sum|x * w16|."""
+    if rows is not None:
+        wq, sc = wq[rows], sc[rows]
+        N = len(rows)
+    w16 = oracle.round_f16(oracle.dequant(wq, sc, N, K).ravel()).reshape(N, K).astype(np.float64)
+    x64 = x.astype(np.float64)
+    return x64 @ w16.T, np.abs(x64) @ np.abs(w16).T
+
+
+def _check(oracle, y, wq, sc, x, N, K, what, rows=None):
+    if K >= STATED_BAR_MIN_K:
+        y_ref, S = oracle.gemv(wq, sc, x, N, K, rows=rows)
+        assert_within(y, y_ref, S, what)
+    y16, S16 = _y16(oracle, wq, sc, x, N, K, rows)
+    assert_within(y, y16, S16, what + " (f16 dequant)", bound=np.ldexp(np.abs(y16), -10) + np.ldexp(S16, -16))
+
+
+# (M, N, K): M from the 64-row threshold up, ragged in M (tiles of 128), N
+# (tiles of 256) and K (stages of 64; K % 64 == 32 leaves a half stage)
+SHAPES = [
+    (64, 256, 256), (65, 300, 544), (64, 1, 32), (127, 17, 96), (128, 512, 1024),
+    (129, 257, 64), (200, 520, 3072), (300, 260, 2560), (256, 768, 8192), (1024, 384, 3072),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_prefill_gemm_parity(zq4, oracle, M, N, K):
+    wq, sc, x = _case("prefill", M, N, K)
+    y = host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K))
+    _check(oracle, y, wq, sc, x, N, K, f"prefill M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,I,K", [(64, 128, 512), (130, 100, 3072), (257, 24, 288), (1024, 136, 3072)])
+def test_prefill_gate_up_parity(zq4, oracle, M, I, K):
+    wq, sc, x = _case("prefill_gu", M, 2 * I, K)
+    h = host_f16(zq4.gate_up_silu(dev(wq), dev(sc), dev(x), 2 * I, K))
+    h_ref, Sh = oracle.gate_up_silu(wq, sc, x, 2 * I, K, interleaved=True)
+    assert_within(h, h_ref, Sh, f"prefill gate_up M={M} I={I} K={K}")
+
+
+def test_prefill_one_hot_bit_exact(zq4, oracle):
+    """x rows = e_k: each output is one product 1 * f16(w[n, k]), exact in
+    fp32, so y must equal the f16-rounded dequantized weight bit for bit."""
+    N, K = 300, 512
+    wq, sc, _ = _case("pf_onehot", 1, N, K)
+    ks = np.array([0, 1, 7, 8, 31, 32, 63, 64, 65, 127, 128, 300, 511] * 5)
+    M = len(ks)
+    x = np.zeros((M, K), np.float16)
+    x[np.arange(M), ks] = 1.0
+    y = host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K))
+    want = oracle.round_f16(oracle.dequant(wq, sc, N, K).ravel()).reshape(N, K)
+    assert np.array_equal(y.view(np.uint16), want[:, ks].T.view(np.uint16))
+
+
+def test_prefill_all_zero_point_codes_exact_zero(zq4):
+    M, N, K = 96, 300, 3072
+    rng = synth.rng_for("pf_zp7", K)
+    x = (rng.standard_normal((M, K)) * 300).astype(np.float16)
+    wq = np.full((N, K // 8), 0x77777777, np.uint32)
+    sc = synth.group_scales(rng, N, K)
+    assert np.all(host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K)) == 0)
+    assert np.all(host_f16(zq4.gate_up_silu(dev(wq), dev(sc), dev(x), N, K)) == 0)
+
+
+def test_prefill_constant_codes_closed_form(zq4, oracle):
+    M, N, K = 70, 260, 1024
+    rng = synth.rng_for("pf_const", N, K)
+    x = synth.activations(rng, M, K)
+    sx = x.astype(np.float64).sum(axis=1)
+    for c in (0, 15):
+        wq = np.full((N, K // 8), c * 0x11111111, np.uint32)
+        sc = np.full((N, K // 32), 0.0137, np.float16)
+        y = host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K)).astype(np.float64)
+        want = (c - 7) * float(sc[0, 0]) * sx
+        S = np.abs(x.astype(np.float64)).sum(axis=1) * abs(c - 7) * float(sc[0, 0])
+        assert_within(y, np.repeat(want[:, None], N, 1), np.repeat(S[:, None], N, 1), f"c={c}")
+
+
+def test_prefill_guard_band_and_unaligned_output(zq4, oracle):
+    """Output rows of odd length at an odd element offset (no 16-byte stores
+    possible) and nothing written past the output."""
+    M, N, K = 130, 261, 512
+    wq, sc, x = _case("pf_guard", M, N, K)
+    buf = torch.full((M * N + 4097,), float("nan"), dtype=torch.float16, device="cuda")
+    y = buf[1: 1 + M * N].view(M, N)
+    zq4.gemv(dev(wq), dev(sc), dev(x), N, K, y=y)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[0]) and torch.isnan(buf[1 + M * N:]).all(), "kernel wrote outside its output"
+    _check(oracle, host_f16(y), wq, sc, x, N, K, "unaligned y")
+
+
+def test_prefill_in_cuda_graph(zq4, oracle):
+    M, N, K = 192, 512, 3072
+    wq, sc, x = _case("pf_graph", M, N, K)
+    W, Sd, X = dev(wq), dev(sc), dev(x)
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        zq4.gemv(W, Sd, X, N, K, y=y)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            zq4.gemv(W, Sd, X, N, K, y=y)
+    y.zero_()
+    g.replay()
+    _check(oracle, host_f16(y), wq, sc, x, N, K, "graph replay")
+
+
+# The two prefill-chunk workloads at full size (1024 tokens): the Phi-3
+# gate_up shape and the down shape, run exactly as the benchmark runs them.
+FULL = [(1024, 16384, 3072), (1024, 3072, 8192)]
+
+
+@pytest.mark.parametrize("M,N,K", FULL)
+def test_prefill_full_size_sampled(zq4, oracle, M, N, K):
+    wq, sc, x = _case("prefill_full", M, N, K)
+    y = host_f16(zq4.gemv(dev(wq), dev(sc), dev(x), N, K))
+    assert np.all(np.isfinite(y))
+    rng = np.random.default_rng(N + K)
+    # two weight rows from every 256-row tile, plus the last row; all 1024 tokens
+    rows = np.unique(np.concatenate([t * 256 + rng.integers(0, min(256, N - t * 256), 2)
+                                     for t in range((N + 255) // 256)] + [[N - 1]]))
+    _check(oracle, y[:, rows], wq, sc, x, N, K, f"full M={M} N={N} K={K}", rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", FULL)
+def test_prefill_full_size_all_outputs(zq4, M, N, K):
+    """Every output against the f16-dequantized weights (our bit-exact
+    dequant kernel, pinned by the dequant tests) times x in fp32."""
+    wq, sc, x = _case("prefill_full", M, N, K)
+    W, Sd, X = dev(wq), dev(sc), dev(x)
+    y = zq4.gemv(W, Sd, X, N, K).float()
+    w16 = zq4.dequant_f16(W, Sd, N, K).float()
+    xf = X.float()
+    ref = xf @ w16.T
+    S = xf.abs() @ w16.abs().T
+    err = (y - ref).abs()
+    tol = ref.abs() * 2.0 ** -10 + S * 2.0 ** -14
+    assert bool(torch.isfinite(y).all())
+    assert bool((err <= tol).all()), float((err / tol.clamp_min(1e-30)).max())
+
+
+def test_prefill_no_device_errors_recorded(zq4):
+    assert zq4.device_errors(clear=True) == 0
