@@ -9,25 +9,30 @@
 // benchmarks", the matrix-unit GEMM sections: weights dequantized into shared
 // memory and fed to the matrix units with f32 accumulation).
 //
-// How, per CTA (one output tile of 128 tokens x 256 weight rows; K in steps
-// of 64 through a 3-stage shared-memory ring):
-//  * warp 0 (one lane): TMA producer. The x tile [128 x 64] f16 arrives with
-//    the 128-byte swizzle, which is exactly the K-major SW128 operand layout
-//    the tensor core reads; the packed weight tile [256 rows x 8 words] lands
-//    dense next to it.
-//  * warps 2..5 (128 threads): dequantize. Each thread takes two weight rows:
-//    exact f16 (q - 7) from the packed words, one f16x2 multiply by the group
-//    scale (the single rounding of the pages' f16 dequantization formula,
-//    bit-identical to zq4_dequant_f16), reorder into natural k order and store
-//    16-byte chunks into the SW128-swizzled B tile; then fence the generic
-//    writes to the async proxy and arrive on the stage's barrier.
-//  * warp 1: allocates 256 TMEM columns (the 128 x 256 fp32 accumulator); one
-//    lane issues four tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16)
-//    per stage and commits them to the stage's "empty" barrier, which frees
-//    the stage for the producer when the tensor core is done with it.
-//  * epilogue: warps 2..5 read their 32-lane quarter of the accumulator with
-//    tcgen05.ld, convert to f16 (or silu(g)*u for interleaved gate/up rows)
-//    and store.
+// How, per CTA (one output tile of 128*MB tokens x 256 weight rows, MB = 1
+// or 2; K in steps of 64):
+//  * warp 0 (one lane): TMA producer into a deep ring of raw stages. Each
+//    stage holds the x tile [128*MB x 64] f16, landed with the 128-byte
+//    swizzle that is exactly the K-major SW128 operand layout the tensor core
+//    reads, and the packed weight tile [256 rows x 8 words].
+//  * warps 2..9 (256 threads, one weight row each): dequantize. Exact f16
+//    (q - 7) from the packed words, one f16x2 multiply by the group scale
+//    (the single rounding of the pages' f16 dequantization, bit-identical to
+//    zq4_dequant_f16), reorder into natural k order and store 16-byte chunks
+//    into a 2-slot ring of SW128-swizzled B tiles; then fence the generic
+//    writes to the async proxy and arrive on the slot's barrier. Scales come
+//    as one 16-byte load per row every four stages, a group ahead.
+//  * warp 1: allocates 256*MB TMEM columns (MB fp32 accumulators of
+//    128 x 256); one lane issues, per K = 16 step, MB tcgen05.mma.cta_group::1
+//    .kind::f16 (M = 128, N = 256) that share the B tile, and commits each
+//    stage to the raw slot's and the B slot's "empty" barriers.
+//  * epilogue: warps 2..9 read their 32-lane quarter and column half of each
+//    accumulator with tcgen05.ld, convert to f16 (or silu(g)*u for
+//    interleaved gate/up rows) and store.
+// The raw ring is deep (4 to 6 stages) because a refill can only be issued
+// once the tensor core has finished with a slot, and the copy latency under
+// load is several stages' worth of MMA time; the B ring needs only two slots
+// (dequantize stage k+1 while the tensor core consumes stage k).
 // Every mbarrier wait is bounded; on expiry the kernel records
 // ZQ4_DEVERR_WAIT_TIMEOUT, lets its issued copies and MMAs complete, frees
 // its tensor memory and returns.
@@ -50,21 +55,32 @@ __device__ unsigned g_prefill_error = 0;
 
 namespace pf {
 
-constexpr int kBM = 128;                          // tokens per tile (MMA M)
+constexpr int kBM = 128;                          // tokens per MMA (M)
 constexpr int kBN = 256;                          // weight rows per tile (MMA N)
 constexpr int kBK = 64;                           // K per stage (one 128-byte swizzle row of f16)
-constexpr int kStages = 3;
-constexpr int kABytes = kBM * kBK * 2;            // 16 KB
+constexpr int kABytes = kBM * kBK * 2;            // 16 KB per 128-token block
 constexpr int kBBytes = kBN * kBK * 2;            // 32 KB
 constexpr int kWBytes = kBN * kBK / 2;            // 8 KB packed
-constexpr int kStageBytes = kABytes + kBBytes + kWBytes;
-constexpr int kDqWarps = 8;                     // dequant / epilogue warps
+constexpr int kBSlots = 2;
+constexpr int kDqWarps = 8;                       // dequant / epilogue warps
 constexpr int kThreads = 64 + 32 * kDqWarps;
-constexpr int kTmemCols = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB swizzle alignment");
 static_assert(32 * kDqWarps == kBN, "one dequant thread per weight row of the tile");
+
+template <int MB> struct Cfg {
+    static constexpr int kRawSlots = MB == 1 ? 6 : 4;
+    static constexpr int kRawBytes = MB * kABytes + kWBytes;
+    static constexpr int kRawOff = 0;
+    static constexpr int kBOff = kRawSlots * kRawBytes;
+    static constexpr int kBarOff = kBOff + kBSlots * kBBytes;
+    // mbarriers: full/empty per raw slot, full/empty per B slot, accumulator
+    static constexpr int kNumBars = 2 * kRawSlots + 2 * kBSlots + 1;
+    static constexpr int kSmem = 1024 + kBarOff + 8 * kNumBars + 16;
+    static constexpr int kTmemCols = 256 * MB;
+    static_assert(kRawBytes % 1024 == 0 && kBBytes % 1024 == 0, "1 KB swizzle alignment");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 __device__ __forceinline__ unsigned long long globaltimer()
 {
@@ -187,31 +203,123 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return uint32_t(float_to_f16_bits(lo)) | (uint32_t(float_to_f16_bits(hi)) << 16);
 }
 
-// Shared layout: [ring: kStages x (A | B | Wp)] [mbarriers] [tmem address]
-constexpr int kBarOff = kStages * kStageBytes;
+// Convert 32 consecutive accumulator columns (weight rows n .. n+31) of
+// token row m and store them: f16(acc), or f16(silu(g) * u) for interleaved
+// gate/up rows (16 outputs).
+__device__ __forceinline__ void store_outputs(const PrefillArgs &a, const float (&v)[32], int m, int n)
+{
+    const bool full = n + 32 <= a.N && a.vec_ok;
+    if (!a.gate_up) {
+        uint16_t *yo = a.y + size_t(m) * a.y_stride + n;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 o;
+                o.x = pack_f16x2(v[i], v[i + 1]);
+                o.y = pack_f16x2(v[i + 2], v[i + 3]);
+                o.z = pack_f16x2(v[i + 4], v[i + 5]);
+                o.w = pack_f16x2(v[i + 6], v[i + 7]);
+                *reinterpret_cast<uint4 *>(yo + i) = o;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n + i < a.N) yo[i] = float_to_f16_bits(v[i]);
+        }
+    } else {
+        float hv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hv[i] = silu_f32(v[2 * i]) * v[2 * i + 1];
+        uint16_t *yo = a.y + size_t(m) * a.y_stride + (n >> 1);
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 8) {
+                uint4 o;
+                o.x = pack_f16x2(hv[i], hv[i + 1]);
+                o.y = pack_f16x2(hv[i + 2], hv[i + 3]);
+                o.z = pack_f16x2(hv[i + 4], hv[i + 5]);
+                o.w = pack_f16x2(hv[i + 6], hv[i + 7]);
+                *reinterpret_cast<uint4 *>(yo + i) = o;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (n + 2 * i + 1 < a.N) yo[i] = float_to_f16_bits(hv[i]);
+        }
+    }
+}
 
+// Scales of groups g0 .. g0+7 of one row (zero past G or for a row past N),
+// as 8 f16 in a uint4; one 16-byte load when the row allows it.
+__device__ __forceinline__ uint4 load_scales8(const uint16_t *srow, int g0, int G, bool row_ok, bool vec)
+{
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (!row_ok || g0 >= G) return r;
+    if (vec) return *reinterpret_cast<const uint4 *>(srow + g0);   // G % 8 == 0: aligned, in range
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = g0 + i < G ? ldg_u16(srow + g0 + i) : 0u;
+    r.x = v[0] | (v[1] << 16);
+    r.y = v[2] | (v[3] << 16);
+    r.z = v[4] | (v[5] << 16);
+    r.w = v[6] | (v[7] << 16);
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pick_u32(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Dequantize four packed words (32 codes, one scale group) of a weight row
+// into four 16-byte chunks of the SW128-swizzled B tile row.
+__device__ __forceinline__ void dequant4(const uint4 &w4, uint32_t s2, uint8_t *brow, int chunk0, int sw)
+{
+    const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t p[4];
+        unpack_word_f16x2(words[w], p);          // (q-7) pairs (0,4),(1,5),(2,6),(3,7)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = hmul2(p[j], s2);
+        uint4 o;                                  // natural order e0..e7
+        o.x = __byte_perm(p[0], p[1], 0x5410);
+        o.y = __byte_perm(p[2], p[3], 0x5410);
+        o.z = __byte_perm(p[0], p[1], 0x7632);
+        o.w = __byte_perm(p[2], p[3], 0x7632);
+        *reinterpret_cast<uint4 *>(brow + (((chunk0 + w) ^ sw) << 4)) = o;
+    }
+}
+
+template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_w,
                                                          PrefillArgs a)
 {
+    using C = Cfg<MB>;
+    constexpr int kRaw = C::kRawSlots;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t full_tma0 = sbase + kBarOff;           // producer -> dequant
-    const uint32_t full_b0 = full_tma0 + 8 * kStages;     // dequant -> MMA
-    const uint32_t empty0 = full_b0 + 8 * kStages;        // MMA -> producer
-    const uint32_t accum_bar = empty0 + 8 * kStages;      // MMA -> epilogue
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kBarOff + 8 * (3 * kStages + 1));
+    const uint32_t raw_full0 = sbase + C::kBarOff;        // producer -> dequant (tx bytes)
+    const uint32_t raw_empty0 = raw_full0 + 8 * kRaw;     // MMA done -> producer
+    const uint32_t b_full0 = raw_empty0 + 8 * kRaw;       // dequant -> MMA
+    const uint32_t b_empty0 = b_full0 + 8 * kBSlots;      // MMA done -> dequant
+    const uint32_t accum_bar = b_empty0 + 8 * kBSlots;    // all MMAs done -> epilogue
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOff + 8 * C::kNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % a.m_tiles, n_tile = blockIdx.x / a.m_tiles;
-    const int m0 = m_tile * kBM, n0 = n_tile * kBN;
+    const int m0 = m_tile * kBM * MB, n0 = n_tile * kBN;
     const int ksteps = (a.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_tma0 + 8 * s, 1);
-            mbar_init(full_b0 + 8 * s, kDqWarps);
-            mbar_init(empty0 + 8 * s, 1);
+        for (int s = 0; s < kRaw; ++s) {
+            mbar_init(raw_full0 + 8 * s, 1);
+            mbar_init(raw_empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < kBSlots; ++s) {
+            mbar_init(b_full0 + 8 * s, kDqWarps);
+            mbar_init(b_empty0 + 8 * s, 1);
         }
         mbar_init(accum_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -219,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
-                     "r"(kTmemCols)
+                     "r"(C::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -234,22 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
         int issued = 0;
         if (lane == 0) {
             for (int ks = 0; ks < ksteps; ++ks, ++issued) {
-                const int s = ks % kStages;
-                if (!mbar_wait(empty0 + 8 * s, ((ks / kStages) & 1) ^ 1)) {
+                const int s = ks % kRaw;
+                if (!mbar_wait(raw_empty0 + 8 * s, ((ks / kRaw) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                const uint32_t st = sbase + s * kStageBytes;
-                mbar_arrive_expect_tx(full_tma0 + 8 * s, kABytes + kWBytes);
-                tma_load_2d(st + kABytes + kBBytes, &tm_w, ks * (kBK / 8), n0, full_tma0 + 8 * s);
+                const uint32_t st = sbase + C::kRawOff + s * C::kRawBytes;
+                mbar_arrive_expect_tx(raw_full0 + 8 * s, MB * kABytes + kWBytes);
+                tma_load_2d(st + MB * kABytes, &tm_w, ks * (kBK / 8), n0, raw_full0 + 8 * s);
                 // the weights are constant; x may be the previous kernel's output
-                if (ks < kStages) griddep_wait();
-                tma_load_2d(st, &tm_x, ks * kBK, m0, full_tma0 + 8 * s);
+                if (ks < kRaw) griddep_wait();
+                tma_load_2d(st, &tm_x, ks * kBK, m0, raw_full0 + 8 * s);
             }
             if (!ok) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
             // drain: every issued fill lands before this CTA tears down
-            for (int j = std::max(0, issued - kStages); j < issued; ++j)
-                if (!mbar_wait(full_tma0 + 8 * (j % kStages), (j / kStages) & 1)) {
+            for (int j = std::max(0, issued - kRaw); j < issued; ++j)
+                if (!mbar_wait(raw_full0 + 8 * (j % kRaw), (j / kRaw) & 1)) {
                     atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -259,21 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             for (int ks = 0; ks < ksteps; ++ks) {
-                const int s = ks % kStages;
-                if (!mbar_wait(full_b0 + 8 * s, (ks / kStages) & 1)) {
+                const int s = ks % kRaw, b = ks % kBSlots;
+                // the B slot is filled only after its raw stage landed, so this
+                // one wait covers both operands
+                if (!mbar_wait(b_full0 + 8 * b, (ks / kBSlots) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t st = sbase + s * kStageBytes;
+                const uint32_t at = sbase + C::kRawOff + s * C::kRawBytes;
+                const uint32_t bt = sbase + C::kBOff + b * kBBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    // K = 16 is 32 bytes along the 128-byte swizzled row
-                    const uint64_t ad = smem_desc_sw128(st + kk * 32);
-                    const uint64_t bd = smem_desc_sw128(st + kABytes + kk * 32);
-                    umma_f16(tmem, ad, bd, (ks | kk) != 0);
+                    // K = 16 is 32 bytes along the 128-byte swizzled rows
+                    const uint64_t bd = smem_desc_sw128(bt + kk * 32);
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb)
+                        umma_f16(tmem + uint32_t(mb * kBN), smem_desc_sw128(at + mb * kABytes + kk * 32), bd,
+                                 (ks | kk) != 0);
                 }
-                umma_commit(empty0 + 8 * s);         // stage free once these MMAs are done
+                umma_commit(raw_empty0 + 8 * s);     // raw slot free once these MMAs are done
+                umma_commit(b_empty0 + 8 * b);       // and the B slot
             }
             if (!ok) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
             umma_commit(accum_bar);                  // all issued MMAs done -> epilogue
@@ -284,105 +398,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
         const int nl = threadIdx.x - 64;             // weight row of the tile owned by this thread
         const int n = n0 + nl;
         const int G = a.K >> 5;
-        const uint16_t *srow = a.scales + size_t(n < a.N ? n : 0) * G;
+        const bool row_ok = n < a.N;
+        const bool vec = (G & 7) == 0;
+        const uint16_t *srow = a.scales + size_t(row_ok ? n : 0) * G;
+        // conflict-free reads of the packed row (32 bytes): threads whose bit 2
+        // is set read the second half first
+        const int h0 = (nl >> 2) & 1;
+        const int sw = nl & 7;
         griddep_wait();
         griddep_launch_dependents();
-        uint32_t scn[2] = {0, 0};                    // scales of the next stage's two groups
-        if (n < a.N) {
-            scn[0] = ldg_u16(srow);
-            if (G > 1) scn[1] = ldg_u16(srow + 1);
-        }
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const int s = ks % kStages;
-            uint32_t sc2[2] = {scn[0] | (scn[0] << 16), scn[1] | (scn[1] << 16)};
-            if (n < a.N) {                           // prefetch the following stage's scales
-                const int g0 = 2 * ks + 2;
-                scn[0] = g0 < G ? ldg_u16(srow + g0) : 0;
-                scn[1] = g0 + 1 < G ? ldg_u16(srow + g0 + 1) : 0;
-            }
-            if (!mbar_wait(full_tma0 + 8 * s, (ks / kStages) & 1)) {
-                ok = false;
-                break;
-            }
-            const uint8_t *wp = smem + s * kStageBytes + kABytes + kBBytes;
-            uint8_t *bt = smem + s * kStageBytes + kABytes;
-            const uint4 w03 = *reinterpret_cast<const uint4 *>(wp + nl * 32);
-            const uint4 w47 = *reinterpret_cast<const uint4 *>(wp + nl * 32 + 16);
-            const uint32_t words[8] = {w03.x, w03.y, w03.z, w03.w, w47.x, w47.y, w47.z, w47.w};
+        uint4 sc_next = load_scales8(srow, 0, G, row_ok, vec);
+        for (int kq = 0; kq < ksteps && ok; kq += 4) {
+            const uint4 sc_cur = sc_next;           // groups 2kq .. 2kq+7
+            sc_next = load_scales8(srow, 2 * kq + 8, G, row_ok, vec);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                uint32_t p[4];
-                unpack_word_f16x2(words[w], p);          // (q-7) pairs (0,4),(1,5),(2,6),(3,7)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) p[j] = hmul2(p[j], sc2[w >> 2]);
-                uint4 o;                                  // natural order e0..e7
-                o.x = __byte_perm(p[0], p[1], 0x5410);
-                o.y = __byte_perm(p[2], p[3], 0x5410);
-                o.z = __byte_perm(p[0], p[1], 0x7632);
-                o.w = __byte_perm(p[2], p[3], 0x7632);
-                *reinterpret_cast<uint4 *>(bt + nl * 128 + ((w ^ (nl & 7)) << 4)) = o;
+            for (int u = 0; u < 4; ++u) {
+                const int ks = kq + u;
+                if (ks >= ksteps) break;
+                const int s = ks % kRaw, b = ks % kBSlots;
+                const uint32_t sp = pick_u32(sc_cur, u);           // (group 2ks, group 2ks+1)
+                const uint32_t sg0 = __byte_perm(sp, 0, 0x1010), sg1 = __byte_perm(sp, 0, 0x3232);
+                const bool got = mbar_wait(raw_full0 + 8 * s, (ks / kRaw) & 1) &&
+                                 mbar_wait(b_empty0 + 8 * b, ((ks / kBSlots) & 1) ^ 1);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *wp = smem + C::kRawOff + s * C::kRawBytes + MB * kABytes + nl * 32;
+                uint8_t *brow = smem + C::kBOff + b * kBBytes + nl * 128;
+                const uint4 wa = *reinterpret_cast<const uint4 *>(wp + h0 * 16);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(wp + (h0 ^ 1) * 16);
+                dequant4(wa, h0 ? sg1 : sg0, brow, 4 * h0, sw);
+                dequant4(wb, h0 ? sg0 : sg1, brow, 4 * (h0 ^ 1), sw);
+                // make the generic-proxy stores visible to the tensor core, then hand over
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_full0 + 8 * b);
             }
-            // make the generic-proxy stores visible to the tensor core, then hand over
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_b0 + 8 * s);
         }
         if (!ok && lane == 0) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
 
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its 32 tokens) and
-        // the column half (w-2)/4 of the tile
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its 32 tokens of
+        // each 128-token block) and the column half (w-2)/4 of the tile
         // (tcgen05.ld is warp-collective: the decision to read must be warp-uniform)
-        const bool got = mbar_wait(accum_bar, 0);
-        const bool acc_ready = __all_sync(0xffffffffu, got && ok);
+        const bool acc_got = mbar_wait(accum_bar, 0);
+        const bool acc_ready = __all_sync(0xffffffffu, acc_got && ok);
         if (!acc_ready && lane == 0) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
         tc_fence_after();
         const int q = warp & 3;
         const int cbase = ((warp - 2) >> 2) * (kBN / 2);
-        const int m = m0 + 32 * q + lane;
         if (acc_ready) {
 #pragma unroll 1
-            for (int c0 = cbase; c0 < cbase + kBN / 2; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(c0), v);
-                if (m >= a.M || n0 + c0 >= a.N) continue;
-                const bool full = n0 + c0 + 32 <= a.N && a.vec_ok;
-                if (!a.gate_up) {
-                    uint16_t *yo = a.y + size_t(m) * a.y_stride + n0 + c0;
-                    if (full) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            uint4 o;
-                            o.x = pack_f16x2(v[i], v[i + 1]);
-                            o.y = pack_f16x2(v[i + 2], v[i + 3]);
-                            o.z = pack_f16x2(v[i + 4], v[i + 5]);
-                            o.w = pack_f16x2(v[i + 6], v[i + 7]);
-                            *reinterpret_cast<uint4 *>(yo + i) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + c0 + i < a.N) yo[i] = float_to_f16_bits(v[i]);
-                    }
-                } else {
-                    float hv[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) hv[i] = silu_f32(v[2 * i]) * v[2 * i + 1];
-                    uint16_t *yo = a.y + size_t(m) * a.y_stride + ((n0 + c0) >> 1);
-                    if (full) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 8) {
-                            uint4 o;
-                            o.x = pack_f16x2(hv[i], hv[i + 1]);
-                            o.y = pack_f16x2(hv[i + 2], hv[i + 3]);
-                            o.z = pack_f16x2(hv[i + 4], hv[i + 5]);
-                            o.w = pack_f16x2(hv[i + 6], hv[i + 7]);
-                            *reinterpret_cast<uint4 *>(yo + i) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (n0 + c0 + 2 * i + 1 < a.N) yo[i] = float_to_f16_bits(hv[i]);
-                    }
+            for (int mb = 0; mb < MB; ++mb) {
+                const int m = m0 + mb * kBM + 32 * q + lane;
+#pragma unroll 1
+                for (int c0 = cbase; c0 < cbase + kBN / 2; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(mb * kBN + c0), v);
+                    if (m >= a.M || n0 + c0 >= a.N) continue;
+                    store_outputs(a, v, m, n0 + c0);
                 }
             }
         }
@@ -391,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
                      : "memory");
     }
 }
@@ -411,17 +485,44 @@ cudaError_t read_prefill_error(unsigned *flags, bool clear)
     return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(unsigned));
 }
 
+#ifndef ZQ4_PF_FORCE_MB
+#define ZQ4_PF_FORCE_MB 0          // 0: choose per shape; 1 or 2: always that many 128-token blocks
+#endif
+
+template <int MB>
+static cudaError_t launch_mb(const CUtensorMap &tmx, const CUtensorMap &tmw, const pf::PrefillArgs &a, int n_tiles,
+                             cudaStream_t s)
+{
+    static int smem_set[kMaxDevices] = {};
+    auto kern = pf::k_prefill<MB>;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), pf::Cfg<MB>::kSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(a.m_tiles * n_tiles), dim3(pf::kThreads), size_t(pf::Cfg<MB>::kSmem), s, tmx,
+                      tmw, a);
+}
+
 cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
                            int M, int N, int K, bool gate_up, cudaStream_t s)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
+    const int n_tiles = (N + pf::kBN - 1) / pf::kBN;
+    // 256-token tiles halve the dequantization per FLOP; take them when they
+    // still fill the SMs as well as 128-token tiles do
+    int MB = ZQ4_PF_FORCE_MB;
+    if (MB == 0) {
+        const long sms = sm_count();
+        const long t1 = long((M + 127) / 128) * n_tiles, t2 = long((M + 255) / 256) * n_tiles;
+        const long waves1 = (t1 + sms - 1) / sms, waves2 = (t2 + sms - 1) / sms;
+        // a 256-token tile costs about 4/3 of a 128-token one (measured)
+        MB = 4 * waves2 <= 3 * waves1 ? 2 : 1;
+    }
     CUtensorMap tmx, tmw;
     const cuuint32_t estr[2] = {1, 1};
     {
         const cuuint64_t dim[2] = {cuuint64_t(K), cuuint64_t(M)};
         const cuuint64_t stride[1] = {cuuint64_t(K) * 2};
-        const cuuint32_t box[2] = {pf::kBK, pf::kBM};
+        const cuuint32_t box[2] = {pf::kBK, cuuint32_t(pf::kBM * MB)};
         if (enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(x), dim, stride, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -442,16 +543,11 @@ cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uin
     a.M = M;
     a.N = N;
     a.K = K;
-    a.m_tiles = (M + pf::kBM - 1) / pf::kBM;
+    a.m_tiles = (M + pf::kBM * MB - 1) / (pf::kBM * MB);
     a.gate_up = gate_up ? 1 : 0;
     a.y_stride = gate_up ? N / 2 : N;
     a.vec_ok = (reinterpret_cast<uintptr_t>(y) & 15) == 0 && a.y_stride % 8 == 0;
-    const int n_tiles = (N + pf::kBN - 1) / pf::kBN;
-    const size_t smem = 1024 + pf::kBarOff + 8 * (3 * pf::kStages + 1) + 16;
-    static int smem_set[kMaxDevices] = {};
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(pf::k_prefill), smem, smem_set);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(pf::k_prefill, dim3(a.m_tiles * n_tiles), dim3(pf::kThreads), smem, s, tmx, tmw, a);
+    return MB == 2 ? launch_mb<2>(tmx, tmw, a, n_tiles, s) : launch_mb<1>(tmx, tmw, a, n_tiles, s);
 }
 
 }  // namespace zq4
