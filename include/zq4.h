@@ -35,6 +35,7 @@
 #ifndef ZQ4_H
 #define ZQ4_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -163,9 +164,11 @@ ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_
                         const int32_t *expert_ids, const float *route_w, int top_k, int mode,
                         int32_t *dev_status, void *stream);
 
-/* Flags of zq4_prepare_weight. */
+/* Flags of zq4_prepare_weight (ZQ4_PREP_SEGMENTED may be OR-ed with
+ * ZQ4_PREP_CONCAT_TO_INTERLEAVED). */
 #define ZQ4_PREP_COPY 0                  /* plain copy of the canonical layout */
 #define ZQ4_PREP_CONCAT_TO_INTERLEAVED 1 /* [gate; up] rows -> g0,u0,g1,u1,... */
+#define ZQ4_PREP_SEGMENTED 2             /* the segmented layout (below) */
 
 /*
  * zq4_prepare_weight -- rewrite a q4f16_1 matrix into the layout the kernels
@@ -178,12 +181,27 @@ ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_
  *
  *   wq_src/scales_src [N, K/8] / [N, K/32]  ->  wq_dst/scales_dst (same shapes)
  * N even for ZQ4_PREP_CONCAT_TO_INTERLEAVED. Source and destination must
- * not overlap. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_FLAGS,
- * ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
+ * not overlap.
+ *
+ * ZQ4_PREP_SEGMENTED (K % 256 == 0; scales_dst must be NULL) writes the
+ * segmented layout into wq_dst (zq4_segmented_bytes(N, K) bytes): for each
+ * 16-row tile t (tile-major) and 256-column block s, 2304 contiguous bytes:
+ * first the 16 rows' 128-byte code runs (words 32s .. 32s+31 of row 16t+i),
+ * the 16-byte chunk c of row i stored at byte i*128 + 16*(c XOR (i mod 8)),
+ * then the 16 rows' scales 8s .. 8s+7 (16 bytes per row, at 2048 + 16*i).
+ * Rows past N are zero. A pure byte permutation of the canonical matrix; the
+ * layout zq4_stack_run streams with one contiguous copy per segment.
+ *
+ * Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_FLAGS, ZQ4_ERR_ALIGN,
+ * ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
  */
 ZQ4_API zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src,
                               uint32_t *wq_dst, uint16_t *scales_dst, int N, int K, int flags,
                               void *stream);
+
+/* Bytes of an N x K matrix in the segmented layout (0 unless N > 0 and
+ * K % 256 == 0). */
+ZQ4_API size_t zq4_segmented_bytes(int N, int K);
 
 /*
  * zq4_dequant_f32 -- w[n,k] = (q - 7) * s as float32, exact (a 4-bit integer
@@ -206,6 +224,74 @@ ZQ4_API zq4_status zq4_dequant_f32(const uint32_t *wq, const uint16_t *scales, f
  */
 ZQ4_API zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N, int K,
                            void *stream);
+
+/*
+ * Decode step as one launch: an ordered list of projections ("jobs") run by
+ * a persistent kernel, each job starting only after every output of the job
+ * before it is written -- the dependency of a decode step, in which every
+ * projection consumes the previous one's result. Source: "Zero TVM
+ * Documentation", section "Decode loop" (the fixed per-token sequence of
+ * dispatches) with the projections of cards 5 "int4 Matmul" and 6 "Fused
+ * FFN"; each job computes exactly what zq4_gemv (gate_up = 0) or
+ * zq4_gate_up_silu (gate_up = 1) computes.
+ *
+ * Job: wq = the matrix in the segmented layout (zq4_prepare_weight with
+ * ZQ4_PREP_SEGMENTED; it carries the scales, so `scales` must be NULL), x
+ * [M, K] f16, y [M, N] f16 (or [M, N/2] for gate_up); device pointers,
+ * caller-owned; K % 256 == 0, N even for gate_up; wq and x 16-byte aligned.
+ * A job may read the y of an earlier job as its x.
+ */
+typedef struct zq4_stack_job {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;
+    uint16_t *y;
+    int N;
+    int K;
+    int gate_up;
+} zq4_stack_job;
+
+/* Filled by zq4_stack_plan_init; pass to zq4_stack_run. `dev` is the
+ * caller's device buffer (job table with tensor maps, counters, scratch). */
+typedef struct zq4_stack_plan {
+    void *dev;
+    size_t bytes;
+    int n_jobs;
+    int M;
+    int grid;
+    int max_k;
+    int max_tiles;
+} zq4_stack_plan;
+
+/*
+ * zq4_stack_plan_bytes -- device bytes a plan for these jobs needs on the
+ * current device (1 <= M <= 8). Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE,
+ * ZQ4_ERR_ALIGN, ZQ4_ERR_UNSUPPORTED (x of the largest K does not fit in
+ * shared memory).
+ */
+ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
+
+/*
+ * zq4_stack_plan_init -- write the plan into `dev` (256-byte aligned, at
+ * least zq4_stack_plan_bytes bytes, owned by the caller and kept alive while
+ * the plan is used) and fill *plan. Synchronises `stream` (it copies the job
+ * table); call it outside stream capture. The job list is copied: later
+ * changes to `jobs` do not affect the plan, but the buffers it points to
+ * must stay allocated.
+ */
+ZQ4_API zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
+                                       zq4_stack_plan *plan, void *stream);
+
+/*
+ * zq4_stack_run -- run every job of the plan, in order, as one cooperative
+ * launch on `stream` (capturable into a CUDA graph; replays reuse the plan).
+ * One plan must not run on two streams at once: its counters and scratch
+ * are per plan. If a device-side wait gives up (ZQ4_DEVERR_WAIT_TIMEOUT in
+ * zq4_device_errors) the plan is left inconsistent and must be initialised
+ * again. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE (plan made on a device with a
+ * different SM count), ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
 
 #ifdef __cplusplus
 }

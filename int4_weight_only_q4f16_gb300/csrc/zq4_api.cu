@@ -200,10 +200,11 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
 zq4_status zq4_device_errors(uint32_t *flags, int clear)
 {
     if (!flags) return ZQ4_ERR_NULL;
-    unsigned v = 0, vp = 0;
+    unsigned v = 0, vp = 0, vk = 0;
     zq4_status st = cuda_status(read_device_error(&v, clear != 0));
     if (st == ZQ4_OK) st = cuda_status(read_prefill_error(&vp, clear != 0));
-    *flags = v | vp;
+    if (st == ZQ4_OK) st = cuda_status(read_stack_error(&vk, clear != 0));
+    *flags = v | vp | vk;
     return st;
 }
 
@@ -211,9 +212,21 @@ zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src
                               uint32_t *wq_dst, uint16_t *scales_dst, int N, int K, int flags,
                               void *stream)
 {
-    if (flags != ZQ4_PREP_COPY && flags != ZQ4_PREP_CONCAT_TO_INTERLEAVED) return ZQ4_ERR_FLAGS;
+    if (flags & ~(ZQ4_PREP_CONCAT_TO_INTERLEAVED | ZQ4_PREP_SEGMENTED)) return ZQ4_ERR_FLAGS;
     zq4_status st = check_matrix(wq_src, scales_src, N, K);
     if (st != ZQ4_OK) return st;
+    const bool interleave = (flags & ZQ4_PREP_CONCAT_TO_INTERLEAVED) != 0;
+    if (flags & ZQ4_PREP_SEGMENTED) {
+        if (!wq_dst) return ZQ4_ERR_NULL;
+        if (scales_dst) return ZQ4_ERR_FLAGS;               // the scales travel inside wq_dst
+        if (K % 256 != 0 || (interleave && (N & 1))) return ZQ4_ERR_SHAPE;
+        if (!aligned16(wq_dst)) return ZQ4_ERR_ALIGN;
+        const size_t db = segmented_bytes(N, K);
+        if (overlap(wq_dst, db, wq_src, wq_bytes(N, K)) || overlap(wq_dst, db, scales_src, sc_bytes(N, K)))
+            return ZQ4_ERR_OVERLAP;
+        return cuda_status(launch_prepare_segmented(wq_src, scales_src, reinterpret_cast<uint8_t *>(wq_dst), N, K,
+                                                    interleave, static_cast<cudaStream_t>(stream)));
+    }
     if (!wq_dst || !scales_dst) return ZQ4_ERR_NULL;
     if (!aligned16(wq_dst) || !aligned16(scales_dst)) return ZQ4_ERR_ALIGN;
     if (flags == ZQ4_PREP_CONCAT_TO_INTERLEAVED && (N & 1)) return ZQ4_ERR_SHAPE;
@@ -222,9 +235,14 @@ zq4_status zq4_prepare_weight(const uint32_t *wq_src, const uint16_t *scales_src
         overlap(scales_dst, sb, wq_src, wb) || overlap(scales_dst, sb, scales_src, sb) ||
         overlap(wq_dst, wb, scales_dst, sb))
         return ZQ4_ERR_OVERLAP;
-    return cuda_status(launch_prepare(wq_src, scales_src, wq_dst, scales_dst, N, K,
-                                      flags == ZQ4_PREP_CONCAT_TO_INTERLEAVED,
+    return cuda_status(launch_prepare(wq_src, scales_src, wq_dst, scales_dst, N, K, interleave,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t zq4_segmented_bytes(int N, int K)
+{
+    if (N <= 0 || K <= 0 || K % 256 != 0) return 0;
+    return segmented_bytes(N, K);
 }
 
 zq4_status zq4_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
@@ -245,6 +263,22 @@ zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t 
     if (!w) return ZQ4_ERR_NULL;
     if (!aligned16(w)) return ZQ4_ERR_ALIGN;
     return cuda_status(launch_dequant_f16(wq, scales, w, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes)
+{
+    return stack_plan_bytes(jobs, n_jobs, M, bytes);
+}
+
+zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
+                               zq4_stack_plan *plan, void *stream)
+{
+    return stack_plan_init(jobs, n_jobs, M, dev, bytes, plan, static_cast<cudaStream_t>(stream));
+}
+
+zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream)
+{
+    return stack_run(plan, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -370,6 +370,40 @@ __global__ void k_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32
         sc_dst[size_t(dst_row) * G + i] = sc_src[size_t(src_row) * G + i];
 }
 
+// Segmented layout: segment (tile t, column block s) of 16 rows x 256
+// columns is 2304 contiguous bytes -- the 16 rows' 128-byte code runs, the
+// 16-byte chunk c of row i stored at i*128 + ((c ^ (i & 7)) * 16) (the
+// 128-byte swizzle, so a plain copy of the segment into shared memory is
+// bank-conflict-free for the decode kernels' fragment loads), then the 16
+// rows' 8 scales (16 bytes each). Segments are stored tile-major. Rows past N
+// are zero. Source row = dst row, or the gate/up interleave of the
+// concatenated [gate; up] matrix. One CTA (144 threads) per segment.
+__global__ void k_prepare_segmented(const uint32_t *wq_src, const uint16_t *sc_src, uint8_t *dst, int N, int K,
+                                    int interleave)
+{
+    const int KW = K >> 3, G = K >> 5, S = K >> 8, half = N >> 1;
+    const int tile = blockIdx.x / S, seg = blockIdx.x - tile * S;
+    uint8_t *base = dst + size_t(blockIdx.x) * 2304;
+    const int i = threadIdx.x;
+    if (i < 128) {
+        const int row = i >> 3, c = i & 7, n = tile * 16 + row;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < N) {
+            const int src = interleave ? ((n & 1) ? half + (n >> 1) : (n >> 1)) : n;
+            v = *reinterpret_cast<const uint4 *>(wq_src + size_t(src) * KW + seg * 32 + c * 4);
+        }
+        *reinterpret_cast<uint4 *>(base + row * 128 + ((c ^ (row & 7)) << 4)) = v;
+    } else if (i < 144) {
+        const int row = i - 128, n = tile * 16 + row;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < N) {
+            const int src = interleave ? ((n & 1) ? half + (n >> 1) : (n >> 1)) : n;
+            v = *reinterpret_cast<const uint4 *>(sc_src + size_t(src) * G + seg * 8);
+        }
+        *reinterpret_cast<uint4 *>(base + 2048 + row * 16) = v;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
@@ -527,6 +561,15 @@ cudaError_t launch_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint3
                            uint16_t *sc_dst, int N, int K, int interleave, cudaStream_t s)
 {
     k_prepare<<<N, 128, 0, s>>>(wq_src, sc_src, wq_dst, sc_dst, N, K, interleave);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_segmented(const uint32_t *wq_src, const uint16_t *sc_src, uint8_t *dst, int N, int K,
+                                     int interleave, cudaStream_t s)
+{
+    const long long segs = (long long)((N + 15) / 16) * (K / 256);
+    if (segs > 0x7fffffff) return cudaErrorInvalidValue;
+    k_prepare_segmented<<<unsigned(segs), 144, 0, s>>>(wq_src, sc_src, dst, N, K, interleave);
     return cudaGetLastError();
 }
 

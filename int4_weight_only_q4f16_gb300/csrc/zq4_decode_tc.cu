@@ -48,6 +48,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
 
@@ -95,89 +96,15 @@ constexpr int kStageBytes = kSegs * kSegBytes + kScaleBytes;   // 9 KB, a multip
 constexpr int kStages = ZQ4_TC_STAGES;
 constexpr int kUnrollG = ZQ4_TC_UNROLL;           // groups unrolled per loop trip
 constexpr int kGpw = (kKC / 32 + kWarps - 1) / kWarps;   // groups of a stage per warp
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint32_t kSevenEighths = 0x3B003B00u;   // f16x2 (7/8, 7/8)
 constexpr int kUnpack = ZQ4_TC_UNPACK;
 constexpr int kPrefetch = ZQ4_TC_PREFETCH;
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1 KB swizzle alignment");
 
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t addr, unsigned count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t addr)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
-                 : "memory");
-}
-
-// Wait for the phase of the given parity to complete; false once the wait
-// has lasted longer than the time limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
-{
-    const unsigned long long t0 = globaltimer();
-    for (unsigned i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-// Bring the box at (x, y) of a tensor map into L2 (no shared memory).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// 2D tensor-map TMA load of one box at (x, y) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t mbar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
-        : "memory");
-}
-
 __device__ __forceinline__ void named_barrier_compute()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-}
-
-// D = A * B + C, m16n8k16, f16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                         const float (&c)[4])
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-          "f"(c[2]), "f"(c[3]));
 }
 
 // ---------------------------------------------------------------------------
@@ -185,7 +112,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // ---------------------------------------------------------------------------
 __host__ __device__ inline size_t xs_row_bytes(int K) { return size_t(K) * 2 + 64; }
 constexpr size_t kRingBytes = size_t(kStages) * kStageBytes;
-constexpr size_t kMbarBytes = 128;
+constexpr size_t kMbarBytes = (16 * kStages + 127) / 128 * 128;   // full + empty per stage
 template <int NB>
 __host__ __device__ inline size_t red_bytes() { return size_t(kWarps) * NB * 16 * 8 * 4; }
 __host__ __device__ inline size_t scale_bytes() { return size_t(kWarps) * kGpw * 8 * 8; }

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/zq4.h"
+
 namespace zq4 {
 
 constexpr int kMaxDevices = 64;
@@ -52,6 +54,13 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
                              uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t read_device_error(unsigned *flags, bool clear);
 
+// zq4_stack.cu: the persistent decode-step kernel
+zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
+zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
+                           zq4_stack_plan *plan, cudaStream_t s);
+zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s);
+cudaError_t read_stack_error(unsigned *flags, bool clear);
+
 // zq4_prefill_tc.cu: the tensor-core GEMM for chunks of kPrefillMinRows or
 // more activation rows
 constexpr int kPrefillMinRows = 64;
@@ -72,5 +81,9 @@ cudaError_t launch_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint1
                                int K, cudaStream_t s);
 cudaError_t launch_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32_t *wq_dst,
                            uint16_t *sc_dst, int N, int K, int interleave, cudaStream_t s);
+cudaError_t launch_prepare_segmented(const uint32_t *wq_src, const uint16_t *sc_src, uint8_t *dst, int N, int K,
+                                     int interleave, cudaStream_t s);
+// bytes of one matrix in the segmented layout (16-row tiles x 256-column segments of 2304 B)
+inline size_t segmented_bytes(int N, int K) { return size_t((N + 15) / 16) * size_t(K / 256) * 2304; }
 
 }  // namespace zq4

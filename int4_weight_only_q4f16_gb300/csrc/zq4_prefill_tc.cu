@@ -42,6 +42,7 @@
 
 #include <algorithm>
 
+#include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
 
@@ -64,7 +65,6 @@ constexpr int kWBytes = kBN * kBK / 2;            // 8 KB packed
 constexpr int kBSlots = 2;
 constexpr int kDqWarps = 8;                       // dequant / epilogue warps
 constexpr int kThreads = 64 + 32 * kDqWarps;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 static_assert(32 * kDqWarps == kBN, "one dequant thread per weight row of the tile");
 
@@ -81,56 +81,6 @@ template <int MB> struct Cfg {
     static_assert(kRawBytes % 1024 == 0 && kBBytes % 1024 == 0, "1 KB swizzle alignment");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
-
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t addr, unsigned count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t addr)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
-{
-    const unsigned long long t0 = globaltimer();
-    for (unsigned i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t mbar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
-        : "memory");
-}
 
 // Shared-memory matrix descriptor of a K-major operand tile with the
 // 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (stride byte

@@ -49,8 +49,13 @@ class DecodeStack:
     epilogue and the one named "down" reads its output."""
 
     def __init__(self, layer_shapes, n_layers, head=None, M=1, device="cuda",
-                 keep_host=False, seed=synth.MASTER_SEED):
+                 keep_host=False, seed=synth.MASTER_SEED, mode="calls"):
+        """mode "plan": the whole step is one persistent launch
+        (zq4_stack_run); "calls": one zq4_gemv / zq4_gate_up_silu per
+        projection."""
         self.M, self.device, self.n_layers = M, torch.device(device), n_layers
+        self.mode = mode
+        self.plan = None
         self.layers = []
         for l in range(n_layers):
             self.layers.append({name: Projection(name, N, K, l, self.device, keep_host, seed)
@@ -91,6 +96,8 @@ class DecodeStack:
         return self.weight_bytes() + self.activation_bytes()
 
     def launches_per_step(self) -> int:
+        if self.mode == "plan":
+            return 1
         per_layer = 0
         for name in self.order:
             p = self.layers[0][name]
@@ -102,7 +109,35 @@ class DecodeStack:
     def input_for(self, l, name):
         return self.y[(l, "gate_up")] if name == "down" else self.x[(l, name)]
 
+    def jobs(self):
+        """(wq, scales, x, y, N, K, gate_up) of every projection in step order."""
+        out = []
+        for l, layer in enumerate(self.layers):
+            for name in self.order:
+                p = layer[name]
+                out.append((p.wq, p.sc, self.input_for(l, name), self.y[(l, name)], p.N, p.K,
+                            name == "gate_up"))
+        if self.head:
+            out.append((self.head.wq, self.head.sc, self.x[("head",)], self.y[("head",)],
+                        self.head.N, self.head.K, False))
+        return out
+
+    def build_plan(self, stream=None):
+        """Segmented copies of every matrix (kept on the projections) and the
+        one-launch plan over them."""
+        pjobs = []
+        for wq, sc, x, y, N, K, gate_up in self.jobs():
+            seg, _ = zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED, stream=stream)
+            pjobs.append((seg, x, y, N, K, gate_up))
+        self.plan = zq4.StackPlan(pjobs, self.M, stream=stream)
+        return self.plan
+
     def launch_step(self, stream=None):
+        if self.mode == "plan":
+            if self.plan is None:
+                self.build_plan(stream)
+            self.plan.run(stream)
+            return
         for l, layer in enumerate(self.layers):
             for name in self.order:
                 p = layer[name]

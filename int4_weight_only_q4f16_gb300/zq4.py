@@ -33,10 +33,11 @@ MOE_DOWN_COMBINE = 2
 DEV_BAD_EXPERT_ID = 1
 PREP_COPY = 0
 PREP_CONCAT_TO_INTERLEAVED = 1
+PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16")
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes")
 
 
 class Zq4Error(RuntimeError):
@@ -69,12 +70,30 @@ def _load():
         "zq4_prepare_weight": [P, P, P, P, I, I, I, P],
         "zq4_dequant_f32": [P, P, P, I, I, P],
         "zq4_dequant_f16": [P, P, P, I, I, P],
+        "zq4_stack_plan_bytes": [P, I, I, P],
+        "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
+        "zq4_stack_run": [P, P],
     }
+    lib.zq4_segmented_bytes.argtypes = [I, I]
+    lib.zq4_segmented_bytes.restype = ctypes.c_size_t
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = I
     return lib
+
+
+class StackJob(ctypes.Structure):
+    """zq4_stack_job."""
+    _fields_ = [("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int), ("gate_up", ctypes.c_int)]
+
+
+class StackPlanC(ctypes.Structure):
+    """zq4_stack_plan."""
+    _fields_ = [("dev", ctypes.c_void_p), ("bytes", ctypes.c_size_t), ("n_jobs", ctypes.c_int),
+                ("M", ctypes.c_int), ("grid", ctypes.c_int), ("max_k", ctypes.c_int),
+                ("max_tiles", ctypes.c_int)]
 
 
 lib = _load()
@@ -156,8 +175,24 @@ def moe_gemv(wq_bank, scales_bank, num_experts, x, N, K, expert_ids, mode, route
     return y
 
 
+def segmented_bytes(N, K):
+    return int(lib.zq4_segmented_bytes(N, K))
+
+
 def prepare_weight(wq_src, scales_src, N, K, flags=PREP_CONCAT_TO_INTERLEAVED, wq_dst=None,
                    scales_dst=None, stream=None):
+    """Rewrite a matrix into a kernel layout. With PREP_SEGMENTED the result
+    is one uint8 tensor of segmented_bytes(N, K) (scales inside) and None."""
+    if flags & PREP_SEGMENTED:
+        nb = segmented_bytes(N, K)
+        if nb == 0:
+            raise ValueError("segmented layout needs N > 0 and K % 256 == 0")
+        if wq_dst is None:
+            wq_dst = torch.empty(nb, dtype=torch.uint8, device=wq_src.device)
+        w, s = _mat(wq_src, scales_src, N, K)
+        _check("zq4_prepare_weight", lib.zq4_prepare_weight(w, s, _ptr(wq_dst, "wq_dst", nb), None, N, K, flags,
+                                                            _stream(stream)))
+        return wq_dst, None
     if wq_dst is None:
         wq_dst = torch.empty_like(wq_src)
     if scales_dst is None:
@@ -195,3 +230,36 @@ def device_errors(clear: bool = True) -> int:
 
 def status_string(status: int) -> str:
     return lib.zq4_status_string(status).decode()
+
+
+class StackPlan:
+    """A decode step as one launch (zq4_stack_plan_init / zq4_stack_run).
+
+    ``jobs`` is a list of (seg, x, y, N, K, gate_up) with torch CUDA tensors,
+    seg the matrix in the segmented layout (prepare_weight with
+    PREP_SEGMENTED); a job may take an earlier job's y as its x. The plan keeps
+    references to every tensor (they must stay allocated) and owns its
+    device buffer."""
+
+    def __init__(self, jobs, M, stream=None):
+        arr = (StackJob * len(jobs))()
+        self._keep = []
+        for i, (seg, x, y, N, K, gate_up) in enumerate(jobs):
+            w = _ptr(seg, "seg", segmented_bytes(N, K))
+            xp = _ptr(x, "x", M * K * 2, 2)
+            yp = _ptr(y, "y", M * (N // 2 if gate_up else N) * 2, 2)
+            arr[i] = StackJob(w.value, None, xp.value, yp.value, N, K, 1 if gate_up else 0)
+            self._keep += [seg, x, y]
+        nbytes = ctypes.c_size_t(0)
+        _check("zq4_stack_plan_bytes", lib.zq4_stack_plan_bytes(ctypes.cast(arr, ctypes.c_void_p), len(jobs), M, ctypes.byref(nbytes)))
+        dev = x.device if jobs else None
+        self.buffer = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        self.plan = StackPlanC()
+        _check("zq4_stack_plan_init",
+               lib.zq4_stack_plan_init(ctypes.cast(arr, ctypes.c_void_p), len(jobs), M, ctypes.c_void_p(self.buffer.data_ptr()),
+                                       nbytes.value, ctypes.byref(self.plan), _stream(stream)))
+        self.n_jobs, self.M = len(jobs), M
+
+    def run(self, stream=None):
+        _check("zq4_stack_run", lib.zq4_stack_run(ctypes.byref(self.plan), _stream(stream)))
+

@@ -149,6 +149,42 @@ def test_prepare_concat_to_interleaved(zq4, oracle):
     assert np.array_equal(wc.cpu().numpy().view(np.uint32), wq)
 
 
+def _segmented_reference(wq, sc, N, K):
+    """The segmented layout, built byte by byte from its definition in the
+    C header (tile-major 2304-byte segments: swizzled code runs, then
+    scales; rows past N zero)."""
+    T, S = (N + 15) // 16, K // 256
+    codes = wq.view(np.uint8).reshape(N, K // 2)
+    scb = sc.view(np.uint8).reshape(N, K // 16)
+    out = np.zeros(T * S * 2304, np.uint8)
+    for t in range(T):
+        for s in range(S):
+            base = (t * S + s) * 2304
+            for i in range(16):
+                n = 16 * t + i
+                if n >= N:
+                    continue
+                for c in range(8):
+                    off = base + i * 128 + 16 * (c ^ (i % 8))
+                    out[off:off + 16] = codes[n, 128 * s + 16 * c: 128 * s + 16 * c + 16]
+                out[base + 2048 + 16 * i: base + 2048 + 16 * i + 16] = scb[n, 16 * s: 16 * s + 16]
+    return out
+
+
+@pytest.mark.parametrize("N,K,interleave", [(37, 512, False), (16, 256, False), (40, 768, True)])
+def test_prepare_segmented_layout_bytes(zq4, N, K, interleave):
+    wq, sc, _ = _case("segl", 1, N, K)
+    flags = zq4.PREP_SEGMENTED | (zq4.PREP_CONCAT_TO_INTERLEAVED if interleave else 0)
+    seg, none = zq4.prepare_weight(dev(wq), dev(sc), N, K, flags)
+    assert none is None and seg.numel() == zq4.segmented_bytes(N, K)
+    if interleave:
+        order = np.empty(N, np.int64)
+        order[0::2] = np.arange(N // 2)
+        order[1::2] = N // 2 + np.arange(N // 2)
+        wq, sc = wq[order], sc[order]
+    assert np.array_equal(seg.cpu().numpy(), _segmented_reference(wq, sc, N, K))
+
+
 @pytest.mark.parametrize("N,K", [(1, 32), (13, 96), (64, 3072), (5, 9728)])
 def test_dequant_bit_exact(zq4, oracle, N, K):
     wq, sc, _ = _case("deq", 1, N, K)
