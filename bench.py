@@ -41,7 +41,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
-    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel"])
+    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill"])
+    ap.add_argument("--stack-mode", default="calls", choices=["calls", "plan"],
+                    help="phi3/qwen3: one launch per projection, or the whole step as one launch")
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
     ap.add_argument("--gate-up", action="store_true", help="kernel workload: fused gate_up + SiLU*mul")
@@ -170,12 +172,19 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash():
+# the source files that define each profiled kernel (its traffic figure is
+# dropped as soon as one of them changes)
+KERNEL_SOURCES = {
+    "gate_up_phi3_M1": ("zq4_decode_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
+    "prefill_gate_up_M1024": ("zq4_prefill_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
+}
+
+
+def kernel_source_hash(tag: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int4_weight_only_q4f16_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in KERNEL_SOURCES[tag]:
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -193,7 +202,7 @@ def profiled_traffic(kernel_tag: str):
             if v.startswith("`"):
                 v = v[1:].split("`", 1)[0]
             vals[k.strip()] = v
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(kernel_tag):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -226,10 +235,15 @@ def oracle_sample_rate(projs, budget_s: float, M: int = 1):
             covered += rows.size * (K // 8 * 4 + K // 32 * 2)
             if spent >= budget_s:
                 done.append(f"{name}[layer {layer}] rows 0..{rows[-1]}")
-                desc = "; ".join(done)
-                return covered / spent, o.num_threads(), desc
+                return covered / spent, o.num_threads(), _sample_desc(done)
         done.append(f"{name}[layer {layer}]")
-    return covered / max(spent, 1e-9), o.num_threads(), "; ".join(done)
+    return covered / max(spent, 1e-9), o.num_threads(), _sample_desc(done)
+
+
+def _sample_desc(done):
+    if len(done) <= 4:
+        return "; ".join(done)
+    return f"{len(done)} projections in step order ({done[0]} ... {done[-1]})"
 
 
 def phi3_projs():
@@ -280,7 +294,7 @@ def capture(torch, fn, stream):
 def run_phi3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod, synth, zq4
     dev = torch.device("cuda", dist.local)
-    st = stack_mod.phi3_stack(M=1, device=dev)
+    st = stack_mod.phi3_stack(M=1, device=dev, mode=args.stack_mode)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         st.launch_step(stream)                         # eager step: sets kernel attributes
@@ -317,7 +331,7 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
     p0 = gu[0]
     gu_bytes = p0.nbytes + st.M * p0.K * 2 + st.M * (p0.N // 2) * 2
     achieved = gu_bytes / gu_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_dense<1,32,2> (gate_up + SiLU*mul, 16384x3072)",
+    roofline = {"bound": "hbm", "kernel": "k_decode_tc<1,2> (gate_up + SiLU*mul, 16384x3072)",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
@@ -352,6 +366,9 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
                    "l2": f"inputs larger than L2: {st.weight_bytes() / 1e9:.2f} GB of distinct "
                          f"weights per step vs {L2_BYTES >> 20} MiB L2",
                    "parallelism": f"replicas x{dist.world}", "graph": "one CUDA graph per step",
+                   "step": ("one launch per projection (zq4_gemv / zq4_gate_up_silu)" if args.stack_mode == "calls"
+                            else "whole step as one persistent launch (zq4_stack_run)"),
+                   "dependencies": "every projection starts after the previous one completes",
                    "arith": "int4 codes -> exact f16 (q-7); f16*f16 products, fp32 accumulate; "
                             "f16 out"},
         "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
@@ -440,7 +457,7 @@ def run_gemv3072(args, torch, dist, peaks, peak_kind):
 
 def run_qwen3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod
-    st = stack_mod.qwen3_4b_stack(M=args.m)
+    st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode if args.m <= 8 else "calls")
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         st.launch_step(stream)
@@ -545,6 +562,62 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
                        "l2": f"{C} distinct copies, {C * b / 1e6:.0f} MB"}}
 
 
+def run_prefill(args, torch, dist, peaks, peak_kind):
+    """The prefill-chunk GEMM workloads: 1024 tokens through the Phi-3 gate_up
+    shape (16384 x 3072) and the down shape (3072 x 8192), each timed over
+    distinct weight copies that together exceed L2. Reports TFLOP/s of the
+    pair (2*M*N*K per GEMM) against the measured dense bf16 peak (f16 has the
+    same nominal tensor rate)."""
+    from int4_weight_only_q4f16_gb300 import synth, zq4
+    M = 1024
+    shapes = [("gate_up shape", 16384, 3072), ("down shape", 3072, 8192)]
+    stream = torch.cuda.Stream()
+    per_shape, tot_flop, tot_s = [], 0, 0.0
+    for name, N, K in shapes:
+        wbytes = N * (K // 8) * 4 + N * (K // 32) * 2
+        copies = max(2, int(4 * L2_BYTES // wbytes) + 1)
+        wq, sc = synth.weight("prefill_" + name, N, K, 0)
+        W = torch.from_numpy(wq.view(np.int32)).cuda().repeat(copies, 1).view(copies, N, K // 8)
+        S = torch.from_numpy(sc).cuda().repeat(copies, 1).view(copies, N, K // 32)
+        x = torch.from_numpy(synth.activations(synth.rng_for("prefill_x", N, K), M, K)).cuda()
+        y = torch.empty((copies, M, N), dtype=torch.float16, device="cuda")
+
+        def chain():
+            for c in range(copies):
+                zq4.gemv(W[c], S[c], x, N, K, y=y[c], stream=stream)
+        with torch.cuda.stream(stream):
+            chain()
+        g = capture(torch, chain, stream)
+        replay_on(torch, g, stream, max(3, args.warmup))
+        reps = max(3, min(args.steps // copies, 50))
+        el = time_replays(torch, g.replay, reps, stream)
+        torch.cuda.synchronize()
+        assert torch.isfinite(y).all() and (y != 0).any(), "prefill output zero/non-finite"
+        per = el / (reps * copies)
+        flop = 2 * M * N * K
+        per_shape.append({"shape": f"{M}x{N}x{K}", "name": name, "us_per_gemm": round(per * 1e6, 2),
+                          "tflops": round(flop / per / 1e12, 1), "copies": copies,
+                          "frac_of_measured_bf16": round(flop / per / 1e12 / peaks["bf16_tflops"], 4)})
+        tot_flop += flop
+        tot_s += per
+        del W, S, y, g
+        torch.cuda.empty_cache()
+    tf = tot_flop / tot_s / 1e12
+    best = max(per_shape, key=lambda d: d["tflops"])
+    return {"metric": "prefill-chunk dequant GEMM TFLOP/s (M=1024, gate_up and down shapes)",
+            "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": dist.world, "higher_is_better": True,
+            "dtype": "f16 x f16 -> fp32", "data": "synthetic", "shapes": per_shape,
+            "roofline": {"bound": "tensor", "kernel": "k_prefill (tcgen05 kind::f16, dequant into SMEM)",
+                         "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops burst; f16 nominal = bf16)",
+                         "traffic": profiled_traffic("prefill_gate_up_M1024"),
+                         "traffic_note": "DRAM bytes of one gate_up-shape launch (ncu)",
+                         "best_shape": best["shape"]},
+            "config": {"workload": "prefill chunk, 1024 tokens, Phi-3 gate_up 16384x3072 and down 3072x8192",
+                       "l2": "distinct weight copies per shape exceed 4x L2"}}
+
+
 def run_reference(args, dist):
     """The CPU oracle on the host cores, timed on a bounded sample of the
     Phi-3 stack; each step covers the same row sample."""
@@ -615,7 +688,7 @@ def main():
     torch.cuda.set_device(dist.local)
     peaks, kind = measured_peaks()
     fn = {"phi3": run_phi3, "gemv3072": run_gemv3072, "qwen3": run_qwen3, "moe": run_moe,
-          "kernel": run_kernel}[args.workload]
+          "kernel": run_kernel, "prefill": run_prefill}[args.workload]
     line = fn(args, torch, dist, peaks, kind)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
