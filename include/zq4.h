@@ -293,6 +293,36 @@ ZQ4_API zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, in
  */
 ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
 
+/*
+ * zq4_stack_plan_init_static -- zq4_stack_plan_init for callers that cannot
+ * give the library device memory: the plan is written into a fixed array
+ * inside the library (64 KiB of device memory reserved when the library
+ * loads) instead of a caller buffer, and the call itself allocates nothing
+ * (no device or host heap allocation; it issues a memset and one small copy
+ * per job). Meant for a host layer that has no handle on the device
+ * allocator (the memory pool belongs to another framework and is not
+ * reachable from it), and for code that must not allocate once it is
+ * running (an allocation can block, synchronise or fail). The method on the
+ * pages has no counterpart of this call; it is a deployment variant of
+ * zq4_stack_plan_init, and the plan it fills runs with zq4_stack_run.
+ *
+ * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
+ * 64 KiB array, i.e. at most 1257 jobs; a longer list returns
+ * ZQ4_ERR_UNSUPPORTED and changes nothing. What must start at zero (the
+ * plan's launch counter, abort flag and per-job counters) is cleared by
+ * every call. The first call on a device resolves the array's address
+ * (cudaGetSymbolAddress); every call synchronises `stream`, so call it
+ * before any stream capture begins.
+ *
+ * There is one such plan per device: a second zq4_stack_plan_init_static
+ * replaces the first, and a call that overlaps a zq4_stack_run of the static
+ * plan on another stream -- or two such runs on different streams -- race
+ * on the same counters and give wrong results. Errors as
+ * zq4_stack_plan_init.
+ */
+ZQ4_API zq4_status zq4_stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M,
+                                              zq4_stack_plan *plan, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

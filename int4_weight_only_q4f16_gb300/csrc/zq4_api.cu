@@ -281,4 +281,10 @@ zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream)
     return stack_run(plan, static_cast<cudaStream_t>(stream));
 }
 
+zq4_status zq4_stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, zq4_stack_plan *plan,
+                                      void *stream)
+{
+    return stack_plan_init_static(jobs, n_jobs, M, plan, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -59,6 +59,8 @@ zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t
 zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
                            zq4_stack_plan *plan, cudaStream_t s);
 zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s);
+zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, zq4_stack_plan *plan,
+                                  cudaStream_t s);
 cudaError_t read_stack_error(unsigned *flags, bool clear);
 
 // zq4_prefill_tc.cu: the tensor-core GEMM for chunks of kPrefillMinRows or

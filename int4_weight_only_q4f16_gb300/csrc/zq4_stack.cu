@@ -54,6 +54,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -511,6 +512,10 @@ namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Largest dynamic shared memory k_stack has been allowed per device: one
+// record for every caller, so the limit only ever grows.
+int stack_smem_set[kMaxDevices] = {};
+
 struct Layout {
     size_t hdr, jobs, job_cnt, total;
 };
@@ -575,9 +580,8 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     const Layout l = layout_for(n_jobs);
     if (bytes < l.total) return ZQ4_ERR_SHAPE;
     // the kernel needs every CTA resident at once
-    static int smem_set[kMaxDevices] = {};
     const size_t smem = st::smem_bytes(M, mk);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, smem_set);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
     if (e != cudaSuccess) return cuda_status(e);
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, st::k_stack, st::kThreads, smem);
@@ -630,6 +634,89 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
     void *args[] = {&p};
     return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),
                                                    dim3(st::kThreads), args, st::smem_bytes(p.M, p.max_k), s));
+}
+
+// ---------------------------------------------------------------------------
+// A plan without a caller buffer: the library's own fixed-size device array
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1257 jobs
+static_assert(sizeof(st::Job) == 48, "the documented job limit assumes 48-byte job entries");
+
+// The plan lives here when the caller has no device memory to give. Header
+// and counters are cleared by every zq4_stack_plan_init_static.
+static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
+
+// Device address of g_static_plan on the current device, resolved once per
+// device.
+cudaError_t static_plan_address(void **ptr)
+{
+    static std::atomic<void *> cache[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_static_plan);
+        if (e != cudaSuccess) return e;
+        cache[dev].store(p, std::memory_order_release);
+    }
+    *ptr = p;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, zq4_stack_plan *plan,
+                                  cudaStream_t s)
+{
+    if (!plan) return ZQ4_ERR_NULL;
+    int mk, mt;
+    zq4_status stt = check_jobs(jobs, n_jobs, M, sm_count(), &mk, &mt);
+    if (stt != ZQ4_OK) return stt;
+    const Layout l = layout_for(n_jobs);
+    if (l.total > kStaticPlanBytes) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
+    const size_t smem = st::smem_bytes(M, mk);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
+    if (e != cudaSuccess) return cuda_status(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, st::k_stack, st::kThreads, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (per_sm < 1) return ZQ4_ERR_UNSUPPORTED;
+    void *dev = nullptr;
+    e = static_plan_address(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    uint8_t *base = static_cast<uint8_t *>(dev);
+    // header and counters start at zero; the job table is written after
+    e = cudaMemsetAsync(base, 0, l.total, s);
+    for (int j = 0; j < n_jobs && e == cudaSuccess; ++j) {
+        const zq4_stack_job &b = jobs[j];
+        st::Job jb;
+        memset(&jb, 0, sizeof(jb));
+        jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
+        jb.x = b.x;
+        jb.y = b.y;
+        jb.N = b.N;
+        jb.K = b.K;
+        jb.T = (b.N + 15) / 16;
+        jb.S = b.K / st::kSegCols;
+        jb.gate_up = b.gate_up ? 1 : 0;
+        jb.y_stride = b.gate_up ? b.N / 2 : b.N;
+        // from pageable memory: the entry is staged before the call returns
+        e = cudaMemcpyAsync(base + l.jobs + size_t(j) * sizeof(st::Job), &jb, sizeof(jb), cudaMemcpyHostToDevice, s);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    plan->dev = dev;
+    plan->bytes = l.total;
+    plan->n_jobs = n_jobs;
+    plan->M = M;
+    plan->grid = sm_count();
+    plan->max_k = mk;
+    plan->max_tiles = mt;
+    return ZQ4_OK;
 }
 
 cudaError_t read_stack_error(unsigned *flags, bool clear)

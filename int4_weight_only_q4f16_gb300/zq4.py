@@ -37,7 +37,7 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes")
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static")
 
 
 class Zq4Error(RuntimeError):
@@ -73,6 +73,7 @@ def _load():
         "zq4_stack_plan_bytes": [P, I, I, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
+        "zq4_stack_plan_init_static": [P, I, I, P, P],
     }
     lib.zq4_segmented_bytes.argtypes = [I, I]
     lib.zq4_segmented_bytes.restype = ctypes.c_size_t
@@ -258,6 +259,30 @@ class StackPlan:
         _check("zq4_stack_plan_init",
                lib.zq4_stack_plan_init(ctypes.cast(arr, ctypes.c_void_p), len(jobs), M, ctypes.c_void_p(self.buffer.data_ptr()),
                                        nbytes.value, ctypes.byref(self.plan), _stream(stream)))
+        self.n_jobs, self.M = len(jobs), M
+
+    def run(self, stream=None):
+        _check("zq4_stack_run", lib.zq4_stack_run(ctypes.byref(self.plan), _stream(stream)))
+
+
+class StaticStackPlan:
+    """A decode-step plan held in the library's fixed device array
+    (zq4_stack_plan_init_static): no device memory is allocated for it. One
+    per device at a time; jobs as StackPlan."""
+
+    def __init__(self, jobs, M, stream=None):
+        arr = (StackJob * len(jobs))()
+        self._keep = []
+        for i, (seg, x, y, N, K, gate_up) in enumerate(jobs):
+            w = _ptr(seg, "seg", segmented_bytes(N, K))
+            xp = _ptr(x, "x", M * K * 2, 2)
+            yp = _ptr(y, "y", M * (N // 2 if gate_up else N) * 2, 2)
+            arr[i] = StackJob(w.value, None, xp.value, yp.value, N, K, 1 if gate_up else 0)
+            self._keep += [seg, x, y]
+        self.plan = StackPlanC()
+        _check("zq4_stack_plan_init_static",
+               lib.zq4_stack_plan_init_static(ctypes.cast(arr, ctypes.c_void_p), len(jobs), M,
+                                              ctypes.byref(self.plan), _stream(stream)))
         self.n_jobs, self.M = len(jobs), M
 
     def run(self, stream=None):
