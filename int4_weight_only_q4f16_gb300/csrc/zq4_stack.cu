@@ -33,16 +33,15 @@
 //    fp32 result times the fp32 group scale to its accumulator.
 //  * CTA c takes the whole 16-row tiles [c*T/G, (c+1)*T/G) of every job and
 //    splits their segments evenly over its warps. A tile that lies in one
-//    warp's range is written by that warp; a tile split between warps has
-//    each part parked in shared memory and the CTA's last warp on it (a
-//    shared arrival counter) sums the parts in warp order (bit-reproducible)
-//    and writes the outputs. Tiles never span CTAs, so no partial sum goes
-//    through global memory: every job boundary costs one grid barrier and
-//    nothing else.
-//  * Job boundary: CTA barrier, one release-add per CTA on the job's
-//    counter, acquire-poll until every CTA has arrived, CTA barrier, then x
-//    of the next job is staged into shared memory (L2 reads: it may have
-//    been written by other SMs during this kernel).
+//    warp's range is written by that warp; a warp holding part of a tile
+//    parks the part in shared memory, and at the end of the job all threads
+//    of the CTA sum the parked parts of every split tile in warp order
+//    (bit-reproducible) and write them. Tiles never span CTAs, so no partial
+//    sum goes through global memory.
+//  * Job boundary: CTA barrier, split tiles summed, one release-add per CTA
+//    on the job's counter, acquire-poll until every CTA has arrived, CTA
+//    barrier, then x of the next job is staged into shared memory (L2 reads:
+//    it may have been written by other SMs during this kernel).
 //  * Counters grow monotonically: a launch waits for (launch index + 1) x
 //    grid arrivals, the launch index being read from the plan at start and
 //    advanced by the last CTA to finish.
@@ -76,7 +75,6 @@ constexpr int kSegCols = 256;
 constexpr int kCodeBytes = 16 * 128;
 constexpr int kSegBytes = kCodeBytes + 16 * 8 * 2;   // codes + scales of one segment
 constexpr int kTokCols = 8;                       // MMA columns = tokens (M <= 8)
-constexpr int kOutPerLane = 16 * kTokCols / 32;   // tile outputs per lane when one warp writes a tile
 
 struct Header {
     unsigned epoch;     // launches completed
@@ -105,9 +103,7 @@ constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
 constexpr size_t kMiscOff = kBarOff + size_t(kWarps) * kSlots * 8;
 constexpr size_t kParkOff = kMiscOff + 128;                          // warp partials [kWarps*2][16][kTokCols]
-constexpr int kLocalTiles = 256;                                     // tile counters per CTA
-constexpr size_t kCntOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;
-constexpr size_t kTabOff = kCntOff + kLocalTiles * 4;                // warp range table [2][kWarps + 1]
+constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range table [2][kWarps + 1]
 constexpr size_t kXsOff = kTabOff + 2 * 4 * (kWarps + 1 + 15) / 16 * 16;
 __host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + size_t(M) * xs_row_bytes(max_k); }
 
@@ -168,57 +164,38 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     return r;
 }
 
-// A tile this warp holds only part of (tiles never cross CTA ranges): park
-// the part in shared memory; the CTA's last warp on the tile sums the parts
-// in warp order and writes the outputs. Lane w (w <= kWarps) brings warp
-// w's range start `wbl` (segments) and first tile `wftl` for this job, so
-// which warps meet the tile and which parking slot each used come out of
-// two ballots, with no divisions and no dependent table lookups. Out of
-// line: it runs once or twice per warp and job.
-__device__ __noinline__ void flush_split(float acc0, float acc1, float acc2, float acc3, int tt, int S, int tb,
-                                         int warp, int gate_up, int M, int N, int y_stride, uint16_t *y,
-                                         float *wpark, unsigned *tcnt, int wbl, int wftl)
+// Tiles of the finished job that were split between warps: every thread of
+// the CTA takes (tile, output) items and sums the parked parts of the
+// contributing warps in warp order (bit-reproducible), then writes the
+// output. `wtab` holds the job's warp range starts (segments, kWarps + 1
+// entries) and each warp's first tile; a warp parked its part of its first
+// tile in slot 0 and of its last in slot 1.
+__device__ __forceinline__ void finalize_split(int tb, int te, int S, int gate_up, int M, int N, int y_stride,
+                                               uint16_t *y, const float *wpark, const int *wtab)
 {
-    const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
-    const float acc[4] = {acc0, acc1, acc2, acc3};
-    const int row0 = tt * 16;
-    const int lo = tt * S, hi = lo + S;
-    const int wb_next = __shfl_down_sync(0xffffffffu, wbl, 1);
-    // warps (lanes < kWarps) whose nonempty range meets the tile, and those
-    // for which the tile is not their first (they parked in slot 1)
-    const unsigned mask = __ballot_sync(0xffffffffu, lane < kWarps && wbl < wb_next && wbl < hi && wb_next > lo);
-    const unsigned slot1 = __ballot_sync(0xffffffffu, lane < kWarps && tt != wftl);
-    // 1) park this warp's part
-    float *pk = wpark + ((warp * 2 + ((slot1 >> warp) & 1)) * 16) * kTokCols;
+    const int *wb = wtab, *wft = wtab + kWarps + 1;
+    const int per_tok = gate_up ? 8 : 16;                // outputs of a tile per token
+    const int items = (te - tb) * per_tok * M;
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+        const int tt = tb + it / (per_tok * M);
+        const int o = it - (tt - tb) * (per_tok * M);
+        const int lo = tt * S, hi = lo + S;
+        unsigned mask = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) pk[(r + 8 * h) * kTokCols + 2 * t + c] = acc[2 * h + c];
-    __threadfence_block();
-    __syncwarp();
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(&tcnt[tt - tb], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != unsigned(__popc(mask) - 1)) return;     // another warp finishes the tile
-    __threadfence_block();
-    if (lane == 0) tcnt[tt - tb] = 0u;
-    // 2) sum the parts in warp order: lane handles output o (raw rows)
-    const int per_tok = gate_up ? 8 : 16;                // outputs of the tile per token
-#pragma unroll
-    for (int q = 0; q < kOutPerLane; ++q) {
-        const int o = lane + 32 * q;
-        if (o >= per_tok * M) continue;
+        for (int w = 0; w < kWarps; ++w)
+            if (wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo) mask |= 1u << w;
+        if (__popc(mask) < 2) continue;                  // one warp held the whole tile
         const int m = o / per_tok, i = o - m * per_tok;
         const int ra = gate_up ? 2 * i : i;
         float v0 = 0.f, v1 = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             if (!((mask >> w) & 1)) continue;
-            const float *qk = wpark + ((w * 2 + ((slot1 >> w) & 1)) * 16) * kTokCols;
+            const float *qk = wpark + ((w * 2 + (tt == wft[w] ? 0 : 1)) * 16) * kTokCols;
             v0 += qk[ra * kTokCols + m];
             if (gate_up) v1 += qk[(ra + 1) * kTokCols + m];
         }
-        // 3) write the output
+        const int row0 = tt * 16;
         if (!gate_up) {
             if (row0 + i < N) y[size_t(m) * y_stride + row0 + i] = float_to_f16_bits(v0);
         } else if (row0 + 2 * i + 1 < N) {
@@ -244,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const uint32_t bar0 = sbase + uint32_t(kBarOff) + uint32_t(warp * kSlots * 8);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kMiscOff);
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
-    unsigned *tcnt = reinterpret_cast<unsigned *>(smem + kCntOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
     uint8_t *xs = smem + kXsOff;
     const uint32_t xrow = uint32_t(xs_row_bytes(p.max_k));
@@ -253,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const unsigned target = (launch + 1u) * unsigned(G);
 
     if (threadIdx.x == 0) *s_abort = 0;
-    for (int i = threadIdx.x; i < kLocalTiles; i += kThreads) tcnt[i] = 0u;
     if (lane == 0) {
         for (int j = 0; j < kSlots; ++j) mbar_init(bar0 + 8 * j, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -316,6 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         // ---- wait until every CTA has finished job j-1, then stage x_j
         if (j > 0) {
             __syncthreads();
+            if (!*s_abort) {
+                const Job &pj = p.jobs[j - 1];
+                int ptb, pte;
+                split(0, pj.T, cta, G, ptb, pte);
+                finalize_split(ptb, pte, pj.S, pj.gate_up, p.M, pj.N, pj.y_stride, pj.y, wpark, wtab);
+            }
+            __syncthreads();
             if (threadIdx.x == 0 && !*s_abort) {
                 // release: this CTA's outputs of job j-1 (ordered before by
                 // the barrier) become visible with the increment
@@ -361,12 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         __syncthreads();
 
         const int S = jb.S, gate_up = jb.gate_up;
-        // lane w: warp w's range start and first tile (lanes past kWarps: unused)
-        const int wbl = wtab[min(lane, kWarps)], wftl = wtab[kWarps + 1 + min(lane, kWarps)];
         int tb, te, ub, ue;
         split(0, jb.T, cta, G, tb, te);
         const int cb = tb * S, ce = te * S;
         split(cb, ce, warp, kWarps, ub, ue);
+        const int first_tile = ub / S;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int cur_tile = -1;
 
@@ -404,8 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     }
                 }
             } else {
-                flush_split(acc[0], acc[1], acc[2], acc[3], tt, S, tb, warp, gate_up, p.M, jb.N, jb.y_stride,
-                            jb.y, wpark, tcnt, wbl, wftl);
+                // part of a tile shared with other warps: park it (summed at job end)
+                float *pk = wpark + ((warp * 2 + (tt == first_tile ? 0 : 1)) * 16) * kTokCols;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) pk[(r + 8 * h) * kTokCols + 2 * t + c] = acc[2 * h + c];
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = 0.f;
@@ -480,6 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     }
     __syncthreads();
     if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+    if (!*s_abort && n > 0) {                            // the last job's split tiles
+        const Job &lj = p.jobs[n - 1];
+        int ltb, lte;
+        split(0, lj.T, cta, G, ltb, lte);
+        finalize_split(ltb, lte, lj.S, lj.gate_up, p.M, lj.N, lj.y_stride, lj.y, wpark, wtab);
+    }
     // let every copy this warp issued land before the CTA exits
     {
         int outstanding = 0;
@@ -545,9 +536,8 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
             return ZQ4_ERR_ALIGN;
         mk = std::max(mk, b.K);
         mt = std::max(mt, (b.N + 15) / 16);
-        // a CTA's tiles must fit its shared tile counters; 32-bit part math
+        // 32-bit part math
         const long long T = (b.N + 15) / 16, U = T * (b.K / st::kSegCols);
-        if ((T + grid - 1) / grid > st::kLocalTiles) return ZQ4_ERR_UNSUPPORTED;
         if (U * std::max(grid, st::kWarps) >= (1ll << 31)) return ZQ4_ERR_UNSUPPORTED;
     }
     if (st::smem_bytes(M, mk) > size_t(227) * 1024) return ZQ4_ERR_UNSUPPORTED;
