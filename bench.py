@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
     ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill"])
-    ap.add_argument("--stack-mode", default="calls", choices=["calls", "plan"],
+    ap.add_argument("--stack-mode", default="calls", choices=["calls", "seg", "plan"],
                     help="phi3/qwen3: one launch per projection, or the whole step as one launch")
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
@@ -366,8 +366,9 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
                    "l2": f"inputs larger than L2: {st.weight_bytes() / 1e9:.2f} GB of distinct "
                          f"weights per step vs {L2_BYTES >> 20} MiB L2",
                    "parallelism": f"replicas x{dist.world}", "graph": "one CUDA graph per step",
-                   "step": ("one launch per projection (zq4_gemv / zq4_gate_up_silu)" if args.stack_mode == "calls"
-                            else "whole step as one persistent launch (zq4_stack_run)"),
+                   "step": {"calls": "one launch per projection (zq4_gemv / zq4_gate_up_silu)",
+                            "seg": "one launch per projection on segmented weights (zq4_gemv_seg / _gate_up_silu_seg)",
+                            "plan": "whole step as one persistent launch (zq4_stack_run)"}[args.stack_mode],
                    "dependencies": "every projection starts after the previous one completes",
                    "arith": "int4 codes -> exact f16 (q-7); f16*f16 products, fp32 accumulate; "
                             "f16 out"},
@@ -457,7 +458,7 @@ def run_gemv3072(args, torch, dist, peaks, peak_kind):
 
 def run_qwen3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod
-    st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode if args.m <= 8 else "calls")
+    st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode if args.m <= 8 else "calls")  # M > 8: canonical only
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         st.launch_step(stream)

@@ -226,6 +226,26 @@ ZQ4_API zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, u
                            void *stream);
 
 /*
+ * zq4_gemv_seg / zq4_gate_up_silu_seg -- zq4_gemv and zq4_gate_up_silu for
+ * 1 <= M <= 8 on a matrix in the segmented layout (zq4_prepare_weight with
+ * ZQ4_PREP_SEGMENTED, prepared once when the weights are loaded); the same
+ * results as the canonical-layout calls up to the order of fp32 additions.
+ * Source as zq4_gemv / zq4_gate_up_silu. The layout lets every weight
+ * segment arrive with one contiguous copy, and the kernel is sized so that
+ * two consecutive launches share the SMs (the next projection's weights
+ * stream while the current one finishes).
+ *   wseg: zq4_segmented_bytes(N, K) bytes, 16-byte aligned; x [M, K] f16,
+ *   16-byte aligned; y [M, N] (or h [M, N2/2]) f16. K % 256 == 0; N2 even.
+ * Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED (M > 8, or x of M rows of K does not fit in shared
+ * memory), ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_gemv_seg(const uint32_t *wseg, const uint16_t *x, uint16_t *y, int M, int N, int K,
+                                void *stream);
+ZQ4_API zq4_status zq4_gate_up_silu_seg(const uint32_t *wseg, const uint16_t *x, uint16_t *h, int M, int N2,
+                                        int K, void *stream);
+
+/*
  * Decode step as one launch: an ordered list of projections ("jobs") run by
  * a persistent kernel, each job starting only after every output of the job
  * before it is written -- the dependency of a decode step, in which every

@@ -200,11 +200,12 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
 zq4_status zq4_device_errors(uint32_t *flags, int clear)
 {
     if (!flags) return ZQ4_ERR_NULL;
-    unsigned v = 0, vp = 0, vk = 0;
+    unsigned v = 0, vp = 0, vk = 0, vs = 0;
     zq4_status st = cuda_status(read_device_error(&v, clear != 0));
     if (st == ZQ4_OK) st = cuda_status(read_prefill_error(&vp, clear != 0));
     if (st == ZQ4_OK) st = cuda_status(read_stack_error(&vk, clear != 0));
-    *flags = v | vp | vk;
+    if (st == ZQ4_OK) st = cuda_status(read_seg_error(&vs, clear != 0));
+    *flags = v | vp | vk | vs;
     return st;
 }
 
@@ -263,6 +264,30 @@ zq4_status zq4_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t 
     if (!w) return ZQ4_ERR_NULL;
     if (!aligned16(w)) return ZQ4_ERR_ALIGN;
     return cuda_status(launch_dequant_f16(wq, scales, w, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+static zq4_status gemv_seg_common(const uint32_t *wseg, const uint16_t *x, uint16_t *y, int M, int N, int K,
+                                  bool gate_up, void *stream)
+{
+    if (!wseg || !x || !y) return ZQ4_ERR_NULL;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 256 != 0 || (gate_up && (N & 1))) return ZQ4_ERR_SHAPE;
+    if (!aligned16(wseg) || !aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 1)) return ZQ4_ERR_ALIGN;
+    if (!seg_gemv_supported(M, K)) return ZQ4_ERR_UNSUPPORTED;
+    const size_t yb = size_t(M) * (gate_up ? N / 2 : N) * 2;
+    if (overlap(y, yb, wseg, segmented_bytes(N, K)) || overlap(y, yb, x, size_t(M) * K * 2)) return ZQ4_ERR_OVERLAP;
+    return cuda_status(launch_gemv_seg(reinterpret_cast<const uint8_t *>(wseg), x, y, M, N, K, gate_up,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_gemv_seg(const uint32_t *wseg, const uint16_t *x, uint16_t *y, int M, int N, int K, void *stream)
+{
+    return gemv_seg_common(wseg, x, y, M, N, K, false, stream);
+}
+
+zq4_status zq4_gate_up_silu_seg(const uint32_t *wseg, const uint16_t *x, uint16_t *h, int M, int N2, int K,
+                                void *stream)
+{
+    return gemv_seg_common(wseg, x, h, M, N2, K, true, stream);
 }
 
 zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes)

@@ -54,6 +54,12 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
                              uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t read_device_error(unsigned *flags, bool clear);
 
+// zq4_decode_seg.cu: decode GEMV / gate_up on the segmented layout, M <= 8
+bool seg_gemv_supported(int M, int K);
+cudaError_t launch_gemv_seg(const uint8_t *wseg, const uint16_t *x, uint16_t *y, int M, int N, int K,
+                            bool gate_up, cudaStream_t s);
+cudaError_t read_seg_error(unsigned *flags, bool clear);
+
 // zq4_stack.cu: the persistent decode-step kernel
 zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
 zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,

@@ -50,9 +50,10 @@ class DecodeStack:
 
     def __init__(self, layer_shapes, n_layers, head=None, M=1, device="cuda",
                  keep_host=False, seed=synth.MASTER_SEED, mode="calls"):
-        """mode "plan": the whole step is one persistent launch
-        (zq4_stack_run); "calls": one zq4_gemv / zq4_gate_up_silu per
-        projection."""
+        """mode "calls": one zq4_gemv / zq4_gate_up_silu per projection on
+        the canonical matrices; "seg": one zq4_gemv_seg / zq4_gate_up_silu_seg
+        per projection on segmented copies made once; "plan": the whole step
+        as one persistent launch (zq4_stack_run) on segmented copies."""
         self.M, self.device, self.n_layers = M, torch.device(device), n_layers
         self.mode = mode
         self.plan = None
@@ -98,6 +99,8 @@ class DecodeStack:
     def launches_per_step(self) -> int:
         if self.mode == "plan":
             return 1
+        if self.mode == "seg":
+            return len(self.jobs())
         per_layer = 0
         for name in self.order:
             p = self.layers[0][name]
@@ -125,18 +128,30 @@ class DecodeStack:
     def build_plan(self, stream=None):
         """Segmented copies of every matrix (kept on the projections) and the
         one-launch plan over them."""
-        pjobs = []
-        for wq, sc, x, y, N, K, gate_up in self.jobs():
-            seg, _ = zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED, stream=stream)
-            pjobs.append((seg, x, y, N, K, gate_up))
+        pjobs = [(seg, x, y, N, K, gate_up)
+                 for seg, (wq, sc, x, y, N, K, gate_up) in zip(self.segmented(stream), self.jobs())]
         self.plan = zq4.StackPlan(pjobs, self.M, stream=stream)
         return self.plan
+
+    def segmented(self, stream=None):
+        """Segmented copies of every matrix, in step order (made once)."""
+        if getattr(self, "_seg", None) is None:
+            self._seg = [zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED, stream=stream)[0]
+                         for wq, sc, x, y, N, K, gate_up in self.jobs()]
+        return self._seg
 
     def launch_step(self, stream=None):
         if self.mode == "plan":
             if self.plan is None:
                 self.build_plan(stream)
             self.plan.run(stream)
+            return
+        if self.mode == "seg":
+            for seg, (wq, sc, x, y, N, K, gate_up) in zip(self.segmented(stream), self.jobs()):
+                if gate_up:
+                    zq4.gate_up_silu_seg(seg, x, N, K, h=y, stream=stream)
+                else:
+                    zq4.gemv_seg(seg, x, N, K, y=y, stream=stream)
             return
         for l, layer in enumerate(self.layers):
             for name in self.order:

@@ -37,7 +37,7 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static")
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg")
 
 
 class Zq4Error(RuntimeError):
@@ -74,6 +74,8 @@ def _load():
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
+        "zq4_gemv_seg": [P, P, P, I, I, I, P],
+        "zq4_gate_up_silu_seg": [P, P, P, I, I, I, P],
     }
     lib.zq4_segmented_bytes.argtypes = [I, I]
     lib.zq4_segmented_bytes.restype = ctypes.c_size_t
@@ -174,6 +176,27 @@ def moe_gemv(wq_bank, scales_bank, num_experts, x, N, K, expert_ids, mode, route
         _ptr(route_w, "route_w", T * top_k * 4, 4), top_k, mode,
         _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
     return y
+
+
+def gemv_seg(wseg, x, N, K, y=None, stream=None):
+    """gemv on a segmented-layout matrix (prepare_weight with PREP_SEGMENTED)."""
+    M = x.numel() // K
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check("zq4_gemv_seg", lib.zq4_gemv_seg(_ptr(wseg, "wseg", segmented_bytes(N, K)), _ptr(x, "x", M * K * 2, 2),
+                                            _ptr(y, "y", M * N * 2, 2), M, N, K, _stream(stream)))
+    return y
+
+
+def gate_up_silu_seg(wseg, x, N2, K, h=None, stream=None):
+    """gate_up_silu on a segmented-layout matrix."""
+    M = x.numel() // K
+    if h is None:
+        h = torch.empty((M, N2 // 2), dtype=torch.float16, device=x.device)
+    _check("zq4_gate_up_silu_seg",
+           lib.zq4_gate_up_silu_seg(_ptr(wseg, "wseg", segmented_bytes(N2, K)), _ptr(x, "x", M * K * 2, 2),
+                                    _ptr(h, "h", M * (N2 // 2) * 2, 2), M, N2, K, _stream(stream)))
+    return h
 
 
 def segmented_bytes(N, K):
