@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_seg(Args a)
 
     // ---- x, once the previous kernel's writes are visible
     griddep_wait();
-    stage_x(xs, xrow, a.x, a.M, a.K, threadIdx.x, kThreads);
+    stage_x<8>(xs, xrow, a.x, a.M, a.K, threadIdx.x, kThreads);
     __syncthreads();
     griddep_launch_dependents();
 

@@ -58,10 +58,10 @@ __device__ __forceinline__ void ldm_offsets(int lane, uint32_t (&off)[4])
 // written by other SMs) and are issued kBatch at a time per thread, so one
 // memory latency covers up to kBatch * nthreads chunks (x is usually cold in
 // L2 in a decode step: the weights stream through it).
+template <int kBatch>
 __device__ __forceinline__ void stage_x(uint8_t *xs, uint32_t xrow, const uint16_t *x, int M, int K, int tid,
                                         int nthreads)
 {
-    constexpr int kBatch = 8;
     const int words = K >> 3, total = M * words;
     for (int i0 = tid; i0 < total; i0 += kBatch * nthreads) {
         uint4 v[kBatch];

@@ -60,6 +60,7 @@
 #include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
+#include "zq4_segment.cuh"
 
 namespace zq4 {
 
@@ -71,10 +72,7 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 4;
 constexpr int kPrefetch = 8;
-constexpr int kSegCols = 256;
-constexpr int kCodeBytes = 16 * 128;
-constexpr int kSegBytes = kCodeBytes + 16 * 8 * 2;   // codes + scales of one segment
-constexpr int kTokCols = 8;                       // MMA columns = tokens (M <= 8)
+using namespace segk;   // segment layout, inner loop, split-tile sums
 
 struct Header {
     unsigned epoch;     // launches completed
@@ -98,7 +96,6 @@ struct Params {
     int n_jobs, M, max_k;
 };
 
-__host__ __device__ inline size_t xs_row_bytes(int K) { return size_t(K) * 2 + 64; }
 constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
 constexpr size_t kMiscOff = kBarOff + size_t(kWarps) * kSlots * 8;
@@ -107,101 +104,11 @@ constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   
 constexpr size_t kXsOff = kTabOff + 2 * 4 * (kWarps + 1 + 15) / 16 * 16;
 __host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + size_t(M) * xs_row_bytes(max_k); }
 
-// Part i of n of the range [lo, hi): [b, e), sizes equal to within one.
-// (32-bit arithmetic: (hi - lo) * n stays far below 2^31 for every shape a
-// plan accepts.)
-__device__ __forceinline__ void split(int lo, int hi, int i, int n, int &b, int &e)
-{
-    const unsigned len = unsigned(hi - lo);
-    b = lo + int(len * unsigned(i) / unsigned(n));
-    e = lo + int(len * unsigned(i + 1) / unsigned(n));
-}
-
-__device__ __forceinline__ int part_begin(int lo, int hi, int i, int n)
-{
-    return lo + int(unsigned(hi - lo) * unsigned(i) / unsigned(n));
-}
-
-// The part of [lo, hi) split n ways that holds u (lo <= u < hi): the largest
-// i with part_begin(i) <= u, i.e. i*len < (u - lo + 1)*n. That part is
-// never empty.
-__device__ __forceinline__ int owner(int lo, int hi, int n, int u)
-{
-    const unsigned len = unsigned(hi - lo);
-    const int i = int((unsigned(u - lo + 1) * unsigned(n) - 1u) / len);
-    return i < n - 1 ? i : n - 1;
-}
-
-// Nonempty parts holding the segments [a, b) of [lo, hi) split n ways: with
-// len >= n no part is empty; with len < n every nonempty part holds exactly
-// one segment.
-__device__ __forceinline__ int contributors(int lo, int hi, int n, int a, int b)
-{
-    if (hi - lo >= n) return owner(lo, hi, n, b - 1) - owner(lo, hi, n, a) + 1;
-    return b - a;
-}
-
-__device__ __forceinline__ uint4 ldg_cg_v4(const void *p)
-{
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ float ldg_cg_f32(const float *p)
-{
-    float r;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {
     unsigned r;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
     return r;
-}
-
-// Tiles of the finished job that were split between warps: every thread of
-// the CTA takes (tile, output) items and sums the parked parts of the
-// contributing warps in warp order (bit-reproducible), then writes the
-// output. `wtab` holds the job's warp range starts (segments, kWarps + 1
-// entries) and each warp's first tile; a warp parked its part of its first
-// tile in slot 0 and of its last in slot 1.
-__device__ __forceinline__ void finalize_split(int tb, int te, int S, int gate_up, int M, int N, int y_stride,
-                                               uint16_t *y, const float *wpark, const int *wtab)
-{
-    const int *wb = wtab, *wft = wtab + kWarps + 1;
-    const int per_tok = gate_up ? 8 : 16;                // outputs of a tile per token
-    const int items = (te - tb) * per_tok * M;
-    for (int it = threadIdx.x; it < items; it += kThreads) {
-        const int tt = tb + it / (per_tok * M);
-        const int o = it - (tt - tb) * (per_tok * M);
-        const int lo = tt * S, hi = lo + S;
-        unsigned mask = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-            if (wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo) mask |= 1u << w;
-        if (__popc(mask) < 2) continue;                  // one warp held the whole tile
-        const int m = o / per_tok, i = o - m * per_tok;
-        const int ra = gate_up ? 2 * i : i;
-        float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            if (!((mask >> w) & 1)) continue;
-            const float *qk = wpark + ((w * 2 + (tt == wft[w] ? 0 : 1)) * 16) * kTokCols;
-            v0 += qk[ra * kTokCols + m];
-            if (gate_up) v1 += qk[(ra + 1) * kTokCols + m];
-        }
-        const int row0 = tt * 16;
-        if (!gate_up) {
-            if (row0 + i < N) y[size_t(m) * y_stride + row0 + i] = float_to_f16_bits(v0);
-        } else if (row0 + 2 * i + 1 < N) {
-            y[size_t(m) * y_stride + (row0 >> 1) + i] = float_to_f16_bits(silu_f32(v0) * v1);
-        }
-    }
 }
 
 // Position in one warp's sequence of (job, segment) pairs.
@@ -278,10 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         for (int q = 0; q < kPrefetch && pf.j < n; ++q, next(pf)) prefetch(pf);
     }
 
-    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lch = lane >> 4;
     uint32_t ldm_off[4];
-#pragma unroll
-    for (int gp = 0; gp < 4; ++gp) ldm_off[gp] = uint32_t(lrow * 128 + (((2 * gp + lch) ^ (lrow & 7)) << 4));
+    ldm_offsets(lane, ldm_off);
     const uint8_t *xr = xs + size_t(min(r, p.M - 1)) * xrow + 16 * t;
 
     bool ok = true;
@@ -295,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 const Job &pj = p.jobs[j - 1];
                 int ptb, pte;
                 split(0, pj.T, cta, G, ptb, pte);
-                finalize_split(ptb, pte, pj.S, pj.gate_up, p.M, pj.N, pj.y_stride, pj.y, wpark, wtab);
+                finalize_split<kWarps, kThreads>(ptb, pte, pj.S, pj.gate_up, p.M, pj.N, pj.y_stride, pj.y, wpark, wtab);
             }
             __syncthreads();
             if (threadIdx.x == 0 && !*s_abort) {
@@ -328,17 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 wtab[threadIdx.x] = b;
                 wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
             }
-            const int words = jb.K >> 3, total = p.M * words;
-            for (int i = threadIdx.x; i < total; i += kThreads) {
-                const int m = i / words, cw = i - m * words;
-                const uint4 v = ldg_cg_v4(jb.x + size_t(m) * jb.K + size_t(cw) * 8);
-                uint4 o;
-                o.x = __byte_perm(v.x, v.z, 0x5410);
-                o.y = __byte_perm(v.x, v.z, 0x7632);
-                o.z = __byte_perm(v.y, v.w, 0x5410);
-                o.w = __byte_perm(v.y, v.w, 0x7632);
-                *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
-            }
+            stage_x<2>(xs, xrow, jb.x, p.M, jb.K, threadIdx.x, kThreads);
         }
         __syncthreads();
 
@@ -352,46 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         int cur_tile = -1;
 
         auto flush = [&](int tt) {
-            const bool whole = tt * S >= ub && (tt + 1) * S <= ue;
-            const int row0 = tt * 16;
-            if (whole) {
-                if (!gate_up) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int nn = row0 + r + 8 * h;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int m = 2 * t + c;
-                            if (nn < jb.N && m < p.M)
-                                jb.y[size_t(m) * jb.y_stride + nn] = float_to_f16_bits(acc[2 * h + c]);
-                        }
-                    }
-                } else {
-                    float up[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) up[i] = __shfl_down_sync(0xffffffffu, acc[i], 4);
-                    if ((r & 1) == 0) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int nn = row0 + r + 8 * h;
-#pragma unroll
-                            for (int c = 0; c < 2; ++c) {
-                                const int m = 2 * t + c;
-                                if (nn + 1 < jb.N && m < p.M)
-                                    jb.y[size_t(m) * jb.y_stride + (nn >> 1)] =
-                                        float_to_f16_bits(silu_f32(acc[2 * h + c]) * up[2 * h + c]);
-                            }
-                        }
-                    }
-                }
-            } else {
-                // part of a tile shared with other warps: park it (summed at job end)
-                float *pk = wpark + ((warp * 2 + (tt == first_tile ? 0 : 1)) * 16) * kTokCols;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) pk[(r + 8 * h) * kTokCols + 2 * t + c] = acc[2 * h + c];
-            }
+            if (tt * S >= ub && (tt + 1) * S <= ue)
+                write_tile(acc, tt * 16, lane, gate_up, p.M, jb.N, jb.y_stride, jb.y);
+            else        // part of a tile shared with other warps: summed at job end
+                park(acc, wpark, warp, tt == first_tile ? 0 : 1, lane);
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = 0.f;
         };
@@ -407,35 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 if (cur_tile >= 0) flush(cur_tile);
                 cur_tile = tt;
             }
-            const uint32_t cb = ring0 + slot * kSegBytes;
-            const uint4 sr = lds_v4(cb + kCodeBytes + r * 16);
-            const uint4 sr8 = lds_v4(cb + kCodeBytes + (r + 8) * 16);
-            const uint32_t srw[4] = {sr.x, sr.y, sr.z, sr.w}, sr8w[4] = {sr8.x, sr8.y, sr8.z, sr8.w};
-            const uint8_t *xg = xr + seg * 32 * 16;
-#pragma unroll
-            for (int gp = 0; gp < 4; ++gp) {
-                const uint4 w = ldmatrix_x4(cb + ldm_off[gp]);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int g = 2 * gp + h;
-                    uint32_t pa[4], pb[4];
-                    unpack_word_f16x2(h == 0 ? w.x : w.z, pa);
-                    unpack_word_f16x2(h == 0 ? w.y : w.w, pb);
-                    const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
-                    const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
-                    const float s_r = f16_bits_to_float(uint16_t(h == 0 ? srw[gp] : srw[gp] >> 16));
-                    const float s_r8 = f16_bits_to_float(uint16_t(h == 0 ? sr8w[gp] : sr8w[gp] >> 16));
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xg + g * 64);
-                    const float z[4] = {0.f, 0.f, 0.f, 0.f};
-                    float d[4];
-                    mma16816(d, a0, xv.x, xv.y, z);
-                    mma16816(d, a1, xv.z, xv.w, d);
-                    acc[0] = fmaf(s_r, d[0], acc[0]);
-                    acc[1] = fmaf(s_r, d[1], acc[1]);
-                    acc[2] = fmaf(s_r8, d[2], acc[2]);
-                    acc[3] = fmaf(s_r8, d[3], acc[3]);
-                }
-            }
+            accumulate(ring0 + slot * kSegBytes, ldm_off, xr + seg * 32 * 16, r, acc);
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (lane == 0 && iss.j < n) {
@@ -469,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         const Job &lj = p.jobs[n - 1];
         int ltb, lte;
         split(0, lj.T, cta, G, ltb, lte);
-        finalize_split(ltb, lte, lj.S, lj.gate_up, p.M, lj.N, lj.y_stride, lj.y, wpark, wtab);
+        st::finalize_split<st::kWarps, st::kThreads>(ltb, lte, lj.S, lj.gate_up, p.M, lj.N, lj.y_stride, lj.y, wpark, wtab);
     }
     // let every copy this warp issued land before the CTA exits
     {
