@@ -146,7 +146,34 @@ struct PrefillArgs {
     int y_stride;       // elements between output rows
     int gate_up;        // 1: rows interleaved gate/up, output silu(g)*u
     int vec_ok;         // 1: y and y_stride allow 16-byte stores
+    int ksplit;         // CTAs (one cluster) sharing an output tile, each a K range
+    int kpart;          // K steps per part (a multiple of 4)
 };
+
+// One thread-block-cluster barrier: every thread of every CTA of the cluster
+// arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, int rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Receive slot of a split-K part: [owned chunk][sender][128 rows][32 floats],
+// float4 j of row r stored at r*128 + 16*(j ^ (r & 7)) (bank-conflict-free).
+constexpr int kRecvSlotBytes = 128 * 32 * 4;
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
@@ -258,9 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
     const uint32_t accum_bar = b_empty0 + 8 * kBSlots;    // all MMAs done -> epilogue
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOff + 8 * C::kNumBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x % a.m_tiles, n_tile = blockIdx.x / a.m_tiles;
+    const int KS = a.ksplit, rank = int(blockIdx.x) % KS, tile = int(blockIdx.x) / KS;
+    const int m_tile = tile % a.m_tiles, n_tile = tile / a.m_tiles;
     const int m0 = m_tile * kBM * MB, n0 = n_tile * kBN;
     const int ksteps = (a.K + kBK - 1) / kBK;
+    const int k_lo = rank * a.kpart, nk = min(ksteps, k_lo + a.kpart) - k_lo;   // this CTA's K steps
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRaw; ++s) {
@@ -286,14 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    bool acc_ready = false;                  // dequant/epilogue warps: the accumulator is complete
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         int issued = 0;
         if (lane == 0) {
-            for (int ks = 0; ks < ksteps; ++ks, ++issued) {
-                const int s = ks % kRaw;
-                if (!mbar_wait(raw_empty0 + 8 * s, ((ks / kRaw) & 1) ^ 1)) {
+            for (int i = 0; i < nk; ++i, ++issued) {
+                const int s = i % kRaw, ks = k_lo + i;
+                if (!mbar_wait(raw_empty0 + 8 * s, ((i / kRaw) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -301,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
                 mbar_arrive_expect_tx(raw_full0 + 8 * s, MB * kABytes + kWBytes);
                 tma_load_2d(st + MB * kABytes, &tm_w, ks * (kBK / 8), n0, raw_full0 + 8 * s);
                 // the weights are constant; x may be the previous kernel's output
-                if (ks < kRaw) griddep_wait();
+                if (i < kRaw) griddep_wait();
                 tma_load_2d(st, &tm_x, ks * kBK, m0, raw_full0 + 8 * s);
             }
             if (!ok) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
@@ -316,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const int s = ks % kRaw, b = ks % kBSlots;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % kRaw, b = i % kBSlots;
                 // the B slot is filled only after its raw stage landed, so this
                 // one wait covers both operands
-                if (!mbar_wait(b_full0 + 8 * b, (ks / kBSlots) & 1)) {
+                if (!mbar_wait(b_full0 + 8 * b, (i / kBSlots) & 1)) {
                     ok = false;
                     break;
                 }
@@ -334,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb)
                         umma_f16(tmem + uint32_t(mb * kBN), smem_desc_sw128(at + mb * kABytes + kk * 32), bd,
-                                 (ks | kk) != 0);
+                                 (i | kk) != 0);
                 }
                 umma_commit(raw_empty0 + 8 * s);     // raw slot free once these MMAs are done
                 umma_commit(b_empty0 + 8 * b);       // and the B slot
@@ -357,19 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
         const int sw = nl & 7;
         griddep_wait();
         griddep_launch_dependents();
-        uint4 sc_next = load_scales8(srow, 0, G, row_ok, vec);
-        for (int kq = 0; kq < ksteps && ok; kq += 4) {
-            const uint4 sc_cur = sc_next;           // groups 2kq .. 2kq+7
-            sc_next = load_scales8(srow, 2 * kq + 8, G, row_ok, vec);
+        // (k_lo is a multiple of 4 steps, so groups 2*(k_lo + kq) .. +7 are
+        // one aligned 16-byte load)
+        uint4 sc_next = load_scales8(srow, 2 * k_lo, G, row_ok, vec);
+        for (int kq = 0; kq < nk && ok; kq += 4) {
+            const uint4 sc_cur = sc_next;           // groups 2(k_lo+kq) .. +7
+            sc_next = load_scales8(srow, 2 * (k_lo + kq) + 8, G, row_ok, vec);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int ks = kq + u;
-                if (ks >= ksteps) break;
-                const int s = ks % kRaw, b = ks % kBSlots;
+                const int i = kq + u;
+                if (i >= nk) break;
+                const int s = i % kRaw, b = i % kBSlots;
                 const uint32_t sp = pick_u32(sc_cur, u);           // (group 2ks, group 2ks+1)
                 const uint32_t sg0 = __byte_perm(sp, 0, 0x1010), sg1 = __byte_perm(sp, 0, 0x3232);
-                const bool got = mbar_wait(raw_full0 + 8 * s, (ks / kRaw) & 1) &&
-                                 mbar_wait(b_empty0 + 8 * b, ((ks / kBSlots) & 1) ^ 1);
+                const bool got = mbar_wait(raw_full0 + 8 * s, (i / kRaw) & 1) &&
+                                 mbar_wait(b_empty0 + 8 * b, ((i / kBSlots) & 1) ^ 1);
                 if (!got) {
                     ok = false;
                     break;
@@ -388,26 +420,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_prefill(const __grid_constant__
         }
         if (!ok && lane == 0) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
 
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its 32 tokens of
-        // each 128-token block) and the column half (w-2)/4 of the tile
         // (tcgen05.ld is warp-collective: the decision to read must be warp-uniform)
         const bool acc_got = mbar_wait(accum_bar, 0);
-        const bool acc_ready = __all_sync(0xffffffffu, acc_got && ok);
+        acc_ready = __all_sync(0xffffffffu, acc_got && ok);
         if (!acc_ready && lane == 0) atomicOr(&g_prefill_error, ZQ4_DEVERR_WAIT_TIMEOUT);
         tc_fence_after();
-        const int q = warp & 3;
-        const int cbase = ((warp - 2) >> 2) * (kBN / 2);
-        if (acc_ready) {
+    }
+
+    // ---- epilogue: warp w (2..9) reads TMEM lanes 32*(w%4) .. +31 (its 32
+    // tokens of each 128-token block) and the column half (w-2)/4, in 32-column
+    // chunks. With a K split, chunk c's owner is CTA c % KS of the cluster:
+    // the others send their parts into the owner's shared memory (free once
+    // every CTA of the cluster has passed the first cluster barrier), and the
+    // owner sums the parts in rank order after the second.
+    const bool epi = warp >= 2;
+    const int q = warp & 3;
+    const int cbase = ((warp - 2) >> 2) * (kBN / 2);
+    const int row = 32 * q + lane;                           // TMEM lane = token row in the block
+    auto slot_addr = [&](int cid, int sender, int owner) {   // in the owner's shared memory
+        const int compact = sender < owner ? sender : sender - 1;
+        return sbase + uint32_t(((cid / KS) * (KS - 1) + compact) * kRecvSlotBytes + row * 128);
+    };
+    if (KS > 1) {
+        cluster_sync();                                      // every ring of the cluster is idle
+        if (epi && acc_ready) {
 #pragma unroll 1
-            for (int mb = 0; mb < MB; ++mb) {
-                const int m = m0 + mb * kBM + 32 * q + lane;
+            for (int mb = 0; mb < MB; ++mb)
 #pragma unroll 1
                 for (int c0 = cbase; c0 < cbase + kBN / 2; c0 += 32) {
+                    const int cid = mb * (kBN / 32) + c0 / 32, owner = cid % KS;
+                    if (owner == rank) continue;
                     float v[32];
                     tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(mb * kBN + c0), v);
-                    if (m >= a.M || n0 + c0 >= a.N) continue;
-                    store_outputs(a, v, m, n0 + c0);
+                    const uint32_t dst = cluster_addr(slot_addr(cid, rank, owner), owner);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_cluster_v4(dst + uint32_t((j ^ (row & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                      v[4 * j + 3]);
                 }
+        }
+        cluster_sync();                                      // every part has landed
+    }
+    if (epi && acc_ready) {
+#pragma unroll 1
+        for (int mb = 0; mb < MB; ++mb) {
+            const int m = m0 + mb * kBM + row;
+#pragma unroll 1
+            for (int c0 = cbase; c0 < cbase + kBN / 2; c0 += 32) {
+                const int cid = mb * (kBN / 32) + c0 / 32;
+                if (cid % KS != rank) continue;
+                float v[32];
+                tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(mb * kBN + c0), v);
+                if (KS > 1) {
+                    float tot[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) tot[e] = 0.f;
+                    for (int sdr = 0; sdr < KS; ++sdr) {             // rank order
+                        if (sdr == rank) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) tot[e] += v[e];
+                        } else {
+                            const uint32_t src = slot_addr(cid, sdr, rank);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint4 w = lds_v4(src + uint32_t((j ^ (row & 7)) << 4));
+                                tot[4 * j] += __uint_as_float(w.x);
+                                tot[4 * j + 1] += __uint_as_float(w.y);
+                                tot[4 * j + 2] += __uint_as_float(w.z);
+                                tot[4 * j + 3] += __uint_as_float(w.w);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = tot[e];
+                }
+                if (m >= a.M || n0 + c0 >= a.N) continue;
+                store_outputs(a, v, m, n0 + c0);
             }
         }
     }
@@ -438,6 +526,9 @@ cudaError_t read_prefill_error(unsigned *flags, bool clear)
 #ifndef ZQ4_PF_FORCE_MB
 #define ZQ4_PF_FORCE_MB 0          // 0: choose per shape; 1 or 2: always that many 128-token blocks
 #endif
+#ifndef ZQ4_PF_FORCE_KS
+#define ZQ4_PF_FORCE_KS 0          // 0: choose per shape; 1 or 2: always split K that many ways
+#endif
 
 template <int MB>
 static cudaError_t launch_mb(const CUtensorMap &tmx, const CUtensorMap &tmw, const pf::PrefillArgs &a, int n_tiles,
@@ -447,8 +538,60 @@ static cudaError_t launch_mb(const CUtensorMap &tmx, const CUtensorMap &tmw, con
     auto kern = pf::k_prefill<MB>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), pf::Cfg<MB>::kSmem, smem_set);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(a.m_tiles * n_tiles), dim3(pf::kThreads), size_t(pf::Cfg<MB>::kSmem), s, tmx,
-                      tmw, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.m_tiles * n_tiles * a.ksplit));
+    cfg.blockDim = dim3(pf::kThreads);
+    cfg.dynamicSmemBytes = size_t(pf::Cfg<MB>::kSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;       // the CTAs sharing a tile, adjacent in x
+    attr[1].val.clusterDim.x = unsigned(a.ksplit);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.ksplit > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmx, tmw, a);
+}
+
+// Tile height (MB x 128 tokens) and K split (1 or 2 CTAs of a cluster per
+// tile) for a shape, from a cost model fitted to measurements on GB300: a CTA
+// costs a fixed ~8 us (TMEM set-up, first-copy latency, epilogue) plus its
+// share of the tile's work (35 us for a 256-token tile at K = 3072, 23.3 us
+// for a 128-token one: the taller tile halves the dequantization per flop)
+// plus ~3 us per 128 tokens for the split's reduction through distributed
+// shared memory; a launch costs its number of waves of CTAs times that.
+// Splits over 3 or 4 CTAs measured slower (more reduction traffic, and
+// 3-CTA clusters leave SMs idle in the GPCs). Every part keeps at least 8 K
+// steps and starts on a multiple of 4.
+static void choose_tiling(int M, int N, int K, int sms, int *mb_out, int *ks_out, int *kpart_out)
+{
+    const int n_tiles = (N + pf::kBN - 1) / pf::kBN, ksteps = (K + pf::kBK - 1) / pf::kBK;
+    double best = 1e30;
+    int bmb = 1, bks = 1;
+    for (int mb = 2; mb >= 1; --mb) {
+        if (ZQ4_PF_FORCE_MB && mb != ZQ4_PF_FORCE_MB) continue;
+        const long tiles = long((M + 128 * mb - 1) / (128 * mb)) * n_tiles;
+        const double work = (mb == 2 ? 35.0 : 23.3) * double(K) / 3072.0;
+        for (int ks = 1; ks <= 2; ++ks) {
+            if (ks > 1 && ksteps / ks < 8) break;
+            if (ZQ4_PF_FORCE_KS && ks != ZQ4_PF_FORCE_KS) continue;
+            const long waves = (tiles * ks + sms - 1) / sms;
+            const double cost = double(waves) * (8.0 + work / ks + 3.0 * mb * (ks - 1));
+            if (cost < best - 1e-9) {
+                best = cost;
+                bmb = mb;
+                bks = ks;
+            }
+        }
+    }
+    int kpart = (ksteps + bks - 1) / bks;
+    kpart = (kpart + 3) / 4 * 4;
+    while (bks > 1 && (bks - 1) * kpart >= ksteps) --bks;    // no empty part
+    *mb_out = bmb;
+    *ks_out = bks;
+    *kpart_out = bks > 1 ? kpart : ksteps;
 }
 
 cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
@@ -457,16 +600,8 @@ cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uin
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const int n_tiles = (N + pf::kBN - 1) / pf::kBN;
-    // 256-token tiles halve the dequantization per FLOP; take them when they
-    // still fill the SMs as well as 128-token tiles do
-    int MB = ZQ4_PF_FORCE_MB;
-    if (MB == 0) {
-        const long sms = sm_count();
-        const long t1 = long((M + 127) / 128) * n_tiles, t2 = long((M + 255) / 256) * n_tiles;
-        const long waves1 = (t1 + sms - 1) / sms, waves2 = (t2 + sms - 1) / sms;
-        // a 256-token tile costs about 4/3 of a 128-token one (measured)
-        MB = 4 * waves2 <= 3 * waves1 ? 2 : 1;
-    }
+    int MB, KS, kpart;
+    choose_tiling(M, N, K, sm_count(), &MB, &KS, &kpart);
     CUtensorMap tmx, tmw;
     const cuuint32_t estr[2] = {1, 1};
     {
@@ -497,6 +632,8 @@ cudaError_t launch_prefill(const uint32_t *wq, const uint16_t *scales, const uin
     a.gate_up = gate_up ? 1 : 0;
     a.y_stride = gate_up ? N / 2 : N;
     a.vec_ok = (reinterpret_cast<uintptr_t>(y) & 15) == 0 && a.y_stride % 8 == 0;
+    a.ksplit = KS;
+    a.kpart = kpart;
     return MB == 2 ? launch_mb<2>(tmx, tmw, a, n_tiles, s) : launch_mb<1>(tmx, tmw, a, n_tiles, s);
 }
 

@@ -61,6 +61,7 @@ def _check(oracle, y, wq, sc, x, N, K, what, rows=None):
 SHAPES = [
     (64, 256, 256), (65, 300, 544), (64, 1, 32), (127, 17, 96), (128, 512, 1024),
     (129, 257, 64), (200, 520, 3072), (300, 260, 2560), (256, 768, 8192), (1024, 384, 3072),
+    (512, 3072, 3072),   # K split over a cluster, 128-token tiles
 ]
 
 
@@ -182,3 +183,16 @@ def test_prefill_full_size_all_outputs(zq4, M, N, K):
 
 def test_prefill_no_device_errors_recorded(zq4):
     assert zq4.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 520, 3072), (1024, 3072, 8192)])
+def test_prefill_split_k_is_reproducible(zq4, M, N, K):
+    """Shapes the library may split over K across a cluster: the parts are
+    summed in a fixed order, so repeated calls agree bit for bit."""
+    wq, sc, x = _case("pf_repro", M, N, K)
+    W, Sd, X = dev(wq), dev(sc), dev(x)
+    a = host_f16(zq4.gemv(W, Sd, X, N, K))
+    b = host_f16(zq4.gemv(W, Sd, X, N, K))
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert zq4.device_errors(clear=True) == 0
+
