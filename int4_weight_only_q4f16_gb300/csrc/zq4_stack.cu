@@ -25,7 +25,7 @@
 //    ZQ4_PREP_SEGMENTED): each segment is 2304 contiguous bytes (swizzled
 //    codes, then scales), so one bulk copy fills a shared-memory slot and no
 //    tensor map is involved. Each warp runs its own ring of segment slots
-//    across job boundaries, with a look-ahead of L2 prefetches. Per 32-column
+//    across job boundaries. Per 32-column
 //    group, lane (r, t) (r = lane/4, t = lane%4) takes word t of rows r and
 //    r+8 (ldmatrix.x4 fetches two groups, conflict-free on the swizzle),
 //    unpacks exact f16 (q - 7) pairs as the A fragments of two chained
@@ -40,8 +40,14 @@
 //    sum goes through global memory.
 //  * Job boundary: CTA barrier, split tiles summed, one release-add per CTA
 //    on the job's counter, acquire-poll until every CTA has arrived, CTA
-//    barrier, then x of the next job is staged into shared memory (L2 reads:
-//    it may have been written by other SMs during this kernel).
+//    barrier. x of the next job is staged into shared memory with L2 reads
+//    (it may have been written by other SMs during this kernel): after the
+//    poll, or, when no earlier job of the plan writes any byte of it (decided
+//    when the plan is made), already before the split-tile sums, so that its
+//    latency hides behind them and the poll.
+//  * The job table (as much of it as fits next to the rings) is copied to
+//    shared memory once per launch; each warp's copy iterator and tile
+//    position advance incrementally (no division per segment).
 //  * Counters grow monotonically: a launch waits for (launch index + 1) x
 //    grid arrivals, the launch index being read from the plan at start and
 //    advanced by the last CTA to finish.
@@ -71,8 +77,8 @@ namespace st {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 4;
-constexpr int kPrefetch = 8;
-using namespace segk;   // segment layout, inner loop, split-tile sums
+constexpr int kEarly = 2;   // x chunks (16 B) per thread read before the job barrier
+using namespace segk;       // segment layout, inner loop, split-tile sums
 
 struct Header {
     unsigned epoch;     // launches completed
@@ -81,12 +87,15 @@ struct Header {
     unsigned pad[29];
 };
 
+constexpr int kJobGateUp = 1;   // rows are interleaved gate/up pairs: silu(g) * u output
+constexpr int kJobXEarly = 2;   // x is not written by an earlier job: it may be read at any time
+
 struct alignas(16) Job {
     const uint8_t *seg; // the matrix in the segmented layout
     const uint16_t *x;  // [M][K]
     uint16_t *y;        // [M][y_stride]
     int N, K, T, S;
-    int gate_up, y_stride;
+    int flags, y_stride;
 };
 
 struct Params {
@@ -94,6 +103,7 @@ struct Params {
     const Job *jobs;
     unsigned *job_cnt;   // [n_jobs]
     int n_jobs, M, max_k;
+    int cached;          // jobs [0, cached) are copied to shared memory at start
 };
 
 constexpr size_t kRingOff = 0;
@@ -102,7 +112,14 @@ constexpr size_t kMiscOff = kBarOff + size_t(kWarps) * kSlots * 8;
 constexpr size_t kParkOff = kMiscOff + 128;                          // warp partials [kWarps*2][16][kTokCols]
 constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range table [2][kWarps + 1]
 constexpr size_t kXsOff = kTabOff + 2 * 4 * (kWarps + 1 + 15) / 16 * 16;
-__host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + size_t(M) * xs_row_bytes(max_k); }
+__host__ __device__ inline size_t xs_bytes(int M, int max_k) { return (size_t(M) * xs_row_bytes(max_k) + 15) / 16 * 16; }
+__host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + xs_bytes(M, max_k); }
+// jobs that fit in shared memory next to everything else (the rest are read from the plan)
+inline int cached_jobs(int n, int M, int max_k)
+{
+    const size_t left = size_t(227) * 1024 - smem_bytes(M, max_k);
+    return int(std::min<size_t>(size_t(n), left / sizeof(Job)));
+}
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {
@@ -111,10 +128,18 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     return r;
 }
 
-// Position in one warp's sequence of (job, segment) pairs.
-struct SegIt {
-    int j, u, e;
-};
+// x chunk i of M*K/8 (16 bytes of token i / (K/8)) into its staged place,
+// pair-permuted as the unpack produces: (x0,x4),(x1,x5),(x2,x6),(x3,x7)
+__device__ __forceinline__ void put_x(uint8_t *xs, uint32_t xrow, int words, int i, uint4 v)
+{
+    const int m = i / words, cw = i - m * words;
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
+}
 
 __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
 {
@@ -130,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
     uint8_t *xs = smem + kXsOff;
+    Job *sjobs = reinterpret_cast<Job *>(smem + kXsOff + xs_bytes(p.M, p.max_k));
     const uint32_t xrow = uint32_t(xs_row_bytes(p.max_k));
-    const int n = p.n_jobs;
+    const int n = p.n_jobs, M = p.M;
     const unsigned launch = *reinterpret_cast<volatile unsigned *>(&p.hdr->epoch);
     const unsigned target = (launch + 1u) * unsigned(G);
 
@@ -140,7 +166,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         for (int j = 0; j < kSlots; ++j) mbar_init(bar0 + 8 * j, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncwarp();
+    {
+        // the job table (or its first p.cached entries) into shared memory
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.jobs);
+        uint4 *dst = reinterpret_cast<uint4 *>(sjobs);
+        const int words = p.cached * int(sizeof(Job) / 16);
+        for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
+    }
+    __syncthreads();
+    auto job = [&](int j) -> const Job & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
 
     // this warp's segment range of a job: CTA part of the job, then warp part
     // (CTA ranges are whole tiles, so a tile never spans two CTAs)
@@ -149,63 +183,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         split(0, T, cta, G, tb, te);
         split(tb * S, te * S, warp, kWarps, ub, ue);
     };
-    auto seek = [&](SegIt &it, int j) {
+
+    // ---- lane 0: the copy iterator, one job ahead of nothing (it runs
+    // through the warp's (job, segment) sequence; segment u of a job, tile
+    // major, is at byte u * kSegBytes of its matrix)
+    int it_j = 0, it_u = 0, it_e = 0;
+    const uint8_t *it_seg = nullptr;
+    auto seek = [&](int j) {
         for (; j < n; ++j) {
-            const Job &jb = p.jobs[j];
+            const Job &jb = job(j);
             int ub, ue;
             warp_range(jb.T, jb.S, ub, ue);
             if (ub < ue) {
-                it.j = j;
-                it.u = ub;
-                it.e = ue;
+                it_j = j;
+                it_u = ub;
+                it_e = ue;
+                it_seg = jb.seg;
                 return;
             }
         }
-        it.j = n;
+        it_j = n;
     };
-    auto next = [&](SegIt &it) {
-        if (++it.u >= it.e) seek(it, it.j + 1);
-    };
-    // segment u of a job (tile-major) is at byte u * kSegBytes of its matrix
-    auto issue = [&](const SegIt &it, int slot) {       // lane 0
+    int issued = 0;
+    auto issue_next = [&]() {                           // lane 0
+        const int slot = issued % kSlots;
         const uint32_t bar = bar0 + 8 * slot;
         mbar_arrive_expect_tx(bar, kSegBytes);
-        bulk_load(ring0 + slot * kSegBytes, p.jobs[it.j].seg + size_t(it.u) * kSegBytes, kSegBytes, bar);
+        bulk_load(ring0 + slot * kSegBytes, it_seg + size_t(it_u) * kSegBytes, kSegBytes, bar);
+        ++issued;
+        if (++it_u >= it_e) seek(it_j + 1);
     };
-    auto prefetch = [&](const SegIt &it) {              // lane 0
-        prefetch_l2_bulk(p.jobs[it.j].seg + size_t(it.u) * kSegBytes, kSegBytes);
-    };
-
-    // ---- first copies of this warp's sequence, and the L2 look-ahead
-    SegIt iss, pf;
-    seek(iss, 0);
     if (lane == 0) {
-        for (int q = 0; q < kSlots && iss.j < n; ++q, next(iss)) issue(iss, q);
-        pf = iss;
-        for (int q = 0; q < kPrefetch && pf.j < n; ++q, next(pf)) prefetch(pf);
+        seek(0);
+        for (int q = 0; q < kSlots && it_j < n; ++q) issue_next();
     }
 
     uint32_t ldm_off[4];
     ldm_offsets(lane, ldm_off);
-    const uint8_t *xr = xs + size_t(min(r, p.M - 1)) * xrow + 16 * t;
+    const uint8_t *xr = xs + size_t(min(r, M - 1)) * xrow + 16 * t;
+
+    // stage x of a job synchronously (all threads; caller barriers)
+    auto stage_now = [&](const Job &jb, int from) {
+        const int words = jb.K >> 3, total = M * words;
+        for (int i0 = from + int(threadIdx.x); i0 < total; i0 += 2 * kThreads) {
+            uint4 v0, v1;
+            const int i1 = i0 + kThreads;
+            v0 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i0);
+            if (i1 < total) v1 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i1);
+            put_x(xs, xrow, words, i0, v0);
+            if (i1 < total) put_x(xs, xrow, words, i1, v1);
+        }
+    };
+    auto set_wtab = [&](const Job &jb) {              // threads 0..kWarps
+        if (threadIdx.x <= kWarps) {
+            int tb0, te0;
+            split(0, jb.T, cta, G, tb0, te0);
+            const int b = part_begin(tb0 * jb.S, te0 * jb.S, threadIdx.x, kWarps);
+            wtab[threadIdx.x] = b;
+            wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
+        }
+    };
 
     bool ok = true;
     int consumed = 0;
     for (int j = 0; j < n; ++j) {
-        const Job &jb = p.jobs[j];
-        // ---- wait until every CTA has finished job j-1, then stage x_j
-        if (j > 0) {
+        const Job &jb = job(j);
+        if (j == 0) {
+            set_wtab(jb);
+            stage_now(jb, 0);
             __syncthreads();
+        } else {
+            // every warp of this CTA is done with job j-1 (x buffer free,
+            // partial tiles parked)
+            __syncthreads();
+            const bool early = (jb.flags & kJobXEarly) != 0 && !*s_abort;
+            const int words = jb.K >> 3, total = M * words;
+            uint4 xv[kEarly];
+            if (early) {
+#pragma unroll
+                for (int e = 0; e < kEarly; ++e) {
+                    const int i = int(threadIdx.x) + e * kThreads;
+                    if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
+                }
+            }
+            const Job &pj = job(j - 1);
             if (!*s_abort) {
-                const Job &pj = p.jobs[j - 1];
                 int ptb, pte;
                 split(0, pj.T, cta, G, ptb, pte);
-                finalize_split<kWarps, kThreads>(ptb, pte, pj.S, pj.gate_up, p.M, pj.N, pj.y_stride, pj.y, wpark, wtab);
+                finalize_split<kWarps, kThreads>(ptb, pte, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y,
+                                                 wpark, wtab);
             }
-            __syncthreads();
+            if (early) {
+#pragma unroll
+                for (int e = 0; e < kEarly; ++e) {
+                    const int i = int(threadIdx.x) + e * kThreads;
+                    if (i < total) put_x(xs, xrow, words, i, xv[e]);
+                }
+                if (total > kEarly * kThreads) stage_now(jb, kEarly * kThreads);
+            }
+            __syncthreads();      // finalize writes (and staged x) before the release below
             if (threadIdx.x == 0 && !*s_abort) {
-                // release: this CTA's outputs of job j-1 (ordered before by
-                // the barrier) become visible with the increment
+                // release: this CTA's outputs of job j-1 become visible with the increment
                 asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
                 const unsigned long long t0 = globaltimer();
                 for (;;) {
@@ -218,64 +296,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     }
                 }
             }
+            set_wtab(jb);          // finalize of job j-1 (the table's last reader) is behind the barrier
             __syncthreads();
             if (*s_abort) {
                 ok = false;
                 break;
             }
-        }
-        {
-            // this job's warp range boundaries and each warp's first tile
-            if (threadIdx.x <= kWarps) {
-                int tb0, te0;
-                split(0, jb.T, cta, G, tb0, te0);
-                const int b = part_begin(tb0 * jb.S, te0 * jb.S, threadIdx.x, kWarps);
-                wtab[threadIdx.x] = b;
-                wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
+            if (!early) {
+                stage_now(jb, 0);
+                __syncthreads();
             }
-            stage_x<2>(xs, xrow, jb.x, p.M, jb.K, threadIdx.x, kThreads);
         }
-        __syncthreads();
 
-        const int S = jb.S, gate_up = jb.gate_up;
-        int tb, te, ub, ue;
-        split(0, jb.T, cta, G, tb, te);
-        const int cb = tb * S, ce = te * S;
-        split(cb, ce, warp, kWarps, ub, ue);
+        const int S = jb.S, gate_up = jb.flags & kJobGateUp;
+        int ub, ue;
+        warp_range(jb.T, S, ub, ue);
         const int first_tile = ub / S;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int cur_tile = -1;
-
         auto flush = [&](int tt) {
             if (tt * S >= ub && (tt + 1) * S <= ue)
-                write_tile(acc, tt * 16, lane, gate_up, p.M, jb.N, jb.y_stride, jb.y);
+                write_tile(acc, tt * 16, lane, gate_up, M, jb.N, jb.y_stride, jb.y);
             else        // part of a tile shared with other warps: summed at job end
                 park(acc, wpark, warp, tt == first_tile ? 0 : 1, lane);
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = 0.f;
         };
 
+        int tt = first_tile, sg = ub - first_tile * S;
         for (int u = ub; u < ue; ++u, ++consumed) {
             const int slot = consumed % kSlots;
             if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, (consumed / kSlots) & 1))) {
                 ok = false;
                 break;
             }
-            const int tt = u / S, seg = u - tt * S;
             if (tt != cur_tile) {
                 if (cur_tile >= 0) flush(cur_tile);
                 cur_tile = tt;
             }
-            accumulate(ring0 + slot * kSegBytes, ldm_off, xr + seg * 32 * 16, r, acc);
+            accumulate(ring0 + slot * kSegBytes, ldm_off, xr + sg * 32 * 16, r, acc);
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (lane == 0 && iss.j < n) {
-                issue(iss, slot);
-                next(iss);
-                if (pf.j < n) {
-                    prefetch(pf);
-                    next(pf);
-                }
+            if (lane == 0 && it_j < n) issue_next();
+            if (++sg == S) {
+                sg = 0;
+                ++tt;
             }
         }
         if (!ok) {
@@ -297,23 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     __syncthreads();
     if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
     if (!*s_abort && n > 0) {                            // the last job's split tiles
-        const Job &lj = p.jobs[n - 1];
+        const Job &lj = job(n - 1);
         int ltb, lte;
         split(0, lj.T, cta, G, ltb, lte);
-        st::finalize_split<st::kWarps, st::kThreads>(ltb, lte, lj.S, lj.gate_up, p.M, lj.N, lj.y_stride, lj.y, wpark, wtab);
+        finalize_split<kWarps, kThreads>(ltb, lte, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark,
+                                         wtab);
     }
     // let every copy this warp issued land before the CTA exits
     {
-        int outstanding = 0;
-        if (lane == 0) {
-            // copies issued = min(kSlots, total) initially + one per consumed segment while any remained
-            SegIt probe;
-            seek(probe, 0);
-            int total = 0;
-            for (; probe.j < n; next(probe)) ++total;
-            outstanding = std::min(total, consumed + kSlots) - consumed;
-        }
-        outstanding = __shfl_sync(0xffffffffu, outstanding, 0);
+        const int outstanding = __shfl_sync(0xffffffffu, issued, 0) - consumed;
         for (int c = consumed; c < consumed + outstanding; ++c)
             if (!mbar_wait(bar0 + 8 * (c % kSlots), (c / kSlots) & 1)) break;
     }
@@ -377,6 +434,40 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
     return ZQ4_OK;
 }
 
+// Device entry of job j. kJobXEarly: no earlier job's output overlaps x_j,
+// so the kernel may read x_j before the previous job has finished.
+st::Job make_job(const zq4_stack_job *jobs, int j, int M)
+{
+    const zq4_stack_job &b = jobs[j];
+    st::Job jb;
+    memset(&jb, 0, sizeof(jb));
+    jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
+    jb.x = b.x;
+    jb.y = b.y;
+    jb.N = b.N;
+    jb.K = b.K;
+    jb.T = (b.N + 15) / 16;
+    jb.S = b.K / st::kSegCols;
+    jb.y_stride = b.gate_up ? b.N / 2 : b.N;
+    jb.flags = b.gate_up ? st::kJobGateUp : 0;
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(b.x), x1 = x0 + size_t(M) * size_t(b.K) * 2;
+    bool early = true;
+    for (int k = 0; k < j && early; ++k) {
+        const zq4_stack_job &q = jobs[k];
+        const size_t ys = q.gate_up ? size_t(q.N / 2) : size_t(q.N);
+        const uintptr_t y0 = reinterpret_cast<uintptr_t>(q.y), y1 = y0 + size_t(M) * ys * 2;
+        if (y0 < x1 && x0 < y1) early = false;
+    }
+    if (early) jb.flags |= st::kJobXEarly;
+    return jb;
+}
+
+// Dynamic shared memory of a launch: the fixed part plus the cached jobs.
+size_t launch_smem(int n_jobs, int M, int max_k)
+{
+    return st::smem_bytes(M, max_k) + size_t(st::cached_jobs(n_jobs, M, max_k)) * sizeof(st::Job);
+}
+
 }  // namespace
 
 zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes)
@@ -401,7 +492,7 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     const Layout l = layout_for(n_jobs);
     if (bytes < l.total) return ZQ4_ERR_SHAPE;
     // the kernel needs every CTA resident at once
-    const size_t smem = st::smem_bytes(M, mk);
+    const size_t smem = launch_smem(n_jobs, M, mk);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
     if (e != cudaSuccess) return cuda_status(e);
     int per_sm = 0;
@@ -412,18 +503,7 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     std::vector<uint8_t> host(l.total, 0);
     uint8_t *hjobs = host.data() + l.jobs;
     for (int j = 0; j < n_jobs; ++j) {
-        const zq4_stack_job &b = jobs[j];
-        st::Job jb;
-        memset(&jb, 0, sizeof(jb));
-        jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
-        jb.x = b.x;
-        jb.y = b.y;
-        jb.N = b.N;
-        jb.K = b.K;
-        jb.T = (b.N + 15) / 16;
-        jb.S = b.K / st::kSegCols;
-        jb.gate_up = b.gate_up ? 1 : 0;
-        jb.y_stride = b.gate_up ? b.N / 2 : b.N;
+        const st::Job jb = make_job(jobs, j, M);
         memcpy(hjobs + size_t(j) * sizeof(st::Job), &jb, sizeof(jb));
     }
     e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
@@ -452,9 +532,11 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.n_jobs = plan->n_jobs;
     p.M = plan->M;
     p.max_k = plan->max_k;
+    p.cached = st::cached_jobs(p.n_jobs, p.M, p.max_k);
     void *args[] = {&p};
     return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),
-                                                   dim3(st::kThreads), args, st::smem_bytes(p.M, p.max_k), s));
+                                                   dim3(st::kThreads), args,
+                                                   launch_smem(p.n_jobs, p.M, p.max_k), s));
 }
 
 // ---------------------------------------------------------------------------
@@ -499,7 +581,7 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     if (stt != ZQ4_OK) return stt;
     const Layout l = layout_for(n_jobs);
     if (l.total > kStaticPlanBytes) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
-    const size_t smem = st::smem_bytes(M, mk);
+    const size_t smem = launch_smem(n_jobs, M, mk);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
     if (e != cudaSuccess) return cuda_status(e);
     int per_sm = 0;
@@ -513,18 +595,7 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     // header and counters start at zero; the job table is written after
     e = cudaMemsetAsync(base, 0, l.total, s);
     for (int j = 0; j < n_jobs && e == cudaSuccess; ++j) {
-        const zq4_stack_job &b = jobs[j];
-        st::Job jb;
-        memset(&jb, 0, sizeof(jb));
-        jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
-        jb.x = b.x;
-        jb.y = b.y;
-        jb.N = b.N;
-        jb.K = b.K;
-        jb.T = (b.N + 15) / 16;
-        jb.S = b.K / st::kSegCols;
-        jb.gate_up = b.gate_up ? 1 : 0;
-        jb.y_stride = b.gate_up ? b.N / 2 : b.N;
+        const st::Job jb = make_job(jobs, j, M);
         // from pageable memory: the entry is staged before the call returns
         e = cudaMemcpyAsync(base + l.jobs + size_t(j) * sizeof(st::Job), &jb, sizeof(jb), cudaMemcpyHostToDevice, s);
     }
