@@ -273,15 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 finalize_split<kWarps, kThreads>(ptb, pte, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y,
                                                  wpark, wtab);
             }
-            if (early) {
-#pragma unroll
-                for (int e = 0; e < kEarly; ++e) {
-                    const int i = int(threadIdx.x) + e * kThreads;
-                    if (i < total) put_x(xs, xrow, words, i, xv[e]);
-                }
-                if (total > kEarly * kThreads) stage_now(jb, kEarly * kThreads);
-            }
-            __syncthreads();      // finalize writes (and staged x) before the release below
+            __syncthreads();      // finalize writes before the release below
             if (threadIdx.x == 0 && !*s_abort) {
                 // release: this CTA's outputs of job j-1 become visible with the increment
                 asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
@@ -297,6 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 }
             }
             set_wtab(jb);          // finalize of job j-1 (the table's last reader) is behind the barrier
+            if (early) {
+                // the loads were issued before the sums and the poll: stored only now,
+                // so that their latency hides behind both
+#pragma unroll
+                for (int e = 0; e < kEarly; ++e) {
+                    const int i = int(threadIdx.x) + e * kThreads;
+                    if (i < total) put_x(xs, xrow, words, i, xv[e]);
+                }
+                if (total > kEarly * kThreads) stage_now(jb, kEarly * kThreads);
+            }
             __syncthreads();
             if (*s_abort) {
                 ok = false;
@@ -309,9 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         }
 
         const int S = jb.S, gate_up = jb.flags & kJobGateUp;
-        int ub, ue;
-        warp_range(jb.T, S, ub, ue);
-        const int first_tile = ub / S;
+        const int ub = wtab[warp], ue = wtab[warp + 1], first_tile = wtab[kWarps + 1 + warp];
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int cur_tile = -1;
         auto flush = [&](int tt) {
@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 cur_tile = tt;
             }
             accumulate(ring0 + slot * kSegBytes, ldm_off, xr + sg * 32 * 16, r, acc);
+            // every lane's reads of the slot (their values are in registers)
+            // are done before lane 0 lets the copy engine overwrite it
             __syncwarp();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (lane == 0 && it_j < n) issue_next();
             if (++sg == S) {
                 sg = 0;
