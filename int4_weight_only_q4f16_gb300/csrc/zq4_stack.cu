@@ -19,7 +19,7 @@
 //
 // How:
 //  * Grid = one CTA per SM (cooperative launch, so all CTAs are resident
-//    and may wait on one another), 16 warps each. Work unit = a segment, 16
+//    and may wait on one another), 12 warps each. Work unit = a segment, 16
 //    weight rows x 256 columns.
 //  * The weights are in the segmented layout (zq4_prepare_weight,
 //    ZQ4_PREP_SEGMENTED): each segment is 2304 contiguous bytes (swizzled
@@ -74,9 +74,9 @@ __device__ unsigned g_stack_error = 0;
 
 namespace st {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 4;
+constexpr int kSlots = 5;
 constexpr int kEarly = 2;   // x chunks (16 B) per thread read before the job barrier
 using namespace segk;       // segment layout, inner loop, split-tile sums
 
