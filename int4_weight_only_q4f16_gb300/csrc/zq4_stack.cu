@@ -19,15 +19,18 @@
 //
 // How:
 //  * Grid = one CTA per SM (cooperative launch, so all CTAs are resident
-//    and may wait on one another), 12 warps each. Work unit = a segment, 16
-//    weight rows x 256 columns.
+//    and may wait on one another): 12 compute warps and one copy warp. Work
+//    unit = a segment, 16 weight rows x 256 columns.
 //  * The weights are in the segmented layout (zq4_prepare_weight,
 //    ZQ4_PREP_SEGMENTED): each segment is 2304 contiguous bytes (swizzled
 //    codes, then scales), so one bulk copy fills a shared-memory slot and no
-//    tensor map is involved. Each warp runs its own ring of segment slots
-//    across job boundaries. Per 32-column
-//    group, lane (r, t) (r = lane/4, t = lane%4) takes word t of rows r and
-//    r+8 (ldmatrix.x4 fetches two groups, conflict-free on the swizzle),
+//    tensor map is involved. Each compute warp has its own ring of segment
+//    slots; lane w of the copy warp refills ring w as soon as compute warp w
+//    releases a slot (an mbarrier per slot each way), across job
+//    boundaries, so the compute warps never spend issue slots on copies.
+//    Per 32-column group, lane (r, t) (r = lane/4, t = lane%4) takes word t
+//    of rows r and r+8 (ldmatrix.x4 fetches two groups, conflict-free on the
+//    swizzle),
 //    unpacks exact f16 (q - 7) pairs as the A fragments of two chained
 //    m16n8k16 MMAs against the matching pair-permuted x chunk, and adds the
 //    fp32 result times the fp32 group scale to its accumulator.
@@ -74,8 +77,9 @@ __device__ unsigned g_stack_error = 0;
 
 namespace st {
 
-constexpr int kWarps = 12;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 12;                  // compute warps, one ring each
+constexpr int kCompute = kWarps * 32;
+constexpr int kThreads = kCompute + 32;      // + the copy warp
 constexpr int kSlots = 5;
 constexpr int kEarly = 2;   // x chunks (16 B) per thread read before the job barrier
 using namespace segk;       // segment layout, inner loop, split-tile sums
@@ -108,7 +112,7 @@ struct Params {
 
 constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
-constexpr size_t kMiscOff = kBarOff + size_t(kWarps) * kSlots * 8;
+constexpr size_t kMiscOff = kBarOff + 2 * size_t(kWarps) * kSlots * 8;   // full, then empty barriers
 constexpr size_t kParkOff = kMiscOff + 128;                          // warp partials [kWarps*2][16][kTokCols]
 constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range table [2][kWarps + 1]
 constexpr size_t kXsOff = kTabOff + 2 * 4 * (kWarps + 1 + 15) / 16 * 16;
@@ -119,6 +123,26 @@ inline int cached_jobs(int n, int M, int max_k)
 {
     const size_t left = size_t(227) * 1024 - smem_bytes(M, max_k);
     return int(std::min<size_t>(size_t(n), left / sizeof(Job)));
+}
+
+// Has the phase of this parity completed? (never waits)
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// barrier among the compute warps only (the copy warp runs on its own)
+__device__ __forceinline__ void compute_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
@@ -149,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, t = lane & 3;
     const int G = gridDim.x, cta = blockIdx.x;
-    const uint32_t ring0 = sbase + uint32_t(kRingOff) + uint32_t(warp * kSlots * kSegBytes);
-    const uint32_t bar0 = sbase + uint32_t(kBarOff) + uint32_t(warp * kSlots * 8);
+    const uint32_t full0 = sbase + uint32_t(kBarOff), empty0 = full0 + uint32_t(kWarps * kSlots * 8);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kMiscOff);
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
@@ -162,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const unsigned target = (launch + 1u) * unsigned(G);
 
     if (threadIdx.x == 0) *s_abort = 0;
-    if (lane == 0) {
-        for (int j = 0; j < kSlots; ++j) mbar_init(bar0 + 8 * j, 1);
+    if (warp < kWarps && lane == 0) {
+        for (int j = 0; j < kSlots; ++j) {
+            mbar_init(full0 + 8 * (warp * kSlots + j), 1);    // the copy's bytes
+            mbar_init(empty0 + 8 * (warp * kSlots + j), 1);   // the consuming warp is done
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {
@@ -176,204 +202,233 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     __syncthreads();
     auto job = [&](int j) -> const Job & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
 
-    // this warp's segment range of a job: CTA part of the job, then warp part
-    // (CTA ranges are whole tiles, so a tile never spans two CTAs)
-    auto warp_range = [&](int T, int S, int &ub, int &ue) {
+    // compute warp w's segment range of a job: CTA part of the job, then
+    // warp part (CTA ranges are whole tiles, so a tile never spans two CTAs)
+    auto warp_range = [&](int T, int S, int w, int &ub, int &ue) {
         int tb, te;
         split(0, T, cta, G, tb, te);
-        split(tb * S, te * S, warp, kWarps, ub, ue);
+        split(tb * S, te * S, w, kWarps, ub, ue);
     };
 
-    // ---- lane 0: the copy iterator, one job ahead of nothing (it runs
-    // through the warp's (job, segment) sequence; segment u of a job, tile
-    // major, is at byte u * kSegBytes of its matrix)
-    int it_j = 0, it_u = 0, it_e = 0;
-    const uint8_t *it_seg = nullptr;
-    auto seek = [&](int j) {
-        for (; j < n; ++j) {
-            const Job &jb = job(j);
-            int ub, ue;
-            warp_range(jb.T, jb.S, ub, ue);
-            if (ub < ue) {
-                it_j = j;
-                it_u = ub;
-                it_e = ue;
-                it_seg = jb.seg;
-                return;
-            }
-        }
-        it_j = n;
-    };
-    int issued = 0;
-    auto issue_next = [&]() {                           // lane 0
-        const int slot = issued % kSlots;
-        const uint32_t bar = bar0 + 8 * slot;
-        mbar_arrive_expect_tx(bar, kSegBytes);
-        bulk_load(ring0 + slot * kSegBytes, it_seg + size_t(it_u) * kSegBytes, kSegBytes, bar);
-        ++issued;
-        if (++it_u >= it_e) seek(it_j + 1);
-    };
-    if (lane == 0) {
-        seek(0);
-        for (int q = 0; q < kSlots && it_j < n; ++q) issue_next();
-    }
-
-    uint32_t ldm_off[4];
-    ldm_offsets(lane, ldm_off);
-    const uint8_t *xr = xs + size_t(min(r, M - 1)) * xrow + 16 * t;
-
-    // stage x of a job synchronously (all threads; caller barriers)
-    auto stage_now = [&](const Job &jb, int from) {
-        const int words = jb.K >> 3, total = M * words;
-        for (int i0 = from + int(threadIdx.x); i0 < total; i0 += 2 * kThreads) {
-            uint4 v0, v1;
-            const int i1 = i0 + kThreads;
-            v0 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i0);
-            if (i1 < total) v1 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i1);
-            put_x(xs, xrow, words, i0, v0);
-            if (i1 < total) put_x(xs, xrow, words, i1, v1);
-        }
-    };
-    auto set_wtab = [&](const Job &jb) {              // threads 0..kWarps
-        if (threadIdx.x <= kWarps) {
-            int tb0, te0;
-            split(0, jb.T, cta, G, tb0, te0);
-            const int b = part_begin(tb0 * jb.S, te0 * jb.S, threadIdx.x, kWarps);
-            wtab[threadIdx.x] = b;
-            wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
-        }
-    };
-
-    bool ok = true;
-    int consumed = 0;
-    for (int j = 0; j < n; ++j) {
-        const Job &jb = job(j);
-        if (j == 0) {
-            set_wtab(jb);
-            stage_now(jb, 0);
-            __syncthreads();
-        } else {
-            // every warp of this CTA is done with job j-1 (x buffer free,
-            // partial tiles parked)
-            __syncthreads();
-            const bool early = (jb.flags & kJobXEarly) != 0 && !*s_abort;
-            const int words = jb.K >> 3, total = M * words;
-            uint4 xv[kEarly];
-            if (early) {
-#pragma unroll
-                for (int e = 0; e < kEarly; ++e) {
-                    const int i = int(threadIdx.x) + e * kThreads;
-                    if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
+    if (warp == kWarps) {
+        // ---------------- the copy warp ----------------
+        // Lane w keeps ring w full: it walks compute warp w's (job, segment)
+        // sequence (segment u of a job, tile major, is at byte u * kSegBytes
+        // of its matrix) and refills a slot as soon as that warp has released
+        // it, across job boundaries: the weights never depend on earlier jobs.
+        const int w = lane;
+        const uint32_t ring = sbase + uint32_t(kRingOff) + uint32_t(w * kSlots * kSegBytes);
+        int it_j = n, it_u = 0, it_e = 0, issued = 0;
+        const uint8_t *it_seg = nullptr;
+        auto seek = [&](int j) {
+            for (; j < n; ++j) {
+                const Job &jb = job(j);
+                int ub, ue;
+                warp_range(jb.T, jb.S, w, ub, ue);
+                if (ub < ue) {
+                    it_j = j;
+                    it_u = ub;
+                    it_e = ue;
+                    it_seg = jb.seg;
+                    return;
                 }
             }
-            const Job &pj = job(j - 1);
-            if (!*s_abort) {
-                int ptb, pte;
-                split(0, pj.T, cta, G, ptb, pte);
-                finalize_split<kWarps, kThreads>(ptb, pte, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y,
-                                                 wpark, wtab);
-            }
-            __syncthreads();      // finalize writes before the release below
-            if (threadIdx.x == 0 && !*s_abort) {
-                // release: this CTA's outputs of job j-1 become visible with the increment
-                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
-                const unsigned long long t0 = globaltimer();
-                for (;;) {
-                    if (ld_acquire(&p.job_cnt[j - 1]) >= target) break;
-                    if (*reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
-                        globaltimer() - t0 > kWaitLimitNs) {
-                        atomicOr(&p.hdr->abort, 1u);
-                        *s_abort = 1;
-                        break;
-                    }
-                }
-            }
-            set_wtab(jb);          // finalize of job j-1 (the table's last reader) is behind the barrier
-            if (early) {
-                // the loads were issued before the sums and the poll: stored only now,
-                // so that their latency hides behind both
-#pragma unroll
-                for (int e = 0; e < kEarly; ++e) {
-                    const int i = int(threadIdx.x) + e * kThreads;
-                    if (i < total) put_x(xs, xrow, words, i, xv[e]);
-                }
-                if (total > kEarly * kThreads) stage_now(jb, kEarly * kThreads);
-            }
-            __syncthreads();
-            if (*s_abort) {
-                ok = false;
-                break;
-            }
-            if (!early) {
-                stage_now(jb, 0);
-                __syncthreads();
-            }
-        }
-
-        const int S = jb.S, gate_up = jb.flags & kJobGateUp;
-        const int ub = wtab[warp], ue = wtab[warp + 1], first_tile = wtab[kWarps + 1 + warp];
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        int cur_tile = -1;
-        auto flush = [&](int tt) {
-            if (tt * S >= ub && (tt + 1) * S <= ue)
-                write_tile(acc, tt * 16, lane, gate_up, M, jb.N, jb.y_stride, jb.y);
-            else        // part of a tile shared with other warps: summed at job end
-                park(acc, wpark, warp, tt == first_tile ? 0 : 1, lane);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+            it_j = n;
         };
-
-        int tt = first_tile, sg = ub - first_tile * S;
-        for (int u = ub; u < ue; ++u, ++consumed) {
-            const int slot = consumed % kSlots;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, (consumed / kSlots) & 1))) {
-                ok = false;
-                break;
+        if (w < kWarps) seek(0);
+        unsigned long long t0 = globaltimer();
+        bool timed_out = false;
+        for (;;) {
+            const bool more = w < kWarps && it_j < n && !*s_abort;
+            bool did = false;
+            if (more) {
+                const int slot = issued % kSlots, f = issued / kSlots;
+                const uint32_t full = full0 + 8 * (w * kSlots + slot);
+                if (f == 0 || mbar_test(empty0 + 8 * (w * kSlots + slot), (f - 1) & 1)) {
+                    mbar_arrive_expect_tx(full, kSegBytes);
+                    bulk_load(ring + slot * kSegBytes, it_seg + size_t(it_u) * kSegBytes, kSegBytes, full);
+                    ++issued;
+                    did = true;
+                    if (++it_u >= it_e) seek(it_j + 1);
+                }
             }
-            if (tt != cur_tile) {
-                if (cur_tile >= 0) flush(cur_tile);
-                cur_tile = tt;
-            }
-            accumulate(ring0 + slot * kSegBytes, ldm_off, xr + sg * 32 * 16, r, acc);
-            // every lane's reads of the slot (their values are in registers)
-            // are done before lane 0 lets the copy engine overwrite it
-            __syncwarp();
-            if (lane == 0 && it_j < n) issue_next();
-            if (++sg == S) {
-                sg = 0;
-                ++tt;
+            if (!__any_sync(0xffffffffu, more)) break;
+            if (__any_sync(0xffffffffu, did)) {
+                t0 = globaltimer();
+            } else {
+                // no slot free: the compute warps are busy or between jobs
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    timed_out = true;
+                    break;
+                }
+                __nanosleep(100);
             }
         }
-        if (!ok) {
-            // leave together at the next job boundary: every warp must still
-            // take part in the CTA barriers there
-            *s_abort = 1;
-            continue;
-        }
-        if (cur_tile >= 0) flush(cur_tile);
-    }
-
-    if (!ok) {
-        if (lane == 0) {
+        if (timed_out && lane == 0) {
             atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
             atomicOr(&p.hdr->abort, 1u);
+            *s_abort = 1;
         }
-        *s_abort = 1;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
-    if (!*s_abort && n > 0) {                            // the last job's split tiles
-        const Job &lj = job(n - 1);
-        int ltb, lte;
-        split(0, lj.T, cta, G, ltb, lte);
-        finalize_split<kWarps, kThreads>(ltb, lte, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark,
-                                         wtab);
-    }
-    // let every copy this warp issued land before the CTA exits
-    {
-        const int outstanding = __shfl_sync(0xffffffffu, issued, 0) - consumed;
-        for (int c = consumed; c < consumed + outstanding; ++c)
-            if (!mbar_wait(bar0 + 8 * (c % kSlots), (c / kSlots) & 1)) break;
+        // every copy this lane issued has landed before the CTA may exit (the
+        // last fill of each slot; earlier fills were consumed before a refill)
+        if (w < kWarps)
+            for (int c = max(0, issued - kSlots); c < issued; ++c)
+                if (!mbar_wait(full0 + 8 * (w * kSlots + c % kSlots), (c / kSlots) & 1)) break;
+    } else {
+        // ---------------- compute warps ----------------
+        const uint32_t ring0 = sbase + uint32_t(kRingOff) + uint32_t(warp * kSlots * kSegBytes);
+        const uint32_t bfull = full0 + uint32_t(8 * warp * kSlots), bempty = empty0 + uint32_t(8 * warp * kSlots);
+        uint32_t ldm_off[4];
+        ldm_offsets(lane, ldm_off);
+        const uint8_t *xr = xs + size_t(min(r, M - 1)) * xrow + 16 * t;
+
+        // stage x of a job synchronously (compute threads; caller barriers)
+        auto stage_now = [&](const Job &jb, int from) {
+            const int words = jb.K >> 3, total = M * words;
+            for (int i0 = from + int(threadIdx.x); i0 < total; i0 += 2 * kCompute) {
+                uint4 v0, v1;
+                const int i1 = i0 + kCompute;
+                v0 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i0);
+                if (i1 < total) v1 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i1);
+                put_x(xs, xrow, words, i0, v0);
+                if (i1 < total) put_x(xs, xrow, words, i1, v1);
+            }
+        };
+        auto set_wtab = [&](const Job &jb) {              // threads 0..kWarps
+            if (threadIdx.x <= kWarps) {
+                int tb0, te0;
+                split(0, jb.T, cta, G, tb0, te0);
+                const int b = part_begin(tb0 * jb.S, te0 * jb.S, threadIdx.x, kWarps);
+                wtab[threadIdx.x] = b;
+                wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
+            }
+        };
+
+        bool ok = true;
+        int consumed = 0;
+        for (int j = 0; j < n; ++j) {
+            const Job &jb = job(j);
+            if (j == 0) {
+                set_wtab(jb);
+                stage_now(jb, 0);
+                compute_sync();
+            } else {
+                // every compute warp of this CTA is done with job j-1 (x
+                // buffer free, partial tiles parked)
+                compute_sync();
+                const bool early = (jb.flags & kJobXEarly) != 0 && !*s_abort;
+                const int words = jb.K >> 3, total = M * words;
+                uint4 xv[kEarly];
+                if (early) {
+#pragma unroll
+                    for (int e = 0; e < kEarly; ++e) {
+                        const int i = int(threadIdx.x) + e * kCompute;
+                        if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
+                    }
+                }
+                const Job &pj = job(j - 1);
+                if (!*s_abort) {
+                    int ptb, pte;
+                    split(0, pj.T, cta, G, ptb, pte);
+                    finalize_split<kWarps, kCompute>(ptb, pte, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride,
+                                                     pj.y, wpark, wtab);
+                }
+                compute_sync();      // finalize writes before the release below
+                if (threadIdx.x == 0 && !*s_abort) {
+                    // release: this CTA's outputs of job j-1 become visible with the increment
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
+                    const unsigned long long t0 = globaltimer();
+                    for (;;) {
+                        if (ld_acquire(&p.job_cnt[j - 1]) >= target) break;
+                        if (*reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
+                            globaltimer() - t0 > kWaitLimitNs) {
+                            atomicOr(&p.hdr->abort, 1u);
+                            *s_abort = 1;
+                            break;
+                        }
+                    }
+                }
+                set_wtab(jb);          // finalize of job j-1 (the table's last reader) is behind the barrier
+                if (early) {
+                    // the loads were issued before the sums and the poll: stored only now,
+                    // so that their latency hides behind both
+#pragma unroll
+                    for (int e = 0; e < kEarly; ++e) {
+                        const int i = int(threadIdx.x) + e * kCompute;
+                        if (i < total) put_x(xs, xrow, words, i, xv[e]);
+                    }
+                    if (total > kEarly * kCompute) stage_now(jb, kEarly * kCompute);
+                }
+                compute_sync();
+                if (*s_abort) {
+                    ok = false;
+                    break;
+                }
+                if (!early) {
+                    stage_now(jb, 0);
+                    compute_sync();
+                }
+            }
+
+            const int S = jb.S, gate_up = jb.flags & kJobGateUp;
+            const int ub = wtab[warp], ue = wtab[warp + 1], first_tile = wtab[kWarps + 1 + warp];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            int cur_tile = -1;
+            auto flush = [&](int tt) {
+                if (tt * S >= ub && (tt + 1) * S <= ue)
+                    write_tile(acc, tt * 16, lane, gate_up, M, jb.N, jb.y_stride, jb.y);
+                else        // part of a tile shared with other warps: summed at job end
+                    park(acc, wpark, warp, tt == first_tile ? 0 : 1, lane);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+            };
+
+            int tt = first_tile, sg = ub - first_tile * S;
+            for (int u = ub; u < ue; ++u, ++consumed) {
+                const int slot = consumed % kSlots;
+                if (!__all_sync(0xffffffffu, mbar_wait(bfull + 8 * slot, (consumed / kSlots) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (tt != cur_tile) {
+                    if (cur_tile >= 0) flush(cur_tile);
+                    cur_tile = tt;
+                }
+                accumulate(ring0 + slot * kSegBytes, ldm_off, xr + sg * 32 * 16, r, acc);
+                // every lane's reads of the slot (their values are in registers)
+                // are done before the copy warp may overwrite it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bempty + 8 * slot);
+                if (++sg == S) {
+                    sg = 0;
+                    ++tt;
+                }
+            }
+            if (!ok) {
+                // leave together at the next job boundary: every compute warp
+                // must still take part in the barriers there
+                *s_abort = 1;
+                continue;
+            }
+            if (cur_tile >= 0) flush(cur_tile);
+        }
+
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                atomicOr(&p.hdr->abort, 1u);
+            }
+            *s_abort = 1;
+        }
+        compute_sync();
+        if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+        if (!*s_abort && n > 0) {                            // the last job's split tiles
+            const Job &lj = job(n - 1);
+            int ltb, lte;
+            split(0, lj.T, cta, G, ltb, lte);
+            finalize_split<kWarps, kCompute>(ltb, lte, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark,
+                                             wtab);
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0 && !*s_abort) {
