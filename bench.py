@@ -5,8 +5,10 @@ Default workload: the Phi-3-mini-shaped decode layer stack at M = 1
 (32 layers x {QKV 9216x3072, O 3072x3072, gate_up 16384x3072 -> SiLU*mul
 8192, down 3072x8192} + LM head 32064x3072, every matrix distinct, seeded
 synthetic weights; 2.09 GB of packed weights per token). One step = one
-decode token through the whole stack = 129 kernel launches, replayed from a
-CUDA graph. Prints one JSON line (rank 0).
+decode token through the whole stack: by default one cooperative launch of
+the persistent step kernel over a plan of the 129 projections
+(--stack-mode plan); --stack-mode calls issues one launch per projection.
+The step is replayed from a CUDA graph. Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zq4|reference]
                   [--workload phi3|gemv3072|qwen3|moe] [--m M] [--t T]
@@ -42,7 +44,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
     ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill"])
-    ap.add_argument("--stack-mode", default="calls", choices=["calls", "seg", "plan"],
+    ap.add_argument("--stack-mode", default="plan", choices=["calls", "seg", "plan"],
                     help="phi3/qwen3: one launch per projection, or the whole step as one launch")
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
@@ -50,6 +52,8 @@ def parse_args():
     ap.add_argument("--copies", type=int, default=8, help="distinct weight copies (kernel workload)")
     ap.add_argument("--eager", action="store_true", help="kernel workload: plain launches, no graph")
     ap.add_argument("--m", type=int, default=1, help="tokens per step (qwen3 workload)")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers of the Phi-3 stack (32 is the workload; fewer only for profiling)")
     ap.add_argument("--t", type=int, default=16, help="tokens per step (moe workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -176,6 +180,7 @@ def measured_peaks():
 # dropped as soon as one of them changes)
 KERNEL_SOURCES = {
     "gate_up_phi3_M1": ("zq4_decode_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
+    "stack_phi3_M1": ("zq4_stack.cu", "zq4_segment.cuh", "zq4_async.cuh", "zq4_common.cuh"),
     "prefill_gate_up_M1024": ("zq4_prefill_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
 }
 
@@ -294,7 +299,8 @@ def capture(torch, fn, stream):
 def run_phi3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod, synth, zq4
     dev = torch.device("cuda", dist.local)
-    st = stack_mod.phi3_stack(M=1, device=dev, mode=args.stack_mode)
+    st = stack_mod.DecodeStack(synth.PHI3_LAYER, args.layers, synth.PHI3_LM_HEAD, M=1, device=dev,
+                               mode=args.stack_mode)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         st.launch_step(stream)                         # eager step: sets kernel attributes
@@ -317,27 +323,38 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
     bytes_step = st.bytes_per_step()
     tok_s = dist.world * st.M / step_s
 
-    # dominant kernel: gate_up + SiLU*mul over the stack's 32 distinct matrices
-    gu = [st.layers[l]["gate_up"] for l in range(st.n_layers)]
+    if args.stack_mode == "plan":
+        # the whole step is one launch of k_stack: it is the dominant kernel
+        achieved = bytes_step / step_s / 1e9
+        roofline = {"bound": "hbm", "kernel": "k_stack (whole decode step, one cooperative launch)",
+                    "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                    "traffic": profiled_traffic("stack_phi3_M1") if args.layers == 32 else None,
+                    "bytes_per_launch": bytes_step, "avg_launch_us": round(step_s * 1e6, 3),
+                    "launches_timed": args.steps}
+    else:
+        # dominant kernel: gate_up + SiLU*mul over the stack's distinct matrices
+        gu = [st.layers[l]["gate_up"] for l in range(st.n_layers)]
 
-    def gate_up_chain():
-        for l, p in enumerate(gu):
-            zq4.gate_up_silu(p.wq, p.sc, st.x[(l, "gate_up")], p.N, p.K, h=st.y[(l, "gate_up")],
-                             stream=stream)
-    gg = capture(torch, gate_up_chain, stream)
-    replay_on(torch, gg, stream, 3)
-    reps = max(10, min(200, args.steps // 10))
-    gu_s = time_replays(torch, gg.replay, reps, stream) / (reps * len(gu))
-    p0 = gu[0]
-    gu_bytes = p0.nbytes + st.M * p0.K * 2 + st.M * (p0.N // 2) * 2
-    achieved = gu_bytes / gu_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_decode_tc<1,2> (gate_up + SiLU*mul, 16384x3072)",
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                "traffic": profiled_traffic("gate_up_phi3_M1"),
-                "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_s * 1e6, 3),
-                "launches_timed": reps * len(gu)}
+        def gate_up_chain():
+            for l, p in enumerate(gu):
+                zq4.gate_up_silu(p.wq, p.sc, st.x[(l, "gate_up")], p.N, p.K, h=st.y[(l, "gate_up")],
+                                 stream=stream)
+        gg = capture(torch, gate_up_chain, stream)
+        replay_on(torch, gg, stream, 3)
+        reps = max(10, min(200, args.steps // 10))
+        gu_s = time_replays(torch, gg.replay, reps, stream) / (reps * len(gu))
+        p0 = gu[0]
+        gu_bytes = p0.nbytes + st.M * p0.K * 2 + st.M * (p0.N // 2) * 2
+        achieved = gu_bytes / gu_s / 1e9
+        roofline = {"bound": "hbm", "kernel": "k_decode_tc<1,2> (gate_up + SiLU*mul, 16384x3072)",
+                    "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                    "traffic": profiled_traffic("gate_up_phi3_M1"),
+                    "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_s * 1e6, 3),
+                    "launches_timed": reps * len(gu)}
 
     e2e = None
     if not args.no_e2e:
@@ -360,8 +377,8 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
         "hbm_gbs": round(bytes_step / step_s / 1e9, 1),
         "hbm_frac_of_measured": round(bytes_step / step_s / 1e9 / peaks["hbm_gbs"], 4),
         "hbm_frac_of_8tbs": round(bytes_step / step_s / 8e12, 4),
-        "config": {"workload": "phi3-mini decode layer stack, M=1 (32 layers + LM head)",
-                   "M": 1, "layers": 32, "launches_per_step": st.launches_per_step(),
+        "config": {"workload": f"phi3-mini decode layer stack, M=1 ({args.layers} layers + LM head)",
+                   "M": 1, "layers": args.layers, "launches_per_step": st.launches_per_step(),
                    "bytes_per_step": bytes_step, "weight_bytes_per_step": st.weight_bytes(),
                    "l2": f"inputs larger than L2: {st.weight_bytes() / 1e9:.2f} GB of distinct "
                          f"weights per step vs {L2_BYTES >> 20} MiB L2",
@@ -397,9 +414,13 @@ def phi3_e2e(args, torch, st, stream, dist):
     out = st.y[("head",)]
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     # the step's inputs are read from dev_in: rebind the stack's inputs to it
-    saved = dict(st.x)
+    saved, saved_plan = dict(st.x), st.plan
     for (k, _), (_, v) in zip(zip(keys, sizes), views):
         st.x[k] = v
+    st.plan = None                     # plan mode: the job table must point at the rebound inputs
+    with torch.cuda.stream(stream):
+        st.launch_step(stream)
+    torch.cuda.synchronize()
     g = st.capture(stream)
     steps = max(3, min(args.steps, 500))
 
@@ -418,6 +439,7 @@ def phi3_e2e(args, torch, st, stream, dist):
     torch.cuda.synchronize()
     el = dist.max(time.perf_counter() - t0)
     st.x.update(saved)
+    st.plan = saved_plan
     return {"value": round(dist.world * st.M * steps / el, 2), "unit": "tok/s",
             "h2d_bytes_per_step": int(host_in.numel() * 2),
             "d2h_bytes_per_step": int(host_out.numel() * 2), "steps": steps,

@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         };
 
         bool ok = true;
-        int consumed = 0;
+        int slot = 0;             // ring position of the next segment and the parity of its fill
+        uint32_t phase = 0;
         for (int j = 0; j < n; ++j) {
             const Job &jb = job(j);
             if (j == 0) {
@@ -384,9 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             };
 
             int tt = first_tile, sg = ub - first_tile * S;
-            for (int u = ub; u < ue; ++u, ++consumed) {
-                const int slot = consumed % kSlots;
-                if (!__all_sync(0xffffffffu, mbar_wait(bfull + 8 * slot, (consumed / kSlots) & 1))) {
+            for (int u = ub; u < ue; ++u) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bfull + 8 * slot, phase))) {
                     ok = false;
                     break;
                 }
@@ -399,6 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 // are done before the copy warp may overwrite it
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bempty + 8 * slot);
+                if (++slot == kSlots) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
                 if (++sg == S) {
                     sg = 0;
                     ++tt;
