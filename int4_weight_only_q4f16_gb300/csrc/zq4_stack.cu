@@ -152,6 +152,50 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     return r;
 }
 
+// After a barrier of the compute warps: the tiles [tb, tb + nt) of a job
+// that were split between warps get the parked parts of their warps summed
+// in warp order (bit-reproducible) and written. One output per thread and
+// pass; `shift` = log2 of the outputs per tile rounded up to a power of
+// two, so no division. `wtab` = the warp range starts (kWarps + 1 entries)
+// then each warp's first tile.
+__device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_up, int M, int N, int y_stride,
+                                                uint16_t *y, const float *wpark, const int *wtab)
+{
+    const int per_tok = gate_up ? 8 : 16, tok_shift = gate_up ? 3 : 4;
+    const int outs = per_tok * M;
+    int shift = 3;
+    while ((1 << shift) < outs) ++shift;
+    int wb[kWarps + 1], wf[kWarps];
+#pragma unroll
+    for (int w = 0; w <= kWarps; ++w) wb[w] = wtab[w];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) wf[w] = wtab[kWarps + 1 + w];
+    for (int it = threadIdx.x; it < (nt << shift); it += kCompute) {
+        const int o = it & ((1 << shift) - 1);
+        if (o >= outs) continue;
+        const int tt = tb + (it >> shift), lo = tt * S, hi = lo + S;
+        const int m = o >> tok_shift, i = o & (per_tok - 1), ra = gate_up ? 2 * i : i;
+        float v0 = 0.f, v1 = 0.f;
+        int parts = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            if (wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo) {
+                ++parts;
+                const float *qk = wpark + ((w * 2 + (tt == wf[w] ? 0 : 1)) * 16) * kTokCols;
+                v0 += qk[ra * kTokCols + m];
+                if (gate_up) v1 += qk[(ra + 1) * kTokCols + m];
+            }
+        }
+        if (parts < 2) continue;                 // one warp held the whole tile and wrote it
+        const int row0 = tt * 16;
+        if (!gate_up) {
+            if (row0 + i < N) y[size_t(m) * y_stride + row0 + i] = float_to_f16_bits(v0);
+        } else if (row0 + 2 * i + 1 < N) {
+            y[size_t(m) * y_stride + (row0 >> 1) + i] = float_to_f16_bits(silu_f32(v0) * v1);
+        }
+    }
+}
+
 // x chunk i of M*K/8 (16 bytes of token i / (K/8)) into its staged place,
 // pair-permuted as the unpack produces: (x0,x4),(x1,x5),(x2,x6),(x3,x7)
 __device__ __forceinline__ void put_x(uint8_t *xs, uint32_t xrow, int words, int i, uint4 v)
@@ -331,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 if (!*s_abort) {
                     int ptb, pte;
                     split(0, pj.T, cta, G, ptb, pte);
-                    finalize_split<kWarps, kCompute>(ptb, pte, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride,
-                                                     pj.y, wpark, wtab);
+                    sum_split_tiles(ptb, pte - ptb, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y, wpark,
+                                    wtab);
                 }
                 compute_sync();      // finalize writes before the release below
                 if (threadIdx.x == 0 && !*s_abort) {
@@ -430,8 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             const Job &lj = job(n - 1);
             int ltb, lte;
             split(0, lj.T, cta, G, ltb, lte);
-            finalize_split<kWarps, kCompute>(ltb, lte, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark,
-                                             wtab);
+            sum_split_tiles(ltb, lte - ltb, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark, wtab);
         }
     }
     __syncthreads();
