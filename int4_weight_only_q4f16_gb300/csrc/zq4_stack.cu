@@ -114,8 +114,9 @@ constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
 constexpr size_t kMiscOff = kBarOff + 2 * size_t(kWarps) * kSlots * 8;   // full, then empty barriers
 constexpr size_t kParkOff = kMiscOff + 128;                          // warp partials [kWarps*2][16][kTokCols]
-constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range table [2][kWarps + 1]
-constexpr size_t kXsOff = kTabOff + 2 * 4 * (kWarps + 1 + 15) / 16 * 16;
+constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range tables, two jobs
+constexpr int kTabInts = 2 * (kWarps + 1) + 2;                       // one job: range starts, first tiles, CTA tiles
+constexpr size_t kXsOff = kTabOff + (2 * kTabInts * 4 + 15) / 16 * 16;
 __host__ __device__ inline size_t xs_bytes(int M, int max_k) { return (size_t(M) * xs_row_bytes(max_k) + 15) / 16 * 16; }
 __host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + xs_bytes(M, max_k); }
 // jobs that fit in shared memory next to everything else (the rest are read from the plan)
@@ -175,18 +176,27 @@ __device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_
         if (o >= outs) continue;
         const int tt = tb + (it >> shift), lo = tt * S, hi = lo + S;
         const int m = o >> tok_shift, i = o & (per_tok - 1), ra = gate_up ? 2 * i : i;
-        float v0 = 0.f, v1 = 0.f;
+        // every warp's parked value is read (all loads in flight at once);
+        // those of warps not holding part of tile tt are added as +0, which
+        // leaves the warp-order sum bit-identical
+        float p0[kWarps], p1[kWarps];
+        bool in[kWarps];
         int parts = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            if (wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo) {
-                ++parts;
-                const float *qk = wpark + ((w * 2 + (tt == wf[w] ? 0 : 1)) * 16) * kTokCols;
-                v0 += qk[ra * kTokCols + m];
-                if (gate_up) v1 += qk[(ra + 1) * kTokCols + m];
-            }
+            in[w] = wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo;
+            parts += in[w];
+            const float *qk = wpark + ((w * 2 + (tt == wf[w] ? 0 : 1)) * 16 + ra) * kTokCols + m;
+            p0[w] = qk[0];
+            p1[w] = gate_up ? qk[kTokCols] : 0.f;
         }
         if (parts < 2) continue;                 // one warp held the whole tile and wrote it
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            v0 += in[w] ? p0[w] : 0.f;
+            v1 += in[w] ? p1[w] : 0.f;
+        }
         const int row0 = tt * 16;
         if (!gate_up) {
             if (row0 + i < N) y[size_t(m) * y_stride + row0 + i] = float_to_f16_bits(v0);
@@ -338,13 +348,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 if (i1 < total) put_x(xs, xrow, words, i1, v1);
             }
         };
-        auto set_wtab = [&](const Job &jb) {              // threads 0..kWarps
-            if (threadIdx.x <= kWarps) {
+        // the warp range table of job j (one of two buffers, so that the table
+        // of the next job can be made while the sums of the last one read theirs):
+        // lanes 0..kWarps of warp `tw`
+        auto set_wtab = [&](const Job &jb, int j, int tw) {
+            const int q = int(threadIdx.x) - 32 * tw;
+            if (q >= 0 && q <= kWarps) {
                 int tb0, te0;
                 split(0, jb.T, cta, G, tb0, te0);
-                const int b = part_begin(tb0 * jb.S, te0 * jb.S, threadIdx.x, kWarps);
-                wtab[threadIdx.x] = b;
-                wtab[kWarps + 1 + threadIdx.x] = b / jb.S;
+                const int b = part_begin(tb0 * jb.S, te0 * jb.S, q, kWarps);
+                int *tab = wtab + (j & 1) * kTabInts;
+                tab[q] = b;
+                tab[kWarps + 1 + q] = b / jb.S;
+                if (q == 0) {
+                    tab[2 * (kWarps + 1)] = tb0;      // this CTA's tiles of the job
+                    tab[2 * (kWarps + 1) + 1] = te0;
+                }
             }
         };
 
@@ -354,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         for (int j = 0; j < n; ++j) {
             const Job &jb = job(j);
             if (j == 0) {
-                set_wtab(jb);
+                set_wtab(jb, 0, 0);
                 stage_now(jb, 0);
                 compute_sync();
             } else {
@@ -373,12 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 }
                 const Job &pj = job(j - 1);
                 if (!*s_abort) {
-                    int ptb, pte;
-                    split(0, pj.T, cta, G, ptb, pte);
+                    const int *ptab = wtab + ((j - 1) & 1) * kTabInts;
+                    const int ptb = ptab[2 * (kWarps + 1)], pte = ptab[2 * (kWarps + 1) + 1];
                     sum_split_tiles(ptb, pte - ptb, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y, wpark,
-                                    wtab);
+                                    ptab);
                 }
                 compute_sync();      // finalize writes before the release below
+                set_wtab(jb, j, 1);  // warp 1, while thread 0 waits at the grid barrier
                 if (threadIdx.x == 0 && !*s_abort) {
                     // release: this CTA's outputs of job j-1 become visible with the increment
                     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
@@ -393,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                         }
                     }
                 }
-                set_wtab(jb);          // finalize of job j-1 (the table's last reader) is behind the barrier
                 if (early) {
                     // the loads were issued before the sums and the poll: stored only now,
                     // so that their latency hides behind both
@@ -416,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             }
 
             const int S = jb.S, gate_up = jb.flags & kJobGateUp;
-            const int ub = wtab[warp], ue = wtab[warp + 1], first_tile = wtab[kWarps + 1 + warp];
+            const int *tab = wtab + (j & 1) * kTabInts;
+            const int ub = tab[warp], ue = tab[warp + 1], first_tile = tab[kWarps + 1 + warp];
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             int cur_tile = -1;
             auto flush = [&](int tt) {
@@ -472,9 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
         if (!*s_abort && n > 0) {                            // the last job's split tiles
             const Job &lj = job(n - 1);
-            int ltb, lte;
-            split(0, lj.T, cta, G, ltb, lte);
-            sum_split_tiles(ltb, lte - ltb, lj.S, lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark, wtab);
+            const int *ltab = wtab + ((n - 1) & 1) * kTabInts;
+            sum_split_tiles(ltab[2 * (kWarps + 1)], ltab[2 * (kWarps + 1) + 1] - ltab[2 * (kWarps + 1)], lj.S,
+                            lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark, ltab);
         }
     }
     __syncthreads();
