@@ -113,8 +113,13 @@ struct Params {
 constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
 constexpr size_t kMiscOff = kBarOff + 2 * size_t(kWarps) * kSlots * 8;   // full, then empty barriers
-constexpr size_t kParkOff = kMiscOff + 128;                          // warp partials [kWarps*2][16][kTokCols]
-constexpr size_t kTabOff = kParkOff + size_t(kWarps) * 2 * 16 * kTokCols * 4;   // warp range tables, two jobs
+// Warp partials: slot [kWarps*2], each [kTokCols][kParkRow] floats (token
+// major, rows padded to 17 so that the 16 rows of one token, read by 16
+// lanes, fall in distinct banks).
+constexpr int kParkRow = 17;
+constexpr int kParkSlot = kTokCols * kParkRow;
+constexpr size_t kParkOff = kMiscOff + 128;
+constexpr size_t kTabOff = kParkOff + (size_t(kWarps) * 2 * kParkSlot * 4 + 15) / 16 * 16;   // warp range tables, two jobs
 constexpr int kTabInts = 2 * (kWarps + 1) + 2;                       // one job: range starts, first tiles, CTA tiles
 constexpr size_t kXsOff = kTabOff + (2 * kTabInts * 4 + 15) / 16 * 16;
 __host__ __device__ inline size_t xs_bytes(int M, int max_k) { return (size_t(M) * xs_row_bytes(max_k) + 15) / 16 * 16; }
@@ -186,9 +191,9 @@ __device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_
         for (int w = 0; w < kWarps; ++w) {
             in[w] = wb[w] < wb[w + 1] && wb[w] < hi && wb[w + 1] > lo;
             parts += in[w];
-            const float *qk = wpark + ((w * 2 + (tt == wf[w] ? 0 : 1)) * 16 + ra) * kTokCols + m;
+            const float *qk = wpark + (w * 2 + (tt == wf[w] ? 0 : 1)) * kParkSlot + m * kParkRow + ra;
             p0[w] = qk[0];
-            p1[w] = gate_up ? qk[kTokCols] : 0.f;
+            p1[w] = gate_up ? qk[1] : 0.f;
         }
         if (parts < 2) continue;                 // one warp held the whole tile and wrote it
         float v0 = 0.f, v1 = 0.f;
@@ -383,19 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 const bool early = (jb.flags & kJobXEarly) != 0 && !*s_abort;
                 const int words = jb.K >> 3, total = M * words;
                 uint4 xv[kEarly];
-                if (early) {
-#pragma unroll
-                    for (int e = 0; e < kEarly; ++e) {
-                        const int i = int(threadIdx.x) + e * kCompute;
-                        if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
-                    }
-                }
                 const Job &pj = job(j - 1);
                 if (!*s_abort) {
                     const int *ptab = wtab + ((j - 1) & 1) * kTabInts;
                     const int ptb = ptab[2 * (kWarps + 1)], pte = ptab[2 * (kWarps + 1) + 1];
                     sum_split_tiles(ptb, pte - ptb, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y, wpark,
                                     ptab);
+                }
+                if (early) {
+                    // read now, stored after the grid barrier: the latency hides behind it
+#pragma unroll
+                    for (int e = 0; e < kEarly; ++e) {
+                        const int i = int(threadIdx.x) + e * kCompute;
+                        if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
+                    }
                 }
                 compute_sync();      // finalize writes before the release below
                 set_wtab(jb, j, 1);  // warp 1, while thread 0 waits at the grid barrier
@@ -414,8 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     }
                 }
                 if (early) {
-                    // the loads were issued before the sums and the poll: stored only now,
-                    // so that their latency hides behind both
+                    // the loads were issued before the poll: stored only now
 #pragma unroll
                     for (int e = 0; e < kEarly; ++e) {
                         const int i = int(threadIdx.x) + e * kCompute;
@@ -443,7 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 if (tt * S >= ub && (tt + 1) * S <= ue)
                     write_tile(acc, tt * 16, lane, gate_up, M, jb.N, jb.y_stride, jb.y);
                 else        // part of a tile shared with other warps: summed at job end
-                    park(acc, wpark, warp, tt == first_tile ? 0 : 1, lane);
+                {
+                    // lane (r, t) holds rows r, r+8 of tokens 2t, 2t+1
+                    float *pk = wpark + (warp * 2 + (tt == first_tile ? 0 : 1)) * kParkSlot;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) pk[(2 * t + c) * kParkRow + r + 8 * h] = acc[2 * h + c];
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
             };
