@@ -14,7 +14,7 @@ import torch
 
 from int4_weight_only_q4f16_gb300 import synth
 from int4_weight_only_q4f16_gb300 import stack as stk
-from helpers import assert_within, host_f16
+from helpers import assert_within, dev, host_f16
 
 pytestmark = pytest.mark.gpu
 
@@ -115,3 +115,51 @@ def test_phi3_full_step_sampled(oracle):
 def test_stack_no_device_errors():
     from int4_weight_only_q4f16_gb300 import zq4
     assert zq4.device_errors(clear=True) == 0
+
+
+def _plan_outputs(jobs, M):
+    """Run `jobs` [(wq, sc, x, N, K, gate_up)] as one plan on segmented
+    copies; returns the host f16 outputs."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    pj, ys = [], []
+    for wq, sc, x, N, K, gate_up in jobs:
+        seg, _ = zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED)
+        y = torch.full((M, N // 2 if gate_up else N), float("nan"), dtype=torch.float16, device="cuda")
+        pj.append((seg, x, y, N, K, gate_up))
+        ys.append(y)
+    zq4.StackPlan(pj, M).run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    return [host_f16(y) for y in ys]
+
+
+@pytest.mark.parametrize("K", [256, 3072, 8192])
+def test_stack_all_zero_point_codes_give_exact_zero(K):
+    """Codes all 7 make every weight exactly 0 (S = 0): the one-launch step,
+    tiles split between warps included, must give exactly 0 for large
+    activations too, in both epilogues."""
+    M, N = 3, 400
+    rng = synth.rng_for("stack_zp7", K)
+    x = dev((rng.standard_normal((M, K)) * 300).astype(np.float16))
+    wq = dev(np.full((N, K // 8), 0x77777777, np.uint32))
+    sc = dev(synth.group_scales(rng, N, K))
+    y, h = _plan_outputs([(wq, sc, x, N, K, False), (wq, sc, x, N, K, True)], M)
+    assert np.all(y == 0) and np.all(h == 0)
+
+
+def test_stack_one_hot_bit_exact(oracle):
+    """x = e_k returns f16(w[:, k]) exactly through the one-launch step
+    (one non-zero product per output, whichever warp or split tile holds it)."""
+    N, K = 640, 3072
+    wq_h, sc_h = synth.weight("stack_onehot", N, K, 0)
+    w = oracle.dequant(wq_h, sc_h, N, K)
+    ks = (0, 1, 7, 8, 255, 256, 1029, 3071)
+    xs = np.zeros((len(ks), K), np.float16)
+    for i, k in enumerate(ks):
+        xs[i, k] = 1.0
+    wq, sc = dev(wq_h), dev(sc_h)
+    jobs = [(wq, sc, dev(xs[i:i + 1]), N, K, False) for i in range(len(ks))]
+    outs = _plan_outputs(jobs, 1)
+    for i, k in enumerate(ks):
+        want = oracle.round_f16(w[:, k])
+        assert np.array_equal(outs[i][0].view(np.uint16), want.view(np.uint16)), k
