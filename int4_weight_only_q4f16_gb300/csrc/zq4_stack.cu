@@ -395,19 +395,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     sum_split_tiles(ptb, pte - ptb, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y, wpark,
                                     ptab);
                 }
+                compute_sync();      // finalize writes before the release below
+                set_wtab(jb, j, 1);  // warp 1, while thread 0 waits at the grid barrier
+                if (threadIdx.x == 0 && !*s_abort) {
+                    // release: this CTA's outputs of job j-1 become visible with the increment
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
+                }
                 if (early) {
-                    // read now, stored after the grid barrier: the latency hides behind it
+                    // read now (thread 0 after its release, which would otherwise wait
+                    // for these loads), stored after the grid barrier: the latency hides
+                    // behind it
 #pragma unroll
                     for (int e = 0; e < kEarly; ++e) {
                         const int i = int(threadIdx.x) + e * kCompute;
                         if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
                     }
                 }
-                compute_sync();      // finalize writes before the release below
-                set_wtab(jb, j, 1);  // warp 1, while thread 0 waits at the grid barrier
                 if (threadIdx.x == 0 && !*s_abort) {
-                    // release: this CTA's outputs of job j-1 become visible with the increment
-                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
                     const unsigned long long t0 = globaltimer();
                     for (;;) {
                         if (ld_acquire(&p.job_cnt[j - 1]) >= target) break;
