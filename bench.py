@@ -43,7 +43,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
-    ap.add_argument("--workload", default="phi3", choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill"])
+    ap.add_argument("--workload", default="phi3",
+                    choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill", "lmhead"])
     ap.add_argument("--stack-mode", default="plan", choices=["calls", "seg", "plan"],
                     help="phi3/qwen3: one launch per projection, or the whole step as one launch")
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
@@ -478,6 +479,53 @@ def run_gemv3072(args, torch, dist, peaks, peak_kind):
                        "l2": f"{copies} distinct copies ({copies * b / 1e6:.0f} MB) > 4x L2"}}
 
 
+def run_lmhead(args, torch, dist, peaks, peak_kind):
+    """The LM-head step of decode: Phi-3 LM head 32064x3072 at M = 1 with
+    fp32 logits and the fused argmax (zq4_gemv_argmax), over rotating weight
+    copies that together exceed 4x L2; the plain f16 GEMV of the same shape
+    is timed beside it."""
+    from int4_weight_only_q4f16_gb300 import synth, zq4
+    _, N, K = synth.PHI3_LM_HEAD
+    copies = 10
+    wq, sc = synth.weight("lm_head", N, K, 0)
+    W = torch.from_numpy(wq.view(np.int32)).cuda().repeat(copies, 1).view(copies, N, K // 8)
+    S = torch.from_numpy(sc).cuda().repeat(copies, 1).view(copies, N, K // 32)
+    x = torch.from_numpy(synth.activations(synth.rng_for("lmhead_x"), 1, K)).cuda()
+    y32 = torch.empty((copies, 1, N), dtype=torch.float32, device="cuda")
+    y16 = torch.empty((copies, 1, N), dtype=torch.float16, device="cuda")
+    idx = torch.empty((copies, 1), dtype=torch.int32, device="cuda")
+    mx = torch.empty((copies, 1), dtype=torch.float32, device="cuda")
+    work = torch.zeros((copies, 9), dtype=torch.int64, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def chain_argmax():
+        for c in range(copies):
+            zq4.gemv_argmax(W[c], S[c], x, N, K, y32=y32[c], idx=idx[c], maxval=mx[c], work=work[c],
+                            stream=stream)
+
+    def chain_plain():
+        for c in range(copies):
+            zq4.gemv(W[c], S[c], x, N, K, y=y16[c], stream=stream)
+    res = {}
+    for name, fn in (("argmax", chain_argmax), ("plain", chain_plain)):
+        with torch.cuda.stream(stream):
+            fn()
+        g = capture(torch, fn, stream)
+        replay_on(torch, g, stream, max(3, args.warmup))
+        reps = max(5, min(args.steps // copies, 200))
+        res[name] = time_replays(torch, g.replay, reps, stream) / (reps * copies)
+    torch.cuda.synchronize()
+    b = N * (K // 8) * 4 + N * (K // 32) * 2 + K * 2
+    gbs = (b + N * 4) / res["argmax"] / 1e9
+    return {"metric": "LM-head GEMV 32064x3072 M=1 with fp32 logits + fused argmax, achieved HBM GB/s",
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(res["argmax"] * 1e6, 3),
+            "frac_of_measured": round(gbs / peaks["hbm_gbs"], 4),
+            "plain_f16_gemv_us": round(res["plain"] * 1e6, 3),
+            "argmax_token": int(idx[0, 0].item()),
+            "config": {"workload": "Phi-3 LM head 32064x3072, M=1, argmax", "copies": copies,
+                       "l2": f"{copies} distinct copies ({copies * b / 1e6:.0f} MB) > 4x L2"}}
+
+
 def run_qwen3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod, zq4
     st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode if args.m <= 8 else "calls")  # M > 8: canonical only
@@ -718,7 +766,7 @@ def main():
     torch.cuda.set_device(dist.local)
     peaks, kind = measured_peaks()
     fn = {"phi3": run_phi3, "gemv3072": run_gemv3072, "qwen3": run_qwen3, "moe": run_moe,
-          "kernel": run_kernel, "prefill": run_prefill}[args.workload]
+          "kernel": run_kernel, "prefill": run_prefill, "lmhead": run_lmhead}[args.workload]
     line = fn(args, torch, dist, peaks, kind)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)

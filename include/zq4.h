@@ -124,6 +124,37 @@ ZQ4_API zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const ui
 ZQ4_API zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
                             uint16_t *h, int M, int N2, int K, void *stream);
 
+/*
+ * zq4_gemv_argmax -- the LM-head step of decode: fp32 logits and, per token,
+ * the index of the largest logit.
+ * Source: "Zero TVM Documentation", section "WGSL Kernel Roles" (the LM-head
+ * matmul writes f32 logits for a stable argmax, followed by the argmax
+ * shader) and its decode loop (argmax of the last logits picks the token).
+ *
+ *   wq [N, K/8] uint32, scales [N, K/32] f16, x [M, K] f16  (as zq4_gemv)
+ *   y32    [M, N] float, device, or NULL (logits not stored)
+ *   idx    [M] int32, device: idx[m] = the n of the largest y32[m, n]; the
+ *          lowest such n when several are equal (a NaN logit counts as the
+ *          largest)
+ *   maxval [M] float, device, or NULL: that largest logit
+ *   work   [M + 8] uint64, device, caller-owned scratch: ALL ZERO before the
+ *          first call (e.g. cudaMemset); every call leaves it all zero
+ *          again. Calls sharing one work buffer must be ordered on one
+ *          stream.
+ *   y32[m, n] = sum_k x[m,k] * w[n,k] in fp32 (no f16 rounding)
+ *
+ * 1 <= M <= 64, 1 <= N, K a multiple of 256 (the tensor-core decode path).
+ * One launch per block of up to 16 tokens: each CTA folds the largest logit
+ * of every token in its tiles into an atomic maximum, and the last CTA to
+ * finish writes idx / maxval and zeroes work. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE,
+ * ZQ4_ERR_ALIGN (x 16 B; y32, idx, maxval 4 B; work 8 B), ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED (K not a multiple of 256, or x too large for shared
+ * memory), ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_gemv_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
+                                   int32_t *idx, float *maxval, uint64_t *work, int M, int N, int K,
+                                   void *stream);
+
 /* Modes of zq4_moe_gemv. */
 #define ZQ4_MOE_GATE_UP_SILU 1
 #define ZQ4_MOE_DOWN_COMBINE 2

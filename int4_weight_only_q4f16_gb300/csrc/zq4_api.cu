@@ -1,5 +1,6 @@
 // zq4_api.cu -- the extern "C" entry points declared in include/zq4.h:
 // host-side argument checks, then stream-ordered launches.
+#include <algorithm>
 #include <atomic>
 
 #include "zq4_common.cuh"
@@ -47,7 +48,10 @@ size_t smem_per_sm()
 
 cudaError_t ensure_smem(const void *kernel, size_t bytes, int *cache_by_device)
 {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    // Without the attribute a launch may use 48 KB of shared memory, static
+    // and dynamic together; the kernels here have up to a few hundred bytes
+    // of static arrays, so the attribute is set for anything above 32 KB.
+    if (bytes <= 32 * 1024) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -127,6 +131,33 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
                                             static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_decode(wq, scales, x, y, M, N, K, false,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_gemv_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
+                           int32_t *idx, float *maxval, uint64_t *work, int M, int N, int K, void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !idx || !work) return ZQ4_ERR_NULL;
+    if (M <= 0 || M > 64) return ZQ4_ERR_SHAPE;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y32) & 3) || (reinterpret_cast<uintptr_t>(idx) & 3) ||
+        (reinterpret_cast<uintptr_t>(maxval) & 3) || (reinterpret_cast<uintptr_t>(work) & 7))
+        return ZQ4_ERR_ALIGN;
+    if (!decode_tc_supported(std::min(M, 8), K)) return ZQ4_ERR_UNSUPPORTED;
+    const size_t ybytes = y32 ? size_t(M) * N * 4 : 0, wbytes = size_t(M + 8) * 8;
+    const void *outs[4] = {y32, idx, maxval, work};
+    const size_t obytes[4] = {ybytes, size_t(M) * 4, maxval ? size_t(M) * 4 : 0, wbytes};
+    for (int i = 0; i < 4; ++i) {
+        if (!obytes[i]) continue;
+        if (overlap(outs[i], obytes[i], wq, wq_bytes(N, K)) || overlap(outs[i], obytes[i], scales, sc_bytes(N, K)) ||
+            overlap(outs[i], obytes[i], x, size_t(M) * K * 2))
+            return ZQ4_ERR_OVERLAP;
+        for (int j = 0; j < i; ++j)
+            if (obytes[j] && overlap(outs[i], obytes[i], outs[j], obytes[j])) return ZQ4_ERR_OVERLAP;
+    }
+    return cuda_status(launch_decode_tc_argmax(wq, scales, x, y32, idx, maxval,
+                                               reinterpret_cast<unsigned long long *>(work), M, N, K,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,

@@ -127,6 +127,23 @@ __host__ __device__ inline size_t smem_bytes(int M, int K)
            zp_bytes<NB>(K) + size_t(M) * xs_row_bytes(K);
 }
 
+// Argmax key of logit v at row n: the float's bits made order-preserving as
+// an unsigned integer in the high word, ~n in the low word, so that the
+// largest key is the largest logit and, among equal logits, the lowest row.
+// -0 is taken as +0 (equal values tie), and every NaN gets the top value
+// (a NaN counts as the largest; the first one wins).
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n)
+{
+    unsigned ord;
+    if (v != v) {
+        ord = 0xffffffffu;
+    } else {
+        const unsigned b = v == 0.f ? 0u : __float_as_uint(v);
+        ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return (static_cast<unsigned long long>(ord) << 32) | static_cast<unsigned>(~unsigned(n));
+}
+
 template <int NB, int RU>
 __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ CUtensorMap tm_codes,
                                                         const __grid_constant__ CUtensorMap tm_scales,
@@ -380,6 +397,27 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     a.y[size_t(m) * a.y_stride + row0 + i] = float_to_f16_bits(v);
                 }
             }
+        } else if (RU == 3) {
+            // fp32 logits, and the tile's largest logit of every token folded
+            // into the token's argmax key: the 16 rows of a token are 16
+            // consecutive lanes of one warp (16 * M <= 256 outputs, one pass)
+            const int o = threadIdx.x, m = o >> 4, i = o & 15;
+            unsigned long long key = 0ull;
+            if (o < 16 * a.M && row0 + i < N) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) v += red[((w * NB + (m >> 3)) * 16 + i) * 8 + (m & 7)];
+                if (a.y32) a.y32[size_t(m) * a.y_stride + row0 + i] = v;
+                key = argmax_key(v, row0 + i);
+            }
+            if (o < ((16 * a.M + 31) & ~31)) {
+#pragma unroll
+                for (int d = 8; d >= 1; d >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, d);
+                    key = other > key ? other : key;
+                }
+                if (i == 0 && o < 16 * a.M) atomicMax(a.amax + m, key);
+            }
         } else {
             for (int o = threadIdx.x; o < 8 * a.M; o += kWarps * 32) {
                 const int m = o >> 3, j = o & 7;
@@ -398,6 +436,29 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
         named_barrier_compute();
     }
     if (!ok && lane == 0) atomicOr(&g_device_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+    if (RU == 3) {
+        // The last CTA to finish turns the keys into rows and logits and
+        // leaves keys and counter at zero for the next call (every CTA
+        // counts itself, also after a timeout, so the count stays exact).
+        __shared__ int s_last;
+        named_barrier_compute();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = atomicAdd(a.done, 1ull) == gridDim.x - 1;
+        }
+        named_barrier_compute();
+        if (s_last) {
+            __threadfence();
+            for (int m = threadIdx.x; m < a.M; m += kWarps * 32) {
+                const unsigned long long key = __ldcg(a.amax + m);
+                const unsigned ord = unsigned(key >> 32);
+                a.idx[m] = int32_t(~unsigned(key & 0xffffffffu));
+                if (a.maxval) a.maxval[m] = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+                a.amax[m] = 0ull;
+            }
+            if (threadIdx.x == 0) *a.done = 0ull;
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -498,6 +559,40 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
             e = gate_up ? tc::launch_t<2, 2>(mc, ms, a, s) : tc::launch_t<2, 1>(mc, ms, a, s);
         else
             e = gate_up ? tc::launch_t<1, 2>(mc, ms, a, s) : tc::launch_t<1, 1>(mc, ms, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
+                                    int32_t *idx, float *maxval, unsigned long long *work, int M, int N, int K,
+                                    cudaStream_t s)
+{
+    CUtensorMap mc, ms;
+    cudaError_t e = tc::make_maps(wq, scales, N, K, &mc, &ms);
+    if (e != cudaSuccess) return e;
+    TcArgs a;
+    a.wq = wq;
+    a.scales = scales;
+    a.y = nullptr;
+    a.N = N;
+    a.K = K;
+    a.tiles = (N + 15) / 16;
+    a.y_stride = N;
+    const bool fit16 = tc::smem_bytes<2>(16, K) <= 220 * 1024;
+    for (int m0 = 0, blk = 0; m0 < M; ++blk) {
+        const int rem = M - m0;
+        const int nb = (rem > 8 && fit16) ? 2 : 1;
+        const int mt = std::min(rem, 8 * nb);
+        a.x = x + size_t(m0) * K;
+        a.y32 = y32 ? y32 + size_t(m0) * N : nullptr;
+        a.amax = work + m0;
+        a.done = work + M + blk;                 // one counter per block of tokens (at most 8 blocks)
+        a.idx = idx + m0;
+        a.maxval = maxval ? maxval + m0 : nullptr;
+        a.M = mt;
+        e = nb == 2 ? tc::launch_t<2, 3>(mc, ms, a, s) : tc::launch_t<1, 3>(mc, ms, a, s);
         if (e != cudaSuccess) return e;
         m0 += mt;
     }

@@ -44,6 +44,11 @@ struct TcArgs {
     int M, N, K;
     int tiles;          // 16-row tiles of W
     int y_stride;       // elements between output rows
+    float *y32;                     // fp32 logits [M][y_stride] (argmax epilogue; may be null)
+    unsigned long long *amax;       // [M] argmax keys (argmax epilogue; zero on entry, left zero)
+    unsigned long long *done;       // CTAs finished (argmax epilogue; zero on entry, left zero)
+    int32_t *idx;                   // [M] argmax rows, written by the last CTA
+    float *maxval;                  // [M] argmax logits or null, written by the last CTA
 };
 
 size_t smem_per_sm();      // shared memory per SM of the current device (cached)
@@ -52,6 +57,12 @@ size_t smem_per_sm();      // shared memory per SM of the current device (cached
 bool decode_tc_supported(int M, int K);
 cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
                              uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
+// fp32 logits (y32 may be null) and the per-token argmax in the same launch
+// (per block of tokens): work = [M] keys then 8 counters, zero on entry and
+// left zero
+cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
+                                    int32_t *idx, float *maxval, unsigned long long *work, int M, int N, int K,
+                                    cudaStream_t s);
 cudaError_t read_device_error(unsigned *flags, bool clear);
 
 // zq4_decode_seg.cu: decode GEMV / gate_up on the segmented layout, M <= 8

@@ -37,7 +37,8 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg")
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
+           "zq4_gemv_argmax")
 
 
 class Zq4Error(RuntimeError):
@@ -65,6 +66,7 @@ def _load():
     lib.zq4_device_errors.restype = I
     sig = {
         "zq4_gemv": [P, P, P, P, I, I, I, P],
+        "zq4_gemv_argmax": [P, P, P, P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu": [P, P, P, P, I, I, I, P],
         "zq4_moe_gemv": [P, P, I, P, P, I, I, I, P, P, I, I, P, P],
         "zq4_prepare_weight": [P, P, P, P, I, I, I, P],
@@ -141,6 +143,30 @@ def gemv(wq, scales, x, N, K, y=None, stream=None):
     _check("zq4_gemv", lib.zq4_gemv(w, s, _ptr(x, "x", M * K * 2, 2), _ptr(y, "y", M * N * 2, 2),
                                     M, N, K, _stream(stream)))
     return y
+
+
+def gemv_argmax(wq, scales, x, N, K, y32=None, logits=True, maxval=None, idx=None, work=None, stream=None):
+    """LM-head step: fp32 logits y32[M, N] (unless logits=False) and, per
+    token, the index of the largest logit (lowest index on ties) and that
+    logit. Returns (idx int32 [M], maxval float32 [M], y32 or None). A given
+    `work` (int64 [M + 8]) must be all zero before its first call; every
+    call leaves it zero."""
+    M = x.numel() // K
+    dev = x.device
+    if logits and y32 is None:
+        y32 = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if idx is None:
+        idx = torch.empty((M,), dtype=torch.int32, device=dev)
+    if maxval is None:
+        maxval = torch.empty((M,), dtype=torch.float32, device=dev)
+    if work is None:
+        work = torch.zeros((M + 8,), dtype=torch.int64, device=dev)   # zero before the first call
+    w, s = _mat(wq, scales, N, K)
+    _check("zq4_gemv_argmax",
+           lib.zq4_gemv_argmax(w, s, _ptr(x, "x", M * K * 2, 2), _ptr(y32, "y32", M * N * 4, 4) if logits else None,
+                               _ptr(idx, "idx", M * 4, 4), _ptr(maxval, "maxval", M * 4, 4),
+                               _ptr(work, "work", (M + 8) * 8, 8), M, N, K, _stream(stream)))
+    return idx, maxval, (y32 if logits else None)
 
 
 def gate_up_silu(wq, scales, x, N2, K, h=None, stream=None):

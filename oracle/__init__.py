@@ -80,6 +80,7 @@ def _load(mutant: int = 0):
         lib.zo_moe_down_combine.argtypes = [_p, _p, _i64, _p, _p, _i64, _i64, _i64, _p,
                                             _i64, _p, _p]
         lib.zo_moe_down_combine.restype = _i64
+        lib.zo_argmax.argtypes = [_p, _i64, _i64, _p]
         lib.zo_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -185,6 +186,16 @@ class Oracle:
         bad = self.lib.zo_moe_down_combine(_ptr(wq), _ptr(sc), E, _ptr(hh), _ptr(rr), T, N, K,
                                            _ptr(ids), top_k, _ptr(y), _ptr(S))
         return y, S, int(bad)
+
+    # --- LM head ------------------------------------------------------------
+    def argmax(self, y) -> np.ndarray:
+        """Per row of y [M, N] (taken as fp64): the lowest index of the largest
+        value, a NaN counting as the largest."""
+        yy = np.ascontiguousarray(np.atleast_2d(y), dtype=np.float64)
+        M, N = yy.shape
+        idx = np.empty(M, dtype=np.int32)
+        self.lib.zo_argmax(_ptr(yy), M, N, _ptr(idx))
+        return idx
 
     def num_threads(self) -> int:
         return int(self.lib.zo_num_threads())

@@ -22,6 +22,8 @@
  *            Operations" (fused_dequantize + NT_matmul; split + SiLU +
  *            multiply) and "Matmul Shader Analysis" (one output element is a
  *            dot product over all K of input * (code - 7) * group scale).
+ *  [DOC-ARGMAX] same page, "WGSL Kernel Roles": the LM-head matmul writes
+ *            f32 logits for a stable argmax (zo_argmax).
  *  [BENCH-MOE] "Zero-TVM benchmarks" (BENCH.md), section "MoE chunked
  *            prefill": per (token, slot) the expert index comes from the
  *            routing ids, experts never mix tokens, and a combine sums the
@@ -341,6 +343,31 @@ int64_t zo_moe_down_combine(const uint32_t *wq_bank, const uint16_t *sc_bank, in
         free(w);
     }
     return bad;
+}
+
+/*
+ * [DOC-ARGMAX] "Zero TVM Documentation", section "WGSL Kernel Roles": the
+ * LM-head matmul writes f32 logits and the argmax step picks the next token
+ * as the position of the largest one. Reading where the pages are silent:
+ * ties go to the lowest index, and a NaN counts as larger than any number
+ * (the first NaN wins). idx[m] = that position in row m of y [M][N].
+ */
+void zo_argmax(const double *y, int64_t M, int64_t N, int32_t *idx)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const double *row = y + m * N;
+        int64_t best = 0;
+        for (int64_t n = 1; n < N; ++n) {
+            const double v = row[n], b = row[best];
+            if (isnan(b)) break;                 /* a NaN already holds the place */
+#if ZO_MUTANT == 6
+            if (isnan(v) || v >= b) best = n;    /* mutant: ties to the highest index */
+#else
+            if (isnan(v) || v > b) best = n;
+#endif
+        }
+        idx[m] = (int32_t)best;
+    }
 }
 
 /* Threads the OpenMP regions above use (1 without OpenMP). */

@@ -335,6 +335,32 @@ def test_moe_invalid_ids_contribute_nothing(oracle):
     assert np.array_equal(y, y2)
 
 
+def test_argmax_hand_cases(oracle):
+    """The LM-head argmax on rows whose answer is fixed by the definition:
+    the position of the largest value, the lowest one on ties, a NaN above
+    every number, -inf below every finite number."""
+    nan, inf = float("nan"), float("inf")
+    rows = [
+        ([1.0, 3.0, 2.0], 1),
+        ([-5.0, -1.0, -3.0], 1),
+        ([2.0, 7.0, 7.0, 1.0, 7.0], 1),           # ties: lowest index
+        ([0.0, -0.0], 0),                         # equal values
+        ([-inf, -inf, -1e300], 2),
+        ([1.0, nan, 5.0, nan], 1),                # NaN counts as the largest
+        ([inf, 4.0, inf], 0),
+        ([4.0], 0),
+    ]
+    for vals, want in rows:
+        assert oracle.argmax(np.array([vals]))[0] == want, vals
+    # a brute-force check on random integer rows with many ties
+    rng = np.random.default_rng(7)
+    y = rng.integers(-3, 4, size=(50, 37)).astype(np.float64)
+    got = oracle.argmax(y)
+    for m in range(50):
+        mx = max(y[m])
+        assert got[m] == min(n for n in range(37) if y[m, n] == mx)
+
+
 # --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
@@ -346,12 +372,13 @@ def _pins_pass(o) -> bool:
         test_closed_form_constant_codes(o)
         test_silu_values(o)
         test_gate_up_brute_force(o)
+        test_argmax_hand_cases(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
