@@ -278,19 +278,22 @@ ZQ4_API zq4_status zq4_gate_up_silu_seg(const uint32_t *wseg, const uint16_t *x,
 
 /*
  * Decode step as one launch: an ordered list of projections ("jobs") run by
- * a persistent kernel, each job starting only after every output of the job
- * before it is written -- the dependency of a decode step, in which every
- * projection consumes the previous one's result. Source: "Zero TVM
- * Documentation", section "Decode loop" (the fixed per-token sequence of
- * dispatches) with the projections of cards 5 "int4 Matmul" and 6 "Fused
- * FFN"; each job computes exactly what zq4_gemv (gate_up = 0) or
- * zq4_gate_up_silu (gate_up = 1) computes.
+ * a persistent kernel, with the results of running them one after another.
+ * Source: "Zero TVM Documentation", section "Decode loop" (the fixed
+ * per-token sequence of dispatches) with the projections of cards 5 "int4
+ * Matmul" and 6 "Fused FFN"; each job computes exactly what zq4_gemv
+ * (gate_up = 0) or zq4_gate_up_silu (gate_up = 1) computes.
  *
  * Job: wq = the matrix in the segmented layout (zq4_prepare_weight with
  * ZQ4_PREP_SEGMENTED; it carries the scales, so `scales` must be NULL), x
  * [M, K] f16, y [M, N] f16 (or [M, N/2] for gate_up); device pointers,
  * caller-owned; K % 256 == 0, N even for gate_up; wq and x 16-byte aligned.
- * A job may read the y of an earlier job as its x.
+ * A job may read the y of an earlier job as its x, and may write over the x
+ * or y of an earlier job. Order is kept only where buffers meet: two jobs
+ * that touch the same bytes, one of them writing, run in the given order
+ * (the second waiting for the first), others may run in another order or
+ * at once. zq4_stack_plan_waits tells the order and the waits a plan uses.
+ * The weights are only read.
  */
 typedef struct zq4_stack_job {
     const uint32_t *wq;
@@ -321,6 +324,28 @@ typedef struct zq4_stack_plan {
  * shared memory).
  */
 ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
+
+/*
+ * zq4_stack_plan_waits -- the run order and the waits a plan of these jobs
+ * uses (host only: no device call; pointers are compared, never read). Two
+ * jobs conflict when they touch the same bytes and one of them writes them
+ * (y of one meets x or y of the other). Conflicting jobs keep their order;
+ * within that, a job that would wait for a job run shortly before it lets
+ * later jobs that conflict with nothing still to run go first, until about
+ * as much other work as that job's lies between the two.
+ *   order[r] = the index (in `jobs`) of the r-th job run;
+ *   dep[i]   = the job every CTA must have finished before job i starts, or
+ *              -1: the last one run before i that conflicts with it -- unless
+ *              that one feeds job i (x_i is exactly its y: same address, row
+ *              stride K_i, nothing else shared), then src[i] = it and each
+ *              256-column chunk c of x_i waits only for the CTAs that write
+ *              those columns, and dep[i] is the last conflicting job before it;
+ *   src[i]   = that feeding job, or -1.
+ * Indices refer to `jobs`. The arrays hold n_jobs ints, caller-owned.
+ * Errors: as zq4_stack_plan_bytes, and ZQ4_ERR_NULL for a NULL array.
+ */
+ZQ4_API zq4_status zq4_stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src,
+                                        int *dep);
 
 /*
  * zq4_stack_plan_init -- write the plan into `dev` (256-byte aligned, at
@@ -358,7 +383,7 @@ ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
  * zq4_stack_plan_init, and the plan it fills runs with zq4_stack_run.
  *
  * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
- * 64 KiB array, i.e. at most 1257 jobs; a longer list returns
+ * 64 KiB array, i.e. at most 1218 jobs; a longer list returns
  * ZQ4_ERR_UNSUPPORTED and changes nothing. What must start at zero (the
  * plan's launch counter, abort flag and per-job counters) is cleared by
  * every call. The first call on a device resolves the array's address

@@ -79,9 +79,12 @@ namespace st {
 
 constexpr int kWarps = 12;                  // compute warps, one ring each
 constexpr int kCompute = kWarps * 32;
-constexpr int kThreads = kCompute + 32;      // + the copy warp
+constexpr int kCopyWarp = kWarps, kXWarp = kWarps + 1;
+constexpr int kThreads = kCompute + 64;      // + the copy warp + the x warp
+constexpr int kMaxChunks = 64;               // 256-column chunks of x: K <= 16384
+constexpr int kXBatch = 12;                 // x rows in flight per lane of the x warp
+constexpr int kMaxGrid = 256;                // CTAs whose done flags a plan holds
 constexpr int kSlots = 5;
-constexpr int kEarly = 2;   // x chunks (16 B) per thread read before the job barrier
 using namespace segk;       // segment layout, inner loop, split-tile sums
 
 struct Header {
@@ -91,28 +94,50 @@ struct Header {
     unsigned pad[29];
 };
 
-constexpr int kJobGateUp = 1;   // rows are interleaved gate/up pairs: silu(g) * u output
-constexpr int kJobXEarly = 2;   // x is not written by an earlier job: it may be read at any time
+// Job::flags: bit 0 gate_up (rows are interleaved gate/up pairs, silu(g) * u
+// output); bits 8.. the earlier job d + 1 that every CTA must be done with
+// before x of this job is staged (0: none).
+constexpr int kJobGateUp = 1;
+constexpr int kDepShift = 8;
 
+// Tile t of a job (16 output rows) is CTA (t + off) mod G's: the tiles of
+// consecutive jobs are dealt round the CTAs as one sequence (off = the tiles
+// of the earlier jobs, mod G), so a CTA that drew a tile more in one job draws
+// its next only after every other CTA has, and the work of a run of jobs is
+// even to within one tile across the CTAs whatever the sizes of the jobs.
 struct alignas(16) Job {
     const uint8_t *seg; // the matrix in the segmented layout
     const uint16_t *x;  // [M][K]
-    uint16_t *y;        // [M][y_stride]
-    int N, K, T, S;
-    int flags, y_stride;
+    uint16_t *y;        // [M][N] ([M][N / 2] for gate_up)
+    int N, K, T, off;
+    int flags;
+    int src;            // x is exactly the output of job src (chunk-wise wait on it), or -1
 };
+__host__ __device__ inline int y_stride(const Job &jb) { return (jb.flags & 1) ? jb.N / 2 : jb.N; }
+
+// This CTA's tiles of a job: t0, t0 + G, .. (nt of them).
+__device__ __forceinline__ void cta_tiles(const Job &jb, int cta, int G, int &t0, int &nt)
+{
+    int d = cta - jb.off;
+    if (d < 0) d += G;
+    t0 = d;
+    nt = d < jb.T ? (jb.T - 1 - d) / G + 1 : 0;
+}
 
 struct Params {
     Header *hdr;
     const Job *jobs;
-    unsigned *job_cnt;   // [n_jobs]
+    unsigned *job_cnt;            // [n_jobs]: CTAs done with each job (monotone)
+    unsigned long long *flags;    // [kMaxGrid]: per CTA, (launch + 1) << 32 | (last job done + 1)
     int n_jobs, M, max_k;
+    int x_bufs;          // x buffers in shared memory (1 .. kMaxXBufs)
     int cached;          // jobs [0, cached) are copied to shared memory at start
 };
 
 constexpr size_t kRingOff = 0;
 constexpr size_t kBarOff = kRingOff + size_t(kWarps) * kSlots * kSegBytes;
-constexpr size_t kMiscOff = kBarOff + 2 * size_t(kWarps) * kSlots * 8;   // full, then empty barriers
+constexpr size_t kXCntOff = kBarOff + 2 * size_t(kWarps) * kSlots * 8;  // full, then empty barriers
+constexpr size_t kMiscOff = kXCntOff + (kMaxChunks + 4) * 4;            // chunk counters, then "x free"
 // Warp partials: slot [kWarps*2], each [kTokCols][kParkRow] floats (token
 // major, rows padded to 17 so that the 16 rows of one token, read by 16
 // lanes, fall in distinct banks).
@@ -124,10 +149,21 @@ constexpr int kTabInts = 2 * (kWarps + 1) + 2;                       // one job:
 constexpr size_t kXsOff = kTabOff + (2 * kTabInts * 4 + 15) / 16 * 16;
 __host__ __device__ inline size_t xs_bytes(int M, int max_k) { return (size_t(M) * xs_row_bytes(max_k) + 15) / 16 * 16; }
 __host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + xs_bytes(M, max_k); }
+// x buffers: as many as fit (up to kMaxXBufs) next to room for 64 cached
+// jobs, so that x of the next jobs is staged while this one computes
+constexpr int kMaxXBufs = 4;
+inline int x_buffers(int M, int max_k)
+{
+    int nb = 1;
+    while (nb < kMaxXBufs && smem_bytes(M, max_k) + nb * xs_bytes(M, max_k) + 64 * sizeof(Job) <= size_t(227) * 1024)
+        ++nb;
+    return nb;
+}
+inline size_t smem_fixed(int M, int max_k) { return smem_bytes(M, max_k) + (x_buffers(M, max_k) - 1) * xs_bytes(M, max_k); }
 // jobs that fit in shared memory next to everything else (the rest are read from the plan)
 inline int cached_jobs(int n, int M, int max_k)
 {
-    const size_t left = size_t(227) * 1024 - smem_bytes(M, max_k);
+    const size_t left = size_t(227) * 1024 - smem_fixed(M, max_k);
     return int(std::min<size_t>(size_t(n), left / sizeof(Job)));
 }
 
@@ -164,7 +200,7 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 // pass; `shift` = log2 of the outputs per tile rounded up to a power of
 // two, so no division. `wtab` = the warp range starts (kWarps + 1 entries)
 // then each warp's first tile.
-__device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_up, int M, int N, int y_stride,
+__device__ __forceinline__ void sum_split_tiles(int t0, int G, int nt, int S, int gate_up, int M, int N, int y_stride,
                                                 uint16_t *y, const float *wpark, const int *wtab)
 {
     const int per_tok = gate_up ? 8 : 16, tok_shift = gate_up ? 3 : 4;
@@ -179,7 +215,7 @@ __device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_
     for (int it = threadIdx.x; it < (nt << shift); it += kCompute) {
         const int o = it & ((1 << shift) - 1);
         if (o >= outs) continue;
-        const int tt = tb + (it >> shift), lo = tt * S, hi = lo + S;
+        const int tt = it >> shift, lo = tt * S, hi = lo + S;      // local tile tt is tile t0 + tt G
         const int m = o >> tok_shift, i = o & (per_tok - 1), ra = gate_up ? 2 * i : i;
         // every warp's parked value is read (all loads in flight at once);
         // those of warps not holding part of tile tt are added as +0, which
@@ -202,7 +238,7 @@ __device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_
             v0 += in[w] ? p0[w] : 0.f;
             v1 += in[w] ? p1[w] : 0.f;
         }
-        const int row0 = tt * 16;
+        const int row0 = (t0 + tt * G) * 16;
         if (!gate_up) {
             if (row0 + i < N) y[size_t(m) * y_stride + row0 + i] = float_to_f16_bits(v0);
         } else if (row0 + 2 * i + 1 < N) {
@@ -213,16 +249,58 @@ __device__ __forceinline__ void sum_split_tiles(int tb, int nt, int S, int gate_
 
 // x chunk i of M*K/8 (16 bytes of token i / (K/8)) into its staged place,
 // pair-permuted as the unpack produces: (x0,x4),(x1,x5),(x2,x6),(x3,x7)
-__device__ __forceinline__ void put_x(uint8_t *xs, uint32_t xrow, int words, int i, uint4 v)
+// x chunk of 8 values as the (x0,x4),(x1,x5),(x2,x6),(x3,x7) pairs the unpack produces
+__device__ __forceinline__ uint4 pair_perm(uint4 v)
 {
-    const int m = i / words, cw = i - m * words;
     uint4 o;
     o.x = __byte_perm(v.x, v.z, 0x5410);
     o.y = __byte_perm(v.x, v.z, 0x7632);
     o.z = __byte_perm(v.y, v.w, 0x5410);
     o.w = __byte_perm(v.y, v.w, 0x7632);
-    *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
+    return o;
 }
+
+// Monotone counters in shared memory between the x warp and the compute
+// warps (release / acquire at CTA scope).
+__device__ __forceinline__ void st_release_cta(int *p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+// Wait (bounded) until *p >= v; false once the wait has lasted longer than
+// kWaitLimitNs. Between polls the warp sleeps, leaving its issue slots to the
+// warps that do the work.
+__device__ __forceinline__ bool wait_at_least(const int *p, int v)
+{
+    if (ld_acquire_cta(p) >= v) return true;
+    const unsigned long long t0 = globaltimer();
+    for (unsigned i = 0;; ++i) {
+        __nanosleep(32);
+        if (ld_acquire_cta(p) >= v) return true;
+        if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Flags are polled with relaxed loads, all in flight at once; one
+// fence.acq_rel.gpu after the polls that saw a release makes it an acquire.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
+{
+    unsigned long long r;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
+{
+    unsigned r;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
 {
@@ -233,24 +311,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const int r = lane >> 2, t = lane & 3;
     const int G = gridDim.x, cta = blockIdx.x;
     const uint32_t full0 = sbase + uint32_t(kBarOff), empty0 = full0 + uint32_t(kWarps * kSlots * 8);
+    // s_chunk[c]: jobs whose x chunk c is staged; s_xfree: jobs the compute
+    // warps are done with (so x of the next one may be staged)
+    int *s_chunk = reinterpret_cast<int *>(smem + kXCntOff);
+    int *s_xfree = s_chunk + kMaxChunks;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kMiscOff);
+    // the compute warps' copy of the abort flag, written by thread 0 before a
+    // compute barrier and read by all of them after it: the other warps may set
+    // s_abort at any time, and every compute warp must take the same branch
+    volatile int *s_cbrk = s_abort + 1;
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
-    uint8_t *xs = smem + kXsOff;
-    Job *sjobs = reinterpret_cast<Job *>(smem + kXsOff + xs_bytes(p.M, p.max_k));
+    uint8_t *xs = smem + kXsOff;                       // x of job j: xs + (j % x_bufs) * xs_size
+    const int xs_size = int(xs_bytes(p.M, p.max_k));
+    Job *sjobs = reinterpret_cast<Job *>(smem + kXsOff + p.x_bufs * xs_bytes(p.M, p.max_k));
     const uint32_t xrow = uint32_t(xs_row_bytes(p.max_k));
     const int n = p.n_jobs, M = p.M;
     const unsigned launch = *reinterpret_cast<volatile unsigned *>(&p.hdr->epoch);
     const unsigned target = (launch + 1u) * unsigned(G);
+    const unsigned long long tag = static_cast<unsigned long long>(launch + 1u) << 32;
 
-    if (threadIdx.x == 0) *s_abort = 0;
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        *s_cbrk = 0;
+        for (int c = 0; c < kMaxChunks; ++c) s_chunk[c] = 0;
+        *s_xfree = 0;
+    }
     if (warp < kWarps && lane == 0) {
         for (int j = 0; j < kSlots; ++j) {
             mbar_init(full0 + 8 * (warp * kSlots + j), 1);    // the copy's bytes
             mbar_init(empty0 + 8 * (warp * kSlots + j), 1);   // the consuming warp is done
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     {
         // the job table (or its first p.cached entries) into shared memory
         const uint4 *src = reinterpret_cast<const uint4 *>(p.jobs);
@@ -261,34 +354,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     __syncthreads();
     auto job = [&](int j) -> const Job & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
 
-    // compute warp w's segment range of a job: CTA part of the job, then
-    // warp part (CTA ranges are whole tiles, so a tile never spans two CTAs)
-    auto warp_range = [&](int T, int S, int w, int &ub, int &ue) {
-        int tb, te;
-        split(0, T, cta, G, tb, te);
-        split(tb * S, te * S, w, kWarps, ub, ue);
+    // compute warp w's part of this CTA's segments of a job, numbered tile
+    // major over the CTA's tiles (local segment u: tile t0 + (u / S) G,
+    // column segment u % S); a tile never spans two CTAs
+    auto warp_range = [&](const Job &jb, int w, int &ub, int &ue, int &t0) {
+        int nt;
+        cta_tiles(jb, cta, G, t0, nt);
+        split(0, nt * (jb.K >> 8), w, kWarps, ub, ue);
     };
 
-    if (warp == kWarps) {
+    if (warp == kCopyWarp) {
         // ---------------- the copy warp ----------------
         // Lane w keeps ring w full: it walks compute warp w's (job, segment)
-        // sequence (segment u of a job, tile major, is at byte u * kSegBytes
-        // of its matrix) and refills a slot as soon as that warp has released
-        // it, across job boundaries: the weights never depend on earlier jobs.
+        // sequence (segment sg of tile t of a job is at byte (t S + sg) *
+        // kSegBytes of its matrix) and refills a slot as soon as that warp
+        // has released it, across job boundaries: the weights never depend on
+        // earlier jobs.
         const int w = lane;
         const uint32_t ring = sbase + uint32_t(kRingOff) + uint32_t(w * kSlots * kSegBytes);
-        int it_j = n, it_u = 0, it_e = 0, issued = 0;
-        const uint8_t *it_seg = nullptr;
+        int it_j = n, it_left = 0, it_S = 1, it_sg = 0, issued = 0;
+        const uint8_t *it_ptr = nullptr;          // the next segment
         auto seek = [&](int j) {
             for (; j < n; ++j) {
                 const Job &jb = job(j);
-                int ub, ue;
-                warp_range(jb.T, jb.S, w, ub, ue);
+                int ub, ue, t0;
+                warp_range(jb, w, ub, ue, t0);
                 if (ub < ue) {
+                    const int S = jb.K >> 8, k = ub / S;
                     it_j = j;
-                    it_u = ub;
-                    it_e = ue;
-                    it_seg = jb.seg;
+                    it_left = ue - ub;
+                    it_S = S;
+                    it_sg = ub - k * S;
+                    it_ptr = jb.seg + (size_t(t0 + k * G) * S + it_sg) * kSegBytes;
                     return;
                 }
             }
@@ -305,10 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 const uint32_t full = full0 + 8 * (w * kSlots + slot);
                 if (f == 0 || mbar_test(empty0 + 8 * (w * kSlots + slot), (f - 1) & 1)) {
                     mbar_arrive_expect_tx(full, kSegBytes);
-                    bulk_load(ring + slot * kSegBytes, it_seg + size_t(it_u) * kSegBytes, kSegBytes, full);
+                    bulk_load(ring + slot * kSegBytes, it_ptr, kSegBytes, full);
                     ++issued;
                     did = true;
-                    if (++it_u >= it_e) seek(it_j + 1);
+                    if (--it_left == 0) {
+                        seek(it_j + 1);
+                    } else if (++it_sg == it_S) {       // next tile of this CTA: G tiles on
+                        it_sg = 0;
+                        it_ptr += (size_t(G - 1) * it_S + 1) * kSegBytes;
+                    } else {
+                        it_ptr += kSegBytes;
+                    }
                 }
             }
             if (!__any_sync(0xffffffffu, more)) break;
@@ -333,6 +437,161 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         if (w < kWarps)
             for (int c = max(0, issued - kSlots); c < issued; ++c)
                 if (!mbar_wait(full0 + 8 * (w * kSlots + c % kSlots), (c / kSlots) & 1)) break;
+    } else if (warp == kXWarp) {
+        // ---------------- the x warp ----------------
+        // Stages x of every job into shared memory, one 256-column chunk at a
+        // time, after the wait the host derived for the job from the buffers
+        // (Job::flags): none when the job touches no buffer an earlier job
+        // writes or reads; "all CTAs done with job d" for the last such job d;
+        // and when x is exactly the previous job's output, per chunk, "the
+        // CTAs that produce those columns of the previous job are done", so
+        // compute warps start on the chunks already there instead of waiting
+        // for the whole previous job. s_chunk[c] = j + 1 once chunk c of job
+        // j is staged (monotone, so a fast compute warp can never mistake an
+        // earlier job's chunk for this one's).
+        bool stop = false;
+        for (int j = 0; j < n && !stop; ++j) {
+            const Job &jb = job(j);
+            // the compute warps are past the job that last used this buffer
+            if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs)) {
+                stop = true;
+                break;
+            }
+            uint8_t *xsj = xs + (j % p.x_bufs) * xs_size;
+            const int nch = jb.K >> 8, words = jb.K >> 3;
+            const int dep = (jb.flags >> kDepShift) - 1;
+            unsigned long long t0 = globaltimer();
+            if (dep >= 0 && lane == 0) {
+                // every CTA is done with job dep
+                for (;;) {
+                    if (ld_relaxed_u32(&p.job_cnt[dep]) >= target) break;
+                    if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                        stop = true;
+                        break;
+                    }
+                }
+                fence_acq_rel_gpu();
+            }
+            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+            __syncwarp();                        // lane 0's acquire before every lane's loads of x
+            // per chunk (lane l tracks chunks l and l + 32): the CTAs whose
+            // tiles [tlo, thi] of job src produce its columns, (t + off) mod G
+            // for each: one cyclic run of CTAs, as up to two ranges
+            // [olo[h][0], ohi[h][0]] and [olo[h][1], ohi[h][1]] (empty: hi < lo)
+            const bool elem = jb.src >= 0;
+            int olo[2][2] = {{0, 0}, {0, 0}}, ohi[2][2] = {{-1, -1}, {-1, -1}};
+            if (elem) {
+                const Job &pj = job(jb.src);
+                const int es = (pj.flags & kJobGateUp) ? 3 : 4;       // log2(outputs per 16-row tile)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int kc = lane + 32 * h;
+                    const int tlo = min(pj.T - 1, (kc * 256) >> es), thi = min(pj.T - 1, (kc * 256 + 255) >> es);
+                    const int len = thi - tlo + 1;
+                    if (len >= G) {
+                        ohi[h][0] = G - 1;
+                    } else {
+                        int o0 = tlo % G + pj.off;
+                        if (o0 >= G) o0 -= G;
+                        olo[h][0] = o0;
+                        ohi[h][0] = min(o0 + len - 1, G - 1);
+                        ohi[h][1] = o0 + len - 1 - G;
+                    }
+                }
+            }
+            const unsigned long long need = tag | unsigned(jb.src + 1);    // CTA done with job src
+            unsigned long long pending = nch >= 64 ? ~0ull : ((1ull << nch) - 1ull);
+            t0 = globaltimer();
+            while (pending && !stop) {
+                unsigned long long ready = pending;
+                if (elem) {
+                    // every CTA's flag once (all loads in flight together), as
+                    // bit sets of the CTAs done with job j-1
+                    unsigned long long fv[kMaxGrid / 32];
+#pragma unroll
+                    for (int q = 0; q < kMaxGrid / 32; ++q)
+                        fv[q] = q * 32 < G && q * 32 + lane < G ? ld_relaxed_u64(p.flags + q * 32 + lane) : 0ull;
+                    unsigned done[kMaxGrid / 32];
+#pragma unroll
+                    for (int q = 0; q < kMaxGrid / 32; ++q) done[q] = __ballot_sync(0xffffffffu, fv[q] >= need);
+                    bool rdy[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        bool all = true;
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+#pragma unroll
+                            for (int q = 0; q < kMaxGrid / 32; ++q) {
+                                const int lo = max(olo[h][g], 32 * q), hi = min(ohi[h][g], 32 * q + 31);
+                                if (lo <= hi) {
+                                    const unsigned want =
+                                        hi - lo == 31 ? 0xffffffffu : ((1u << (hi - lo + 1)) - 1u) << (lo - 32 * q);
+                                    all = all && (done[q] & want) == want;
+                                }
+                            }
+                        rdy[h] = all;
+                    }
+                    ready &= (unsigned long long)__ballot_sync(0xffffffffu, rdy[0]) |
+                             ((unsigned long long)__ballot_sync(0xffffffffu, rdy[1]) << 32);
+                }
+                if (ready) {
+                    if (elem) {
+                        fence_acq_rel_gpu();     // the polls that saw the flags become acquires
+                        __syncwarp();
+                    }
+                    // stage the ready chunks, kXBatch (chunk, token) rows of 512
+                    // bytes in flight at a time; lane l moves bytes 16l.. of each
+                    unsigned long long rem = ready;
+                    int ck = __ffsll(rem) - 1, cm = 0;
+                    const uint4 *xg = reinterpret_cast<const uint4 *>(jb.x) + lane;
+                    while (rem) {
+                        int qc[kXBatch];                  // chunk | token << 8, or -1
+#pragma unroll
+                        for (int q = 0; q < kXBatch; ++q) {
+                            qc[q] = -1;
+                            if (rem) {
+                                qc[q] = ck | (cm << 8);
+                                if (++cm == M) {
+                                    cm = 0;
+                                    rem &= rem - 1;
+                                    ck = __ffsll(rem) - 1;
+                                }
+                            }
+                        }
+                        uint4 v[kXBatch];
+#pragma unroll
+                        for (int q = 0; q < kXBatch; ++q)
+                            if (qc[q] >= 0) v[q] = __ldcg(xg + (qc[q] >> 8) * words + (qc[q] & 255) * 32);
+#pragma unroll
+                        for (int q = 0; q < kXBatch; ++q)
+                            if (qc[q] >= 0)
+                                *reinterpret_cast<uint4 *>(xsj + (qc[q] >> 8) * int(xrow) + ((qc[q] & 255) * 32 + lane) * 16) =
+                                    pair_perm(v[q]);
+                    }
+                    __syncwarp();
+                    // lane l publishes chunks l and l + 32
+                    if ((ready >> lane) & 1ull) st_release_cta(s_chunk + lane, j + 1);
+                    if ((ready >> (lane + 32)) & 1ull) st_release_cta(s_chunk + lane + 32, j + 1);
+                    pending &= ~ready;
+                    t0 = globaltimer();
+                } else {
+                    if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                        stop = true;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            // when stopping, the chunks never staged are released too, so that
+            // no compute warp waits on them (the results are void then)
+            if (stop && lane == 0)
+                for (int kc = 0; kc < kMaxChunks; ++kc) st_release_cta(s_chunk + kc, 1 << 30);
+        }
+        if (stop && lane == 0) {
+            atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+            atomicOr(&p.hdr->abort, 1u);
+            *s_abort = 1;
+        }
     } else {
         // ---------------- compute warps ----------------
         const uint32_t ring0 = sbase + uint32_t(kRingOff) + uint32_t(warp * kSlots * kSegBytes);
@@ -341,33 +600,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         ldm_offsets(lane, ldm_off);
         const uint8_t *xr = xs + size_t(min(r, M - 1)) * xrow + 16 * t;
 
-        // stage x of a job synchronously (compute threads; caller barriers)
-        auto stage_now = [&](const Job &jb, int from) {
-            const int words = jb.K >> 3, total = M * words;
-            for (int i0 = from + int(threadIdx.x); i0 < total; i0 += 2 * kCompute) {
-                uint4 v0, v1;
-                const int i1 = i0 + kCompute;
-                v0 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i0);
-                if (i1 < total) v1 = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i1);
-                put_x(xs, xrow, words, i0, v0);
-                if (i1 < total) put_x(xs, xrow, words, i1, v1);
-            }
-        };
         // the warp range table of job j (one of two buffers, so that the table
         // of the next job can be made while the sums of the last one read theirs):
         // lanes 0..kWarps of warp `tw`
         auto set_wtab = [&](const Job &jb, int j, int tw) {
             const int q = int(threadIdx.x) - 32 * tw;
             if (q >= 0 && q <= kWarps) {
-                int tb0, te0;
-                split(0, jb.T, cta, G, tb0, te0);
-                const int b = part_begin(tb0 * jb.S, te0 * jb.S, q, kWarps);
+                int t0, nt;
+                cta_tiles(jb, cta, G, t0, nt);
+                const int S = jb.K >> 8;
+                const int b = part_begin(0, nt * S, q, kWarps);
                 int *tab = wtab + (j & 1) * kTabInts;
-                tab[q] = b;
-                tab[kWarps + 1 + q] = b / jb.S;
+                tab[q] = b;                           // local segments, tile major
+                tab[kWarps + 1 + q] = b / S;          // local tile
                 if (q == 0) {
-                    tab[2 * (kWarps + 1)] = tb0;      // this CTA's tiles of the job
-                    tab[2 * (kWarps + 1) + 1] = te0;
+                    tab[2 * (kWarps + 1)] = t0;       // this CTA's tiles of the job: t0, t0 + G, ..
+                    tab[2 * (kWarps + 1) + 1] = nt;
                 }
             }
         };
@@ -375,84 +623,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         bool ok = true;
         int slot = 0;             // ring position of the next segment and the parity of its fill
         uint32_t phase = 0;
+        set_wtab(job(0), 0, 0);
+        compute_sync();
         for (int j = 0; j < n; ++j) {
             const Job &jb = job(j);
-            if (j == 0) {
-                set_wtab(jb, 0, 0);
-                stage_now(jb, 0);
-                compute_sync();
-            } else {
-                // every compute warp of this CTA is done with job j-1 (x
-                // buffer free, partial tiles parked)
-                compute_sync();
-                const bool early = (jb.flags & kJobXEarly) != 0 && !*s_abort;
-                const int words = jb.K >> 3, total = M * words;
-                uint4 xv[kEarly];
-                const Job &pj = job(j - 1);
-                if (!*s_abort) {
-                    const int *ptab = wtab + ((j - 1) & 1) * kTabInts;
-                    const int ptb = ptab[2 * (kWarps + 1)], pte = ptab[2 * (kWarps + 1) + 1];
-                    sum_split_tiles(ptb, pte - ptb, pj.S, pj.flags & kJobGateUp, M, pj.N, pj.y_stride, pj.y, wpark,
-                                    ptab);
-                }
-                compute_sync();      // finalize writes before the release below
-                set_wtab(jb, j, 1);  // warp 1, while thread 0 waits at the grid barrier
-                if (threadIdx.x == 0 && !*s_abort) {
-                    // release: this CTA's outputs of job j-1 become visible with the increment
-                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j - 1]) : "memory");
-                }
-                if (early) {
-                    // read now (thread 0 after its release, which would otherwise wait
-                    // for these loads), stored after the grid barrier: the latency hides
-                    // behind it
-#pragma unroll
-                    for (int e = 0; e < kEarly; ++e) {
-                        const int i = int(threadIdx.x) + e * kCompute;
-                        if (i < total) xv[e] = __ldcg(reinterpret_cast<const uint4 *>(jb.x) + i);
-                    }
-                }
-                if (threadIdx.x == 0 && !*s_abort) {
-                    const unsigned long long t0 = globaltimer();
-                    for (;;) {
-                        if (ld_acquire(&p.job_cnt[j - 1]) >= target) break;
-                        if (*reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
-                            globaltimer() - t0 > kWaitLimitNs) {
-                            atomicOr(&p.hdr->abort, 1u);
-                            *s_abort = 1;
-                            break;
-                        }
-                    }
-                }
-                if (early) {
-                    // the loads were issued before the poll: stored only now
-#pragma unroll
-                    for (int e = 0; e < kEarly; ++e) {
-                        const int i = int(threadIdx.x) + e * kCompute;
-                        if (i < total) put_x(xs, xrow, words, i, xv[e]);
-                    }
-                    if (total > kEarly * kCompute) stage_now(jb, kEarly * kCompute);
-                }
-                compute_sync();
-                if (*s_abort) {
-                    ok = false;
-                    break;
-                }
-                if (!early) {
-                    stage_now(jb, 0);
-                    compute_sync();
-                }
-            }
-
-            const int S = jb.S, gate_up = jb.flags & kJobGateUp;
+            const int S = jb.K >> 8, gate_up = jb.flags & kJobGateUp;
             const int *tab = wtab + (j & 1) * kTabInts;
             const int ub = tab[warp], ue = tab[warp + 1], first_tile = tab[kWarps + 1 + warp];
+            const int ct0 = tab[2 * (kWarps + 1)];   // local tile k is tile ct0 + k G
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             int cur_tile = -1;
             auto flush = [&](int tt) {
                 if (tt * S >= ub && (tt + 1) * S <= ue)
-                    write_tile(acc, tt * 16, lane, gate_up, M, jb.N, jb.y_stride, jb.y);
-                else        // part of a tile shared with other warps: summed at job end
-                {
+                    write_tile(acc, (ct0 + tt * G) * 16, lane, gate_up, M, jb.N, y_stride(jb), jb.y);
+                else {
                     // lane (r, t) holds rows r, r+8 of tokens 2t, 2t+1
                     float *pk = wpark + (warp * 2 + (tt == first_tile ? 0 : 1)) * kParkSlot;
 #pragma unroll
@@ -465,7 +649,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             };
 
             int tt = first_tile, sg = ub - first_tile * S;
-            for (int u = ub; u < ue; ++u) {
+            const uint8_t *xrj = xr + (j % p.x_bufs) * xs_size;
+            unsigned long long seen = 0;          // x chunks of this job known to be staged
+            for (int u = ub; u < ue && ok; ++u) {
+                // x chunk sg of this job (segment sg of a tile covers columns 256 sg ..)
+                if (!((seen >> sg) & 1ull)) {
+                    if (!__all_sync(0xffffffffu, wait_at_least(s_chunk + sg, j + 1))) {
+                        ok = false;
+                        break;
+                    }
+                    seen |= 1ull << sg;
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(bfull + 8 * slot, phase))) {
                     ok = false;
                     break;
@@ -474,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     if (cur_tile >= 0) flush(cur_tile);
                     cur_tile = tt;
                 }
-                accumulate(ring0 + slot * kSegBytes, ldm_off, xr + sg * 32 * 16, r, acc);
+                accumulate(ring0 + slot * kSegBytes, ldm_off, xrj + sg * 32 * 16, r, acc);
                 // every lane's reads of the slot (their values are in registers)
                 // are done before the copy warp may overwrite it
                 __syncwarp();
@@ -488,32 +682,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     ++tt;
                 }
             }
-            if (!ok) {
-                // leave together at the next job boundary: every compute warp
-                // must still take part in the barriers there
-                *s_abort = 1;
-                continue;
+            if (ok && cur_tile >= 0) flush(cur_tile);
+            if (!ok) *s_abort = 1;
+            compute_sync();                       // every compute warp is done with x and its segments
+            if (threadIdx.x == 0) st_release_cta(s_xfree, j + 1);
+            if (j + 1 < n) set_wtab(job(j + 1), j + 1, 1);
+            if (!*s_abort) {
+                const int *ptab = wtab + (j & 1) * kTabInts;
+                sum_split_tiles(ptab[2 * (kWarps + 1)], G, ptab[2 * (kWarps + 1) + 1], S, gate_up, M, jb.N, y_stride(jb),
+                                jb.y, wpark, ptab);
             }
-            if (cur_tile >= 0) flush(cur_tile);
-        }
-
-        if (!ok) {
-            if (lane == 0) {
-                atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
-                atomicOr(&p.hdr->abort, 1u);
+            if (threadIdx.x == 0) *s_cbrk = *s_abort;
+            compute_sync();                       // the split-tile sums before the release below
+            const bool brk = *s_cbrk != 0;
+            if (threadIdx.x == 0 && !brk) {
+                // release: this CTA's outputs of job j become visible with its flag
+                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.flags + cta), "l"(tag | unsigned(j + 1))
+                             : "memory");
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j]) : "memory");
             }
-            *s_abort = 1;
+            if (brk) break;
         }
-        compute_sync();
-        if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
-        if (!*s_abort && n > 0) {                            // the last job's split tiles
-            const Job &lj = job(n - 1);
-            const int *ltab = wtab + ((n - 1) & 1) * kTabInts;
-            sum_split_tiles(ltab[2 * (kWarps + 1)], ltab[2 * (kWarps + 1) + 1] - ltab[2 * (kWarps + 1)], lj.S,
-                            lj.flags & kJobGateUp, M, lj.N, lj.y_stride, lj.y, wpark, ltab);
+        if (!ok && lane == 0) {
+            atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+            atomicOr(&p.hdr->abort, 1u);
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0 && *s_abort) atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
     if (threadIdx.x == 0 && !*s_abort) {
         __threadfence();
         const unsigned d = atomicAdd(&p.hdr->done, 1u);
@@ -535,7 +731,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int stack_smem_set[kMaxDevices] = {};
 
 struct Layout {
-    size_t hdr, jobs, job_cnt, total;
+    size_t hdr, jobs, job_cnt, flags, total;
 };
 
 Layout layout_for(int n_jobs)
@@ -544,7 +740,8 @@ Layout layout_for(int n_jobs)
     l.hdr = 0;
     l.jobs = align_up(sizeof(st::Header), 128);
     l.job_cnt = l.jobs + size_t(n_jobs) * sizeof(st::Job);
-    l.total = align_up(l.job_cnt + size_t(n_jobs) * 4, 256);
+    l.flags = align_up(l.job_cnt + size_t(n_jobs) * 4, 16);
+    l.total = align_up(l.flags + size_t(st::kMaxGrid) * 8, 256);
     return l;
 }
 
@@ -552,12 +749,14 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
 {
     if (!jobs) return ZQ4_ERR_NULL;
     if (n_jobs <= 0 || M < 1 || M > st::kTokCols) return ZQ4_ERR_SHAPE;
+    if (grid > st::kMaxGrid) return ZQ4_ERR_UNSUPPORTED;      // more CTAs than the plan's done flags
     int mk = 0, mt = 0;
     for (int j = 0; j < n_jobs; ++j) {
         const zq4_stack_job &b = jobs[j];
         if (!b.wq || !b.x || !b.y) return ZQ4_ERR_NULL;
         if (b.scales) return ZQ4_ERR_FLAGS;     // the segmented layout carries the scales
         if (b.N <= 0 || b.K <= 0 || b.K % st::kSegCols != 0 || (b.gate_up && (b.N & 1))) return ZQ4_ERR_SHAPE;
+        if (b.K > st::kMaxChunks * st::kSegCols) return ZQ4_ERR_UNSUPPORTED;   // x staged in at most 64 chunks
         if (!aligned16(b.wq) || !aligned16(b.x) ||
             (reinterpret_cast<uintptr_t>(b.y) & 1))
             return ZQ4_ERR_ALIGN;
@@ -573,11 +772,116 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
     return ZQ4_OK;
 }
 
-// Device entry of job j. kJobXEarly: no earlier job's output overlaps x_j,
-// so the kernel may read x_j before the previous job has finished.
-st::Job make_job(const zq4_stack_job *jobs, int j, int M)
+// Byte ranges of a job's x and y.
+struct Span {
+    uintptr_t lo, hi;
+    bool meets(const Span &o) const { return lo < o.hi && o.lo < hi; }
+};
+inline Span x_span(const zq4_stack_job &b, int M)
 {
-    const zq4_stack_job &b = jobs[j];
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(b.x);
+    return {x0, x0 + size_t(M) * size_t(b.K) * 2};
+}
+inline Span y_span(const zq4_stack_job &b, int M)
+{
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(b.y);
+    return {y0, y0 + size_t(M) * size_t(b.gate_up ? b.N / 2 : b.N) * 2};
+}
+
+// Do jobs a and b touch the same bytes, one of them writing?
+bool conflict(const zq4_stack_job &a, const zq4_stack_job &b, int M)
+{
+    const Span xa = x_span(a, M), ya = y_span(a, M), xb = x_span(b, M), yb = y_span(b, M);
+    return ya.meets(xb) || ya.meets(yb) || xa.meets(yb);
+}
+
+// x of b is exactly the output of a (same address and row stride) and
+// that is all the two share.
+bool feeds(const zq4_stack_job &a, const zq4_stack_job &b, int M)
+{
+    return a.y == b.x && (a.gate_up ? a.N / 2 : a.N) == b.K && !x_span(a, M).meets(y_span(b, M)) &&
+           !y_span(a, M).meets(y_span(b, M));
+}
+
+constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
+
+// The order the kernel runs the jobs in and the wait before each. The
+// results are those of the given order: two jobs that conflict keep their
+// order. Within that, a job that would wait for a job run shortly before it
+// lets later jobs that conflict with no job still to place (it included)
+// and wait for nothing go first, until about as much other work as that
+// job's has been placed between the two: the CTAs that finish it early
+// work on those meanwhile instead of waiting for the last ones.
+//
+// Waits (positions in run order): dep[r] = the last job before r that
+// conflicts with it, which every CTA must have finished first; unless that
+// job feeds job r (feeds()), in which case src[r] = it (each 256-column
+// chunk of x waits only for the CTAs that write those columns) and dep[r]
+// is the last conflicting job before src[r]. -1: none.
+//
+// Scratch (n entries each) comes from the caller, so that this allocates
+// nothing: work, at (segments; total placed work right after placing a job)
+// and placed.
+struct SchedScratch {
+    long long *work, *at;
+    char *placed;
+};
+void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *src, int *dep, SchedScratch sc)
+{
+    long long *work = sc.work, *at = sc.at;
+    char *placed = sc.placed;
+    for (int i = 0; i < n; ++i) {
+        work[i] = (long long)((jobs[i].N + 15) / 16) * (jobs[i].K / st::kSegCols);
+        at[i] = -1;
+        placed[i] = 0;
+    }
+    int n_placed = 0;
+    long long total = 0;
+    // how much more work must be placed before job j runs without a wait on a recent job
+    auto short_by = [&](int j) {
+        long long need = 0;
+        for (int i = 0; i < n; ++i)
+            if (placed[i] && conflict(jobs[i], jobs[j], M)) need = std::max(need, work[i] - (total - at[i]));
+        return need;
+    };
+    int first = 0;
+    while (n_placed < n) {
+        while (placed[first]) ++first;
+        int pick = first;
+        if (short_by(first) > 0) {
+            for (int k = first + 1; k < n && k <= first + kLookAhead; ++k) {
+                if (placed[k]) continue;
+                bool free = true;
+                for (int i = first; i < k && free; ++i)
+                    if (!placed[i] && conflict(jobs[i], jobs[k], M)) free = false;
+                if (free && short_by(k) <= 0) {
+                    pick = k;
+                    break;
+                }
+            }
+        }
+        placed[pick] = 1;
+        total += work[pick];
+        at[pick] = total;
+        order[n_placed++] = pick;
+    }
+    for (int r = 0; r < n; ++r) {
+        src[r] = -1;
+        const zq4_stack_job &b = jobs[order[r]];
+        int q = r - 1;
+        while (q >= 0 && !conflict(jobs[order[q]], b, M)) --q;
+        if (q >= 0 && feeds(jobs[order[q]], b, M)) {
+            src[r] = q;
+            --q;
+            while (q >= 0 && !conflict(jobs[order[q]], b, M)) --q;
+        }
+        dep[r] = q;
+    }
+}
+
+// Device entry of the job run at position r.
+st::Job make_job(const zq4_stack_job &b, int off, int src, int dep)
+{
     st::Job jb;
     memset(&jb, 0, sizeof(jb));
     jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
@@ -586,28 +890,57 @@ st::Job make_job(const zq4_stack_job *jobs, int j, int M)
     jb.N = b.N;
     jb.K = b.K;
     jb.T = (b.N + 15) / 16;
-    jb.S = b.K / st::kSegCols;
-    jb.y_stride = b.gate_up ? b.N / 2 : b.N;
-    jb.flags = b.gate_up ? st::kJobGateUp : 0;
-    const uintptr_t x0 = reinterpret_cast<uintptr_t>(b.x), x1 = x0 + size_t(M) * size_t(b.K) * 2;
-    bool early = true;
-    for (int k = 0; k < j && early; ++k) {
-        const zq4_stack_job &q = jobs[k];
-        const size_t ys = q.gate_up ? size_t(q.N / 2) : size_t(q.N);
-        const uintptr_t y0 = reinterpret_cast<uintptr_t>(q.y), y1 = y0 + size_t(M) * ys * 2;
-        if (y0 < x1 && x0 < y1) early = false;
-    }
-    if (early) jb.flags |= st::kJobXEarly;
+    jb.off = off;
+    jb.src = src;
+    jb.flags = (b.gate_up ? st::kJobGateUp : 0) | ((dep + 1) << st::kDepShift);
     return jb;
 }
+
+// The job table in run order (into t[n]), round-robin offsets for G CTAs;
+// order, src and dep hold n ints of scratch.
+void job_table(const zq4_stack_job *jobs, int n, int M, int G, st::Job *t, int *order, int *src, int *dep,
+               SchedScratch sc)
+{
+    schedule(jobs, n, M, order, src, dep, sc);
+    for (int r = 0, off = 0; r < n; ++r) {
+        t[r] = make_job(jobs[order[r]], off, src[r], dep[r]);
+        off = int((off + (long long)t[r].T) % G);
+    }
+}
+
+// Heap scratch for the calls that may allocate.
+struct SchedBuffers {
+    std::vector<int> order, src, dep;
+    std::vector<long long> work, at;
+    std::vector<char> placed;
+    explicit SchedBuffers(int n) : order(n), src(n), dep(n), work(n), at(n), placed(n) {}
+    SchedScratch scratch() { return {work.data(), at.data(), placed.data()}; }
+};
 
 // Dynamic shared memory of a launch: the fixed part plus the cached jobs.
 size_t launch_smem(int n_jobs, int M, int max_k)
 {
-    return st::smem_bytes(M, max_k) + size_t(st::cached_jobs(n_jobs, M, max_k)) * sizeof(st::Job);
+    return st::smem_fixed(M, max_k) + size_t(st::cached_jobs(n_jobs, M, max_k)) * sizeof(st::Job);
 }
 
 }  // namespace
+
+zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src, int *dep)
+{
+    if (!order || !src || !dep) return ZQ4_ERR_NULL;
+    int mk, mt;
+    const zq4_status st = check_jobs(jobs, n_jobs, M, 1, &mk, &mt);
+    if (st != ZQ4_OK) return st;
+    SchedBuffers b(n_jobs);
+    schedule(jobs, n_jobs, M, b.order.data(), b.src.data(), b.dep.data(), b.scratch());
+    for (int r = 0; r < n_jobs; ++r) {
+        const int *o = b.order.data();
+        order[r] = o[r];
+        src[o[r]] = b.src[r] >= 0 ? o[b.src[r]] : -1;      // as indices of the given list
+        dep[o[r]] = b.dep[r] >= 0 ? o[b.dep[r]] : -1;
+    }
+    return ZQ4_OK;
+}
 
 zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes)
 {
@@ -641,9 +974,11 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
 
     std::vector<uint8_t> host(l.total, 0);
     uint8_t *hjobs = host.data() + l.jobs;
-    for (int j = 0; j < n_jobs; ++j) {
-        const st::Job jb = make_job(jobs, j, M);
-        memcpy(hjobs + size_t(j) * sizeof(st::Job), &jb, sizeof(jb));
+    {
+        SchedBuffers b(n_jobs);
+        std::vector<st::Job> table(n_jobs);
+        job_table(jobs, n_jobs, M, grid, table.data(), b.order.data(), b.src.data(), b.dep.data(), b.scratch());
+        memcpy(hjobs, table.data(), table.size() * sizeof(st::Job));
     }
     e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -668,10 +1003,12 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.hdr = reinterpret_cast<st::Header *>(base + l.hdr);
     p.jobs = reinterpret_cast<const st::Job *>(base + l.jobs);
     p.job_cnt = reinterpret_cast<unsigned *>(base + l.job_cnt);
+    p.flags = reinterpret_cast<unsigned long long *>(base + l.flags);
     p.n_jobs = plan->n_jobs;
     p.M = plan->M;
     p.max_k = plan->max_k;
     p.cached = st::cached_jobs(p.n_jobs, p.M, p.max_k);
+    p.x_bufs = st::x_buffers(p.M, p.max_k);
     void *args[] = {&p};
     return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),
                                                    dim3(st::kThreads), args,
@@ -683,7 +1020,8 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1257 jobs
+constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1218 jobs (and the per-CTA flags)
+constexpr int kStaticMaxJobs = 1218;                // the most whose layout fits in kStaticPlanBytes
 static_assert(sizeof(st::Job) == 48, "the documented job limit assumes 48-byte job entries");
 
 // The plan lives here when the caller has no device memory to give. Header
@@ -719,7 +1057,7 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     zq4_status stt = check_jobs(jobs, n_jobs, M, sm_count(), &mk, &mt);
     if (stt != ZQ4_OK) return stt;
     const Layout l = layout_for(n_jobs);
-    if (l.total > kStaticPlanBytes) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
+    if (l.total > kStaticPlanBytes || n_jobs > kStaticMaxJobs) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
     const size_t smem = launch_smem(n_jobs, M, mk);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
     if (e != cudaSuccess) return cuda_status(e);
@@ -733,10 +1071,16 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     uint8_t *base = static_cast<uint8_t *>(dev);
     // header and counters start at zero; the job table is written after
     e = cudaMemsetAsync(base, 0, l.total, s);
-    for (int j = 0; j < n_jobs && e == cudaSuccess; ++j) {
-        const st::Job jb = make_job(jobs, j, M);
-        // from pageable memory: the entry is staged before the call returns
-        e = cudaMemcpyAsync(base + l.jobs + size_t(j) * sizeof(st::Job), &jb, sizeof(jb), cudaMemcpyHostToDevice, s);
+    {
+        // scratch on the stack: this call allocates nothing
+        st::Job table[kStaticMaxJobs];
+        int order[kStaticMaxJobs], src[kStaticMaxJobs], dep[kStaticMaxJobs];
+        long long work[kStaticMaxJobs], at[kStaticMaxJobs];
+        char placed[kStaticMaxJobs];
+        job_table(jobs, n_jobs, M, sm_count(), table, order, src, dep, {work, at, placed});
+        // from pageable memory: the table is staged before the call returns
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(base + l.jobs, table, size_t(n_jobs) * sizeof(st::Job), cudaMemcpyHostToDevice, s);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e);

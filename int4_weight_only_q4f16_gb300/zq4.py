@@ -37,7 +37,7 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
            "zq4_gemv_argmax")
 
 
@@ -73,6 +73,7 @@ def _load():
         "zq4_dequant_f32": [P, P, P, I, I, P],
         "zq4_dequant_f16": [P, P, P, I, I, P],
         "zq4_stack_plan_bytes": [P, I, I, P],
+        "zq4_stack_plan_waits": [P, I, I, P, P, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -280,6 +281,22 @@ def device_errors(clear: bool = True) -> int:
 
 def status_string(status: int) -> str:
     return lib.zq4_status_string(status).decode()
+
+
+def stack_plan_waits(jobs, M):
+    """zq4_stack_plan_waits on addresses: ``jobs`` is a list of (wq, x, y, N,
+    K, gate_up) with plain integer addresses (nothing is read at them).
+    Returns (order, src, dep): the run order as indices of ``jobs``, and per
+    job the feeding job it waits on chunk-wise and the job it waits for
+    whole (-1: none)."""
+    n = len(jobs)
+    arr = (StackJob * n)()
+    for i, (wq, x, y, N, K, gate_up) in enumerate(jobs):
+        arr[i] = StackJob(wq, None, x, y, N, K, 1 if gate_up else 0)
+    order, src, dep = (ctypes.c_int * n)(), (ctypes.c_int * n)(), (ctypes.c_int * n)()
+    _check("zq4_stack_plan_waits",
+           lib.zq4_stack_plan_waits(ctypes.cast(arr, ctypes.c_void_p), n, M, order, src, dep))
+    return list(order), list(src), list(dep)
 
 
 class StackPlan:

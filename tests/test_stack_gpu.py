@@ -163,3 +163,69 @@ def test_stack_one_hot_bit_exact(oracle):
     for i, k in enumerate(ks):
         want = oracle.round_f16(w[:, k])
         assert np.array_equal(outs[i][0].view(np.uint16), want.view(np.uint16)), k
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_stack_orders_jobs_that_share_buffers(oracle, M):
+    """Jobs that read an earlier output exactly (chunk-wise wait), through an
+    offset view (whole-job wait), and that write over an earlier job's input
+    or output (the plan may also run them in another order where they do not
+    conflict): the final buffers equal a sequential host replay of the jobs
+    in the given order with the oracle, each job on the f16 values its x
+    holds at its turn.
+    Buffers start as NaN, so a read before its write shows as NaN. The bound
+    is wider than one job's (2^-6 S): the replay's inputs are the oracle's
+    f16 outputs, the GPU's its own; a read out of order is off by O(S)."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    width = 1024
+    pool = torch.full((8, M * width), float("nan"), dtype=torch.float16, device="cuda")
+    host = np.full((8, M * width), np.nan, np.float64)
+    for b in (0, 5, 7):                                   # fresh inputs
+        a = synth.activations(synth.rng_for("stack_order_x", b, M), M, width).ravel()
+        pool[b] = dev(a)
+        host[b] = a.astype(np.float64)
+
+    def view(b, cols, off):
+        return pool[b][off:off + M * cols].view(M, cols)
+
+    # (N, K, gate_up, (x buffer, x offset), (y buffer, y offset)); offsets in elements
+    spec = [(768, 512, False, (0, 0), (1, 0)),
+            (1024, 768, True, (1, 0), (2, 0)),          # x == y0: chunk-wise
+            (256, 512, False, (2, 0), (3, 0)),          # x == y1 (gate_up output)
+            (256, 512, False, (1, 256), (4, 0)),        # x inside y0 at an offset
+            (768, 256, False, (5, 0), (1, 0)),          # y over y0 / x1 / x3
+            (512, 768, False, (1, 0), (6, 0)),          # x == y4
+            (512, 512, False, (6, 0), (2, 0)),          # x == y5; y over y1 / x2
+            (256, 512, False, (7, 0), (6, 0))]          # y over y5 / x6
+    jobs, mats = [], []
+    for i, (N, K, gu, (xb, xo), (yb, yo)) in enumerate(spec):
+        wq_h, sc_h = synth.weight("stack_order_w", N, K, i)
+        seg, _ = zq4.prepare_weight(dev(wq_h), dev(sc_h), N, K, zq4.PREP_SEGMENTED)
+        cols = N // 2 if gu else N
+        jobs.append((seg, view(xb, K, xo), view(yb, cols, yo), N, K, gu))
+        mats.append((wq_h, sc_h))
+    order, src, dep = zq4.stack_plan_waits(
+        [(j[0].data_ptr(), j[1].data_ptr(), j[2].data_ptr(), j[3], j[4], j[5]) for j in jobs], M)
+    assert src == [-1, 0, 1, -1, -1, 4, 5, -1] and dep == [-1, -1, -1, 0, 3, 0, 2, 6]
+    zq4.StackPlan(jobs, M).run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+
+    S_img = np.zeros_like(host)
+    for i, (N, K, gu, (xb, xo), (yb, yo)) in enumerate(spec):
+        x_h = host[xb][xo:xo + M * K].reshape(M, K).astype(np.float16)
+        assert np.all(np.isfinite(x_h)), f"replay reads job {i}'s x before it is written"
+        wq_h, sc_h = mats[i]
+        if gu:
+            y, S = oracle.gate_up_silu(wq_h, sc_h, x_h, N, K, interleaved=True)
+        else:
+            y, S = oracle.gemv(wq_h, sc_h, x_h, N, K)
+        cols = y.shape[1]
+        host[yb][yo:yo + M * cols] = oracle.round_f16(y).astype(np.float64).ravel()
+        S_img[yb][yo:yo + M * cols] = S.ravel()
+    got = host_f16(pool).astype(np.float64)
+    written = np.isfinite(host)
+    assert np.array_equal(np.isfinite(got), written), "a buffer written or left unwritten out of order"
+    err = np.abs(got[written] - host[written])
+    bound = 2.0 ** -6 * S_img[written] + 2.0 ** -10 * np.abs(host[written]) + 2.0 ** -24
+    assert np.all(err <= bound), f"{int((err > bound).sum())} values off; worst {float((err - bound).max())}"
