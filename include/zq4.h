@@ -334,18 +334,13 @@ ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, i
  * later jobs that conflict with nothing still to run go first, until about
  * as much other work as that job's lies between the two.
  *   order[r] = the index (in `jobs`) of the r-th job run;
- *   dep[i]   = the job every CTA must have finished before job i starts, or
- *              -1: the last one run before i that conflicts with it -- unless
- *              that one feeds job i (x_i is exactly its y: same address, row
- *              stride K_i, nothing else shared), then src[i] = it and each
- *              256-column chunk c of x_i waits only for the CTAs that write
- *              those columns, and dep[i] is the last conflicting job before it;
- *   src[i]   = that feeding job, or -1.
+ *   dep[i]   = the last job run before job i that conflicts with it, or -1:
+ *              every CTA finishes it before job i starts (x of a job with no
+ *              such job is staged ahead, while earlier jobs compute).
  * Indices refer to `jobs`. The arrays hold n_jobs ints, caller-owned.
  * Errors: as zq4_stack_plan_bytes, and ZQ4_ERR_NULL for a NULL array.
  */
-ZQ4_API zq4_status zq4_stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src,
-                                        int *dep);
+ZQ4_API zq4_status zq4_stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *dep);
 
 /*
  * zq4_stack_plan_init -- write the plan into `dev` (256-byte aligned, at
@@ -383,7 +378,7 @@ ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
  * zq4_stack_plan_init, and the plan it fills runs with zq4_stack_run.
  *
  * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
- * 64 KiB array, i.e. at most 1218 jobs; a longer list returns
+ * 64 KiB array, i.e. at most 1257 jobs; a longer list returns
  * ZQ4_ERR_UNSUPPORTED and changes nothing. What must start at zero (the
  * plan's launch counter, abort flag and per-job counters) is cleared by
  * every call. The first call on a device resolves the array's address

@@ -326,9 +326,9 @@ zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, si
     return stack_plan_bytes(jobs, n_jobs, M, bytes);
 }
 
-zq4_status zq4_stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src, int *dep)
+zq4_status zq4_stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *dep)
 {
-    return stack_plan_waits(jobs, n_jobs, M, order, src, dep);
+    return stack_plan_waits(jobs, n_jobs, M, order, dep);
 }
 
 zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,

@@ -73,7 +73,7 @@ cudaError_t read_seg_error(unsigned *flags, bool clear);
 
 // zq4_stack.cu: the persistent decode-step kernel
 zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
-zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src, int *dep);
+zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *dep);
 zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
                            zq4_stack_plan *plan, cudaStream_t s);
 zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s);

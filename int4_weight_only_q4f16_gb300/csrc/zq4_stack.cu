@@ -79,11 +79,10 @@ namespace st {
 
 constexpr int kWarps = 12;                  // compute warps, one ring each
 constexpr int kCompute = kWarps * 32;
-constexpr int kCopyWarp = kWarps, kXWarp = kWarps + 1;
-constexpr int kThreads = kCompute + 64;      // + the copy warp + the x warp
+constexpr int kCopyWarp = kWarps, kXWarp = kWarps + 1, kRelWarp = kWarps + 2;
+constexpr int kThreads = kCompute + 96;      // + the copy warp, the x warp and the release warp
 constexpr int kMaxChunks = 64;               // 256-column chunks of x: K <= 16384
 constexpr int kXBatch = 12;                 // x rows in flight per lane of the x warp
-constexpr int kMaxGrid = 256;                // CTAs whose done flags a plan holds
 constexpr int kSlots = 5;
 using namespace segk;       // segment layout, inner loop, split-tile sums
 
@@ -111,9 +110,9 @@ struct alignas(16) Job {
     uint16_t *y;        // [M][N] ([M][N / 2] for gate_up)
     int N, K, T, off;
     int flags;
-    int src;            // x is exactly the output of job src (chunk-wise wait on it), or -1
+    int y_stride;       // N, or N / 2 for gate_up
 };
-__host__ __device__ inline int y_stride(const Job &jb) { return (jb.flags & 1) ? jb.N / 2 : jb.N; }
+__host__ __device__ inline int y_stride(const Job &jb) { return jb.y_stride; }
 
 // This CTA's tiles of a job: t0, t0 + G, .. (nt of them).
 __device__ __forceinline__ void cta_tiles(const Job &jb, int cta, int G, int &t0, int &nt)
@@ -128,7 +127,6 @@ struct Params {
     Header *hdr;
     const Job *jobs;
     unsigned *job_cnt;            // [n_jobs]: CTAs done with each job (monotone)
-    unsigned long long *flags;    // [kMaxGrid]: per CTA, (launch + 1) << 32 | (last job done + 1)
     int n_jobs, M, max_k;
     int x_bufs;          // x buffers in shared memory (1 .. kMaxXBufs)
     int cached;          // jobs [0, cached) are copied to shared memory at start
@@ -148,7 +146,8 @@ constexpr size_t kTabOff = kParkOff + (size_t(kWarps) * 2 * kParkSlot * 4 + 15) 
 constexpr int kTabInts = 2 * (kWarps + 1) + 2;                       // one job: range starts, first tiles, CTA tiles
 constexpr size_t kXsOff = kTabOff + (2 * kTabInts * 4 + 15) / 16 * 16;
 __host__ __device__ inline size_t xs_bytes(int M, int max_k) { return (size_t(M) * xs_row_bytes(max_k) + 15) / 16 * 16; }
-__host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 1024 + kXsOff + xs_bytes(M, max_k); }
+// (+128: the base is aligned up to 128 bytes in the kernel)
+__host__ __device__ inline size_t smem_bytes(int M, int max_k) { return 128 + kXsOff + xs_bytes(M, max_k); }
 // x buffers: as many as fit (up to kMaxXBufs) next to room for 64 cached
 // jobs, so that x of the next jobs is staged while this one computes
 constexpr int kMaxXBufs = 4;
@@ -286,26 +285,12 @@ __device__ __forceinline__ bool wait_at_least(const int *p, int v)
     }
 }
 
-// Flags are polled with relaxed loads, all in flight at once; one
-// fence.acq_rel.gpu after the polls that saw a release makes it an acquire.
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
-{
-    unsigned long long r;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(r) : "l"(p));
-    return r;
-}
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
-{
-    unsigned r;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
 {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, t = lane & 3;
@@ -320,6 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     // compute barrier and read by all of them after it: the other warps may set
     // s_abort at any time, and every compute warp must take the same branch
     volatile int *s_cbrk = s_abort + 1;
+    // jobs whose outputs this CTA has written (compute thread 0, after the
+    // sums); the release warp publishes them. s_rstop: the compute warps
+    // stopped early (abort), nothing more to publish
+    int *s_rdone = const_cast<int *>(s_abort + 2);
+    volatile int *s_rstop = s_abort + 3;
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
     uint8_t *xs = smem + kXsOff;                       // x of job j: xs + (j % x_bufs) * xs_size
@@ -329,11 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     const int n = p.n_jobs, M = p.M;
     const unsigned launch = *reinterpret_cast<volatile unsigned *>(&p.hdr->epoch);
     const unsigned target = (launch + 1u) * unsigned(G);
-    const unsigned long long tag = static_cast<unsigned long long>(launch + 1u) << 32;
 
     if (threadIdx.x == 0) {
         *s_abort = 0;
         *s_cbrk = 0;
+        *s_rdone = 0;
+        *s_rstop = 0;
         for (int c = 0; c < kMaxChunks; ++c) s_chunk[c] = 0;
         *s_xfree = 0;
     }
@@ -437,160 +428,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         if (w < kWarps)
             for (int c = max(0, issued - kSlots); c < issued; ++c)
                 if (!mbar_wait(full0 + 8 * (w * kSlots + c % kSlots), (c / kSlots) & 1)) break;
+    } else if (warp == kRelWarp) {
+        // ---------------- the release warp ----------------
+        // Publishes "this CTA is done with job j" (an add on the job's
+        // counter) once the compute warps have written the CTA's outputs of
+        // job j: one GPU-scope fence, then the add. The fence
+        // waits for the CTA's writes to reach the whole GPU (about a
+        // microsecond under a full memory stream); here it holds up no
+        // compute warp. The release is cumulative: the outputs were written
+        // before compute thread 0's CTA-scope release of s_rdone, which this
+        // lane acquires first.
+        if (lane == 0) {
+            for (int j = 0; j < n; ++j) {
+                if (!wait_at_least(s_rdone, j + 1)) {
+                    atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                    atomicOr(&p.hdr->abort, 1u);
+                    *s_abort = 1;
+                    break;
+                }
+                if (*s_rstop) break;
+                fence_acq_rel_gpu();
+                asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j]) : "memory");
+            }
+        }
     } else if (warp == kXWarp) {
         // ---------------- the x warp ----------------
-        // Stages x of every job into shared memory, one 256-column chunk at a
-        // time, after the wait the host derived for the job from the buffers
-        // (Job::flags): none when the job touches no buffer an earlier job
-        // writes or reads; "all CTAs done with job d" for the last such job d;
-        // and when x is exactly the previous job's output, per chunk, "the
-        // CTAs that produce those columns of the previous job are done", so
-        // compute warps start on the chunks already there instead of waiting
-        // for the whole previous job. s_chunk[c] = j + 1 once chunk c of job
-        // j is staged (monotone, so a fast compute warp can never mistake an
-        // earlier job's chunk for this one's).
+        // Stages x of every job that depends on no earlier job (decided on
+        // the host from the buffers: Job::flags) into shared memory ahead of
+        // the compute warps, kXBatch 512-byte rows of 256-column chunks in
+        // flight at a time (lane l moves bytes 16l.. of each row), into
+        // buffer j % x_bufs once the compute warps are past the job that used
+        // it last. s_chunk[c] = j + 1 once chunk c of job j is staged
+        // (monotone, so a fast compute warp can never mistake an earlier
+        // job's chunk for this one's). x of a job that does depend on an
+        // earlier one is staged by the compute warps after their wait.
         bool stop = false;
         for (int j = 0; j < n && !stop; ++j) {
             const Job &jb = job(j);
-            // the compute warps are past the job that last used this buffer
+            if ((jb.flags >> kDepShift) != 0) continue;
             if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs)) {
+                stop = true;
+                break;
+            }
+            if (*s_abort) {
                 stop = true;
                 break;
             }
             uint8_t *xsj = xs + (j % p.x_bufs) * xs_size;
             const int nch = jb.K >> 8, words = jb.K >> 3;
-            const int dep = (jb.flags >> kDepShift) - 1;
-            unsigned long long t0 = globaltimer();
-            if (dep >= 0 && lane == 0) {
-                // every CTA is done with job dep
-                for (;;) {
-                    if (ld_relaxed_u32(&p.job_cnt[dep]) >= target) break;
-                    if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
-                        stop = true;
-                        break;
-                    }
-                }
-                fence_acq_rel_gpu();
-            }
-            stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-            __syncwarp();                        // lane 0's acquire before every lane's loads of x
-            // per chunk (lane l tracks chunks l and l + 32): the CTAs whose
-            // tiles [tlo, thi] of job src produce its columns, (t + off) mod G
-            // for each: one cyclic run of CTAs, as up to two ranges
-            // [olo[h][0], ohi[h][0]] and [olo[h][1], ohi[h][1]] (empty: hi < lo)
-            const bool elem = jb.src >= 0;
-            int olo[2][2] = {{0, 0}, {0, 0}}, ohi[2][2] = {{-1, -1}, {-1, -1}};
-            if (elem) {
-                const Job &pj = job(jb.src);
-                const int es = (pj.flags & kJobGateUp) ? 3 : 4;       // log2(outputs per 16-row tile)
+            const unsigned long long all = nch >= 64 ? ~0ull : ((1ull << nch) - 1ull);
+            unsigned long long rem = all;
+            int ck = __ffsll(rem) - 1, cm = 0;
+            const uint4 *xg = reinterpret_cast<const uint4 *>(jb.x) + lane;
+            while (rem) {
+                int qc[kXBatch];                  // chunk | token << 8, or -1
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int kc = lane + 32 * h;
-                    const int tlo = min(pj.T - 1, (kc * 256) >> es), thi = min(pj.T - 1, (kc * 256 + 255) >> es);
-                    const int len = thi - tlo + 1;
-                    if (len >= G) {
-                        ohi[h][0] = G - 1;
-                    } else {
-                        int o0 = tlo % G + pj.off;
-                        if (o0 >= G) o0 -= G;
-                        olo[h][0] = o0;
-                        ohi[h][0] = min(o0 + len - 1, G - 1);
-                        ohi[h][1] = o0 + len - 1 - G;
-                    }
-                }
-            }
-            const unsigned long long need = tag | unsigned(jb.src + 1);    // CTA done with job src
-            unsigned long long pending = nch >= 64 ? ~0ull : ((1ull << nch) - 1ull);
-            t0 = globaltimer();
-            while (pending && !stop) {
-                unsigned long long ready = pending;
-                if (elem) {
-                    // every CTA's flag once (all loads in flight together), as
-                    // bit sets of the CTAs done with job j-1
-                    unsigned long long fv[kMaxGrid / 32];
-#pragma unroll
-                    for (int q = 0; q < kMaxGrid / 32; ++q)
-                        fv[q] = q * 32 < G && q * 32 + lane < G ? ld_relaxed_u64(p.flags + q * 32 + lane) : 0ull;
-                    unsigned done[kMaxGrid / 32];
-#pragma unroll
-                    for (int q = 0; q < kMaxGrid / 32; ++q) done[q] = __ballot_sync(0xffffffffu, fv[q] >= need);
-                    bool rdy[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        bool all = true;
-#pragma unroll
-                        for (int g = 0; g < 2; ++g)
-#pragma unroll
-                            for (int q = 0; q < kMaxGrid / 32; ++q) {
-                                const int lo = max(olo[h][g], 32 * q), hi = min(ohi[h][g], 32 * q + 31);
-                                if (lo <= hi) {
-                                    const unsigned want =
-                                        hi - lo == 31 ? 0xffffffffu : ((1u << (hi - lo + 1)) - 1u) << (lo - 32 * q);
-                                    all = all && (done[q] & want) == want;
-                                }
-                            }
-                        rdy[h] = all;
-                    }
-                    ready &= (unsigned long long)__ballot_sync(0xffffffffu, rdy[0]) |
-                             ((unsigned long long)__ballot_sync(0xffffffffu, rdy[1]) << 32);
-                }
-                if (ready) {
-                    if (elem) {
-                        fence_acq_rel_gpu();     // the polls that saw the flags become acquires
-                        __syncwarp();
-                    }
-                    // stage the ready chunks, kXBatch (chunk, token) rows of 512
-                    // bytes in flight at a time; lane l moves bytes 16l.. of each
-                    unsigned long long rem = ready;
-                    int ck = __ffsll(rem) - 1, cm = 0;
-                    const uint4 *xg = reinterpret_cast<const uint4 *>(jb.x) + lane;
-                    while (rem) {
-                        int qc[kXBatch];                  // chunk | token << 8, or -1
-#pragma unroll
-                        for (int q = 0; q < kXBatch; ++q) {
-                            qc[q] = -1;
-                            if (rem) {
-                                qc[q] = ck | (cm << 8);
-                                if (++cm == M) {
-                                    cm = 0;
-                                    rem &= rem - 1;
-                                    ck = __ffsll(rem) - 1;
-                                }
-                            }
+                for (int q = 0; q < kXBatch; ++q) {
+                    qc[q] = -1;
+                    if (rem) {
+                        qc[q] = ck | (cm << 8);
+                        if (++cm == M) {
+                            cm = 0;
+                            rem &= rem - 1;
+                            ck = __ffsll(rem) - 1;
                         }
-                        uint4 v[kXBatch];
-#pragma unroll
-                        for (int q = 0; q < kXBatch; ++q)
-                            if (qc[q] >= 0) v[q] = __ldcg(xg + (qc[q] >> 8) * words + (qc[q] & 255) * 32);
-#pragma unroll
-                        for (int q = 0; q < kXBatch; ++q)
-                            if (qc[q] >= 0)
-                                *reinterpret_cast<uint4 *>(xsj + (qc[q] >> 8) * int(xrow) + ((qc[q] & 255) * 32 + lane) * 16) =
-                                    pair_perm(v[q]);
                     }
-                    __syncwarp();
-                    // lane l publishes chunks l and l + 32
-                    if ((ready >> lane) & 1ull) st_release_cta(s_chunk + lane, j + 1);
-                    if ((ready >> (lane + 32)) & 1ull) st_release_cta(s_chunk + lane + 32, j + 1);
-                    pending &= ~ready;
-                    t0 = globaltimer();
-                } else {
-                    if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
-                        stop = true;
-                        break;
-                    }
-                    __nanosleep(64);
                 }
+                uint4 v[kXBatch];
+#pragma unroll
+                for (int q = 0; q < kXBatch; ++q)
+                    if (qc[q] >= 0) v[q] = __ldcg(xg + (qc[q] >> 8) * words + (qc[q] & 255) * 32);
+#pragma unroll
+                for (int q = 0; q < kXBatch; ++q)
+                    if (qc[q] >= 0)
+                        *reinterpret_cast<uint4 *>(xsj + (qc[q] >> 8) * int(xrow) + ((qc[q] & 255) * 32 + lane) * 16) =
+                            pair_perm(v[q]);
             }
-            // when stopping, the chunks never staged are released too, so that
-            // no compute warp waits on them (the results are void then)
-            if (stop && lane == 0)
-                for (int kc = 0; kc < kMaxChunks; ++kc) st_release_cta(s_chunk + kc, 1 << 30);
+            __syncwarp();
+            // lane l publishes chunks l and l + 32
+            if ((all >> lane) & 1ull) st_release_cta(s_chunk + lane, j + 1);
+            if ((all >> (lane + 32)) & 1ull) st_release_cta(s_chunk + lane + 32, j + 1);
         }
-        if (stop && lane == 0) {
-            atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
-            atomicOr(&p.hdr->abort, 1u);
-            *s_abort = 1;
+        if (stop) {
+            // release every chunk, so that no compute warp waits on one (the results are void)
+            if (lane == 0)
+                for (int kc = 0; kc < kMaxChunks; ++kc) st_release_cta(s_chunk + kc, 1 << 30);
+            if (lane == 0 && !*s_abort) {
+                atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                atomicOr(&p.hdr->abort, 1u);
+                *s_abort = 1;
+            }
         }
     } else {
         // ---------------- compute warps ----------------
@@ -651,6 +578,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             int tt = first_tile, sg = ub - first_tile * S;
             const uint8_t *xrj = xr + (j % p.x_bufs) * xs_size;
             unsigned long long seen = 0;          // x chunks of this job known to be staged
+            const int dep = (jb.flags >> kDepShift) - 1;
+            if (dep >= 0) {
+                // x depends on earlier jobs: every CTA must be done with job
+                // dep (thread 0 waits; the barrier passes its acquire on), then
+                // the compute threads stage x, all loads in one round trip
+                if (threadIdx.x == 0) {
+                    const unsigned long long t0 = globaltimer();
+                    while (ld_acquire(&p.job_cnt[dep]) < target) {
+                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                            atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                            atomicOr(&p.hdr->abort, 1u);
+                            *s_abort = 1;
+                            break;
+                        }
+                    }
+                }
+                compute_sync();
+                uint8_t *xsj = xs + (j % p.x_bufs) * xs_size;
+                const int words = jb.K >> 3, total = M * words;
+                const uint4 *xg = reinterpret_cast<const uint4 *>(jb.x);
+                for (int i0 = int(threadIdx.x); i0 < total; i0 += 4 * kCompute) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (i0 + q * kCompute < total) v[q] = __ldcg(xg + i0 + q * kCompute);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int i = i0 + q * kCompute;
+                        if (i < total) {
+                            const int m = i / words;
+                            *reinterpret_cast<uint4 *>(xsj + m * int(xrow) + (i - m * words) * 16) = pair_perm(v[q]);
+                        }
+                    }
+                }
+                compute_sync();
+                seen = ~0ull;
+            }
             for (int u = ub; u < ue && ok; ++u) {
                 // x chunk sg of this job (segment sg of a tile covers columns 256 sg ..)
                 if (!((seen >> sg) & 1ull)) {
@@ -695,11 +659,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             if (threadIdx.x == 0) *s_cbrk = *s_abort;
             compute_sync();                       // the split-tile sums before the release below
             const bool brk = *s_cbrk != 0;
-            if (threadIdx.x == 0 && !brk) {
-                // release: this CTA's outputs of job j become visible with its flag
-                asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.flags + cta), "l"(tag | unsigned(j + 1))
-                             : "memory");
-                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.job_cnt[j]) : "memory");
+            if (threadIdx.x == 0) {
+                // the release warp publishes this CTA's outputs of job j
+                if (brk) *s_rstop = 1;
+                st_release_cta(s_rdone, brk ? (1 << 30) : j + 1);
             }
             if (brk) break;
         }
@@ -731,7 +694,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int stack_smem_set[kMaxDevices] = {};
 
 struct Layout {
-    size_t hdr, jobs, job_cnt, flags, total;
+    size_t hdr, jobs, job_cnt, total;
 };
 
 Layout layout_for(int n_jobs)
@@ -740,8 +703,7 @@ Layout layout_for(int n_jobs)
     l.hdr = 0;
     l.jobs = align_up(sizeof(st::Header), 128);
     l.job_cnt = l.jobs + size_t(n_jobs) * sizeof(st::Job);
-    l.flags = align_up(l.job_cnt + size_t(n_jobs) * 4, 16);
-    l.total = align_up(l.flags + size_t(st::kMaxGrid) * 8, 256);
+    l.total = align_up(l.job_cnt + size_t(n_jobs) * 4, 256);
     return l;
 }
 
@@ -749,7 +711,6 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
 {
     if (!jobs) return ZQ4_ERR_NULL;
     if (n_jobs <= 0 || M < 1 || M > st::kTokCols) return ZQ4_ERR_SHAPE;
-    if (grid > st::kMaxGrid) return ZQ4_ERR_UNSUPPORTED;      // more CTAs than the plan's done flags
     int mk = 0, mt = 0;
     for (int j = 0; j < n_jobs; ++j) {
         const zq4_stack_job &b = jobs[j];
@@ -795,14 +756,6 @@ bool conflict(const zq4_stack_job &a, const zq4_stack_job &b, int M)
     return ya.meets(xb) || ya.meets(yb) || xa.meets(yb);
 }
 
-// x of b is exactly the output of a (same address and row stride) and
-// that is all the two share.
-bool feeds(const zq4_stack_job &a, const zq4_stack_job &b, int M)
-{
-    return a.y == b.x && (a.gate_up ? a.N / 2 : a.N) == b.K && !x_span(a, M).meets(y_span(b, M)) &&
-           !y_span(a, M).meets(y_span(b, M));
-}
-
 constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
 
 // The order the kernel runs the jobs in and the wait before each. The
@@ -814,10 +767,7 @@ constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
 // work on those meanwhile instead of waiting for the last ones.
 //
 // Waits (positions in run order): dep[r] = the last job before r that
-// conflicts with it, which every CTA must have finished first; unless that
-// job feeds job r (feeds()), in which case src[r] = it (each 256-column
-// chunk of x waits only for the CTAs that write those columns) and dep[r]
-// is the last conflicting job before src[r]. -1: none.
+// conflicts with it, which every CTA must have finished first; -1: none.
 //
 // Scratch (n entries each) comes from the caller, so that this allocates
 // nothing: work, at (segments; total placed work right after placing a job)
@@ -826,7 +776,7 @@ struct SchedScratch {
     long long *work, *at;
     char *placed;
 };
-void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *src, int *dep, SchedScratch sc)
+void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, SchedScratch sc)
 {
     long long *work = sc.work, *at = sc.at;
     char *placed = sc.placed;
@@ -866,21 +816,14 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *src, int
         order[n_placed++] = pick;
     }
     for (int r = 0; r < n; ++r) {
-        src[r] = -1;
-        const zq4_stack_job &b = jobs[order[r]];
         int q = r - 1;
-        while (q >= 0 && !conflict(jobs[order[q]], b, M)) --q;
-        if (q >= 0 && feeds(jobs[order[q]], b, M)) {
-            src[r] = q;
-            --q;
-            while (q >= 0 && !conflict(jobs[order[q]], b, M)) --q;
-        }
+        while (q >= 0 && !conflict(jobs[order[q]], jobs[order[r]], M)) --q;
         dep[r] = q;
     }
 }
 
 // Device entry of the job run at position r.
-st::Job make_job(const zq4_stack_job &b, int off, int src, int dep)
+st::Job make_job(const zq4_stack_job &b, int off, int dep)
 {
     st::Job jb;
     memset(&jb, 0, sizeof(jb));
@@ -891,29 +834,29 @@ st::Job make_job(const zq4_stack_job &b, int off, int src, int dep)
     jb.K = b.K;
     jb.T = (b.N + 15) / 16;
     jb.off = off;
-    jb.src = src;
+    jb.y_stride = b.gate_up ? b.N / 2 : b.N;
     jb.flags = (b.gate_up ? st::kJobGateUp : 0) | ((dep + 1) << st::kDepShift);
     return jb;
 }
 
 // The job table in run order (into t[n]), round-robin offsets for G CTAs;
-// order, src and dep hold n ints of scratch.
-void job_table(const zq4_stack_job *jobs, int n, int M, int G, st::Job *t, int *order, int *src, int *dep,
+// order and dep hold n ints of scratch.
+void job_table(const zq4_stack_job *jobs, int n, int M, int G, st::Job *t, int *order, int *dep,
                SchedScratch sc)
 {
-    schedule(jobs, n, M, order, src, dep, sc);
+    schedule(jobs, n, M, order, dep, sc);
     for (int r = 0, off = 0; r < n; ++r) {
-        t[r] = make_job(jobs[order[r]], off, src[r], dep[r]);
+        t[r] = make_job(jobs[order[r]], off, dep[r]);
         off = int((off + (long long)t[r].T) % G);
     }
 }
 
 // Heap scratch for the calls that may allocate.
 struct SchedBuffers {
-    std::vector<int> order, src, dep;
+    std::vector<int> order, dep;
     std::vector<long long> work, at;
     std::vector<char> placed;
-    explicit SchedBuffers(int n) : order(n), src(n), dep(n), work(n), at(n), placed(n) {}
+    explicit SchedBuffers(int n) : order(n), dep(n), work(n), at(n), placed(n) {}
     SchedScratch scratch() { return {work.data(), at.data(), placed.data()}; }
 };
 
@@ -925,19 +868,18 @@ size_t launch_smem(int n_jobs, int M, int max_k)
 
 }  // namespace
 
-zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *src, int *dep)
+zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *dep)
 {
-    if (!order || !src || !dep) return ZQ4_ERR_NULL;
+    if (!order || !dep) return ZQ4_ERR_NULL;
     int mk, mt;
     const zq4_status st = check_jobs(jobs, n_jobs, M, 1, &mk, &mt);
     if (st != ZQ4_OK) return st;
     SchedBuffers b(n_jobs);
-    schedule(jobs, n_jobs, M, b.order.data(), b.src.data(), b.dep.data(), b.scratch());
+    schedule(jobs, n_jobs, M, b.order.data(), b.dep.data(), b.scratch());
     for (int r = 0; r < n_jobs; ++r) {
         const int *o = b.order.data();
         order[r] = o[r];
-        src[o[r]] = b.src[r] >= 0 ? o[b.src[r]] : -1;      // as indices of the given list
-        dep[o[r]] = b.dep[r] >= 0 ? o[b.dep[r]] : -1;
+        dep[o[r]] = b.dep[r] >= 0 ? o[b.dep[r]] : -1;      // as indices of the given list
     }
     return ZQ4_OK;
 }
@@ -977,7 +919,7 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     {
         SchedBuffers b(n_jobs);
         std::vector<st::Job> table(n_jobs);
-        job_table(jobs, n_jobs, M, grid, table.data(), b.order.data(), b.src.data(), b.dep.data(), b.scratch());
+        job_table(jobs, n_jobs, M, grid, table.data(), b.order.data(), b.dep.data(), b.scratch());
         memcpy(hjobs, table.data(), table.size() * sizeof(st::Job));
     }
     e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
@@ -1003,7 +945,6 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.hdr = reinterpret_cast<st::Header *>(base + l.hdr);
     p.jobs = reinterpret_cast<const st::Job *>(base + l.jobs);
     p.job_cnt = reinterpret_cast<unsigned *>(base + l.job_cnt);
-    p.flags = reinterpret_cast<unsigned long long *>(base + l.flags);
     p.n_jobs = plan->n_jobs;
     p.M = plan->M;
     p.max_k = plan->max_k;
@@ -1020,8 +961,8 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1218 jobs (and the per-CTA flags)
-constexpr int kStaticMaxJobs = 1218;                // the most whose layout fits in kStaticPlanBytes
+constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1257 jobs
+constexpr int kStaticMaxJobs = 1257;                // the most whose layout fits in kStaticPlanBytes
 static_assert(sizeof(st::Job) == 48, "the documented job limit assumes 48-byte job entries");
 
 // The plan lives here when the caller has no device memory to give. Header
@@ -1074,10 +1015,10 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     {
         // scratch on the stack: this call allocates nothing
         st::Job table[kStaticMaxJobs];
-        int order[kStaticMaxJobs], src[kStaticMaxJobs], dep[kStaticMaxJobs];
+        int order[kStaticMaxJobs], dep[kStaticMaxJobs];
         long long work[kStaticMaxJobs], at[kStaticMaxJobs];
         char placed[kStaticMaxJobs];
-        job_table(jobs, n_jobs, M, sm_count(), table, order, src, dep, {work, at, placed});
+        job_table(jobs, n_jobs, M, sm_count(), table, order, dep, {work, at, placed});
         // from pageable memory: the table is staged before the call returns
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(base + l.jobs, table, size_t(n_jobs) * sizeof(st::Job), cudaMemcpyHostToDevice, s);

@@ -32,9 +32,9 @@ def _dev(a: np.ndarray, device) -> torch.Tensor:
 class Projection:
     """One q4f16_1 matrix on the device (+ optional host copy)."""
 
-    def __init__(self, name, N, K, layer, device, keep_host, seed):
+    def __init__(self, name, N, K, layer, device, keep_host, seed, sigma=0.02, signed=False):
         self.name, self.N, self.K, self.layer = name, N, K, layer
-        wq, sc = synth.weight(name, N, K, layer, seed=seed)
+        wq, sc = synth.weight(name, N, K, layer, seed=seed, sigma=sigma, signed=signed)
         self.wq, self.sc = _dev(wq, device), _dev(sc, device)
         self.host = (wq, sc) if keep_host else None
 
@@ -49,34 +49,64 @@ class DecodeStack:
     epilogue and the one named "down" reads its output."""
 
     def __init__(self, layer_shapes, n_layers, head=None, M=1, device="cuda",
-                 keep_host=False, seed=synth.MASTER_SEED, mode="calls"):
+                 keep_host=False, seed=synth.MASTER_SEED, mode="calls", chain=False):
         """mode "calls": one zq4_gemv / zq4_gate_up_silu per projection on
         the canonical matrices; "seg": one zq4_gemv_seg / zq4_gate_up_silu_seg
         per projection on segmented copies made once; "plan": the whole step
-        as one persistent launch (zq4_stack_run) on segmented copies."""
+        as one persistent launch (zq4_stack_run) on segmented copies.
+
+        chain=False: every projection reads a fresh seeded x except "down",
+        which reads its layer's gate_up output. chain=True: the dependencies
+        of a decode step without its attention and norms -- each projection
+        reads the output of the one before it (the first qkv a seeded x);
+        where the widths differ (o after qkv) x is a view over the first
+        M * K values of that output, standing in for attention, which reads
+        all of it. Chained stacks draw signed scales N(0, sigma) with sigma =
+        synth.unit_gain_sigma(K) instead of |N(0, 0.02)| (a stand-in for the
+        norms between projections: activations stay O(1) through the
+        layers)."""
+        self.chain = chain
         self.M, self.device, self.n_layers = M, torch.device(device), n_layers
         self.mode = mode
         self.plan = None
         self.layers = []
         for l in range(n_layers):
-            self.layers.append({name: Projection(name, N, K, l, self.device, keep_host, seed)
+            self.layers.append({name: Projection(name, N, K, l, self.device, keep_host, seed,
+                                                 synth.unit_gain_sigma(K, name == "gate_up") if chain else 0.02,
+                                                 signed=chain)
                                 for name, N, K in layer_shapes})
         self.order = [name for name, _, _ in layer_shapes]
-        self.head = Projection(head[0], head[1], head[2], 0, self.device, keep_host, seed) if head else None
+        self.head = Projection(head[0], head[1], head[2], 0, self.device, keep_host, seed,
+                               synth.unit_gain_sigma(head[2]) if chain else 0.02, signed=chain) if head else None
         # activations: a fresh seeded input for every projection that does
         # not read another projection's output
         self.x, self.y = {}, {}
+        self.fresh = []                               # keys of the seeded inputs (the rest are outputs)
+        prev = None                                   # key of the previous output
         for l, layer in enumerate(self.layers):
             for name in self.order:
                 p = layer[name]
-                if name != "down":
+                if chain and prev is not None:
+                    y_prev = self.y[prev]
+                    if y_prev.shape[1] != p.K and y_prev.numel() < M * p.K:
+                        raise ValueError(f"chain: {name} reads {M * p.K} values, the previous output "
+                                         f"holds {y_prev.numel()}")
+                    self.x[(l, name)] = y_prev if y_prev.shape[1] == p.K else \
+                        y_prev.view(-1)[:M * p.K].view(M, p.K)
+                elif name != "down" or chain:
                     xa = synth.activations(synth.rng_for("x_" + name, l, M, seed=seed), M, p.K)
                     self.x[(l, name)] = _dev(xa, self.device)
+                    self.fresh.append((l, name))
                 cols = p.N // 2 if name == "gate_up" else p.N
                 self.y[(l, name)] = torch.empty((M, cols), dtype=torch.float16, device=self.device)
+                prev = (l, name)
         if self.head:
-            xa = synth.activations(synth.rng_for("x_head", 0, M, seed=seed), M, self.head.K)
-            self.x[("head",)] = _dev(xa, self.device)
+            if chain and prev is not None and self.y[prev].shape[1] == self.head.K:
+                self.x[("head",)] = self.y[prev]
+            else:
+                xa = synth.activations(synth.rng_for("x_head", 0, M, seed=seed), M, self.head.K)
+                self.x[("head",)] = _dev(xa, self.device)
+                self.fresh.append(("head",))
             self.y[("head",)] = torch.empty((M, self.head.N), dtype=torch.float16, device=self.device)
         self.graph = None
 
@@ -86,10 +116,9 @@ class DecodeStack:
         return b + (self.head.nbytes if self.head else 0)
 
     def activation_bytes(self) -> int:
-        return sum(t.numel() * 2 for t in self.x.values()) + \
-            sum(t.numel() * 2 for t in self.y.values()) + \
-            sum(self.y[(l, "gate_up")].numel() * 2 for l in range(self.n_layers)
-                if (l, "gate_up") in self.y and "down" in self.order)
+        """Every projection's x read once and y written once."""
+        return sum(self.input_for(k[0], k[1]).numel() * 2 if len(k) == 2 else self.x[k].numel() * 2
+                   for k in self.y) + sum(t.numel() * 2 for t in self.y.values())
 
     def bytes_per_step(self) -> int:
         """Algorithmic bytes: every packed weight and scale once, every
@@ -110,7 +139,9 @@ class DecodeStack:
 
     # --- execution -----------------------------------------------------------
     def input_for(self, l, name):
-        return self.y[(l, "gate_up")] if name == "down" else self.x[(l, name)]
+        if (l, name) in self.x:
+            return self.x[(l, name)]
+        return self.y[(l, "gate_up")]                  # down, unchained
 
     def jobs(self):
         """(wq, scales, x, y, N, K, gate_up) of every projection in step order."""

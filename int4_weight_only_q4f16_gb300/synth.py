@@ -59,12 +59,13 @@ def packed_codes(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
     return raw.astype("<u8", copy=False).view("<u4").astype(np.uint32, copy=False).reshape(N, K // 8)
 
 
-def group_scales(rng: np.random.Generator, N: int, K: int, sigma: float = 0.02) -> np.ndarray:
-    """f16(|N(0, sigma)|), shape [N, K/32] float16."""
+def group_scales(rng: np.random.Generator, N: int, K: int, sigma: float = 0.02,
+                 signed: bool = False) -> np.ndarray:
+    """f16(|N(0, sigma)|) (signed: f16(N(0, sigma))), shape [N, K/32] float16."""
     if K % 32:
         raise ValueError("K must be a multiple of 32")
-    g = rng.standard_normal((N, K // 32), dtype=np.float32)
-    return np.abs(g * np.float32(sigma)).astype(np.float16)
+    g = rng.standard_normal((N, K // 32), dtype=np.float32) * np.float32(sigma)
+    return (g if signed else np.abs(g)).astype(np.float16)
 
 
 def activations(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
@@ -86,7 +87,21 @@ def routing(rng: np.random.Generator, T: int, E: int, top_k: int):
     return ids, r
 
 
-def weight(tag: str, N: int, K: int, *index: int, seed: int = MASTER_SEED):
+def weight(tag: str, N: int, K: int, *index: int, seed: int = MASTER_SEED, sigma: float = 0.02,
+           signed: bool = False):
     """(packed codes, scales) of one q4f16_1 matrix."""
     rng = rng_for(tag, *index, seed=seed)
-    return packed_codes(rng, N, K), group_scales(rng, N, K)
+    return packed_codes(rng, N, K), group_scales(rng, N, K, sigma, signed)
+
+
+def unit_gain_sigma(K: int, gate_up: bool = False) -> float:
+    """Scale sigma for which a projection with signed scales (N(0, sigma))
+    keeps the size of its input x: uniform codes give E[(q - 7)^2] = 21.5
+    and E[s^2] = sigma^2, so E[y^2] = K * 21.5 * sigma^2 * E[x^2]; the fused
+    silu(g) * u output has mean square 1 when g and u have standard
+    deviation ~1.27 (so gate_up rows take 1.27 times the sigma). Chained
+    synthetic stacks use it in place of the norms a real decode step applies
+    between projections. (With the default positive scales, (q - 7) s has
+    mean 0.5 E[s]: every output shares a term in sum(x) that grows ~5x per
+    3072-wide projection, and f16 overflows within a few layers.)"""
+    return float((21.5 * K) ** -0.5) * (1.27 if gate_up else 1.0)

@@ -73,7 +73,7 @@ def _load():
         "zq4_dequant_f32": [P, P, P, I, I, P],
         "zq4_dequant_f16": [P, P, P, I, I, P],
         "zq4_stack_plan_bytes": [P, I, I, P],
-        "zq4_stack_plan_waits": [P, I, I, P, P, P],
+        "zq4_stack_plan_waits": [P, I, I, P, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -286,17 +286,15 @@ def status_string(status: int) -> str:
 def stack_plan_waits(jobs, M):
     """zq4_stack_plan_waits on addresses: ``jobs`` is a list of (wq, x, y, N,
     K, gate_up) with plain integer addresses (nothing is read at them).
-    Returns (order, src, dep): the run order as indices of ``jobs``, and per
-    job the feeding job it waits on chunk-wise and the job it waits for
-    whole (-1: none)."""
+    Returns (order, dep): the run order as indices of ``jobs``, and per job
+    the job it waits for (-1: none)."""
     n = len(jobs)
     arr = (StackJob * n)()
     for i, (wq, x, y, N, K, gate_up) in enumerate(jobs):
         arr[i] = StackJob(wq, None, x, y, N, K, 1 if gate_up else 0)
-    order, src, dep = (ctypes.c_int * n)(), (ctypes.c_int * n)(), (ctypes.c_int * n)()
-    _check("zq4_stack_plan_waits",
-           lib.zq4_stack_plan_waits(ctypes.cast(arr, ctypes.c_void_p), n, M, order, src, dep))
-    return list(order), list(src), list(dep)
+    order, dep = (ctypes.c_int * n)(), (ctypes.c_int * n)()
+    _check("zq4_stack_plan_waits", lib.zq4_stack_plan_waits(ctypes.cast(arr, ctypes.c_void_p), n, M, order, dep))
+    return list(order), list(dep)
 
 
 class StackPlan:

@@ -53,6 +53,31 @@ def test_small_stack_matches_oracle(oracle, M):
         _check_job(oracle, job, what)
 
 
+CHAIN_LAYER = (("qkv", 768, 256), ("o", 256, 512), ("gate_up", 1024, 256), ("down", 256, 512))
+CHAIN_HEAD = ("lm_head", 333, 256)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_chained_stack_matches_oracle(oracle, M):
+    """Every projection reads the previous one's output (o a view over
+    qkv's): each job waits for the one before, and matches
+    the oracle on the values its x holds after the step (each buffer is
+    written once)."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    s = stk.DecodeStack(CHAIN_LAYER, 3, CHAIN_HEAD, M=M, mode="plan", chain=True)
+    s.launch_step()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    jobs = s.jobs()
+    _, dep = zq4.stack_plan_waits([(j[0].data_ptr(), j[2].data_ptr(), j[3].data_ptr(), j[4], j[5], j[6])
+                                   for j in jobs], M)
+    assert dep[1:5] == [0, 1, 2, 3]
+    names = [n for n, _, _ in CHAIN_LAYER]
+    for i, job in enumerate(jobs):
+        l, name = divmod(i, len(names))
+        _check_job(oracle, job, f"M={M} job {i} " + ("lm_head" if l == 3 else f"layer {l} {names[name]}"))
+
+
 def test_stack_runs_and_graph_replays_are_bit_identical():
     s = stk.DecodeStack(SMALL_LAYER, 3, SMALL_HEAD, M=2, mode="plan")
     strm = torch.cuda.Stream()
@@ -167,8 +192,8 @@ def test_stack_one_hot_bit_exact(oracle):
 
 @pytest.mark.parametrize("M", [1, 3])
 def test_stack_orders_jobs_that_share_buffers(oracle, M):
-    """Jobs that read an earlier output exactly (chunk-wise wait), through an
-    offset view (whole-job wait), and that write over an earlier job's input
+    """Jobs that read an earlier output, exactly or through an offset view,
+    and that write over an earlier job's input
     or output (the plan may also run them in another order where they do not
     conflict): the final buffers equal a sequential host replay of the jobs
     in the given order with the oracle, each job on the f16 values its x
@@ -204,9 +229,9 @@ def test_stack_orders_jobs_that_share_buffers(oracle, M):
         cols = N // 2 if gu else N
         jobs.append((seg, view(xb, K, xo), view(yb, cols, yo), N, K, gu))
         mats.append((wq_h, sc_h))
-    order, src, dep = zq4.stack_plan_waits(
+    order, dep = zq4.stack_plan_waits(
         [(j[0].data_ptr(), j[1].data_ptr(), j[2].data_ptr(), j[3], j[4], j[5]) for j in jobs], M)
-    assert src == [-1, 0, 1, -1, -1, 4, 5, -1] and dep == [-1, -1, -1, 0, 3, 0, 2, 6]
+    assert dep == [-1, 0, 1, 0, 3, 4, 5, 6]
     zq4.StackPlan(jobs, M).run()
     torch.cuda.synchronize()
     assert zq4.device_errors(clear=True) == 0

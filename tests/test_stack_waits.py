@@ -3,7 +3,7 @@
 (nothing is read at the addresses). Hand-derived cases, plus a check on
 seeded random job lists that conflicting jobs (touching the same bytes, one
 of them writing) keep their order and that every job waits for the last
-conflicting job run before it (chunk-wise when that job feeds it exactly)."""
+conflicting job run before it."""
 import numpy as np
 import pytest
 
@@ -37,12 +37,7 @@ def conflict(a, b, M):
     return meets(ya, xb) or meets(ya, yb) or meets(xa, yb)
 
 
-def feeds(a, b, M):
-    (xa, ya), (_, yb) = spans(a, M), spans(b, M)
-    return a[2] == b[1] and (a[3] // 2 if a[5] else a[3]) == b[4] and not meets(xa, yb) and not meets(ya, yb)
-
-
-def check_valid(jobs, M, order, src, dep):
+def check_valid(jobs, M, order, dep):
     n = len(jobs)
     assert sorted(order) == list(range(n))
     pos = {j: r for r, j in enumerate(order)}
@@ -51,36 +46,27 @@ def check_valid(jobs, M, order, src, dep):
             if conflict(jobs[i], jobs[j], M):
                 assert pos[i] < pos[j], f"jobs {i} and {j} conflict but run out of order"
         before = sorted((pos[i], i) for i in range(n) if pos[i] < pos[j] and conflict(jobs[i], jobs[j], M))
-        if not before:
-            assert (src[j], dep[j]) == (-1, -1), j
-            continue
-        last = before[-1][1]
-        if feeds(jobs[last], jobs[j], M):
-            assert src[j] == last, j
-            assert dep[j] == (before[-2][1] if len(before) > 1 else -1), j
-        else:
-            assert (src[j], dep[j]) == (-1, last), j
+        assert dep[j] == (before[-1][1] if before else -1), j
 
 
 def test_mixed_job_list(zq4):
     M = 2
     jobs = [
         (W, buf(0), buf(1), 768, 512, 0),         # 0 touches nothing earlier
-        (W, buf(1), buf(2), 1024, 768, 1),        # 1 x == y0 exactly: fed by 0
-        (W, buf(2), buf(3), 256, 512, 0),         # 2 x == y1 (gate_up row stride 1024 / 2)
+        (W, buf(1), buf(2), 1024, 768, 1),        # 1 x == y0: waits for 0
+        (W, buf(2), buf(3), 256, 512, 0),         # 2 x == y1 (gate_up output)
         (W, buf(1, 512), buf(4), 256, 512, 0),    # 3 x inside y0 at an offset: whole job 0
         (W, buf(5), buf(1), 768, 256, 0),         # 4 y over y0 / x1 / x3: whole job 3
-        (W, buf(1), buf(6), 512, 768, 0),         # 5 x == y4; y0 (older) meets x5 too
+        (W, buf(1), buf(6), 512, 768, 0),         # 5 x == y4 (and y0, older)
         (W, buf(6), buf(2), 512, 512, 0),         # 6 x == y5; y over y1 / x2
         (W, buf(7), buf(6), 256, 512, 0),         # 7 y over y5 / x6
     ]
-    order, src, dep = zq4.stack_plan_waits(jobs, M)
+    order, dep = zq4.stack_plan_waits(jobs, M)
     # job 2 would wait at once for job 1: job 3 (free of every job still to
     # place) goes first; nothing else may pass job 2
     assert order == [0, 1, 3, 2, 4, 5, 6, 7]
-    assert src == [-1, 0, 1, -1, -1, 4, 5, -1]
-    assert dep == [-1, -1, -1, 0, 3, 0, 2, 6]
-    check_valid(jobs, M, order, src, dep)
+    assert dep == [-1, 0, 1, 0, 3, 4, 5, 6]
+    check_valid(jobs, M, order, dep)
 
 
 def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
@@ -91,46 +77,45 @@ def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
         jobs += [(W, buf(b), buf(b + 1), 9216, 3072, 0), (W, buf(b + 2), buf(b + 3), 3072, 3072, 0),
                  (W, buf(b + 4), buf(b + 5), 16384, 3072, 1), (W, buf(b + 5), buf(b + 6), 3072, 8192, 0)]
     jobs.append((W, buf(99), buf(98), 32064, 3072, 0))
-    order, src, dep = zq4.stack_plan_waits(jobs, 1)
-    # down of layer l waits chunk-wise on its gate_up; it is put after work
-    # as large as that gate_up: the next layer's qkv, o (and gate_up)
+    order, dep = zq4.stack_plan_waits(jobs, 1)
+    # down of layer l waits for its gate_up; it is put after work as large
+    # as that gate_up: the next layer's qkv, o (and gate_up)
     assert order == [0, 1, 2, 4, 5, 6, 3, 8, 7, 9, 10, 12, 11]
-    assert src == [-1, -1, -1, 2, -1, -1, -1, 6, -1, -1, -1, 10, -1]
-    assert dep == [-1] * 13
-    check_valid(jobs, 1, order, src, dep)
+    assert dep == [-1, -1, -1, 2, -1, -1, -1, 6, -1, -1, -1, 10, -1]
+    check_valid(jobs, 1, order, dep)
 
 
 def test_a_chain_keeps_its_order(zq4):
     # every job reads the one before: nothing may move
     jobs = [(W, buf(i), buf(i + 1), 256, 256, 0) for i in range(6)]
-    order, src, dep = zq4.stack_plan_waits(jobs, 3)
+    order, dep = zq4.stack_plan_waits(jobs, 3)
     assert order == list(range(6))
-    assert src == [-1, 0, 1, 2, 3, 4] and dep == [-1] * 6
+    assert dep == [-1, 0, 1, 2, 3, 4]
 
 
 def test_exact_address_but_other_stride_waits_for_the_whole_job(zq4):
     # y0 is [M, 512]; x1 starts at y0 but is read as [M, 256] rows
     jobs = [(W, buf(0), buf(1), 512, 256, 0), (W, buf(1), buf(2), 64, 256, 0)]
     for M in (1, 2):
-        assert zq4.stack_plan_waits(jobs, M) == ([0, 1], [-1, -1], [-1, 0])
+        assert zq4.stack_plan_waits(jobs, M) == ([0, 1], [-1, 0])
 
 
 def test_exact_input_but_output_over_the_previous_input(zq4):
     # x1 == y0, but y1 overwrites x0: job 1 waits for all of job 0
     jobs = [(W, buf(0), buf(1), 256, 256, 0), (W, buf(1), buf(0), 256, 256, 0)]
-    assert zq4.stack_plan_waits(jobs, 1) == ([0, 1], [-1, -1], [-1, 0])
+    assert zq4.stack_plan_waits(jobs, 1) == ([0, 1], [-1, 0])
 
 
 def test_meeting_depends_on_M(zq4):
     # x1 starts 1024 bytes after y0: y0 spans M * 256 * 2 bytes
     jobs = [(W, buf(0), buf(1), 256, 256, 0), (W, buf(1, 1024), buf(2), 64, 256, 0)]
-    assert zq4.stack_plan_waits(jobs, 2) == ([0, 1], [-1, -1], [-1, -1])      # y0 ends at 1024
-    assert zq4.stack_plan_waits(jobs, 3) == ([0, 1], [-1, -1], [-1, 0])       # y0 ends at 1536
+    assert zq4.stack_plan_waits(jobs, 2) == ([0, 1], [-1, -1])      # y0 ends at 1024
+    assert zq4.stack_plan_waits(jobs, 3) == ([0, 1], [-1, 0])       # y0 ends at 1536
 
 
 def test_reads_of_the_same_buffer_do_not_order(zq4):
     jobs = [(W, buf(0), buf(1), 256, 256, 0), (W, buf(0), buf(2), 256, 256, 0), (W, buf(0), buf(3), 256, 256, 0)]
-    assert zq4.stack_plan_waits(jobs, 4) == ([0, 1, 2], [-1] * 3, [-1] * 3)
+    assert zq4.stack_plan_waits(jobs, 4) == ([0, 1, 2], [-1] * 3)
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -153,8 +138,8 @@ def test_random_job_lists_keep_conflicting_jobs_in_order(zq4, seed):
         else:
             xb_addr = buf(xb, xo)
         jobs.append((W, xb_addr, buf(yb), N, K, gu))
-    order, src, dep = zq4.stack_plan_waits(jobs, M)
-    check_valid(jobs, M, order, src, dep)
+    order, dep = zq4.stack_plan_waits(jobs, M)
+    check_valid(jobs, M, order, dep)
 
 
 def test_waits_reject_bad_jobs(zq4):

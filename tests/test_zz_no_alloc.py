@@ -59,5 +59,5 @@ def test_static_plan_rejects_more_jobs_than_it_holds():
     wq, sc, x, y, N, K, gu = s.jobs()[0]
     seg, _ = zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED)
     with pytest.raises(zq4.Zq4Error, match="UNSUPPORTED"):
-        zq4.StaticStackPlan([(seg, x, y, N, K, gu)] * 1219, 1)
-    zq4.StaticStackPlan([(seg, x, y, N, K, gu)] * 1218, 1)     # the documented limit fits
+        zq4.StaticStackPlan([(seg, x, y, N, K, gu)] * 1258, 1)
+    zq4.StaticStackPlan([(seg, x, y, N, K, gu)] * 1257, 1)     # the documented limit fits
