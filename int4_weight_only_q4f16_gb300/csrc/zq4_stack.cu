@@ -461,9 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         // it last. s_chunk[c] = j + 1 once chunk c of job j is staged
         // (monotone, so a fast compute warp can never mistake an earlier
         // job's chunk for this one's). x of a job that does depend on an
-        // earlier one is staged by the compute warps after their wait.
+        // earlier one is staged by the compute warps after their wait, and so
+        // is every x when there is one buffer only (nothing to stage ahead
+        // into; the compute threads move it in one round trip).
         bool stop = false;
-        for (int j = 0; j < n && !stop; ++j) {
+        for (int j = 0; j < n && !stop && p.x_bufs > 1; ++j) {
             const Job &jb = job(j);
             if ((jb.flags >> kDepShift) != 0) continue;
             if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs)) {
@@ -579,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             const uint8_t *xrj = xr + (j % p.x_bufs) * xs_size;
             unsigned long long seen = 0;          // x chunks of this job known to be staged
             const int dep = (jb.flags >> kDepShift) - 1;
-            if (dep >= 0) {
-                // x depends on earlier jobs: every CTA must be done with job
-                // dep (thread 0 waits; the barrier passes its acquire on), then
-                // the compute threads stage x, all loads in one round trip
-                if (threadIdx.x == 0) {
+            if (dep >= 0 || p.x_bufs == 1) {
+                // x depends on earlier jobs (every CTA must be done with job
+                // dep: thread 0 waits, the barrier passes its acquire on) or
+                // there is no buffer to stage ahead into: the compute threads
+                // stage x, all loads in one round trip
+                if (threadIdx.x == 0 && dep >= 0) {
                     const unsigned long long t0 = globaltimer();
                     while (ld_acquire(&p.job_cnt[dep]) < target) {
                         if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {

@@ -254,3 +254,30 @@ def test_stack_orders_jobs_that_share_buffers(oracle, M):
     err = np.abs(got[written] - host[written])
     bound = 2.0 ** -6 * S_img[written] + 2.0 ** -10 * np.abs(host[written]) + 2.0 ** -24
     assert np.all(err <= bound), f"{int((err > bound).sum())} values off; worst {float((err - bound).max())}"
+
+
+def test_stack_with_one_x_buffer(oracle):
+    """M = 4 and K = 8192 leave room for one x buffer only: the compute
+    threads stage x of every job (independent ones and the one that reads
+    an earlier output); each job matches the oracle on its input."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    M, K = 4, 8192
+    rng = synth.rng_for("stack_onebuf", M)
+    x0 = dev(synth.activations(rng, M, K))
+    x2 = dev(synth.activations(rng, M, K))
+    spec = [(8192, False, x0), (1024, True, None), (256, False, x2)]   # job 1 reads job 0's output
+    jobs, mats, ys = [], [], []
+    for i, (N, gu, x) in enumerate(spec):
+        # unit-gain scales: a gate_up on a 8192-wide output of |N(0, 0.02)|
+        # scales would overflow f16
+        wq_h, sc_h = synth.weight("stack_onebuf_w", N, K, i, sigma=synth.unit_gain_sigma(K, gu), signed=True)
+        seg, _ = zq4.prepare_weight(dev(wq_h), dev(sc_h), N, K, zq4.PREP_SEGMENTED)
+        y = torch.full((M, N // 2 if gu else N), float("nan"), dtype=torch.float16, device="cuda")
+        jobs.append((seg, ys[0] if x is None else x, y, N, K, gu))
+        mats.append((dev(wq_h), dev(sc_h)))
+        ys.append(y)
+    zq4.StackPlan(jobs, M).run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    for i, ((seg, x, y, N, K_, gu), (wq, sc)) in enumerate(zip(jobs, mats)):
+        _check_job(oracle, (wq, sc, x, y, N, K_, gu), f"one-buffer job {i}")
