@@ -1,26 +1,24 @@
-// zq4_stack.cu -- a whole decode step (an ordered list of q4f16_1
-// projections, each reading an activation the previous ones may have
-// written) as one persistent cooperative kernel.
+// zq4_stack.cu -- a whole decode step (a list of q4f16_1 projections, some
+// reading activations that earlier ones write) as one persistent
+// cooperative kernel.
 //
-// What it computes: for every job j in order, y_j = x_j * W_j^T, or the fused
-// gate_up + SiLU*mul output for interleaved gate/up rows ("Zero TVM
-// Documentation", section "Q4F16 quantization format", cards 5 "int4 Matmul"
-// and 6 "Fused FFN"; the per-token dispatch sequence of its "Decode loop"
-// section). Every job starts only after the previous job's outputs are all
-// written, as in a decode step where each projection consumes the one
-// before it.
+// What it computes: for every job j, y_j = x_j * W_j^T, or the fused gate_up
+// + SiLU*mul output for interleaved gate/up rows ("Zero TVM Documentation",
+// section "Q4F16 quantization format", cards 5 "int4 Matmul" and 6 "Fused
+// FFN"; the per-token dispatch sequence of its "Decode loop" section), with
+// the results of running the jobs one after another in the given order.
 //
 // Why one kernel: with one launch per projection, every projection pays the
 // kernel boundary (drain, launch, first-copy latency) and the small ones
 // (few 16-row tiles) leave most SMs idle. Here each SM keeps streaming
-// weights across job boundaries: its warps request the next jobs' segments
-// into their shared-memory rings and L2 while the grid waits for the
-// current job's last outputs; only the activation dependency synchronizes.
+// weights across job boundaries, and a job waits only where its buffers
+// meet an earlier job's.
 //
 // How:
 //  * Grid = one CTA per SM (cooperative launch, so all CTAs are resident
-//    and may wait on one another): 12 compute warps and one copy warp. Work
-//    unit = a segment, 16 weight rows x 256 columns.
+//    and may wait on one another): 12 compute warps, a copy warp, an x warp
+//    and a release warp. Work unit = a segment, 16 weight rows x 256
+//    columns.
 //  * The weights are in the segmented layout (zq4_prepare_weight,
 //    ZQ4_PREP_SEGMENTED): each segment is 2304 contiguous bytes (swizzled
 //    codes, then scales), so one bulk copy fills a shared-memory slot and no
@@ -30,27 +28,33 @@
 //    boundaries, so the compute warps never spend issue slots on copies.
 //    Per 32-column group, lane (r, t) (r = lane/4, t = lane%4) takes word t
 //    of rows r and r+8 (ldmatrix.x4 fetches two groups, conflict-free on the
-//    swizzle),
-//    unpacks exact f16 (q - 7) pairs as the A fragments of two chained
-//    m16n8k16 MMAs against the matching pair-permuted x chunk, and adds the
-//    fp32 result times the fp32 group scale to its accumulator.
-//  * CTA c takes the whole 16-row tiles [c*T/G, (c+1)*T/G) of every job and
-//    splits their segments evenly over its warps. A tile that lies in one
-//    warp's range is written by that warp; a warp holding part of a tile
-//    parks the part in shared memory, and at the end of the job all threads
-//    of the CTA sum the parked parts of every split tile in warp order
-//    (bit-reproducible) and write them. Tiles never span CTAs, so no partial
-//    sum goes through global memory.
-//  * Job boundary: CTA barrier, split tiles summed, one release-add per CTA
-//    on the job's counter, acquire-poll until every CTA has arrived, CTA
-//    barrier. x of the next job is staged into shared memory with L2 reads
-//    (it may have been written by other SMs during this kernel): after the
-//    poll, or, when no earlier job of the plan writes any byte of it (decided
-//    when the plan is made), already before the split-tile sums, so that its
-//    latency hides behind them and the poll.
-//  * The job table (as much of it as fits next to the rings) is copied to
-//    shared memory once per launch; each warp's copy iterator and tile
-//    position advance incrementally (no division per segment).
+//    swizzle), unpacks exact f16 (q - 7) pairs as the A fragments of two
+//    chained m16n8k16 MMAs against the matching pair-permuted x chunk, and
+//    adds the fp32 result times the fp32 group scale to its accumulator.
+//  * Tiles (16 output rows) are dealt round-robin over the CTAs, the jobs'
+//    tiles as one sequence (Job::off), so per-CTA work over a run of jobs
+//    is even to within one tile. A CTA splits the segments of its tiles
+//    evenly over its compute warps; a tile that lies in one warp's range is
+//    written by that warp, a warp holding part of a tile parks the part in
+//    shared memory, and after a CTA barrier all compute threads sum the
+//    parked parts of every split tile in warp order (bit-reproducible).
+//    Tiles never span CTAs, so no partial sum goes through global memory.
+//  * Order (decided on the host from the buffers' byte ranges): a job waits
+//    only for the last earlier job it conflicts with (one of them writes
+//    bytes the other reads or writes), until every CTA has added itself to
+//    that job's counter; conflicting jobs keep their order, others may be
+//    run earlier (see schedule()).
+//  * x: the x warp stages x of jobs that wait for nothing into up to four
+//    shared buffers ahead of the compute warps (monotone per-chunk counters
+//    tell them what is there); x of a job that waits is staged by the
+//    compute threads after the wait, in one round trip, and so is every x
+//    when only one buffer fits.
+//  * After a job's sums, the release warp makes the CTA's outputs visible
+//    (one GPU-scope fence) and adds the CTA to the job's counter, off the
+//    compute warps' path.
+//  * The job table (as much of it as fits) is copied to shared memory once
+//    per launch; each warp's copy iterator and tile position advance
+//    incrementally (no division per segment).
 //  * Counters grow monotonically: a launch waits for (launch index + 1) x
 //    grid arrivals, the launch index being read from the plan at start and
 //    advanced by the last CTA to finish.
