@@ -81,6 +81,11 @@ def _load(mutant: int = 0):
                                             _i64, _p, _p]
         lib.zo_moe_down_combine.restype = _i64
         lib.zo_argmax.argtypes = [_p, _i64, _i64, _p]
+        lib.zo_weight_affine.argtypes = [_p, _p, _p, _i64, _i64, _i64]
+        lib.zo_weight_affine.restype = ctypes.c_double
+        lib.zo_dequant_affine.argtypes = [_p, _p, _p, _i64, _i64, _p]
+        lib.zo_gemv_affine_rows.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
+        lib.zo_gate_up_silu_affine.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p]
         lib.zo_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -149,6 +154,41 @@ class Oracle:
 
     def silu(self, z: float) -> float:
         return self.lib.zo_silu(float(z))
+
+    # --- MLX affine format (w = s q + b, groups of 64) -------------------------
+    def weight_affine(self, wq, scales, biases, K: int, n: int, k: int) -> float:
+        wq, sc, bi = _u32(wq), _f16(scales), _f16(biases)
+        return self.lib.zo_weight_affine(_ptr(wq), _ptr(sc), _ptr(bi), K, n, k)
+
+    def dequant_affine(self, wq, scales, biases, N: int, K: int) -> np.ndarray:
+        wq, sc, bi = _u32(wq), _f16(scales), _f16(biases)
+        out = np.empty((N, K), dtype=np.float64)
+        self.lib.zo_dequant_affine(_ptr(wq), _ptr(sc), _ptr(bi), N, K, _ptr(out))
+        return out
+
+    def gemv_affine(self, wq, scales, biases, x, N: int, K: int, rows=None):
+        """y_ref, Sa (both [M, N] or [M, len(rows)] fp64); Sa = sum |x| (|s| q + |b|)."""
+        wq, sc, bi, xx = _u32(wq), _f16(scales), _f16(biases), _f16(x)
+        M = xx.size // K if K else 0
+        if rows is None:
+            R, rp = N, None
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            R, rp = rows.size, rows
+        y = np.empty((M, R), dtype=np.float64)
+        S = np.empty((M, R), dtype=np.float64)
+        self.lib.zo_gemv_affine_rows(_ptr(wq), _ptr(sc), _ptr(bi), _ptr(xx), M, N, K,
+                                     None if rp is None else _ptr(rp), R, _ptr(y), _ptr(S))
+        return y, S
+
+    def gate_up_silu_affine(self, wq, scales, biases, x, N2: int, K: int):
+        """h_ref, Sh ([M, N2/2] fp64) over interleaved gate/up rows."""
+        wq, sc, bi, xx = _u32(wq), _f16(scales), _f16(biases), _f16(x)
+        M = xx.size // K if K else 0
+        h = np.empty((M, N2 // 2), dtype=np.float64)
+        Sh = np.empty((M, N2 // 2), dtype=np.float64)
+        self.lib.zo_gate_up_silu_affine(_ptr(wq), _ptr(sc), _ptr(bi), _ptr(xx), M, N2, K, _ptr(h), _ptr(Sh))
+        return h, Sh
 
     def gate_up_silu(self, wq, scales, x, N2: int, K: int, interleaved: bool = True,
                      parts: bool = False):

@@ -28,11 +28,19 @@
  *            prefill": per (token, slot) the expert index comes from the
  *            routing ids, experts never mix tokens, and a combine sums the
  *            slots of one token weighted by the router scores.
+ *  [DOC-AFF] "Zero TVM Documentation", section "Qwen3.6-35B-A3B MoE", and
+ *            "Zero-TVM benchmarks", sections "Chunked prefill for
+ *            plain-attention + MLX-affine specs" and "Affine wide loads":
+ *            the MLX affine format, value = scale * code + bias with one
+ *            scale and one bias per 64 weights (a pair of u32 words covers a
+ *            quarter of a group, so a group is 8 words of 8 codes).
  *
  * Readings where the pages are silent (the same list is kept with the design
  * notes): SiLU(z) = z / (1 + e^-z); gate/up "interleaved" layout puts gate row
  * j at row 2j and up row j at row 2j+1, "concatenated" puts gate rows first;
- * an expert id outside [0, E) contributes nothing and is counted.
+ * an expert id outside [0, E) contributes nothing and is counted. Affine
+ * format: the codes are packed as in q4f16_1 (LSB-first, 8 per word) and are
+ * unsigned (no zero point); scales and biases are f16 arrays [N, K/64].
  *
  * Arithmetic is IEEE fp64 throughout. The dequantized weight (q-7)*s is exact
  * in fp64 (4-bit integer times an 11-bit significand). Sums are taken in
@@ -145,6 +153,37 @@ double zo_weight(const uint32_t *wq, const uint16_t *scales, int64_t K, int64_t 
 #else
     return (double)(q - 7) * s;
 #endif
+}
+
+/* [DOC-AFF] w[n,k] = s[n,k/64] * q[n,k] + b[n,k/64]: exact in fp64 (a 4-bit
+ * integer times an 11-bit significand, plus an f16) unless the exponents of
+ * s*q and b differ by more than 38, when it is rounded once. */
+double zo_weight_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, int64_t K,
+                        int64_t n, int64_t k)
+{
+    int q = zo_code(wq, K, n, k);
+#if ZO_MUTANT == 7
+    int64_t g = (k / 32) % (K / 64);   /* mutant: groups of 32 */
+#else
+    int64_t g = k / 64;
+#endif
+    double s = zo_f16_to_f64(scales[n * (K / 64) + g]);
+    double b = zo_f16_to_f64(biases[n * (K / 64) + g]);
+#if ZO_MUTANT == 8
+    (void)b;
+    return s * (double)q;              /* mutant: bias dropped */
+#else
+    return s * (double)q + b;
+#endif
+}
+
+/* [DOC-AFF] whole matrix, w[n*K + k]. */
+void zo_dequant_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, int64_t N, int64_t K,
+                       double *w)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) w[n * K + k] = zo_weight_affine(wq, scales, biases, K, n, k);
 }
 
 /* Dequantized row n into w[0..K). */
@@ -265,6 +304,68 @@ void zo_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t 
         free(wg);
         free(wu);
     }
+}
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-AFF], [DOC-MM]: y[m,n] = sum_k x[m,k] * w[n,k] with the affine       */
+/* weights, and the tolerance scale of this format, Sa[m,n] = sum_k |x[m,k]| */
+/* (|s| q + |b|): the sum the two halves of s * sum(x q) + b * sum(x) are    */
+/* each bounded by (where w ~ 0 through s q ~ -b, |x w| is not).            */
+/* rows as in zo_gemv_rows.                                                 */
+/* ---------------------------------------------------------------------- */
+void zo_gemv_affine_rows(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
+                         int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t R, double *y, double *Sa)
+{
+    int64_t count = rows ? R : N;
+    #pragma omp parallel
+    {
+        double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        double *wa = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < count; ++i) {
+            int64_t n = rows ? rows[i] : i;
+            for (int64_t k = 0; k < K; ++k) {
+                w[k] = zo_weight_affine(wq, scales, biases, K, n, k);
+                int64_t g = k / 64;
+                wa[k] = fabs(zo_f16_to_f64(scales[n * (K / 64) + g])) * (double)zo_code(wq, K, n, k) +
+                        fabs(zo_f16_to_f64(biases[n * (K / 64) + g]));
+            }
+            for (int64_t m = 0; m < M; ++m) {
+                double acc = 0.0, sabs = 0.0;
+                for (int64_t k = 0; k < ZO_KEND(K); ++k) {
+                    double xv = zo_f16_to_f64(x[m * K + k]);
+                    acc += xv * w[k];
+                    sabs += fabs(xv) * wa[k];
+                }
+                y[m * count + i] = acc;
+                Sa[m * count + i] = sabs;
+            }
+        }
+        free(w);
+        free(wa);
+    }
+}
+
+/* [DOC-AFF], [DOC-FFN]: h[m,j] = silu(g[m,j]) * u[m,j] over interleaved      */
+/* gate/up rows (gate j = row 2j, up j = row 2j+1) of affine weights, with   */
+/* the propagated tolerance scale Sh = |silu'(g) u| Sa_g + |silu(g)| Sa_u.   */
+/* ---------------------------------------------------------------------- */
+void zo_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                            const uint16_t *x, int64_t M, int64_t N2, int64_t K, double *h, double *Sh)
+{
+    int64_t I = N2 / 2;
+    double *g = (double *)malloc(sizeof(double) * (size_t)(M * N2 > 0 ? M * N2 : 1));
+    double *Sa = (double *)malloc(sizeof(double) * (size_t)(M * N2 > 0 ? M * N2 : 1));
+    zo_gemv_affine_rows(wq, scales, biases, x, M, N2, K, NULL, 0, g, Sa);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < I; ++j) {
+            double gv = g[m * N2 + 2 * j], uv = g[m * N2 + 2 * j + 1];
+            double a = zo_silu(gv);
+            h[m * I + j] = a * uv;
+            Sh[m * I + j] = fabs(zo_silu_deriv(gv) * uv) * Sa[m * N2 + 2 * j] + fabs(a) * Sa[m * N2 + 2 * j + 1];
+        }
+    free(g);
+    free(Sa);
 }
 
 /* ---------------------------------------------------------------------- */

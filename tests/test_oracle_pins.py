@@ -362,6 +362,97 @@ def test_argmax_hand_cases(oracle):
 
 
 # --------------------------------------------------------------------------
+# the MLX affine format: w = s * q + b, one scale and one bias per 64 weights
+# --------------------------------------------------------------------------
+def _patterned_affine(N, K, seed=4):
+    """codes q[n,k] = (5n + k) mod 16, distinct scales and biases per (n, group of 64)."""
+    n = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    codes = (5 * n + k) % 16
+    rng = np.random.default_rng(seed)
+    sc = (rng.random((N, K // 64)) * 0.9 + 0.05).astype(np.float16)
+    bi = (rng.random((N, K // 64)) * 2.0 - 1.0).astype(np.float16)
+    return codes, pack_codes(codes), sc, bi
+
+
+def test_affine_one_hot_columns_exact(oracle):
+    """x = e_k returns s[n, k // 64] * q[n,k] + b[n, k // 64] exactly, with
+    two groups whose scales and biases differ (k = 63 and 64 fall in
+    different groups; a group of 32 would not split there)."""
+    N, K = 10, 128
+    codes, wq, sc, bi = _patterned_affine(N, K)
+    for k in range(K):
+        x = np.zeros((1, K), dtype=np.float16)
+        x[0, k] = 1.0
+        y, Sa = oracle.gemv_affine(wq, sc, bi, x, N, K)
+        s_, b_ = sc[:, k // 64].astype(np.float64), bi[:, k // 64].astype(np.float64)
+        want = s_ * codes[:, k] + b_
+        assert np.array_equal(y[0], want), k
+        assert np.array_equal(Sa[0], np.abs(s_) * codes[:, k] + np.abs(b_))
+
+
+def test_affine_closed_form_constant_codes(oracle):
+    """All codes c, scales s and biases b: y = (s c + b) * sum_k x_k; zero
+    exactly when s c + b = 0 in exact arithmetic."""
+    rng = np.random.default_rng(13)
+    N, K = 3, 256
+    x = synth.activations(rng, 2, K)
+    xs = x.astype(np.float64).sum(axis=1)
+    for c in (0, 1, 7, 15):
+        wq = np.full((N, K // 8), c * 0x11111111, dtype=np.uint32)
+        for s_, b_ in ((0.5, -3.5), (0.0137, 0.25), (2.0, 0.0), (0.25, -0.25 * c)):
+            sc = np.full((N, K // 64), s_, dtype=np.float16)
+            bi = np.full((N, K // 64), b_, dtype=np.float16)
+            wv = float(sc[0, 0]) * c + float(bi[0, 0])
+            y, Sa = oracle.gemv_affine(wq, sc, bi, x, N, K)
+            assert np.allclose(y, (wv * xs)[:, None], rtol=0, atol=1e-12 * max(1.0, Sa.max()))
+            if wv == 0.0:
+                assert np.all(y == 0.0)
+
+
+def test_affine_brute_force_exact_rationals(oracle):
+    """2 x 128 activations against 3 x 128 affine weights in exact rational
+    arithmetic, codes read through the hex-digit route."""
+    rng = np.random.default_rng(17)
+    M, N, K = 2, 3, 128
+    wq = synth.packed_codes(rng, N, K)
+    sc = (rng.random((N, K // 64)) * 0.05).astype(np.float16)
+    bi = (rng.standard_normal((N, K // 64)) * 0.1).astype(np.float16)
+    x = synth.activations(rng, M, K)
+    y, Sa = oracle.gemv_affine(wq, sc, bi, x, N, K)
+    for n in range(N):
+        codes = sum((codes_by_hex(int(w)) for w in wq[n]), [])
+        wrow = [Fraction(float(sc[n, k // 64])) * codes[k] + Fraction(float(bi[n, k // 64])) for k in range(K)]
+        wabs = [abs(Fraction(float(sc[n, k // 64]))) * codes[k] + abs(Fraction(float(bi[n, k // 64])))
+                for k in range(K)]
+        for m in range(M):
+            exact = sum(Fraction(float(x[m, k])) * wrow[k] for k in range(K))
+            sabs = sum(abs(Fraction(float(x[m, k]))) * wabs[k] for k in range(K))
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(1, 10 ** 12) * sabs
+            assert abs(Fraction(Sa[m, n]) - sabs) <= Fraction(1, 10 ** 12) * sabs
+
+
+def test_affine_gate_up_brute_force(oracle):
+    """h = silu(g) * u over interleaved affine rows, against a direct fp64
+    computation from hex-decoded codes."""
+    rng = np.random.default_rng(19)
+    M, N2, K = 2, 6, 128
+    wq = synth.packed_codes(rng, N2, K)
+    sc = (rng.random((N2, K // 64)) * 0.05).astype(np.float16)
+    bi = (rng.standard_normal((N2, K // 64)) * 0.1).astype(np.float16)
+    x = synth.activations(rng, M, K)
+    h, Sh = oracle.gate_up_silu_affine(wq, sc, bi, x, N2, K)
+    w = np.array([[float(sc[n, k // 64]) * sum((codes_by_hex(int(v)) for v in wq[n]), [])[k] + float(bi[n, k // 64])
+                   for k in range(K)] for n in range(N2)])
+    for m in range(M):
+        for j in range(N2 // 2):
+            g = float(np.dot(x[m].astype(np.float64), w[2 * j]))
+            u = float(np.dot(x[m].astype(np.float64), w[2 * j + 1]))
+            want = g / (1.0 + math.exp(-g)) * u
+            assert abs(h[m, j] - want) <= 1e-12 * (abs(want) + Sh[m, j] + 1e-300)
+
+
+# --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
 def _pins_pass(o) -> bool:
@@ -373,12 +464,15 @@ def _pins_pass(o) -> bool:
         test_silu_values(o)
         test_gate_up_brute_force(o)
         test_argmax_hand_cases(o)
+        test_affine_one_hot_columns_exact(o)
+        test_affine_closed_form_constant_codes(o)
+        test_affine_brute_force_exact_rationals(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
