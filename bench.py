@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
     ap.add_argument("--gate-up", action="store_true", help="kernel workload: fused gate_up + SiLU*mul")
+    ap.add_argument("--affine", action="store_true",
+                    help="kernel workload: the MLX affine format (w = s q + b, groups of 64)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight copies (kernel workload)")
     ap.add_argument("--eager", action="store_true", help="kernel workload: plain launches, no graph")
     ap.add_argument("--m", type=int, default=1, help="tokens per step (qwen3 workload)")
@@ -619,18 +621,30 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
     graph of them, or plain launches with --eager, e.g. under a profiler)."""
     from int4_weight_only_q4f16_gb300 import synth, zq4
     N, K, M, C = args.n, args.k, args.m, args.copies
+    gs = 64 if args.affine else 32                  # weights per scale
     wq, sc = synth.weight("kernel", N, K, 0)
+    if args.affine:                                 # one scale and one bias per 64 weights
+        sc = sc[:, ::2].copy()
+        bi = (-8.0 * sc.astype(np.float32)).astype(np.float16)
+        B = torch.from_numpy(bi).cuda().repeat(C, 1).view(C, N, K // gs)
     W = torch.from_numpy(wq.view(np.int32)).cuda().repeat(C, 1).view(C, N, K // 8)
-    S = torch.from_numpy(sc).cuda().repeat(C, 1).view(C, N, K // 32)
+    S = torch.from_numpy(sc).cuda().repeat(C, 1).view(C, N, K // gs)
     x = torch.from_numpy(synth.activations(synth.rng_for("kernel_x"), M, K)).cuda()
     cols = N // 2 if args.gate_up else N
     y = torch.empty((C, M, cols), dtype=torch.float16, device="cuda")
-    f = zq4.gate_up_silu if args.gate_up else zq4.gemv
     stream = torch.cuda.Stream()
+    if args.affine:
+        fa = zq4.gate_up_silu_affine if args.gate_up else zq4.gemv_affine
 
-    def chain():
-        for c in range(C):
-            f(W[c], S[c], x, N, K, y[c], stream=stream)
+        def chain():
+            for c in range(C):
+                fa(W[c], S[c], B[c], x, N, K, y[c], stream=stream)
+    else:
+        f = zq4.gate_up_silu if args.gate_up else zq4.gemv
+
+        def chain():
+            for c in range(C):
+                f(W[c], S[c], x, N, K, y[c], stream=stream)
     reps = max(1, args.steps // C)
     if args.eager:
         with torch.cuda.stream(stream):
@@ -646,8 +660,9 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
     torch.cuda.synchronize()
     assert torch.isfinite(y).all() and (y != 0).any(), "kernel output zero/non-finite"
     per = el / (reps * C)
-    b = N * (K // 8) * 4 + N * (K // 32) * 2 + M * K * 2 + M * cols * 2
-    return {"metric": f"{'gate_up+SiLU' if args.gate_up else 'GEMV'} {N}x{K} M={M} achieved HBM GB/s",
+    b = N * (K // 8) * 4 + N * (K // gs) * 2 * (2 if args.affine else 1) + M * K * 2 + M * cols * 2
+    kind = ("MLX affine " if args.affine else "") + ("gate_up+SiLU" if args.gate_up else "GEMV")
+    return {"metric": f"{kind} {N}x{K} M={M} achieved HBM GB/s",
             "value": round(b / per / 1e9, 1), "unit": "GB/s", "us_per_call": round(per * 1e6, 3),
             "bytes_per_call": b, "frac_of_measured": round(b / per / 1e9 / peaks["hbm_gbs"], 4),
             "config": {"workload": f"kernel {N}x{K} M={M}", "copies": C, "graph": not args.eager,

@@ -125,6 +125,34 @@ ZQ4_API zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, 
                             uint16_t *h, int M, int N2, int K, void *stream);
 
 /*
+ * zq4_gemv_affine / zq4_gate_up_silu_affine -- zq4_gemv and
+ * zq4_gate_up_silu on weights in the MLX affine format:
+ *   value w[n,k] = s[n, k/64] * q[n,k] + b[n, k/64]
+ * with q the unsigned 4-bit code (packed as in q4f16_1: 8 per uint32,
+ * element i of a word in bits 4i..4i+3, no zero point) and one f16 scale
+ * and one f16 bias per 64 weights. Source: "Zero TVM Documentation",
+ * section "Qwen3.6-35B-A3B MoE" (affine w = s*q + b, group 64, per-tensor
+ * biases); "Zero-TVM benchmarks", sections "Chunked prefill for
+ * plain-attention + MLX-affine specs" and "Affine wide loads" (a u32 pair
+ * is a quarter of a group).
+ *
+ *   wq [N, K/8] uint32   scales [N, K/64] f16   biases [N, K/64] f16
+ *   x [M, K] f16         y [M, N] f16 (h [M, N2/2] for gate_up, rows
+ *                        interleaved as in zq4_gate_up_silu)
+ * Per 64-weight group the product is s * sum(x q) + b * sum(x), fp32.
+ * M >= 1 (blocks of up to 8 tokens per launch), N >= 1 (N2 even), K a
+ * multiple of 64. wq and x 16-byte aligned, scales, biases and the output
+ * 2-byte aligned; the output must not overlap any input. Device pointers,
+ * caller-owned. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
+ * ZQ4_ERR_OVERLAP, ZQ4_ERR_UNSUPPORTED (x of K does not fit in shared
+ * memory), ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_gemv_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                   const uint16_t *x, uint16_t *y, int M, int N, int K, void *stream);
+ZQ4_API zq4_status zq4_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                           const uint16_t *x, uint16_t *h, int M, int N2, int K, void *stream);
+
+/*
  * zq4_gemv_argmax -- the LM-head step of decode: fp32 logits and, per token,
  * the index of the largest logit.
  * Source: "Zero TVM Documentation", section "WGSL Kernel Roles" (the LM-head

@@ -129,7 +129,7 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
     if (decode_tc_supported(M, K))
         return cuda_status(launch_decode_tc(wq, scales, x, y, M, N, K, false,
                                             static_cast<cudaStream_t>(stream)));
-    return cuda_status(launch_decode(wq, scales, x, y, M, N, K, false,
+    return cuda_status(launch_decode(wq, scales, nullptr, x, y, M, N, K, false,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -179,8 +179,49 @@ zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const ui
     if (decode_tc_supported(M, K))
         return cuda_status(launch_decode_tc(wq, scales, x, h, M, N2, K, true,
                                             static_cast<cudaStream_t>(stream)));
-    return cuda_status(launch_decode(wq, scales, x, h, M, N2, K, true,
+    return cuda_status(launch_decode(wq, scales, nullptr, x, h, M, N2, K, true,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------------
+// MLX affine format (value = scale * code + bias, groups of 64)
+// ---------------------------------------------------------------------------
+namespace {
+
+zq4_status affine_common(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
+                         const uint16_t *out, int M, int N, int K, size_t out_bytes)
+{
+    if (!wq || !scales || !biases || !x || !out) return ZQ4_ERR_NULL;
+    if (M <= 0 || N <= 0 || K <= 0 || (K % 64) != 0) return ZQ4_ERR_SHAPE;
+    if (!aligned16(wq) || !aligned16(x) || (reinterpret_cast<uintptr_t>(scales) & 1) ||
+        (reinterpret_cast<uintptr_t>(biases) & 1) || (reinterpret_cast<uintptr_t>(out) & 1))
+        return ZQ4_ERR_ALIGN;
+    if (size_t(K) * 2 + size_t(K / 32) * 4 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    const size_t gb = size_t(N) * (K / 64) * 2;
+    if (overlap(out, out_bytes, wq, wq_bytes(N, K)) || overlap(out, out_bytes, scales, gb) ||
+        overlap(out, out_bytes, biases, gb) || overlap(out, out_bytes, x, size_t(M) * K * 2))
+        return ZQ4_ERR_OVERLAP;
+    return ZQ4_OK;
+}
+
+}  // namespace
+
+zq4_status zq4_gemv_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
+                           uint16_t *y, int M, int N, int K, void *stream)
+{
+    const zq4_status st = affine_common(wq, scales, biases, x, y, M, N, K, size_t(M > 0 ? M : 0) * (N > 0 ? N : 0) * 2);
+    if (st != ZQ4_OK) return st;
+    return cuda_status(launch_decode(wq, scales, biases, x, y, M, N, K, false, static_cast<cudaStream_t>(stream)));
+}
+
+zq4_status zq4_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                   const uint16_t *x, uint16_t *h, int M, int N2, int K, void *stream)
+{
+    if (N2 > 0 && (N2 & 1)) return ZQ4_ERR_SHAPE;
+    const zq4_status st =
+        affine_common(wq, scales, biases, x, h, M, N2, K, size_t(M > 0 ? M : 0) * (N2 > 0 ? N2 / 2 : 0) * 2);
+    if (st != ZQ4_OK) return st;
+    return cuda_status(launch_decode(wq, scales, biases, x, h, M, N2, K, true, static_cast<cudaStream_t>(stream)));
 }
 
 zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, int num_experts,

@@ -23,6 +23,14 @@
 //    each CTA asks L2 to prefetch the weight rows it owns: weights never
 //    depend on the previous kernel, so the stream of weights continues
 //    across kernel boundaries.
+//
+// The dense kernel also reads the MLX affine format (AFF): value = scale *
+// code + bias, one scale and one bias per 64 weights ("Zero TVM
+// Documentation", section "Qwen3.6-35B-A3B MoE"; "Zero-TVM benchmarks",
+// "Affine wide loads"). Per 32-weight chunk it adds
+// b * sum(x) + s * sum(x * q): the codes become exact f16 q (no zero point),
+// the products are exact, and sum(x) of every chunk is taken once per CTA
+// when x is staged.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -67,19 +75,57 @@ __device__ __forceinline__ void stage_rows(uint8_t *xs, const uint16_t *src, int
     }
 }
 
+// Codes of one word to exact f16 q (no zero point), in the pair order of
+// unpack_word_f16x2: 1024 + q (or 1024 + 16 q) minus the magic.
+__device__ __forceinline__ void unpack_word_f16x2_q(uint32_t w, uint32_t p[4])
+{
+    const uint32_t kMagic = 0x64006400u;       // (1024, 1024)
+    const uint32_t kSixteenth = 0x2C002C00u;   // (1/16, 1/16)
+    const uint32_t kNeg64 = 0xD400D400u;       // (-64, -64): 1024/16
+    uint32_t w8 = w >> 8;
+    p[0] = hsub2((w & 0x000F000Fu) | kMagic, kMagic);                  // elements 0, 4
+    p[1] = hfma2((w & 0x00F000F0u) | kMagic, kSixteenth, kNeg64);      // elements 1, 5
+    p[2] = hsub2((w8 & 0x000F000Fu) | kMagic, kMagic);                 // elements 2, 6
+    p[3] = hfma2((w8 & 0x00F000F0u) | kMagic, kSixteenth, kNeg64);     // elements 3, 7
+}
+
+// sum(x) of every 32-weight chunk of rows [0, rows) of src (fp32, ascending
+// k), rows [rows, rows_alloc) zero: xsum[r * (K/32) + g].
+__device__ __forceinline__ void chunk_sums(float *xsum, const uint16_t *src, int rows, int rows_alloc, int K)
+{
+    const int G = K >> 5, total = rows_alloc * G;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int r = i / G, g = i - r * G;
+        float acc = 0.f;
+        if (r < rows) {
+            const uint16_t *p = src + size_t(r) * K + size_t(g) * 32;
+            for (int k = 0; k < 32; ++k) acc += f16_bits_to_float(p[k]);
+        }
+        xsum[i] = acc;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // One 32-weight group of one row against MT staged activation rows.
 // part[m] += s * sum_{k in group} x[m,k] * (q[k] - 7)
 // ---------------------------------------------------------------------------
-template <int MT>
-__device__ __forceinline__ void group_dot(const uint4 wv, float s, uint32_t xs_base, int g,
-                                          uint32_t row_bytes, float (&part)[MT])
+// AFF: part[m] += b * xsum[m][g] + s * sum_{k in group} x[m,k] * q[k].
+template <int MT, bool AFF>
+__device__ __forceinline__ void group_dot(const uint4 wv, float s, float b, uint32_t xs_base, int g,
+                                          uint32_t row_bytes, const float *xsum, int G, float (&part)[MT])
 {
     uint32_t p[4][4];
-    unpack_word_f16x2(wv.x, p[0]);
-    unpack_word_f16x2(wv.y, p[1]);
-    unpack_word_f16x2(wv.z, p[2]);
-    unpack_word_f16x2(wv.w, p[3]);
+    if (AFF) {
+        unpack_word_f16x2_q(wv.x, p[0]);
+        unpack_word_f16x2_q(wv.y, p[1]);
+        unpack_word_f16x2_q(wv.z, p[2]);
+        unpack_word_f16x2_q(wv.w, p[3]);
+    } else {
+        unpack_word_f16x2(wv.x, p[0]);
+        unpack_word_f16x2(wv.y, p[1]);
+        unpack_word_f16x2(wv.z, p[2]);
+        unpack_word_f16x2(wv.w, p[3]);
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float a0 = 0.f, a1 = 0.f;
@@ -91,6 +137,7 @@ __device__ __forceinline__ void group_dot(const uint4 wv, float s, uint32_t xs_b
             fma2_f16_f32(p[c][2], xv.z, a0, a1);
             fma2_f16_f32(p[c][3], xv.w, a0, a1);
         }
+        if (AFF) part[m] = fmaf(b, xsum[m * G + g], part[m]);
         part[m] = fmaf(s, a0 + a1, part[m]);
     }
 }
@@ -114,25 +161,28 @@ __device__ __forceinline__ unsigned segment_mask()
 
 // Accumulate RU consecutive rows (starting at row0) of a matrix against MT
 // staged activation rows: part[r][m] holds this lane's partial sums.
-template <int MT, int LPR, int RU>
-__device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *scales, int K,
-                                         int row0, uint32_t xs_base, int lane,
+// AFF: scales and biases [rows][K/64]; xsum = the staged chunk sums of x.
+template <int MT, int LPR, int RU, bool AFF>
+__device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, int K,
+                                         int row0, uint32_t xs_base, const float *xsum, int lane,
                                          float (&part)[RU][MT])
 {
-    const int G = K >> 5, KW = K >> 3;
+    const int G = K >> 5, KW = K >> 3, GS = AFF ? K >> 6 : G;
     const uint32_t row_bytes = uint32_t(K) * 2;
     const uint32_t *wrow[RU];
     const uint16_t *srow[RU];
+    const uint16_t *brow[RU];
 #pragma unroll
     for (int r = 0; r < RU; ++r) {
         wrow[r] = wq + size_t(row0 + r) * KW;
-        srow[r] = scales + size_t(row0 + r) * G;
+        srow[r] = scales + size_t(row0 + r) * GS;
+        brow[r] = AFF ? biases + size_t(row0 + r) * GS : nullptr;
 #pragma unroll
         for (int m = 0; m < MT; ++m) part[r][m] = 0.f;
     }
     for (int g0 = lane; g0 < G; g0 += kUnroll * LPR) {
         uint4 wv[RU][kUnroll];
-        uint16_t sv[RU][kUnroll];
+        uint16_t sv[RU][kUnroll], bv[RU][kUnroll];
 #pragma unroll
         for (int i = 0; i < kUnroll; ++i) {
             int g = g0 + i * LPR;
@@ -140,10 +190,12 @@ __device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *sca
             for (int r = 0; r < RU; ++r) {
                 if (g < G) {
                     wv[r][i] = ldg_stream_v4(wrow[r] + 4 * g);
-                    sv[r][i] = ldg_u16(srow[r] + g);
+                    sv[r][i] = ldg_u16(srow[r] + (AFF ? g >> 1 : g));
+                    bv[r][i] = AFF ? ldg_u16(brow[r] + (g >> 1)) : uint16_t(0);
                 } else {
                     wv[r][i] = make_uint4(0, 0, 0, 0);
                     sv[r][i] = 0;
+                    bv[r][i] = 0;
                 }
             }
         }
@@ -153,21 +205,24 @@ __device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *sca
             if (g < G) {
 #pragma unroll
                 for (int r = 0; r < RU; ++r)
-                    group_dot<MT>(wv[r][i], f16_bits_to_float(sv[r][i]), xs_base, g, row_bytes,
-                                  part[r]);
+                    group_dot<MT, AFF>(wv[r][i], f16_bits_to_float(sv[r][i]), f16_bits_to_float(bv[r][i]), xs_base,
+                                       g, row_bytes, xsum, G, part[r]);
             }
         }
     }
 }
 
 // L2 prefetch of rows [row_lo, row_hi) of a q4f16_1 matrix by warp 0.
-__device__ __forceinline__ void prefetch_rows(const uint32_t *wq, const uint16_t *scales, int K,
-                                              size_t row_lo, size_t row_hi)
+// (gs = scales per row: K/32, or K/64 for the affine format, whose biases
+// are prefetched too when given)
+__device__ __forceinline__ void prefetch_rows(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                              int K, int gs, size_t row_lo, size_t row_hi)
 {
     if (threadIdx.x < 32) {
-        const size_t KW = size_t(K) >> 3, G = size_t(K) >> 5;
+        const size_t KW = size_t(K) >> 3, G = size_t(gs);
         prefetch_l2_range(wq + row_lo * KW, wq + row_hi * KW, threadIdx.x, 32);
         prefetch_l2_range(scales + row_lo * G, scales + row_hi * G, threadIdx.x, 32);
+        if (biases) prefetch_l2_range(biases + row_lo * G, biases + row_hi * G, threadIdx.x, 32);
     }
 }
 
@@ -175,15 +230,19 @@ __device__ __forceinline__ void prefetch_rows(const uint32_t *wq, const uint16_t
 // Dense GEMV (RU = 1) and gate_up + SiLU*mul (RU = 2, interleaved rows).
 // A "unit" is RU consecutive rows; CTA b owns units [b*upc, (b+1)*upc).
 // ---------------------------------------------------------------------------
-template <int MT, int LPR, int RU>
+// AFF: the MLX affine format (a.biases; scales and biases per 64 weights).
+template <int MT, int LPR, int RU, bool AFF>
 __global__ void __launch_bounds__(kThreads) k_dense(DenseArgs a)
 {
     extern __shared__ __align__(16) uint8_t xs[];
+    float *xsum = reinterpret_cast<float *>(xs + size_t(MT) * a.K * 2);   // AFF: [MT][K/32]
     const int u0 = blockIdx.x * a.units_per_cta;
     const int u1 = min(u0 + a.units_per_cta, a.units);
-    prefetch_rows(a.wq, a.scales, a.K, size_t(u0) * RU, size_t(u1) * RU);
+    prefetch_rows(a.wq, a.scales, AFF ? a.biases : nullptr, a.K, AFF ? a.K >> 6 : a.K >> 5, size_t(u0) * RU,
+                  size_t(u1) * RU);
     griddep_wait();
     stage_rows(xs, a.x, a.M, MT, a.K);
+    if (AFF) chunk_sums(xsum, a.x, a.M, MT, a.K);
     __syncthreads();
     griddep_launch_dependents();
 
@@ -192,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) k_dense(DenseArgs a)
     const uint32_t xs_base = smem_addr(xs);
     for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
         float part[RU][MT];
-        rows_dot<MT, LPR, RU>(a.wq, a.scales, a.K, u * RU, xs_base, lane, part);
+        rows_dot<MT, LPR, RU, AFF>(a.wq, a.scales, a.biases, a.K, u * RU, xs_base, xsum, lane, part);
 #pragma unroll
         for (int r = 0; r < RU; ++r)
 #pragma unroll
@@ -243,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
     const uint32_t xs_base = smem_addr(xs);
     for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
         float part[2][1];
-        rows_dot<1, LPR, 2>(wq, sc, a.K, 2 * u, xs_base, lane, part);
+        rows_dot<1, LPR, 2, false>(wq, sc, nullptr, a.K, 2 * u, xs_base, nullptr, lane, part);
         float g = segment_sum<LPR>(part[0][0], mask);
         float v = segment_sum<LPR>(part[1][0], mask);
         if (lane == 0) yo[u] = float_to_f16_bits(silu_f32(g) * v);
@@ -304,8 +363,8 @@ __global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
                     int j = j0 + i;
                     if (j < a.top_k && s_ids[j] >= 0) {
                         float part[1] = {0.f};
-                        group_dot<1>(wv[i], f16_bits_to_float(sv[i]), xs_base + uint32_t(j) * row_bytes,
-                                     g, row_bytes, part);
+                        group_dot<1, false>(wv[i], f16_bits_to_float(sv[i]), 0.f,
+                                            xs_base + uint32_t(j) * row_bytes, g, row_bytes, nullptr, 0, part);
                         acc = fmaf(s_r[j], part[0], acc);
                     }
                 }
@@ -426,36 +485,40 @@ int units_per_cta(int units, int lpr)
     return upc;
 }
 
-template <int MT, int LPR, int RU>
+// Shared memory of a dense launch: x rows, and for the affine format the
+// chunk sums of x.
+size_t dense_smem(int MT, int K, bool aff) { return size_t(MT) * K * 2 + (aff ? size_t(MT) * (K >> 5) * 4 : 0); }
+
+template <int MT, int LPR, int RU, bool AFF>
 cudaError_t launch_dense_t(const DenseArgs &a, cudaStream_t s)
 {
     static int smem_set[kMaxDevices] = {};
-    auto kern = k_dense<MT, LPR, RU>;
-    size_t smem = size_t(MT) * a.K * 2;
+    auto kern = k_dense<MT, LPR, RU, AFF>;
+    size_t smem = dense_smem(MT, a.K, AFF);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
     int grid = (a.units + a.units_per_cta - 1) / a.units_per_cta;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
-template <int MT, int RU>
+template <int MT, int RU, bool AFF>
 cudaError_t launch_dense_lpr(const DenseArgs &a, cudaStream_t s)
 {
     switch (pick_lpr(a.K)) {
-    case 32: return launch_dense_t<MT, 32, RU>(a, s);
-    case 16: return launch_dense_t<MT, 16, RU>(a, s);
-    default: return launch_dense_t<MT, 8, RU>(a, s);
+    case 32: return launch_dense_t<MT, 32, RU, AFF>(a, s);
+    case 16: return launch_dense_t<MT, 16, RU, AFF>(a, s);
+    default: return launch_dense_t<MT, 8, RU, AFF>(a, s);
     }
 }
 
-template <int RU>
+template <int RU, bool AFF>
 cudaError_t launch_dense_mt(int MT, const DenseArgs &a, cudaStream_t s)
 {
     switch (MT) {
-    case 8: return launch_dense_lpr<8, RU>(a, s);
-    case 4: return launch_dense_lpr<4, RU>(a, s);
-    case 2: return launch_dense_lpr<2, RU>(a, s);
-    default: return launch_dense_lpr<1, RU>(a, s);
+    case 8: return launch_dense_lpr<8, RU, AFF>(a, s);
+    case 4: return launch_dense_lpr<4, RU, AFF>(a, s);
+    case 2: return launch_dense_lpr<2, RU, AFF>(a, s);
+    default: return launch_dense_lpr<1, RU, AFF>(a, s);
     }
 }
 
@@ -463,31 +526,37 @@ cudaError_t launch_dense_mt(int MT, const DenseArgs &a, cudaStream_t s)
 
 size_t decode_max_smem() { return 227 * 1024; }
 
-int decode_tokens_per_launch(int M, int K)
+int decode_tokens_per_launch(int M, int K, bool aff)
 {
     int mt = 8;
-    while (mt > 1 && (mt > M || size_t(mt) * K * 2 > decode_max_smem())) mt >>= 1;
+    while (mt > 1 && (mt > M || dense_smem(mt, K, aff) > decode_max_smem())) mt >>= 1;
     return mt;
 }
 
-cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+int decode_tokens_per_launch(int M, int K) { return decode_tokens_per_launch(M, K, false); }
+
+// biases != nullptr: the MLX affine format (scales and biases per 64 weights).
+cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s)
 {
     const int RU = gate_up ? 2 : 1;
     const int out_cols = N / RU;
+    const bool aff = biases != nullptr;
     DenseArgs a;
     a.wq = wq;
     a.scales = scales;
+    a.biases = biases;
     a.K = K;
     a.units = out_cols;
     a.units_per_cta = units_per_cta(a.units, pick_lpr(K));
     a.y_stride = out_cols;
     for (int m0 = 0; m0 < M;) {
-        int mt = decode_tokens_per_launch(M - m0, K);
+        int mt = decode_tokens_per_launch(M - m0, K, aff);
         a.x = x + size_t(m0) * K;
         a.y = y + size_t(m0) * out_cols;
         a.M = std::min(mt, M - m0);
-        cudaError_t e = gate_up ? launch_dense_mt<2>(mt, a, s) : launch_dense_mt<1>(mt, a, s);
+        cudaError_t e = aff ? (gate_up ? launch_dense_mt<2, true>(mt, a, s) : launch_dense_mt<1, true>(mt, a, s))
+                            : (gate_up ? launch_dense_mt<2, false>(mt, a, s) : launch_dense_mt<1, false>(mt, a, s));
         if (e != cudaSuccess) return e;
         m0 += a.M;
     }

@@ -14,6 +14,7 @@ constexpr int kMaxDevices = 64;
 struct DenseArgs {
     const uint32_t *wq;
     const uint16_t *scales;
+    const uint16_t *biases;   // MLX affine format only (else unused)
     const uint16_t *x;
     uint16_t *y;
     int M;              // activation rows in this launch (<= the kernel's MT)
@@ -92,7 +93,7 @@ cudaError_t read_prefill_error(unsigned *flags, bool clear);
 // zq4_decode.cu
 int decode_tokens_per_launch(int M, int K);
 size_t decode_max_smem();
-cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs &a, int mode, cudaStream_t s);
 cudaError_t launch_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,

@@ -38,7 +38,7 @@ PREP_SEGMENTED = 2
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
            "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
-           "zq4_gemv_argmax")
+           "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine")
 
 
 class Zq4Error(RuntimeError):
@@ -74,6 +74,8 @@ def _load():
         "zq4_dequant_f16": [P, P, P, I, I, P],
         "zq4_stack_plan_bytes": [P, I, I, P],
         "zq4_stack_plan_waits": [P, I, I, P, P],
+        "zq4_gemv_affine": [P, P, P, P, P, I, I, I, P],
+        "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -133,6 +135,36 @@ def _check(fn, status):
 
 def _mat(wq, scales, N, K):
     return (_ptr(wq, "wq", N * (K // 8) * 4, 4), _ptr(scales, "scales", N * (K // 32) * 2, 2))
+
+
+def _mat_affine(wq, scales, biases, N, K):
+    gb = N * (K // 64) * 2
+    return (_ptr(wq, "wq", N * (K // 8) * 4, 4), _ptr(scales, "scales", gb, 2), _ptr(biases, "biases", gb, 2))
+
+
+def gemv_affine(wq, scales, biases, x, N, K, y=None, stream=None):
+    """y = x @ W^T for W in the MLX affine format (zq4_gemv_affine):
+    scales and biases [N, K/64] f16."""
+    M = x.numel() // K
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    w, s, b = _mat_affine(wq, scales, biases, N, K)
+    _check("zq4_gemv_affine", lib.zq4_gemv_affine(w, s, b, _ptr(x, "x", M * K * 2, 2),
+                                                   _ptr(y, "y", M * N * 2, 2), M, N, K, _stream(stream)))
+    return y
+
+
+def gate_up_silu_affine(wq, scales, biases, x, N2, K, h=None, stream=None):
+    """h = silu(x Wg^T) * (x Wu^T), interleaved rows, MLX affine format
+    (zq4_gate_up_silu_affine)."""
+    M = x.numel() // K
+    if h is None:
+        h = torch.empty((M, N2 // 2), dtype=torch.float16, device=x.device)
+    w, s, b = _mat_affine(wq, scales, biases, N2, K)
+    _check("zq4_gate_up_silu_affine",
+           lib.zq4_gate_up_silu_affine(w, s, b, _ptr(x, "x", M * K * 2, 2), _ptr(h, "h", M * (N2 // 2) * 2, 2),
+                                       M, N2, K, _stream(stream)))
+    return h
 
 
 def gemv(wq, scales, x, N, K, y=None, stream=None):

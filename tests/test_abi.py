@@ -84,3 +84,20 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.lib.zq4_dequant_f32(P(A), P(B), P(0), 4, 64, P(0)) == lib.ZQ4_ERR_NULL
     assert lib.lib.zq4_dequant_f16(P(A), P(B), P(Y), 4, 40, P(0)) == lib.ZQ4_ERR_SHAPE
     assert lib.lib.zq4_device_errors(P(0), 1) == lib.ZQ4_ERR_NULL
+
+
+def test_affine_host_checks_reject_before_launch(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000          # fake, 16-byte aligned, never dereferenced
+    S, Bi, X, Y = A + (1 << 30), A + (2 << 30), A + (3 << 30), A + (4 << 30)
+    g = lib.lib.zq4_gemv_affine
+    assert g(P(A), P(S), P(0), P(X), P(Y), 1, 64, 64, P(0)) == lib.ZQ4_ERR_NULL       # biases required
+    assert g(P(A), P(S), P(Bi), P(X), P(Y), 1, 64, 96, P(0)) == lib.ZQ4_ERR_SHAPE     # K % 64
+    assert g(P(A), P(S), P(Bi), P(X), P(Y), 0, 64, 64, P(0)) == lib.ZQ4_ERR_SHAPE
+    assert g(P(A + 4), P(S), P(Bi), P(X), P(Y), 1, 64, 64, P(0)) == lib.ZQ4_ERR_ALIGN
+    assert g(P(A), P(S + 1), P(Bi), P(X), P(Y), 1, 64, 64, P(0)) == lib.ZQ4_ERR_ALIGN
+    assert g(P(A), P(S), P(Bi), P(X), P(Bi + 64), 1, 64, 64, P(0)) == lib.ZQ4_ERR_OVERLAP
+    assert g(P(A), P(S), P(Bi), P(X), P(Y), 1, 64, 1 << 20, P(0)) == lib.ZQ4_ERR_UNSUPPORTED
+    gu = lib.lib.zq4_gate_up_silu_affine
+    assert gu(P(A), P(S), P(Bi), P(X), P(Y), 1, 63, 64, P(0)) == lib.ZQ4_ERR_SHAPE
+    assert gu(P(A), P(S), P(Bi), P(X), P(X), 1, 64, 64, P(0)) == lib.ZQ4_ERR_OVERLAP

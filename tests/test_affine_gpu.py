@@ -1,0 +1,76 @@
+"""GPU parity of the MLX affine format (zq4_gemv_affine,
+zq4_gate_up_silu_affine: value = s * q + b, one f16 scale and bias per 64
+weights) against the CPU oracle. The tolerance is the format's:
+|y - y_ref| <= 2^-10 |y_ref| + 1e-4 Sa with Sa = sum_k |x_k| (|s| q_k + |b|),
+the size of each of the two sums (s * sum(x q), b * sum(x)) the kernel adds."""
+import numpy as np
+import pytest
+import torch
+
+from int4_weight_only_q4f16_gb300 import synth
+from helpers import assert_within, dev, host_f16
+
+pytestmark = pytest.mark.gpu
+
+
+def _affine_weight(tag, N, K, i=0):
+    rng = synth.rng_for(tag, N, K, i)
+    wq = synth.packed_codes(rng, N, K)
+    sc = np.abs(rng.standard_normal((N, K // 64)) * 0.02).astype(np.float16)
+    # biases near -8 s (codes centred, as quantizers choose them) plus noise
+    bi = (-8.0 * sc.astype(np.float32) + rng.standard_normal((N, K // 64)).astype(np.float32) * 0.01).astype(np.float16)
+    return wq, sc, bi
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 3072, 2560), (3, 333, 192), (8, 1000, 9728), (16, 256, 640),
+                                   (5, 64, 64), (1, 2560, 9728)])
+def test_affine_gemv_matches_oracle(oracle, M, N, K):
+    from int4_weight_only_q4f16_gb300 import zq4
+    wq, sc, bi = _affine_weight("aff_gemv", N, K)
+    x = synth.activations(synth.rng_for("aff_x", M, K), M, K)
+    y = zq4.gemv_affine(dev(wq), dev(sc), dev(bi), dev(x), N, K)
+    y_ref, Sa = oracle.gemv_affine(wq, sc, bi, x, N, K)
+    assert_within(host_f16(y), y_ref, Sa, f"affine gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N2,K", [(1, 2048, 2560), (4, 66, 192), (9, 512, 1024)])
+def test_affine_gate_up_matches_oracle(oracle, M, N2, K):
+    from int4_weight_only_q4f16_gb300 import zq4
+    wq, sc, bi = _affine_weight("aff_gu", N2, K)
+    x = synth.activations(synth.rng_for("aff_gux", M, K), M, K)
+    h = zq4.gate_up_silu_affine(dev(wq), dev(sc), dev(bi), dev(x), N2, K)
+    h_ref, Sh = oracle.gate_up_silu_affine(wq, sc, bi, x, N2, K)
+    assert_within(host_f16(h), h_ref, Sh, f"affine gate_up M={M} N2={N2} K={K}")
+
+
+def test_affine_one_hot_bit_exact(oracle):
+    """x = e_k returns f16(s q + b) exactly: scales and biases are multiples
+    of 2^-8 below 1, so s q + b is exact in fp32 and f16 rounds it once."""
+    N, K = 96, 256
+    rng = synth.rng_for("aff_onehot")
+    wq = synth.packed_codes(rng, N, K)
+    sc = (rng.integers(1, 64, (N, K // 64)) / 256.0).astype(np.float16)
+    bi = (rng.integers(-255, 256, (N, K // 64)) / 256.0).astype(np.float16)
+    w = oracle.dequant_affine(wq, sc, bi, N, K)
+    from int4_weight_only_q4f16_gb300 import zq4
+    for k in (0, 7, 63, 64, 130, 255):
+        x = np.zeros((1, K), np.float16)
+        x[0, k] = 1.0
+        y = host_f16(zq4.gemv_affine(dev(wq), dev(sc), dev(bi), dev(x), N, K))
+        assert np.array_equal(y[0].view(np.uint16), oracle.round_f16(w[:, k]).view(np.uint16)), k
+
+
+def test_affine_zero_weights_give_exact_zero():
+    """Scales and biases all 0 (any codes), and codes all 0 with biases 0:
+    every weight is exactly 0, so y is exactly 0 for large activations too."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    M, N, K = 4, 200, 512
+    rng = synth.rng_for("aff_zero")
+    x = dev((rng.standard_normal((M, K)) * 300).astype(np.float16))
+    wq = dev(synth.packed_codes(rng, N, K))
+    z = dev(np.zeros((N, K // 64), np.float16))
+    assert torch.all(zq4.gemv_affine(wq, z, z, x, N, K) == 0)
+    sc = dev(np.abs(rng.standard_normal((N, K // 64)) * 0.02).astype(np.float16))
+    w0 = dev(np.zeros((N, K // 8), np.uint32))
+    assert torch.all(zq4.gemv_affine(w0, sc, z, x, N, K) == 0)
+    assert zq4.device_errors(clear=True) == 0
