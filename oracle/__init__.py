@@ -86,6 +86,10 @@ def _load(mutant: int = 0):
         lib.zo_dequant_affine.argtypes = [_p, _p, _p, _i64, _i64, _p]
         lib.zo_gemv_affine_rows.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
         lib.zo_gate_up_silu_affine.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p]
+        lib.zo_moe_gate_up_affine.argtypes = [_p, _p, _p, _i64, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
+        lib.zo_moe_gate_up_affine.restype = _i64
+        lib.zo_moe_down_combine_affine.argtypes = [_p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
+        lib.zo_moe_down_combine_affine.restype = _i64
         lib.zo_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -225,6 +229,29 @@ class Oracle:
         S = np.empty((T, N), dtype=np.float64)
         bad = self.lib.zo_moe_down_combine(_ptr(wq), _ptr(sc), E, _ptr(hh), _ptr(rr), T, N, K,
                                            _ptr(ids), top_k, _ptr(y), _ptr(S))
+        return y, S, int(bad)
+
+    def moe_gate_up_affine(self, wq_bank, sc_bank, bi_bank, E: int, x, N2: int, K: int, ids):
+        """h_ref, Sh ([T, top_k, N2/2]) and the count of invalid ids; affine banks."""
+        wq, sc, bi, xx = _u32(wq_bank), _f16(sc_bank), _f16(bi_bank), _f16(x)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        T, top_k = ids.shape
+        h = np.empty((T, top_k, N2 // 2), dtype=np.float64)
+        Sh = np.empty((T, top_k, N2 // 2), dtype=np.float64)
+        bad = self.lib.zo_moe_gate_up_affine(_ptr(wq), _ptr(sc), _ptr(bi), E, _ptr(xx), T, N2, K, _ptr(ids),
+                                             top_k, _ptr(h), _ptr(Sh))
+        return h, Sh, int(bad)
+
+    def moe_down_combine_affine(self, wq_bank, sc_bank, bi_bank, E: int, h, r, N: int, K: int, ids):
+        """y_ref, Sa ([T, N]) and the count of invalid ids; affine banks, h f16 [T, top_k, K]."""
+        wq, sc, bi, hh = _u32(wq_bank), _f16(sc_bank), _f16(bi_bank), _f16(h)
+        rr = np.ascontiguousarray(r, dtype=np.float32)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        T, top_k = ids.shape
+        y = np.empty((T, N), dtype=np.float64)
+        S = np.empty((T, N), dtype=np.float64)
+        bad = self.lib.zo_moe_down_combine_affine(_ptr(wq), _ptr(sc), _ptr(bi), E, _ptr(hh), _ptr(rr), T, N, K,
+                                                  _ptr(ids), top_k, _ptr(y), _ptr(S))
         return y, S, int(bad)
 
     # --- LM head ------------------------------------------------------------

@@ -453,6 +453,64 @@ int64_t zo_moe_down_combine(const uint32_t *wq_bank, const uint16_t *sc_bank, in
  * ties go to the lowest index, and a NaN counts as larger than any number
  * (the first NaN wins). idx[m] = that position in row m of y [M][N].
  */
+/* ---------------------------------------------------------------------- */
+/* [BENCH-MOE] with [DOC-AFF] weights (the MoE model the pages run in the    */
+/* affine format): the expert stages of zo_moe_gate_up (interleaved rows)   */
+/* and zo_moe_down_combine on affine banks. Expert e's codes start at word  */
+/* e * N * K/8, its scales and biases at e * N * K/64. Tolerance scales as  */
+/* in zo_gemv_affine_rows (Sa), propagated through SiLU and the combine.    */
+/* ---------------------------------------------------------------------- */
+int64_t zo_moe_gate_up_affine(const uint32_t *wq_bank, const uint16_t *sc_bank, const uint16_t *bi_bank,
+                              int64_t E, const uint16_t *x, int64_t T, int64_t N2, int64_t K,
+                              const int32_t *ids, int64_t top_k, double *h, double *Sh)
+{
+    int64_t I = N2 / 2, bad = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            double *ho = h + (t * top_k + j) * I, *so = Sh + (t * top_k + j) * I;
+            if (e < 0 || e >= E) {
+                ++bad;
+                for (int64_t i = 0; i < I; ++i) ho[i] = so[i] = 0.0;
+                continue;
+            }
+            zo_gate_up_silu_affine(wq_bank + e * N2 * (K / 8), sc_bank + e * N2 * (K / 64),
+                                   bi_bank + e * N2 * (K / 64), x + t * K, 1, N2, K, ho, so);
+        }
+    return bad;
+}
+
+int64_t zo_moe_down_combine_affine(const uint32_t *wq_bank, const uint16_t *sc_bank, const uint16_t *bi_bank,
+                                   int64_t E, const uint16_t *h, const float *r, int64_t T, int64_t N, int64_t K,
+                                   const int32_t *ids, int64_t top_k, double *y, double *Sa)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            if (e < 0 || e >= E) ++bad;
+        }
+    double *z = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *sz = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < N; ++n) y[t * N + n] = Sa[t * N + n] = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = ids[t * top_k + j];
+            if (e < 0 || e >= E) continue;
+            zo_gemv_affine_rows(wq_bank + e * N * (K / 8), sc_bank + e * N * (K / 64), bi_bank + e * N * (K / 64),
+                                h + (t * top_k + j) * K, 1, N, K, NULL, 0, z, sz);
+            double rj = (double)r[t * top_k + j];
+            for (int64_t n = 0; n < N; ++n) {
+                y[t * N + n] += rj * z[n];
+                Sa[t * N + n] += fabs(rj) * sz[n];
+            }
+        }
+    }
+    free(z);
+    free(sz);
+    return bad;
+}
+
 void zo_argmax(const double *y, int64_t M, int64_t N, int32_t *idx)
 {
     for (int64_t m = 0; m < M; ++m) {

@@ -452,6 +452,67 @@ def test_affine_gate_up_brute_force(oracle):
             assert abs(h[m, j] - want) <= 1e-12 * (abs(want) + Sh[m, j] + 1e-300)
 
 
+def _affine_bank(rng, E, N, K):
+    wq = synth.packed_codes(rng, E * N, K)
+    sc = (rng.random((E * N, K // 64)) * 0.05).astype(np.float16)
+    bi = (rng.standard_normal((E * N, K // 64)) * 0.1).astype(np.float16)
+    return wq, sc, bi
+
+
+def test_affine_moe_single_slot_is_plain_gemv(oracle):
+    """One slot per token with router weight 1 reduces both affine MoE stages
+    to the (pinned) affine GEMV / gate_up of the chosen expert."""
+    rng = np.random.default_rng(31)
+    E, I, K, N, T = 5, 32, 128, 24, 3
+    gq, gs, gb = _affine_bank(rng, E, 2 * I, K)
+    dq, ds, db = _affine_bank(rng, E, N, 2 * I)
+    x = synth.activations(rng, T, K)
+    ids = np.array([[3], [0], [4]], dtype=np.int32)
+    h, Sh, bad = oracle.moe_gate_up_affine(gq, gs, gb, E, x, 2 * I, K, ids)
+    assert bad == 0
+    for t in range(T):
+        e = ids[t, 0]
+        sl = slice(e * 2 * I, (e + 1) * 2 * I)
+        hr, Shr = oracle.gate_up_silu_affine(gq[sl], gs[sl], gb[sl], x[t:t + 1], 2 * I, K)
+        assert np.array_equal(h[t, 0], hr[0]) and np.array_equal(Sh[t, 0], Shr[0])
+    hf = synth.activations(rng, T, 2 * I).reshape(T, 1, 2 * I)
+    y, S, bad = oracle.moe_down_combine_affine(dq, ds, db, E, hf, np.ones((T, 1), np.float32), N, 2 * I, ids)
+    assert bad == 0
+    for t in range(T):
+        e = ids[t, 0]
+        sl = slice(e * N, (e + 1) * N)
+        yr, Sr = oracle.gemv_affine(dq[sl], ds[sl], db[sl], hf[t, 0][None], N, 2 * I)
+        assert np.array_equal(y[t], yr[0]) and np.array_equal(S[t], Sr[0])
+
+
+def test_affine_moe_combine_weighted_sum_and_invalid_ids(oracle):
+    rng = np.random.default_rng(32)
+    E, N, K, T, top_k = 7, 16, 128, 3, 3
+    dq, ds, db = _affine_bank(rng, E, N, K)
+    h = synth.activations(rng, T * top_k, K).reshape(T, top_k, K)
+    ids, r = synth.routing(rng, T, E, top_k)
+    y, S, bad = oracle.moe_down_combine_affine(dq, ds, db, E, h, r, N, K, ids)
+    assert bad == 0
+    for t in range(T):
+        acc = np.zeros(N)
+        for j in range(top_k):
+            e = ids[t, j]
+            z, _ = oracle.gemv_affine(dq[e * N:(e + 1) * N], ds[e * N:(e + 1) * N], db[e * N:(e + 1) * N],
+                                      h[t, j][None], N, K)
+            acc += float(r[t, j]) * z[0]
+        assert np.allclose(y[t], acc, rtol=0, atol=1e-13 * S[t].max())
+    bad_ids = ids.copy()
+    bad_ids[0, 1] = E
+    bad_ids[2, 0] = -3
+    y2, _, bad = oracle.moe_down_combine_affine(dq, ds, db, E, h, r, N, K, bad_ids)
+    assert bad == 2
+    r2 = r.copy()
+    r2[0, 1] = 0.0
+    r2[2, 0] = 0.0
+    y3, _, _ = oracle.moe_down_combine_affine(dq, ds, db, E, h, r2, N, K, ids)
+    assert np.allclose(y2, y3, rtol=0, atol=1e-13 * S.max())
+
+
 # --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
