@@ -576,15 +576,26 @@ def run_moe(args, torch, dist, peaks, peak_kind):
     E, top_k, T = synth.MOE_EXPERTS, synth.MOE_TOP_K, args.t
     (N2, D), (Dn, I) = synth.MOE_GATE_UP, synth.MOE_DOWN
     banks = 4
-    gq, gs, dq, ds, xs, ids, rs, hs, ys = [], [], [], [], [], [], [], [], []
+    gq, gs, gbi, dq, ds, dbi, xs, ids, rs, hs, ys = [], [], [], [], [], [], [], [], [], [], []
     uniq_bytes = []
+    aff = args.affine                            # MLX affine banks: a scale and a bias per 64 weights
+    per_scale = 64 if aff else 32
+
+    def to_dev(a, s):
+        if aff:
+            s = s[:, ::2].copy()
+            return (torch.from_numpy(a.view(np.int32)).cuda(), torch.from_numpy(s).cuda(),
+                    torch.from_numpy((-8.0 * s.astype(np.float32)).astype(np.float16)).cuda())
+        return torch.from_numpy(a.view(np.int32)).cuda(), torch.from_numpy(s).cuda(), None
     for b in range(banks):
-        a, s = synth.weight("moe_gu", E * N2, D, b)
-        gq.append(torch.from_numpy(a.view(np.int32)).cuda())
-        gs.append(torch.from_numpy(s).cuda())
-        a, s = synth.weight("moe_dn", E * Dn, I, b)
-        dq.append(torch.from_numpy(a.view(np.int32)).cuda())
-        ds.append(torch.from_numpy(s).cuda())
+        w_, s_, b_ = to_dev(*synth.weight("moe_gu", E * N2, D, b))
+        gq.append(w_)
+        gs.append(s_)
+        gbi.append(b_)
+        w_, s_, b_ = to_dev(*synth.weight("moe_dn", E * Dn, I, b))
+        dq.append(w_)
+        ds.append(s_)
+        dbi.append(b_)
         rng = synth.rng_for("moe_route", b, T)
         i_, r_ = synth.routing(rng, T, E, top_k)
         xs.append(torch.from_numpy(synth.activations(rng, T, D)).cuda())
@@ -593,15 +604,23 @@ def run_moe(args, torch, dist, peaks, peak_kind):
         hs.append(torch.empty((T, top_k, N2 // 2), dtype=torch.float16, device="cuda"))
         ys.append(torch.empty((T, Dn), dtype=torch.float16, device="cuda"))
         nu = len(np.unique(i_))
-        uniq_bytes.append(nu * (N2 * (D // 8) * 4 + N2 * (D // 32) * 2 + Dn * (I // 8) * 4 + Dn * (I // 32) * 2))
+        sb = (4 if aff else 2)                  # scale (+ bias) bytes per group
+        uniq_bytes.append(nu * (N2 * (D // 8) * 4 + N2 * (D // per_scale) * sb + Dn * (I // 8) * 4 +
+                                Dn * (I // per_scale) * sb))
     stream = torch.cuda.Stream()
 
     def chain():
         for b in range(banks):
-            zq4.moe_gemv(gq[b], gs[b], E, xs[b], N2, D, ids[b], zq4.MOE_GATE_UP_SILU, y=hs[b],
-                         stream=stream)
-            zq4.moe_gemv(dq[b], ds[b], E, hs[b], Dn, I, ids[b], zq4.MOE_DOWN_COMBINE,
-                         route_w=rs[b], y=ys[b], stream=stream)
+            if aff:
+                zq4.moe_gemv_affine(gq[b], gs[b], gbi[b], E, xs[b], N2, D, ids[b], zq4.MOE_GATE_UP_SILU, y=hs[b],
+                                    stream=stream)
+                zq4.moe_gemv_affine(dq[b], ds[b], dbi[b], E, hs[b], Dn, I, ids[b], zq4.MOE_DOWN_COMBINE,
+                                    route_w=rs[b], y=ys[b], stream=stream)
+            else:
+                zq4.moe_gemv(gq[b], gs[b], E, xs[b], N2, D, ids[b], zq4.MOE_GATE_UP_SILU, y=hs[b],
+                             stream=stream)
+                zq4.moe_gemv(dq[b], ds[b], E, hs[b], Dn, I, ids[b], zq4.MOE_DOWN_COMBINE,
+                             route_w=rs[b], y=ys[b], stream=stream)
     with torch.cuda.stream(stream):
         chain()
     g = capture(torch, chain, stream)
@@ -610,7 +629,8 @@ def run_moe(args, torch, dist, peaks, peak_kind):
     el = time_replays(torch, g.replay, reps, stream)
     per = el / (reps * banks)
     ub = sum(uniq_bytes) / banks
-    return {"metric": "MoE expert GEMV block (gate_up+SiLU, down+combine) GB/s over unique experts",
+    return {"metric": ("MLX affine " if aff else "") +
+                      "MoE expert GEMV block (gate_up+SiLU, down+combine) GB/s over unique experts",
             "value": round(ub / per / 1e9, 1), "unit": "GB/s", "T": T, "us_per_block": round(per * 1e6, 3),
             "unique_expert_bytes": ub, "frac_of_measured": round(ub / per / 1e9 / peaks["hbm_gbs"], 4),
             "config": {"workload": f"MoE 128 experts top-8, T={T}", "banks": banks}}

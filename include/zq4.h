@@ -153,6 +153,21 @@ ZQ4_API zq4_status zq4_gate_up_silu_affine(const uint32_t *wq, const uint16_t *s
                                            const uint16_t *x, uint16_t *h, int M, int N2, int K, void *stream);
 
 /*
+ * zq4_moe_gemv_affine -- zq4_moe_gemv on expert banks in the MLX affine
+ * format (the MoE model the pages run is an MLX checkpoint: "Zero TVM
+ * Documentation", section "Qwen3.6-35B-A3B MoE"). Expert e's codes start at
+ * word e * N * K/8 of wq_bank, its scales and biases at e * N * K/64 of
+ * scales_bank / biases_bank (f16, [num_experts * N, K/64]). Modes, shapes,
+ * routing, invalid-id handling and errors as zq4_moe_gemv, with K a multiple
+ * of 64, scales and biases 2-byte aligned, and ZQ4_ERR_NULL for a NULL
+ * biases_bank.
+ */
+ZQ4_API zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *scales_bank,
+                                       const uint16_t *biases_bank, int num_experts, const uint16_t *x, uint16_t *y,
+                                       int T, int N, int K, const int32_t *expert_ids, const float *route_w,
+                                       int top_k, int mode, int32_t *dev_status, void *stream);
+
+/*
  * zq4_gemv_argmax -- the LM-head step of decode: fp32 logits and, per token,
  * the index of the largest logit.
  * Source: "Zero TVM Documentation", section "WGSL Kernel Roles" (the LM-head

@@ -224,14 +224,26 @@ zq4_status zq4_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, c
     return cuda_status(launch_decode(wq, scales, biases, x, h, M, N2, K, true, static_cast<cudaStream_t>(stream)));
 }
 
-zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, int num_experts,
-                        const uint16_t *x, uint16_t *y, int T, int N, int K,
-                        const int32_t *expert_ids, const float *route_w, int top_k, int mode,
-                        int32_t *dev_status, void *stream)
+namespace {
+
+// zq4_moe_gemv and zq4_moe_gemv_affine (biases_bank != nullptr: affine banks).
+zq4_status moe_common(const uint32_t *wq_bank, const uint16_t *scales_bank, const uint16_t *biases_bank,
+                      int num_experts, const uint16_t *x, uint16_t *y, int T, int N, int K,
+                      const int32_t *expert_ids, const float *route_w, int top_k, int mode, int32_t *dev_status,
+                      void *stream)
 {
+    const bool aff = biases_bank != nullptr;
     if (mode != ZQ4_MOE_GATE_UP_SILU && mode != ZQ4_MOE_DOWN_COMBINE) return ZQ4_ERR_FLAGS;
-    zq4_status st = check_matrix(wq_bank, scales_bank, N, K);
-    if (st != ZQ4_OK) return st;
+    if (aff) {
+        if (!wq_bank || !scales_bank) return ZQ4_ERR_NULL;
+        if (N <= 0 || K <= 0 || (K % 64) != 0) return ZQ4_ERR_SHAPE;
+        if (!aligned16(wq_bank) || (reinterpret_cast<uintptr_t>(scales_bank) & 1) ||
+            (reinterpret_cast<uintptr_t>(biases_bank) & 1))
+            return ZQ4_ERR_ALIGN;
+    } else {
+        zq4_status st = check_matrix(wq_bank, scales_bank, N, K);
+        if (st != ZQ4_OK) return st;
+    }
     if (!x || !y || !expert_ids) return ZQ4_ERR_NULL;
     if (mode == ZQ4_MOE_DOWN_COMBINE && !route_w) return ZQ4_ERR_NULL;
     if (num_experts <= 0 || T <= 0 || top_k <= 0 || top_k > 32) return ZQ4_ERR_SHAPE;
@@ -243,19 +255,20 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
         (reinterpret_cast<uintptr_t>(dev_status) & 3))
         return ZQ4_ERR_ALIGN;
     const size_t xrows = mode == ZQ4_MOE_GATE_UP_SILU ? size_t(T) : size_t(T) * top_k;
-    const size_t staged_rows = mode == ZQ4_MOE_GATE_UP_SILU ? 1 : size_t(top_k);
-    if (staged_rows * K * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    if (moe_smem(mode, K, top_k, aff) > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
     const size_t ybytes = mode == ZQ4_MOE_GATE_UP_SILU ? size_t(T) * top_k * (N / 2) * 2
                                                        : size_t(T) * N * 2;
     const size_t E = size_t(num_experts);
-    if (overlap(y, ybytes, wq_bank, E * wq_bytes(N, K)) ||
-        overlap(y, ybytes, scales_bank, E * sc_bytes(N, K)) ||
+    const size_t sbytes = aff ? E * size_t(N) * (K / 64) * 2 : E * sc_bytes(N, K);
+    if (overlap(y, ybytes, wq_bank, E * wq_bytes(N, K)) || overlap(y, ybytes, scales_bank, sbytes) ||
+        (aff && overlap(y, ybytes, biases_bank, sbytes)) ||
         overlap(y, ybytes, x, xrows * K * 2) ||
         overlap(y, ybytes, expert_ids, size_t(T) * top_k * 4))
         return ZQ4_ERR_OVERLAP;
     MoeArgs a = {};
     a.wq = wq_bank;
     a.scales = scales_bank;
+    a.biases = biases_bank;
     a.x = x;
     a.y = y;
     a.ids = expert_ids;
@@ -267,6 +280,27 @@ zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, in
     a.K = K;
     a.top_k = top_k;
     return cuda_status(launch_moe(a, mode, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_bank, int num_experts,
+                        const uint16_t *x, uint16_t *y, int T, int N, int K,
+                        const int32_t *expert_ids, const float *route_w, int top_k, int mode,
+                        int32_t *dev_status, void *stream)
+{
+    return moe_common(wq_bank, scales_bank, nullptr, num_experts, x, y, T, N, K, expert_ids, route_w, top_k, mode,
+                      dev_status, stream);
+}
+
+zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *scales_bank, const uint16_t *biases_bank,
+                               int num_experts, const uint16_t *x, uint16_t *y, int T, int N, int K,
+                               const int32_t *expert_ids, const float *route_w, int top_k, int mode,
+                               int32_t *dev_status, void *stream)
+{
+    if (!biases_bank) return ZQ4_ERR_NULL;
+    return moe_common(wq_bank, scales_bank, biases_bank, num_experts, x, y, T, N, K, expert_ids, route_w, top_k,
+                      mode, dev_status, stream);
 }
 
 zq4_status zq4_device_errors(uint32_t *flags, int clear)

@@ -272,10 +272,12 @@ __global__ void __launch_bounds__(kThreads) k_dense(DenseArgs a)
 // MoE, mode GATE_UP_SILU: blockIdx.y = slot (t*top_k + j); the slot's expert
 // is read after the wait (the ids may come from the previous kernel).
 // ---------------------------------------------------------------------------
-template <int LPR>
+// AFF: affine banks (a.biases; scales and biases per 64 weights).
+template <int LPR, bool AFF>
 __global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
 {
     extern __shared__ __align__(16) uint8_t xs[];
+    float *xsum = reinterpret_cast<float *>(xs + size_t(a.K) * 2);     // AFF: [K/32]
     const int slot = blockIdx.y, t = slot / a.top_k;
     const int units = a.N >> 1;
     const int u0 = blockIdx.x * a.units_per_cta;
@@ -291,9 +293,12 @@ __global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
         griddep_launch_dependents();
         return;
     }
+    const int gs = AFF ? a.K >> 6 : a.K >> 5;                          // scales per row
     const uint32_t *wq = a.wq + size_t(e) * a.N * (a.K >> 3);
-    const uint16_t *sc = a.scales + size_t(e) * a.N * (a.K >> 5);
+    const uint16_t *sc = a.scales + size_t(e) * a.N * gs;
+    const uint16_t *bi = AFF ? a.biases + size_t(e) * a.N * gs : nullptr;
     stage_rows(xs, a.x + size_t(t) * a.K, 1, 1, a.K);
+    if (AFF) chunk_sums(xsum, a.x + size_t(t) * a.K, 1, 1, a.K);
     __syncthreads();
     griddep_launch_dependents();
 
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
     const uint32_t xs_base = smem_addr(xs);
     for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
         float part[2][1];
-        rows_dot<1, LPR, 2, false>(wq, sc, nullptr, a.K, 2 * u, xs_base, nullptr, lane, part);
+        rows_dot<1, LPR, 2, AFF>(wq, sc, bi, a.K, 2 * u, xs_base, xsum, lane, part);
         float g = segment_sum<LPR>(part[0][0], mask);
         float v = segment_sum<LPR>(part[1][0], mask);
         if (lane == 0) yo[u] = float_to_f16_bits(silu_f32(g) * v);
@@ -313,10 +318,11 @@ __global__ void __launch_bounds__(kThreads) k_moe_gate_up(MoeArgs a)
 // MoE, mode DOWN_COMBINE: blockIdx.y = token t; each unit is one output row
 // n; y[t,n] = sum_j r[t,j] * (x[t,j,:] . w_{e_j}[n,:]).
 // ---------------------------------------------------------------------------
-template <int LPR>
+template <int LPR, bool AFF>
 __global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
 {
     extern __shared__ __align__(16) uint8_t xs[];
+    float *xsum = reinterpret_cast<float *>(xs + size_t(a.top_k) * a.K * 2);   // AFF: [top_k][K/32]
     __shared__ int s_ids[32];
     __shared__ float s_r[32];
     const int t = blockIdx.y;
@@ -332,12 +338,13 @@ __global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
         s_r[threadIdx.x] = a.route_w[t * a.top_k + threadIdx.x];
     }
     stage_rows(xs, a.x + size_t(t) * a.top_k * a.K, a.top_k, a.top_k, a.K);
+    if (AFF) chunk_sums(xsum, a.x + size_t(t) * a.top_k * a.K, a.top_k, a.top_k, a.K);
     __syncthreads();
     griddep_launch_dependents();
 
-    const int G = a.K >> 5, KW = a.K >> 3;
+    const int G = a.K >> 5, KW = a.K >> 3, GS = AFF ? a.K >> 6 : G;
     const uint32_t row_bytes = uint32_t(a.K) * 2;
-    const size_t expert_words = size_t(a.N) * KW, expert_scales = size_t(a.N) * G;
+    const size_t expert_words = size_t(a.N) * KW, expert_scales = size_t(a.N) * GS;
     const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
     const unsigned mask = segment_mask<LPR>();
     const uint32_t xs_base = smem_addr(xs);
@@ -346,16 +353,19 @@ __global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
         for (int g = lane; g < G; g += LPR) {
             for (int j0 = 0; j0 < a.top_k; j0 += kMoeSlotChunk) {
                 uint4 wv[kMoeSlotChunk];
-                uint16_t sv[kMoeSlotChunk];
+                uint16_t sv[kMoeSlotChunk], bv[kMoeSlotChunk];
 #pragma unroll
                 for (int i = 0; i < kMoeSlotChunk; ++i) {
                     int j = j0 + i, e = j < a.top_k ? s_ids[j] : -1;
                     if (e >= 0) {
+                        const size_t so = size_t(e) * expert_scales + size_t(n) * GS + (AFF ? g >> 1 : g);
                         wv[i] = ldg_stream_v4(a.wq + size_t(e) * expert_words + size_t(n) * KW + 4 * g);
-                        sv[i] = ldg_u16(a.scales + size_t(e) * expert_scales + size_t(n) * G + g);
+                        sv[i] = ldg_u16(a.scales + so);
+                        bv[i] = AFF ? ldg_u16(a.biases + so) : uint16_t(0);
                     } else {
                         wv[i] = make_uint4(0, 0, 0, 0);
                         sv[i] = 0;
+                        bv[i] = 0;
                     }
                 }
 #pragma unroll
@@ -363,8 +373,9 @@ __global__ void __launch_bounds__(kThreads) k_moe_down(MoeArgs a)
                     int j = j0 + i;
                     if (j < a.top_k && s_ids[j] >= 0) {
                         float part[1] = {0.f};
-                        group_dot<1, false>(wv[i], f16_bits_to_float(sv[i]), 0.f,
-                                            xs_base + uint32_t(j) * row_bytes, g, row_bytes, nullptr, 0, part);
+                        group_dot<1, AFF>(wv[i], f16_bits_to_float(sv[i]), f16_bits_to_float(bv[i]),
+                                          xs_base + uint32_t(j) * row_bytes, g, row_bytes,
+                                          AFF ? xsum + j * G : nullptr, G, part);
                         acc = fmaf(s_r[j], part[0], acc);
                     }
                 }
@@ -563,46 +574,56 @@ cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint
     return cudaSuccess;
 }
 
+namespace {
+
+template <int LPR, bool AFF>
+cudaError_t launch_moe_t(const MoeArgs &a, int mode, dim3 grid, size_t smem, cudaStream_t s)
+{
+    static int set_gu[kMaxDevices] = {}, set_dn[kMaxDevices] = {};
+    if (mode == ZQ4_MOE_GATE_UP_SILU) {
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<LPR, AFF>), smem, set_gu);
+        return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<LPR, AFF>, grid, dim3(kThreads), smem, s, a);
+    }
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<LPR, AFF>), smem, set_dn);
+    return e != cudaSuccess ? e : launch_pdl(k_moe_down<LPR, AFF>, grid, dim3(kThreads), smem, s, a);
+}
+
+template <bool AFF>
+cudaError_t launch_moe_lpr(int lpr, const MoeArgs &a, int mode, dim3 grid, size_t smem, cudaStream_t s)
+{
+    switch (lpr) {
+    case 32: return launch_moe_t<32, AFF>(a, mode, grid, smem, s);
+    case 16: return launch_moe_t<16, AFF>(a, mode, grid, smem, s);
+    default: return launch_moe_t<8, AFF>(a, mode, grid, smem, s);
+    }
+}
+
+}  // namespace
+
+// Shared memory of a MoE launch: the staged x rows (1 for gate_up, top_k for
+// down) and, for affine banks, their chunk sums.
+size_t moe_smem(int mode, int K, int top_k, bool aff)
+{
+    const size_t rows = mode == ZQ4_MOE_GATE_UP_SILU ? 1 : size_t(top_k);
+    return rows * K * 2 + (aff ? rows * (K >> 5) * 4 : 0);
+}
+
+// a.biases != nullptr: affine banks.
 cudaError_t launch_moe(const MoeArgs &a0, int mode, cudaStream_t s)
 {
     MoeArgs a = a0;
+    const bool aff = a.biases != nullptr;
     const int lpr = pick_lpr(a.K);
+    const size_t smem = moe_smem(mode, a.K, a.top_k, aff);
+    dim3 grid;
     if (mode == ZQ4_MOE_GATE_UP_SILU) {
         a.units_per_cta = units_per_cta(a.N >> 1, lpr);
-        int gx = ((a.N >> 1) + a.units_per_cta - 1) / a.units_per_cta;
-        dim3 grid(gx, a.T * a.top_k);
-        size_t smem = size_t(a.K) * 2;
-        static int set32[kMaxDevices] = {}, set16[kMaxDevices] = {}, set8[kMaxDevices] = {};
-        cudaError_t e;
-        switch (lpr) {
-        case 32:
-            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<32>), smem, set32);
-            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<32>, grid, dim3(kThreads), smem, s, a);
-        case 16:
-            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<16>), smem, set16);
-            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<16>, grid, dim3(kThreads), smem, s, a);
-        default:
-            e = ensure_smem(reinterpret_cast<const void *>(k_moe_gate_up<8>), smem, set8);
-            return e != cudaSuccess ? e : launch_pdl(k_moe_gate_up<8>, grid, dim3(kThreads), smem, s, a);
-        }
+        grid = dim3(((a.N >> 1) + a.units_per_cta - 1) / a.units_per_cta, a.T * a.top_k);
+    } else {
+        a.units_per_cta = units_per_cta(a.N, lpr);
+        grid = dim3((a.N + a.units_per_cta - 1) / a.units_per_cta, a.T);
     }
-    a.units_per_cta = units_per_cta(a.N, lpr);
-    int gx = (a.N + a.units_per_cta - 1) / a.units_per_cta;
-    dim3 grid(gx, a.T);
-    size_t smem = size_t(a.top_k) * a.K * 2;
-    static int set32[kMaxDevices] = {}, set16[kMaxDevices] = {}, set8[kMaxDevices] = {};
-    cudaError_t e;
-    switch (lpr) {
-    case 32:
-        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<32>), smem, set32);
-        return e != cudaSuccess ? e : launch_pdl(k_moe_down<32>, grid, dim3(kThreads), smem, s, a);
-    case 16:
-        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<16>), smem, set16);
-        return e != cudaSuccess ? e : launch_pdl(k_moe_down<16>, grid, dim3(kThreads), smem, s, a);
-    default:
-        e = ensure_smem(reinterpret_cast<const void *>(k_moe_down<8>), smem, set8);
-        return e != cudaSuccess ? e : launch_pdl(k_moe_down<8>, grid, dim3(kThreads), smem, s, a);
-    }
+    return aff ? launch_moe_lpr<true>(lpr, a, mode, grid, smem, s) : launch_moe_lpr<false>(lpr, a, mode, grid, smem, s);
 }
 
 static int elementwise_grid(size_t items)

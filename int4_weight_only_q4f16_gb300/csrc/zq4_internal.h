@@ -27,6 +27,7 @@ struct DenseArgs {
 struct MoeArgs {
     const uint32_t *wq;
     const uint16_t *scales;
+    const uint16_t *biases;   // affine banks only (else nullptr)
     const uint16_t *x;
     uint16_t *y;
     const int32_t *ids;
@@ -96,6 +97,7 @@ size_t decode_max_smem();
 cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs &a, int mode, cudaStream_t s);
+size_t moe_smem(int mode, int K, int top_k, bool aff);
 cudaError_t launch_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
                                cudaStream_t s);
 cudaError_t launch_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N,

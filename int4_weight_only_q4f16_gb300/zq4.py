@@ -38,7 +38,7 @@ PREP_SEGMENTED = 2
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
            "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
-           "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine")
+           "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine")
 
 
 class Zq4Error(RuntimeError):
@@ -76,6 +76,7 @@ def _load():
         "zq4_stack_plan_waits": [P, I, I, P, P],
         "zq4_gemv_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
+        "zq4_moe_gemv_affine": [P, P, P, I, P, P, I, I, I, P, P, I, I, P, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -232,6 +233,30 @@ def moe_gemv(wq_bank, scales_bank, num_experts, x, N, K, expert_ids, mode, route
     _check("zq4_moe_gemv", lib.zq4_moe_gemv(
         w, s, num_experts, _ptr(x, "x", xrows * K * 2, 2), _ptr(y, "y", ybytes, 2), T, N, K,
         _ptr(expert_ids, "expert_ids", T * top_k * 4, 4),
+        _ptr(route_w, "route_w", T * top_k * 4, 4), top_k, mode,
+        _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
+    return y
+
+
+def moe_gemv_affine(wq_bank, scales_bank, biases_bank, num_experts, x, N, K, expert_ids, mode, route_w=None,
+                    y=None, dev_status=None, stream=None):
+    """moe_gemv on affine expert banks (zq4_moe_gemv_affine): scales and
+    biases [num_experts * N, K/64] f16."""
+    T, top_k = expert_ids.shape
+    if mode == MOE_GATE_UP_SILU:
+        xrows, yshape = T, (T, top_k, N // 2)
+    else:
+        xrows, yshape = T * top_k, (T, N)
+    if y is None:
+        y = torch.empty(yshape, dtype=torch.float16, device=x.device)
+    ybytes = 2
+    for d in yshape:
+        ybytes *= d
+    gb = num_experts * N * (K // 64) * 2
+    _check("zq4_moe_gemv_affine", lib.zq4_moe_gemv_affine(
+        _ptr(wq_bank, "wq_bank", num_experts * N * (K // 8) * 4, 4), _ptr(scales_bank, "scales_bank", gb, 2),
+        _ptr(biases_bank, "biases_bank", gb, 2), num_experts, _ptr(x, "x", xrows * K * 2, 2),
+        _ptr(y, "y", ybytes, 2), T, N, K, _ptr(expert_ids, "expert_ids", T * top_k * 4, 4),
         _ptr(route_w, "route_w", T * top_k * 4, 4), top_k, mode,
         _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
     return y

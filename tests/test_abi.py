@@ -101,3 +101,19 @@ def test_affine_host_checks_reject_before_launch(lib):
     gu = lib.lib.zq4_gate_up_silu_affine
     assert gu(P(A), P(S), P(Bi), P(X), P(Y), 1, 63, 64, P(0)) == lib.ZQ4_ERR_SHAPE
     assert gu(P(A), P(S), P(Bi), P(X), P(X), 1, 64, 64, P(0)) == lib.ZQ4_ERR_OVERLAP
+
+
+def test_affine_moe_host_checks(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000
+    S, Bi, X, Y, ids, r = (A + (i << 30) for i in range(1, 7))
+    m = lib.lib.zq4_moe_gemv_affine
+    assert m(P(A), P(S), P(0), 4, P(X), P(Y), 1, 64, 64, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
+             P(0), P(0)) == lib.ZQ4_ERR_NULL
+    assert m(P(A), P(S), P(Bi), 4, P(X), P(Y), 1, 64, 96, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
+             P(0), P(0)) == lib.ZQ4_ERR_SHAPE
+    assert m(P(A), P(S), P(Bi), 4, P(X), P(Y), 1, 64, 64, P(ids), P(r), 2, 9, P(0), P(0)) == lib.ZQ4_ERR_FLAGS
+    assert m(P(A), P(S + 1), P(Bi), 4, P(X), P(Y), 1, 64, 64, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
+             P(0), P(0)) == lib.ZQ4_ERR_ALIGN
+    assert m(P(A), P(S), P(Bi), 4, P(X), P(Bi), 1, 64, 64, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
+             P(0), P(0)) == lib.ZQ4_ERR_OVERLAP

@@ -74,3 +74,37 @@ def test_affine_zero_weights_give_exact_zero():
     w0 = dev(np.zeros((N, K // 8), np.uint32))
     assert torch.all(zq4.gemv_affine(w0, sc, z, x, N, K) == 0)
     assert zq4.device_errors(clear=True) == 0
+
+
+def _affine_bank(tag, E, N, K):
+    rng = synth.rng_for(tag, E, N, K)
+    wq = synth.packed_codes(rng, E * N, K)
+    sc = np.abs(rng.standard_normal((E * N, K // 64)) * 0.02).astype(np.float16)
+    bi = (-8.0 * sc.astype(np.float32) + rng.standard_normal((E * N, K // 64)).astype(np.float32) * 0.01).astype(np.float16)
+    return wq, sc, bi
+
+
+@pytest.mark.parametrize("E,T,top_k,I,D", [(8, 1, 2, 64, 128), (16, 4, 8, 128, 256), (128, 3, 8, 512, 2048),
+                                           (5, 6, 5, 192, 64)])
+def test_affine_moe_two_stage_parity(oracle, E, T, top_k, I, D):
+    """Both expert stages on affine banks; the down stage is checked on the
+    GPU's own f16 intermediate, so each call's error is isolated."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    gq, gs, gb = _affine_bank("aff_moe_gu", E, 2 * I, D)     # gate_up: [2I, D] per expert
+    dq, ds, db = _affine_bank("aff_moe_dn", E, D, I)         # down:    [D, I]  per expert
+    rng = synth.rng_for("aff_moe_x", E, T)
+    x = synth.activations(rng, T, D)
+    ids, r = synth.routing(rng, T, E, top_k)
+    ids[0, 0] = E + 3                                         # one invalid id: reported, contributes nothing
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = zq4.moe_gemv_affine(dev(gq), dev(gs), dev(gb), E, dev(x), 2 * I, D, dev(ids), zq4.MOE_GATE_UP_SILU,
+                            dev_status=status)
+    h_ref, Sh, bad = oracle.moe_gate_up_affine(gq, gs, gb, E, x, 2 * I, D, ids)
+    h_gpu = host_f16(h)
+    assert_within(h_gpu, h_ref, Sh, "affine moe gate_up")
+    y = zq4.moe_gemv_affine(dev(dq), dev(ds), dev(db), E, h, D, I, dev(ids), zq4.MOE_DOWN_COMBINE,
+                            route_w=dev(r), dev_status=status)
+    y_ref, S, bad2 = oracle.moe_down_combine_affine(dq, ds, db, E, h_gpu, r, D, I, ids)
+    assert_within(host_f16(y), y_ref, S, "affine moe down+combine")
+    assert bad == bad2 == 1 and int(status.item()) != 0
+    assert zq4.device_errors(clear=True) == 0
