@@ -90,6 +90,7 @@ def _load(mutant: int = 0):
         lib.zo_moe_gate_up_affine.restype = _i64
         lib.zo_moe_down_combine_affine.argtypes = [_p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
         lib.zo_moe_down_combine_affine.restype = _i64
+        lib.zo_gemv_add_rmsnorm.argtypes = [_p, _p, _p, _p, _p, ctypes.c_double, _i64, _i64, _i64, _p, _p, _p, _p]
         lib.zo_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -253,6 +254,19 @@ class Oracle:
         bad = self.lib.zo_moe_down_combine_affine(_ptr(wq), _ptr(sc), _ptr(bi), E, _ptr(hh), _ptr(rr), T, N, K,
                                                   _ptr(ids), top_k, _ptr(y), _ptr(S))
         return y, S, int(bad)
+
+    # --- GEMV + residual add + RMSNorm -----------------------------------------
+    def gemv_add_rmsnorm(self, wq, scales, x, resid, gamma, eps: float, N: int, K: int):
+        """(r, out, S, Tn), each [M, N] fp64: r = resid + x W^T, out =
+        RMSNorm(r) * gamma, S the dot products' tolerance scale and Tn the
+        propagated bound on out."""
+        wq, sc, xx = _u32(wq), _f16(scales), _f16(x)
+        rr, gg = _f16(resid), _f16(gamma)
+        M = xx.size // K if K else 0
+        r, out, S, Tn = (np.empty((M, N), dtype=np.float64) for _ in range(4))
+        self.lib.zo_gemv_add_rmsnorm(_ptr(wq), _ptr(sc), _ptr(xx), _ptr(rr), _ptr(gg), float(eps), M, N, K,
+                                     _ptr(r), _ptr(out), _ptr(S), _ptr(Tn))
+        return r, out, S, Tn
 
     # --- LM head ------------------------------------------------------------
     def argmax(self, y) -> np.ndarray:

@@ -28,6 +28,12 @@
  *            prefill": per (token, slot) the expert index comes from the
  *            routing ids, experts never mix tokens, and a combine sums the
  *            slots of one token weighted by the router scores.
+ *  [DOC-ADDNORM] "Zero TVM Documentation", section "WGSL Kernel Roles",
+ *            card 7 "Fused Add + RMSNorm": residual_out = A + B (A the new
+ *            contribution, the O or down projection's output; B the running
+ *            residual), output = RMSNorm(residual_out) * gamma; "Zero-TVM
+ *            benchmarks", "Remaining levers" item 2: folded into the matmul
+ *            that produces A, as a reduction at its tail.
  *  [DOC-AFF] "Zero TVM Documentation", section "Qwen3.6-35B-A3B MoE", and
  *            "Zero-TVM benchmarks", sections "Chunked prefill for
  *            plain-attention + MLX-affine specs" and "Affine wide loads":
@@ -41,6 +47,9 @@
  * an expert id outside [0, E) contributes nothing and is counted. Affine
  * format: the codes are packed as in q4f16_1 (LSB-first, 8 per word) and are
  * unsigned (no zero point); scales and biases are f16 arrays [N, K/64].
+ * RMSNorm (named, not defined, by the pages): y / sqrt(mean(y^2) + eps) over
+ * the N features of one token, eps given by the caller; in the fused form A
+ * is the exact dot product, not its f16 rounding.
  *
  * Arithmetic is IEEE fp64 throughout. The dequantized weight (q-7)*s is exact
  * in fp64 (4-bit integer times an 11-bit significand). Sums are taken in
@@ -366,6 +375,47 @@ void zo_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, const ui
         }
     free(g);
     free(Sa);
+}
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-ADDNORM], [DOC-MM]: for each token m, r[m,n] = B[m,n] + sum_k       */
+/* x[m,k] w[n,k] (exact dot product), rms[m] = sqrt(mean_n r[m,n]^2 + eps), */
+/* out[m,n] = r[m,n] / rms[m] * gamma[n]. Also S[m,n] = sum_k |x w| (the   */
+/* dot product's tolerance scale) and the first-order propagation of an    */
+/* error e[m,n] = tol_r[m,n] = 2^-10 |r| + 1e-4 S + 2^-25 in r to out:      */
+/* Tn[m,n] = |gamma[n]| / rms[m] * (e[m,n] + |r[m,n]| * sum_j |r_j| e_j /  */
+/* (N rms[m]^2)), bounding |d out| (d rms / rms = sum_j r_j d r_j /         */
+/* (N rms^2)).                                                             */
+/* ---------------------------------------------------------------------- */
+void zo_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                         const uint16_t *resid, const uint16_t *gamma, double eps, int64_t M, int64_t N,
+                         int64_t K, double *r, double *out, double *S, double *Tn)
+{
+    zo_gemv_rows(wq, scales, x, M, N, K, NULL, 0, r, S);
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0, se = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double v = r[m * N + n] + zo_f16_to_f64(resid[m * N + n]);
+            r[m * N + n] = v;
+            ss += v * v;
+        }
+#if ZO_MUTANT == 9
+        double rms = sqrt(ss / (double)N);          /* mutant: eps dropped */
+#else
+        double rms = sqrt(ss / (double)N + eps);
+#endif
+        double *e = Tn + m * N;                      /* holds e first */
+        for (int64_t n = 0; n < N; ++n) {
+            e[n] = ldexp(fabs(r[m * N + n]), -10) + 1e-4 * S[m * N + n] + ldexp(1.0, -25);
+            se += fabs(r[m * N + n]) * e[n];
+        }
+        double drel = se / ((double)N * rms * rms);
+        for (int64_t n = 0; n < N; ++n) {
+            double g = zo_f16_to_f64(gamma[n]);
+            out[m * N + n] = r[m * N + n] / rms * g;
+            Tn[m * N + n] = fabs(g) / rms * (e[n] + fabs(r[m * N + n]) * drel);
+        }
+    }
 }
 
 /* ---------------------------------------------------------------------- */

@@ -514,6 +514,78 @@ def test_affine_moe_combine_weighted_sum_and_invalid_ids(oracle):
 
 
 # --------------------------------------------------------------------------
+# GEMV + residual add + RMSNorm (the add-norm step at the O / down tails)
+# --------------------------------------------------------------------------
+def test_add_rmsnorm_zero_weights_closed_form(oracle):
+    """All codes 7 (W = 0): r is the residual exactly and out is its RMSNorm,
+    computed here with fsum / sqrt from the definition (eps matters)."""
+    rng = np.random.default_rng(41)
+    M, N, K = 3, 37, 64
+    wq = np.full((N, K // 8), 0x77777777, np.uint32)
+    sc = synth.group_scales(rng, N, K)
+    x = synth.activations(rng, M, K)
+    res = synth.activations(rng, M, N)
+    gam = (rng.random(N) * 2 - 0.5).astype(np.float16)
+    eps = 0.25
+    r, out, S, Tn = oracle.gemv_add_rmsnorm(wq, sc, x, res, gam, eps, N, K)
+    for m in range(M):
+        rv = [float(v) for v in res[m]]
+        assert list(r[m]) == rv
+        rms = math.sqrt(math.fsum(v * v for v in rv) / N + eps)
+        want = [v / rms * float(g) for v, g in zip(rv, gam)]
+        assert np.allclose(out[m], want, rtol=1e-14, atol=0)
+
+
+def test_add_rmsnorm_zero_residual_is_gemv(oracle):
+    rng = np.random.default_rng(42)
+    M, N, K = 2, 48, 96
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x = synth.activations(rng, M, K)
+    r, out, S, _ = oracle.gemv_add_rmsnorm(wq, sc, x, np.zeros((M, N), np.float16), np.ones(N, np.float16),
+                                            1e-6, N, K)
+    y, Sy = oracle.gemv(wq, sc, x, N, K)
+    assert np.array_equal(r, y) and np.array_equal(S, Sy)
+
+
+def test_add_rmsnorm_scale_invariance(oracle):
+    """eps = 0: doubling every scale and the residual doubles r exactly and
+    leaves the normalised output unchanged."""
+    rng = np.random.default_rng(43)
+    M, N, K = 2, 40, 64
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x, res = synth.activations(rng, M, K), synth.activations(rng, M, N)
+    gam = (rng.random(N) + 0.5).astype(np.float16)
+    r1, o1, _, _ = oracle.gemv_add_rmsnorm(wq, sc, x, res, gam, 0.0, N, K)
+    r2, o2, _, _ = oracle.gemv_add_rmsnorm(wq, (sc.astype(np.float32) * 2).astype(np.float16), x,
+                                           (res.astype(np.float32) * 2).astype(np.float16), gam, 0.0, N, K)
+    assert np.array_equal(r2, 2 * r1)
+    assert np.allclose(o2, o1, rtol=1e-14, atol=0)
+
+
+def test_add_rmsnorm_brute_force(oracle):
+    """r in exact rationals from hex-decoded codes; out from fsum / sqrt."""
+    rng = np.random.default_rng(44)
+    M, N, K = 2, 5, 64
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x, res = synth.activations(rng, M, K), synth.activations(rng, M, N)
+    gam = (rng.random(N) + 0.5).astype(np.float16)
+    eps = 1e-3
+    r, out, S, _ = oracle.gemv_add_rmsnorm(wq, sc, x, res, gam, eps, N, K)
+    for m in range(M):
+        rex = []
+        for n in range(N):
+            codes = sum((codes_by_hex(int(w)) for w in wq[n]), [])
+            dot = sum(Fraction(float(x[m, k])) * (codes[k] - 7) * Fraction(float(sc[n, k // 32])) for k in range(K))
+            rex.append(dot + Fraction(float(res[m, n])))
+        for n in range(N):
+            assert abs(Fraction(r[m, n]) - rex[n]) <= Fraction(1, 10 ** 12) * (abs(rex[n]) + Fraction(S[m, n]))
+        rms = math.sqrt(math.fsum(float(v) ** 2 for v in rex) / N + eps)
+        for n in range(N):
+            want = float(rex[n]) / rms * float(gam[n])
+            assert abs(out[m, n] - want) <= 1e-12 * (abs(want) + 1e-300)
+
+
+# --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
 def _pins_pass(o) -> bool:
@@ -528,12 +600,14 @@ def _pins_pass(o) -> bool:
         test_affine_one_hot_columns_exact(o)
         test_affine_closed_form_constant_codes(o)
         test_affine_brute_force_exact_rationals(o)
+        test_add_rmsnorm_zero_weights_closed_form(o)
+        test_add_rmsnorm_brute_force(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
