@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
     ap.add_argument("--gate-up", action="store_true", help="kernel workload: fused gate_up + SiLU*mul")
+    ap.add_argument("--add-rmsnorm", action="store_true",
+                    help="kernel workload: the GEMV with the residual add and RMSNorm folded in")
     ap.add_argument("--affine", action="store_true",
                     help="kernel workload: the MLX affine format (w = s q + b, groups of 64)")
     ap.add_argument("--copies", type=int, default=8, help="distinct weight copies (kernel workload)")
@@ -653,7 +655,17 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
     cols = N // 2 if args.gate_up else N
     y = torch.empty((C, M, cols), dtype=torch.float16, device="cuda")
     stream = torch.cuda.Stream()
-    if args.affine:
+    if args.add_rmsnorm:
+        resid = torch.from_numpy(synth.activations(synth.rng_for("kernel_res"), M, N)).cuda()
+        gam = torch.ones(N, dtype=torch.float16, device="cuda")
+        y2 = torch.empty_like(y)
+        works = [torch.zeros(zq4.add_rmsnorm_work_bytes(M, N), dtype=torch.uint8, device="cuda") for _ in range(C)]
+
+        def chain():
+            for c in range(C):
+                zq4.gemv_add_rmsnorm(W[c], S[c], x, resid, gam, 1e-5, N, K, res_out=y[c], out=y2[c], work=works[c],
+                                     stream=stream)
+    elif args.affine:
         fa = zq4.gate_up_silu_affine if args.gate_up else zq4.gemv_affine
 
         def chain():
@@ -681,7 +693,10 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
     assert torch.isfinite(y).all() and (y != 0).any(), "kernel output zero/non-finite"
     per = el / (reps * C)
     b = N * (K // 8) * 4 + N * (K // gs) * 2 * (2 if args.affine else 1) + M * K * 2 + M * cols * 2
-    kind = ("MLX affine " if args.affine else "") + ("gate_up+SiLU" if args.gate_up else "GEMV")
+    if args.add_rmsnorm:
+        b += M * N * 2 * 2 + N * 2              # + residual in, normalised out, gamma
+    kind = ("MLX affine " if args.affine else "") + ("gate_up+SiLU" if args.gate_up else "GEMV") + \
+        (" + add + RMSNorm" if args.add_rmsnorm else "")
     return {"metric": f"{kind} {N}x{K} M={M} achieved HBM GB/s",
             "value": round(b / per / 1e9, 1), "unit": "GB/s", "us_per_call": round(per * 1e6, 3),
             "bytes_per_call": b, "frac_of_measured": round(b / per / 1e9 / peaks["hbm_gbs"], 4),

@@ -168,6 +168,36 @@ ZQ4_API zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *
                                        int top_k, int mode, int32_t *dev_status, void *stream);
 
 /*
+ * zq4_gemv_add_rmsnorm -- the O or down projection with the residual add
+ * and RMSNorm that follow it, folded into the GEMV as a tail reduction.
+ * Source: "Zero TVM Documentation", section "WGSL Kernel Roles", card 7
+ * "Fused Add + RMSNorm" (residual_out = A + B, output = RMSNorm(residual_out)
+ * x gamma; A the projection's output, B the running residual), and
+ * "Zero-TVM benchmarks", "Remaining levers" item 2 (fuse the add-norm into
+ * the matmul that feeds it, as a reduction at its tail).
+ *
+ *   r[m,n]       = resid[m,n] + sum_k x[m,k] w[n,k]     (fp32, w as zq4_gemv)
+ *   res_out[m,n] = f16(r[m,n])                          (the new residual)
+ *   out[m,n]     = f16(r[m,n] / sqrt(mean_n r[m,n]^2 + eps) * gamma[n])
+ *
+ * wq [N, K/8] u32, scales [N, K/32] f16, x [M, K] f16, resid / res_out / out
+ * [M, N] f16, gamma [N] f16; eps >= 0 (finite). work: caller-owned device
+ * scratch of zq4_add_rmsnorm_work_bytes(M, N) bytes, 16-byte aligned, whose
+ * first 16 bytes must be zero before the first call; every call leaves them
+ * zero (the rest is overwritten). One launch per block of up to 8 tokens;
+ * the last CTA of each normalises all N outputs (fixed reduction order, no
+ * floating-point atomics: repeated calls give identical bits). Outputs and
+ * work must not overlap each other or any input. Errors: ZQ4_ERR_NULL,
+ * ZQ4_ERR_SHAPE (M, N or K, or eps), ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED (x of K does not fit in shared memory), ZQ4_ERR_CUDA.
+ */
+ZQ4_API size_t zq4_add_rmsnorm_work_bytes(int M, int N);
+ZQ4_API zq4_status zq4_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                                        const uint16_t *resid, const uint16_t *gamma, float eps,
+                                        uint16_t *res_out, uint16_t *out, void *work, int M, int N, int K,
+                                        void *stream);
+
+/*
  * zq4_gemv_argmax -- the LM-head step of decode: fp32 logits and, per token,
  * the index of the largest logit.
  * Source: "Zero TVM Documentation", section "WGSL Kernel Roles" (the LM-head

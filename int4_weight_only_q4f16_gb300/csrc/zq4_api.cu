@@ -133,6 +133,39 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
                                      static_cast<cudaStream_t>(stream)));
 }
 
+size_t zq4_add_rmsnorm_work_bytes(int M, int N)
+{
+    return M > 0 && N > 0 ? 16 + size_t(M) * N * 4 : 0;
+}
+
+zq4_status zq4_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                                const uint16_t *resid, const uint16_t *gamma, float eps, uint16_t *res_out,
+                                uint16_t *out, void *work, int M, int N, int K, void *stream)
+{
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !resid || !gamma || !res_out || !out || !work) return ZQ4_ERR_NULL;
+    if (M <= 0 || !(eps >= 0.f) || !(eps < 3.0e38f)) return ZQ4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(work) || (reinterpret_cast<uintptr_t>(resid) & 1) ||
+        (reinterpret_cast<uintptr_t>(gamma) & 1) || (reinterpret_cast<uintptr_t>(res_out) & 1) ||
+        (reinterpret_cast<uintptr_t>(out) & 1))
+        return ZQ4_ERR_ALIGN;
+    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    const size_t mn = size_t(M) * N * 2, wbytes = zq4_add_rmsnorm_work_bytes(M, N);
+    const void *ins[5] = {wq, scales, x, resid, gamma};
+    const size_t inb[5] = {wq_bytes(N, K), sc_bytes(N, K), size_t(M) * K * 2, mn, size_t(N) * 2};
+    const void *outs[3] = {res_out, out, work};
+    const size_t outb[3] = {mn, mn, wbytes};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlap(outs[o], outb[o], ins[i], inb[i])) return ZQ4_ERR_OVERLAP;
+        for (int q = o + 1; q < 3; ++q)
+            if (overlap(outs[o], outb[o], outs[q], outb[q])) return ZQ4_ERR_OVERLAP;
+    }
+    return cuda_status(launch_add_rmsnorm(wq, scales, x, resid, gamma, eps, res_out, out, work, M, N, K,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 zq4_status zq4_gemv_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
                            int32_t *idx, float *maxval, uint64_t *work, int M, int N, int K, void *stream)
 {

@@ -269,6 +269,85 @@ __global__ void __launch_bounds__(kThreads) k_dense(DenseArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// GEMV + residual add + RMSNorm ("Zero TVM Documentation", card 7 "Fused
+// Add + RMSNorm", folded into the matmul that produces its input as a tail
+// reduction): every CTA writes r = resid + x W^T for its rows (fp32 to the
+// scratch, f16 as the new residual); the last CTA to finish (a counter)
+// reduces sum(r^2) of each token in a fixed order, and writes
+// f16(r * (1 / sqrt(mean + eps)) * gamma) for every row, then resets the
+// counter. Deterministic: no floating-point atomics.
+// ---------------------------------------------------------------------------
+template <int MT, int LPR>
+__global__ void __launch_bounds__(kThreads) k_dense_rms(RmsArgs a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];
+    __shared__ float s_red[kThreads / 32];
+    __shared__ float s_inv[MT];
+    __shared__ int s_last;
+    const int u0 = blockIdx.x * a.units_per_cta;
+    const int u1 = min(u0 + a.units_per_cta, a.N);
+    prefetch_rows(a.wq, a.scales, nullptr, a.K, a.K >> 5, size_t(u0), size_t(u1));
+    griddep_wait();
+    stage_rows(xs, a.x, a.M, MT, a.K);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
+    const unsigned mask = segment_mask<LPR>();
+    const uint32_t xs_base = smem_addr(xs);
+    for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
+        float part[1][MT];
+        rows_dot<MT, LPR, 1, false>(a.wq, a.scales, nullptr, a.K, u, xs_base, nullptr, lane, part);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[0][m] = segment_sum<LPR>(part[0][m], mask);
+        if (lane == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < a.M) {
+                    const size_t o = size_t(m) * a.N + u;
+                    const float v = part[0][m] + f16_bits_to_float(a.resid[o]);
+                    a.res_out[o] = float_to_f16_bits(v);
+                    a.r32[o] = v;
+                }
+            }
+        }
+    }
+    // the last CTA normalises every row of every token
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int warp = threadIdx.x >> 5, wl = threadIdx.x & 31;
+    for (int m = 0; m < a.M; ++m) {
+        float acc = 0.f;
+        for (int n = threadIdx.x; n < a.N; n += kThreads) {
+            const float v = __ldcg(a.r32 + size_t(m) * a.N + n);
+            acc = fmaf(v, v, acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (wl == 0) s_red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float t = 0.f;
+            for (int w = 0; w < kThreads / 32; ++w) t += s_red[w];
+            s_inv[m] = 1.0f / sqrtf(t / float(a.N) + a.eps);
+        }
+        __syncthreads();
+    }
+    const int total = a.M * a.N;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int m = i / a.N, n = i - m * a.N;
+        a.out[i] = float_to_f16_bits(__ldcg(a.r32 + i) * s_inv[m] * f16_bits_to_float(a.gamma[n]));
+    }
+    if (threadIdx.x == 0) *a.counter = 0u;
+}
+
+// ---------------------------------------------------------------------------
 // MoE, mode GATE_UP_SILU: blockIdx.y = slot (t*top_k + j); the slot's expert
 // is read after the wait (the ids may come from the previous kernel).
 // ---------------------------------------------------------------------------
@@ -547,6 +626,70 @@ int decode_tokens_per_launch(int M, int K, bool aff)
 int decode_tokens_per_launch(int M, int K) { return decode_tokens_per_launch(M, K, false); }
 
 // biases != nullptr: the MLX affine format (scales and biases per 64 weights).
+namespace {
+
+template <int MT, int LPR>
+cudaError_t launch_rms_t(const RmsArgs &a, cudaStream_t s)
+{
+    static int smem_set[kMaxDevices] = {};
+    auto kern = k_dense_rms<MT, LPR>;
+    const size_t smem = dense_smem(MT, a.K, false);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const int grid = (a.N + a.units_per_cta - 1) / a.units_per_cta;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+template <int MT>
+cudaError_t launch_rms_lpr(const RmsArgs &a, cudaStream_t s)
+{
+    switch (pick_lpr(a.K)) {
+    case 32: return launch_rms_t<MT, 32>(a, s);
+    case 16: return launch_rms_t<MT, 16>(a, s);
+    default: return launch_rms_t<MT, 8>(a, s);
+    }
+}
+
+}  // namespace
+
+// work: 16 bytes of counter (zero before the first call, left zero), then
+// the fp32 r of M x N.
+cudaError_t launch_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, const uint16_t *resid,
+                               const uint16_t *gamma, float eps, uint16_t *res_out, uint16_t *out, void *work, int M,
+                               int N, int K, cudaStream_t s)
+{
+    RmsArgs a;
+    a.wq = wq;
+    a.scales = scales;
+    a.gamma = gamma;
+    a.eps = eps;
+    a.N = N;
+    a.K = K;
+    a.counter = static_cast<unsigned *>(work);
+    a.units_per_cta = units_per_cta(N, pick_lpr(K));
+    float *r32 = reinterpret_cast<float *>(static_cast<uint8_t *>(work) + 16);
+    for (int m0 = 0; m0 < M;) {
+        const int mt = decode_tokens_per_launch(M - m0, K, false);
+        const size_t o = size_t(m0) * N;
+        a.x = x + size_t(m0) * K;
+        a.resid = resid + o;
+        a.res_out = res_out + o;
+        a.out = out + o;
+        a.r32 = r32 + o;
+        a.M = std::min(mt, M - m0);
+        cudaError_t e;
+        switch (mt) {
+        case 8: e = launch_rms_lpr<8>(a, s); break;
+        case 4: e = launch_rms_lpr<4>(a, s); break;
+        case 2: e = launch_rms_lpr<2>(a, s); break;
+        default: e = launch_rms_lpr<1>(a, s); break;
+        }
+        if (e != cudaSuccess) return e;
+        m0 += a.M;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, const uint16_t *x,
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s)
 {

@@ -24,6 +24,22 @@ struct DenseArgs {
     int y_stride;       // elements between output rows
 };
 
+// GEMV + residual add + RMSNorm (zq4_gemv_add_rmsnorm), one block of tokens.
+struct RmsArgs {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;        // [M, K]
+    const uint16_t *resid;    // [M, N]
+    const uint16_t *gamma;    // [N]
+    uint16_t *res_out;        // [M, N] f16(r)
+    uint16_t *out;            // [M, N] f16(r / rms * gamma)
+    float *r32;               // [M, N] scratch: r in fp32
+    unsigned *counter;        // CTAs done (the last one normalises and resets it)
+    float eps;
+    int M, N, K;
+    int units_per_cta;
+};
+
 struct MoeArgs {
     const uint32_t *wq;
     const uint16_t *scales;
@@ -98,6 +114,9 @@ cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs &a, int mode, cudaStream_t s);
 size_t moe_smem(int mode, int K, int top_k, bool aff);
+cudaError_t launch_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, const uint16_t *resid,
+                               const uint16_t *gamma, float eps, uint16_t *res_out, uint16_t *out, void *work, int M,
+                               int N, int K, cudaStream_t s);
 cudaError_t launch_dequant_f32(const uint32_t *wq, const uint16_t *scales, float *w, int N, int K,
                                cudaStream_t s);
 cudaError_t launch_dequant_f16(const uint32_t *wq, const uint16_t *scales, uint16_t *w, int N,

@@ -38,7 +38,8 @@ PREP_SEGMENTED = 2
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
            "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
-           "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine")
+           "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine",
+           "zq4_add_rmsnorm_work_bytes", "zq4_gemv_add_rmsnorm")
 
 
 class Zq4Error(RuntimeError):
@@ -77,6 +78,7 @@ def _load():
         "zq4_gemv_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_moe_gemv_affine": [P, P, P, I, P, P, I, I, I, P, P, I, I, P, P],
+        "zq4_gemv_add_rmsnorm": [P, P, P, P, P, ctypes.c_float, P, P, P, I, I, I, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -85,6 +87,8 @@ def _load():
     }
     lib.zq4_segmented_bytes.argtypes = [I, I]
     lib.zq4_segmented_bytes.restype = ctypes.c_size_t
+    lib.zq4_add_rmsnorm_work_bytes.argtypes = [I, I]
+    lib.zq4_add_rmsnorm_work_bytes.restype = ctypes.c_size_t
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -177,6 +181,31 @@ def gemv(wq, scales, x, N, K, y=None, stream=None):
     _check("zq4_gemv", lib.zq4_gemv(w, s, _ptr(x, "x", M * K * 2, 2), _ptr(y, "y", M * N * 2, 2),
                                     M, N, K, _stream(stream)))
     return y
+
+
+def add_rmsnorm_work_bytes(M, N):
+    return int(lib.zq4_add_rmsnorm_work_bytes(M, N))
+
+
+def gemv_add_rmsnorm(wq, scales, x, resid, gamma, eps, N, K, res_out=None, out=None, work=None, stream=None):
+    """(res_out, out): res_out = f16(resid + x W^T), out = f16(RMSNorm(that) *
+    gamma) (zq4_gemv_add_rmsnorm). ``work``: a zeroed uint8 device tensor of
+    add_rmsnorm_work_bytes(M, N) bytes, reusable across calls (made here if
+    not given)."""
+    M = x.numel() // K
+    if res_out is None:
+        res_out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    wb = add_rmsnorm_work_bytes(M, N)
+    if work is None:
+        work = torch.zeros(wb, dtype=torch.uint8, device=x.device)
+    w, s = _mat(wq, scales, N, K)
+    _check("zq4_gemv_add_rmsnorm", lib.zq4_gemv_add_rmsnorm(
+        w, s, _ptr(x, "x", M * K * 2, 2), _ptr(resid, "resid", M * N * 2, 2), _ptr(gamma, "gamma", N * 2, 2),
+        float(eps), _ptr(res_out, "res_out", M * N * 2, 2), _ptr(out, "out", M * N * 2, 2),
+        _ptr(work, "work", wb), M, N, K, _stream(stream)))
+    return res_out, out
 
 
 def gemv_argmax(wq, scales, x, N, K, y32=None, logits=True, maxval=None, idx=None, work=None, stream=None):

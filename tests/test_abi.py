@@ -117,3 +117,25 @@ def test_affine_moe_host_checks(lib):
              P(0), P(0)) == lib.ZQ4_ERR_ALIGN
     assert m(P(A), P(S), P(Bi), 4, P(X), P(Bi), 1, 64, 64, P(ids), P(r), 2, lib.MOE_DOWN_COMBINE,
              P(0), P(0)) == lib.ZQ4_ERR_OVERLAP
+
+
+def test_add_rmsnorm_host_checks(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000
+    S, X, R, G, O1, O2, W = (A + (i << 30) for i in range(1, 8))
+    f = lib.lib.zq4_gemv_add_rmsnorm
+    ok = (P(A), P(S), P(X), P(R), P(G), 1e-5, P(O1), P(O2), P(W), 1, 64, 64, P(0))
+    assert lib.lib.zq4_add_rmsnorm_work_bytes(2, 64) == 16 + 2 * 64 * 4
+    assert lib.lib.zq4_add_rmsnorm_work_bytes(0, 64) == 0
+    args = list(ok); args[8] = P(0)
+    assert f(*args) == lib.ZQ4_ERR_NULL
+    args = list(ok); args[5] = -1.0
+    assert f(*args) == lib.ZQ4_ERR_SHAPE                          # eps < 0
+    args = list(ok); args[5] = float("nan")
+    assert f(*args) == lib.ZQ4_ERR_SHAPE
+    args = list(ok); args[8] = P(W + 8)
+    assert f(*args) == lib.ZQ4_ERR_ALIGN                          # work 16-byte aligned
+    args = list(ok); args[7] = P(O1 + 2)
+    assert f(*args) == lib.ZQ4_ERR_OVERLAP                        # the two outputs
+    args = list(ok); args[6] = P(R)
+    assert f(*args) == lib.ZQ4_ERR_OVERLAP                        # res_out over resid (not in place)
