@@ -91,6 +91,7 @@ def _load(mutant: int = 0):
         lib.zo_moe_down_combine_affine.argtypes = [_p, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
         lib.zo_moe_down_combine_affine.restype = _i64
         lib.zo_gemv_add_rmsnorm.argtypes = [_p, _p, _p, _p, _p, ctypes.c_double, _i64, _i64, _i64, _p, _p, _p, _p]
+        lib.zo_qkv_rope.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _p] + [_p] * 9
         lib.zo_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
@@ -267,6 +268,20 @@ class Oracle:
         self.lib.zo_gemv_add_rmsnorm(_ptr(wq), _ptr(sc), _ptr(xx), _ptr(rr), _ptr(gg), float(eps), M, N, K,
                                      _ptr(r), _ptr(out), _ptr(S), _ptr(Tn))
         return r, out, S, Tn
+
+    # --- QKV + RoPE + KV append ------------------------------------------------
+    def qkv_rope(self, wq, scales, x, K: int, H: int, Hkv: int, D: int, base: float, pos):
+        """dict of fp64 arrays: q [M, H D], k and v [M, Hkv D] (the token's
+        cache rows), S_q/S_k/S_v (dot-product scales, summed over a RoPE
+        pair), A_q/A_k/A_v (|a| + |b| of the pair, |y| for V)."""
+        wq, sc, xx = _u32(wq), _f16(scales), _f16(x)
+        p = np.ascontiguousarray(pos, dtype=np.int32)
+        M = xx.size // K
+        o = {n: np.empty((M, (H if n.endswith("q") else Hkv) * D), dtype=np.float64)
+             for n in ("q", "k", "v", "S_q", "S_k", "S_v", "A_q", "A_k", "A_v")}
+        self.lib.zo_qkv_rope(_ptr(wq), _ptr(sc), _ptr(xx), M, K, H, Hkv, D, float(base), _ptr(p),
+                             *[_ptr(o[n]) for n in ("q", "k", "v", "S_q", "S_k", "S_v", "A_q", "A_k", "A_v")])
+        return o
 
     # --- LM head ------------------------------------------------------------
     def argmax(self, y) -> np.ndarray:

@@ -34,6 +34,11 @@
  *            residual), output = RMSNorm(residual_out) * gamma; "Zero-TVM
  *            benchmarks", "Remaining levers" item 2: folded into the matmul
  *            that produces A, as a reduction at its tail.
+ *  [DOC-QKV] "Zero TVM Documentation", section "WGSL Kernel Roles", card 3
+ *            "QKV + RoPE + KV-append (fused, decode)": the int4 QKV matmul,
+ *            the RoPE rotation of Q and K over the pair (dim, dim + D/2) of
+ *            one head (dim and dim+48 for D = 96), and the write of K and V
+ *            into the KV cache in one pass.
  *  [DOC-AFF] "Zero TVM Documentation", section "Qwen3.6-35B-A3B MoE", and
  *            "Zero-TVM benchmarks", sections "Chunked prefill for
  *            plain-attention + MLX-affine specs" and "Affine wide loads":
@@ -47,6 +52,10 @@
  * an expert id outside [0, E) contributes nothing and is counted. Affine
  * format: the codes are packed as in q4f16_1 (LSB-first, 8 per word) and are
  * unsigned (no zero point); scales and biases are f16 arrays [N, K/64].
+ * QKV rows: Q heads, then K heads, then V heads, D rows each (H, H_kv,
+ * H_kv heads); RoPE angle of pair i of a token at position p: p *
+ * base^(-2i/D), (a, b) -> (a cos - b sin, a sin + b cos); the KV cache as
+ * rows [slot][H_kv * D] of K and of V, the slot per token given.
  * RMSNorm (named, not defined, by the pages): y / sqrt(mean(y^2) + eps) over
  * the N features of one token, eps given by the caller; in the fused form A
  * is the exact dot product, not its f16 rounding.
@@ -416,6 +425,62 @@ void zo_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint1
             Tn[m * N + n] = fabs(g) / rms * (e[n] + fabs(r[m * N + n]) * drel);
         }
     }
+}
+
+/* ---------------------------------------------------------------------- */
+/* [DOC-QKV], [DOC-MM]: y = x W^T over the (H + 2 H_kv) D rows (exact dot   */
+/* products); for Q and K heads each pair (i, i + D/2), i < D/2, rotated by */
+/* theta = pos[m] * base^(-2i/D): q_out[m, h D + i] = a cos - b sin,        */
+/* q_out[m, h D + i + D/2] = a sin + b cos (K alike into kc, V copied into  */
+/* vc), kc/vc[m, c] = the token's row of the cache (written at its slot by  */
+/* the kernel). S[m, row] = sum_k |x w| of each of the two rows of a pair,  */
+/* added: Sp[m, c] = S_a + S_b for both outputs of the pair (for V: the     */
+/* row's own S); Ap[m, c] = |a| + |b| (V: |y|).                            */
+/* ---------------------------------------------------------------------- */
+void zo_qkv_rope(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, int64_t M, int64_t K, int64_t H,
+                 int64_t Hkv, int64_t D, double base, const int32_t *pos, double *q, double *kc, double *vc,
+                 double *Sq, double *Sk, double *Sv, double *Aq, double *Ak, double *Av)
+{
+    int64_t N = (H + 2 * Hkv) * D, half = D / 2;
+    double *y = (double *)malloc(sizeof(double) * (size_t)(M * N > 0 ? M * N : 1));
+    double *S = (double *)malloc(sizeof(double) * (size_t)(M * N > 0 ? M * N : 1));
+    zo_gemv_rows(wq, scales, x, M, N, K, NULL, 0, y, S);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t hb = 0; hb < H + 2 * Hkv; ++hb) {
+            for (int64_t i = 0; i < half; ++i) {
+                int64_t ra = hb * D + i, rb = ra + half;
+                double a = y[m * N + ra], b = y[m * N + rb];
+                double sa = S[m * N + ra], sb = S[m * N + rb];
+                if (hb < H + Hkv) {
+#if ZO_MUTANT == 10
+                    double th = (double)pos[m] * pow(base, -2.0 * (double)(i + 1) / (double)D); /* mutant: i+1 */
+#else
+                    double th = (double)pos[m] * pow(base, -2.0 * (double)i / (double)D);
+#endif
+                    double c = cos(th), sn = sin(th);
+                    double oa = a * c - b * sn, ob = a * sn + b * c;
+                    double *o = hb < H ? q + m * H * D : kc + m * Hkv * D;
+                    double *so = hb < H ? Sq + m * H * D : Sk + m * Hkv * D;
+                    double *ao = hb < H ? Aq + m * H * D : Ak + m * Hkv * D;
+                    int64_t h = hb < H ? hb : hb - H;
+                    o[h * D + i] = oa;
+                    o[h * D + i + half] = ob;
+                    so[h * D + i] = so[h * D + i + half] = sa + sb;
+                    ao[h * D + i] = ao[h * D + i + half] = fabs(a) + fabs(b);
+                } else {
+                    int64_t h = hb - H - Hkv;
+                    vc[m * Hkv * D + h * D + i] = a;
+                    vc[m * Hkv * D + h * D + i + half] = b;
+                    Sv[m * Hkv * D + h * D + i] = sa;
+                    Sv[m * Hkv * D + h * D + i + half] = sb;
+                    Av[m * Hkv * D + h * D + i] = fabs(a);
+                    Av[m * Hkv * D + h * D + i + half] = fabs(b);
+                }
+            }
+        }
+    }
+    free(y);
+    free(S);
 }
 
 /* ---------------------------------------------------------------------- */

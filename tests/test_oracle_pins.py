@@ -586,6 +586,70 @@ def test_add_rmsnorm_brute_force(oracle):
 
 
 # --------------------------------------------------------------------------
+# QKV projection + RoPE over (i, i + D/2) pairs + the token's K / V rows
+# --------------------------------------------------------------------------
+def _qkv_case(seed, H=3, Hkv=1, D=8, K=64, M=2):
+    rng = np.random.default_rng(seed)
+    N = (H + 2 * Hkv) * D
+    return rng, synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K), synth.activations(rng, M, K)
+
+
+def test_qkv_rope_position_zero_is_gemv(oracle):
+    H, Hkv, D, K = 3, 1, 8, 64
+    rng, wq, sc, x = _qkv_case(51, H, Hkv, D, K)
+    o = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, 10000.0, [0, 0])
+    y, S = oracle.gemv(wq, sc, x, (H + 2 * Hkv) * D, K)
+    assert np.array_equal(o["q"], y[:, :H * D])
+    assert np.array_equal(o["k"], y[:, H * D:(H + Hkv) * D])
+    assert np.array_equal(o["v"], y[:, (H + Hkv) * D:])
+
+
+def test_qkv_rope_rotation_closed_form(oracle):
+    """Each Q / K pair rotated by pos * base^(-2i/D), computed here with
+    math.pow / cos / sin from the GEMV outputs (V untouched)."""
+    H, Hkv, D, K = 2, 2, 16, 64
+    rng, wq, sc, x = _qkv_case(52, H, Hkv, D, K, M=3)
+    pos, base = [3, 17, 250], 500.0
+    o = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, pos)
+    y, _ = oracle.gemv(wq, sc, x, (H + 2 * Hkv) * D, K)
+    half = D // 2
+    for m in range(3):
+        for hb in range(H + Hkv):
+            for i in range(half):
+                a, b = y[m, hb * D + i], y[m, hb * D + i + half]
+                th = pos[m] * math.pow(base, -2.0 * i / D)
+                want = (a * math.cos(th) - b * math.sin(th), a * math.sin(th) + b * math.cos(th))
+                out, h = (o["q"], hb) if hb < H else (o["k"], hb - H)
+                got = (out[m, h * D + i], out[m, h * D + i + half])
+                assert abs(got[0] - want[0]) <= 1e-12 * (abs(a) + abs(b)) + 1e-300
+                assert abs(got[1] - want[1]) <= 1e-12 * (abs(a) + abs(b)) + 1e-300
+        assert np.array_equal(o["v"][m], y[m, (H + Hkv) * D:])
+
+
+def test_qkv_rope_rotations_compose_and_keep_norms(oracle):
+    """Rotating at p1 + p2 equals rotating the p1 result by p2's angles, and
+    every pair keeps its length."""
+    H, Hkv, D, K = 2, 1, 12, 64
+    rng, wq, sc, x = _qkv_case(53, H, Hkv, D, K, M=1)
+    base, p1, p2 = 10000.0, 7, 30
+    o0 = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, [0])
+    o1 = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, [p1])
+    o12 = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, [p1 + p2])
+    half = D // 2
+    for name in ("q", "k"):
+        for h in range(o1[name].shape[1] // D):
+            for i in range(half):
+                a0, b0 = o0[name][0, h * D + i], o0[name][0, h * D + i + half]
+                a1, b1 = o1[name][0, h * D + i], o1[name][0, h * D + i + half]
+                assert abs(math.hypot(a1, b1) - math.hypot(a0, b0)) <= 1e-12 * math.hypot(a0, b0) + 1e-300
+                th = p2 * math.pow(base, -2.0 * i / D)
+                want = (a1 * math.cos(th) - b1 * math.sin(th), a1 * math.sin(th) + b1 * math.cos(th))
+                got = (o12[name][0, h * D + i], o12[name][0, h * D + i + half])
+                assert abs(got[0] - want[0]) <= 1e-11 * math.hypot(a0, b0) + 1e-300
+                assert abs(got[1] - want[1]) <= 1e-11 * math.hypot(a0, b0) + 1e-300
+
+
+# --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
 def _pins_pass(o) -> bool:
@@ -602,12 +666,13 @@ def _pins_pass(o) -> bool:
         test_affine_brute_force_exact_rationals(o)
         test_add_rmsnorm_zero_weights_closed_form(o)
         test_add_rmsnorm_brute_force(o)
+        test_qkv_rope_rotation_closed_form(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
