@@ -168,6 +168,39 @@ ZQ4_API zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *
                                        int top_k, int mode, int32_t *dev_status, void *stream);
 
 /*
+ * zq4_qkv_rope_append -- the attention input projection of a decode step
+ * with the RoPE rotation and the KV-cache write folded in. Source: "Zero
+ * TVM Documentation", section "WGSL Kernel Roles", card 3 "QKV + RoPE +
+ * KV-append (fused, decode)": the int4 QKV matmul, the rotation of Q and K
+ * over the pair (dim, dim + D/2) of one head, and the write of K and V into
+ * the cache, in one pass, with each pair rotated where it is computed.
+ *
+ *   wq [(H + 2 H_kv) D, K/8] u32, scales [(H + 2 H_kv) D, K/32] f16: rows
+ *   of the H query heads, then the H_kv key heads, then the H_kv value
+ *   heads, D rows each (as zq4_gemv's matrix); x [M, K] f16.
+ *   y = x W^T (fp32). For token m, head h and i < D/2, with
+ *   theta = pos[m] * rope_base^(-2i/D) (fp64):
+ *     q_out[m, h D + i]       = f16(a cos theta - b sin theta)
+ *     q_out[m, h D + i + D/2] = f16(a sin theta + b cos theta)
+ *   with (a, b) = y of rows (h D + i, h D + i + D/2) of the Q block; the K
+ *   block alike into k_cache[slot[m], h D ..], and V unrotated into
+ *   v_cache[slot[m], h D ..]. Caches [n_slots, H_kv D] f16; pos and slot
+ *   int32 [M] (device). A slot outside [0, n_slots) writes nothing for that
+ *   token and ORs ZQ4_DEV_BAD_SLOT into *dev_status (a device int32, may be
+ *   NULL).
+ *
+ * D even, H, H_kv, M, n_slots >= 1, K a multiple of 32, rope_base > 0. x
+ * 16-byte aligned, outputs 2-byte, pos / slot / dev_status 4-byte aligned;
+ * outputs must not overlap each other or the inputs. One launch per block
+ * of up to 8 tokens. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
+ * ZQ4_ERR_OVERLAP, ZQ4_ERR_UNSUPPORTED (sizes), ZQ4_ERR_CUDA.
+ */
+ZQ4_API zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, int M, int K,
+                                       int H, int H_kv, int D, double rope_base, const int32_t *pos,
+                                       const int32_t *slot, uint16_t *q_out, uint16_t *k_cache, uint16_t *v_cache,
+                                       int n_slots, int32_t *dev_status, void *stream);
+
+/*
  * zq4_gemv_add_rmsnorm -- the O or down projection with the residual add
  * and RMSNorm that follow it, folded into the GEMV as a tail reduction.
  * Source: "Zero TVM Documentation", section "WGSL Kernel Roles", card 7
@@ -234,6 +267,7 @@ ZQ4_API zq4_status zq4_gemv_argmax(const uint32_t *wq, const uint16_t *scales, c
 
 /* Bits of the device status word of zq4_moe_gemv. */
 #define ZQ4_DEV_BAD_EXPERT_ID 1u
+#define ZQ4_DEV_BAD_SLOT 2u          /* zq4_qkv_rope_append: a slot outside [0, n_slots) */
 
 /*
  * zq4_moe_gemv -- expert-gather q4f16_1 GEMV of a mixture-of-experts block.

@@ -133,6 +133,55 @@ zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *
                                      static_cast<cudaStream_t>(stream)));
 }
 
+zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, int M, int K, int H,
+                               int H_kv, int D, double rope_base, const int32_t *pos, const int32_t *slot,
+                               uint16_t *q_out, uint16_t *k_cache, uint16_t *v_cache, int n_slots,
+                               int32_t *dev_status, void *stream)
+{
+    if (H <= 0 || H_kv <= 0 || D <= 0 || (D & 1) || M <= 0 || n_slots <= 0) return ZQ4_ERR_SHAPE;
+    if (!(rope_base > 0.0) || !(rope_base < 1e300)) return ZQ4_ERR_SHAPE;
+    const long long Nl = (long long)(H + 2LL * H_kv) * D;
+    if (Nl > (1LL << 30) || (long long)n_slots * H_kv * D > (1LL << 40)) return ZQ4_ERR_UNSUPPORTED;
+    const int N = int(Nl);
+    zq4_status st = check_matrix(wq, scales, N, K);
+    if (st != ZQ4_OK) return st;
+    if (!x || !pos || !slot || !q_out || !k_cache || !v_cache) return ZQ4_ERR_NULL;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(q_out) & 1) || (reinterpret_cast<uintptr_t>(k_cache) & 1) ||
+        (reinterpret_cast<uintptr_t>(v_cache) & 1) || (reinterpret_cast<uintptr_t>(pos) & 3) ||
+        (reinterpret_cast<uintptr_t>(slot) & 3) || (reinterpret_cast<uintptr_t>(dev_status) & 3))
+        return ZQ4_ERR_ALIGN;
+    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    const size_t qb = size_t(M) * H * D * 2, cb = size_t(n_slots) * H_kv * D * 2;
+    const void *ins[5] = {wq, scales, x, pos, slot};
+    const size_t inb[5] = {wq_bytes(N, K), sc_bytes(N, K), size_t(M) * K * 2, size_t(M) * 4, size_t(M) * 4};
+    const void *outs[3] = {q_out, k_cache, v_cache};
+    const size_t outb[3] = {qb, cb, cb};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlap(outs[o], outb[o], ins[i], inb[i])) return ZQ4_ERR_OVERLAP;
+        for (int q = o + 1; q < 3; ++q)
+            if (overlap(outs[o], outb[o], outs[q], outb[q])) return ZQ4_ERR_OVERLAP;
+    }
+    QkvArgs a = {};
+    a.wq = wq;
+    a.scales = scales;
+    a.x = x;
+    a.pos = pos;
+    a.slot = slot;
+    a.q_out = q_out;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.dev_status = dev_status;
+    a.base = rope_base;
+    a.M = M;
+    a.K = K;
+    a.H = H;
+    a.Hkv = H_kv;
+    a.D = D;
+    a.n_slots = n_slots;
+    return cuda_status(launch_qkv_rope(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t zq4_add_rmsnorm_work_bytes(int M, int N)
 {
     return M > 0 && N > 0 ? 16 + size_t(M) * N * 4 : 0;

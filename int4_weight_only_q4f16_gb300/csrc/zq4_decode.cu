@@ -162,10 +162,11 @@ __device__ __forceinline__ unsigned segment_mask()
 // Accumulate RU consecutive rows (starting at row0) of a matrix against MT
 // staged activation rows: part[r][m] holds this lane's partial sums.
 // AFF: scales and biases [rows][K/64]; xsum = the staged chunk sums of x.
+// The RU rows are row0, row0 + row_step, ..
 template <int MT, int LPR, int RU, bool AFF>
 __device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases, int K,
                                          int row0, uint32_t xs_base, const float *xsum, int lane,
-                                         float (&part)[RU][MT])
+                                         float (&part)[RU][MT], int row_step = 1)
 {
     const int G = K >> 5, KW = K >> 3, GS = AFF ? K >> 6 : G;
     const uint32_t row_bytes = uint32_t(K) * 2;
@@ -174,9 +175,10 @@ __device__ __forceinline__ void rows_dot(const uint32_t *wq, const uint16_t *sca
     const uint16_t *brow[RU];
 #pragma unroll
     for (int r = 0; r < RU; ++r) {
-        wrow[r] = wq + size_t(row0 + r) * KW;
-        srow[r] = scales + size_t(row0 + r) * GS;
-        brow[r] = AFF ? biases + size_t(row0 + r) * GS : nullptr;
+        const size_t row = size_t(row0) + size_t(r) * row_step;
+        wrow[r] = wq + row * KW;
+        srow[r] = scales + row * GS;
+        brow[r] = AFF ? biases + row * GS : nullptr;
 #pragma unroll
         for (int m = 0; m < MT; ++m) part[r][m] = 0.f;
     }
@@ -345,6 +347,74 @@ __global__ void __launch_bounds__(kThreads) k_dense_rms(RmsArgs a)
         a.out[i] = float_to_f16_bits(__ldcg(a.r32 + i) * s_inv[m] * f16_bits_to_float(a.gamma[n]));
     }
     if (threadIdx.x == 0) *a.counter = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// QKV projection + RoPE + KV append ("Zero TVM Documentation", card 3 "QKV +
+// RoPE + KV-append (fused, decode)"): a unit is one RoPE pair, rows
+// (hb D + i, hb D + i + D/2) of head block hb (Q heads, then K, then V), so
+// the pair is rotated in registers. Angle pos * base^(-2i/D) in fp64 (a few
+// thousand per call). Q goes to q_out, rotated K and plain V to the cache
+// rows of the token's slot; a slot outside [0, n_slots) writes nothing and
+// sets ZQ4_DEV_BAD_SLOT.
+// ---------------------------------------------------------------------------
+template <int MT, int LPR>
+__global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];
+    const int half = a.D >> 1;
+    const int u0 = blockIdx.x * a.units_per_cta;
+    const int u1 = min(u0 + a.units_per_cta, a.units);
+    if (u0 < u1) {
+        const int r0 = (u0 / half) * a.D, r1 = ((u1 - 1) / half + 1) * a.D;
+        prefetch_rows(a.wq, a.scales, nullptr, a.K, a.K >> 5, size_t(r0), size_t(r1));
+    }
+    griddep_wait();
+    stage_rows(xs, a.x, a.M, MT, a.K);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    const int sub = threadIdx.x / LPR, lane = threadIdx.x % LPR;
+    const unsigned mask = segment_mask<LPR>();
+    const uint32_t xs_base = smem_addr(xs);
+    const int kv_row = a.Hkv * a.D;
+    for (int u = u0 + sub; u < u1; u += kThreads / LPR) {
+        const int hb = u / half, i = u - hb * half;
+        float part[2][MT];
+        rows_dot<MT, LPR, 2, false>(a.wq, a.scales, nullptr, a.K, hb * a.D + i, xs_base, nullptr, lane, part,
+                                    half);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) part[r][m] = segment_sum<LPR>(part[r][m], mask);
+        if (lane != 0) continue;
+        const bool rot = hb < a.H + a.Hkv;
+        const double inv_freq = rot ? pow(a.base, -2.0 * double(i) / double(a.D)) : 0.0;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= a.M) continue;
+            float oa = part[0][m], ob = part[1][m];
+            if (rot) {
+                double sn, cs;
+                sincos(double(a.pos[m]) * inv_freq, &sn, &cs);
+                oa = float(double(part[0][m]) * cs - double(part[1][m]) * sn);
+                ob = float(double(part[0][m]) * sn + double(part[1][m]) * cs);
+            }
+            uint16_t *dst;
+            if (hb < a.H) {
+                dst = a.q_out + size_t(m) * a.H * a.D + size_t(hb) * a.D;
+            } else {
+                const int sl = a.slot[m];
+                if (sl < 0 || sl >= a.n_slots) {
+                    if (a.dev_status) atomicOr(reinterpret_cast<unsigned *>(a.dev_status), ZQ4_DEV_BAD_SLOT);
+                    continue;
+                }
+                dst = (rot ? a.k_cache : a.v_cache) + size_t(sl) * kv_row + size_t(rot ? hb - a.H : hb - a.H - a.Hkv) * a.D;
+            }
+            dst[i] = float_to_f16_bits(oa);
+            dst[i + half] = float_to_f16_bits(ob);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -651,6 +721,59 @@ cudaError_t launch_rms_lpr(const RmsArgs &a, cudaStream_t s)
 }
 
 }  // namespace
+
+namespace {
+
+template <int MT, int LPR>
+cudaError_t launch_qkv_t(const QkvArgs &a, cudaStream_t s)
+{
+    static int smem_set[kMaxDevices] = {};
+    auto kern = k_qkv_rope<MT, LPR>;
+    const size_t smem = dense_smem(MT, a.K, false);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const int grid = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+template <int MT>
+cudaError_t launch_qkv_lpr(const QkvArgs &a, cudaStream_t s)
+{
+    switch (pick_lpr(a.K)) {
+    case 32: return launch_qkv_t<MT, 32>(a, s);
+    case 16: return launch_qkv_t<MT, 16>(a, s);
+    default: return launch_qkv_t<MT, 8>(a, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_rope(const QkvArgs &a0, cudaStream_t s)
+{
+    QkvArgs a = a0;
+    a.units = (a.H + 2 * a.Hkv) * (a.D >> 1);
+    a.units_per_cta = units_per_cta(a.units, pick_lpr(a.K));
+    const uint16_t *x = a0.x;
+    uint16_t *q = a0.q_out;
+    for (int m0 = 0; m0 < a0.M;) {
+        const int mt = decode_tokens_per_launch(a0.M - m0, a0.K, false);
+        a.x = x + size_t(m0) * a.K;
+        a.q_out = q + size_t(m0) * a.H * a.D;
+        a.pos = a0.pos + m0;
+        a.slot = a0.slot + m0;
+        a.M = std::min(mt, a0.M - m0);
+        cudaError_t e;
+        switch (mt) {
+        case 8: e = launch_qkv_lpr<8>(a, s); break;
+        case 4: e = launch_qkv_lpr<4>(a, s); break;
+        case 2: e = launch_qkv_lpr<2>(a, s); break;
+        default: e = launch_qkv_lpr<1>(a, s); break;
+        }
+        if (e != cudaSuccess) return e;
+        m0 += a.M;
+    }
+    return cudaSuccess;
+}
 
 // work: 16 bytes of counter (zero before the first call, left zero), then
 // the fp32 r of M x N.

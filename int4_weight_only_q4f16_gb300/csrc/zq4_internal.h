@@ -40,6 +40,22 @@ struct RmsArgs {
     int units_per_cta;
 };
 
+// QKV projection + RoPE + KV append (zq4_qkv_rope_append), one block of tokens.
+struct QkvArgs {
+    const uint32_t *wq;
+    const uint16_t *scales;
+    const uint16_t *x;        // [M, K]
+    const int32_t *pos;       // [M] RoPE positions
+    const int32_t *slot;      // [M] cache rows
+    uint16_t *q_out;          // [M, H*D]
+    uint16_t *k_cache;        // [n_slots, Hkv*D]
+    uint16_t *v_cache;        // [n_slots, Hkv*D]
+    int32_t *dev_status;
+    double base;
+    int M, K, H, Hkv, D, n_slots;
+    int units, units_per_cta;
+};
+
 struct MoeArgs {
     const uint32_t *wq;
     const uint16_t *scales;
@@ -114,6 +130,7 @@ cudaError_t launch_decode(const uint32_t *wq, const uint16_t *scales, const uint
                           uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs &a, int mode, cudaStream_t s);
 size_t moe_smem(int mode, int K, int top_k, bool aff);
+cudaError_t launch_qkv_rope(const QkvArgs &a, cudaStream_t s);
 cudaError_t launch_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, const uint16_t *resid,
                                const uint16_t *gamma, float eps, uint16_t *res_out, uint16_t *out, void *work, int M,
                                int N, int K, cudaStream_t s);

@@ -39,7 +39,7 @@ EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_devic
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
            "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
            "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine",
-           "zq4_add_rmsnorm_work_bytes", "zq4_gemv_add_rmsnorm")
+           "zq4_add_rmsnorm_work_bytes", "zq4_gemv_add_rmsnorm", "zq4_qkv_rope_append")
 
 
 class Zq4Error(RuntimeError):
@@ -79,6 +79,7 @@ def _load():
         "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_moe_gemv_affine": [P, P, P, I, P, P, I, I, I, P, P, I, I, P, P],
         "zq4_gemv_add_rmsnorm": [P, P, P, P, P, ctypes.c_float, P, P, P, I, I, I, P],
+        "zq4_qkv_rope_append": [P, P, P, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, I, P, P],
         "zq4_stack_plan_init": [P, I, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_run": [P, P],
         "zq4_stack_plan_init_static": [P, I, I, P, P],
@@ -181,6 +182,28 @@ def gemv(wq, scales, x, N, K, y=None, stream=None):
     _check("zq4_gemv", lib.zq4_gemv(w, s, _ptr(x, "x", M * K * 2, 2), _ptr(y, "y", M * N * 2, 2),
                                     M, N, K, _stream(stream)))
     return y
+
+
+DEV_BAD_SLOT = 2
+
+
+def qkv_rope_append(wq, scales, x, K, H, H_kv, D, rope_base, pos, slot, k_cache, v_cache, q_out=None,
+                    dev_status=None, stream=None):
+    """q_out [M, H*D]: the rotated queries; rotated keys and the values are
+    written into k_cache / v_cache [n_slots, H_kv*D] at rows slot[m]
+    (zq4_qkv_rope_append). pos, slot: int32 device tensors [M]."""
+    M = x.numel() // K
+    N = (H + 2 * H_kv) * D
+    n_slots = k_cache.numel() // (H_kv * D)
+    if q_out is None:
+        q_out = torch.empty((M, H * D), dtype=torch.float16, device=x.device)
+    w, s = _mat(wq, scales, N, K)
+    cb = n_slots * H_kv * D * 2
+    _check("zq4_qkv_rope_append", lib.zq4_qkv_rope_append(
+        w, s, _ptr(x, "x", M * K * 2, 2), M, K, H, H_kv, D, float(rope_base), _ptr(pos, "pos", M * 4, 4),
+        _ptr(slot, "slot", M * 4, 4), _ptr(q_out, "q_out", M * H * D * 2, 2), _ptr(k_cache, "k_cache", cb, 2),
+        _ptr(v_cache, "v_cache", cb, 2), n_slots, _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
+    return q_out
 
 
 def add_rmsnorm_work_bytes(M, N):

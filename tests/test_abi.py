@@ -139,3 +139,21 @@ def test_add_rmsnorm_host_checks(lib):
     assert f(*args) == lib.ZQ4_ERR_OVERLAP                        # the two outputs
     args = list(ok); args[6] = P(R)
     assert f(*args) == lib.ZQ4_ERR_OVERLAP                        # res_out over resid (not in place)
+
+
+def test_qkv_rope_host_checks(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000
+    S, X, Pp, Sl, Q, Kc, Vc = (A + (i << 30) for i in range(1, 8))
+    f = lib.lib.zq4_qkv_rope_append
+    ok = [P(A), P(S), P(X), 1, 64, 4, 2, 8, 10000.0, P(Pp), P(Sl), P(Q), P(Kc), P(Vc), 16, P(0), P(0)]
+    args = list(ok); args[7] = 7
+    assert f(*args) == lib.ZQ4_ERR_SHAPE          # odd head dim
+    args = list(ok); args[8] = 0.0
+    assert f(*args) == lib.ZQ4_ERR_SHAPE          # rope base
+    args = list(ok); args[9] = P(0)
+    assert f(*args) == lib.ZQ4_ERR_NULL
+    args = list(ok); args[10] = P(Sl + 2)
+    assert f(*args) == lib.ZQ4_ERR_ALIGN
+    args = list(ok); args[13] = P(Kc)
+    assert f(*args) == lib.ZQ4_ERR_OVERLAP        # k and v caches the same
