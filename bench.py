@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
     ap.add_argument("--k", type=int, default=3072, help="columns of W (kernel workload)")
     ap.add_argument("--gate-up", action="store_true", help="kernel workload: fused gate_up + SiLU*mul")
+    ap.add_argument("--qkv-rope", action="store_true",
+                    help="kernel workload: the Phi-3 QKV projection (32 + 2 x 32 heads of 96) with RoPE and the "
+                         "KV-cache write folded in (--n is taken as 9216)")
     ap.add_argument("--add-rmsnorm", action="store_true",
                     help="kernel workload: the GEMV with the residual add and RMSNorm folded in")
     ap.add_argument("--affine", action="store_true",
@@ -655,7 +658,21 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
     cols = N // 2 if args.gate_up else N
     y = torch.empty((C, M, cols), dtype=torch.float16, device="cuda")
     stream = torch.cuda.Stream()
-    if args.add_rmsnorm:
+    if args.qkv_rope:
+        Hh, Hk, Dh = 32, 32, 96
+        assert N == (Hh + 2 * Hk) * Dh, "--qkv-rope takes --n 9216"
+        n_slots = 4096
+        kcs = [torch.zeros((n_slots, Hk * Dh), dtype=torch.float16, device="cuda") for _ in range(C)]
+        vcs = [torch.zeros_like(kcs[0]) for _ in range(C)]
+        posd = torch.full((M,), 1000, dtype=torch.int32, device="cuda")
+        slotd = torch.arange(M, dtype=torch.int32, device="cuda")
+        qo = torch.empty((C, M, Hh * Dh), dtype=torch.float16, device="cuda")
+
+        def chain():
+            for c in range(C):
+                zq4.qkv_rope_append(W[c], S[c], x, K, Hh, Hk, Dh, 10000.0, posd, slotd, kcs[c], vcs[c], q_out=qo[c],
+                                    stream=stream)
+    elif args.add_rmsnorm:
         resid = torch.from_numpy(synth.activations(synth.rng_for("kernel_res"), M, N)).cuda()
         gam = torch.ones(N, dtype=torch.float16, device="cuda")
         y2 = torch.empty_like(y)
@@ -690,13 +707,16 @@ def run_kernel(args, torch, dist, peaks, peak_kind):
         replay_on(torch, g, stream, max(3, args.warmup))
         el = time_replays(torch, g.replay, reps, stream)
     torch.cuda.synchronize()
-    assert torch.isfinite(y).all() and (y != 0).any(), "kernel output zero/non-finite"
+    out_chk = qo if args.qkv_rope else y
+    assert torch.isfinite(out_chk).all() and (out_chk != 0).any(), "kernel output zero/non-finite"
     per = el / (reps * C)
     b = N * (K // 8) * 4 + N * (K // gs) * 2 * (2 if args.affine else 1) + M * K * 2 + M * cols * 2
     if args.add_rmsnorm:
         b += M * N * 2 * 2 + N * 2              # + residual in, normalised out, gamma
+    if args.qkv_rope:
+        b += M * 8                              # + pos, slot (the outputs are the N columns already counted)
     kind = ("MLX affine " if args.affine else "") + ("gate_up+SiLU" if args.gate_up else "GEMV") + \
-        (" + add + RMSNorm" if args.add_rmsnorm else "")
+        (" + add + RMSNorm" if args.add_rmsnorm else "") + (" + RoPE + KV append" if args.qkv_rope else "")
     return {"metric": f"{kind} {N}x{K} M={M} achieved HBM GB/s",
             "value": round(b / per / 1e9, 1), "unit": "GB/s", "us_per_call": round(per * 1e6, 3),
             "bytes_per_call": b, "frac_of_measured": round(b / per / 1e9 / peaks["hbm_gbs"], 4),
