@@ -189,7 +189,7 @@ ZQ4_API zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *
  *   token and ORs ZQ4_DEV_BAD_SLOT into *dev_status (a device int32, may be
  *   NULL).
  *
- * D even, H, H_kv, M, n_slots >= 1, K a multiple of 32, rope_base > 0. x
+ * D even (<= 512), H, H_kv, M, n_slots >= 1, K a multiple of 32, rope_base > 0. x
  * 16-byte aligned, outputs 2-byte, pos / slot / dev_status 4-byte aligned;
  * outputs must not overlap each other or the inputs. One launch per block
  * of up to 8 tokens. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,

@@ -139,6 +139,7 @@ zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const
                                int32_t *dev_status, void *stream)
 {
     if (H <= 0 || H_kv <= 0 || D <= 0 || (D & 1) || M <= 0 || n_slots <= 0) return ZQ4_ERR_SHAPE;
+    if (D > 512) return ZQ4_ERR_UNSUPPORTED;
     if (!(rope_base > 0.0) || !(rope_base < 1e300)) return ZQ4_ERR_SHAPE;
     const long long Nl = (long long)(H + 2LL * H_kv) * D;
     if (Nl > (1LL << 30) || (long long)n_slots * H_kv * D > (1LL << 40)) return ZQ4_ERR_UNSUPPORTED;
@@ -150,7 +151,7 @@ zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const
         (reinterpret_cast<uintptr_t>(v_cache) & 1) || (reinterpret_cast<uintptr_t>(pos) & 3) ||
         (reinterpret_cast<uintptr_t>(slot) & 3) || (reinterpret_cast<uintptr_t>(dev_status) & 3))
         return ZQ4_ERR_ALIGN;
-    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    if (size_t(K) * 2 + 2048 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;   // x beside the frequency table
     const size_t qb = size_t(M) * H * D * 2, cb = size_t(n_slots) * H_kv * D * 2;
     const void *ins[5] = {wq, scales, x, pos, slot};
     const size_t inb[5] = {wq_bytes(N, K), sc_bytes(N, K), size_t(M) * K * 2, size_t(M) * 4, size_t(M) * 4};

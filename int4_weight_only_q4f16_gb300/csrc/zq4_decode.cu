@@ -357,12 +357,19 @@ __global__ void __launch_bounds__(kThreads) k_dense_rms(RmsArgs a)
 // thousand per call). Q goes to q_out, rotated K and plain V to the cache
 // rows of the token's slot; a slot outside [0, n_slots) writes nothing and
 // sets ZQ4_DEV_BAD_SLOT.
+// Angles: base^(-2i/D) once per CTA in fp64 (shared memory); per value the
+// fp64 angle pos * f_i is reduced modulo 2 pi (Cody-Waite, 2 pi split into a
+// double and its remainder), and the reduced angle, in [-pi, pi], goes to
+// fp32 sincosf: ~1e-7 rad, far inside the bound the rotation carries.
 // ---------------------------------------------------------------------------
+constexpr int kMaxRopeHalf = 256;                 // D <= 512
 template <int MT, int LPR>
 __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
 {
     extern __shared__ __align__(16) uint8_t xs[];
+    __shared__ double s_freq[kMaxRopeHalf];
     const int half = a.D >> 1;
+    for (int i = threadIdx.x; i < half; i += kThreads) s_freq[i] = pow(a.base, -2.0 * double(i) / double(a.D));
     const int u0 = blockIdx.x * a.units_per_cta;
     const int u1 = min(u0 + a.units_per_cta, a.units);
     if (u0 < u1) {
@@ -389,16 +396,20 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
             for (int m = 0; m < MT; ++m) part[r][m] = segment_sum<LPR>(part[r][m], mask);
         if (lane != 0) continue;
         const bool rot = hb < a.H + a.Hkv;
-        const double inv_freq = rot ? pow(a.base, -2.0 * double(i) / double(a.D)) : 0.0;
+        const double inv_freq = rot ? s_freq[i] : 0.0;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m >= a.M) continue;
             float oa = part[0][m], ob = part[1][m];
             if (rot) {
-                double sn, cs;
-                sincos(double(a.pos[m]) * inv_freq, &sn, &cs);
-                oa = float(double(part[0][m]) * cs - double(part[1][m]) * sn);
-                ob = float(double(part[0][m]) * sn + double(part[1][m]) * cs);
+                const double kTwoPiHi = 6.283185307179586, kTwoPiLo = 2.4492935982947064e-16;
+                const double th = double(a.pos[m]) * inv_freq;
+                const double k = rint(th * (1.0 / kTwoPiHi));
+                const float r = float(fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, th)));
+                float sn, cs;
+                sincosf(r, &sn, &cs);
+                oa = part[0][m] * cs - part[1][m] * sn;
+                ob = part[0][m] * sn + part[1][m] * cs;
             }
             uint16_t *dst;
             if (hb < a.H) {
@@ -756,7 +767,12 @@ cudaError_t launch_qkv_rope(const QkvArgs &a0, cudaStream_t s)
     const uint16_t *x = a0.x;
     uint16_t *q = a0.q_out;
     for (int m0 = 0; m0 < a0.M;) {
-        const int mt = decode_tokens_per_launch(a0.M - m0, a0.K, false);
+        // tokens per launch: x in dynamic shared memory next to the static
+        // frequency table
+        int mt = 8;
+        while (mt > 1 && (mt > a0.M - m0 || dense_smem(mt, a0.K, false) + sizeof(double) * kMaxRopeHalf >
+                                                  decode_max_smem()))
+            mt >>= 1;
         a.x = x + size_t(m0) * a.K;
         a.q_out = q + size_t(m0) * a.H * a.D;
         a.pos = a0.pos + m0;
