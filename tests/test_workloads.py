@@ -58,3 +58,28 @@ def test_generator_shapes_and_ranges():
     b = synth.packed_codes(synth.rng_for("w", 3), 4, 64)
     c = synth.packed_codes(synth.rng_for("w", 4), 4, 64)
     assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
+def test_chained_stack_wiring_and_bytes():
+    """DecodeStack(chain=True): every projection reads the previous output
+    (o a view over the first M*K values of qkv's), only the first input is
+    seeded, and the algorithmic bytes count each projection's input and
+    output once, as for the unchained stack."""
+    import torch
+    from int4_weight_only_q4f16_gb300 import stack as st
+    layer = (("qkv", 96, 64), ("o", 32, 64), ("gate_up", 128, 32), ("down", 64, 64))
+    for M in (1, 3):
+        s = st.DecodeStack(layer, 2, ("lm_head", 40, 64), M=M, device="cpu", chain=True)
+        assert s.fresh == [(0, "qkv")]
+        prev = None
+        for l in range(2):
+            for name, N, K in layer:
+                x = s.input_for(l, name)
+                assert tuple(x.shape) == (M, K)
+                if prev is not None:
+                    assert x.data_ptr() == s.y[prev].data_ptr()
+                prev = (l, name)
+        assert s.x[("head",)].data_ptr() == s.y[(1, "down")].data_ptr()
+        plain = st.DecodeStack(layer, 2, ("lm_head", 40, 64), M=M, device="cpu")
+        assert s.bytes_per_step() == plain.bytes_per_step()
+        assert len(plain.fresh) == 2 * 3 + 1                       # qkv, o, gate_up per layer + head
