@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
 {
     extern __shared__ __align__(16) uint8_t xs[];
     __shared__ double s_freq[kMaxRopeHalf];
+    __shared__ int s_pos[MT], s_slot[MT];
     const int half = a.D >> 1;
     for (int i = threadIdx.x; i < half; i += kThreads) s_freq[i] = pow(a.base, -2.0 * double(i) / double(a.D));
     const int u0 = blockIdx.x * a.units_per_cta;
@@ -378,6 +379,10 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
     }
     griddep_wait();
     stage_rows(xs, a.x, a.M, MT, a.K);
+    if (threadIdx.x < MT) {                     // positions and slots of the block's tokens, read once
+        s_pos[threadIdx.x] = threadIdx.x < a.M ? a.pos[threadIdx.x] : 0;
+        s_slot[threadIdx.x] = threadIdx.x < a.M ? a.slot[threadIdx.x] : -1;
+    }
     __syncthreads();
     griddep_launch_dependents();
 
@@ -403,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
             float oa = part[0][m], ob = part[1][m];
             if (rot) {
                 const double kTwoPiHi = 6.283185307179586, kTwoPiLo = 2.4492935982947064e-16;
-                const double th = double(a.pos[m]) * inv_freq;
+                const double th = double(s_pos[m]) * inv_freq;
                 const double k = rint(th * (1.0 / kTwoPiHi));
                 const float r = float(fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, th)));
                 float sn, cs;
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
             if (hb < a.H) {
                 dst = a.q_out + size_t(m) * a.H * a.D + size_t(hb) * a.D;
             } else {
-                const int sl = a.slot[m];
+                const int sl = s_slot[m];
                 if (sl < 0 || sl >= a.n_slots) {
                     if (a.dev_status) atomicOr(reinterpret_cast<unsigned *>(a.dev_status), ZQ4_DEV_BAD_SLOT);
                     continue;
