@@ -55,7 +55,7 @@ typedef enum zq4_status {
     ZQ4_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
     ZQ4_ERR_FLAGS = -4,       /* unknown mode or flags */
     ZQ4_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
-    ZQ4_ERR_UNSUPPORTED = -6, /* valid arguments this build does not handle */
+    ZQ4_ERR_UNSUPPORTED = -6, /* valid arguments this library does not handle */
     ZQ4_ERR_OVERLAP = -7      /* input and output buffers overlap */
 } zq4_status;
 

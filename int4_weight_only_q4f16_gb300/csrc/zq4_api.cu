@@ -100,7 +100,7 @@ const char *zq4_status_string(int status)
     case ZQ4_ERR_ALIGN: return "ZQ4_ERR_ALIGN: a pointer is not 16-byte aligned";
     case ZQ4_ERR_FLAGS: return "ZQ4_ERR_FLAGS: unknown mode or flags";
     case ZQ4_ERR_CUDA: return "ZQ4_ERR_CUDA: a CUDA call or launch failed";
-    case ZQ4_ERR_UNSUPPORTED: return "ZQ4_ERR_UNSUPPORTED: not handled by this build";
+    case ZQ4_ERR_UNSUPPORTED: return "ZQ4_ERR_UNSUPPORTED: not handled by this library";
     case ZQ4_ERR_OVERLAP: return "ZQ4_ERR_OVERLAP: input and output buffers overlap";
     default: return "ZQ4: unknown status";
     }
