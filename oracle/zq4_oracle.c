@@ -421,7 +421,11 @@ void zo_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint1
         double drel = se / ((double)N * rms * rms);
         for (int64_t n = 0; n < N; ++n) {
             double g = zo_f16_to_f64(gamma[n]);
+#if ZO_MUTANT == 12
+            out[m * N + n] = r[m * N + n] / rms;         /* mutant: gamma dropped */
+#else
             out[m * N + n] = r[m * N + n] / rms * g;
+#endif
             Tn[m * N + n] = fabs(g) / rms * (e[n] + fabs(r[m * N + n]) * drel);
         }
     }
@@ -448,7 +452,12 @@ void zo_qkv_rope(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, 
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t hb = 0; hb < H + 2 * Hkv; ++hb) {
             for (int64_t i = 0; i < half; ++i) {
-                int64_t ra = hb * D + i, rb = ra + half;
+#if ZO_MUTANT == 11
+                int64_t ia = 2 * i, ib = 2 * i + 1;   /* mutant: adjacent pairs */
+#else
+                int64_t ia = i, ib = i + half;
+#endif
+                int64_t ra = hb * D + ia, rb = hb * D + ib;
                 double a = y[m * N + ra], b = y[m * N + rb];
                 double sa = S[m * N + ra], sb = S[m * N + rb];
                 if (hb < H + Hkv) {
@@ -463,18 +472,18 @@ void zo_qkv_rope(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, 
                     double *so = hb < H ? Sq + m * H * D : Sk + m * Hkv * D;
                     double *ao = hb < H ? Aq + m * H * D : Ak + m * Hkv * D;
                     int64_t h = hb < H ? hb : hb - H;
-                    o[h * D + i] = oa;
-                    o[h * D + i + half] = ob;
-                    so[h * D + i] = so[h * D + i + half] = sa + sb;
-                    ao[h * D + i] = ao[h * D + i + half] = fabs(a) + fabs(b);
+                    o[h * D + ia] = oa;
+                    o[h * D + ib] = ob;
+                    so[h * D + ia] = so[h * D + ib] = sa + sb;
+                    ao[h * D + ia] = ao[h * D + ib] = fabs(a) + fabs(b);
                 } else {
                     int64_t h = hb - H - Hkv;
-                    vc[m * Hkv * D + h * D + i] = a;
-                    vc[m * Hkv * D + h * D + i + half] = b;
-                    Sv[m * Hkv * D + h * D + i] = sa;
-                    Sv[m * Hkv * D + h * D + i + half] = sb;
-                    Av[m * Hkv * D + h * D + i] = fabs(a);
-                    Av[m * Hkv * D + h * D + i + half] = fabs(b);
+                    vc[m * Hkv * D + h * D + ia] = a;
+                    vc[m * Hkv * D + h * D + ib] = b;
+                    Sv[m * Hkv * D + h * D + ia] = sa;
+                    Sv[m * Hkv * D + h * D + ib] = sb;
+                    Av[m * Hkv * D + h * D + ia] = fabs(a);
+                    Av[m * Hkv * D + h * D + ib] = fabs(b);
                 }
             }
         }

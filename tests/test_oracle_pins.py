@@ -649,6 +649,42 @@ def test_qkv_rope_rotations_compose_and_keep_norms(oracle):
                 assert abs(got[1] - want[1]) <= 1e-11 * math.hypot(a0, b0) + 1e-300
 
 
+def _rope_pairs_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "rope_pairs.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
+def test_qkv_rope_pairs_golden(oracle):
+    """One nonzero projection output at a time (every code 7 but one 8, x
+    one-hot): after the rotation at position 1 exactly that dimension and its
+    partner from the golden table are nonzero in a Q or K head, and a V head
+    keeps the one value where it was."""
+    rows = _rope_pairs_golden()
+    D = rows[0][0]
+    H, Hkv, K = 1, 1, 32
+    N = (H + 2 * Hkv) * D
+    sc = np.full((N, K // 32), 0.5, np.float16)
+    x = np.zeros((1, K), np.float16)
+    x[0, 0] = 1.0
+    for d, dim, partner in rows:
+        assert d == D
+        for hb in range(H + 2 * Hkv):
+            wq = np.full((N, K // 8), 0x77777777, np.uint32)
+            wq[hb * D + dim, 0] = 0x77777778              # element 0: code 8, weight +0.5
+            o = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, 10000.0, [1])
+            out = o["q"] if hb < H else (o["k"] if hb < H + Hkv else o["v"])
+            h = hb if hb < H else (hb - H if hb < H + Hkv else hb - H - Hkv)
+            head = out[0, h * D:(h + 1) * D]
+            nz = set(np.flatnonzero(head).tolist())
+            assert nz == ({dim, partner} if hb < H + Hkv else {dim}), (hb, dim, sorted(nz))
+            assert np.count_nonzero(out) == len(nz)       # nothing outside this head
+            assert abs(math.hypot(head[dim], head[partner]) - 0.5) <= 1e-15
+
+
 # --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
@@ -667,12 +703,13 @@ def _pins_pass(o) -> bool:
         test_add_rmsnorm_zero_weights_closed_form(o)
         test_add_rmsnorm_brute_force(o)
         test_qkv_rope_rotation_closed_form(o)
+        test_qkv_rope_pairs_golden(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
+@pytest.mark.parametrize("mutant", list(range(1, 13)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
