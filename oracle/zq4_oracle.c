@@ -550,14 +550,22 @@ int64_t zo_moe_down_combine(const uint32_t *wq_bank, const uint16_t *sc_bank, in
                     int64_t e = ids[t * top_k + j];
                     if (e < 0 || e >= E) continue;
                     zo_dequant_row(wq_bank + e * N * (K / 8), sc_bank + e * N * (K / 32), K, n, w);
+#if ZO_MUTANT == 14
+                    const uint16_t *hv = h + t * K;           /* mutant: slot's h row ignored */
+#else
                     const uint16_t *hv = h + (t * top_k + j) * K;
+#endif
                     double z = 0.0, sz = 0.0;
                     for (int64_t k = 0; k < K; ++k) {
                         double p = zo_f16_to_f64(hv[k]) * w[k];
                         z += p;
                         sz += fabs(p);
                     }
+#if ZO_MUTANT == 13
+                    double rj = 1.0;                          /* mutant: router weight dropped */
+#else
                     double rj = (double)r[t * top_k + j];
+#endif
                     acc += rj * z;
                     sabs += fabs(rj) * sz;
                 }

@@ -704,12 +704,15 @@ def _pins_pass(o) -> bool:
         test_add_rmsnorm_brute_force(o)
         test_qkv_rope_rotation_closed_form(o)
         test_qkv_rope_pairs_golden(o)
+        test_moe_single_slot_is_plain_gemv(o)
+        test_moe_combine_weighted_sum_and_slot_permutation(o)
+        test_moe_invalid_ids_contribute_nothing(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", list(range(1, 13)))
+@pytest.mark.parametrize("mutant", list(range(1, 15)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
