@@ -426,7 +426,11 @@ void zo_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint1
 #else
             out[m * N + n] = r[m * N + n] / rms * g;
 #endif
+#if ZO_MUTANT == 15
+            Tn[m * N + n] = fabs(g) / rms * e[n];        /* mutant: the norm's cross term dropped */
+#else
             Tn[m * N + n] = fabs(g) / rms * (e[n] + fabs(r[m * N + n]) * drel);
+#endif
         }
     }
 }

@@ -585,6 +585,44 @@ def test_add_rmsnorm_brute_force(oracle):
             assert abs(out[m, n] - want) <= 1e-12 * (abs(want) + 1e-300)
 
 
+def test_add_rmsnorm_bound_is_the_first_order_propagation(oracle):
+    """T_n bounds how far out[n] moves when every r_j moves by at most its
+    GEMV bar e_j (to first order), and the worst sign pattern reaches it up to
+    the triangle inequality's slack on the r_n term: a dropped or doubled
+    term in T_n fails one of the two."""
+    rng = np.random.default_rng(45)
+    M, N, K = 2, 24, 64
+    wq, sc = synth.packed_codes(rng, N, K), synth.group_scales(rng, N, K)
+    x, res = synth.activations(rng, M, K), synth.activations(rng, M, N)
+    gam = (rng.random(N) * 2 - 0.5).astype(np.float16)
+    eps = 0.05
+    r, out, S, Tn = oracle.gemv_add_rmsnorm(wq, sc, x, res, gam, eps, N, K)
+    g = gam.astype(np.float64)
+    t = 1e-6                                           # a small step keeps second-order terms tiny
+
+    def norm(v):
+        return v / math.sqrt(math.fsum(v * v) / N + eps) * g
+
+    for m in range(M):
+        e = np.ldexp(np.abs(r[m]), -10) + 1e-4 * S[m] + np.ldexp(1.0, -25)
+        rms = math.sqrt(math.fsum(r[m] * r[m]) / N + eps)
+        assert np.allclose(norm(r[m]), out[m], rtol=1e-13, atol=0)
+        for n in range(N):
+            # the sign pattern that moves out[n] the most: d out_n / d r_n has
+            # the sign of gamma_n, d out_n / d r_j (j != n) that of
+            # -gamma_n r_n r_j; T_n exceeds that pattern's move only by the
+            # triangle inequality on the r_n term (2 r_n^2 e_n / (N rms^2))
+            d = -np.sign(r[m]) * np.sign(r[m, n]) * e
+            d[n] = e[n]
+            worst = abs(norm(r[m] + t * d)[n] - out[m, n]) / t
+            assert worst <= Tn[m, n] * (1 + 1e-6)
+            slack = 2 * abs(g[n]) / rms * r[m, n] ** 2 * e[n] / (N * rms * rms)
+            assert abs(worst - (Tn[m, n] - slack)) <= 1e-4 * Tn[m, n]
+            for _ in range(4):
+                dr = (rng.random(N) * 2 - 1) * e
+                assert abs(norm(r[m] + t * dr)[n] - out[m, n]) / t <= Tn[m, n] * (1 + 1e-6)
+
+
 # --------------------------------------------------------------------------
 # QKV projection + RoPE over (i, i + D/2) pairs + the token's K / V rows
 # --------------------------------------------------------------------------
@@ -702,6 +740,7 @@ def _pins_pass(o) -> bool:
         test_affine_brute_force_exact_rationals(o)
         test_add_rmsnorm_zero_weights_closed_form(o)
         test_add_rmsnorm_brute_force(o)
+        test_add_rmsnorm_bound_is_the_first_order_propagation(o)
         test_qkv_rope_rotation_closed_form(o)
         test_qkv_rope_pairs_golden(o)
         test_moe_single_slot_is_plain_gemv(o)
@@ -712,7 +751,7 @@ def _pins_pass(o) -> bool:
     return True
 
 
-@pytest.mark.parametrize("mutant", list(range(1, 15)))
+@pytest.mark.parametrize("mutant", list(range(1, 16)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
