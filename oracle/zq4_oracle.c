@@ -312,7 +312,11 @@ void zo_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t 
                 int64_t o = m * I + j;
                 double a = zo_silu(g);
                 h[o] = a * u;
+#if ZO_MUTANT == 16
+                if (Sh) Sh[o] = fabs(zo_silu_deriv(g)) * sg + fabs(a) * su;   /* mutant: u dropped */
+#else
                 if (Sh) Sh[o] = fabs(zo_silu_deriv(g) * u) * sg + fabs(a) * su;
+#endif
                 if (g_out) g_out[o] = g;
                 if (u_out) u_out[o] = u;
                 if (Sg_out) Sg_out[o] = sg;

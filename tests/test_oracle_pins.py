@@ -251,6 +251,40 @@ def test_gate_up_equals_two_gemvs(oracle):
     assert np.array_equal(hc, h) and np.array_equal(Shc, Sh)
 
 
+def test_gate_up_bar_is_the_first_order_propagation(oracle):
+    """S_h is the first-order sensitivity of h = silu(g) u to moves of g and
+    u within their scales S_g and S_u: the worst of the four sign patterns
+    reaches it, random moves inside never exceed it (SiLU itself is pinned
+    above)."""
+    rng = np.random.default_rng(13)
+    I, K, M = 16, 64, 2
+    wq, sc = synth.packed_codes(rng, 2 * I, K), synth.group_scales(rng, 2 * I, K)
+    x = synth.activations(rng, M, K)
+    h, Sh, g, u, Sg, Su = oracle.gate_up_silu(wq, sc, x, 2 * I, K, True, parts=True)
+    t = 1e-7
+    for m in range(M):
+        for j in range(I):
+            def moved(a, b):
+                return oracle.silu(g[m, j] + t * a * Sg[m, j]) * (u[m, j] + t * b * Su[m, j])
+            worst = max(abs(moved(a, b) - h[m, j]) for a in (-1, 1) for b in (-1, 1)) / t
+            assert abs(worst - Sh[m, j]) <= 1e-5 * Sh[m, j]
+            for _ in range(3):
+                a, b = rng.random(2) * 2 - 1
+                assert abs(moved(a, b) - h[m, j]) / t <= Sh[m, j] * (1 + 1e-5)
+    # the affine form carries the same propagation of its own scales
+    wa, sa, ba = synth.packed_codes(rng, 2 * I, K), synth.group_scales(rng, 2 * I, K), \
+        synth.group_scales(rng, 2 * I, K)
+    sa, ba = sa[:, : K // 64], ba[:, : K // 64]
+    ha, Sha = oracle.gate_up_silu_affine(wa, sa, ba, x, 2 * I, K)
+    ya, Sa = oracle.gemv_affine(wa, sa, ba, x, 2 * I, K)
+    for m in range(M):
+        for j in range(I):
+            ga, ua, sga, sua = ya[m, 2 * j], ya[m, 2 * j + 1], Sa[m, 2 * j], Sa[m, 2 * j + 1]
+            worst = max(abs(oracle.silu(ga + t * a * sga) * (ua + t * b * sua) - ha[m, j])
+                        for a in (-1, 1) for b in (-1, 1)) / t
+            assert abs(worst - Sha[m, j]) <= 1e-5 * Sha[m, j]
+
+
 def test_gate_up_brute_force(oracle):
     """gate_up on one row pair in exact rationals (SiLU through math.exp)."""
     rng = np.random.default_rng(12)
@@ -734,6 +768,7 @@ def _pins_pass(o) -> bool:
         test_closed_form_constant_codes(o)
         test_silu_values(o)
         test_gate_up_brute_force(o)
+        test_gate_up_bar_is_the_first_order_propagation(o)
         test_argmax_hand_cases(o)
         test_affine_one_hot_columns_exact(o)
         test_affine_closed_form_constant_codes(o)
@@ -751,7 +786,7 @@ def _pins_pass(o) -> bool:
     return True
 
 
-@pytest.mark.parametrize("mutant", list(range(1, 16)))
+@pytest.mark.parametrize("mutant", list(range(1, 17)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
