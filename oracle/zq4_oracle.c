@@ -482,7 +482,11 @@ void zo_qkv_rope(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, 
                     int64_t h = hb < H ? hb : hb - H;
                     o[h * D + ia] = oa;
                     o[h * D + ib] = ob;
+#if ZO_MUTANT == 17
+                    so[h * D + ia] = so[h * D + ib] = sa;        /* mutant: the partner's scale dropped */
+#else
                     so[h * D + ia] = so[h * D + ib] = sa + sb;
+#endif
                     ao[h * D + ia] = ao[h * D + ib] = fabs(a) + fabs(b);
                 } else {
                     int64_t h = hb - H - Hkv;

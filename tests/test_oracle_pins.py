@@ -757,6 +757,33 @@ def test_qkv_rope_pairs_golden(oracle):
             assert abs(math.hypot(head[dim], head[partner]) - 0.5) <= 1e-15
 
 
+def test_qkv_rope_bar_covers_the_pair(oracle):
+    """The bar of a rotated output, 2^-10 A + 1e-4 S over its pair, covers
+    the worst move of the rotation when a and b move within their own GEMV
+    bars (|cos| e_a + |sin| e_b); a V output keeps its row's GEMV bar."""
+    H, Hkv, D, K = 2, 1, 16, 64
+    rng, wq, sc, x = _qkv_case(54, H, Hkv, D, K, M=3)
+    pos, base = [0, 5, 900], 10000.0
+    o = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, pos)
+    y, S = oracle.gemv(wq, sc, x, (H + 2 * Hkv) * D, K)
+    e = np.ldexp(np.abs(y), -10) + 1e-4 * S
+    half = D // 2
+    for m in range(3):
+        for hb in range(H + Hkv):
+            name, h = ("q", hb) if hb < H else ("k", hb - H)
+            for i in range(half):
+                ra, rb = hb * D + i, hb * D + i + half
+                th = pos[m] * math.pow(base, -2.0 * i / D)
+                move = abs(math.cos(th)) * e[m, ra] + abs(math.sin(th)) * e[m, rb]
+                for c in (h * D + i, h * D + i + half):
+                    bar = math.ldexp(o["A_" + name][m, c], -10) + 1e-4 * o["S_" + name][m, c]
+                    assert move <= bar * (1 + 1e-12)
+                    assert bar <= (e[m, ra] + e[m, rb]) * (1 + 1e-12)
+        v0 = (H + Hkv) * D
+        bar_v = np.ldexp(o["A_v"][m], -10) + 1e-4 * o["S_v"][m]
+        assert np.allclose(bar_v, e[m, v0:], rtol=1e-14, atol=0)
+
+
 # --------------------------------------------------------------------------
 # the pins must be able to fail: mutants planted in the oracle (CPU only)
 # --------------------------------------------------------------------------
@@ -778,6 +805,7 @@ def _pins_pass(o) -> bool:
         test_add_rmsnorm_bound_is_the_first_order_propagation(o)
         test_qkv_rope_rotation_closed_form(o)
         test_qkv_rope_pairs_golden(o)
+        test_qkv_rope_bar_covers_the_pair(o)
         test_moe_single_slot_is_plain_gemv(o)
         test_moe_combine_weighted_sum_and_slot_permutation(o)
         test_moe_invalid_ids_contribute_nothing(o)
@@ -786,7 +814,7 @@ def _pins_pass(o) -> bool:
     return True
 
 
-@pytest.mark.parametrize("mutant", list(range(1, 17)))
+@pytest.mark.parametrize("mutant", list(range(1, 18)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
