@@ -278,7 +278,7 @@ double zo_silu_deriv(double z)
 }
 
 /* Row of gate j and of up j under the two layouts of a 2*I-row matrix. */
-static int64_t zo_gate_row(int64_t j, int64_t I, int interleaved) { return interleaved ? 2 * j : j; }
+static int64_t zo_gate_row(int64_t j, int interleaved) { return interleaved ? 2 * j : j; }
 static int64_t zo_up_row(int64_t j, int64_t I, int interleaved) { return interleaved ? 2 * j + 1 : I + j; }
 
 /* ---------------------------------------------------------------------- */
@@ -300,7 +300,7 @@ void zo_gate_up_silu(const uint32_t *wq, const uint16_t *scales, const uint16_t 
         double *wu = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
         #pragma omp for schedule(dynamic, 16)
         for (int64_t j = 0; j < I; ++j) {
-            zo_dequant_row(wq, scales, K, zo_gate_row(j, I, interleaved), wg);
+            zo_dequant_row(wq, scales, K, zo_gate_row(j, interleaved), wg);
             zo_dequant_row(wq, scales, K, zo_up_row(j, I, interleaved), wu);
             for (int64_t m = 0; m < M; ++m) {
                 double g = 0, u = 0, sg = 0, su = 0;
