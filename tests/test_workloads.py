@@ -83,3 +83,34 @@ def test_chained_stack_wiring_and_bytes():
         plain = st.DecodeStack(layer, 2, ("lm_head", 40, 64), M=M, device="cpu")
         assert s.bytes_per_step() == plain.bytes_per_step()
         assert len(plain.fresh) == 2 * 3 + 1                       # qkv, o, gate_up per layer + head
+
+
+def test_generator_distributions():
+    """The input recipe: every nibble a uniform code 0..15, scales
+    |N(0, 0.02)| (mean 0.02 sqrt(2/pi)), activations N(0, 1)."""
+    rng = synth.rng_for("dist", 0)
+    wq = synth.packed_codes(rng, 256, 256)
+    for i in range(8):
+        counts = np.bincount(((wq >> (4 * i)) & 0xF).ravel(), minlength=16)
+        assert counts.size == 16 and np.all(np.abs(counts / counts.mean() - 1) < 0.15), (i, counts)
+    sc = synth.group_scales(rng, 4096, 256).astype(np.float64)
+    assert abs(sc.mean() / (0.02 * np.sqrt(2 / np.pi)) - 1) < 0.02
+    x = synth.activations(rng, 64, 4096).astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1) < 0.01
+
+
+def test_unit_gain_scales_keep_the_activation_size():
+    """Signed scales N(0, unit_gain_sigma(K)) keep the root mean square of a
+    projection's output near that of its N(0, 1) input (E[(q - 7)^2] = 21.5
+    for uniform codes), and the gate_up sigma does the same for silu(g) u."""
+    import oracle
+    o = oracle.get()
+    K, N = 3072, 512
+    x = synth.activations(synth.rng_for("ug_x"), 4, K)
+    assert np.mean([(q - 7) ** 2 for q in range(16)]) == 21.5
+    wq, sc = synth.weight("ug", N, K, 0, sigma=synth.unit_gain_sigma(K), signed=True)
+    y, _ = o.gemv(wq, sc, x, N, K)
+    assert abs(np.sqrt(np.mean(y * y)) - 1) < 0.1
+    wq, sc = synth.weight("ug_gu", 2 * N, K, 0, sigma=synth.unit_gain_sigma(K, gate_up=True), signed=True)
+    h, _ = o.gate_up_silu(wq, sc, x, 2 * N, K)
+    assert abs(np.sqrt(np.mean(h * h)) - 1) < 0.15
