@@ -157,3 +157,50 @@ def test_qkv_rope_host_checks(lib):
     assert f(*args) == lib.ZQ4_ERR_ALIGN
     args = list(ok); args[13] = P(Kc)
     assert f(*args) == lib.ZQ4_ERR_OVERLAP        # k and v caches the same
+
+
+def test_header_is_plain_c_and_a_c_program_links(lib):
+    """include/zq4.h compiles as strict C99 (no C++ in the boundary), every
+    declared entry point resolves when a C program links libzq4.so, and the
+    host checks answer a C caller (a NULL matrix: ZQ4_ERR_NULL, no launch)."""
+    import shutil
+    import subprocess
+    from int4_weight_only_q4f16_gb300 import build
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    syms = declared_symbols()
+    out_dir = os.path.join(build.BUILD, "c_abi_check")
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "c_abi_check.c")
+    exe = os.path.join(out_dir, "c_abi_check")
+    table = ",\n".join(f"    (zq4_fn){s}" for s in syms)
+    with open(src, "w") as f:
+        f.write(f"""#include <stdio.h>
+#include "zq4.h"
+
+typedef void (*zq4_fn)(void);
+static zq4_fn const every_entry[] = {{
+{table}
+}};
+
+int main(void)
+{{
+    size_t i, n = sizeof every_entry / sizeof every_entry[0];
+    int bad = 0;
+    for (i = 0; i < n; ++i)
+        if (!every_entry[i]) ++bad;
+    if (zq4_version() <= 0) ++bad;
+    if (zq4_gemv(NULL, NULL, NULL, NULL, 1, 64, 64, NULL) != ZQ4_ERR_NULL) ++bad;
+    if (!zq4_status_string(ZQ4_ERR_SHAPE)) ++bad;
+    printf("%lu %d\\n", (unsigned long)n, bad);
+    return bad;
+}}
+""")
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           src, "-o", exe, "-L", build.BUILD, "-lzq4", f"-Wl,-rpath,{build.BUILD}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.split() == [str(len(syms)), "0"]
