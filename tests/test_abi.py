@@ -204,3 +204,24 @@ int main(void)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.split() == [str(len(syms)), "0"]
+
+
+def test_binding_fails_loudly_without_the_library():
+    """No CPU fallback: with libzq4.so absent, importing the binding (and the
+    decode-stack driver that uses it) raises ImportError."""
+    import subprocess
+    import sys
+    code = (
+        "import os\n"
+        "import int4_weight_only_q4f16_gb300.build as b\n"
+        "b.LIB = os.path.join(b.BUILD, 'absent', 'libzq4.so')\n"
+        "for mod in ('zq4', 'stack'):\n"
+        "    try:\n"
+        "        __import__('int4_weight_only_q4f16_gb300.' + mod)\n"
+        "    except ImportError as e:\n"
+        "        print(mod, 'ImportError', 'not built' in str(e))\n"
+        "    else:\n"
+        "        print(mod, 'loaded')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.split("\n")[:2] == ["zq4 ImportError True", "stack ImportError True"], r.stdout
