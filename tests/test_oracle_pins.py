@@ -757,6 +757,29 @@ def test_qkv_rope_pairs_golden(oracle):
             assert abs(math.hypot(head[dim], head[partner]) - 0.5) <= 1e-15
 
 
+def test_qkv_rope_frequency_schedule(oracle):
+    """The angle of each pair, read back from the output of a single nonzero
+    projection value (atan2 of the pair): pair 0 turns by exactly pos
+    radians, and each next pair turns base^(2/D) times slower (a geometric
+    schedule), at position 1 where no angle wraps."""
+    H, Hkv, D, K = 1, 1, 16, 32
+    N, half, base = (H + 2 * Hkv) * D, D // 2, 500.0
+    sc = np.full((N, 1), 0.5, np.float16)
+    x = np.zeros((1, K), np.float16)
+    x[0, 0] = 1.0
+    for pos in (1, 2):
+        angles = []
+        for i in range(half):
+            wq = np.full((N, K // 8), 0x77777777, np.uint32)
+            wq[i, 0] = 0x77777778                          # q row i: value +0.5
+            q = oracle.qkv_rope(wq, sc, x, K, H, Hkv, D, base, [pos])["q"][0]
+            angles.append(math.atan2(q[i + half], q[i]))
+        assert abs(angles[0] - pos) <= 1e-15 * pos
+        if pos == 1:
+            for i in range(half - 1):
+                assert abs(angles[i] / angles[i + 1] - base ** (2.0 / D)) <= 1e-12
+
+
 def test_qkv_rope_bar_covers_the_pair(oracle):
     """The bar of a rotated output, 2^-10 A + 1e-4 S over its pair, covers
     the worst move of the rotation when a and b move within their own GEMV
@@ -806,6 +829,7 @@ def _pins_pass(o) -> bool:
         test_qkv_rope_rotation_closed_form(o)
         test_qkv_rope_pairs_golden(o)
         test_qkv_rope_bar_covers_the_pair(o)
+        test_qkv_rope_frequency_schedule(o)
         test_moe_single_slot_is_plain_gemv(o)
         test_moe_combine_weighted_sum_and_slot_permutation(o)
         test_moe_invalid_ids_contribute_nothing(o)
