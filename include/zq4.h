@@ -31,6 +31,13 @@
  *     kernel may start while the previous kernel of the stream finishes and
  *     read its WEIGHTS early, but it reads its activation input and writes
  *     its output only after that previous kernel has completed.
+ *   - Threads: any entry point may be called from several host threads at
+ *     once (the library's host-side caches are atomic and the last CUDA
+ *     error is kept per thread). What is shared: the device error words
+ *     (one set per process and device; zq4_device_errors with clear != 0
+ *     clears them for every caller), the one static stack plan per device
+ *     (zq4_stack_plan_init_static), and any caller scratch (work buffers,
+ *     plans), which concurrent calls on different streams must not share.
  */
 #ifndef ZQ4_H
 #define ZQ4_H
@@ -217,7 +224,8 @@ ZQ4_API zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scale
  * [M, N] f16, gamma [N] f16; eps >= 0 (finite). work: caller-owned device
  * scratch of zq4_add_rmsnorm_work_bytes(M, N) bytes, 16-byte aligned, whose
  * first 16 bytes must be zero before the first call; every call leaves them
- * zero (the rest is overwritten). One launch per block of up to 8 tokens;
+ * zero (the rest is overwritten); calls sharing one work buffer must be
+ * ordered on one stream. One launch per block of up to 8 tokens;
  * the last CTA of each normalises all N outputs (fixed reduction order, no
  * floating-point atomics: repeated calls give identical bits). Outputs and
  * work must not overlap each other or any input. Errors: ZQ4_ERR_NULL,
