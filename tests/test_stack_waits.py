@@ -118,8 +118,7 @@ def test_reads_of_the_same_buffer_do_not_order(zq4):
     assert zq4.stack_plan_waits(jobs, 4) == ([0, 1, 2], [-1] * 3)
 
 
-@pytest.mark.parametrize("seed", range(6))
-def test_random_job_lists_keep_conflicting_jobs_in_order(zq4, seed):
+def _random_jobs(seed):
     rng = np.random.default_rng(seed)
     M = int(rng.integers(1, 5))
     jobs = []
@@ -138,8 +137,34 @@ def test_random_job_lists_keep_conflicting_jobs_in_order(zq4, seed):
         else:
             xb_addr = buf(xb, xo)
         jobs.append((W, xb_addr, buf(yb), N, K, gu))
+    return jobs, M
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_job_lists_keep_conflicting_jobs_in_order(zq4, seed):
+    jobs, M = _random_jobs(seed)
     order, dep = zq4.stack_plan_waits(jobs, M)
     check_valid(jobs, M, order, dep)
+
+
+def test_concurrent_calls_from_host_threads_agree_with_sequential_ones(zq4):
+    """The scheduler runs on the host in caller-owned scratch: calls from
+    several threads at once (ctypes releases the GIL) give what one thread
+    gets, and a rejected call on one thread leaves the others unaffected."""
+    from concurrent.futures import ThreadPoolExecutor
+    cases = [_random_jobs(seed) for seed in range(8)]
+    want = [zq4.stack_plan_waits(jobs, M) for jobs, M in cases]
+
+    def work(i):
+        jobs, M = cases[i % len(cases)]
+        if i % 5 == 4:
+            with pytest.raises(zq4.Zq4Error, match="ALIGN"):
+                zq4.stack_plan_waits([(W, buf(0, 8), buf(1), 256, 256, 0)], 1)
+        return i, zq4.stack_plan_waits(jobs, M)
+
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        for i, got in ex.map(work, range(200)):
+            assert got == want[i % len(cases)], i
 
 
 def test_waits_reject_bad_jobs(zq4):
