@@ -618,8 +618,13 @@ int64_t zo_moe_gate_up_affine(const uint32_t *wq_bank, const uint16_t *sc_bank, 
                 for (int64_t i = 0; i < I; ++i) ho[i] = so[i] = 0.0;
                 continue;
             }
+#if ZO_MUTANT == 18
+            zo_gate_up_silu_affine(wq_bank + e * N2 * (K / 8), sc_bank + e * N2 * (K / 64),
+                                   bi_bank, x + t * K, 1, N2, K, ho, so);  /* mutant: bias bank not offset */
+#else
             zo_gate_up_silu_affine(wq_bank + e * N2 * (K / 8), sc_bank + e * N2 * (K / 64),
                                    bi_bank + e * N2 * (K / 64), x + t * K, 1, N2, K, ho, so);
+#endif
         }
     return bad;
 }

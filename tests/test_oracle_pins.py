@@ -833,12 +833,14 @@ def _pins_pass(o) -> bool:
         test_moe_single_slot_is_plain_gemv(o)
         test_moe_combine_weighted_sum_and_slot_permutation(o)
         test_moe_invalid_ids_contribute_nothing(o)
+        test_affine_moe_single_slot_is_plain_gemv(o)
+        test_affine_moe_combine_weighted_sum_and_invalid_ids(o)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mutant", list(range(1, 18)))
+@pytest.mark.parametrize("mutant", list(range(1, 19)))
 def test_mutants_are_caught(mutant):
     o = oracle_mod.Oracle(mutant)
     assert o.lib.zo_mutant() == mutant
