@@ -70,6 +70,8 @@
  *
  * Mutants: building with -DZO_MUTANT=<n> plants one deliberate mistake so
  * that the tests can show their pins catch it. The normal build has none.
+ * Every mutant keeps each access inside its arrays (an index mistake wraps
+ * or stays within the row), so a mutant gives wrong numbers, never a crash.
  */
 #include <math.h>
 #include <stdint.h>
