@@ -114,3 +114,27 @@ def test_unit_gain_scales_keep_the_activation_size():
     wq, sc = synth.weight("ug_gu", 2 * N, K, 0, sigma=synth.unit_gain_sigma(K, gate_up=True), signed=True)
     h, _ = o.gate_up_silu(wq, sc, x, 2 * N, K)
     assert abs(np.sqrt(np.mean(h * h)) - 1) < 0.15
+
+
+def _definition_bytes(layer, layers, head, M):
+    """Per projection: codes N K/2, scales N K/16, x read M K 2, y written
+    M N_out 2 (N_out = N/2 for gate_up)."""
+    def one(name, N, K):
+        n_out = N // 2 if name == "gate_up" else N
+        return N * K // 2 + N * K // 16 + M * K * 2 + M * n_out * 2
+    return layers * sum(one(*p) for p in layer) + (one(*head) if head else 0)
+
+
+def test_stack_bytes_follow_the_definition():
+    """DecodeStack.bytes_per_step (the roofline numerator of the bench) is
+    the algorithmic byte count, and the Phi-3 step at M = 1 moves
+    2,096,530,048 bytes (2,093,838,336 of them packed weights)."""
+    from int4_weight_only_q4f16_gb300 import stack as st
+    layer = (("qkv", 96, 64), ("o", 32, 64), ("gate_up", 128, 32), ("down", 64, 64))
+    head = ("lm_head", 40, 64)
+    for M in (1, 4):
+        s = st.DecodeStack(layer, 3, head, M=M, device="cpu")
+        assert s.bytes_per_step() == _definition_bytes(layer, 3, head, M)
+    phi3 = _definition_bytes(synth.PHI3_LAYER, synth.PHI3_LAYERS, synth.PHI3_LM_HEAD, 1)
+    assert phi3 == 2_096_530_048
+    assert _definition_bytes(synth.PHI3_LAYER, synth.PHI3_LAYERS, synth.PHI3_LM_HEAD, 0) == 2_093_838_336
