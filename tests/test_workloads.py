@@ -138,3 +138,5 @@ def test_stack_bytes_follow_the_definition():
     phi3 = _definition_bytes(synth.PHI3_LAYER, synth.PHI3_LAYERS, synth.PHI3_LM_HEAD, 1)
     assert phi3 == 2_096_530_048
     assert _definition_bytes(synth.PHI3_LAYER, synth.PHI3_LAYERS, synth.PHI3_LM_HEAD, 0) == 2_093_838_336
+    gate_up = [p for p in synth.PHI3_LAYER if p[0] == "gate_up"]
+    assert _definition_bytes(gate_up, 1, None, 1) == 28_334_080      # the per-call roofline's launch
