@@ -35,6 +35,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "W4A16 dequant-GEMV achieved HBM GB/s (% of peak); Phi-3-shape decode tok/s"
 L2_BYTES = 126 * 1024 * 1024
+# the arithmetic of the GPU path: 4-bit weights dequantized exactly to f16,
+# f16 activations, f16 x f16 products accumulated in fp32, f16 outputs
+DTYPE = "w4a16: f16*f16 products, fp32 accumulate"
 
 
 def parse_args():
@@ -44,7 +47,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="zq4", choices=["zq4", "reference"])
     ap.add_argument("--workload", default="phi3",
-                    choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill", "lmhead"])
+                    choices=["phi3", "gemv3072", "qwen3", "moe", "kernel", "prefill", "lmhead", "oracle-table"])
     ap.add_argument("--stack-mode", default="plan", choices=["calls", "seg", "plan"],
                     help="phi3/qwen3: one launch per projection, or the whole step as one launch")
     ap.add_argument("--n", type=int, default=16384, help="rows of W (kernel workload)")
@@ -192,6 +195,7 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "gate_up_phi3_M1": ("zq4_decode_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
     "stack_phi3_M1": ("zq4_stack.cu", "zq4_segment.cuh", "zq4_async.cuh", "zq4_common.cuh"),
+    "step_phi3_M1": ("zq4_step.cu", "zq4_step.h", "zq4_segment.cuh", "zq4_async.cuh", "zq4_common.cuh"),
     "prefill_gate_up_M1024": ("zq4_prefill_tc.cu", "zq4_async.cuh", "zq4_common.cuh"),
 }
 
@@ -337,13 +341,16 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
     tok_s = dist.world * st.M / step_s
 
     if args.stack_mode == "plan":
-        # the whole step is one launch of k_stack: it is the dominant kernel
+        # the whole step is one launch of the step kernel: it is the dominant kernel
         achieved = bytes_step / step_s / 1e9
-        roofline = {"bound": "hbm", "kernel": "k_stack (whole decode step, one cooperative launch)",
+        kname, ktag = (("k_step<1> (whole decode step, one cooperative launch)", "step_phi3_M1")
+                       if st.plan.plan.engine == 1 else
+                       ("k_stack (whole decode step, one cooperative launch)", "stack_phi3_M1"))
+        roofline = {"bound": "hbm", "kernel": kname,
                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                    "traffic": profiled_traffic("stack_phi3_M1") if args.layers == 32 else None,
+                    "traffic": profiled_traffic(ktag) if args.layers == 32 else None,
                     "bytes_per_launch": bytes_step, "avg_launch_us": round(step_s * 1e6, 3),
                     "launches_timed": args.steps}
     else:
@@ -386,7 +393,7 @@ def run_phi3(args, torch, dist, peaks, peak_kind):
         "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
         "hbm_gbs": round(bytes_step / step_s / 1e9, 1),
         "hbm_frac_of_measured": round(bytes_step / step_s / 1e9 / peaks["hbm_gbs"], 4),
         "hbm_frac_of_8tbs": round(bytes_step / step_s / 8e12, 4),
@@ -834,9 +841,86 @@ def run_reference(args, dist):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_oracle_table(args):
+    """The fp64 oracle timed on every workload, on one host thread and on all
+    of them (a reported baseline; host CPU only, no GPU). Each cell runs a
+    bounded sample and is scaled by weight bytes (GEMV stacks) or flops
+    (prefill) to the workload's unit."""
+    import oracle
+    from int4_weight_only_q4f16_gb300 import synth
+    o = oracle.get()
+    all_threads = o.num_threads()
+    budget = max(0.5, args.cpu_seconds / 10)
+
+    def timed(fn, min_s):
+        n, t = 0, 0.0
+        while t < min_s or n == 0:
+            t0 = time.perf_counter()
+            fn()
+            t += time.perf_counter() - t0
+            n += 1
+        return t / n
+
+    def qwen_projs(M):
+        return [(name, N, K, 0) for name, N, K in synth.QWEN3_4B_LAYER]
+
+    cells = []
+    for threads in (1, all_threads):
+        used = o.set_num_threads(threads)
+        # config 0: one 3072 x 3072 GEMV, M = 1
+        wq, sc = synth.weight("gemv3072", 3072, 3072, 0)
+        x = synth.activations(synth.rng_for("ot_x0"), 1, 3072)
+        t = timed(lambda: o.gemv(wq, sc, x, 3072, 3072), budget)
+        cells.append({"config": 0, "threads": used, "value": round(t * 1e6, 1), "unit": "us per call",
+                      "sample": "whole call"})
+        # config 1: the Phi-3 stack, M = 1 (rows of the projections in step order)
+        rate, _, desc = oracle_sample_rate(phi3_projs(), 2 * budget)
+        wb = sum(N * (K // 8 * 4 + K // 32 * 2) for _, N, K, _ in phi3_projs()[:4]) * synth.PHI3_LAYERS + \
+            synth.PHI3_LM_HEAD[1] * (synth.PHI3_LM_HEAD[2] // 8 * 4 + synth.PHI3_LM_HEAD[2] // 32 * 2)
+        cells.append({"config": 1, "threads": used, "value": round(wb / rate, 3), "unit": "s per token",
+                      "sample": desc + ", scaled by weight bytes"})
+        # config 2: the Qwen3-4B stack at M tokens (layer-0 rows, scaled to 36 layers)
+        qb = sum(N * (K // 8 * 4 + K // 32 * 2) for _, N, K in synth.QWEN3_4B_LAYER) * synth.QWEN3_4B_LAYERS
+        for M in (1, 2, 4, 8, 16):
+            rate, _, desc = oracle_sample_rate(qwen_projs(M), budget, M=M)
+            cells.append({"config": 2, "M": M, "threads": used, "value": round(qb / rate, 3),
+                          "unit": "s per step", "tok_s": round(M * rate / qb, 4),
+                          "sample": desc + ", scaled by weight bytes"})
+        # config 3: the MoE block (gate_up + SiLU*mul, down + combine), T tokens, bank 0
+        E, top_k = synth.MOE_EXPERTS, synth.MOE_TOP_K
+        (N2, D), (Dn, I) = synth.MOE_GATE_UP, synth.MOE_DOWN
+        gq, gs = synth.weight("moe_gu", E * N2, D, 0)
+        dq, ds = synth.weight("moe_dn", E * Dn, I, 0)
+        for T in (1, 4, 16):
+            rng = synth.rng_for("moe_route", 0, T)
+            ids, r = synth.routing(rng, T, E, top_k)
+            xm = synth.activations(rng, T, D)
+
+            def block():
+                h, _, _ = o.moe_gate_up(gq, gs, E, xm, N2, D, ids)
+                o.moe_down_combine(dq, ds, E, o.round_f16(h.ravel()).reshape(h.shape), r, Dn, I, ids)
+            t = timed(block, budget)
+            cells.append({"config": 3, "T": T, "threads": used, "value": round(t * 1e6, 1),
+                          "unit": "us per block", "sample": "whole block"})
+        # config 4: prefill GEMMs at M = 1024 (8 token rows, scaled by flops)
+        for N, K in ((16384, 3072), (3072, 8192)):
+            wq, sc = synth.weight("ot_prefill", N, K, 0)
+            xs = synth.activations(synth.rng_for("ot_xp", N), 8, K)
+            t = timed(lambda: o.gemv(wq, sc, xs, N, K), budget / 2) * (1024 / 8)
+            cells.append({"config": 4, "shape": f"1024x{N}x{K}", "threads": used, "value": round(t, 2),
+                          "unit": "s per call", "tflops": round(2 * 1024 * N * K / t / 1e12, 6),
+                          "sample": "8 of the 1024 token rows, scaled by flops"})
+    o.set_num_threads(all_threads)
+    return {"impl": "oracle", "metric": "fp64 oracle time per workload unit (host CPU)",
+            "cores": all_threads, "cells": cells}
+
+
 def main():
     args = parse_args()
     dist = Dist()
+    if args.workload == "oracle-table":
+        print(json.dumps(run_oracle_table(args)), flush=True)
+        return 0
     if args.impl == "reference":
         line = run_reference(args, dist)
         if line is not None:

@@ -318,8 +318,10 @@ ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_
 
 /*
  * zq4_prepare_weight -- rewrite a q4f16_1 matrix into the layout the kernels
- * take. The row order is the only thing that changes; each row's words and
- * scales are copied bit for bit, so dequantized values are identical.
+ * take. With ZQ4_PREP_COPY and ZQ4_PREP_CONCAT_TO_INTERLEAVED the row order
+ * is the only thing that changes (each row's words and scales are copied bit
+ * for bit); ZQ4_PREP_SEGMENTED also regroups the words and reorders the
+ * codes within them (below). Dequantized values are identical either way.
  * Source: "Zero-TVM benchmarks" (BENCH.md), section "Qwen3.5 hybrid perf
  * round" (q4f16_1 matrices are concatenated row-wise by concatenating their
  * bytes) and "Zero TVM Documentation", card 6 "Fused FFN" (the gate_up
@@ -331,12 +333,16 @@ ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_
  *
  * ZQ4_PREP_SEGMENTED (K % 256 == 0; scales_dst must be NULL) writes the
  * segmented layout into wq_dst (zq4_segmented_bytes(N, K) bytes): for each
- * 16-row tile t (tile-major) and 256-column block s, 2304 contiguous bytes:
- * first the 16 rows' 128-byte code runs (words 32s .. 32s+31 of row 16t+i),
- * the 16-byte chunk c of row i stored at byte i*128 + 16*(c XOR (i mod 8)),
- * then the 16 rows' scales 8s .. 8s+7 (16 bytes per row, at 2048 + 16*i).
- * Rows past N are zero. A pure byte permutation of the canonical matrix; the
- * layout zq4_stack_run streams with one contiguous copy per segment.
+ * 16-row tile t (tile-major) and 256-column block s, 2304 contiguous bytes,
+ * one 144-byte record per row i (row 16t+i) at byte 144*i: 32 code words,
+ * then the row's scales 8s .. 8s+7 (16 bytes, at 144*i + 128). Record word
+ * 8q + g (q = 0..3, g = 0..7) is word 32s + 4g + q of the row (word q of
+ * group g), with its nibbles reordered: nibble slot j of the stored word
+ * (bits 4j..4j+3) holds element (0, 2, 4, 6, 1, 3, 5, 7)[j] of the canonical
+ * word. Rows past N are zero. A bijection of the canonical matrix's codes
+ * and scales (same bytes count, every code and scale kept bit for bit); the
+ * layout the one-launch step and zq4_gemv_seg stream with one contiguous
+ * copy per segment.
  *
  * Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_FLAGS, ZQ4_ERR_ALIGN,
  * ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
@@ -409,6 +415,14 @@ ZQ4_API zq4_status zq4_gate_up_silu_seg(const uint32_t *wseg, const uint16_t *x,
  * (the second waiting for the first), others may run in another order or
  * at once. zq4_stack_plan_waits tells the order and the waits a plan uses.
  * The weights are only read.
+ *
+ * Two kernels run plans. For M = 1 or 2: every warp computes whole 16-row
+ * tiles, handed out one at a time across all jobs (no barrier between
+ * jobs), each job waiting for the earlier jobs it conflicts with (at most 3
+ * after dropping those implied by the others; a job list that needs more
+ * runs on the other kernel). For M = 3..8 (and the lists above): every CTA
+ * takes its share of each job in turn, a job waiting for the last earlier
+ * job it conflicts with. Both give the results of the given order.
  */
 typedef struct zq4_stack_job {
     const uint32_t *wq;
@@ -420,8 +434,11 @@ typedef struct zq4_stack_job {
     int gate_up;
 } zq4_stack_job;
 
-/* Filled by zq4_stack_plan_init; pass to zq4_stack_run. `dev` is the
- * caller's device buffer (job table with tensor maps, counters, scratch). */
+/* Filled by zq4_stack_plan_init (or _init_static); pass to zq4_stack_run.
+ * `dev` is the device buffer holding the plan (job table, counters);
+ * `device` the CUDA device the plan was made on (it runs only there). The
+ * fields after `device` are the library's own bookkeeping: leave them as
+ * the init call wrote them. */
 typedef struct zq4_stack_plan {
     void *dev;
     size_t bytes;
@@ -430,13 +447,18 @@ typedef struct zq4_stack_plan {
     int grid;
     int max_k;
     int max_tiles;
+    int device;
+    int engine;
+    int tiles;
+    int n_pub;
+    int gen;
 } zq4_stack_plan;
 
 /*
  * zq4_stack_plan_bytes -- device bytes a plan for these jobs needs on the
  * current device (1 <= M <= 8). Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE,
- * ZQ4_ERR_ALIGN, ZQ4_ERR_UNSUPPORTED (x of the largest K does not fit in
- * shared memory).
+ * ZQ4_ERR_ALIGN, ZQ4_ERR_UNSUPPORTED (M >= 3 and x of the largest K does not
+ * fit in shared memory).
  */
 ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes);
 
@@ -446,12 +468,12 @@ ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, i
  * jobs conflict when they touch the same bytes and one of them writes them
  * (y of one meets x or y of the other). Conflicting jobs keep their order;
  * within that, a job that would wait for a job run shortly before it lets
- * later jobs that conflict with nothing still to run go first, until about
- * as much other work as that job's lies between the two.
+ * later jobs that conflict with nothing still to run go first, until the
+ * job it waits for is followed by its own work and twice 152 x 12 of its
+ * 16-row tiles' worth of other work (a constant, the same on any device).
  *   order[r] = the index (in `jobs`) of the r-th job run;
  *   dep[i]   = the last job run before job i that conflicts with it, or -1:
- *              every CTA finishes it before job i starts (x of a job with no
- *              such job is staged ahead, while earlier jobs compute).
+ *              it is finished before any part of job i starts.
  * Indices refer to `jobs`. The arrays hold n_jobs ints, caller-owned.
  * Errors: as zq4_stack_plan_bytes, and ZQ4_ERR_NULL for a NULL array.
  */
@@ -474,8 +496,9 @@ ZQ4_API zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, in
  * One plan must not run on two streams at once: its counters and scratch
  * are per plan. If a device-side wait gives up (ZQ4_DEVERR_WAIT_TIMEOUT in
  * zq4_device_errors) the plan is left inconsistent and must be initialised
- * again. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE (plan made on a device with a
- * different SM count), ZQ4_ERR_CUDA.
+ * again. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE (the current device is not the
+ * one the plan was made on, or the plan is a static plan that a later
+ * zq4_stack_plan_init_static has replaced), ZQ4_ERR_CUDA.
  */
 ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
 
@@ -484,8 +507,10 @@ ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
  * give the library device memory: the plan is written into a fixed array
  * inside the library (64 KiB of device memory reserved when the library
  * loads) instead of a caller buffer, and the call itself allocates nothing
- * (no device or host heap allocation; it issues a memset and one small copy
- * per job). Meant for a host layer that has no handle on the device
+ * (no device or host heap allocation; it issues one copy of the plan image
+ * from a fixed host array inside the library, so calls are serialised by a
+ * lock and need no stack space of the caller beyond an ordinary call).
+ * Meant for a host layer that has no handle on the device
  * allocator (the memory pool belongs to another framework and is not
  * reachable from it), and for code that must not allocate once it is
  * running (an allocation can block, synchronise or fail). The method on the
@@ -493,17 +518,19 @@ ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
  * zq4_stack_plan_init, and the plan it fills runs with zq4_stack_run.
  *
  * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
- * 64 KiB array, i.e. at most 1257 jobs; a longer list returns
- * ZQ4_ERR_UNSUPPORTED and changes nothing. What must start at zero (the
- * plan's launch counter, abort flag and per-job counters) is cleared by
- * every call. The first call on a device resolves the array's address
- * (cudaGetSymbolAddress); every call synchronises `stream`, so call it
- * before any stream capture begins.
+ * 64 KiB array, i.e. at most 961 jobs for a plan run by the one- and
+ * two-token kernel (64-byte job entries) and 1257 for the other (48-byte
+ * entries); a longer list returns ZQ4_ERR_UNSUPPORTED and changes nothing.
+ * What must start at zero (the plan's launch counter, abort flag and
+ * per-job counters) is cleared by every call. The first call on a device
+ * resolves the array's address (cudaGetSymbolAddress); every call
+ * synchronises `stream`, so call it before any stream capture begins.
  *
  * There is one such plan per device: a second zq4_stack_plan_init_static
- * replaces the first, and a call that overlaps a zq4_stack_run of the static
- * plan on another stream -- or two such runs on different streams -- race
- * on the same counters and give wrong results. Errors as
+ * replaces the first, after which zq4_stack_run refuses the first one's
+ * plan struct (ZQ4_ERR_SHAPE); a call that overlaps a zq4_stack_run of the
+ * static plan on another stream -- or two such runs on different streams --
+ * race on the same counters and give wrong results. Errors as
  * zq4_stack_plan_init.
  */
 ZQ4_API zq4_status zq4_stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M,

@@ -606,36 +606,48 @@ __global__ void k_prepare(const uint32_t *wq_src, const uint16_t *sc_src, uint32
 }
 
 // Segmented layout: segment (tile t, column block s) of 16 rows x 256
-// columns is 2304 contiguous bytes -- the 16 rows' 128-byte code runs, the
-// 16-byte chunk c of row i stored at i*128 + ((c ^ (i & 7)) * 16) (the
-// 128-byte swizzle, so a plain copy of the segment into shared memory is
-// bank-conflict-free for the decode kernels' fragment loads), then the 16
-// rows' 8 scales (16 bytes each). Segments are stored tile-major. Rows past N
-// are zero. Source row = dst row, or the gate/up interleave of the
-// concatenated [gate; up] matrix. One CTA (144 threads) per segment.
+// columns is 2304 contiguous bytes, one 144-byte record per row: the row's
+// 32 code words of the block, then its 8 group scales (16 bytes). Within a
+// record, word 8q + g (q = 0..3, g = 0..7) holds word q of group g (column
+// word 32 s + 4 g + q), so a decode lane that takes word q of every group
+// reads 32 contiguous bytes; within a word, nibble slot i holds element
+// (0, 2, 4, 6, 1, 3, 5, 7)[i], so that the unpack's four f16 pairs are the
+// consecutive element pairs (0,1), (2,3), (4,5), (6,7) and x needs no
+// reordering. The 144-byte row stride staggers the rows over the shared
+// memory banks (no conflicts for the fragment loads). Segments are stored
+// tile-major; rows past N are zero. Source row = dst row, or the gate/up
+// interleave of the concatenated [gate; up] matrix. One CTA (144 threads)
+// per segment: thread 36 i + c writes 4-byte word c of row record i.
+__device__ __forceinline__ uint32_t seg_nibble_order(uint32_t w)
+{
+    uint32_t o = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = (i < 4) ? 2 * i : 2 * (i - 4) + 1;    // element in nibble slot i
+        o |= ((w >> (4 * e)) & 0xFu) << (4 * i);
+    }
+    return o;
+}
+
 __global__ void k_prepare_segmented(const uint32_t *wq_src, const uint16_t *sc_src, uint8_t *dst, int N, int K,
                                     int interleave)
 {
     const int KW = K >> 3, G = K >> 5, S = K >> 8, half = N >> 1;
     const int tile = blockIdx.x / S, seg = blockIdx.x - tile * S;
-    uint8_t *base = dst + size_t(blockIdx.x) * 2304;
-    const int i = threadIdx.x;
-    if (i < 128) {
-        const int row = i >> 3, c = i & 7, n = tile * 16 + row;
-        uint4 v = make_uint4(0, 0, 0, 0);
+    uint32_t *base = reinterpret_cast<uint32_t *>(dst + size_t(blockIdx.x) * 2304);
+    for (int i = threadIdx.x; i < 16 * 36; i += blockDim.x) {
+        const int row = i / 36, c = i - row * 36, n = tile * 16 + row;
+        uint32_t v = 0;
         if (n < N) {
             const int src = interleave ? ((n & 1) ? half + (n >> 1) : (n >> 1)) : n;
-            v = *reinterpret_cast<const uint4 *>(wq_src + size_t(src) * KW + seg * 32 + c * 4);
+            if (c < 32) {
+                const int q = c >> 3, g = c & 7;
+                v = seg_nibble_order(wq_src[size_t(src) * KW + seg * 32 + 4 * g + q]);
+            } else {
+                v = *reinterpret_cast<const uint32_t *>(sc_src + size_t(src) * G + seg * 8 + 2 * (c - 32));
+            }
         }
-        *reinterpret_cast<uint4 *>(base + row * 128 + ((c ^ (row & 7)) << 4)) = v;
-    } else if (i < 144) {
-        const int row = i - 128, n = tile * 16 + row;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < N) {
-            const int src = interleave ? ((n & 1) ? half + (n >> 1) : (n >> 1)) : n;
-            v = *reinterpret_cast<const uint4 *>(sc_src + size_t(src) * G + seg * 8);
-        }
-        *reinterpret_cast<uint4 *>(base + 2048 + row * 16) = v;
+        base[i] = v;
     }
 }
 

@@ -12,8 +12,9 @@
 //    warps. Each warp streams its segments through its own ring of 4
 //    shared-memory slots, one contiguous bulk copy (2304 bytes) per segment,
 //    with a look-ahead of L2 prefetches, and computes each with the segment
-//    routine of zq4_segment.cuh (ldmatrix.x4, exact (q - 7) unpack, two
-//    chained m16n8k16 MMAs per group, fp32 scale-and-accumulate).
+//    routine of zq4_segment.cuh (16-byte shared loads of the row records,
+//    exact (q - 7) unpack, two chained m16n8k16 MMAs per group, fp32
+//    scale-and-accumulate).
 //  * The weights never depend on the previous kernel, so each warp requests
 //    its first segments before griddepcontrol.wait; with about 100 KB of
 //    shared memory and at most 128 registers per thread, a CTA of the next
@@ -113,8 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_seg(Args a)
     __syncthreads();
     griddep_launch_dependents();
 
-    uint32_t ldm_off[4];
-    ldm_offsets(lane, ldm_off);
+    const uint32_t aoff = lane_code_offset(lane);
     const uint8_t *xr = xs + size_t(min(r, a.M - 1)) * xrow + 16 * t;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int cur_tile = -1;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_seg(Args a)
             if (cur_tile >= 0) flush(cur_tile);
             cur_tile = tt;
         }
-        accumulate(ring0 + (i % kSlots) * kSegBytes, ldm_off, xr + seg * 32 * 16, r, acc);
+        accumulate(ring0 + (i % kSlots) * kSegBytes, aoff, xr + seg * 32 * 16, r, acc);
         // every lane's reads of the slot are done before the refill overwrites it
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

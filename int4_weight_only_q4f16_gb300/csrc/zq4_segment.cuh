@@ -1,17 +1,21 @@
 // zq4_segment.cuh -- the work unit of the decode kernels that stream the
 // segmented weight layout (zq4_prepare_weight with ZQ4_PREP_SEGMENTED): one
-// segment = 16 weight rows x 256 columns = 2304 contiguous bytes (the 16
-// rows' 128-byte code runs, 16-byte chunk c of row i at i*128 +
-// 16*(c ^ (i & 7)), then the rows' 8 group scales, 16 bytes each).
+// segment = 16 weight rows x 256 columns = 2304 contiguous bytes, one
+// 144-byte record per row (32 code words, then the row's 8 group scales).
+// Record word 8q + g holds word q of group g, its nibbles ordered so that the
+// exact unpack yields the element pairs (0,1), (2,3), (4,5), (6,7).
 //
 // Per 32-column group, lane (r, t) (r = lane/4, t = lane%4) takes word t of
-// rows r and r+8 -- ldmatrix.x4 fetches two groups at once, bank-conflict-
-// free on the swizzled rows -- and unpacks them into exact f16 (q - 7)
-// pairs (0,4),(1,5),(2,6),(3,7): the A fragments of two chained m16n8k16
-// MMAs against the matching pair-permuted x chunk of token r (B), fp32
-// accumulation; the group result times the fp32 group scale goes into the
-// lane's accumulator (rows r, r+8 x tokens 2t, 2t+1). q4f16_1 itself is the
-// format of "Zero TVM Documentation", section "Q4F16 quantization format".
+// rows r and r+8 -- the 32 contiguous bytes 144 r + 32 t .. of the segment
+// hold word t of all eight groups, so four 16-byte shared loads fetch the
+// lane's words of the whole segment, without bank conflicts (the 144-byte
+// row stride staggers the rows over the banks) -- and unpacks them into
+// exact f16 (q - 7) pairs: the A fragments of two chained m16n8k16 MMAs
+// against x of token r at columns 32 g + 8 t .. 32 g + 8 t + 7 (B, read as
+// it is stored), fp32 accumulation; the group result times the fp32 group
+// scale goes into the lane's accumulator (rows r, r+8 x tokens 2t, 2t+1).
+// q4f16_1 itself is the format of "Zero TVM Documentation", section "Q4F16
+// quantization format".
 #pragma once
 
 #include <stdint.h>
@@ -43,21 +47,11 @@ __device__ __forceinline__ int part_begin(int lo, int hi, int i, int n)
     return lo + int(unsigned(hi - lo) * unsigned(i) / unsigned(n));
 }
 
-// ldmatrix row addresses of this lane for the four group pairs of a slot:
-// lane L gives row (L & 7) + 8 * ((L >> 3) & 1) of chunk 2*gp + (L >> 4).
-__device__ __forceinline__ void ldm_offsets(int lane, uint32_t (&off)[4])
-{
-    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lch = lane >> 4;
-#pragma unroll
-    for (int gp = 0; gp < 4; ++gp) off[gp] = uint32_t(lrow * 128 + (((2 * gp + lch) ^ (lrow & 7)) << 4));
-}
-
-// Stage x [M][K] into shared memory rows of `xrow` bytes, the 8 values of
-// word chunk cw of token m stored as the pairs (x0,x4),(x1,x5),(x2,x6),
-// (x3,x7) the unpack produces. Loads go through L2 only (x may have been
-// written by other SMs) and are issued kBatch at a time per thread, so one
-// memory latency covers up to kBatch * nthreads chunks (x is usually cold in
-// L2 in a decode step: the weights stream through it).
+// Stage x [M][K] into shared memory rows of `xrow` bytes, as stored. Loads
+// go through L2 only (x may have been written by other SMs) and are issued
+// kBatch at a time per thread, so one memory latency covers up to kBatch *
+// nthreads chunks (x is usually cold in L2 in a decode step: the weights
+// stream through it).
 template <int kBatch>
 __device__ __forceinline__ void stage_x(uint8_t *xs, uint32_t xrow, const uint16_t *x, int M, int K, int tid,
                                         int nthreads)
@@ -78,48 +72,54 @@ __device__ __forceinline__ void stage_x(uint8_t *xs, uint32_t xrow, const uint16
             const int i = i0 + b * nthreads;
             if (i < total) {
                 const int m = i / words, cw = i - m * words;
-                uint4 o;
-                o.x = __byte_perm(v[b].x, v[b].z, 0x5410);
-                o.y = __byte_perm(v[b].x, v[b].z, 0x7632);
-                o.z = __byte_perm(v[b].y, v[b].w, 0x5410);
-                o.w = __byte_perm(v[b].y, v[b].w, 0x7632);
-                *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = o;
+                *reinterpret_cast<uint4 *>(xs + size_t(m) * xrow + size_t(cw) * 16) = v[b];
             }
         }
     }
 }
 
-// acc += one segment held in shared memory at `cb`; `xg` = the staged x row
-// of this lane's token at the segment's first word chunk (+16 t).
-__device__ __forceinline__ void accumulate(uint32_t cb, const uint32_t (&ldm_off)[4], const uint8_t *xg, int r,
-                                           float (&acc)[4])
+// Byte offset of lane (r, t)'s code words of row r within a segment.
+__device__ __forceinline__ uint32_t lane_code_offset(int lane)
 {
-    const uint4 sr = lds_v4(cb + kCodeBytes + r * 16);          // row r, groups 0..7
-    const uint4 sr8 = lds_v4(cb + kCodeBytes + (r + 8) * 16);   // row r+8
+    return uint32_t((lane >> 2) * 144 + 32 * (lane & 3));
+}
+
+// The lane's word of group g (0..7) from its two 16-byte loads of one row.
+__device__ __forceinline__ uint32_t group_word(const uint4 &lo, const uint4 &hi, int g)
+{
+    const uint4 &v = g < 4 ? lo : hi;
+    const int i = g & 3;
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// acc += one segment held in shared memory at `cb`; `aoff` =
+// lane_code_offset(lane); `xg` = the staged x row of this lane's token at the
+// segment's first column (+16 t).
+__device__ __forceinline__ void accumulate(uint32_t cb, uint32_t aoff, const uint8_t *xg, int r, float (&acc)[4])
+{
+    const uint4 c0 = lds_v4(cb + aoff), c1 = lds_v4(cb + aoff + 16);               // row r, groups 0-3, 4-7
+    const uint4 c8 = lds_v4(cb + aoff + 1152), c9 = lds_v4(cb + aoff + 1168);      // row r+8
+    const uint4 sr = lds_v4(cb + r * 144 + 128);                                    // row r, scales 0..7
+    const uint4 sr8 = lds_v4(cb + (r + 8) * 144 + 128);
     const uint32_t srw[4] = {sr.x, sr.y, sr.z, sr.w}, sr8w[4] = {sr8.x, sr8.y, sr8.z, sr8.w};
 #pragma unroll
-    for (int gp = 0; gp < 4; ++gp) {
-        const uint4 w = ldmatrix_x4(cb + ldm_off[gp]);           // (r, g0), (r+8, g0), (r, g1), (r+8, g1)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int g = 2 * gp + h;
-            uint32_t pa[4], pb[4];
-            unpack_word_f16x2(h == 0 ? w.x : w.z, pa);
-            unpack_word_f16x2(h == 0 ? w.y : w.w, pb);
-            const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
-            const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
-            const float s_r = f16_bits_to_float(uint16_t(h == 0 ? srw[gp] : srw[gp] >> 16));
-            const float s_r8 = f16_bits_to_float(uint16_t(h == 0 ? sr8w[gp] : sr8w[gp] >> 16));
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xg + g * 64);
-            const float z[4] = {0.f, 0.f, 0.f, 0.f};
-            float d[4];
-            mma16816(d, a0, xv.x, xv.y, z);
-            mma16816(d, a1, xv.z, xv.w, d);
-            acc[0] = fmaf(s_r, d[0], acc[0]);
-            acc[1] = fmaf(s_r, d[1], acc[1]);
-            acc[2] = fmaf(s_r8, d[2], acc[2]);
-            acc[3] = fmaf(s_r8, d[3], acc[3]);
-        }
+    for (int g = 0; g < 8; ++g) {
+        uint32_t pa[4], pb[4];
+        unpack_word_f16x2(group_word(c0, c1, g), pa);
+        unpack_word_f16x2(group_word(c8, c9, g), pb);
+        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+        const float s_r = f16_bits_to_float(uint16_t((g & 1) ? srw[g >> 1] >> 16 : srw[g >> 1]));
+        const float s_r8 = f16_bits_to_float(uint16_t((g & 1) ? sr8w[g >> 1] >> 16 : sr8w[g >> 1]));
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xg + g * 64);
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float d[4];
+        mma16816(d, a0, xv.x, xv.y, z);
+        mma16816(d, a1, xv.z, xv.w, d);
+        acc[0] = fmaf(s_r, d[0], acc[0]);
+        acc[1] = fmaf(s_r, d[1], acc[1]);
+        acc[2] = fmaf(s_r8, d[2], acc[2]);
+        acc[3] = fmaf(s_r8, d[3], acc[3]);
     }
 }
 

@@ -27,10 +27,11 @@
 //    releases a slot (an mbarrier per slot each way), across job
 //    boundaries, so the compute warps never spend issue slots on copies.
 //    Per 32-column group, lane (r, t) (r = lane/4, t = lane%4) takes word t
-//    of rows r and r+8 (ldmatrix.x4 fetches two groups, conflict-free on the
-//    swizzle), unpacks exact f16 (q - 7) pairs as the A fragments of two
-//    chained m16n8k16 MMAs against the matching pair-permuted x chunk, and
-//    adds the fp32 result times the fp32 group scale to its accumulator.
+//    of rows r and r+8 (four 16-byte shared loads fetch its words of all
+//    eight groups, conflict-free in the row-record layout), unpacks exact f16
+//    (q - 7) pairs as the A fragments of two chained m16n8k16 MMAs against
+//    the matching x chunk (as stored), and adds the fp32 result times the
+//    fp32 group scale to its accumulator.
 //  * Tiles (16 output rows) are dealt round-robin over the CTAs, the jobs'
 //    tiles as one sequence (Job::off), so per-CTA work over a run of jobs
 //    is even to within one tile. A CTA splits the segments of its tiles
@@ -68,12 +69,14 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
 #include "zq4_segment.cuh"
+#include "zq4_step.h"
 
 namespace zq4 {
 
@@ -250,19 +253,6 @@ __device__ __forceinline__ void sum_split_tiles(int t0, int G, int nt, int S, in
     }
 }
 
-// x chunk i of M*K/8 (16 bytes of token i / (K/8)) into its staged place,
-// pair-permuted as the unpack produces: (x0,x4),(x1,x5),(x2,x6),(x3,x7)
-// x chunk of 8 values as the (x0,x4),(x1,x5),(x2,x6),(x3,x7) pairs the unpack produces
-__device__ __forceinline__ uint4 pair_perm(uint4 v)
-{
-    uint4 o;
-    o.x = __byte_perm(v.x, v.z, 0x5410);
-    o.y = __byte_perm(v.x, v.z, 0x7632);
-    o.z = __byte_perm(v.y, v.w, 0x5410);
-    o.w = __byte_perm(v.y, v.w, 0x7632);
-    return o;
-}
-
 // Monotone counters in shared memory between the x warp and the compute
 // warps (release / acquire at CTA scope).
 __device__ __forceinline__ void st_release_cta(int *p, int v)
@@ -314,6 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
     // stopped early (abort), nothing more to publish
     int *s_rdone = const_cast<int *>(s_abort + 2);
     volatile int *s_rstop = s_abort + 3;
+    // s_xprog: the x warp is done with every job before this one (staged or
+    // skipped); x of a dependent job is staged by the compute threads only
+    // then, so that they never share a buffer with the x warp's staging of an
+    // earlier job (CTAs without tiles in a run of jobs can get far ahead of it)
+    int *s_xprog = const_cast<int *>(s_abort + 4);
     float *wpark = reinterpret_cast<float *>(smem + kParkOff);
     int *wtab = reinterpret_cast<int *>(smem + kTabOff);
     uint8_t *xs = smem + kXsOff;                       // x of job j: xs + (j % x_bufs) * xs_size
@@ -329,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         *s_cbrk = 0;
         *s_rdone = 0;
         *s_rstop = 0;
+        *s_xprog = p.x_bufs > 1 ? 0 : p.n_jobs;
         for (int c = 0; c < kMaxChunks; ++c) s_chunk[c] = 0;
         *s_xfree = 0;
     }
@@ -471,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         bool stop = false;
         for (int j = 0; j < n && !stop && p.x_bufs > 1; ++j) {
             const Job &jb = job(j);
+            if (lane == 0) st_release_cta(s_xprog, j);       // every earlier job's x is in place
             if ((jb.flags >> kDepShift) != 0) continue;
             if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs)) {
                 stop = true;
@@ -508,13 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 for (int q = 0; q < kXBatch; ++q)
                     if (qc[q] >= 0)
                         *reinterpret_cast<uint4 *>(xsj + (qc[q] >> 8) * int(xrow) + ((qc[q] & 255) * 32 + lane) * 16) =
-                            pair_perm(v[q]);
+                            v[q];
             }
             __syncwarp();
             // lane l publishes chunks l and l + 32
             if ((all >> lane) & 1ull) st_release_cta(s_chunk + lane, j + 1);
             if ((all >> (lane + 32)) & 1ull) st_release_cta(s_chunk + lane + 32, j + 1);
         }
+        if (lane == 0) st_release_cta(s_xprog, stop ? (1 << 30) : n);
         if (stop) {
             // release every chunk, so that no compute warp waits on one (the results are void)
             if (lane == 0)
@@ -529,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         // ---------------- compute warps ----------------
         const uint32_t ring0 = sbase + uint32_t(kRingOff) + uint32_t(warp * kSlots * kSegBytes);
         const uint32_t bfull = full0 + uint32_t(8 * warp * kSlots), bempty = empty0 + uint32_t(8 * warp * kSlots);
-        uint32_t ldm_off[4];
-        ldm_offsets(lane, ldm_off);
+        const uint32_t aoff = lane_code_offset(lane);
         const uint8_t *xr = xs + size_t(min(r, M - 1)) * xrow + 16 * t;
 
         // the warp range table of job j (one of two buffers, so that the table
@@ -590,9 +587,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 // dep: thread 0 waits, the barrier passes its acquire on) or
                 // there is no buffer to stage ahead into: the compute threads
                 // stage x, all loads in one round trip
+                if (threadIdx.x == 0 && !wait_at_least(s_xprog, j)) {
+                    atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+                    atomicOr(&p.hdr->abort, 1u);
+                    *s_abort = 1;
+                }
                 if (threadIdx.x == 0 && dep >= 0) {
                     const unsigned long long t0 = globaltimer();
-                    while (ld_acquire(&p.job_cnt[dep]) < target) {
+                    while (int(ld_acquire(&p.job_cnt[dep]) - target) < 0) {   // wrap-safe: counters grow across launches
                         if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
                             atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
                             atomicOr(&p.hdr->abort, 1u);
@@ -615,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                         const int i = i0 + q * kCompute;
                         if (i < total) {
                             const int m = i / words;
-                            *reinterpret_cast<uint4 *>(xsj + m * int(xrow) + (i - m * words) * 16) = pair_perm(v[q]);
+                            *reinterpret_cast<uint4 *>(xsj + m * int(xrow) + (i - m * words) * 16) = v[q];
                         }
                     }
                 }
@@ -639,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                     if (cur_tile >= 0) flush(cur_tile);
                     cur_tile = tt;
                 }
-                accumulate(ring0 + slot * kSegBytes, ldm_off, xrj + sg * 32 * 16, r, acc);
+                accumulate(ring0 + slot * kSegBytes, aoff, xrj + sg * 32 * 16, r, acc);
                 // every lane's reads of the slot (their values are in registers)
                 // are done before the copy warp may overwrite it
                 __syncwarp();
@@ -690,11 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
 }  // namespace st
 
 // ---------------------------------------------------------------------------
-// Host side
+// Host side: the plan API shared by both engines (this file's k_stack for 3..8
+// tokens, zq4_step.cu's k_step for 1 or 2)
 // ---------------------------------------------------------------------------
 namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+enum Engine { kEngineStack = 0, kEngineStep = 1 };
 
 // Largest dynamic shared memory k_stack has been allowed per device: one
 // record for every caller, so the limit only ever grows.
@@ -714,17 +719,22 @@ Layout layout_for(int n_jobs)
     return l;
 }
 
+size_t plan_bytes_for(int engine, int n_jobs)
+{
+    return engine == kEngineStep ? StepLayout(n_jobs).total : layout_for(n_jobs).total;
+}
+
 zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, int *max_k, int *max_tiles)
 {
     if (!jobs) return ZQ4_ERR_NULL;
     if (n_jobs <= 0 || M < 1 || M > st::kTokCols) return ZQ4_ERR_SHAPE;
     int mk = 0, mt = 0;
+    long long tiles = 0;
     for (int j = 0; j < n_jobs; ++j) {
         const zq4_stack_job &b = jobs[j];
         if (!b.wq || !b.x || !b.y) return ZQ4_ERR_NULL;
         if (b.scales) return ZQ4_ERR_FLAGS;     // the segmented layout carries the scales
         if (b.N <= 0 || b.K <= 0 || b.K % st::kSegCols != 0 || (b.gate_up && (b.N & 1))) return ZQ4_ERR_SHAPE;
-        if (b.K > st::kMaxChunks * st::kSegCols) return ZQ4_ERR_UNSUPPORTED;   // x staged in at most 64 chunks
         if (!aligned16(b.wq) || !aligned16(b.x) ||
             (reinterpret_cast<uintptr_t>(b.y) & 1))
             return ZQ4_ERR_ALIGN;
@@ -733,10 +743,19 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
         // 32-bit part math
         const long long T = (b.N + 15) / 16, U = T * (b.K / st::kSegCols);
         if (U * std::max(grid, st::kWarps) >= (1ll << 31)) return ZQ4_ERR_UNSUPPORTED;
+        tiles += T;
     }
-    if (st::smem_bytes(M, mk) > size_t(227) * 1024) return ZQ4_ERR_UNSUPPORTED;
+    if (tiles >= (1ll << 31)) return ZQ4_ERR_UNSUPPORTED;
     *max_k = mk;
     *max_tiles = mt;
+    return ZQ4_OK;
+}
+
+// What only the stack engine (k_stack) requires.
+zq4_status stack_engine_fits(int M, int max_k)
+{
+    if (max_k > st::kMaxChunks * st::kSegCols) return ZQ4_ERR_UNSUPPORTED;   // x staged in at most 64 chunks
+    if (st::smem_bytes(M, max_k) > size_t(227) * 1024) return ZQ4_ERR_UNSUPPORTED;
     return ZQ4_OK;
 }
 
@@ -765,30 +784,45 @@ bool conflict(const zq4_stack_job &a, const zq4_stack_job &b, int M)
 
 constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
 
+// Work (segments) to place between a job and a job that waits for it, beyond
+// the job's own work: two tiles per compute warp of a full GB300 (152 SMs x
+// 12 warps), so that in the step engine, where each warp takes tiles one at
+// a time, the last tiles of the job are done before the first tiles of the
+// waiting job are handed out. A constant, so the order does not depend on
+// the device (a smaller GPU only gets more room than it needs).
+constexpr long long kSlackTiles = 2ll * 152 * kStepWarps;
+
+// Scratch for the host scheduling (n entries each; anc: n bitsets of
+// `words` 64-bit words), from the caller so that the static-plan path
+// allocates nothing.
+struct SchedScratch {
+    long long *work, *need, *at;
+    char *placed;
+    int *nwait;
+    int (*waits)[kStepMaxWaits];
+    uint64_t *anc;
+    int words;
+};
+
 // The order the kernel runs the jobs in and the wait before each. The
 // results are those of the given order: two jobs that conflict keep their
-// order. Within that, a job that would wait for a job run shortly before it
-// lets later jobs that conflict with no job still to place (it included)
-// and wait for nothing go first, until about as much other work as that
-// job's has been placed between the two: the CTAs that finish it early
-// work on those meanwhile instead of waiting for the last ones.
+// order. Within that, a job that would wait for a job placed shortly before
+// it lets later jobs that conflict with no job still to place (it included)
+// and wait for nothing recent go first, until the job it waits for is
+// followed by at least its own work and kSlackTiles of its tiles' segments:
+// the SMs that finish the first job early work on those meanwhile instead of
+// waiting for the last ones.
 //
-// Waits (positions in run order): dep[r] = the last job before r that
-// conflicts with it, which every CTA must have finished first; -1: none.
-//
-// Scratch (n entries each) comes from the caller, so that this allocates
-// nothing: work, at (segments; total placed work right after placing a job)
-// and placed.
-struct SchedScratch {
-    long long *work, *at;
-    char *placed;
-};
-void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, SchedScratch sc)
+// dep[r] (positions in run order) = the last job before r that conflicts
+// with it (-1: none).
+void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, const SchedScratch &sc)
 {
-    long long *work = sc.work, *at = sc.at;
+    long long *work = sc.work, *need = sc.need, *at = sc.at;
     char *placed = sc.placed;
     for (int i = 0; i < n; ++i) {
-        work[i] = (long long)((jobs[i].N + 15) / 16) * (jobs[i].K / st::kSegCols);
+        const long long S = jobs[i].K / st::kSegCols;
+        work[i] = (long long)((jobs[i].N + 15) / 16) * S;
+        need[i] = std::max(work[i], kSlackTiles * S);
         at[i] = -1;
         placed[i] = 0;
     }
@@ -796,10 +830,10 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, Sch
     long long total = 0;
     // how much more work must be placed before job j runs without a wait on a recent job
     auto short_by = [&](int j) {
-        long long need = 0;
+        long long sh = 0;
         for (int i = 0; i < n; ++i)
-            if (placed[i] && conflict(jobs[i], jobs[j], M)) need = std::max(need, work[i] - (total - at[i]));
-        return need;
+            if (placed[i] && conflict(jobs[i], jobs[j], M)) sh = std::max(sh, need[i] - (total - at[i]));
+        return sh;
     };
     int first = 0;
     while (n_placed < n) {
@@ -829,7 +863,31 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, Sch
     }
 }
 
-// Device entry of the job run at position r.
+// The step engine's waits (positions in run order): every earlier job that
+// conflicts with job r, except those already complete when another of its
+// waits is (a job's tiles start only after its own waits are complete).
+// False if some job would need more than kStepMaxWaits.
+bool wait_lists(const zq4_stack_job *jobs, int n, int M, const int *order, const SchedScratch &sc)
+{
+    const int W = sc.words;
+    for (int r = 0; r < n; ++r) {
+        uint64_t *ar = sc.anc + size_t(r) * W;
+        for (int w = 0; w < W; ++w) ar[w] = 0;
+        sc.nwait[r] = 0;
+        for (int q = r - 1; q >= 0; --q) {
+            if ((ar[q >> 6] >> (q & 63)) & 1u) continue;               // implied by a later wait
+            if (!conflict(jobs[order[q]], jobs[order[r]], M)) continue;
+            if (sc.nwait[r] == kStepMaxWaits) return false;
+            sc.waits[r][sc.nwait[r]++] = q;
+            const uint64_t *aq = sc.anc + size_t(q) * W;
+            for (int w = 0; w < W; ++w) ar[w] |= aq[w];
+            ar[q >> 6] |= uint64_t(1) << (q & 63);
+        }
+    }
+    return true;
+}
+
+// Device entry of the job run at position r (stack engine).
 st::Job make_job(const zq4_stack_job &b, int off, int dep)
 {
     st::Job jb;
@@ -846,31 +904,132 @@ st::Job make_job(const zq4_stack_job &b, int off, int dep)
     return jb;
 }
 
-// The job table in run order (into t[n]), round-robin offsets for G CTAs;
-// order and dep hold n ints of scratch.
-void job_table(const zq4_stack_job *jobs, int n, int M, int G, st::Job *t, int *order, int *dep,
-               SchedScratch sc)
-{
-    schedule(jobs, n, M, order, dep, sc);
-    for (int r = 0, off = 0; r < n; ++r) {
-        t[r] = make_job(jobs[order[r]], off, dep[r]);
-        off = int((off + (long long)t[r].T) % G);
-    }
-}
-
 // Heap scratch for the calls that may allocate.
 struct SchedBuffers {
-    std::vector<int> order, dep;
-    std::vector<long long> work, at;
+    std::vector<int> order, dep, nwait;
+    std::vector<long long> work, need, at;
     std::vector<char> placed;
-    explicit SchedBuffers(int n) : order(n), dep(n), work(n), at(n), placed(n) {}
-    SchedScratch scratch() { return {work.data(), at.data(), placed.data()}; }
+    std::vector<int> waits;
+    std::vector<uint64_t> anc;
+    int words;
+    explicit SchedBuffers(int n)
+        : order(n), dep(n), nwait(n), work(n), need(n), at(n), placed(n), waits(size_t(n) * kStepMaxWaits),
+          anc(size_t(n) * ((n + 63) / 64)), words((n + 63) / 64) {}
+    SchedScratch scratch()
+    {
+        return {work.data(), need.data(), at.data(), placed.data(), nwait.data(),
+                reinterpret_cast<int(*)[kStepMaxWaits]>(waits.data()), anc.data(), words};
+    }
 };
 
-// Dynamic shared memory of a launch: the fixed part plus the cached jobs.
+// Jobs that wait for a job placed with less than half its room before them
+// (a chain of projections, each reading the one before, has nothing to put
+// in between).
+int tight_waits(int n, const int *order, const int *dep, const SchedScratch &sc)
+{
+    int tight = 0;
+    for (int r = 0; r < n; ++r) {
+        if (dep[r] < 0) continue;
+        const int j = order[r], d = order[dep[r]];
+        if (2 * ((sc.at[j] - sc.work[j]) - sc.at[d]) < sc.need[d]) ++tight;
+    }
+    return tight;
+}
+
+// The engine a plan of these jobs runs on: k_step for one or two tokens
+// when every job needs at most kStepMaxWaits waits and at most one job in
+// eight waits for a job placed shortly before it (k_step computes a whole
+// tile per warp: a job's last tiles take a tile's time, which a waiting job
+// pays in full, where k_stack splits every tile of a job over a CTA's warps);
+// else k_stack.
+int choose_engine(const zq4_stack_job *jobs, int n, int M, const int *order, const int *dep, const SchedScratch &sc)
+{
+    if (M <= kStepMaxM && 8 * tight_waits(n, order, dep, sc) <= n && wait_lists(jobs, n, M, order, sc))
+        return kEngineStep;
+    return kEngineStack;
+}
+
+// The plan's device image (header zero, job table, counters zero) into `host`
+// (plan_bytes_for(engine, n) bytes), for G CTAs. The schedule must have been
+// computed into sc / order / dep (and the wait lists for the step engine).
+void write_image(int engine, const zq4_stack_job *jobs, int n, const int *order, const int *dep,
+                 const SchedScratch &sc, int G, uint8_t *host, long long *tiles_out, int *n_pub_out)
+{
+    memset(host, 0, plan_bytes_for(engine, n));
+    if (engine == kEngineStack) {
+        st::Job *t = reinterpret_cast<st::Job *>(host + layout_for(n).jobs);
+        for (int r = 0, off = 0; r < n; ++r) {
+            t[r] = make_job(jobs[order[r]], off, dep[r]);
+            off = int((off + (long long)t[r].T) % G);
+        }
+        *tiles_out = 0;
+        *n_pub_out = 0;
+        return;
+    }
+    StepJob *t = reinterpret_cast<StepJob *>(host + StepLayout(n).jobs);
+    long long tile0 = 0;
+    for (int r = 0; r < n; ++r) {
+        const zq4_stack_job &b = jobs[order[r]];
+        StepJob &jb = t[r];
+        jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
+        jb.x = b.x;
+        jb.y = b.y;
+        jb.N = b.N;
+        jb.K = b.K;
+        jb.T = (b.N + 15) / 16;
+        jb.tile0 = int(tile0);
+        jb.flags = b.gate_up ? kStepGateUp : 0;
+        jb.y_stride = b.gate_up ? b.N / 2 : b.N;
+        jb.nwait = sc.nwait[r];
+        for (int w = 0; w < kStepMaxWaits; ++w) jb.wait[w] = w < sc.nwait[r] ? sc.waits[r][w] : 0;
+        tile0 += jb.T;
+    }
+    int n_pub = 0;
+    for (int r = 0; r < n; ++r)
+        for (int w = 0; w < t[r].nwait; ++w) t[t[r].wait[w]].flags |= kStepPublish;
+    for (int r = 0; r < n; ++r)
+        if (t[r].flags & kStepPublish) t[r].flags |= (n_pub++) << kStepPubShift;
+    *tiles_out = tile0;
+    *n_pub_out = n_pub;
+}
+
+// Kernel attributes and residency for a launch of this plan shape.
+zq4_status check_resident(int engine, int n_jobs, int M, int max_k, int n_pub);
+
+// Dynamic shared memory of a stack-engine launch: the fixed part plus the cached jobs.
 size_t launch_smem(int n_jobs, int M, int max_k)
 {
     return st::smem_fixed(M, max_k) + size_t(st::cached_jobs(n_jobs, M, max_k)) * sizeof(st::Job);
+}
+
+zq4_status check_resident(int engine, int n_jobs, int M, int max_k, int n_pub)
+{
+    if (engine == kEngineStep) return step_check_resident(M, max_k, n_jobs, n_pub);
+    const size_t smem = launch_smem(n_jobs, M, max_k);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
+    if (e != cudaSuccess) return cuda_status(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, st::k_stack, st::kThreads, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    return per_sm < 1 ? ZQ4_ERR_UNSUPPORTED : ZQ4_OK;
+}
+
+// Checks, schedule and engine choice shared by every entry point.
+zq4_status plan_common(const zq4_stack_job *jobs, int n_jobs, int M, int grid, int *order, int *dep,
+                       const SchedScratch &sc, int *engine, int *max_k, int *max_tiles)
+{
+    zq4_status st = check_jobs(jobs, n_jobs, M, grid, max_k, max_tiles);
+    if (st != ZQ4_OK) return st;
+    schedule(jobs, n_jobs, M, order, dep, sc);
+    *engine = choose_engine(jobs, n_jobs, M, order, dep, sc);
+    if (*engine == kEngineStack) return stack_engine_fits(M, *max_k);
+    return ZQ4_OK;
+}
+
+int current_device()
+{
+    int d = -1;
+    return cudaGetDevice(&d) == cudaSuccess ? d : -1;
 }
 
 }  // namespace
@@ -878,11 +1037,12 @@ size_t launch_smem(int n_jobs, int M, int max_k)
 zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *order, int *dep)
 {
     if (!order || !dep) return ZQ4_ERR_NULL;
-    int mk, mt;
-    const zq4_status st = check_jobs(jobs, n_jobs, M, 1, &mk, &mt);
-    if (st != ZQ4_OK) return st;
+    if (!jobs) return ZQ4_ERR_NULL;
+    if (n_jobs <= 0) return ZQ4_ERR_SHAPE;
     SchedBuffers b(n_jobs);
-    schedule(jobs, n_jobs, M, b.order.data(), b.dep.data(), b.scratch());
+    int engine, mk, mt;
+    const zq4_status st = plan_common(jobs, n_jobs, M, 1, b.order.data(), b.dep.data(), b.scratch(), &engine, &mk, &mt);
+    if (st != ZQ4_OK) return st;
     for (int r = 0; r < n_jobs; ++r) {
         const int *o = b.order.data();
         order[r] = o[r];
@@ -894,73 +1054,63 @@ zq4_status stack_plan_waits(const zq4_stack_job *jobs, int n_jobs, int M, int *o
 zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t *bytes)
 {
     if (!bytes) return ZQ4_ERR_NULL;
-    int mk, mt;
-    zq4_status s = check_jobs(jobs, n_jobs, M, sm_count(), &mk, &mt);
+    if (!jobs) return ZQ4_ERR_NULL;
+    if (n_jobs <= 0) return ZQ4_ERR_SHAPE;
+    SchedBuffers b(n_jobs);
+    int engine, mk, mt;
+    const zq4_status s = plan_common(jobs, n_jobs, M, sm_count(), b.order.data(), b.dep.data(), b.scratch(), &engine,
+                                     &mk, &mt);
     if (s != ZQ4_OK) return s;
-    *bytes = layout_for(n_jobs).total;
+    *bytes = plan_bytes_for(engine, n_jobs);
     return ZQ4_OK;
 }
 
-zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
-                           zq4_stack_plan *plan, cudaStream_t s)
-{
-    if (!dev || !plan) return ZQ4_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(dev) & 255) return ZQ4_ERR_ALIGN;
-    int mk, mt;
-    zq4_status stt = check_jobs(jobs, n_jobs, M, sm_count(), &mk, &mt);
-    if (stt != ZQ4_OK) return stt;
-    const int grid = sm_count();
-    const Layout l = layout_for(n_jobs);
-    if (bytes < l.total) return ZQ4_ERR_SHAPE;
-    // the kernel needs every CTA resident at once
-    const size_t smem = launch_smem(n_jobs, M, mk);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
-    if (e != cudaSuccess) return cuda_status(e);
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, st::k_stack, st::kThreads, smem);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (per_sm < 1) return ZQ4_ERR_UNSUPPORTED;
+namespace {
 
-    std::vector<uint8_t> host(l.total, 0);
-    uint8_t *hjobs = host.data() + l.jobs;
-    {
-        SchedBuffers b(n_jobs);
-        std::vector<st::Job> table(n_jobs);
-        job_table(jobs, n_jobs, M, grid, table.data(), b.order.data(), b.dep.data(), b.scratch());
-        memcpy(hjobs, table.data(), table.size() * sizeof(st::Job));
-    }
-    e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_status(e);
+void fill_plan(zq4_stack_plan *plan, void *dev, int engine, int n_jobs, int M, int grid, int mk, int mt,
+               long long tiles, int n_pub, int gen)
+{
     plan->dev = dev;
-    plan->bytes = l.total;
+    plan->bytes = plan_bytes_for(engine, n_jobs);
     plan->n_jobs = n_jobs;
     plan->M = M;
     plan->grid = grid;
     plan->max_k = mk;
     plan->max_tiles = mt;
-    return ZQ4_OK;
+    plan->device = current_device();
+    plan->engine = engine;
+    plan->tiles = int(tiles);
+    plan->n_pub = n_pub;
+    plan->gen = gen;
 }
 
-zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
+}  // namespace
+
+zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *dev, size_t bytes,
+                           zq4_stack_plan *plan, cudaStream_t s)
 {
-    if (!plan || !plan->dev) return ZQ4_ERR_NULL;
-    if (plan->grid != sm_count()) return ZQ4_ERR_SHAPE;   // initialised for another device
-    const Layout l = layout_for(plan->n_jobs);
-    uint8_t *base = static_cast<uint8_t *>(plan->dev);
-    st::Params p;
-    p.hdr = reinterpret_cast<st::Header *>(base + l.hdr);
-    p.jobs = reinterpret_cast<const st::Job *>(base + l.jobs);
-    p.job_cnt = reinterpret_cast<unsigned *>(base + l.job_cnt);
-    p.n_jobs = plan->n_jobs;
-    p.M = plan->M;
-    p.max_k = plan->max_k;
-    p.cached = st::cached_jobs(p.n_jobs, p.M, p.max_k);
-    p.x_bufs = st::x_buffers(p.M, p.max_k);
-    void *args[] = {&p};
-    return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),
-                                                   dim3(st::kThreads), args,
-                                                   launch_smem(p.n_jobs, p.M, p.max_k), s));
+    if (!dev || !plan || !jobs) return ZQ4_ERR_NULL;
+    if (n_jobs <= 0) return ZQ4_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(dev) & 255) return ZQ4_ERR_ALIGN;
+    const int grid = sm_count();
+    SchedBuffers b(n_jobs);
+    int engine, mk, mt;
+    zq4_status stt = plan_common(jobs, n_jobs, M, grid, b.order.data(), b.dep.data(), b.scratch(), &engine, &mk, &mt);
+    if (stt != ZQ4_OK) return stt;
+    const size_t need = plan_bytes_for(engine, n_jobs);
+    if (bytes < need) return ZQ4_ERR_SHAPE;
+    std::vector<uint8_t> host(need);
+    long long tiles;
+    int n_pub;
+    write_image(engine, jobs, n_jobs, b.order.data(), b.dep.data(), b.scratch(), grid, host.data(), &tiles, &n_pub);
+    // the kernel needs every CTA resident at once
+    stt = check_resident(engine, n_jobs, M, mk, n_pub);
+    if (stt != ZQ4_OK) return stt;
+    cudaError_t e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    fill_plan(plan, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, 0);
+    return ZQ4_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -968,8 +1118,9 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticPlanBytes = 64 * 1024;     // 1257 jobs
-constexpr int kStaticMaxJobs = 1257;                // the most whose layout fits in kStaticPlanBytes
+constexpr size_t kStaticPlanBytes = 64 * 1024;
+constexpr int kStaticMaxJobs = 1257;          // stack engine: 128 + 52 n bytes (rounded to 256) fit
+constexpr int kStaticMaxJobsStep = 961;       // step engine: 128 + 68 n bytes (rounded to 256) fit
 static_assert(sizeof(st::Job) == 48, "the documented job limit assumes 48-byte job entries");
 
 // The plan lives here when the caller has no device memory to give. Header
@@ -995,57 +1146,99 @@ cudaError_t static_plan_address(void **ptr)
     return cudaSuccess;
 }
 
+// The generation of the static plan each device holds: every
+// zq4_stack_plan_init_static advances it, and a plan struct filled by an
+// earlier call no longer runs.
+std::atomic<int> g_static_gen[kMaxDevices];
+
+// Host scratch of zq4_stack_plan_init_static: file-scope arrays (not the
+// caller's stack, not the heap), one call at a time.
+std::mutex g_static_mutex;
+uint8_t g_static_image[kStaticPlanBytes];
+int g_static_order[kStaticMaxJobs], g_static_dep[kStaticMaxJobs], g_static_nwait[kStaticMaxJobs];
+int g_static_waits[kStaticMaxJobs][kStepMaxWaits];
+long long g_static_work[kStaticMaxJobs], g_static_need[kStaticMaxJobs], g_static_at[kStaticMaxJobs];
+char g_static_placed[kStaticMaxJobs];
+constexpr int kStaticWords = (kStaticMaxJobs + 63) / 64;
+uint64_t g_static_anc[size_t(kStaticMaxJobs) * kStaticWords];
+
 }  // namespace
 
 zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, zq4_stack_plan *plan,
                                   cudaStream_t s)
 {
-    if (!plan) return ZQ4_ERR_NULL;
-    int mk, mt;
-    zq4_status stt = check_jobs(jobs, n_jobs, M, sm_count(), &mk, &mt);
+    if (!plan || !jobs) return ZQ4_ERR_NULL;
+    if (n_jobs <= 0) return ZQ4_ERR_SHAPE;
+    if (n_jobs > kStaticMaxJobs) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    const int words = (n_jobs + 63) / 64;
+    const SchedScratch sc = {g_static_work, g_static_need, g_static_at, g_static_placed, g_static_nwait,
+                             g_static_waits, g_static_anc, words};
+    const int grid = sm_count();
+    int engine, mk, mt;
+    zq4_status stt = plan_common(jobs, n_jobs, M, grid, g_static_order, g_static_dep, sc, &engine, &mk, &mt);
     if (stt != ZQ4_OK) return stt;
-    const Layout l = layout_for(n_jobs);
-    if (l.total > kStaticPlanBytes || n_jobs > kStaticMaxJobs) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
-    const size_t smem = launch_smem(n_jobs, M, mk);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
-    if (e != cudaSuccess) return cuda_status(e);
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, st::k_stack, st::kThreads, smem);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (per_sm < 1) return ZQ4_ERR_UNSUPPORTED;
+    if (engine == kEngineStep && n_jobs > kStaticMaxJobsStep) return ZQ4_ERR_UNSUPPORTED;
+    const size_t need = plan_bytes_for(engine, n_jobs);
+    if (need > kStaticPlanBytes) return ZQ4_ERR_UNSUPPORTED;
+    long long tiles;
+    int n_pub;
+    write_image(engine, jobs, n_jobs, g_static_order, g_static_dep, sc, grid, g_static_image, &tiles, &n_pub);
+    stt = check_resident(engine, n_jobs, M, mk, n_pub);
+    if (stt != ZQ4_OK) return stt;
     void *dev = nullptr;
-    e = static_plan_address(&dev);
+    cudaError_t e = static_plan_address(&dev);
     if (e != cudaSuccess) return cuda_status(e);
-    uint8_t *base = static_cast<uint8_t *>(dev);
-    // header and counters start at zero; the job table is written after
-    e = cudaMemsetAsync(base, 0, l.total, s);
-    {
-        // scratch on the stack: this call allocates nothing
-        st::Job table[kStaticMaxJobs];
-        int order[kStaticMaxJobs], dep[kStaticMaxJobs];
-        long long work[kStaticMaxJobs], at[kStaticMaxJobs];
-        char placed[kStaticMaxJobs];
-        job_table(jobs, n_jobs, M, sm_count(), table, order, dep, {work, at, placed});
-        // from pageable memory: the table is staged before the call returns
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(base + l.jobs, table, size_t(n_jobs) * sizeof(st::Job), cudaMemcpyHostToDevice, s);
-    }
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return ZQ4_ERR_CUDA;
+    // from pageable memory: the image is staged before the call returns
+    e = cudaMemcpyAsync(dev, g_static_image, need, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e);
-    plan->dev = dev;
-    plan->bytes = l.total;
-    plan->n_jobs = n_jobs;
-    plan->M = M;
-    plan->grid = sm_count();
-    plan->max_k = mk;
-    plan->max_tiles = mt;
+    const int gen = g_static_gen[d].fetch_add(1) + 1;
+    fill_plan(plan, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, gen);
     return ZQ4_OK;
+}
+
+zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
+{
+    if (!plan || !plan->dev) return ZQ4_ERR_NULL;
+    const int d = current_device();
+    if (d != plan->device || plan->grid != sm_count()) return ZQ4_ERR_SHAPE;   // made on another device
+    if (plan->gen != 0) {
+        // a static plan: only the latest one of this device is still in the array
+        void *p = nullptr;
+        if (static_plan_address(&p) != cudaSuccess || p != plan->dev || d < 0 || d >= kMaxDevices ||
+            plan->gen != g_static_gen[d].load())
+            return ZQ4_ERR_SHAPE;
+    }
+    if (plan->engine == kEngineStep) return step_run(plan, s);
+    if (plan->engine != kEngineStack) return ZQ4_ERR_SHAPE;
+    const Layout l = layout_for(plan->n_jobs);
+    uint8_t *base = static_cast<uint8_t *>(plan->dev);
+    st::Params p;
+    p.hdr = reinterpret_cast<st::Header *>(base + l.hdr);
+    p.jobs = reinterpret_cast<const st::Job *>(base + l.jobs);
+    p.job_cnt = reinterpret_cast<unsigned *>(base + l.job_cnt);
+    p.n_jobs = plan->n_jobs;
+    p.M = plan->M;
+    p.max_k = plan->max_k;
+    p.cached = st::cached_jobs(p.n_jobs, p.M, p.max_k);
+    p.x_bufs = st::x_buffers(p.M, p.max_k);
+    void *args[] = {&p};
+    return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),
+                                                   dim3(st::kThreads), args,
+                                                   launch_smem(p.n_jobs, p.M, p.max_k), s));
 }
 
 cudaError_t read_stack_error(unsigned *flags, bool clear)
 {
-    cudaError_t e = cudaMemcpyFromSymbol(flags, g_stack_error, sizeof(unsigned));
-    if (e != cudaSuccess || !clear) return e;
+    unsigned a = 0, b = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&a, g_stack_error, sizeof(unsigned));
+    if (e == cudaSuccess) e = read_step_error(&b, clear);
+    if (e != cudaSuccess) return e;
+    *flags = a | b;
+    if (!clear) return e;
     const unsigned zero = 0;
     return cudaMemcpyToSymbol(g_stack_error, &zero, sizeof(unsigned));
 }

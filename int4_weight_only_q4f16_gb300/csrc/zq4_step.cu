@@ -1,0 +1,650 @@
+// zq4_step.cu -- a decode step (an ordered list of q4f16_1 projections) as
+// one persistent launch for one or two tokens: whole 16-row tiles per warp,
+// tiles handed out one at a time from a counter, no barrier between jobs.
+//
+// What it computes: for every job j, y_j = x_j * W_j^T, or the fused gate_up
+// + SiLU*mul output for interleaved gate/up rows ("Zero TVM Documentation",
+// section "Q4F16 quantization format", cards 5 "int4 Matmul" and 6 "Fused
+// FFN"; the per-token dispatch sequence of its "Decode loop" section), with
+// the results of running the jobs one after another in the given order.
+//
+// How:
+//  * Work unit = a tile (16 weight rows x all K columns); the jobs' tiles
+//    form one sequence in run order, and each compute warp takes the next
+//    tile from a device counter (one atomic add per tile, half a tile ahead
+//    of need). A warp computes a whole tile, so no partial sum ever leaves
+//    its registers and no warp waits for another at a job boundary; a slow
+//    SM simply takes fewer tiles.
+//  * Each compute warp streams its segments (16 rows x 256 columns of the
+//    segmented layout, 2304 contiguous bytes) through its own ring of
+//    shared-memory slots: lane 0 refills the slot the warp has just used
+//    with one bulk copy of the next segment. The control flow is the same in
+//    every lane (the copy instructions are predicated on lane 0), so no
+//    issue slot goes to a one-lane branch.
+//  * x of every job is brought into shared memory once per CTA, by a stager
+//    warp, into a window of a few buffers (job j in buffer j mod NB): one
+//    bulk copy per token, issued once the job's waits are met and once no
+//    compute warp of the CTA can still need the job that held the buffer
+//    (each warp publishes a lower bound of the jobs it will still read).
+//  * Inner loop, one token (the MMA's 8 columns would otherwise hold 1
+//    useful token): column c of the m16n8k16 accumulator collects group c
+//    of the segment (a block-diagonal B: lanes of column c read x of group
+//    c, all others a zero row), so the 16 MMAs of a segment leave the eight
+//    group sums of rows r, r+8 in two chains (even and odd groups) and the
+//    group scales are applied once per segment (4 fp32 FMAs per lane instead
+//    of 32). Two tokens: columns = (token, 4 groups), two passes. The codes
+//    are unpacked to exact f16 (q - 7) (magic-number OR, one f16x2 subtract
+//    or multiply-add), the products are exact and accumulate in fp32.
+//  * A job that reads or overwrites another's buffers waits for that job (on
+//    the host's list of waits: every earlier conflicting job not already
+//    implied by another wait) before its x is staged and so before any of
+//    its tiles is computed: each warp counts its finished tiles of a
+//    waited-for job in shared memory, and a publisher warp per CTA makes
+//    them visible GPU-wide in batches (one GPU-scope fence per batch, off the
+//    compute warps) by adding to the job's global counter; the stager polls
+//    that counter (acquire), then fences the async proxy before its bulk
+//    copy reads the data.
+//  * Counters grow monotonically across launches (targets scale with the
+//    launch index); the last CTA to finish resets the tile counter and
+//    advances the launch index.
+//  * Every wait is bounded (2 s). A timeout sets ZQ4_DEVERR_WAIT_TIMEOUT and
+//    the plan's abort flag, which every waiter checks; each warp lets the
+//    copies it issued land before it exits; the plan must then be
+//    initialised again.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "zq4_async.cuh"
+#include "zq4_common.cuh"
+#include "zq4_internal.h"
+#include "zq4_segment.cuh"
+#include "zq4_step.h"
+
+namespace zq4 {
+
+__device__ unsigned g_step_error = 0;
+
+namespace sp {
+
+using segk::kSegBytes;
+using segk::group_word;
+
+constexpr int kWarps = kStepWarps;         // compute warps, one ring each
+constexpr int kStagerWarp = kWarps;
+constexpr int kPubWarp = kWarps + 1;
+constexpr int kThreads = kWarps * 32 + 64;
+
+struct Params {
+    StepHeader *hdr;
+    const StepJob *jobs;
+    unsigned *job_done;      // [n_jobs]: tiles finished (monotone across launches)
+    int n_jobs, total_tiles, M, slots, nb, xrow, cached, n_pub;
+};
+
+// Shared-memory layout (bytes from a 128-byte aligned base).
+struct Smem {
+    uint32_t ring, bars, desc, xbar, xtag, wjob, misc, zero, xwin, cta_done, cta_pub, cta_snap, jobs, total;
+    __host__ __device__ Smem(int M, int slots, int nb, int xrow, int n_pub, int cached)
+    {
+        ring = 0;
+        bars = ring + uint32_t(kWarps * slots) * kSegBytes;
+        desc = bars + uint32_t(kWarps * slots) * 8;
+        xbar = desc + uint32_t(kWarps * slots) * 16;
+        xtag = xbar + uint32_t(nb) * 8;
+        wjob = xtag + uint32_t(nb) * 4;
+        misc = wjob + kWarps * 4;
+        zero = (misc + 64 + 127) / 128 * 128;
+        xwin = zero + 128;
+        cta_done = xwin + uint32_t(nb) * uint32_t(M) * uint32_t(xrow);
+        cta_pub = cta_done + uint32_t(n_pub) * 4;
+        cta_snap = cta_pub + uint32_t(n_pub) * 4;
+        jobs = (cta_snap + uint32_t(n_pub) * 4 + 15) / 16 * 16;
+        total = jobs + uint32_t(cached) * uint32_t(sizeof(StepJob));
+    }
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned r;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+    return r;
+}
+__device__ __forceinline__ int ld_acquire_cta_s32(uint32_t saddr)
+{
+    int r;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(r) : "r"(saddr) : "memory");
+    return r;
+}
+__device__ __forceinline__ void st_release_cta_s32(uint32_t saddr, int v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_cta(uint32_t saddr, unsigned v)
+{
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr)
+{
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr));
+    return r;
+}
+__device__ __forceinline__ int4 lds_s4(uint32_t saddr)
+{
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu_() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// a counter that grows across launches has reached `target` (wrap-safe)
+__device__ __forceinline__ bool reached(unsigned v, unsigned target) { return int(v - target) >= 0; }
+__device__ __forceinline__ float lo_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w)); }
+__device__ __forceinline__ float hi_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w >> 16)); }
+// a value the compiler must keep in a register (not recompute in the loop)
+__device__ __forceinline__ uint32_t opaque(uint32_t v)
+{
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// Lane 0 (predicated, no branch): descriptor of the slot, then the segment's
+// bytes, completing on the slot's barrier.
+__device__ __forceinline__ void issue_segment(bool leader, uint32_t dslot, int4 d, uint32_t bar, uint32_t dst,
+                                              const uint8_t *src)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %0, 0;\n\t"
+        "@p st.shared.v4.s32 [%1], {%2, %3, %4, %5};\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%6], %7;\n\t"
+        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%8], [%9], %7, [%6];\n\t"
+        "}" ::"r"(leader ? 1u : 0u),
+        "r"(dslot), "r"(d.x), "r"(d.y), "r"(d.z), "r"(d.w), "r"(bar), "r"(uint32_t(kSegBytes)), "r"(dst), "l"(src)
+        : "memory");
+}
+
+// One segment into the lane's accumulators. MT tokens per pass: the 8 MMA
+// columns are (token, group) pairs, GP = 8 / MT groups per pass; lane (r, t)
+// supplies column r, i.e. x of token r / GP at group (pass, r % GP), or
+// zeros (mk[g] = 0). `E` = the segment's x in the window for this lane's
+// token minus the even zero row; the x address of group g is
+// mk[g] * E + ka[g]. The lane accumulates groups (pass, (2t mod GP) + {0, 1})
+// of rows r, r+8.
+template <int MT>
+__device__ __forceinline__ void segment(uint32_t cb, uint32_t aoff, uint32_t soff, uint32_t E,
+                                        const uint32_t (&mk)[8], const uint32_t (&ka)[8], float (&acc)[4])
+{
+    constexpr int GP = 8 / MT;
+    const uint4 c0 = lds_v4(cb + aoff), c1 = lds_v4(cb + aoff + 16);            // row r: groups 0-3, 4-7
+    const uint4 c8 = lds_v4(cb + aoff + 1152), c9 = lds_v4(cb + aoff + 1168);   // row r+8
+#pragma unroll
+    for (int p = 0; p < MT; ++p) {
+        float de[4] = {0.f, 0.f, 0.f, 0.f}, dd[4] = {0.f, 0.f, 0.f, 0.f};   // even / odd groups
+#pragma unroll
+        for (int gg = 0; gg < GP; ++gg) {
+            const int g = p * GP + gg;
+            uint32_t pa[4], pb[4];
+            unpack_word_f16x2(group_word(c0, c1, g), pa);
+            unpack_word_f16x2(group_word(c8, c9, g), pb);
+            const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+            const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+            const uint4 xv = lds_v4(mk[g] * E + ka[g]);
+            if (gg & 1) {
+                mma16816(dd, a0, xv.x, xv.y, dd);
+                mma16816(dd, a1, xv.z, xv.w, dd);
+            } else {
+                mma16816(de, a0, xv.x, xv.y, de);
+                mma16816(de, a1, xv.z, xv.w, de);
+            }
+        }
+        // columns 2t (an even group) and 2t+1 (the odd group after it)
+        const uint32_t sr = lds_u32(cb + soff + 2 * p * GP), sr8 = lds_u32(cb + soff + 1152 + 2 * p * GP);
+        acc[0] = fmaf(lo_f32(sr), de[0], acc[0]);
+        acc[1] = fmaf(hi_f32(sr), dd[1], acc[1]);
+        acc[2] = fmaf(lo_f32(sr8), de[2], acc[2]);
+        acc[3] = fmaf(hi_f32(sr8), dd[3], acc[3]);
+    }
+}
+
+// A finished tile: sum the lane's groups, then over the lanes of the same
+// token (fixed order), and write rows row0 + r, row0 + r + 8 of each token.
+template <int MT>
+__device__ __forceinline__ void finish_tile(const float (&acc)[4], const StepJob &jb, int row0, int lane, int M)
+{
+    const int r = lane >> 2, t = lane & 3;
+    float v0 = acc[0] + acc[1], v1 = acc[2] + acc[3];
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    if (MT == 1) {
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    }
+    const int tok = MT == 1 ? 0 : (t >> 1);
+    const bool writer = MT == 1 ? (t == 0) : ((t & 1) == 0 && tok < M);
+    uint16_t *y = jb.y + size_t(tok) * jb.y_stride;
+    if (!(jb.flags & kStepGateUp)) {
+        if (writer) {
+            if (row0 + r < jb.N) y[row0 + r] = float_to_f16_bits(v0);
+            if (row0 + r + 8 < jb.N) y[row0 + r + 8] = float_to_f16_bits(v1);
+        }
+    } else {
+        const float u0 = __shfl_down_sync(0xffffffffu, v0, 4), u1 = __shfl_down_sync(0xffffffffu, v1, 4);
+        if (writer && (r & 1) == 0) {
+            if (row0 + r + 1 < jb.N) y[(row0 + r) >> 1] = float_to_f16_bits(silu_f32(v0) * u0);
+            if (row0 + r + 9 < jb.N) y[(row0 + r + 8) >> 1] = float_to_f16_bits(silu_f32(v1) * u1);
+        }
+    }
+}
+
+__device__ __forceinline__ void fail(const Params &p, volatile int *s_abort)
+{
+    atomicOr(&g_step_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+    atomicOr(&p.hdr->abort, 1u);
+    *s_abort = 1;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
+    const uint32_t sbase = smem_addr(smem);
+    const Smem L(p.M, p.slots, p.nb, p.xrow, p.n_pub, p.cached);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = p.n_jobs, M = p.M, slots = p.slots, nb = p.nb;
+    const uint32_t xbuf_bytes = uint32_t(M * p.xrow);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc);
+    const uint32_t s_warps_done = sbase + L.misc + 4;
+    unsigned *cta_done = reinterpret_cast<unsigned *>(smem + L.cta_done);
+    unsigned *cta_pub = reinterpret_cast<unsigned *>(smem + L.cta_pub);
+    unsigned *cta_snap = reinterpret_cast<unsigned *>(smem + L.cta_snap);
+    StepJob *sjobs = reinterpret_cast<StepJob *>(smem + L.jobs);
+    const unsigned launch = *reinterpret_cast<volatile unsigned *>(&p.hdr->epoch);
+
+    for (int i = threadIdx.x; i < 32; i += kThreads) reinterpret_cast<uint32_t *>(smem + L.zero)[i] = 0;
+    for (int i = threadIdx.x; i < p.n_pub; i += kThreads) cta_done[i] = cta_pub[i] = 0;
+    for (int i = threadIdx.x; i < kWarps; i += kThreads) reinterpret_cast<int *>(smem + L.wjob)[i] = 0;
+    for (int i = threadIdx.x; i < nb; i += kThreads) reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        *reinterpret_cast<int *>(smem + L.misc + 4) = 0;
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.jobs);
+        uint4 *dst = reinterpret_cast<uint4 *>(sjobs);
+        const int words = p.cached * int(sizeof(StepJob) / 16);
+        for (int i = threadIdx.x; i < words; i += kThreads) dst[i] = src[i];
+    }
+    if (warp < kWarps && lane == 0) {
+        for (int j = 0; j < slots; ++j) mbar_init(sbase + L.bars + 8 * (warp * slots + j), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kStagerWarp && lane == 0) {
+        for (int b = 0; b < nb; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto job = [&](int j) -> const StepJob & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
+    const unsigned done_mul = launch + 1u;
+
+    if (warp == kStagerWarp) {
+        // ---------------- the x stager ----------------
+        // x of job j into buffer j % nb, in job order: once no compute warp
+        // of this CTA can still read the job that held the buffer, and once
+        // the job's waits are met (the data it reads is final).
+        const uint32_t wjob0 = sbase + L.wjob;
+        int j = 0;
+        for (; j < n; ++j) {
+            if (__shfl_sync(0xffffffffu, *s_abort, 0)) break;
+            const int b = j % nb;
+            const StepJob &jb = job(j);
+            int ok = 1;
+            if (j >= nb) {
+                // every lane reads one warp's bound; lane 0 alone decides to give up
+                const unsigned long long t0 = globaltimer();
+                for (;;) {
+                    const int wj = lane < kWarps ? ld_acquire_cta_s32(wjob0 + 4 * lane) : 0x7fffffff;
+                    if (__all_sync(0xffffffffu, wj > j - nb)) break;
+                    int stop = 0;
+                    if (lane == 0) stop = *s_abort || globaltimer() - t0 > kWaitLimitNs;
+                    if (__shfl_sync(0xffffffffu, stop, 0)) {
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (lane == 0) {
+                for (int w = 0; ok && w < jb.nwait; ++w) {
+                    const int d = jb.wait[w];
+                    const unsigned target = done_mul * unsigned(job(d).T);
+                    const unsigned long long t0 = globaltimer();
+                    while (!reached(ld_acquire_gpu(&p.job_done[d]), target)) {
+                        if (*s_abort || *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
+                            globaltimer() - t0 > kWaitLimitNs) {
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+                // the buffer's previous fill (job j - nb) has landed before its
+                // barrier is armed again: no compute warp of this CTA may
+                // have waited for it (the CTA can have had no tile of it)
+                if (ok && j >= nb && !mbar_wait(sbase + L.xbar + 8 * b, uint32_t(((j - nb) / nb) & 1))) ok = 0;
+                if (!ok) {
+                    fail(p, s_abort);
+                } else {
+                    // the buffer's last readers (generic proxy) and the data's
+                    // writers are ordered before the copy (async proxy)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    const uint32_t bar = sbase + L.xbar + 8 * b, dst = sbase + L.xwin + uint32_t(b) * xbuf_bytes;
+                    mbar_arrive_expect_tx(bar, uint32_t(M * jb.K * 2));
+                    for (int m = 0; m < M; ++m)
+                        bulk_load(dst + uint32_t(m * p.xrow), jb.x + size_t(m) * jb.K, uint32_t(jb.K * 2), bar);
+                    st_release_cta_s32(sbase + L.xtag + 4 * b, j);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        // the last fill of every buffer has landed before the CTA may exit
+        if (lane == 0)
+            for (int c = max(0, j - nb); c < j; ++c)
+                if (!mbar_wait(sbase + L.xbar + 8 * (c % nb), uint32_t((c / nb) & 1))) break;
+    } else if (warp == kPubWarp) {
+        // ---------------- the publisher ----------------
+        // Makes this CTA's finished tiles of the waited-for jobs visible to
+        // every SM: snapshot the shared counters (acquire: the compute warps
+        // released them after writing the tiles' outputs), one GPU-scope
+        // fence for the whole batch, then one add per changed job.
+        if (p.n_pub > 0) {
+            for (;;) {
+                const bool last = __shfl_sync(0xffffffffu, ld_acquire_cta_s32(s_warps_done) == kWarps || *s_abort, 0);
+                bool any = false;
+                for (int i = lane; i < p.n_pub; i += 32) {
+                    const unsigned c = unsigned(ld_acquire_cta_s32(sbase + L.cta_done + 4 * i));
+                    cta_snap[i] = c;
+                    any |= c != cta_pub[i];
+                }
+                __syncwarp();                             // the snapshot before the adds read it
+                if (__any_sync(0xffffffffu, any)) {
+                    fence_acq_rel_gpu_();
+                    for (int j = lane; j < n; j += 32) {
+                        const StepJob &jb = job(j);
+                        if (!(jb.flags & kStepPublish)) continue;
+                        const int i = jb.flags >> kStepPubShift;
+                        const unsigned c = cta_snap[i];
+                        if (c != cta_pub[i]) {
+                            asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&p.job_done[j]),
+                                         "r"(c - cta_pub[i])
+                                         : "memory");
+                            cta_pub[i] = c;
+                        }
+                    }
+                }
+                if (last) break;
+                __nanosleep(500);
+            }
+        }
+    } else {
+        // ---------------- compute warps ----------------
+        const int r = lane >> 2, t = lane & 3;
+        constexpr int GP = 8 / MT;
+        const bool leader = lane == 0;
+        const uint32_t ring = sbase + L.ring + uint32_t(warp * slots) * kSegBytes;
+        const uint32_t bars = sbase + L.bars + uint32_t(8 * warp * slots);
+        const uint32_t descs = sbase + L.desc + uint32_t(16 * warp * slots);
+        const uint32_t my_wjob = sbase + L.wjob + 4 * warp;
+        const uint32_t aoff = opaque(segk::lane_code_offset(lane));
+        const uint32_t soff = opaque(uint32_t(r * 144 + 128 + 2 * ((2 * t) % GP)));
+        // x addresses: lane column r is token r / GP, group slot r % GP; the
+        // zero rows are two 64-byte rows placed so that the active and the
+        // idle lanes of one load never share a bank (even groups: z0, odd: z1)
+        const int mtok = r / GP;
+        const uint32_t z1 = sbase + L.zero, z0 = z1 + 64;
+        uint32_t mk[8], ka[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const bool act = (r % GP) == (g % GP) && mtok < M;
+            const uint32_t z = (g & 1) ? z1 : z0;
+            mk[g] = opaque(act ? 1u : 0u);
+            ka[g] = opaque(z + 16 * t + (act ? uint32_t(64 * g) + z0 - z : 0u));
+        }
+        const uint32_t ex = opaque(sbase + L.xwin + uint32_t(mtok * p.xrow) - z0);   // + buffer * xbuf_bytes + 512 sg
+
+        // the issue cursor (identical in every lane)
+        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1;
+        const uint8_t *iptr = nullptr;
+        bool ihave = false, iend = false, has_next = false;
+        unsigned next_tile = 0;
+        int issued = 0, islot = 0;
+        auto grab = [&]() {
+            unsigned g;
+            if (has_next) {
+                g = next_tile;
+                has_next = false;
+            } else {
+                unsigned v = 0;
+                if (leader) v = atomicAdd(&p.hdr->next_tile, 1u);
+                g = __shfl_sync(0xffffffffu, v, 0);
+            }
+            if (g >= unsigned(p.total_tiles)) {
+                iend = true;
+                return;
+            }
+            while (int(g) >= job(fj).tile0 + job(fj).T) ++fj;
+            ijob = fj;
+            itile = int(g) - job(fj).tile0;
+            isg = 0;
+            iS = job(fj).K >> 8;
+            iptr = job(fj).seg + size_t(itile) * size_t(iS) * kSegBytes;
+            ihave = true;
+        };
+
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        int consumed = 0, cslot = 0, cjob = -1;
+        uint32_t cphase = 0, E = 0;
+        bool ok = true;
+        for (;;) {
+            // refill: the free slots of the ring, in sequence order
+            while (issued - consumed < slots) {
+                if (!ihave) {
+                    if (iend) break;
+                    grab();
+                    if (iend) break;
+                    if (issued == consumed && leader) st_release_cta_s32(my_wjob, ijob);   // holding nothing else
+                }
+                if (!has_next && isg == (iS >> 1)) {      // the next tile, half a tile ahead
+                    unsigned v = 0;
+                    if (leader) v = atomicAdd(&p.hdr->next_tile, 1u);
+                    next_tile = __shfl_sync(0xffffffffu, v, 0);
+                    has_next = true;
+                }
+                issue_segment(leader, descs + 16 * islot,
+                              make_int4(ijob, itile, (isg == 0 ? 1 : 0) | (isg == iS - 1 ? 2 : 0), 0),
+                              bars + 8 * islot, ring + uint32_t(islot) * kSegBytes, iptr);
+                iptr += kSegBytes;
+                ++issued;
+                if (++islot == slots) islot = 0;
+                if (++isg == iS) ihave = false;
+            }
+            if (issued == consumed) break;                  // no tile left
+            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * cslot, cphase))) {
+                ok = false;
+                break;
+            }
+            const int4 d = lds_s4(descs + 16 * cslot);
+            if (d.z & 1) {
+                // a tile starts: its job's x in the window (staged once per CTA)
+                const int b = d.x % nb;
+                if (d.x != cjob) {
+                    if (leader) st_release_cta_s32(my_wjob, d.x);
+                    const unsigned long long t0 = globaltimer();
+                    bool ready = false;
+                    for (;;) {
+                        if (ld_acquire_cta_s32(sbase + L.xtag + 4 * b) == d.x) {
+                            ready = true;
+                            break;
+                        }
+                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) break;
+                        __nanosleep(32);
+                    }
+                    if (!__all_sync(0xffffffffu, ready && mbar_wait(sbase + L.xbar + 8 * b, uint32_t((d.x / nb) & 1)))) {
+                        ok = false;
+                        break;
+                    }
+                    cjob = d.x;
+                }
+                E = ex + uint32_t(b) * xbuf_bytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+            }
+            const uint32_t cb = ring + uint32_t(cslot) * kSegBytes;
+            segment<MT>(cb, aoff, soff, E, mk, ka, acc);
+            E += 512;
+            // every lane's reads of the slot are done before lane 0 refills it
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (d.z & 2) {
+                const StepJob &jb = job(d.x);
+                finish_tile<MT>(acc, jb, d.y * 16, lane, M);
+                if (jb.flags & kStepPublish) {
+                    __syncwarp();
+                    if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                }
+            }
+            ++consumed;
+            if (++cslot == slots) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
+        }
+        if (!ok && leader) fail(p, s_abort);
+        // the copies still in flight (only after a failed wait) land before the CTA exits
+        if (leader)
+            for (int c = consumed; c < issued; ++c) {
+                const int s = c % slots;
+                if (!mbar_wait(bars + 8 * s, uint32_t((c / slots) & 1))) break;
+            }
+        __syncwarp();
+        if (leader) {
+            st_release_cta_s32(my_wjob, 0x7fffffff);            // reads no more x
+            red_release_cta(s_warps_done, 1u);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (*s_abort) {
+            atomicOr(&g_step_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+        } else {
+            __threadfence();
+            const unsigned target = (launch + 1u) * gridDim.x;
+            const unsigned d = atomicAdd(&p.hdr->done, 1u);
+            if (d == target - 1u) {                       // the last CTA of this launch
+                p.hdr->next_tile = 0;
+                __threadfence();
+                atomicAdd(&p.hdr->epoch, 1u);
+            }
+        }
+    }
+}
+
+}  // namespace sp
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+int step_smem_set[kMaxDevices] = {};
+int step_smem_set2[kMaxDevices] = {};
+
+const void *step_kernel(int M)
+{
+    return M == 1 ? reinterpret_cast<const void *>(sp::k_step<1>) : reinterpret_cast<const void *>(sp::k_step<2>);
+}
+
+}  // namespace
+
+size_t step_plan_layout_bytes(int n_jobs)
+{
+    return StepLayout(n_jobs).total;
+}
+
+// Ring slots, x buffers and cached jobs of a launch: as many slots (5 down to
+// 3) as leave room for at least 3 x buffers (2 if nothing else fits), then as
+// many x buffers as fit (up to 6), then the job table.
+bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh)
+{
+    const size_t cap = size_t(227) * 1024 - 128;
+    const int xrow = (max_k * 2 + 127) / 128 * 128;
+    for (int min_nb = 3; min_nb >= 2; --min_nb)
+        for (int s = 5; s >= 3; --s) {
+            if (sp::Smem(M, s, min_nb, xrow, n_pub, 0).total > cap) continue;
+            int nb = min_nb;
+            while (nb < 6 && sp::Smem(M, s, nb + 1, xrow, n_pub, 0).total <= cap) ++nb;
+            const size_t base = sp::Smem(M, s, nb, xrow, n_pub, 0).total;
+            sh->slots = s;
+            sh->nb = nb;
+            sh->xrow = xrow;
+            sh->cached = int(std::min<size_t>(size_t(n_jobs), (cap - base) / sizeof(StepJob)));
+            sh->smem = sp::Smem(M, s, nb, xrow, n_pub, sh->cached).total + 128;
+            return true;
+        }
+    return false;
+}
+
+zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
+{
+    const StepLayout l(plan->n_jobs);
+    uint8_t *base = static_cast<uint8_t *>(plan->dev);
+    sp::Params p;
+    p.hdr = reinterpret_cast<StepHeader *>(base + l.hdr);
+    p.jobs = reinterpret_cast<const StepJob *>(base + l.jobs);
+    p.job_done = reinterpret_cast<unsigned *>(base + l.job_done);
+    p.n_jobs = plan->n_jobs;
+    p.total_tiles = plan->tiles;
+    p.M = plan->M;
+    p.n_pub = plan->n_pub;
+    StepShape sh;
+    if (!step_launch_shape(p.M, plan->max_k, p.n_jobs, p.n_pub, &sh)) return ZQ4_ERR_UNSUPPORTED;
+    p.slots = sh.slots;
+    p.nb = sh.nb;
+    p.xrow = sh.xrow;
+    p.cached = sh.cached;
+    const void *kern = step_kernel(p.M);
+    cudaError_t e = ensure_smem(kern, sh.smem, p.M == 1 ? step_smem_set : step_smem_set2);
+    if (e != cudaSuccess) return cuda_status(e);
+    void *args[] = {&p};
+    return cuda_status(cudaLaunchCooperativeKernel(kern, dim3(plan->grid), dim3(sp::kThreads), args, sh.smem, s));
+}
+
+zq4_status step_check_resident(int M, int max_k, int n_jobs, int n_pub)
+{
+    StepShape sh;
+    if (!step_launch_shape(M, max_k, n_jobs, n_pub, &sh)) return ZQ4_ERR_UNSUPPORTED;
+    const void *kern = step_kernel(M);
+    cudaError_t e = ensure_smem(kern, sh.smem, M == 1 ? step_smem_set : step_smem_set2);
+    if (e != cudaSuccess) return cuda_status(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sp::kThreads, sh.smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    return per_sm < 1 ? ZQ4_ERR_UNSUPPORTED : ZQ4_OK;
+}
+
+cudaError_t read_step_error(unsigned *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_step_error, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_step_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace zq4

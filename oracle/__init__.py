@@ -93,6 +93,8 @@ def _load(mutant: int = 0):
         lib.zo_gemv_add_rmsnorm.argtypes = [_p, _p, _p, _p, _p, ctypes.c_double, _i64, _i64, _i64, _p, _p, _p, _p]
         lib.zo_qkv_rope.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _p] + [_p] * 9
         lib.zo_num_threads.restype = ctypes.c_int
+        lib.zo_set_num_threads.argtypes = [ctypes.c_int]
+        lib.zo_set_num_threads.restype = ctypes.c_int
         lib.zo_mutant.restype = ctypes.c_int
         _LIBS[mutant] = lib
         return lib
@@ -295,6 +297,11 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.zo_num_threads())
+
+    def set_num_threads(self, n: int) -> int:
+        """Threads of the oracle's parallel loops (timing only); returns the
+        count in effect."""
+        return int(self.lib.zo_set_num_threads(int(n)))
 
 
 _DEFAULT = None

@@ -690,4 +690,17 @@ int zo_num_threads(void)
 #endif
 }
 
+/* Use n threads in the OpenMP regions from now on (timing only; the
+ * results do not depend on it). Returns the count in effect. */
+int zo_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 int zo_mutant(void) { return ZO_MUTANT; }

@@ -150,25 +150,30 @@ def test_prepare_concat_to_interleaved(zq4, oracle):
 
 
 def _segmented_reference(wq, sc, N, K):
-    """The segmented layout, built byte by byte from its definition in the
-    C header (tile-major 2304-byte segments: swizzled code runs, then
-    scales; rows past N zero)."""
+    """The segmented layout, built from its definition in the C header:
+    tile-major 2304-byte segments of 16 row records of 144 bytes (record
+    word 8q + g = word q of group g with nibble slot j holding element
+    (0, 2, 4, 6, 1, 3, 5, 7)[j], then the row's 8 scales); rows past N zero."""
     T, S = (N + 15) // 16, K // 256
-    codes = wq.view(np.uint8).reshape(N, K // 2)
-    scb = sc.view(np.uint8).reshape(N, K // 16)
-    out = np.zeros(T * S * 2304, np.uint8)
+    elem_of_slot = (0, 2, 4, 6, 1, 3, 5, 7)
+    out = np.zeros(T * S * 576, np.uint32)
+    scw = np.ascontiguousarray(sc).view(np.uint32).reshape(N, K // 64)   # scale pairs
     for t in range(T):
-        for s in range(S):
-            base = (t * S + s) * 2304
+        for s_ in range(S):
             for i in range(16):
                 n = 16 * t + i
                 if n >= N:
                     continue
-                for c in range(8):
-                    off = base + i * 128 + 16 * (c ^ (i % 8))
-                    out[off:off + 16] = codes[n, 128 * s + 16 * c: 128 * s + 16 * c + 16]
-                out[base + 2048 + 16 * i: base + 2048 + 16 * i + 16] = scb[n, 16 * s: 16 * s + 16]
-    return out
+                base = (t * S + s_) * 576 + 36 * i
+                for q in range(4):
+                    for g in range(8):
+                        w = int(wq[n, 32 * s_ + 4 * g + q])
+                        v = 0
+                        for j in range(8):
+                            v |= ((w >> (4 * elem_of_slot[j])) & 0xF) << (4 * j)
+                        out[base + 8 * q + g] = v
+                out[base + 32: base + 36] = scw[n, 4 * s_: 4 * s_ + 4]
+    return out.view(np.uint8)
 
 
 @pytest.mark.parametrize("N,K,interleave", [(37, 512, False), (16, 256, False), (40, 768, True)])

@@ -61,6 +61,6 @@ def test_oracle_does_not_reach_the_package():
 
 def test_only_test_infrastructure_imports_the_oracle():
     assert sorted(set(_functions_importing(os.path.join(ROOT, "bench.py"), "oracle"))) == \
-        ["oracle_sample_rate", "run_reference"]
+        ["oracle_sample_rate", "run_oracle_table", "run_reference"]
     assert sorted(set(_functions_importing(os.path.join(ROOT, "__graft_entry__.py"), "oracle"))) == \
         ["build", "smoke"]

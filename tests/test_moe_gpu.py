@@ -90,3 +90,55 @@ def test_moe_invalid_ids_report_and_contribute_nothing(zq4, oracle):
     y_ref, S, bad = oracle.moe_down_combine(dq, ds, E, h_gpu, r, D, I, ids)
     assert bad == 3 and int(status.item()) & zq4.DEV_BAD_EXPERT_ID
     assert_within(host_f16(y), y_ref, S, "down with bad ids")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_moe_full_size_parity(zq4, oracle, T):
+    """The MoE block at its full size: 128 experts, gate_up 1024 x 2048
+    (interleaved, SiLU*mul -> 512) and down 2048 x 512, top-8 routing, T
+    tokens -- bank 0 of the benchmark's MoE workload, both stages exactly as
+    it runs them. Every output is compared with the oracle; the down stage
+    reads the GPU's own f16 h, as in the small cases."""
+    E, top_k = synth.MOE_EXPERTS, synth.MOE_TOP_K
+    (N2, D), (Dn, I) = synth.MOE_GATE_UP, synth.MOE_DOWN
+    gq, gs = synth.weight("moe_gu", E * N2, D, 0)
+    dq, ds = synth.weight("moe_dn", E * Dn, I, 0)
+    rng = synth.rng_for("moe_route", 0, T)
+    ids, r = synth.routing(rng, T, E, top_k)
+    x = synth.activations(rng, T, D)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = zq4.moe_gemv(dev(gq), dev(gs), E, dev(x), N2, D, dev(ids), zq4.MOE_GATE_UP_SILU, dev_status=status)
+    h_gpu = host_f16(h)
+    h_ref, Sh, bad = oracle.moe_gate_up(gq, gs, E, x, N2, D, ids)
+    assert h_gpu.shape == (T, top_k, N2 // 2)
+    assert_within(h_gpu, h_ref, Sh, f"moe gate_up T={T}")
+    y = zq4.moe_gemv(dev(dq), dev(ds), E, h, Dn, I, dev(ids), zq4.MOE_DOWN_COMBINE, route_w=dev(r),
+                     dev_status=status)
+    y_ref, S, bad2 = oracle.moe_down_combine(dq, ds, E, h_gpu, r, Dn, I, ids)
+    assert_within(host_f16(y), y_ref, S, f"moe down+combine T={T}")
+    assert bad == bad2 == 0 and int(status.item()) == 0
+
+
+def test_moe_routing_exact_128_experts(zq4):
+    """Routing at the full bank size: expert e's down matrix (2048 x 512,
+    the MoE workload's shape) has every code 8 and every scale 1 + e/1024
+    (distinct, exact in f16), so with slot j reading a one-hot input and a
+    one-hot router weight on slot j, every output of token t is exactly
+    1 + ids[t, j]/1024: the expert that served each (token, slot) is read
+    back bit for bit, for all 16 tokens of the largest case."""
+    E, T, top_k = synth.MOE_EXPERTS, 16, synth.MOE_TOP_K
+    Dn, I = synth.MOE_DOWN
+    wq = np.full((E * Dn, I // 8), 0x88888888, np.uint32)
+    sc = np.repeat((1.0 + np.arange(E) / 1024.0).astype(np.float16), Dn)[:, None].repeat(I // 32, 1)
+    ids, _ = synth.routing(synth.rng_for("route128", T), T, E, top_k)
+    x = np.zeros((T, top_k, I), np.float16)
+    for j in range(top_k):
+        x[:, j, 5 + 3 * j] = 1.0                                 # slot j reads one column of its own
+    for j in range(top_k):
+        r = np.zeros((T, top_k), np.float32)
+        r[:, j] = 1.0
+        y = host_f16(zq4.moe_gemv(dev(wq), dev(sc), E, dev(x), Dn, I, dev(ids), zq4.MOE_DOWN_COMBINE,
+                                  route_w=dev(r)))
+        want = (1.0 + ids[:, j] / 1024.0).astype(np.float16)
+        assert np.array_equal(y, np.repeat(want[:, None], Dn, 1)), f"slot {j}"

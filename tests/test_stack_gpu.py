@@ -41,16 +41,23 @@ def _check_job(oracle, job, what, rows=None):
         assert_within(y_h if rows is None else y_h[:, rows], y_ref, S, what)
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 def test_small_stack_matches_oracle(oracle, M):
+    """Three runs of one plan, each checked: the plan runs the three down
+    projections last, after a run of small jobs most SMs have no tile of (a
+    CTA with nothing to do in them reaches the dependent jobs early; their
+    inputs must still be the finished gate_up outputs)."""
     s = stk.DecodeStack(SMALL_LAYER, 3, SMALL_HEAD, M=M, mode="plan")
-    s.launch_step()
-    torch.cuda.synchronize()
     names = [n for n, _, _ in SMALL_LAYER]
-    for i, job in enumerate(s.jobs()):
-        l, name = divmod(i, len(names))
-        what = f"M={M} job {i} " + ("lm_head" if l == 3 else f"layer {l} {names[name]}")
-        _check_job(oracle, job, what)
+    for run in range(3):
+        for j in s.jobs():
+            j[3].fill_(float("nan"))
+        s.launch_step()
+        torch.cuda.synchronize()
+        for i, job in enumerate(s.jobs()):
+            l, name = divmod(i, len(names))
+            what = f"M={M} run {run} job {i} " + ("lm_head" if l == 3 else f"layer {l} {names[name]}")
+            _check_job(oracle, job, what)
 
 
 CHAIN_LAYER = (("qkv", 768, 256), ("o", 256, 512), ("gate_up", 1024, 256), ("down", 256, 512))
@@ -281,3 +288,45 @@ def test_stack_with_one_x_buffer(oracle):
     assert zq4.device_errors(clear=True) == 0
     for i, ((seg, x, y, N, K_, gu), (wq, sc)) in enumerate(zip(jobs, mats)):
         _check_job(oracle, (wq, sc, x, y, N, K_, gu), f"one-buffer job {i}")
+
+
+def test_step_engine_job_that_waits_for_two_jobs(oracle):
+    """One- and two-token plans run on the tile-per-warp kernel, whose waits
+    are lists: job C reads job A's output and overwrites job B's, so it waits
+    for both (neither implies the other); independent jobs around them keep
+    the waits from being tight. The final buffers equal the given order."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    M, N, K = 1, 256, 512
+    rng = synth.rng_for("step_two_waits")
+    mats = [synth.weight("step_two_waits_w", N, K, i) for i in range(16)]
+    segs = [zq4.prepare_weight(dev(w), dev(s), N, K, zq4.PREP_SEGMENTED)[0] for w, s in mats]
+    xs = [dev(synth.activations(rng, M, K)) for _ in range(16)]
+    bufA = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    bufB = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    fill = [torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda") for _ in range(13)]
+    jobs = [(segs[0], xs[0], bufA, N, K, False),                     # A: writes bufA
+            (segs[1], xs[1], bufB, N, K, False)]              # B: writes bufB
+    jobs += [(segs[3 + i], xs[3 + i], fill[i], N, K, False) for i in range(6)]
+    # C reads A's output (K = N) and overwrites B's
+    wc, sc_ = synth.weight("step_two_waits_c", N, N, 0)
+    segC = zq4.prepare_weight(dev(wc), dev(sc_), N, N, zq4.PREP_SEGMENTED)[0]
+    jobs.append((segC, bufA, bufB, N, N, False))              # C: reads A, overwrites B
+    jobs += [(segs[9 + i], xs[9 + i], fill[6 + i], N, K, False) for i in range(7)]
+    plan = zq4.StackPlan(jobs, M)
+    assert plan.plan.engine == 1
+    plan.run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    order, dep = zq4.stack_plan_waits([(j[0].data_ptr(), j[1].data_ptr(), j[2].data_ptr(), j[3], j[4], j[5])
+                                       for j in jobs], M)
+    assert order.index(8) > order.index(0) and order.index(8) > order.index(1)
+    a = host_f16(bufA)
+    a_ref, Sa = oracle.gemv(*mats[0], host_f16(xs[0]), N, K)
+    assert_within(a, a_ref, Sa, "job A")
+    c_ref, Sc = oracle.gemv(wc, sc_, a, N, N)
+    assert_within(host_f16(bufB), c_ref, Sc, "job C after A and over B")
+    for i in range(13):
+        w, s = mats[3 + i] if i < 6 else mats[9 + i - 6]
+        x = xs[3 + i] if i < 6 else xs[9 + i - 6]
+        y_ref, S = oracle.gemv(w, s, host_f16(x), N, K)
+        assert_within(host_f16(fill[i]), y_ref, S, f"independent job {i}")

@@ -62,11 +62,21 @@ def test_mixed_job_list(zq4):
         (W, buf(7), buf(6), 256, 512, 0),         # 7 y over y5 / x6
     ]
     order, dep = zq4.stack_plan_waits(jobs, M)
-    # job 2 would wait at once for job 1: job 3 (free of every job still to
-    # place) goes first; nothing else may pass job 2
-    assert order == [0, 1, 3, 2, 4, 5, 6, 7]
+    # every job here is small next to the room a waited-for job gets (its own
+    # work and 2 x 152 x 12 of its tiles' segments), so each wait is on a
+    # recent job for every job after it; the only job free of the jobs still
+    # to place (3) itself waits for job 0: nothing moves forward
+    assert order == list(range(8))
     assert dep == [-1, 0, 1, 0, 3, 4, 5, 6]
     check_valid(jobs, M, order, dep)
+
+
+def test_an_independent_job_passes_a_waiting_one(zq4):
+    # job 1 reads job 0's output; job 2 touches neither: it runs in between
+    jobs = [(W, buf(0), buf(1), 16384, 3072, 0), (W, buf(1), buf(2), 3072, 16384, 0),
+            (W, buf(3), buf(4), 3072, 3072, 0)]
+    for M in (1, 2):
+        assert zq4.stack_plan_waits(jobs, M) == ([0, 2, 1], [-1, 0, -1])
 
 
 def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
@@ -78,9 +88,10 @@ def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
                  (W, buf(b + 4), buf(b + 5), 16384, 3072, 1), (W, buf(b + 5), buf(b + 6), 3072, 8192, 0)]
     jobs.append((W, buf(99), buf(98), 32064, 3072, 0))
     order, dep = zq4.stack_plan_waits(jobs, 1)
-    # down of layer l waits for its gate_up; it is put after work as large
-    # as that gate_up: the next layer's qkv, o (and gate_up)
-    assert order == [0, 1, 2, 4, 5, 6, 3, 8, 7, 9, 10, 12, 11]
+    # down of layer l waits for its gate_up; it is put after at least
+    # 2 x 152 x 12 tiles' worth of that gate_up's segments (43,776): the next
+    # two layers' qkv, o and gate_up (or, at the end, the head)
+    assert order == [0, 1, 2, 4, 5, 6, 8, 9, 10, 12, 3, 7, 11]
     assert dep == [-1, -1, -1, 2, -1, -1, -1, 6, -1, -1, -1, 10, -1]
     check_valid(jobs, 1, order, dep)
 
