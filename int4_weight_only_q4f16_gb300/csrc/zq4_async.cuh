@@ -36,21 +36,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t by
 
 // Wait for the phase of the given parity to complete; false once the wait
 // has lasted longer than kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity)
 {
     const unsigned long long t0 = globaltimer();
     for (unsigned i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (done) return true;
+        if (mbar_try(addr, parity)) return true;
         if ((i & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// One try inline (the phase is usually complete by the time it is waited
+// for), the bounded loop out of line.
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity)
+{
+    return mbar_try(addr, parity) || mbar_wait_slow(addr, parity);
 }
 
 // Bring the box at (x, y) of a tensor map into L2 (no shared memory).

@@ -143,6 +143,16 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
     return d;
 }
 
+// (a & MASK) | c in one three-input logic instruction (the compiler left to
+// itself splits the two constants over two instructions).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+
 // Unpack one packed word into four f16x2 values holding (q - 7) exactly, as
 // the element pairs (0,4), (1,5), (2,6), (3,7) (low half first).
 //
@@ -157,10 +167,10 @@ __device__ __forceinline__ void unpack_word_f16x2(uint32_t w, uint32_t p[4])
     const uint32_t kSixteenth = 0x2C002C00u;   // (1/16, 1/16)
     const uint32_t kNeg71 = 0xD470D470u;       // (-71, -71): 1024/16 + 7
     uint32_t w8 = w >> 8;
-    p[0] = hsub2((w & 0x000F000Fu) | kMagic, kBias);                 // elements 0, 4
-    p[1] = hfma2((w & 0x00F000F0u) | kMagic, kSixteenth, kNeg71);    // elements 1, 5
-    p[2] = hsub2((w8 & 0x000F000Fu) | kMagic, kBias);                // elements 2, 6
-    p[3] = hfma2((w8 & 0x00F000F0u) | kMagic, kSixteenth, kNeg71);   // elements 3, 7
+    p[0] = hsub2(and_or<0x000F000Fu>(w, kMagic), kBias);                 // elements 0, 4
+    p[1] = hfma2(and_or<0x00F000F0u>(w, kMagic), kSixteenth, kNeg71);    // elements 1, 5
+    p[2] = hsub2(and_or<0x000F000Fu>(w8, kMagic), kBias);                // elements 2, 6
+    p[3] = hfma2(and_or<0x00F000F0u>(w8, kMagic), kSixteenth, kNeg71);   // elements 3, 7
 }
 
 // Codes of the low 16 bits / high 16 bits of v (each byte holding one code

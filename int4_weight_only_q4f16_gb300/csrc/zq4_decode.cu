@@ -83,10 +83,10 @@ __device__ __forceinline__ void unpack_word_f16x2_q(uint32_t w, uint32_t p[4])
     const uint32_t kSixteenth = 0x2C002C00u;   // (1/16, 1/16)
     const uint32_t kNeg64 = 0xD400D400u;       // (-64, -64): 1024/16
     uint32_t w8 = w >> 8;
-    p[0] = hsub2((w & 0x000F000Fu) | kMagic, kMagic);                  // elements 0, 4
-    p[1] = hfma2((w & 0x00F000F0u) | kMagic, kSixteenth, kNeg64);      // elements 1, 5
-    p[2] = hsub2((w8 & 0x000F000Fu) | kMagic, kMagic);                 // elements 2, 6
-    p[3] = hfma2((w8 & 0x00F000F0u) | kMagic, kSixteenth, kNeg64);     // elements 3, 7
+    p[0] = hsub2(and_or<0x000F000Fu>(w, kMagic), kMagic);                  // elements 0, 4
+    p[1] = hfma2(and_or<0x00F000F0u>(w, kMagic), kSixteenth, kNeg64);      // elements 1, 5
+    p[2] = hsub2(and_or<0x000F000Fu>(w8, kMagic), kMagic);                 // elements 2, 6
+    p[3] = hfma2(and_or<0x00F000F0u>(w8, kMagic), kSixteenth, kNeg64);     // elements 3, 7
 }
 
 // sum(x) of every 32-weight chunk of rows [0, rows) of src (fp32, ascending

@@ -11,16 +11,17 @@
 // How:
 //  * Work unit = a tile (16 weight rows x all K columns); the jobs' tiles
 //    form one sequence in run order, and each compute warp takes the next
-//    tile from a device counter (one atomic add per tile, half a tile ahead
-//    of need). A warp computes a whole tile, so no partial sum ever leaves
+//    tile from a device counter (one atomic add per tile, a tile ahead of
+//    need). A warp computes a whole tile, so no partial sum ever leaves
 //    its registers and no warp waits for another at a job boundary; a slow
 //    SM simply takes fewer tiles.
 //  * Each compute warp streams its segments (16 rows x 256 columns of the
 //    segmented layout, 2304 contiguous bytes) through its own ring of
-//    shared-memory slots: lane 0 refills the slot the warp has just used
-//    with one bulk copy of the next segment. The control flow is the same in
-//    every lane (the copy instructions are predicated on lane 0), so no
-//    issue slot goes to a one-lane branch.
+//    shared-memory slots: right after computing a segment it refills that
+//    slot with the next one (one bulk copy, issued by lane 0 behind the same
+//    control flow as every other lane), so the copies keep pace with the
+//    warp without a hand-off; the slot's descriptor (job, tile, first/last)
+//    travels with it.
 //  * x of every job is brought into shared memory once per CTA, by a stager
 //    warp, into a window of a few buffers (job j in buffer j mod NB): one
 //    bulk copy per token, issued once the job's waits are met and once no
@@ -78,6 +79,7 @@ constexpr int kWarps = kStepWarps;         // compute warps, one ring each
 constexpr int kStagerWarp = kWarps;
 constexpr int kPubWarp = kWarps + 1;
 constexpr int kThreads = kWarps * 32 + 64;
+constexpr int kDescFirst = 1, kDescLast = 2;   // slot descriptor flags
 
 struct Params {
     StepHeader *hdr;
@@ -151,22 +153,6 @@ __device__ __forceinline__ uint32_t opaque(uint32_t v)
     uint32_t r;
     asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
     return r;
-}
-
-// Lane 0 (predicated, no branch): descriptor of the slot, then the segment's
-// bytes, completing on the slot's barrier.
-__device__ __forceinline__ void issue_segment(bool leader, uint32_t dslot, int4 d, uint32_t bar, uint32_t dst,
-                                              const uint8_t *src)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %0, 0;\n\t"
-        "@p st.shared.v4.s32 [%1], {%2, %3, %4, %5};\n\t"
-        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%6], %7;\n\t"
-        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%8], [%9], %7, [%6];\n\t"
-        "}" ::"r"(leader ? 1u : 0u),
-        "r"(dslot), "r"(d.x), "r"(d.y), "r"(d.z), "r"(d.w), "r"(bar), "r"(uint32_t(kSegBytes)), "r"(dst), "l"(src)
-        : "memory");
 }
 
 // One segment into the lane's accumulators. MT tokens per pass: the 8 MMA
@@ -317,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                         ok = 0;
                         break;
                     }
-                    __nanosleep(64);
+                    __nanosleep(256);
                 }
             }
             if (lane == 0) {
@@ -331,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                             ok = 0;
                             break;
                         }
-                        __nanosleep(64);
+                        __nanosleep(128);
                     }
                 }
                 // the buffer's previous fill (job j - nb) has landed before its
@@ -419,22 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         }
         const uint32_t ex = opaque(sbase + L.xwin + uint32_t(mtok * p.xrow) - z0);   // + buffer * xbuf_bytes + 512 sg
 
-        // the issue cursor (identical in every lane)
-        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1;
+        // The issue cursor, the same in every lane: the tile whose segments
+        // are being copied (job ijob, tile itile, next segment isg of iS) and
+        // the tile reserved after it (its index only in lane 0's `nt`, read
+        // when it is needed, so that the atomic's latency is never waited on).
+        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1, islot = 0;
         const uint8_t *iptr = nullptr;
-        bool ihave = false, iend = false, has_next = false;
-        unsigned next_tile = 0;
-        int issued = 0, islot = 0;
-        auto grab = [&]() {
-            unsigned g;
-            if (has_next) {
-                g = next_tile;
-                has_next = false;
-            } else {
-                unsigned v = 0;
-                if (leader) v = atomicAdd(&p.hdr->next_tile, 1u);
-                g = __shfl_sync(0xffffffffu, v, 0);
-            }
+        bool ihave = false, iend = false, reserved = false;
+        unsigned nt = 0;
+        auto next_tile = [&]() {                      // the next tile into the cursor, or the end
+            if (!reserved && leader) nt = atomicAdd(&p.hdr->next_tile, 1u);
+            reserved = false;
+            const unsigned g = __shfl_sync(0xffffffffu, nt, 0);
             if (g >= unsigned(p.total_tiles)) {
                 iend = true;
                 return;
@@ -447,41 +429,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             iptr = job(fj).seg + size_t(itile) * size_t(iS) * kSegBytes;
             ihave = true;
         };
+        // copy the cursor's next segment into slot islot (lane 0; the
+        // descriptor tells the consumer the job, the tile and where it starts
+        // and ends); false when no tile is left
+        auto issue_next = [&]() -> bool {
+            if (!ihave) {
+                if (iend) return false;
+                next_tile();
+                if (iend) return false;
+            }
+            if (!reserved && isg == (iS >> 1)) {       // the tile after this one, half a tile ahead
+                if (leader) nt = atomicAdd(&p.hdr->next_tile, 1u);
+                reserved = true;
+            }
+            const uint32_t bar = bars + 8 * islot, dsc = descs + 16 * islot;
+            const int flags = (isg == 0 ? kDescFirst : 0) | (isg == iS - 1 ? kDescLast : 0);
+            if (leader) {
+                asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(dsc), "r"(ijob), "r"(itile), "r"(flags),
+                             "r"(0)
+                             : "memory");
+                mbar_arrive_expect_tx(bar, kSegBytes);
+                bulk_load(ring + uint32_t(islot) * kSegBytes, iptr, kSegBytes, bar);
+            }
+            iptr += kSegBytes;
+            if (++isg == iS) ihave = false;
+            if (++islot == slots) islot = 0;
+            return true;
+        };
+
+        int in_flight = 0;
+        while (in_flight < slots && issue_next()) ++in_flight;
 
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        int consumed = 0, cslot = 0, cjob = -1;
+        int cslot = 0, cjob = -1;
         uint32_t cphase = 0, E = 0;
         bool ok = true;
-        for (;;) {
-            // refill: the free slots of the ring, in sequence order
-            while (issued - consumed < slots) {
-                if (!ihave) {
-                    if (iend) break;
-                    grab();
-                    if (iend) break;
-                    if (issued == consumed && leader) st_release_cta_s32(my_wjob, ijob);   // holding nothing else
-                }
-                if (!has_next && isg == (iS >> 1)) {      // the next tile, half a tile ahead
-                    unsigned v = 0;
-                    if (leader) v = atomicAdd(&p.hdr->next_tile, 1u);
-                    next_tile = __shfl_sync(0xffffffffu, v, 0);
-                    has_next = true;
-                }
-                issue_segment(leader, descs + 16 * islot,
-                              make_int4(ijob, itile, (isg == 0 ? 1 : 0) | (isg == iS - 1 ? 2 : 0), 0),
-                              bars + 8 * islot, ring + uint32_t(islot) * kSegBytes, iptr);
-                iptr += kSegBytes;
-                ++issued;
-                if (++islot == slots) islot = 0;
-                if (++isg == iS) ihave = false;
-            }
-            if (issued == consumed) break;                  // no tile left
+        while (in_flight > 0) {
             if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * cslot, cphase))) {
                 ok = false;
                 break;
             }
             const int4 d = lds_s4(descs + 16 * cslot);
-            if (d.z & 1) {
+            if (d.z & kDescFirst) {
                 // a tile starts: its job's x in the window (staged once per CTA)
                 const int b = d.x % nb;
                 if (d.x != cjob) {
@@ -506,13 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
             }
-            const uint32_t cb = ring + uint32_t(cslot) * kSegBytes;
-            segment<MT>(cb, aoff, soff, E, mk, ka, acc);
+            segment<MT>(ring + uint32_t(cslot) * kSegBytes, aoff, soff, E, mk, ka, acc);
             E += 512;
-            // every lane's reads of the slot are done before lane 0 refills it
+            // every lane's reads of the slot (generic proxy) are done before
+            // lane 0's copy (async proxy) refills it
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (d.z & 2) {
+            if (!issue_next()) --in_flight;
+            if (d.z & kDescLast) {
                 const StepJob &jb = job(d.x);
                 finish_tile<MT>(acc, jb, d.y * 16, lane, M);
                 if (jb.flags & kStepPublish) {
@@ -520,18 +510,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                     if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
                 }
             }
-            ++consumed;
             if (++cslot == slots) {
                 cslot = 0;
                 cphase ^= 1u;
             }
         }
         if (!ok && leader) fail(p, s_abort);
-        // the copies still in flight (only after a failed wait) land before the CTA exits
-        if (leader)
-            for (int c = consumed; c < issued; ++c) {
-                const int s = c % slots;
-                if (!mbar_wait(bars + 8 * s, uint32_t((c / slots) & 1))) break;
+        // after a failed wait: the copies still in flight land before the CTA exits
+        if (!ok && leader)
+            for (int c = 0; c < in_flight; ++c) {
+                const int s = (cslot + c) % slots;
+                if (!mbar_wait(bars + 8 * s, cphase ^ (cslot + c >= slots ? 1u : 0u))) break;
             }
         __syncwarp();
         if (leader) {
