@@ -452,6 +452,7 @@ typedef struct zq4_stack_plan {
     int tiles;
     int n_pub;
     int gen;
+    int min_k;
 } zq4_stack_plan;
 
 /*
@@ -470,7 +471,9 @@ ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, i
  * within that, a job that would wait for a job run shortly before it lets
  * later jobs that conflict with nothing still to run go first, until the
  * job it waits for is followed by its own work and twice 152 x 12 of its
- * 16-row tiles' worth of other work (a constant, the same on any device).
+ * 16-row tiles' worth of other work (a constant, the same on any device);
+ * when some job waits, the largest job that conflicts with no other job runs
+ * last.
  *   order[r] = the index (in `jobs`) of the r-th job run;
  *   dep[i]   = the last job run before job i that conflicts with it, or -1:
  *              it is finished before any part of job i starts.

@@ -835,8 +835,23 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, con
             if (placed[i] && conflict(jobs[i], jobs[j], M)) sh = std::max(sh, need[i] - (total - at[i]));
         return sh;
     };
+    // the largest job that touches no other job's bytes runs last: whatever
+    // it waits for, it can fill the end of the step with its tiles while the
+    // last waiting jobs finish
+    // (only when some job waits at all)
+    int last = -1;
+    bool any_wait = false;
+    for (int j = 0; j < n; ++j) {
+        bool alone = true;
+        for (int i = 0; i < n && alone; ++i)
+            if (i != j && conflict(jobs[i], jobs[j], M)) alone = false;
+        any_wait |= !alone;
+        if (alone && (last < 0 || work[j] > work[last])) last = j;
+    }
+    if (!any_wait) last = -1;
+    if (n > 1 && last >= 0) placed[last] = 1;
     int first = 0;
-    while (n_placed < n) {
+    while (n_placed < n - (n > 1 && last >= 0 ? 1 : 0)) {
         while (placed[first]) ++first;
         int pick = first;
         if (short_by(first) > 0) {
@@ -855,6 +870,11 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, con
         total += work[pick];
         at[pick] = total;
         order[n_placed++] = pick;
+    }
+    if (n_placed < n) {
+        total += work[last];
+        at[last] = total;
+        order[n_placed++] = last;
     }
     for (int r = 0; r < n; ++r) {
         int q = r - 1;
@@ -1067,9 +1087,12 @@ zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t
 
 namespace {
 
-void fill_plan(zq4_stack_plan *plan, void *dev, int engine, int n_jobs, int M, int grid, int mk, int mt,
-               long long tiles, int n_pub, int gen)
+void fill_plan(zq4_stack_plan *plan, const zq4_stack_job *jobs, void *dev, int engine, int n_jobs, int M, int grid,
+               int mk, int mt, long long tiles, int n_pub, int gen)
 {
+    int min_k = mk;
+    for (int j = 0; j < n_jobs; ++j) min_k = std::min(min_k, jobs[j].K);
+    plan->min_k = min_k;
     plan->dev = dev;
     plan->bytes = plan_bytes_for(engine, n_jobs);
     plan->n_jobs = n_jobs;
@@ -1109,7 +1132,7 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     cudaError_t e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e);
-    fill_plan(plan, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, 0);
+    fill_plan(plan, jobs, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, 0);
     return ZQ4_OK;
 }
 
@@ -1196,7 +1219,7 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e);
     const int gen = g_static_gen[d].fetch_add(1) + 1;
-    fill_plan(plan, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, gen);
+    fill_plan(plan, jobs, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, gen);
     return ZQ4_OK;
 }
 

@@ -11,8 +11,8 @@
 // How:
 //  * Work unit = a tile (16 weight rows x all K columns); the jobs' tiles
 //    form one sequence in run order, and each compute warp takes the next
-//    tile from a device counter (one atomic add per tile, a tile ahead of
-//    need). A warp computes a whole tile, so no partial sum ever leaves
+//    tile from a device counter (one atomic add per tile, half a tile
+//    ahead of need). A warp computes a whole tile, so no partial sum ever leaves
 //    its registers and no warp waits for another at a job boundary; a slow
 //    SM simply takes fewer tiles.
 //  * Each compute warp streams its segments (16 rows x 256 columns of the
@@ -23,10 +23,11 @@
 //    warp without a hand-off; the slot's descriptor (job, tile, first/last)
 //    travels with it.
 //  * x of every job is brought into shared memory once per CTA, by a stager
-//    warp, into a window of a few buffers (job j in buffer j mod NB): one
-//    bulk copy per token, issued once the job's waits are met and once no
-//    compute warp of the CTA can still need the job that held the buffer
-//    (each warp publishes a lower bound of the jobs it will still read).
+//    warp, into a window of a few buffers: one bulk copy per token, issued
+//    once the job's waits are met, into any buffer whose job no compute warp
+//    of the CTA can still read (each warp publishes the job it is reading
+//    and a lower bound of the jobs it will read after it, so a warp busy
+//    with a long tile holds one buffer, not the window).
 //  * Inner loop, one token (the MMA's 8 columns would otherwise hold 1
 //    useful token): column c of the m16n8k16 accumulator collects group c
 //    of the segment (a block-diagonal B: lanes of column c read x of group
@@ -86,11 +87,12 @@ struct Params {
     const StepJob *jobs;
     unsigned *job_done;      // [n_jobs]: tiles finished (monotone across launches)
     int n_jobs, total_tiles, M, slots, nb, xrow, cached, n_pub;
+    int fine;                // every job's tile is at least `slots` segments long
 };
 
 // Shared-memory layout (bytes from a 128-byte aligned base).
 struct Smem {
-    uint32_t ring, bars, desc, xbar, xtag, wjob, misc, zero, xwin, cta_done, cta_pub, cta_snap, jobs, total;
+    uint32_t ring, bars, desc, xbar, xtag, xpar, wcur, wlb, misc, zero, xwin, cta_done, cta_pub, cta_snap, jobs, total;
     __host__ __device__ Smem(int M, int slots, int nb, int xrow, int n_pub, int cached)
     {
         ring = 0;
@@ -98,8 +100,10 @@ struct Smem {
         desc = bars + uint32_t(kWarps * slots) * 8;
         xbar = desc + uint32_t(kWarps * slots) * 16;
         xtag = xbar + uint32_t(nb) * 8;
-        wjob = xtag + uint32_t(nb) * 4;
-        misc = wjob + kWarps * 4;
+        xpar = xtag + uint32_t(nb) * 4;
+        wcur = xpar + uint32_t(nb) * 4;
+        wlb = wcur + kWarps * 4;
+        misc = wlb + kWarps * 4;
         zero = (misc + 64 + 127) / 128 * 128;
         xwin = zero + 128;
         cta_done = xwin + uint32_t(nb) * uint32_t(M) * uint32_t(xrow);
@@ -255,8 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 
     for (int i = threadIdx.x; i < 32; i += kThreads) reinterpret_cast<uint32_t *>(smem + L.zero)[i] = 0;
     for (int i = threadIdx.x; i < p.n_pub; i += kThreads) cta_done[i] = cta_pub[i] = 0;
-    for (int i = threadIdx.x; i < kWarps; i += kThreads) reinterpret_cast<int *>(smem + L.wjob)[i] = 0;
-    for (int i = threadIdx.x; i < nb; i += kThreads) reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
+    for (int i = threadIdx.x; i < kWarps; i += kThreads) {
+        reinterpret_cast<int *>(smem + L.wcur)[i] = -1;      // no job being read yet
+        reinterpret_cast<int *>(smem + L.wlb)[i] = 0;        // every job may still be read
+    }
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
+        reinterpret_cast<int *>(smem + L.xpar)[i] = 0;
+    }
     if (threadIdx.x == 0) {
         *s_abort = 0;
         *reinterpret_cast<int *>(smem + L.misc + 4) = 0;
@@ -281,49 +291,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 
     if (warp == kStagerWarp) {
         // ---------------- the x stager ----------------
-        // x of job j into buffer j % nb, in job order: once no compute warp
-        // of this CTA can still read the job that held the buffer, and once
-        // the job's waits are met (the data it reads is final).
-        const uint32_t wjob0 = sbase + L.wjob;
+        // x of job j, in job order, into a buffer of the window whose job no
+        // compute warp of this CTA can still read (warp w reads its current
+        // job cur[w] and, after it, only jobs >= lb[w]; a buffer never used
+        // is free), once the job's waits are met (the data it reads is final).
+        // The buffer's tag (the job it holds) and the parity of its fill are
+        // published when the copy is issued; readers wait on the barrier.
+        const uint32_t cur0 = sbase + L.wcur, lb0 = sbase + L.wlb;
+        int *xtag = reinterpret_cast<int *>(smem + L.xtag);
+        int *xpar = reinterpret_cast<int *>(smem + L.xpar);
         int j = 0;
         for (; j < n; ++j) {
             if (__shfl_sync(0xffffffffu, *s_abort, 0)) break;
-            const int b = j % nb;
             const StepJob &jb = job(j);
-            int ok = 1;
-            if (j >= nb) {
-                // every lane reads one warp's bound; lane 0 alone decides to give up
-                const unsigned long long t0 = globaltimer();
-                for (;;) {
-                    const int wj = lane < kWarps ? ld_acquire_cta_s32(wjob0 + 4 * lane) : 0x7fffffff;
-                    if (__all_sync(0xffffffffu, wj > j - nb)) break;
-                    int stop = 0;
-                    if (lane == 0) stop = *s_abort || globaltimer() - t0 > kWaitLimitNs;
-                    if (__shfl_sync(0xffffffffu, stop, 0)) {
-                        ok = 0;
+            int ok = 1, b = -1;
+            const unsigned long long t0 = globaltimer();
+            for (;;) {
+                const int wc = lane < kWarps ? ld_acquire_cta_s32(cur0 + 4 * lane) : -1;
+                int wl = lane < kWarps ? ld_acquire_cta_s32(lb0 + 4 * lane) : 0x7fffffff;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) wl = min(wl, __shfl_xor_sync(0xffffffffu, wl, o));
+                int best_job = 0x7fffffff;
+                for (int c = 0; c < nb; ++c) {
+                    const int k = xtag[c];
+                    const bool busy = __any_sync(0xffffffffu, lane < kWarps && wc == k);
+                    if (k < 0) {                           // never filled
+                        b = c;
                         break;
                     }
-                    __nanosleep(256);
+                    if (!busy && k < wl && k < best_job) {  // the oldest job nobody still reads
+                        b = c;
+                        best_job = k;
+                    }
                 }
+                if (b >= 0) break;
+                int stop = 0;
+                if (lane == 0) stop = *s_abort || globaltimer() - t0 > kWaitLimitNs;
+                if (__shfl_sync(0xffffffffu, stop, 0)) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(256);
             }
-            if (lane == 0) {
+            if (lane == 0 && ok) {
                 for (int w = 0; ok && w < jb.nwait; ++w) {
                     const int d = jb.wait[w];
                     const unsigned target = done_mul * unsigned(job(d).T);
-                    const unsigned long long t0 = globaltimer();
+                    const unsigned long long t1 = globaltimer();
                     while (!reached(ld_acquire_gpu(&p.job_done[d]), target)) {
                         if (*s_abort || *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
-                            globaltimer() - t0 > kWaitLimitNs) {
+                            globaltimer() - t1 > kWaitLimitNs) {
                             ok = 0;
                             break;
                         }
                         __nanosleep(128);
                     }
                 }
-                // the buffer's previous fill (job j - nb) has landed before its
-                // barrier is armed again: no compute warp of this CTA may
-                // have waited for it (the CTA can have had no tile of it)
-                if (ok && j >= nb && !mbar_wait(sbase + L.xbar + 8 * b, uint32_t(((j - nb) / nb) & 1))) ok = 0;
+                // the buffer's previous fill has landed before its barrier is
+                // armed again (no compute warp of this CTA may have waited for
+                // it: the CTA can have had no tile of that job)
+                const bool used = xtag[b] >= 0;
+                if (ok && used && !mbar_wait(sbase + L.xbar + 8 * b, uint32_t(xpar[b]))) ok = 0;
                 if (!ok) {
                     fail(p, s_abort);
                 } else {
@@ -332,18 +360,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     const uint32_t bar = sbase + L.xbar + 8 * b, dst = sbase + L.xwin + uint32_t(b) * xbuf_bytes;
+                    xpar[b] = used ? (xpar[b] ^ 1) : 0;      // the phase this fill completes
                     mbar_arrive_expect_tx(bar, uint32_t(M * jb.K * 2));
                     for (int m = 0; m < M; ++m)
                         bulk_load(dst + uint32_t(m * p.xrow), jb.x + size_t(m) * jb.K, uint32_t(jb.K * 2), bar);
                     st_release_cta_s32(sbase + L.xtag + 4 * b, j);
                 }
             }
+            __syncwarp();
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
         // the last fill of every buffer has landed before the CTA may exit
         if (lane == 0)
-            for (int c = max(0, j - nb); c < j; ++c)
-                if (!mbar_wait(sbase + L.xbar + 8 * (c % nb), uint32_t((c / nb) & 1))) break;
+            for (int c = 0; c < nb; ++c)
+                if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xpar[c]))) break;
     } else if (warp == kPubWarp) {
         // ---------------- the publisher ----------------
         // Makes this CTA's finished tiles of the waited-for jobs visible to
@@ -387,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         const uint32_t ring = sbase + L.ring + uint32_t(warp * slots) * kSegBytes;
         const uint32_t bars = sbase + L.bars + uint32_t(8 * warp * slots);
         const uint32_t descs = sbase + L.desc + uint32_t(16 * warp * slots);
-        const uint32_t my_wjob = sbase + L.wjob + 4 * warp;
+        const uint32_t my_cur = sbase + L.wcur + 4 * warp, my_lb = sbase + L.wlb + 4 * warp;
         const uint32_t aoff = opaque(segk::lane_code_offset(lane));
         const uint32_t soff = opaque(uint32_t(r * 144 + 128 + 2 * ((2 * t) % GP)));
         // x addresses: lane column r is token r / GP, group slot r % GP; the
@@ -428,6 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             iS = job(fj).K >> 8;
             iptr = job(fj).seg + size_t(itile) * size_t(iS) * kSegBytes;
             ihave = true;
+            // every job the warp reads after its current one is >= this one's
+            // (valid when every job's tile is at least a ring long: the tile
+            // issued before this one has started to be read)
+            if (p.fine && leader) st_release_cta_s32(my_lb, ijob);
         };
         // copy the cursor's next segment into slot islot (lane 0; the
         // descriptor tells the consumer the job, the tile and where it starts
@@ -461,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         while (in_flight < slots && issue_next()) ++in_flight;
 
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        int cslot = 0, cjob = -1;
+        int cslot = 0, cjob = -1, cbuf = 0;
         uint32_t cphase = 0, E = 0;
         bool ok = true;
         while (in_flight > 0) {
@@ -472,26 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             const int4 d = lds_s4(descs + 16 * cslot);
             if (d.z & kDescFirst) {
                 // a tile starts: its job's x in the window (staged once per CTA)
-                const int b = d.x % nb;
                 if (d.x != cjob) {
-                    if (leader) st_release_cta_s32(my_wjob, d.x);
+                    if (leader) {
+                        st_release_cta_s32(my_cur, d.x);
+                        if (!p.fine) st_release_cta_s32(my_lb, d.x);
+                    }
                     const unsigned long long t0 = globaltimer();
-                    bool ready = false;
+                    int found = -1;
                     for (;;) {
-                        if (ld_acquire_cta_s32(sbase + L.xtag + 4 * b) == d.x) {
-                            ready = true;
-                            break;
-                        }
+                        for (int c = 0; c < nb && found < 0; ++c)
+                            if (ld_acquire_cta_s32(sbase + L.xtag + 4 * c) == d.x) found = c;
+                        if (found >= 0) break;
                         if (*s_abort || globaltimer() - t0 > kWaitLimitNs) break;
                         __nanosleep(32);
                     }
-                    if (!__all_sync(0xffffffffu, ready && mbar_wait(sbase + L.xbar + 8 * b, uint32_t((d.x / nb) & 1)))) {
+                    const uint32_t par = found >= 0 ? uint32_t(lds_u32(sbase + L.xpar + 4 * found)) : 0u;
+                    if (!__all_sync(0xffffffffu, found >= 0 && mbar_wait(sbase + L.xbar + 8 * found, par))) {
                         ok = false;
                         break;
                     }
                     cjob = d.x;
+                    cbuf = found;
                 }
-                E = ex + uint32_t(b) * xbuf_bytes;
+                E = ex + uint32_t(cbuf) * xbuf_bytes;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
             }
@@ -524,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             }
         __syncwarp();
         if (leader) {
-            st_release_cta_s32(my_wjob, 0x7fffffff);            // reads no more x
+            st_release_cta_s32(my_cur, 0x7fffffff);             // reads no more x
+            st_release_cta_s32(my_lb, 0x7fffffff);
             red_release_cta(s_warps_done, 1u);
         }
     }
@@ -608,6 +646,7 @@ zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.nb = sh.nb;
     p.xrow = sh.xrow;
     p.cached = sh.cached;
+    p.fine = plan->max_k >= 0 && plan->min_k / 256 >= sh.slots ? 1 : 0;
     const void *kern = step_kernel(p.M);
     cudaError_t e = ensure_smem(kern, sh.smem, p.M == 1 ? step_smem_set : step_smem_set2);
     if (e != cudaSuccess) return cuda_status(e);

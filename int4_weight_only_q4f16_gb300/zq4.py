@@ -108,7 +108,8 @@ class StackPlanC(ctypes.Structure):
     _fields_ = [("dev", ctypes.c_void_p), ("bytes", ctypes.c_size_t), ("n_jobs", ctypes.c_int),
                 ("M", ctypes.c_int), ("grid", ctypes.c_int), ("max_k", ctypes.c_int),
                 ("max_tiles", ctypes.c_int), ("device", ctypes.c_int), ("engine", ctypes.c_int),
-                ("tiles", ctypes.c_int), ("n_pub", ctypes.c_int), ("gen", ctypes.c_int)]
+                ("tiles", ctypes.c_int), ("n_pub", ctypes.c_int), ("gen", ctypes.c_int),
+                ("min_k", ctypes.c_int)]
 
 
 lib = _load()

@@ -72,11 +72,12 @@ def test_mixed_job_list(zq4):
 
 
 def test_an_independent_job_passes_a_waiting_one(zq4):
-    # job 1 reads job 0's output; job 2 touches neither: it runs in between
+    # job 1 reads job 0's output; jobs 2 and 3 touch no other job: the
+    # largest of those (3) runs last, the other runs between 0 and 1
     jobs = [(W, buf(0), buf(1), 16384, 3072, 0), (W, buf(1), buf(2), 3072, 16384, 0),
-            (W, buf(3), buf(4), 3072, 3072, 0)]
+            (W, buf(3), buf(4), 3072, 3072, 0), (W, buf(5), buf(6), 32064, 3072, 0)]
     for M in (1, 2):
-        assert zq4.stack_plan_waits(jobs, M) == ([0, 2, 1], [-1, 0, -1])
+        assert zq4.stack_plan_waits(jobs, M) == ([0, 2, 1, 3], [-1, 0, -1, -1])
 
 
 def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
@@ -90,8 +91,9 @@ def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
     order, dep = zq4.stack_plan_waits(jobs, 1)
     # down of layer l waits for its gate_up; it is put after at least
     # 2 x 152 x 12 tiles' worth of that gate_up's segments (43,776): the next
-    # two layers' qkv, o and gate_up (or, at the end, the head)
-    assert order == [0, 1, 2, 4, 5, 6, 8, 9, 10, 12, 3, 7, 11]
+    # two layers' qkv, o and gate_up where there are any; the head, which
+    # touches no other job's bytes and is the largest such job, runs last
+    assert order == [0, 1, 2, 4, 5, 6, 8, 9, 10, 3, 7, 11, 12]
     assert dep == [-1, -1, -1, 2, -1, -1, -1, 6, -1, -1, -1, 10, -1]
     check_valid(jobs, 1, order, dep)
 
