@@ -80,33 +80,40 @@ constexpr int kWarps = kStepWarps;         // compute warps, one ring each
 constexpr int kStagerWarp = kWarps;
 constexpr int kPubWarp = kWarps + 1;
 constexpr int kThreads = kWarps * 32 + 64;
-constexpr int kDescFirst = 1, kDescLast = 2;   // slot descriptor flags
 
 struct Params {
     StepHeader *hdr;
     const StepJob *jobs;
     unsigned *job_done;      // [n_jobs]: tiles finished (monotone across launches)
-    int n_jobs, total_tiles, M, slots, nb, xrow, cached, n_pub;
+    int n_jobs, total_tiles, M, slots, wbytes, cached, n_pub;
     int fine;                // every job's tile is at least `slots` segments long
 };
 
+// x window entries: job j's x is described by entry j % kEntries (barrier,
+// published tag, and the stager's record of the bytes it took)
+constexpr int kEntries = 32;
+// tag word of an entry: job << 12 | (offset / 128) << 1 | parity of the fill
+constexpr int kTagJobShift = 12;
+
 // Shared-memory layout (bytes from a 128-byte aligned base).
 struct Smem {
-    uint32_t ring, bars, desc, xbar, xtag, xpar, wcur, wlb, misc, zero, xwin, cta_done, cta_pub, cta_snap, jobs, total;
-    __host__ __device__ Smem(int M, int slots, int nb, int xrow, int n_pub, int cached)
+    uint32_t ring, bars, desc, xbar, xtag, xstart, xtotal, wcur, wlb, misc, zero, xwin, cta_done, cta_pub, cta_snap,
+        jobs, total;
+    __host__ __device__ Smem(int slots, int wbytes, int n_pub, int cached)
     {
         ring = 0;
         bars = ring + uint32_t(kWarps * slots) * kSegBytes;
         desc = bars + uint32_t(kWarps * slots) * 8;
         xbar = desc + uint32_t(kWarps * slots) * 16;
-        xtag = xbar + uint32_t(nb) * 8;
-        xpar = xtag + uint32_t(nb) * 4;
-        wcur = xpar + uint32_t(nb) * 4;
+        xtag = xbar + kEntries * 8;
+        xstart = xtag + kEntries * 4;
+        xtotal = xstart + kEntries * 4;
+        wcur = xtotal + kEntries * 4;
         wlb = wcur + kWarps * 4;
         misc = wlb + kWarps * 4;
         zero = (misc + 64 + 127) / 128 * 128;
         xwin = zero + 128;
-        cta_done = xwin + uint32_t(nb) * uint32_t(M) * uint32_t(xrow);
+        cta_done = xwin + uint32_t(wbytes);
         cta_pub = cta_done + uint32_t(n_pub) * 4;
         cta_snap = cta_pub + uint32_t(n_pub) * 4;
         jobs = (cta_snap + uint32_t(n_pub) * 4 + 15) / 16 * 16;
@@ -245,10 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
     const uint32_t sbase = smem_addr(smem);
-    const Smem L(p.M, p.slots, p.nb, p.xrow, p.n_pub, p.cached);
+    const Smem L(p.slots, p.wbytes, p.n_pub, p.cached);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = p.n_jobs, M = p.M, slots = p.slots, nb = p.nb;
-    const uint32_t xbuf_bytes = uint32_t(M * p.xrow);
+    const int n = p.n_jobs, M = p.M, slots = p.slots;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc);
     const uint32_t s_warps_done = sbase + L.misc + 4;
     unsigned *cta_done = reinterpret_cast<unsigned *>(smem + L.cta_done);
@@ -263,10 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         reinterpret_cast<int *>(smem + L.wcur)[i] = -1;      // no job being read yet
         reinterpret_cast<int *>(smem + L.wlb)[i] = 0;        // every job may still be read
     }
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-        reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
-        reinterpret_cast<int *>(smem + L.xpar)[i] = 0;
-    }
+    for (int i = threadIdx.x; i < kEntries; i += kThreads) reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
     if (threadIdx.x == 0) {
         *s_abort = 0;
         *reinterpret_cast<int *>(smem + L.misc + 4) = 0;
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kStagerWarp && lane == 0) {
-        for (int b = 0; b < nb; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
+        for (int b = 0; b < kEntries; ++b) mbar_init(sbase + L.xbar + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -291,40 +294,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 
     if (warp == kStagerWarp) {
         // ---------------- the x stager ----------------
-        // x of job j, in job order, into a buffer of the window whose job no
-        // compute warp of this CTA can still read (warp w reads its current
-        // job cur[w] and, after it, only jobs >= lb[w]; a buffer never used
-        // is free), once the job's waits are met (the data it reads is final).
-        // The buffer's tag (the job it holds) and the parity of its fill are
-        // published when the copy is issued; readers wait on the barrier.
-        const uint32_t cur0 = sbase + L.wcur, lb0 = sbase + L.wlb;
+        // x of every job, in job order, into a byte ring (the window): job j
+        // takes M * K_j * 2 bytes (128-byte aligned) at the ring's head, and
+        // the oldest jobs give their bytes back once no compute warp of this
+        // CTA can still read them (warp w reads its current job cur[w] and,
+        // after it, only jobs >= lb[w]). A job's x is copied once its waits
+        // are met (the data it reads is final). Entry j % kEntries holds the
+        // job's barrier and tag (job, offset, parity of the fill), published
+        // when the copy is issued; readers wait on the barrier. The ring
+        // state (head, tail, bytes used) is the same in every lane.
+        const uint32_t lb0 = sbase + L.wlb;
+        const uint32_t W = uint32_t(p.wbytes);
         int *xtag = reinterpret_cast<int *>(smem + L.xtag);
-        int *xpar = reinterpret_cast<int *>(smem + L.xpar);
+        uint32_t *xstart = reinterpret_cast<uint32_t *>(smem + L.xstart);
+        uint32_t *xtotal = reinterpret_cast<uint32_t *>(smem + L.xtotal);
+        uint32_t head = 0, tail = 0, used = 0;
+        int oldest = 0;                                      // the oldest job still holding bytes
         int j = 0;
         for (; j < n; ++j) {
             if (__shfl_sync(0xffffffffu, *s_abort, 0)) break;
             const StepJob &jb = job(j);
-            int ok = 1, b = -1;
+            const uint32_t size = (uint32_t(M * jb.K * 2) + 127u) & ~127u;
+            const int e = j % kEntries;
+            int ok = 1;
+            uint32_t off = 0;
             const unsigned long long t0 = globaltimer();
             for (;;) {
-                const int wc = lane < kWarps ? ld_acquire_cta_s32(cur0 + 4 * lane) : -1;
+                // give back the bytes of the oldest jobs nobody reads any more:
+                // the bound first (acquire), then the current job (a warp
+                // stores its current job before it raises its bound)
                 int wl = lane < kWarps ? ld_acquire_cta_s32(lb0 + 4 * lane) : 0x7fffffff;
+                const int wc = lane < kWarps ? *reinterpret_cast<volatile int *>(smem + L.wcur + 4 * lane) : -1;
 #pragma unroll
                 for (int o = 16; o; o >>= 1) wl = min(wl, __shfl_xor_sync(0xffffffffu, wl, o));
-                int best_job = 0x7fffffff;
-                for (int c = 0; c < nb; ++c) {
-                    const int k = xtag[c];
-                    const bool busy = __any_sync(0xffffffffu, lane < kWarps && wc == k);
-                    if (k < 0) {                           // never filled
-                        b = c;
-                        break;
-                    }
-                    if (!busy && k < wl && k < best_job) {  // the oldest job nobody still reads
-                        b = c;
-                        best_job = k;
+                while (oldest < j && oldest < wl && !__any_sync(0xffffffffu, lane < kWarps && wc == oldest)) {
+                    const int oe = oldest % kEntries;
+                    used -= xtotal[oe];
+                    tail = xstart[oe] + xtotal[oe];
+                    if (tail >= W) tail -= W;
+                    ++oldest;
+                }
+                if (used == 0) head = tail = 0;
+                // room at the head (wrapping to 0 wastes the end of the ring),
+                // and the entry's previous job has given its bytes back
+                bool room = false;
+                uint32_t start = head, total = size;
+                if (j - oldest < kEntries) {
+                    if (used == 0) {                             // empty (head = tail = 0)
+                        room = size <= W;
+                        off = 0;
+                    } else if (tail < head) {                    // data in [tail, head)
+                        if (head + size <= W) {
+                            room = true;
+                            off = head;
+                        } else if (size <= tail) {
+                            room = true;
+                            off = 0;
+                            total = W - head + size;
+                        }
+                    } else if (head + size <= tail) {            // data in [tail, W) and [0, head); full if equal
+                        room = true;
+                        off = head;
                     }
                 }
-                if (b >= 0) break;
+                if (room) {
+                    xstart[e] = start;                       // every lane writes the same values
+                    xtotal[e] = total;
+                    used += total;
+                    head = off + size;
+                    if (head >= W) head = 0;
+                    break;
+                }
                 int stop = 0;
                 if (lane == 0) stop = *s_abort || globaltimer() - t0 > kWaitLimitNs;
                 if (__shfl_sync(0xffffffffu, stop, 0)) {
@@ -347,33 +387,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                         __nanosleep(128);
                     }
                 }
-                // the buffer's previous fill has landed before its barrier is
+                // the entry's previous fill has landed before its barrier is
                 // armed again (no compute warp of this CTA may have waited for
                 // it: the CTA can have had no tile of that job)
-                const bool used = xtag[b] >= 0;
-                if (ok && used && !mbar_wait(sbase + L.xbar + 8 * b, uint32_t(xpar[b]))) ok = 0;
+                const bool used_e = xtag[e] >= 0;
+                if (ok && used_e && !mbar_wait(sbase + L.xbar + 8 * e, uint32_t(xtag[e] & 1))) ok = 0;
                 if (!ok) {
                     fail(p, s_abort);
                 } else {
-                    // the buffer's last readers (generic proxy) and the data's
+                    // the window's last readers (generic proxy) and the data's
                     // writers are ordered before the copy (async proxy)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     asm volatile("fence.proxy.async.global;" ::: "memory");
-                    const uint32_t bar = sbase + L.xbar + 8 * b, dst = sbase + L.xwin + uint32_t(b) * xbuf_bytes;
-                    xpar[b] = used ? (xpar[b] ^ 1) : 0;      // the phase this fill completes
+                    const uint32_t bar = sbase + L.xbar + 8 * e, dst = sbase + L.xwin + off;
+                    const int par = used_e ? ((xtag[e] & 1) ^ 1) : 0;   // the phase this fill completes
                     mbar_arrive_expect_tx(bar, uint32_t(M * jb.K * 2));
                     for (int m = 0; m < M; ++m)
-                        bulk_load(dst + uint32_t(m * p.xrow), jb.x + size_t(m) * jb.K, uint32_t(jb.K * 2), bar);
-                    st_release_cta_s32(sbase + L.xtag + 4 * b, j);
+                        bulk_load(dst + uint32_t(m * jb.K * 2), jb.x + size_t(m) * jb.K, uint32_t(jb.K * 2), bar);
+                    // job, offset and parity in one word: a reader that sees
+                    // the job waits for that phase on the barrier, which orders
+                    // the data
+                    *reinterpret_cast<volatile int *>(xtag + e) =
+                        (j << kTagJobShift) | int((off >> 7) << 1) | par;
                 }
             }
             __syncwarp();
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
-        // the last fill of every buffer has landed before the CTA may exit
+        // the last fill of every entry has landed before the CTA may exit
         if (lane == 0)
-            for (int c = 0; c < nb; ++c)
-                if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xpar[c]))) break;
+            for (int c = 0; c < kEntries; ++c)
+                if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xtag[c] & 1))) break;
     } else if (warp == kPubWarp) {
         // ---------------- the publisher ----------------
         // Makes this CTA's finished tiles of the waited-for jobs visible to
@@ -433,18 +477,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             mk[g] = opaque(act ? 1u : 0u);
             ka[g] = opaque(z + 16 * t + (act ? uint32_t(64 * g) + z0 - z : 0u));
         }
-        const uint32_t ex = opaque(sbase + L.xwin + uint32_t(mtok * p.xrow) - z0);   // + buffer * xbuf_bytes + 512 sg
+        const uint32_t ex = opaque(sbase + L.xwin - z0);   // + the job's offset + token * K * 2 + 512 sg
 
         // The issue cursor, the same in every lane: the tile whose segments
         // are being copied (job ijob, tile itile, next segment isg of iS) and
         // the tile reserved after it (its index only in lane 0's `nt`, read
         // when it is needed, so that the atomic's latency is never waited on).
+        // Lane 0's copies and atomics are predicated, not branched around.
+        const uint32_t lead = leader ? 1u : 0u;
         int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1, islot = 0;
         const uint8_t *iptr = nullptr;
         bool ihave = false, iend = false, reserved = false;
         unsigned nt = 0;
+        unsigned *const ctr = &p.hdr->next_tile;
+        auto reserve = [&](uint32_t pred) {          // lane 0 (when pred): nt = next tile index
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p atom.global.add.u32 %0, [%2], 1;\n\t}"
+                         : "+r"(nt)
+                         : "r"(pred), "l"(ctr)
+                         : "memory");
+        };
         auto next_tile = [&]() {                      // the next tile into the cursor, or the end
-            if (!reserved && leader) nt = atomicAdd(&p.hdr->next_tile, 1u);
+            if (!reserved) reserve(lead);
             reserved = false;
             const unsigned g = __shfl_sync(0xffffffffu, nt, 0);
             if (g >= unsigned(p.total_tiles)) {
@@ -463,31 +516,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             // issued before this one has started to be read)
             if (p.fine && leader) st_release_cta_s32(my_lb, ijob);
         };
-        // copy the cursor's next segment into slot islot (lane 0; the
-        // descriptor tells the consumer the job, the tile and where it starts
-        // and ends); false when no tile is left
+        // copy the cursor's next segment into slot islot; the descriptor
+        // (job, tile, segment, segments in the tile) tells the consumer where
+        // a tile starts and ends. False when no tile is left.
         auto issue_next = [&]() -> bool {
             if (!ihave) {
                 if (iend) return false;
                 next_tile();
                 if (iend) return false;
             }
-            if (!reserved && isg == (iS >> 1)) {       // the tile after this one, half a tile ahead
-                if (leader) nt = atomicAdd(&p.hdr->next_tile, 1u);
-                reserved = true;
-            }
-            const uint32_t bar = bars + 8 * islot, dsc = descs + 16 * islot;
-            const int flags = (isg == 0 ? kDescFirst : 0) | (isg == iS - 1 ? kDescLast : 0);
-            if (leader) {
-                asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(dsc), "r"(ijob), "r"(itile), "r"(flags),
-                             "r"(0)
-                             : "memory");
-                mbar_arrive_expect_tx(bar, kSegBytes);
-                bulk_load(ring + uint32_t(islot) * kSegBytes, iptr, kSegBytes, bar);
-            }
+            const bool res = !reserved && isg == (iS >> 1);     // the tile after this one, half a tile ahead
+            reserve(res ? lead : 0u);
+            reserved |= res;
+            const uint32_t bar = bars + 8 * islot;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.u32 p, %0, 0;\n\t"
+                "@p st.shared.v4.s32 [%1], {%2, %3, %4, %5};\n\t"
+                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%6], %7;\n\t"
+                "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%8], [%9], %7, [%6];\n\t"
+                "}" ::"r"(lead),
+                "r"(descs + 16 * islot), "r"(ijob), "r"(itile), "r"(isg), "r"(iS), "r"(bar),
+                "r"(uint32_t(kSegBytes)), "r"(ring + uint32_t(islot) * kSegBytes), "l"(iptr)
+                : "memory");
             iptr += kSegBytes;
-            if (++isg == iS) ihave = false;
-            if (++islot == slots) islot = 0;
+            ihave = ++isg < iS;
+            islot = islot + 1 == slots ? 0 : islot + 1;
             return true;
         };
 
@@ -503,32 +557,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                 ok = false;
                 break;
             }
-            const int4 d = lds_s4(descs + 16 * cslot);
-            if (d.z & kDescFirst) {
+            const int4 d = lds_s4(descs + 16 * cslot);     // job, tile, segment, segments
+            if (d.z == 0) {
                 // a tile starts: its job's x in the window (staged once per CTA)
                 if (d.x != cjob) {
                     if (leader) {
-                        st_release_cta_s32(my_cur, d.x);
+                        *reinterpret_cast<volatile int *>(smem + L.wcur + 4 * warp) = d.x;
                         if (!p.fine) st_release_cta_s32(my_lb, d.x);
                     }
                     const unsigned long long t0 = globaltimer();
-                    int found = -1;
+                    const int e = d.x % kEntries;
+                    int v = -1;
                     for (;;) {
-                        for (int c = 0; c < nb && found < 0; ++c)
-                            if (ld_acquire_cta_s32(sbase + L.xtag + 4 * c) == d.x) found = c;
-                        if (found >= 0) break;
-                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) break;
+                        v = *reinterpret_cast<volatile int *>(smem + L.xtag + 4 * e);
+                        if (v >= 0 && (v >> kTagJobShift) == d.x) break;
+                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                            v = -1;
+                            break;
+                        }
                         __nanosleep(32);
                     }
-                    const uint32_t par = found >= 0 ? uint32_t(lds_u32(sbase + L.xpar + 4 * found)) : 0u;
-                    if (!__all_sync(0xffffffffu, found >= 0 && mbar_wait(sbase + L.xbar + 8 * found, par))) {
+                    if (!__all_sync(0xffffffffu, v >= 0 && mbar_wait(sbase + L.xbar + 8 * e, uint32_t(v & 1)))) {
                         ok = false;
                         break;
                     }
                     cjob = d.x;
-                    cbuf = found;
+                    cbuf = int(((uint32_t(v) >> 1) & 2047u) << 7) + mtok * job(d.x).K * 2;
                 }
-                E = ex + uint32_t(cbuf) * xbuf_bytes;
+                E = ex + uint32_t(cbuf);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
             }
@@ -539,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (!issue_next()) --in_flight;
-            if (d.z & kDescLast) {
+            if (d.z == d.w - 1) {
                 const StepJob &jb = job(d.x);
                 finish_tile<MT>(acc, jb, d.y * 16, lane, M);
                 if (jb.flags & kStepPublish) {
@@ -605,27 +661,31 @@ size_t step_plan_layout_bytes(int n_jobs)
     return StepLayout(n_jobs).total;
 }
 
-// Ring slots, x buffers and cached jobs of a launch: as many slots (5 down to
-// 3) as leave room for at least 3 x buffers (2 if nothing else fits), then as
-// many x buffers as fit (up to 6), then the job table.
+// Ring slots, x window and cached jobs of a launch: three slots per compute
+// warp (measured: a larger x window pays more than deeper rings), the job
+// table cached while it leaves the window room for eight of the largest jobs'
+// x, and the window every byte that is left (at most 256 KiB: the tag word
+// holds the offset in 128-byte units).
 bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh)
 {
     const size_t cap = size_t(227) * 1024 - 128;
-    const int xrow = (max_k * 2 + 127) / 128 * 128;
-    for (int min_nb = 3; min_nb >= 2; --min_nb)
-        for (int s = 5; s >= 3; --s) {
-            if (sp::Smem(M, s, min_nb, xrow, n_pub, 0).total > cap) continue;
-            int nb = min_nb;
-            while (nb < 6 && sp::Smem(M, s, nb + 1, xrow, n_pub, 0).total <= cap) ++nb;
-            const size_t base = sp::Smem(M, s, nb, xrow, n_pub, 0).total;
-            sh->slots = s;
-            sh->nb = nb;
-            sh->xrow = xrow;
-            sh->cached = int(std::min<size_t>(size_t(n_jobs), (cap - base) / sizeof(StepJob)));
-            sh->smem = sp::Smem(M, s, nb, xrow, n_pub, sh->cached).total + 128;
+    const size_t big = (size_t(M) * size_t(max_k) * 2 + 127) / 128 * 128;
+    const int slots = 3;
+    int cached = std::min(n_jobs, 256);
+    for (;;) {
+        const size_t fixed = sp::Smem(slots, 0, n_pub, cached).total;
+        size_t w = fixed < cap ? (cap - fixed) / 128 * 128 : 0;
+        w = std::min<size_t>(w, size_t(256) * 1024 - 128);
+        if (w >= 8 * big || cached == 0) {
+            if (w < big) return false;                  // one job's x would not fit
+            sh->slots = slots;
+            sh->wbytes = int(w);
+            sh->cached = cached;
+            sh->smem = sp::Smem(slots, int(w), n_pub, cached).total + 128;
             return true;
         }
-    return false;
+        cached = cached > 32 ? cached / 2 : 0;
+    }
 }
 
 zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
@@ -643,8 +703,7 @@ zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
     StepShape sh;
     if (!step_launch_shape(p.M, plan->max_k, p.n_jobs, p.n_pub, &sh)) return ZQ4_ERR_UNSUPPORTED;
     p.slots = sh.slots;
-    p.nb = sh.nb;
-    p.xrow = sh.xrow;
+    p.wbytes = sh.wbytes;
     p.cached = sh.cached;
     p.fine = plan->max_k >= 0 && plan->min_k / 256 >= sh.slots ? 1 : 0;
     const void *kern = step_kernel(p.M);

@@ -56,7 +56,7 @@ struct StepLayout {
 
 // zq4_step.cu
 struct StepShape {
-    int slots, nb, xrow, cached;
+    int slots, wbytes, cached;
     size_t smem;
 };
 size_t step_plan_layout_bytes(int n_jobs);
