@@ -470,7 +470,7 @@ ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, i
  * (y of one meets x or y of the other). Conflicting jobs keep their order;
  * within that, a job that would wait for a job run shortly before it lets
  * later jobs that conflict with nothing still to run go first, until the
- * job it waits for is followed by its own work and twice 152 x 12 of its
+ * job it waits for is followed by its own work and twice 152 x 16 of its
  * 16-row tiles' worth of other work (a constant, the same on any device);
  * when some job waits, the largest job that conflicts with no other job runs
  * last.

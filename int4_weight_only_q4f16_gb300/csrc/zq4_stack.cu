@@ -786,7 +786,7 @@ constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
 
 // Work (segments) to place between a job and a job that waits for it, beyond
 // the job's own work: two tiles per compute warp of a full GB300 (152 SMs x
-// 12 warps), so that in the step engine, where each warp takes tiles one at
+// 16 warps), so that in the step engine, where each warp takes tiles one at
 // a time, the last tiles of the job are done before the first tiles of the
 // waiting job are handed out. A constant, so the order does not depend on
 // the device (a smaller GPU only gets more room than it needs).

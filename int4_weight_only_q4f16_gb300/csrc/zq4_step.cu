@@ -661,7 +661,7 @@ size_t step_plan_layout_bytes(int n_jobs)
     return StepLayout(n_jobs).total;
 }
 
-// Ring slots, x window and cached jobs of a launch: three slots per compute
+// Ring slots, x window and cached jobs of a launch: two slots per compute
 // warp (measured: a larger x window pays more than deeper rings), the job
 // table cached while it leaves the window room for eight of the largest jobs'
 // x, and the window every byte that is left (at most 256 KiB: the tag word
@@ -670,7 +670,7 @@ bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh)
 {
     const size_t cap = size_t(227) * 1024 - 128;
     const size_t big = (size_t(M) * size_t(max_k) * 2 + 127) / 128 * 128;
-    const int slots = 3;
+    const int slots = 2;
     int cached = std::min(n_jobs, 256);
     for (;;) {
         const size_t fixed = sp::Smem(slots, 0, n_pub, cached).total;

@@ -12,7 +12,7 @@
 namespace zq4 {
 
 constexpr int kStepMaxM = 2;          // tokens the step engine handles
-constexpr int kStepWarps = 12;        // compute warps per CTA
+constexpr int kStepWarps = 16;        // compute warps per CTA
 constexpr int kStepMaxWaits = 3;      // jobs one job may wait for
 
 // StepJob::flags

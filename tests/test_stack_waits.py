@@ -63,7 +63,7 @@ def test_mixed_job_list(zq4):
     ]
     order, dep = zq4.stack_plan_waits(jobs, M)
     # every job here is small next to the room a waited-for job gets (its own
-    # work and 2 x 152 x 12 of its tiles' segments), so each wait is on a
+    # work and 2 x 152 x 16 of its tiles' segments), so each wait is on a
     # recent job for every job after it; the only job free of the jobs still
     # to place (3) itself waits for job 0: nothing moves forward
     assert order == list(range(8))
@@ -90,7 +90,7 @@ def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
     jobs.append((W, buf(99), buf(98), 32064, 3072, 0))
     order, dep = zq4.stack_plan_waits(jobs, 1)
     # down of layer l waits for its gate_up; it is put after at least
-    # 2 x 152 x 12 tiles' worth of that gate_up's segments (43,776): the next
+    # 2 x 152 x 16 tiles' worth of that gate_up's segments (58,368): the next
     # two layers' qkv, o and gate_up where there are any; the head, which
     # touches no other job's bytes and is the largest such job, runs last
     assert order == [0, 1, 2, 4, 5, 6, 8, 9, 10, 3, 7, 11, 12]
