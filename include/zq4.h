@@ -420,9 +420,14 @@ ZQ4_API zq4_status zq4_gate_up_silu_seg(const uint32_t *wseg, const uint16_t *x,
  * tiles, handed out one at a time across all jobs (no barrier between
  * jobs), each job waiting for the earlier jobs it conflicts with (at most 3
  * after dropping those implied by the others; a job list that needs more
- * runs on the other kernel). For M = 3..8 (and the lists above): every CTA
- * takes its share of each job in turn, a job waiting for the last earlier
- * job it conflicts with. Both give the results of the given order.
+ * runs on the other kernel). Tiles of a long-K job (more than 12 segments
+ * of 256 columns) that starts so late that one whole tile would outlast the
+ * rest of the step are split along K into parts of at most 12 segments
+ * whose fp32 sums are added in part order (the plan's device buffer holds
+ * them: at most 4 MiB, else nothing is split). For M = 3..8 (and the lists
+ * above): every CTA takes its share of each job in turn, a job waiting for
+ * the last earlier job it conflicts with. Both give the results of the
+ * given order.
  */
 typedef struct zq4_stack_job {
     const uint32_t *wq;
@@ -452,7 +457,10 @@ typedef struct zq4_stack_plan {
     int tiles;
     int n_pub;
     int gen;
-    int min_k;
+    int min_unit;
+    int split_tiles;
+    int part_records;
+    int entries;
 } zq4_stack_plan;
 
 /*
@@ -471,9 +479,10 @@ ZQ4_API zq4_status zq4_stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, i
  * within that, a job that would wait for a job run shortly before it lets
  * later jobs that conflict with nothing still to run go first, until the
  * job it waits for is followed by its own work and twice 152 x 16 of its
- * 16-row tiles' worth of other work (a constant, the same on any device);
- * when some job waits, the largest job that conflicts with no other job runs
- * last.
+ * 16-row tiles' worth of other work (a constant, the same on any device); a
+ * job that some later job waits for runs before up to 12 jobs just ahead of
+ * it that it may pass; when some job waits, the largest job that conflicts
+ * with no other job runs last.
  *   order[r] = the index (in `jobs`) of the r-th job run;
  *   dep[i]   = the last job run before job i that conflicts with it, or -1:
  *              it is finished before any part of job i starts.
@@ -521,11 +530,13 @@ ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
  * zq4_stack_plan_init, and the plan it fills runs with zq4_stack_run.
  *
  * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
- * 64 KiB array, i.e. at most 961 jobs for a plan run by the one- and
- * two-token kernel (64-byte job entries) and 1257 for the other (48-byte
- * entries); a longer list returns ZQ4_ERR_UNSUPPORTED and changes nothing.
- * What must start at zero (the plan's launch counter, abort flag and
- * per-job counters) is cleared by every call. The first call on a device
+ * array's first 64 KiB, i.e. at most 961 entries for a plan run by the one-
+ * and two-token kernel (64-byte entries; a job split along K takes one per
+ * part) and 1257 jobs for the other (48-byte entries); a longer list
+ * returns ZQ4_ERR_UNSUPPORTED and changes nothing. The rest of the array
+ * (4 MiB and a little more) holds the split parts' sums. What must start at
+ * zero (the plan's launch counter, abort flag and per-job and split-tile
+ * counters) is cleared by every call. The first call on a device
  * resolves the array's address (cudaGetSymbolAddress); every call
  * synchronises `stream`, so call it before any stream capture begins.
  *

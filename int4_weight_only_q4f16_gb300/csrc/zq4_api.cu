@@ -108,7 +108,7 @@ const char *zq4_status_string(int status)
 
 int zq4_last_cuda_error(void) { return t_last_cuda_error; }
 
-int zq4_version(void) { return 200; }
+int zq4_version(void) { return 201; }
 
 zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, uint16_t *y,
                     int M, int N, int K, void *stream)

@@ -719,9 +719,75 @@ Layout layout_for(int n_jobs)
     return l;
 }
 
-size_t plan_bytes_for(int engine, int n_jobs)
+// Work (segments) to place between a job and a job that waits for it, beyond
+// the job's own work: two tiles per compute warp of a full GB300 (152 SMs x
+// 16 warps), so that in the step engine, where each warp takes tiles one at
+// a time, the last tiles of the job are done before the first tiles of the
+// waiting job are handed out. A constant, so the order does not depend on
+// the device (a smaller GPU only gets more room than it needs).
+constexpr long long kSlackTiles = 2ll * 152 * kStepWarps;
+
+// Parts per tile of the job run at position r of a step-engine plan: its
+// tiles are split along K (step_split) only when they start so late that a
+// whole tile would outlast the rest of the step, i.e. when the work from the
+// job's start to the end (segments) is less than kSlackTiles tiles of its
+// length (every compute warp of a full GB300 taking two such tiles); earlier
+// tiles run whole, with no workspace traffic. f(r, C) for every position.
+template <class F>
+void for_each_split(const zq4_stack_job *jobs, int n, const int *order, F f)
 {
-    return engine == kEngineStep ? StepLayout(n_jobs).total : layout_for(n_jobs).total;
+    long long rest = 0;
+    for (int r = 0; r < n; ++r) rest += (long long)((jobs[order[r]].N + 15) / 16) * (jobs[order[r]].K / st::kSegCols);
+    for (int r = 0; r < n; ++r) {
+        const zq4_stack_job &b = jobs[order[r]];
+        const long long S = b.K / st::kSegCols;
+        f(r, rest < kSlackTiles * S ? step_split(b.K) : 1);
+        rest -= (long long)((b.N + 15) / 16) * S;
+    }
+}
+
+// The split workspace of a step-engine plan: tiles split along K and their
+// 16-float part records, over all jobs; none at all when the records would
+// take more than kStepMaxWorkBytes.
+struct SplitTotals {
+    long long tiles = 0, records = 0;
+    int entries = 0;          // job-table entries (a split job has one per part)
+    bool on = false;
+};
+SplitTotals split_totals(const zq4_stack_job *jobs, int n, int M, const int *order)
+{
+    SplitTotals t;
+    long long entries = 0;
+    for_each_split(jobs, n, order, [&](int r, int C) {
+        entries += C;
+        if (C == 1) return;
+        const long long rows = (jobs[order[r]].N + 15) / 16;
+        t.tiles += rows;
+        t.records += rows * C * M;
+    });
+    t.on = t.records > 0 && t.records * 64 <= (long long)kStepMaxWorkBytes && entries < (1 << 20);
+    if (!t.on) t.tiles = t.records = 0;
+    t.entries = t.on ? int(entries) : n;
+    return t;
+}
+
+// Device bytes of a plan, and the part of them the host image covers (the
+// rest: the split counters, cleared by a memset, and the part records, which
+// need no initial value).
+size_t plan_bytes_for(int engine, const zq4_stack_job *jobs, int n, int M, const int *order)
+{
+    if (engine != kEngineStep) return layout_for(n).total;
+    const SplitTotals t = split_totals(jobs, n, M, order);
+    return StepLayout(t.entries, t.tiles, t.records).total;
+}
+// `entries`: job-table entries (the step engine), else jobs
+size_t image_bytes_for(int engine, int entries)
+{
+    return engine == kEngineStep ? StepLayout(entries, 0, 0).arrive : layout_for(entries).total;
+}
+int entries_for(int engine, const zq4_stack_job *jobs, int n, int M, const int *order)
+{
+    return engine == kEngineStep ? split_totals(jobs, n, M, order).entries : n;
 }
 
 zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, int *max_k, int *max_tiles)
@@ -783,22 +849,17 @@ bool conflict(const zq4_stack_job &a, const zq4_stack_job &b, int M)
 }
 
 constexpr int kLookAhead = 32;   // jobs a waiting job may be passed by
+constexpr int kProducerAhead = 12; // jobs a job that others wait for may pass (three layers of four projections)
 
-// Work (segments) to place between a job and a job that waits for it, beyond
-// the job's own work: two tiles per compute warp of a full GB300 (152 SMs x
-// 16 warps), so that in the step engine, where each warp takes tiles one at
-// a time, the last tiles of the job are done before the first tiles of the
-// waiting job are handed out. A constant, so the order does not depend on
-// the device (a smaller GPU only gets more room than it needs).
-constexpr long long kSlackTiles = 2ll * 152 * kStepWarps;
 
 // Scratch for the host scheduling (n entries each; anc: n bitsets of
 // `words` 64-bit words), from the caller so that the static-plan path
 // allocates nothing.
 struct SchedScratch {
     long long *work, *need, *at;
-    char *placed;
+    char *placed, *prod;
     int *nwait;
+    int *first;                  // step engine: the job-table entry of each position's part 0
     int (*waits)[kStepMaxWaits];
     uint64_t *anc;
     int words;
@@ -825,6 +886,9 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, con
         need[i] = std::max(work[i], kSlackTiles * S);
         at[i] = -1;
         placed[i] = 0;
+        sc.prod[i] = 0;
+        for (int j = i + 1; j < n && !sc.prod[i]; ++j)
+            if (conflict(jobs[i], jobs[j], M)) sc.prod[i] = 1;
     }
     int n_placed = 0;
     long long total = 0;
@@ -853,19 +917,29 @@ void schedule(const zq4_stack_job *jobs, int n, int M, int *order, int *dep, con
     int first = 0;
     while (n_placed < n - (n > 1 && last >= 0 ? 1 : 0)) {
         while (placed[first]) ++first;
+        // may job k run next: no unplaced job before it conflicts with it,
+        // and whatever it waits for has had its room
+        auto may_run = [&](int k) {
+            if (placed[k]) return false;
+            for (int i = first; i < k; ++i)
+                if (!placed[i] && conflict(jobs[i], jobs[k], M)) return false;
+            return short_by(k) <= 0;
+        };
         int pick = first;
-        if (short_by(first) > 0) {
-            for (int k = first + 1; k < n && k <= first + kLookAhead; ++k) {
-                if (placed[k]) continue;
-                bool free = true;
-                for (int i = first; i < k && free; ++i)
-                    if (!placed[i] && conflict(jobs[i], jobs[k], M)) free = false;
-                if (free && short_by(k) <= 0) {
+        if (short_by(first) > 0)
+            for (int k = first + 1; k < n && k <= first + kLookAhead; ++k)
+                if (may_run(k)) {
                     pick = k;
                     break;
                 }
-            }
-        }
+        // a job some later job waits for goes before the independent jobs
+        // just after the pick, so that the job waiting for it gets more room
+        if (!sc.prod[pick])
+            for (int k = pick + 1; k < n && k <= pick + kProducerAhead; ++k)
+                if (sc.prod[k] && may_run(k)) {
+                    pick = k;
+                    break;
+                }
         placed[pick] = 1;
         total += work[pick];
         at[pick] = total;
@@ -926,18 +1000,18 @@ st::Job make_job(const zq4_stack_job &b, int off, int dep)
 
 // Heap scratch for the calls that may allocate.
 struct SchedBuffers {
-    std::vector<int> order, dep, nwait;
+    std::vector<int> order, dep, nwait, first;
     std::vector<long long> work, need, at;
-    std::vector<char> placed;
+    std::vector<char> placed, prod;
     std::vector<int> waits;
     std::vector<uint64_t> anc;
     int words;
     explicit SchedBuffers(int n)
-        : order(n), dep(n), nwait(n), work(n), need(n), at(n), placed(n), waits(size_t(n) * kStepMaxWaits),
+        : order(n), dep(n), nwait(n), first(n), work(n), need(n), at(n), placed(n), prod(n), waits(size_t(n) * kStepMaxWaits),
           anc(size_t(n) * ((n + 63) / 64)), words((n + 63) / 64) {}
     SchedScratch scratch()
     {
-        return {work.data(), need.data(), at.data(), placed.data(), nwait.data(),
+        return {work.data(), need.data(), at.data(), placed.data(), prod.data(), nwait.data(), first.data(),
                 reinterpret_cast<int(*)[kStepMaxWaits]>(waits.data()), anc.data(), words};
     }
 };
@@ -964,53 +1038,103 @@ int tight_waits(int n, const int *order, const int *dep, const SchedScratch &sc)
 // else k_stack.
 int choose_engine(const zq4_stack_job *jobs, int n, int M, const int *order, const int *dep, const SchedScratch &sc)
 {
-    if (M <= kStepMaxM && 8 * tight_waits(n, order, dep, sc) <= n && wait_lists(jobs, n, M, order, sc))
+    if (M <= kStepMaxM && n < kStepMaxPub && 8 * tight_waits(n, order, dep, sc) <= n &&
+        wait_lists(jobs, n, M, order, sc))
         return kEngineStep;
     return kEngineStack;
 }
 
+// What write_image reports besides the image.
+struct ImageInfo {
+    long long tiles = 0;      // work units of the launch
+    int entries = 0;          // job-table entries (step engine: a split job has one per part)
+    int n_pub = 0;            // jobs another job waits for (step engine)
+    int min_unit = 0;         // segments of the shortest work unit
+    long long split_tiles = 0, part_records = 0;
+};
+
 // The plan's device image (header zero, job table, counters zero) into `host`
-// (plan_bytes_for(engine, n) bytes), for G CTAs. The schedule must have been
-// computed into sc / order / dep (and the wait lists for the step engine).
-void write_image(int engine, const zq4_stack_job *jobs, int n, const int *order, const int *dep,
-                 const SchedScratch &sc, int G, uint8_t *host, long long *tiles_out, int *n_pub_out)
+// (image_bytes_for(engine, entries) bytes), for G CTAs. The schedule must
+// have been computed into sc / order / dep (and the wait lists for the step
+// engine).
+void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int *order, const int *dep,
+                 const SchedScratch &sc, int G, uint8_t *host, ImageInfo *info)
 {
-    memset(host, 0, plan_bytes_for(engine, n));
+    *info = ImageInfo();
     if (engine == kEngineStack) {
+        memset(host, 0, image_bytes_for(engine, n));
+        info->entries = n;
         st::Job *t = reinterpret_cast<st::Job *>(host + layout_for(n).jobs);
         for (int r = 0, off = 0; r < n; ++r) {
             t[r] = make_job(jobs[order[r]], off, dep[r]);
             off = int((off + (long long)t[r].T) % G);
         }
-        *tiles_out = 0;
-        *n_pub_out = 0;
+        info->min_unit = 1 << 30;
+        for (int j = 0; j < n; ++j) info->min_unit = std::min(info->min_unit, jobs[j].K / st::kSegCols);
         return;
     }
-    StepJob *t = reinterpret_cast<StepJob *>(host + StepLayout(n).jobs);
-    long long tile0 = 0;
-    for (int r = 0; r < n; ++r) {
+    const SplitTotals split = split_totals(jobs, n, M, order);
+    memset(host, 0, image_bytes_for(engine, split.entries));
+    StepJob *t = reinterpret_cast<StepJob *>(host + StepLayout(split.entries, 0, 0).jobs);
+    // the entry of part 0 of each position
+    int e = 0;
+    for_each_split(jobs, n, order, [&](int r, int Cr) {
+        sc.first[r] = e;
+        e += split.on ? Cr : 1;
+    });
+    long long tile0 = 0, sbase = 0, pbase = 0;
+    int min_unit = 1 << 30, n_pub = 0;
+    for_each_split(jobs, n, order, [&](int r, int Cr) {
         const zq4_stack_job &b = jobs[order[r]];
-        StepJob &jb = t[r];
-        jb.seg = reinterpret_cast<const uint8_t *>(b.wq);
-        jb.x = b.x;
-        jb.y = b.y;
-        jb.N = b.N;
-        jb.K = b.K;
-        jb.T = (b.N + 15) / 16;
-        jb.tile0 = int(tile0);
-        jb.flags = b.gate_up ? kStepGateUp : 0;
-        jb.y_stride = b.gate_up ? b.N / 2 : b.N;
-        jb.nwait = sc.nwait[r];
-        for (int w = 0; w < kStepMaxWaits; ++w) jb.wait[w] = w < sc.nwait[r] ? sc.waits[r][w] : 0;
-        tile0 += jb.T;
+        const int rows = (b.N + 15) / 16, S = b.K / st::kSegCols;
+        const int C = split.on ? Cr : 1;
+        // jobs some later job waits for count their units for it
+        bool waited = false;
+        for (int q = r + 1; q < n && !waited; ++q)
+            for (int w = 0; w < sc.nwait[q]; ++w) waited |= sc.waits[q][w] == r;
+        const int pub = waited ? n_pub++ : 0;
+        for (int c = 0; c < C; ++c) {
+            const int c0 = c * S / C, len = (c + 1) * S / C - c0;
+            StepJob &jb = t[sc.first[r] + c];
+            jb.seg = reinterpret_cast<const uint8_t *>(b.wq) + size_t(c0) * st::kSegBytes;
+            jb.x = b.x + size_t(c0) * st::kSegCols;
+            jb.y = b.y;
+            jb.N = b.N;
+            jb.K = len * st::kSegCols;
+            jb.tstride = S;
+            jb.tile0 = int(tile0);
+            jb.flags = (b.gate_up ? kStepGateUp : 0) | (sc.nwait[r] << kStepWaitShift) |
+                       ((C - 1) << kStepSplitShift) | (c << kStepPartShift) |
+                       (waited ? kStepPublish | (pub << kStepPubShift) : 0);
+            jb.sbase = C > 1 ? int(sbase) : 0;
+            jb.pbase = C > 1 ? int(pbase) : 0;
+            for (int w = 0; w < kStepMaxWaits; ++w) jb.wait[w] = w < sc.nwait[r] ? sc.first[sc.waits[r][w]] : 0;
+            tile0 += rows;
+            min_unit = std::min(min_unit, len);
+        }
+        if (C > 1) {
+            sbase += rows;
+            pbase += (long long)rows * C;
+        }
+    });
+    info->tiles = tile0;
+    info->entries = split.entries;
+    info->n_pub = n_pub;
+    info->min_unit = min_unit;
+    info->split_tiles = sbase;
+    info->part_records = pbase * M;
+}
+
+// The image, then the split counters cleared, on stream s (synchronised).
+zq4_status upload_plan(void *dev, const uint8_t *image, int engine, const ImageInfo &info, cudaStream_t s)
+{
+    cudaError_t e = cudaMemcpyAsync(dev, image, image_bytes_for(engine, info.entries), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && engine == kEngineStep && info.split_tiles > 0) {
+        const StepLayout l(info.entries, info.split_tiles, info.part_records);
+        e = cudaMemsetAsync(static_cast<uint8_t *>(dev) + l.arrive, 0, l.work - l.arrive, s);
     }
-    int n_pub = 0;
-    for (int r = 0; r < n; ++r)
-        for (int w = 0; w < t[r].nwait; ++w) t[t[r].wait[w]].flags |= kStepPublish;
-    for (int r = 0; r < n; ++r)
-        if (t[r].flags & kStepPublish) t[r].flags |= (n_pub++) << kStepPubShift;
-    *tiles_out = tile0;
-    *n_pub_out = n_pub;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? ZQ4_OK : cuda_status(e);
 }
 
 // Kernel attributes and residency for a launch of this plan shape.
@@ -1081,20 +1205,21 @@ zq4_status stack_plan_bytes(const zq4_stack_job *jobs, int n_jobs, int M, size_t
     const zq4_status s = plan_common(jobs, n_jobs, M, sm_count(), b.order.data(), b.dep.data(), b.scratch(), &engine,
                                      &mk, &mt);
     if (s != ZQ4_OK) return s;
-    *bytes = plan_bytes_for(engine, n_jobs);
+    *bytes = plan_bytes_for(engine, jobs, n_jobs, M, b.order.data());
     return ZQ4_OK;
 }
 
 namespace {
 
-void fill_plan(zq4_stack_plan *plan, const zq4_stack_job *jobs, void *dev, int engine, int n_jobs, int M, int grid,
-               int mk, int mt, long long tiles, int n_pub, int gen)
+void fill_plan(zq4_stack_plan *plan, const zq4_stack_job *jobs, const int *order, void *dev, int engine, int n_jobs,
+               int M, int grid, int mk, int mt, const ImageInfo &info, int gen)
 {
-    int min_k = mk;
-    for (int j = 0; j < n_jobs; ++j) min_k = std::min(min_k, jobs[j].K);
-    plan->min_k = min_k;
+    plan->min_unit = info.min_unit;
+    plan->entries = info.entries;
+    plan->split_tiles = int(info.split_tiles);
+    plan->part_records = int(info.part_records);
     plan->dev = dev;
-    plan->bytes = plan_bytes_for(engine, n_jobs);
+    plan->bytes = plan_bytes_for(engine, jobs, n_jobs, M, order);
     plan->n_jobs = n_jobs;
     plan->M = M;
     plan->grid = grid;
@@ -1102,8 +1227,8 @@ void fill_plan(zq4_stack_plan *plan, const zq4_stack_job *jobs, void *dev, int e
     plan->max_tiles = mt;
     plan->device = current_device();
     plan->engine = engine;
-    plan->tiles = int(tiles);
-    plan->n_pub = n_pub;
+    plan->tiles = int(info.tiles);
+    plan->n_pub = info.n_pub;
     plan->gen = gen;
 }
 
@@ -1120,19 +1245,16 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     int engine, mk, mt;
     zq4_status stt = plan_common(jobs, n_jobs, M, grid, b.order.data(), b.dep.data(), b.scratch(), &engine, &mk, &mt);
     if (stt != ZQ4_OK) return stt;
-    const size_t need = plan_bytes_for(engine, n_jobs);
-    if (bytes < need) return ZQ4_ERR_SHAPE;
-    std::vector<uint8_t> host(need);
-    long long tiles;
-    int n_pub;
-    write_image(engine, jobs, n_jobs, b.order.data(), b.dep.data(), b.scratch(), grid, host.data(), &tiles, &n_pub);
+    if (bytes < plan_bytes_for(engine, jobs, n_jobs, M, b.order.data())) return ZQ4_ERR_SHAPE;
+    std::vector<uint8_t> host(image_bytes_for(engine, entries_for(engine, jobs, n_jobs, M, b.order.data())));
+    ImageInfo info;
+    write_image(engine, jobs, n_jobs, M, b.order.data(), b.dep.data(), b.scratch(), grid, host.data(), &info);
     // the kernel needs every CTA resident at once
-    stt = check_resident(engine, n_jobs, M, mk, n_pub);
+    stt = check_resident(engine, info.entries, M, mk, info.n_pub);
     if (stt != ZQ4_OK) return stt;
-    cudaError_t e = cudaMemcpyAsync(dev, host.data(), host.size(), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_status(e);
-    fill_plan(plan, jobs, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, 0);
+    stt = upload_plan(dev, host.data(), engine, info, s);
+    if (stt != ZQ4_OK) return stt;
+    fill_plan(plan, jobs, b.order.data(), dev, engine, n_jobs, M, grid, mk, mt, info, 0);
     return ZQ4_OK;
 }
 
@@ -1141,14 +1263,17 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticPlanBytes = 64 * 1024;
+constexpr size_t kStaticPlanBytes = 64 * 1024;   // header, job table, counters
+// ... then the split workspace: counters (at most one per two part records)
+// and part records
+constexpr size_t kStaticDevBytes = kStaticPlanBytes + (kStepMaxWorkBytes / 32 + 256) + kStepMaxWorkBytes;
 constexpr int kStaticMaxJobs = 1257;          // stack engine: 128 + 52 n bytes (rounded to 256) fit
 constexpr int kStaticMaxJobsStep = 961;       // step engine: 128 + 68 n bytes (rounded to 256) fit
 static_assert(sizeof(st::Job) == 48, "the documented job limit assumes 48-byte job entries");
 
 // The plan lives here when the caller has no device memory to give. Header
 // and counters are cleared by every zq4_stack_plan_init_static.
-static __device__ __align__(256) uint8_t g_static_plan[kStaticPlanBytes];
+static __device__ __align__(256) uint8_t g_static_plan[kStaticDevBytes];
 
 // Device address of g_static_plan on the current device, resolved once per
 // device.
@@ -1178,10 +1303,11 @@ std::atomic<int> g_static_gen[kMaxDevices];
 // caller's stack, not the heap), one call at a time.
 std::mutex g_static_mutex;
 uint8_t g_static_image[kStaticPlanBytes];
-int g_static_order[kStaticMaxJobs], g_static_dep[kStaticMaxJobs], g_static_nwait[kStaticMaxJobs];
+int g_static_order[kStaticMaxJobs], g_static_dep[kStaticMaxJobs], g_static_nwait[kStaticMaxJobs],
+    g_static_first[kStaticMaxJobs];
 int g_static_waits[kStaticMaxJobs][kStepMaxWaits];
 long long g_static_work[kStaticMaxJobs], g_static_need[kStaticMaxJobs], g_static_at[kStaticMaxJobs];
-char g_static_placed[kStaticMaxJobs];
+char g_static_placed[kStaticMaxJobs], g_static_prod[kStaticMaxJobs];
 constexpr int kStaticWords = (kStaticMaxJobs + 63) / 64;
 uint64_t g_static_anc[size_t(kStaticMaxJobs) * kStaticWords];
 
@@ -1195,19 +1321,20 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     if (n_jobs > kStaticMaxJobs) return ZQ4_ERR_UNSUPPORTED;   // more jobs than the static plan holds
     std::lock_guard<std::mutex> lock(g_static_mutex);
     const int words = (n_jobs + 63) / 64;
-    const SchedScratch sc = {g_static_work, g_static_need, g_static_at, g_static_placed, g_static_nwait,
+    const SchedScratch sc = {g_static_work, g_static_need, g_static_at, g_static_placed, g_static_prod, g_static_nwait,
+                             g_static_first,
                              g_static_waits, g_static_anc, words};
     const int grid = sm_count();
     int engine, mk, mt;
     zq4_status stt = plan_common(jobs, n_jobs, M, grid, g_static_order, g_static_dep, sc, &engine, &mk, &mt);
     if (stt != ZQ4_OK) return stt;
     if (engine == kEngineStep && n_jobs > kStaticMaxJobsStep) return ZQ4_ERR_UNSUPPORTED;
-    const size_t need = plan_bytes_for(engine, n_jobs);
-    if (need > kStaticPlanBytes) return ZQ4_ERR_UNSUPPORTED;
-    long long tiles;
-    int n_pub;
-    write_image(engine, jobs, n_jobs, g_static_order, g_static_dep, sc, grid, g_static_image, &tiles, &n_pub);
-    stt = check_resident(engine, n_jobs, M, mk, n_pub);
+    if (image_bytes_for(engine, entries_for(engine, jobs, n_jobs, M, g_static_order)) > kStaticPlanBytes ||
+        plan_bytes_for(engine, jobs, n_jobs, M, g_static_order) > kStaticDevBytes)
+        return ZQ4_ERR_UNSUPPORTED;
+    ImageInfo info;
+    write_image(engine, jobs, n_jobs, M, g_static_order, g_static_dep, sc, grid, g_static_image, &info);
+    stt = check_resident(engine, info.entries, M, mk, info.n_pub);
     if (stt != ZQ4_OK) return stt;
     void *dev = nullptr;
     cudaError_t e = static_plan_address(&dev);
@@ -1215,11 +1342,10 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return ZQ4_ERR_CUDA;
     // from pageable memory: the image is staged before the call returns
-    e = cudaMemcpyAsync(dev, g_static_image, need, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_status(e);
+    stt = upload_plan(dev, g_static_image, engine, info, s);
+    if (stt != ZQ4_OK) return stt;
     const int gen = g_static_gen[d].fetch_add(1) + 1;
-    fill_plan(plan, jobs, dev, engine, n_jobs, M, grid, mk, mt, tiles, n_pub, gen);
+    fill_plan(plan, jobs, g_static_order, dev, engine, n_jobs, M, grid, mk, mt, info, gen);
     return ZQ4_OK;
 }
 

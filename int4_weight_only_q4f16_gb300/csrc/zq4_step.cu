@@ -23,11 +23,19 @@
 //    warp without a hand-off; the slot's descriptor (job, tile, first/last)
 //    travels with it.
 //  * x of every job is brought into shared memory once per CTA, by a stager
-//    warp, into a window of a few buffers: one bulk copy per token, issued
-//    once the job's waits are met, into any buffer whose job no compute warp
-//    of the CTA can still read (each warp publishes the job it is reading
-//    and a lower bound of the jobs it will read after it, so a warp busy
-//    with a long tile holds one buffer, not the window).
+//    warp, into a byte ring (the window): bytes taken in job order, one bulk
+//    copy per token, issued once the job's waits are met; a job whose waits
+//    are not met yet keeps its bytes and the stager goes on with the jobs
+//    after it. Bytes come back once no compute warp of the CTA can still
+//    read them (each warp publishes the job it is reading and a lower bound
+//    of the jobs it will read after it, so a warp busy with a long tile
+//    holds one job's bytes, not the window).
+//  * Long-K jobs near the end of the step (where one whole tile would
+//    outlast the rest of the work) are split along K into parts of at most
+//    12 segments, each an entry of the job table; a part's warp leaves its
+//    fp32 sums in the plan's workspace and posts the tile to the CTA's
+//    finisher warp, which counts the arrival and, for the last part of a
+//    tile, adds the parts in part order and writes the tile.
 //  * Inner loop, one token (the MMA's 8 columns would otherwise hold 1
 //    useful token): column c of the m16n8k16 accumulator collects group c
 //    of the segment (a block-diagonal B: lanes of column c read x of group
@@ -84,10 +92,18 @@ constexpr int kThreads = kWarps * 32 + 64;
 struct Params {
     StepHeader *hdr;
     const StepJob *jobs;
-    unsigned *job_done;      // [n_jobs]: tiles finished (monotone across launches)
+    unsigned *job_done;      // [n_jobs]: units finished (monotone across launches)
+    unsigned *arrive;        // split tiles: parts finished (monotone across launches)
+    float *work;             // split tiles: the parts' sums
     int n_jobs, total_tiles, M, slots, wbytes, cached, n_pub;
-    int fine;                // every job's tile is at least `slots` segments long
+    int fine;                // every work unit is at least `slots` segments long
+    int split;               // some job is split into parts
 };
+
+// Finished tiles of split parts, posted by each compute warp to the
+// finisher (the publisher warp): a ring of kPosts (entry, tile) pairs per
+// warp, with the counts posted and taken.
+constexpr int kPosts = 4;
 
 // x window entries: job j's x is described by entry j % kEntries (barrier,
 // published tag, and the stager's record of the bytes it took)
@@ -97,7 +113,8 @@ constexpr int kTagJobShift = 12;
 
 // Shared-memory layout (bytes from a 128-byte aligned base).
 struct Smem {
-    uint32_t ring, bars, desc, xbar, xtag, xstart, xtotal, wcur, wlb, misc, zero, xwin, cta_done, cta_pub, cta_snap,
+    uint32_t ring, bars, desc, xbar, xtag, xstart, xtotal, wcur, wlb, posted, taken, posts, misc, zero, xwin, cta_done,
+        cta_pub, cta_snap,
         jobs, total;
     __host__ __device__ Smem(int slots, int wbytes, int n_pub, int cached)
     {
@@ -110,7 +127,10 @@ struct Smem {
         xtotal = xstart + kEntries * 4;
         wcur = xtotal + kEntries * 4;
         wlb = wcur + kWarps * 4;
-        misc = wlb + kWarps * 4;
+        posted = wlb + kWarps * 4;
+        taken = posted + kWarps * 4;
+        posts = taken + kWarps * 4;
+        misc = posts + kWarps * kPosts * 8;
         zero = (misc + 64 + 127) / 128 * 128;
         xwin = zero + 128;
         cta_done = xwin + uint32_t(wbytes);
@@ -156,6 +176,11 @@ __device__ __forceinline__ int4 lds_s4(uint32_t saddr)
 __device__ __forceinline__ void fence_acq_rel_gpu_() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // a counter that grows across launches has reached `target` (wrap-safe)
 __device__ __forceinline__ bool reached(unsigned v, unsigned target) { return int(v - target) >= 0; }
+// units a waited-for job finishes per launch (its tiles times its parts), from its part 0 entry
+__device__ __forceinline__ unsigned unit_count(const StepJob &j)
+{
+    return unsigned((j.N + 15) >> 4) * unsigned(((j.flags >> kStepSplitShift) & 63) + 1);
+}
 __device__ __forceinline__ float lo_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w)); }
 __device__ __forceinline__ float hi_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w >> 16)); }
 // a value the compiler must keep in a register (not recompute in the loop)
@@ -209,22 +234,38 @@ __device__ __forceinline__ void segment(uint32_t cb, uint32_t aoff, uint32_t sof
     }
 }
 
-// A finished tile: sum the lane's groups, then over the lanes of the same
-// token (fixed order), and write rows row0 + r, row0 + r + 8 of each token.
+// Rows r, r+8 of a finished unit: the lane's groups summed, then over the
+// lanes of the same token (fixed order). The sums are whole in the holder
+// lanes (token tok).
 template <int MT>
-__device__ __forceinline__ void finish_tile(const float (&acc)[4], const StepJob &jb, int row0, int lane, int M)
+__device__ __forceinline__ void tile_sums(const float (&acc)[4], float &v0, float &v1)
 {
-    const int r = lane >> 2, t = lane & 3;
-    float v0 = acc[0] + acc[1], v1 = acc[2] + acc[3];
+    v0 = acc[0] + acc[1];
+    v1 = acc[2] + acc[3];
     v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
     v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
     if (MT == 1) {
         v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
         v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
     }
+}
+template <int MT>
+__device__ __forceinline__ bool holder_lane(int lane, int M)
+{
+    const int t = lane & 3;
+    return MT == 1 ? (t == 0) : ((t & 1) == 0 && (t >> 1) < M);
+}
+
+// Rows row0 + r, row0 + r + 8 of each token from the holder lanes' sums
+// (gate_up: silu(gate) * up of the row pairs).
+template <int MT>
+__device__ __forceinline__ void write_rows(float v0, float v1, const StepJob &jb, int row0, int lane, int M)
+{
+    const int r = lane >> 2, t = lane & 3;
     const int tok = MT == 1 ? 0 : (t >> 1);
-    const bool writer = MT == 1 ? (t == 0) : ((t & 1) == 0 && tok < M);
-    uint16_t *y = jb.y + size_t(tok) * jb.y_stride;
+    const bool writer = holder_lane<MT>(lane, M);
+    const int y_stride = (jb.flags & kStepGateUp) ? (jb.N >> 1) : jb.N;
+    uint16_t *y = jb.y + size_t(tok) * y_stride;
     if (!(jb.flags & kStepGateUp)) {
         if (writer) {
             if (row0 + r < jb.N) y[row0 + r] = float_to_f16_bits(v0);
@@ -236,6 +277,84 @@ __device__ __forceinline__ void finish_tile(const float (&acc)[4], const StepJob
             if (row0 + r + 1 < jb.N) y[(row0 + r) >> 1] = float_to_f16_bits(silu_f32(v0) * u0);
             if (row0 + r + 9 < jb.N) y[(row0 + r + 8) >> 1] = float_to_f16_bits(silu_f32(v1) * u1);
         }
+    }
+}
+
+// A finished unit of an unsplit job: the whole tile.
+template <int MT>
+__device__ __forceinline__ void finish_tile(const float (&acc)[4], const StepJob &jb, int row0, int lane, int M)
+{
+    float v0, v1;
+    tile_sums<MT>(acc, v0, v1);
+    write_rows<MT>(v0, v1, jb, row0, lane, M);
+}
+
+// Where part c of tile rt of a split job keeps its sums: 16 fp32 rows per
+// token (parts part_floats apart).
+__device__ __forceinline__ size_t part_floats(const StepJob &jb, int M) { return size_t((jb.N + 15) >> 4) * size_t(M) * 16; }
+__device__ __forceinline__ float *part_record(const Params &p, const StepJob &jb, int rt, int c, int M)
+{
+    return p.work + (size_t(jb.pbase) + size_t(rt)) * size_t(M) * 16 + part_floats(jb, M) * size_t(c);
+}
+
+// A compute warp's finished tile rt of one part of a split job: its sums
+// into the part's record, then (lane 0, once the ring has room) a post to
+// the finisher. False if the finisher never made room (a bounded wait).
+template <int MT>
+__device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &jb, int entry, int rt, int lane, int M,
+                                          const Params &p, uint32_t posted, uint32_t taken, uint32_t posts,
+                                          volatile int *s_abort)
+{
+    float v0, v1;
+    tile_sums<MT>(acc, v0, v1);
+    const int r = lane >> 2, tok = MT == 1 ? 0 : ((lane & 3) >> 1);
+    float *rec = part_record(p, jb, rt, (jb.flags >> kStepPartShift) & 63, M) + size_t(tok) * 16 + r;
+    if (holder_lane<MT>(lane, M)) {
+        rec[0] = v0;
+        rec[8] = v1;
+    }
+    __syncwarp();
+    int ok = 1;
+    if (lane == 0) {
+        const int n = int(lds_u32(posted));
+        const unsigned long long t0 = globaltimer();
+        while (n - ld_acquire_cta_s32(taken) >= kPosts) {
+            if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (ok) {
+            asm volatile("st.shared.v2.s32 [%0], {%1, %2};" ::"r"(posts + 8u * uint32_t(n % kPosts)), "r"(entry), "r"(rt)
+                         : "memory");
+            st_release_cta_s32(posted, n + 1);   // the record (global) and the pair before the count
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// A tile of a split job whose parts have all arrived (the whole warp, after
+// the arrival that completed it and an acquire fence): every part's sums
+// read back and added in part order (the same order whichever part arrived
+// last), the tile's rows written, lane = token * 16 + row.
+__device__ __forceinline__ void complete_part(const Params &p, const StepJob &jb, int rt, int lane, int M)
+{
+    const int C = ((jb.flags >> kStepSplitShift) & 63) + 1;
+    const int tok = lane >> 4, row = lane & 15;
+    float v = 0.f;
+    if (tok < M) {
+        const float *rec = part_record(p, jb, rt, 0, M) + size_t(tok) * 16 + row;
+        const size_t step = part_floats(jb, M);
+        for (int c = 0; c < C; ++c) v += __ldcg(rec + step * size_t(c));
+    }
+    const int n = rt * 16 + row;
+    if (!(jb.flags & kStepGateUp)) {
+        if (tok < M && n < jb.N) jb.y[size_t(tok) * jb.N + n] = float_to_f16_bits(v);
+    } else {
+        const float u = __shfl_down_sync(0xffffffffu, v, 1);
+        if (tok < M && (row & 1) == 0 && n + 1 < jb.N)
+            jb.y[size_t(tok) * (jb.N >> 1) + (n >> 1)] = float_to_f16_bits(silu_f32(v) * u);
     }
 }
 
@@ -268,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
     for (int i = threadIdx.x; i < kWarps; i += kThreads) {
         reinterpret_cast<int *>(smem + L.wcur)[i] = -1;      // no job being read yet
         reinterpret_cast<int *>(smem + L.wlb)[i] = 0;        // every job may still be read
+        reinterpret_cast<int *>(smem + L.posted)[i] = 0;
+        reinterpret_cast<int *>(smem + L.taken)[i] = 0;
     }
     for (int i = threadIdx.x; i < kEntries; i += kThreads) reinterpret_cast<int *>(smem + L.xtag)[i] = -1;
     if (threadIdx.x == 0) {
@@ -294,15 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 
     if (warp == kStagerWarp) {
         // ---------------- the x stager ----------------
-        // x of every job, in job order, into a byte ring (the window): job j
-        // takes M * K_j * 2 bytes (128-byte aligned) at the ring's head, and
-        // the oldest jobs give their bytes back once no compute warp of this
-        // CTA can still read them (warp w reads its current job cur[w] and,
-        // after it, only jobs >= lb[w]). A job's x is copied once its waits
-        // are met (the data it reads is final). Entry j % kEntries holds the
-        // job's barrier and tag (job, offset, parity of the fill), published
-        // when the copy is issued; readers wait on the barrier. The ring
-        // state (head, tail, bytes used) is the same in every lane.
+        // x of every job into a byte ring (the window), bytes taken in job
+        // order: job j takes M * K_j * 2 bytes (128-byte aligned) at the
+        // ring's head, and the oldest jobs give their bytes back once no
+        // compute warp of this CTA can still read them (warp w reads its
+        // current job cur[w] and, after it, only jobs >= lb[w]). A job's x
+        // is copied once its waits are met (the data it reads is final): at
+        // once when they are met when its bytes are taken, else the job is
+        // pending (bit j - oldest of `pend`) and the stager goes on taking
+        // bytes for the jobs after it, copying theirs, and polls the pending
+        // ones; a pending job keeps its bytes (and every later job's). Entry
+        // j % kEntries holds the job's barrier and tag (job, offset, parity
+        // of the fill), published when the copy is issued; readers wait on
+        // the barrier. The ring state (head, tail, bytes used, pend) is the
+        // same in every lane.
         const uint32_t lb0 = sbase + L.wlb;
         const uint32_t W = uint32_t(p.wbytes);
         int *xtag = reinterpret_cast<int *>(smem + L.xtag);
@@ -310,123 +436,192 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         uint32_t *xtotal = reinterpret_cast<uint32_t *>(smem + L.xtotal);
         uint32_t head = 0, tail = 0, used = 0;
         int oldest = 0;                                      // the oldest job still holding bytes
-        int j = 0;
-        for (; j < n; ++j) {
+        int j = 0;                                           // the next job to take bytes
+        unsigned pend = 0;
+        // are job k's waits met (acquire loads, no waiting)
+        auto ready = [&](int k) {
+            const StepJob &jk = job(k);
+            bool r = true;
+            const int nw = (jk.flags >> kStepWaitShift) & 3;
+            for (int w = 0; r && w < nw; ++w) {
+                const int d = jk.wait[w];
+                r = reached(ld_acquire_gpu(&p.job_done[d]), done_mul * unit_count(job(d)));
+            }
+            return r;
+        };
+        // lane 0: the copy of job k's x into its bytes; false on a timeout
+        auto issue = [&](int k) -> bool {
+            const StepJob &jk = job(k);
+            const int e = k % kEntries;
+            const uint32_t off = xstart[e] + xtotal[e] > W ? 0u : xstart[e];    // wrapped: at 0
+            // the entry's previous fill has landed before its barrier is
+            // armed again (no compute warp of this CTA may have waited for
+            // it: the CTA can have had no tile of that job)
+            const bool used_e = xtag[e] >= 0;
+            if (used_e && !mbar_wait(sbase + L.xbar + 8 * e, uint32_t(xtag[e] & 1))) return false;
+            // the window's last readers (generic proxy) and the data's
+            // writers are ordered before the copy (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t bar = sbase + L.xbar + 8 * e, dst = sbase + L.xwin + off;
+            const int par = used_e ? ((xtag[e] & 1) ^ 1) : 0;   // the phase this fill completes
+            mbar_arrive_expect_tx(bar, uint32_t(M * jk.K * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_load(dst + uint32_t(m * jk.K * 2), jk.x + size_t(m) * size_t(jk.tstride) * 256, uint32_t(jk.K * 2), bar);
+            // job, offset and parity in one word: a reader that sees the job
+            // waits for that phase on the barrier, which orders the data
+            *reinterpret_cast<volatile int *>(xtag + e) = (k << kTagJobShift) | int((off >> 7) << 1) | par;
+            return true;
+        };
+        unsigned long long t0 = globaltimer();               // the last progress
+        int ok = 1;
+        while (j < n || pend) {
             if (__shfl_sync(0xffffffffu, *s_abort, 0)) break;
-            const StepJob &jb = job(j);
-            const uint32_t size = (uint32_t(M * jb.K * 2) + 127u) & ~127u;
-            const int e = j % kEntries;
-            int ok = 1;
-            uint32_t off = 0;
-            const unsigned long long t0 = globaltimer();
-            for (;;) {
-                // give back the bytes of the oldest jobs nobody reads any more:
-                // the bound first (acquire), then the current job (a warp
-                // stores its current job before it raises its bound)
-                int wl = lane < kWarps ? ld_acquire_cta_s32(lb0 + 4 * lane) : 0x7fffffff;
-                const int wc = lane < kWarps ? *reinterpret_cast<volatile int *>(smem + L.wcur + 4 * lane) : -1;
+            bool progress = false;
+            // give back the bytes of the oldest jobs nobody reads any more
+            // (never a pending job's): the bound first (acquire), then the
+            // current job (a warp stores its current job before it raises
+            // its bound)
+            int wl = lane < kWarps ? ld_acquire_cta_s32(lb0 + 4 * lane) : 0x7fffffff;
+            const int wc = lane < kWarps ? *reinterpret_cast<volatile int *>(smem + L.wcur + 4 * lane) : -1;
 #pragma unroll
-                for (int o = 16; o; o >>= 1) wl = min(wl, __shfl_xor_sync(0xffffffffu, wl, o));
-                while (oldest < j && oldest < wl && !__any_sync(0xffffffffu, lane < kWarps && wc == oldest)) {
-                    const int oe = oldest % kEntries;
-                    used -= xtotal[oe];
-                    tail = xstart[oe] + xtotal[oe];
-                    if (tail >= W) tail -= W;
-                    ++oldest;
-                }
-                if (used == 0) head = tail = 0;
-                // room at the head (wrapping to 0 wastes the end of the ring),
-                // and the entry's previous job has given its bytes back
-                bool room = false;
-                uint32_t start = head, total = size;
-                if (j - oldest < kEntries) {
-                    if (used == 0) {                             // empty (head = tail = 0)
-                        room = size <= W;
-                        off = 0;
-                    } else if (tail < head) {                    // data in [tail, head)
-                        if (head + size <= W) {
-                            room = true;
-                            off = head;
-                        } else if (size <= tail) {
-                            room = true;
-                            off = 0;
-                            total = W - head + size;
-                        }
-                    } else if (head + size <= tail) {            // data in [tail, W) and [0, head); full if equal
-                        room = true;
-                        off = head;
+            for (int o = 16; o; o >>= 1) wl = min(wl, __shfl_xor_sync(0xffffffffu, wl, o));
+            while (oldest < j && oldest < wl && !(pend & 1u) &&
+                   !__any_sync(0xffffffffu, lane < kWarps && wc == oldest)) {
+                const int oe = oldest % kEntries;
+                used -= xtotal[oe];
+                tail = xstart[oe] + xtotal[oe];
+                if (tail >= W) tail -= W;
+                ++oldest;
+                pend >>= 1;
+                progress = true;
+            }
+            if (used == 0) head = tail = 0;
+            // pending jobs whose waits are now met (each lane polls one; lane
+            // 0 checks again with its own acquire loads before the copy)
+            if (pend) {
+                const bool mine = (pend >> lane) & 1u;
+                unsigned rdy = __ballot_sync(0xffffffffu, mine && ready(oldest + lane));
+                while (rdy) {
+                    const int b = __ffs(rdy) - 1;
+                    rdy &= rdy - 1;
+                    int r = 1;
+                    if (lane == 0) r = ready(oldest + b) ? (issue(oldest + b) ? 1 : -1) : 0;
+                    r = __shfl_sync(0xffffffffu, r, 0);
+                    if (r < 0) {
+                        ok = 0;
+                        break;
+                    }
+                    if (r > 0) {
+                        pend &= ~(1u << b);
+                        progress = true;
                     }
                 }
+                if (!ok) break;
+            }
+            // bytes for job j: room at the head (wrapping to 0 wastes the end
+            // of the ring), and the entry's previous job has given its bytes back
+            if (j < n && j - oldest < kEntries) {
+                const StepJob &jb = job(j);
+                const uint32_t size = (uint32_t(M * jb.K * 2) + 127u) & ~127u;
+                bool room = false;
+                uint32_t off = 0, total = size;
+                if (used == 0) {                             // empty (head = tail = 0)
+                    room = size <= W;
+                } else if (tail < head) {                    // data in [tail, head)
+                    if (head + size <= W) {
+                        room = true;
+                        off = head;
+                    } else if (size <= tail) {
+                        room = true;
+                        total = W - head + size;
+                    }
+                } else if (head + size <= tail) {            // data in [tail, W) and [0, head); full if equal
+                    room = true;
+                    off = head;
+                }
                 if (room) {
-                    xstart[e] = start;                       // every lane writes the same values
+                    const int e = j % kEntries;
+                    xstart[e] = head;                        // every lane writes the same values
                     xtotal[e] = total;
                     used += total;
                     head = off + size;
                     if (head >= W) head = 0;
-                    break;
+                    __syncwarp();
+                    int r = 0;
+                    if (lane == 0) r = ready(j) ? (issue(j) ? 1 : -1) : 0;
+                    r = __shfl_sync(0xffffffffu, r, 0);
+                    if (r < 0) {
+                        ok = 0;
+                        break;
+                    }
+                    if (r == 0) pend |= 1u << (j - oldest);
+                    ++j;
+                    progress = true;
                 }
+            }
+            if (progress) {
+                t0 = globaltimer();
+            } else {
                 int stop = 0;
-                if (lane == 0) stop = *s_abort || globaltimer() - t0 > kWaitLimitNs;
+                if (lane == 0)
+                    stop = *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) || globaltimer() - t0 > kWaitLimitNs;
                 if (__shfl_sync(0xffffffffu, stop, 0)) {
                     ok = 0;
                     break;
                 }
-                __nanosleep(256);
+                __nanosleep(128);
             }
-            if (lane == 0 && ok) {
-                for (int w = 0; ok && w < jb.nwait; ++w) {
-                    const int d = jb.wait[w];
-                    const unsigned target = done_mul * unsigned(job(d).T);
-                    const unsigned long long t1 = globaltimer();
-                    while (!reached(ld_acquire_gpu(&p.job_done[d]), target)) {
-                        if (*s_abort || *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
-                            globaltimer() - t1 > kWaitLimitNs) {
-                            ok = 0;
-                            break;
-                        }
-                        __nanosleep(128);
-                    }
-                }
-                // the entry's previous fill has landed before its barrier is
-                // armed again (no compute warp of this CTA may have waited for
-                // it: the CTA can have had no tile of that job)
-                const bool used_e = xtag[e] >= 0;
-                if (ok && used_e && !mbar_wait(sbase + L.xbar + 8 * e, uint32_t(xtag[e] & 1))) ok = 0;
-                if (!ok) {
-                    fail(p, s_abort);
-                } else {
-                    // the window's last readers (generic proxy) and the data's
-                    // writers are ordered before the copy (async proxy)
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    const uint32_t bar = sbase + L.xbar + 8 * e, dst = sbase + L.xwin + off;
-                    const int par = used_e ? ((xtag[e] & 1) ^ 1) : 0;   // the phase this fill completes
-                    mbar_arrive_expect_tx(bar, uint32_t(M * jb.K * 2));
-                    for (int m = 0; m < M; ++m)
-                        bulk_load(dst + uint32_t(m * jb.K * 2), jb.x + size_t(m) * jb.K, uint32_t(jb.K * 2), bar);
-                    // job, offset and parity in one word: a reader that sees
-                    // the job waits for that phase on the barrier, which orders
-                    // the data
-                    *reinterpret_cast<volatile int *>(xtag + e) =
-                        (j << kTagJobShift) | int((off >> 7) << 1) | par;
-                }
-            }
-            __syncwarp();
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
+        if (!ok && lane == 0) fail(p, s_abort);
+        __syncwarp();
         // the last fill of every entry has landed before the CTA may exit
         if (lane == 0)
             for (int c = 0; c < kEntries; ++c)
                 if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xtag[c] & 1))) break;
     } else if (warp == kPubWarp) {
-        // ---------------- the publisher ----------------
-        // Makes this CTA's finished tiles of the waited-for jobs visible to
-        // every SM: snapshot the shared counters (acquire: the compute warps
-        // released them after writing the tiles' outputs), one GPU-scope
-        // fence for the whole batch, then one add per changed job.
-        if (p.n_pub > 0) {
+        // ---------------- the finisher and publisher ----------------
+        // Finisher (split jobs): takes the compute warps' posted part tiles
+        // (one per warp at a time, lane w for warp w): a GPU-scope fence and
+        // an arrival on the tile's counter each; the lane whose arrival
+        // completes a tile fences (acquire), and the warp adds the parts and
+        // writes the tile. Each taken tile then counts for publishing.
+        // Publisher: makes this CTA's finished units of the waited-for jobs
+        // visible to every SM: snapshot the shared counters (acquire: the
+        // units were counted after their outputs were written), one
+        // GPU-scope fence for the whole batch, then one add per changed job.
+        if (p.n_pub > 0 || p.split) {
+            int taken_l = 0;                              // lane w < kWarps: posts of warp w taken
             for (;;) {
                 const bool last = __shfl_sync(0xffffffffu, ld_acquire_cta_s32(s_warps_done) == kWarps || *s_abort, 0);
+                while (p.split) {
+                    int have = 0, e = 0, rt = 0, done = 0;
+                    if (lane < kWarps && ld_acquire_cta_s32(sbase + L.posted + 4 * lane) != taken_l) {
+                        const int2 pr = *reinterpret_cast<const int2 *>(smem + L.posts +
+                                                                         8 * (lane * kPosts + taken_l % kPosts));
+                        have = 1;
+                        e = pr.x;
+                        rt = pr.y;
+                        const StepJob &jb = job(e);
+                        fence_acq_rel_gpu_();
+                        const unsigned old = atomicAdd(&p.arrive[jb.sbase + rt], 1u);
+                        done = reached(old + 1u, done_mul * unsigned(((jb.flags >> kStepSplitShift) & 63) + 1));
+                        if (done) fence_acq_rel_gpu_();
+                    }
+                    if (!__any_sync(0xffffffffu, have)) break;
+                    __syncwarp();
+                    for (unsigned m = __ballot_sync(0xffffffffu, done); m; m &= m - 1) {
+                        const int w = __ffs(m) - 1;
+                        const int ew = __shfl_sync(0xffffffffu, e, w), rw = __shfl_sync(0xffffffffu, rt, w);
+                        complete_part(p, job(ew), rw, lane, M);
+                    }
+                    __syncwarp();                         // the rows written before the units count
+                    if (have) {
+                        const StepJob &jb = job(e);
+                        if (jb.flags & kStepPublish) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                        st_release_cta_s32(sbase + L.taken + 4 * lane, ++taken_l);
+                    }
+                }
                 bool any = false;
                 for (int i = lane; i < p.n_pub; i += 32) {
                     const unsigned c = unsigned(ld_acquire_cta_s32(sbase + L.cta_done + 4 * i));
@@ -438,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                     fence_acq_rel_gpu_();
                     for (int j = lane; j < n; j += 32) {
                         const StepJob &jb = job(j);
-                        if (!(jb.flags & kStepPublish)) continue;
+                        // every part counts into the job's slot; part 0's entry holds the counter
+                        if (!(jb.flags & kStepPublish) || (jb.flags & (63 << kStepPartShift))) continue;
                         const int i = jb.flags >> kStepPubShift;
                         const unsigned c = cta_snap[i];
                         if (c != cta_pub[i]) {
@@ -450,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                     }
                 }
                 if (last) break;
-                __nanosleep(500);
+                __nanosleep(p.split ? 128 : 500);
             }
         }
     } else {
@@ -462,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
         const uint32_t bars = sbase + L.bars + uint32_t(8 * warp * slots);
         const uint32_t descs = sbase + L.desc + uint32_t(16 * warp * slots);
         const uint32_t my_cur = sbase + L.wcur + 4 * warp, my_lb = sbase + L.wlb + 4 * warp;
+        const uint32_t my_posted = sbase + L.posted + 4 * warp, my_taken = sbase + L.taken + 4 * warp;
+        const uint32_t my_posts = sbase + L.posts + uint32_t(8 * kPosts * warp);
         const uint32_t aoff = opaque(segk::lane_code_offset(lane));
         const uint32_t soff = opaque(uint32_t(r * 144 + 128 + 2 * ((2 * t) % GP)));
         // x addresses: lane column r is token r / GP, group slot r % GP; the
@@ -504,12 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                 iend = true;
                 return;
             }
-            while (int(g) >= job(fj).tile0 + job(fj).T) ++fj;
+            while (int(g) >= job(fj).tile0 + ((job(fj).N + 15) >> 4)) ++fj;
             ijob = fj;
             itile = int(g) - job(fj).tile0;
             isg = 0;
             iS = job(fj).K >> 8;
-            iptr = job(fj).seg + size_t(itile) * size_t(iS) * kSegBytes;
+            iptr = job(fj).seg + size_t(itile) * size_t(job(fj).tstride) * kSegBytes;
             ihave = true;
             // every job the warp reads after its current one is >= this one's
             // (valid when every job's tile is at least a ring long: the tile
@@ -597,16 +795,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             if (!issue_next()) --in_flight;
             if (d.z == d.w - 1) {
                 const StepJob &jb = job(d.x);
-                finish_tile<MT>(acc, jb, d.y * 16, lane, M);
-                if (jb.flags & kStepPublish) {
-                    __syncwarp();
-                    if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                if (!(jb.flags & (63 << kStepSplitShift))) {
+                    finish_tile<MT>(acc, jb, d.y * 16, lane, M);
+                    if (jb.flags & kStepPublish) {
+                        __syncwarp();
+                        if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                    }
+                } else if (!post_part<MT>(acc, jb, d.x, d.y, lane, M, p, my_posted, my_taken, my_posts, s_abort)) {
+                    ok = false;      // (the finisher counts a posted tile: it is published once written)
                 }
             }
             if (++cslot == slots) {
                 cslot = 0;
                 cphase ^= 1u;
             }
+            if (!ok) break;
         }
         if (!ok && leader) fail(p, s_abort);
         // after a failed wait: the copies still in flight land before the CTA exits
@@ -656,11 +859,6 @@ const void *step_kernel(int M)
 
 }  // namespace
 
-size_t step_plan_layout_bytes(int n_jobs)
-{
-    return StepLayout(n_jobs).total;
-}
-
 // Ring slots, x window and cached jobs of a launch: two slots per compute
 // warp (measured: a larger x window pays more than deeper rings), the job
 // table cached while it leaves the window room for eight of the largest jobs'
@@ -690,13 +888,15 @@ bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh)
 
 zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
 {
-    const StepLayout l(plan->n_jobs);
+    const StepLayout l(plan->entries, plan->split_tiles, plan->part_records);
     uint8_t *base = static_cast<uint8_t *>(plan->dev);
     sp::Params p;
     p.hdr = reinterpret_cast<StepHeader *>(base + l.hdr);
     p.jobs = reinterpret_cast<const StepJob *>(base + l.jobs);
     p.job_done = reinterpret_cast<unsigned *>(base + l.job_done);
-    p.n_jobs = plan->n_jobs;
+    p.arrive = reinterpret_cast<unsigned *>(base + l.arrive);
+    p.work = reinterpret_cast<float *>(base + l.work);
+    p.n_jobs = plan->entries;
     p.total_tiles = plan->tiles;
     p.M = plan->M;
     p.n_pub = plan->n_pub;
@@ -705,7 +905,8 @@ zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.slots = sh.slots;
     p.wbytes = sh.wbytes;
     p.cached = sh.cached;
-    p.fine = plan->max_k >= 0 && plan->min_k / 256 >= sh.slots ? 1 : 0;
+    p.fine = plan->min_unit >= sh.slots ? 1 : 0;
+    p.split = plan->split_tiles > 0 ? 1 : 0;
     const void *kern = step_kernel(p.M);
     cudaError_t e = ensure_smem(kern, sh.smem, p.M == 1 ? step_smem_set : step_smem_set2);
     if (e != cudaSuccess) return cuda_status(e);

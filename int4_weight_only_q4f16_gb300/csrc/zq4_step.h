@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/zq4.h"
 
 namespace zq4 {
@@ -15,10 +17,33 @@ constexpr int kStepMaxM = 2;          // tokens the step engine handles
 constexpr int kStepWarps = 16;        // compute warps per CTA
 constexpr int kStepMaxWaits = 3;      // jobs one job may wait for
 
+// Work units: a 16-row tile of a job whose K is longer than kStepUnitSegs
+// segments of 256 columns, and which runs so late that a whole tile would
+// outlast the rest of the step, is split along K into C parts of at most
+// that many segments (C = ceil(S / kStepUnitSegs), part c = segments
+// [c S / C, (c + 1) S / C)). Each part is an entry of its own in the job
+// table (its columns of the weights and of x); the parts' fp32 sums meet in
+// a workspace and the last part of a tile to finish adds them in part order
+// and writes the tile.
+constexpr int kStepUnitSegs = 12;
+constexpr int kStepMaxSplit = 64;
+constexpr size_t kStepMaxWorkBytes = size_t(4) << 20;   // larger: no job is split
+
 // StepJob::flags
 constexpr int kStepGateUp = 1;        // interleaved gate/up rows, silu(g) * u output
-constexpr int kStepPublish = 2;       // a later job waits for this one: count its finished tiles
-constexpr int kStepPubShift = 8;      // bits 8..: index of the job among the waited-for ones
+constexpr int kStepPublish = 2;       // a later job waits for this one: count its finished units
+constexpr int kStepWaitShift = 2;     // bits 2..3: number of waits
+constexpr int kStepSplitShift = 4;    // bits 4..9: C - 1 (parts of the job)
+constexpr int kStepPartShift = 10;    // bits 10..15: c (this entry's part)
+constexpr int kStepPubShift = 16;     // bits 16..: index of the job among the waited-for ones
+constexpr int kStepMaxPub = 1 << 15;
+
+// Parts per tile of a job with K columns, when it is split.
+inline int step_split(int K)
+{
+    const int S = K / 256;
+    return S <= kStepUnitSegs ? 1 : std::min((S + kStepUnitSegs - 1) / kStepUnitSegs, kStepMaxSplit);
+}
 
 struct StepHeader {
     unsigned epoch;       // launches completed
@@ -28,29 +53,38 @@ struct StepHeader {
     unsigned pad[28];
 };
 
-// One job in run order. Its tiles are [tile0, tile0 + T) of the launch's tile
-// sequence; tile t's segment s is at seg + (t * (K / 256) + s) * 2304.
+// One entry of the job table: a job in run order, or one part of a split
+// job (its parts are consecutive entries, part 0 first). Its tiles are
+// [tile0, tile0 + (N + 15) / 16) of the launch's unit sequence; tile t's
+// segment s is at seg + (t * tstride + s) * 2304, s < K / 256 (a part's seg,
+// x and K are those of its columns; tstride = the whole job's K / 256, also
+// the row stride of x in units of 256 columns). Split jobs: tile t counts
+// its finished parts in arrive[sbase + t] and keeps part c of token m in
+// work[((pbase + c * tiles + t) * M + m) * 16 ...] (16 rows, fp32). The waits
+// name the entries of part 0 of the waited-for jobs.
 struct alignas(16) StepJob {
     const uint8_t *seg;   // the matrix in the segmented layout
-    const uint16_t *x;    // [M][K]
-    uint16_t *y;          // [M][y_stride]
-    int N, K, T, tile0;
+    const uint16_t *x;    // [M][tstride * 256]
+    uint16_t *y;          // [M][N] (gate_up: [M][N / 2])
+    int N, K, tstride, tile0;
     int flags;
-    int y_stride;         // N, or N / 2 for gate_up
-    int nwait;
-    int wait[kStepMaxWaits];   // positions (in run order) of the jobs to wait for
+    int sbase, pbase;     // split jobs: first arrival counter, first 16-float part record
+    int wait[kStepMaxWaits];   // entries of the jobs to wait for
 };
 static_assert(sizeof(StepJob) == 64, "step jobs are 64 bytes");
 
-// Device plan: header, job table, per-job finished-tile counters.
+// Device plan: header, job table, per-entry finished-unit counters, then the
+// split workspace: per split tile an arrival counter, and the parts' sums.
 struct StepLayout {
-    size_t hdr, jobs, job_done, total;
-    explicit StepLayout(int n_jobs)
+    size_t hdr, jobs, job_done, arrive, work, total;
+    StepLayout(int n_entries, long long split_tiles, long long part_records)
     {
         hdr = 0;
         jobs = 128;
-        job_done = jobs + size_t(n_jobs) * sizeof(StepJob);
-        total = (job_done + size_t(n_jobs) * 4 + 255) / 256 * 256;
+        job_done = jobs + size_t(n_entries) * sizeof(StepJob);
+        arrive = (job_done + size_t(n_entries) * 4 + 255) / 256 * 256;
+        work = (arrive + size_t(split_tiles) * 4 + 255) / 256 * 256;
+        total = work + size_t(part_records) * 64;
     }
 };
 
@@ -59,7 +93,6 @@ struct StepShape {
     int slots, wbytes, cached;
     size_t smem;
 };
-size_t step_plan_layout_bytes(int n_jobs);
 bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh);
 zq4_status step_check_resident(int M, int max_k, int n_jobs, int n_pub);
 zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s);

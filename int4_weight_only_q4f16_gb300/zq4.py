@@ -109,7 +109,8 @@ class StackPlanC(ctypes.Structure):
                 ("M", ctypes.c_int), ("grid", ctypes.c_int), ("max_k", ctypes.c_int),
                 ("max_tiles", ctypes.c_int), ("device", ctypes.c_int), ("engine", ctypes.c_int),
                 ("tiles", ctypes.c_int), ("n_pub", ctypes.c_int), ("gen", ctypes.c_int),
-                ("min_k", ctypes.c_int)]
+                ("min_unit", ctypes.c_int), ("split_tiles", ctypes.c_int), ("part_records", ctypes.c_int),
+                ("entries", ctypes.c_int)]
 
 
 lib = _load()

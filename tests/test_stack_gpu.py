@@ -60,6 +60,45 @@ def test_small_stack_matches_oracle(oracle, M):
             _check_job(oracle, job, what)
 
 
+@pytest.mark.parametrize("M", [1, 2])
+def test_step_engine_split_tiles_match_oracle(oracle, M):
+    """Tiles of long-K jobs split along K (K = 9728: 4 parts of 9, 10, 9, 10
+    segments; 3328: 6 + 7; 4096 and 4608: 8 + 8 and 9 + 9), a split gate_up
+    and a split job that waits for it included: every part's sums meet in
+    the plan's workspace and the last part adds them in part order, so three
+    runs (counters advancing across launches) give the same bits, each
+    matching the oracle."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    rng = synth.rng_for("step_split", M)
+    spec = [(200, 9728, False), (72, 3328, False), (9216, 4096, True)] + [(256, 3072, False)] * 6 + \
+        [(88, 4608, False), (333, 3072, False)]
+    jobs, mats = [], []
+    for i, (N, K, gu) in enumerate(spec):
+        wq_h, sc_h = synth.weight("step_split_w", N, K, i)
+        seg = zq4.prepare_weight(dev(wq_h), dev(sc_h), N, K, zq4.PREP_SEGMENTED)[0]
+        x = jobs[2][2] if i == 9 else dev(synth.activations(rng, M, K))      # job 9 reads job 2's output
+        y = torch.full((M, N // 2 if gu else N), float("nan"), dtype=torch.float16, device="cuda")
+        jobs.append((seg, x, y, N, K, gu))
+        mats.append((wq_h, sc_h))
+    plan = zq4.StackPlan(jobs, M)
+    assert plan.plan.engine == 1 and plan.plan.split_tiles > 0
+    first = None
+    for run in range(3):
+        for j in jobs:
+            j[2].fill_(float("nan"))
+        plan.run()
+        torch.cuda.synchronize()
+        assert zq4.device_errors(clear=True) == 0
+        bits = [host_f16(j[2]).view(np.uint16).copy() for j in jobs]
+        if first is None:
+            first = bits
+            for i, ((seg, x, y, N, K, gu), (wq_h, sc_h)) in enumerate(zip(jobs, mats)):
+                _check_job(oracle, (dev(wq_h), dev(sc_h), x, y, N, K, gu), f"M={M} split job {i}")
+        else:
+            for i, (a, b) in enumerate(zip(first, bits)):
+                assert np.array_equal(a, b), f"M={M} run {run} job {i} differs from run 0"
+
+
 CHAIN_LAYER = (("qkv", 768, 256), ("o", 256, 512), ("gate_up", 1024, 256), ("down", 256, 512))
 CHAIN_HEAD = ("lm_head", 333, 256)
 

@@ -89,11 +89,13 @@ def test_decode_layers_run_down_after_the_next_layers_projections(zq4):
                  (W, buf(b + 4), buf(b + 5), 16384, 3072, 1), (W, buf(b + 5), buf(b + 6), 3072, 8192, 0)]
     jobs.append((W, buf(99), buf(98), 32064, 3072, 0))
     order, dep = zq4.stack_plan_waits(jobs, 1)
-    # down of layer l waits for its gate_up; it is put after at least
-    # 2 x 152 x 16 tiles' worth of that gate_up's segments (58,368): the next
-    # two layers' qkv, o and gate_up where there are any; the head, which
-    # touches no other job's bytes and is the largest such job, runs last
-    assert order == [0, 1, 2, 4, 5, 6, 8, 9, 10, 3, 7, 11, 12]
+    # down of layer l waits for its gate_up. A job some later job waits for
+    # (each gate_up) goes before up to 12 independent jobs ahead of it, so
+    # the three gate_ups run first; each down is put after at least
+    # 2 x 152 x 16 tiles' worth of its gate_up's segments (58,368) where
+    # there is that much work. The head, which touches no other job's bytes
+    # and is the largest such job, runs last
+    assert order == [2, 6, 10, 0, 1, 4, 5, 8, 9, 3, 7, 11, 12]
     assert dep == [-1, -1, -1, 2, -1, -1, -1, 6, -1, -1, -1, 10, -1]
     check_valid(jobs, 1, order, dep)
 
