@@ -77,7 +77,7 @@ ZQ4_API int zq4_last_cuda_error(void);
 ZQ4_API int zq4_version(void);
 
 /* Bits of the library's device error word. */
-#define ZQ4_DEVERR_WAIT_TIMEOUT 1u   /* a kernel gave up an internal wait (2 s) */
+#define ZQ4_DEVERR_WAIT_TIMEOUT 1u   /* a kernel gave up an internal wait (2 s; stack plans: their set limit) */
 
 /*
  * zq4_device_errors -- read (and with clear != 0, reset) the device error
@@ -461,6 +461,7 @@ typedef struct zq4_stack_plan {
     int split_tiles;
     int part_records;
     int entries;
+    unsigned long long wait_ns;   /* device-wait limit (zq4_stack_plan_set_wait_limit) */
 } zq4_stack_plan;
 
 /*
@@ -513,6 +514,20 @@ ZQ4_API zq4_status zq4_stack_plan_init(const zq4_stack_job *jobs, int n_jobs, in
  * zq4_stack_plan_init_static has replaced), ZQ4_ERR_CUDA.
  */
 ZQ4_API zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream);
+
+/*
+ * zq4_stack_plan_set_wait_limit -- how long (ns) a device-side wait of the
+ * plan's kernel may last before it gives up: a job waiting for the jobs it
+ * depends on, a warp waiting for its x, a warp waiting for room to post a
+ * finished part. The init calls set 2 s; 0 restores that. When a wait
+ * gives up, the kernel sets ZQ4_DEVERR_WAIT_TIMEOUT and the plan's abort
+ * flag, every other wait of the launch sees the flag (or runs out in turn),
+ * each warp lets the copies it issued land, and the launch ends; the plan
+ * must then be initialised again. Waits for a bulk copy of this launch to
+ * land keep their own 2 s bound (such a copy always completes). Errors:
+ * ZQ4_ERR_NULL.
+ */
+ZQ4_API zq4_status zq4_stack_plan_set_wait_limit(zq4_stack_plan *plan, unsigned long long ns);
 
 /*
  * zq4_stack_plan_init_static -- zq4_stack_plan_init for callers that cannot

@@ -500,6 +500,13 @@ zq4_status zq4_stack_run(const zq4_stack_plan *plan, void *stream)
     return stack_run(plan, static_cast<cudaStream_t>(stream));
 }
 
+zq4_status zq4_stack_plan_set_wait_limit(zq4_stack_plan *plan, unsigned long long ns)
+{
+    if (!plan) return ZQ4_ERR_NULL;
+    plan->wait_ns = ns ? ns : 2000000000ull;   // the default: 2 s
+    return ZQ4_OK;
+}
+
 zq4_status zq4_stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, zq4_stack_plan *plan,
                                       void *stream)
 {

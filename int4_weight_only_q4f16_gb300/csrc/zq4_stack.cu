@@ -137,6 +137,7 @@ struct Params {
     int n_jobs, M, max_k;
     int x_bufs;          // x buffers in shared memory (1 .. kMaxXBufs)
     int cached;          // jobs [0, cached) are copied to shared memory at start
+    unsigned long long wait_ns;   // how long a wait on another warp or CTA may last
 };
 
 constexpr size_t kRingOff = 0;
@@ -266,16 +267,16 @@ __device__ __forceinline__ int ld_acquire_cta(const int *p)
     return v;
 }
 // Wait (bounded) until *p >= v; false once the wait has lasted longer than
-// kWaitLimitNs. Between polls the warp sleeps, leaving its issue slots to the
+// `limit` ns. Between polls the warp sleeps, leaving its issue slots to the
 // warps that do the work.
-__device__ __forceinline__ bool wait_at_least(const int *p, int v)
+__device__ __forceinline__ bool wait_at_least(const int *p, int v, unsigned long long limit)
 {
     if (ld_acquire_cta(p) >= v) return true;
     const unsigned long long t0 = globaltimer();
     for (unsigned i = 0;; ++i) {
         __nanosleep(32);
         if (ld_acquire_cta(p) >= v) return true;
-        if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) return false;
+        if ((i & 15u) == 15u && globaltimer() - t0 > limit) return false;
     }
 }
 
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 t0 = globaltimer();
             } else {
                 // no slot free: the compute warps are busy or between jobs
-                if (globaltimer() - t0 > kWaitLimitNs) {
+                if (globaltimer() - t0 > p.wait_ns) {
                     timed_out = true;
                     break;
                 }
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
         // lane acquires first.
         if (lane == 0) {
             for (int j = 0; j < n; ++j) {
-                if (!wait_at_least(s_rdone, j + 1)) {
+                if (!wait_at_least(s_rdone, j + 1, p.wait_ns)) {
                     atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
                     atomicOr(&p.hdr->abort, 1u);
                     *s_abort = 1;
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             const Job &jb = job(j);
             if (lane == 0) st_release_cta(s_xprog, j);       // every earlier job's x is in place
             if ((jb.flags >> kDepShift) != 0) continue;
-            if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs)) {
+            if (j >= p.x_bufs && !wait_at_least(s_xfree, j + 1 - p.x_bufs, p.wait_ns)) {
                 stop = true;
                 break;
             }
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 // dep: thread 0 waits, the barrier passes its acquire on) or
                 // there is no buffer to stage ahead into: the compute threads
                 // stage x, all loads in one round trip
-                if (threadIdx.x == 0 && !wait_at_least(s_xprog, j)) {
+                if (threadIdx.x == 0 && !wait_at_least(s_xprog, j, p.wait_ns)) {
                     atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
                     atomicOr(&p.hdr->abort, 1u);
                     *s_abort = 1;
@@ -595,7 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
                 if (threadIdx.x == 0 && dep >= 0) {
                     const unsigned long long t0 = globaltimer();
                     while (int(ld_acquire(&p.job_cnt[dep]) - target) < 0) {   // wrap-safe: counters grow across launches
-                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                        if (*s_abort || *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
+                            globaltimer() - t0 > p.wait_ns) {
                             atomicOr(&g_stack_error, ZQ4_DEVERR_WAIT_TIMEOUT);
                             atomicOr(&p.hdr->abort, 1u);
                             *s_abort = 1;
@@ -627,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack(Params p)
             for (int u = ub; u < ue && ok; ++u) {
                 // x chunk sg of this job (segment sg of a tile covers columns 256 sg ..)
                 if (!((seen >> sg) & 1ull)) {
-                    if (!__all_sync(0xffffffffu, wait_at_least(s_chunk + sg, j + 1))) {
+                    if (!__all_sync(0xffffffffu, wait_at_least(s_chunk + sg, j + 1, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -1230,6 +1232,7 @@ void fill_plan(zq4_stack_plan *plan, const zq4_stack_job *jobs, const int *order
     plan->tiles = int(info.tiles);
     plan->n_pub = info.n_pub;
     plan->gen = gen;
+    plan->wait_ns = kWaitLimitNs;
 }
 
 }  // namespace
@@ -1373,6 +1376,7 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.M = plan->M;
     p.max_k = plan->max_k;
     p.cached = st::cached_jobs(p.n_jobs, p.M, p.max_k);
+    p.wait_ns = plan->wait_ns ? plan->wait_ns : kWaitLimitNs;
     p.x_bufs = st::x_buffers(p.M, p.max_k);
     void *args[] = {&p};
     return cuda_status(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(st::k_stack), dim3(plan->grid),

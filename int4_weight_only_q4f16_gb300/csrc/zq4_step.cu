@@ -57,7 +57,8 @@
 //  * Counters grow monotonically across launches (targets scale with the
 //    launch index); the last CTA to finish resets the tile counter and
 //    advances the launch index.
-//  * Every wait is bounded (2 s). A timeout sets ZQ4_DEVERR_WAIT_TIMEOUT and
+//  * Every wait is bounded (the plan's limit, 2 s unless the caller set
+//    another; a wait for a bulk copy to land: 2 s). A timeout sets ZQ4_DEVERR_WAIT_TIMEOUT and
 //    the plan's abort flag, which every waiter checks; each warp lets the
 //    copies it issued land before it exits; the plan must then be
 //    initialised again.
@@ -98,6 +99,7 @@ struct Params {
     int n_jobs, total_tiles, M, slots, wbytes, cached, n_pub;
     int fine;                // every work unit is at least `slots` segments long
     int split;               // some job is split into parts
+    unsigned long long wait_ns;   // how long a wait on another warp or CTA may last
 };
 
 // Finished tiles of split parts, posted by each compute warp to the
@@ -319,7 +321,7 @@ __device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &
         const int n = int(lds_u32(posted));
         const unsigned long long t0 = globaltimer();
         while (n - ld_acquire_cta_s32(taken) >= kPosts) {
-            if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+            if (*s_abort || globaltimer() - t0 > p.wait_ns) {
                 ok = 0;
                 break;
             }
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
             } else {
                 int stop = 0;
                 if (lane == 0)
-                    stop = *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) || globaltimer() - t0 > kWaitLimitNs;
+                    stop = *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) || globaltimer() - t0 > p.wait_ns;
                 if (__shfl_sync(0xffffffffu, stop, 0)) {
                     ok = 0;
                     break;
@@ -769,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                     for (;;) {
                         v = *reinterpret_cast<volatile int *>(smem + L.xtag + 4 * e);
                         if (v >= 0 && (v >> kTagJobShift) == d.x) break;
-                        if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+                        if (*s_abort || globaltimer() - t0 > p.wait_ns) {
                             v = -1;
                             break;
                         }
@@ -907,6 +909,7 @@ zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s)
     p.cached = sh.cached;
     p.fine = plan->min_unit >= sh.slots ? 1 : 0;
     p.split = plan->split_tiles > 0 ? 1 : 0;
+    p.wait_ns = plan->wait_ns ? plan->wait_ns : kWaitLimitNs;
     const void *kern = step_kernel(p.M);
     cudaError_t e = ensure_smem(kern, sh.smem, p.M == 1 ? step_smem_set : step_smem_set2);
     if (e != cudaSuccess) return cuda_status(e);

@@ -37,7 +37,7 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_stack_plan_set_wait_limit", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
            "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine",
            "zq4_add_rmsnorm_work_bytes", "zq4_gemv_add_rmsnorm", "zq4_qkv_rope_append")
 
@@ -74,6 +74,7 @@ def _load():
         "zq4_dequant_f32": [P, P, P, I, I, P],
         "zq4_dequant_f16": [P, P, P, I, I, P],
         "zq4_stack_plan_bytes": [P, I, I, P],
+        "zq4_stack_plan_set_wait_limit": [P, ctypes.c_ulonglong],
         "zq4_stack_plan_waits": [P, I, I, P, P],
         "zq4_gemv_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
@@ -110,7 +111,7 @@ class StackPlanC(ctypes.Structure):
                 ("max_tiles", ctypes.c_int), ("device", ctypes.c_int), ("engine", ctypes.c_int),
                 ("tiles", ctypes.c_int), ("n_pub", ctypes.c_int), ("gen", ctypes.c_int),
                 ("min_unit", ctypes.c_int), ("split_tiles", ctypes.c_int), ("part_records", ctypes.c_int),
-                ("entries", ctypes.c_int)]
+                ("entries", ctypes.c_int), ("wait_ns", ctypes.c_ulonglong)]
 
 
 lib = _load()
@@ -384,6 +385,9 @@ def dequant_f16(wq, scales, N, K, out=None, stream=None):
     return out
 
 
+DEVERR_WAIT_TIMEOUT = 1          # ZQ4_DEVERR_WAIT_TIMEOUT
+
+
 def device_errors(clear: bool = True) -> int:
     """Device error word (ZQ4_DEVERR_* bits); synchronises the device."""
     v = ctypes.c_uint32(0)
@@ -439,6 +443,11 @@ class StackPlan:
 
     def run(self, stream=None):
         _check("zq4_stack_run", lib.zq4_stack_run(ctypes.byref(self.plan), _stream(stream)))
+
+    def set_wait_limit(self, ns):
+        """How long (ns) a device-side wait may last before the launch gives
+        up (0: the default, 2 s)."""
+        _check("zq4_stack_plan_set_wait_limit", lib.zq4_stack_plan_set_wait_limit(ctypes.byref(self.plan), int(ns)))
 
 
 class StaticStackPlan:

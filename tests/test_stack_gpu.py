@@ -369,3 +369,50 @@ def test_step_engine_job_that_waits_for_two_jobs(oracle):
         x = xs[3 + i] if i < 6 else xs[9 + i - 6]
         y_ref, S = oracle.gemv(w, s, host_f16(x), N, K)
         assert_within(host_f16(fill[i]), y_ref, S, f"independent job {i}")
+
+
+def test_step_wait_runs_out_then_a_new_plan_runs(oracle):
+    """The bounded-wait recovery path, with host-built data only: the last
+    entry of a one-token plan's job table is made to wait for itself (a
+    counter nothing ever adds to: it is no waited-for job). With a 5 ms
+    limit the launch gives up, reports ZQ4_DEVERR_WAIT_TIMEOUT and ends (no
+    kernel left waiting); a plan initialised again over the same jobs then
+    runs and matches the oracle."""
+    import time
+    from int4_weight_only_q4f16_gb300 import zq4
+    M, N, K = 1, 256, 512
+    rng = synth.rng_for("step_timeout")
+    mats = [synth.weight("step_timeout_w", N, K, i) for i in range(10)]
+    jobs = []
+    for wq_h, sc_h in mats:
+        seg = zq4.prepare_weight(dev(wq_h), dev(sc_h), N, K, zq4.PREP_SEGMENTED)[0]
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        jobs.append((seg, dev(synth.activations(rng, M, K)), y, N, K, False))
+    plan = zq4.StackPlan(jobs, M)
+    assert plan.plan.engine == 1 and plan.plan.entries == len(jobs)
+    # job-table entry e: 64 bytes at 128 + 64 e; int32 word 10 = flags (bits
+    # 2-3: number of waits, bit 1: waited for), word 13 = its first wait
+    e = plan.plan.entries - 1
+    img = plan.buffer.cpu()
+    words = img[128 + 64 * e:128 + 64 * (e + 1)].view(torch.int32)
+    flags = int(words[10])
+    assert (flags >> 2) & 3 == 0 and not flags & 2
+    words[10] = flags | (1 << 2)
+    words[13] = e
+    plan.buffer.copy_(img)
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    plan.set_wait_limit(5_000_000)
+    t0 = time.perf_counter()
+    plan.run()
+    torch.cuda.synchronize()
+    took = time.perf_counter() - t0
+    assert zq4.device_errors(clear=True) & zq4.DEVERR_WAIT_TIMEOUT
+    assert took < 1.0, f"the launch took {took:.3f} s: it should give up after the 5 ms limit"
+    again = zq4.StackPlan(jobs, M)
+    again.run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    for i, ((seg, x, y, N_, K_, gu), (wq_h, sc_h)) in enumerate(zip(jobs, mats)):
+        y_ref, S = oracle.gemv(wq_h, sc_h, host_f16(x), N_, K_)
+        assert_within(host_f16(y), y_ref, S, f"job {i} after the re-initialised plan")
