@@ -556,15 +556,16 @@ def run_lmhead(args, torch, dist, peaks, peak_kind):
 
 def run_qwen3(args, torch, dist, peaks, peak_kind):
     from int4_weight_only_q4f16_gb300 import stack as stack_mod, zq4
-    st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode if args.m <= 8 else "calls")  # M > 8: canonical only
+    st = stack_mod.qwen3_4b_stack(M=args.m, mode=args.stack_mode)
     stream = torch.cuda.Stream()
     if st.mode == "plan":
         try:
             st.build_plan(stream)
-        except zq4.Zq4Error as e:     # x of the widest projection does not fit beside the rings
+        except zq4.Zq4Error as e:     # a plan the library cannot run as one launch
             if "UNSUPPORTED" not in str(e):
                 raise
             st.mode = "calls"
+    engine = {0: "k_stack", 1: "k_step", 2: "k_wide"}.get(st.plan.plan.engine) if st.mode == "plan" else None
     with torch.cuda.stream(stream):
         st.launch_step(stream)
     g = st.capture(stream)
@@ -578,7 +579,7 @@ def run_qwen3(args, torch, dist, peaks, peak_kind):
             "hbm_gbs": round(b / step / 1e9, 1), "frac_of_measured": round(b / step / 1e9 / peaks["hbm_gbs"], 4),
             "launches_per_step": st.launches_per_step(),
             "config": {"workload": f"qwen3-4b 36-layer projection stack, M={st.M}",
-                       "bytes_per_step": b, "stack_mode": st.mode}}
+                       "bytes_per_step": b, "stack_mode": st.mode, "engine": engine}}
 
 
 def run_moe(args, torch, dist, peaks, peak_kind):

@@ -701,7 +701,9 @@ namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-enum Engine { kEngineStack = 0, kEngineStep = 1 };
+enum Engine { kEngineStack = 0, kEngineStep = 1, kEngineWide = 2 };
+// engines that run the step plan (job entries, split parts, finisher)
+inline bool step_like(int engine) { return engine == kEngineStep || engine == kEngineWide; }
 
 // Largest dynamic shared memory k_stack has been allowed per device: one
 // record for every caller, so the limit only ever grows.
@@ -778,24 +780,24 @@ SplitTotals split_totals(const zq4_stack_job *jobs, int n, int M, const int *ord
 // need no initial value).
 size_t plan_bytes_for(int engine, const zq4_stack_job *jobs, int n, int M, const int *order)
 {
-    if (engine != kEngineStep) return layout_for(n).total;
+    if (!step_like(engine)) return layout_for(n).total;
     const SplitTotals t = split_totals(jobs, n, M, order);
-    return StepLayout(t.entries, t.tiles, t.records).total;
+    return StepLayout(t.entries, t.tiles, t.records, engine == kEngineWide).total;
 }
 // `entries`: job-table entries (the step engine), else jobs
 size_t image_bytes_for(int engine, int entries)
 {
-    return engine == kEngineStep ? StepLayout(entries, 0, 0).arrive : layout_for(entries).total;
+    return step_like(engine) ? StepLayout(entries, 0, 0, engine == kEngineWide).arrive : layout_for(entries).total;
 }
 int entries_for(int engine, const zq4_stack_job *jobs, int n, int M, const int *order)
 {
-    return engine == kEngineStep ? split_totals(jobs, n, M, order).entries : n;
+    return step_like(engine) ? split_totals(jobs, n, M, order).entries : n;
 }
 
 zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, int *max_k, int *max_tiles)
 {
     if (!jobs) return ZQ4_ERR_NULL;
-    if (n_jobs <= 0 || M < 1 || M > st::kTokCols) return ZQ4_ERR_SHAPE;
+    if (n_jobs <= 0 || M < 1 || M > kWideMaxM) return ZQ4_ERR_SHAPE;
     int mk = 0, mt = 0;
     long long tiles = 0;
     for (int j = 0; j < n_jobs; ++j) {
@@ -822,6 +824,7 @@ zq4_status check_jobs(const zq4_stack_job *jobs, int n_jobs, int M, int grid, in
 // What only the stack engine (k_stack) requires.
 zq4_status stack_engine_fits(int M, int max_k)
 {
+    if (M > st::kTokCols) return ZQ4_ERR_UNSUPPORTED;                       // eight tokens at most
     if (max_k > st::kMaxChunks * st::kSegCols) return ZQ4_ERR_UNSUPPORTED;   // x staged in at most 64 chunks
     if (st::smem_bytes(M, max_k) > size_t(227) * 1024) return ZQ4_ERR_UNSUPPORTED;
     return ZQ4_OK;
@@ -1037,17 +1040,21 @@ int tight_waits(int n, const int *order, const int *dep, const SchedScratch &sc)
 // eight waits for a job placed shortly before it (k_step computes a whole
 // tile per warp: a job's last tiles take a tile's time, which a waiting job
 // pays in full, where k_stack splits every tile of a job over a CTA's warps);
-// else k_stack.
+// else k_stack. Three to sixteen tokens: k_wide under the same rule (for
+// nine tokens and more whatever the waits, as long as each job needs at most
+// kStepMaxWaits: k_stack holds eight).
 int choose_engine(const zq4_stack_job *jobs, int n, int M, const int *order, const int *dep, const SchedScratch &sc)
 {
-    if (M <= kStepMaxM && n < kStepMaxPub && 8 * tight_waits(n, order, dep, sc) <= n &&
-        wait_lists(jobs, n, M, order, sc))
-        return kEngineStep;
+    if (n >= kStepMaxPub) return kEngineStack;
+    const bool loose = 8 * tight_waits(n, order, dep, sc) <= n;
+    if (M <= kStepMaxM && loose && wait_lists(jobs, n, M, order, sc)) return kEngineStep;
+    if (M > kStepMaxM && (loose || M > st::kTokCols) && wait_lists(jobs, n, M, order, sc)) return kEngineWide;
     return kEngineStack;
 }
 
 // What write_image reports besides the image.
 struct ImageInfo {
+    bool ok = true;           // false: a tensor map could not be encoded
     long long tiles = 0;      // work units of the launch
     int entries = 0;          // job-table entries (step engine: a split job has one per part)
     int n_pub = 0;            // jobs another job waits for (step engine)
@@ -1063,7 +1070,7 @@ void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int 
                  const SchedScratch &sc, int G, uint8_t *host, ImageInfo *info)
 {
     *info = ImageInfo();
-    if (engine == kEngineStack) {
+    if (!step_like(engine)) {
         memset(host, 0, image_bytes_for(engine, n));
         info->entries = n;
         st::Job *t = reinterpret_cast<st::Job *>(host + layout_for(n).jobs);
@@ -1077,7 +1084,8 @@ void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int 
     }
     const SplitTotals split = split_totals(jobs, n, M, order);
     memset(host, 0, image_bytes_for(engine, split.entries));
-    StepJob *t = reinterpret_cast<StepJob *>(host + StepLayout(split.entries, 0, 0).jobs);
+    const StepLayout lay(split.entries, 0, 0, engine == kEngineWide);
+    StepJob *t = reinterpret_cast<StepJob *>(host + lay.jobs);
     // the entry of part 0 of each position
     int e = 0;
     for_each_split(jobs, n, order, [&](int r, int Cr) {
@@ -1111,6 +1119,10 @@ void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int 
             jb.sbase = C > 1 ? int(sbase) : 0;
             jb.pbase = C > 1 ? int(pbase) : 0;
             for (int w = 0; w < kStepMaxWaits; ++w) jb.wait[w] = w < sc.nwait[r] ? sc.first[sc.waits[r][w]] : 0;
+            // k_wide: the entry's x columns as a tensor map of [M][256] boxes
+            if (engine == kEngineWide &&
+                !wide_x_map(host + lay.tmaps + size_t(sc.first[r] + c) * 128, jb.x, M, jb.K, b.K))
+                info->ok = false;
             tile0 += rows;
             min_unit = std::min(min_unit, len);
         }
@@ -1131,8 +1143,8 @@ void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int 
 zq4_status upload_plan(void *dev, const uint8_t *image, int engine, const ImageInfo &info, cudaStream_t s)
 {
     cudaError_t e = cudaMemcpyAsync(dev, image, image_bytes_for(engine, info.entries), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && engine == kEngineStep && info.split_tiles > 0) {
-        const StepLayout l(info.entries, info.split_tiles, info.part_records);
+    if (e == cudaSuccess && step_like(engine) && info.split_tiles > 0) {
+        const StepLayout l(info.entries, info.split_tiles, info.part_records, engine == kEngineWide);
         e = cudaMemsetAsync(static_cast<uint8_t *>(dev) + l.arrive, 0, l.work - l.arrive, s);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -1151,6 +1163,7 @@ size_t launch_smem(int n_jobs, int M, int max_k)
 zq4_status check_resident(int engine, int n_jobs, int M, int max_k, int n_pub)
 {
     if (engine == kEngineStep) return step_check_resident(M, max_k, n_jobs, n_pub);
+    if (engine == kEngineWide) return wide_check_resident(M, n_jobs, n_pub);
     const size_t smem = launch_smem(n_jobs, M, max_k);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(st::k_stack), smem, stack_smem_set);
     if (e != cudaSuccess) return cuda_status(e);
@@ -1252,6 +1265,7 @@ zq4_status stack_plan_init(const zq4_stack_job *jobs, int n_jobs, int M, void *d
     std::vector<uint8_t> host(image_bytes_for(engine, entries_for(engine, jobs, n_jobs, M, b.order.data())));
     ImageInfo info;
     write_image(engine, jobs, n_jobs, M, b.order.data(), b.dep.data(), b.scratch(), grid, host.data(), &info);
+    if (!info.ok) return ZQ4_ERR_UNSUPPORTED;
     // the kernel needs every CTA resident at once
     stt = check_resident(engine, info.entries, M, mk, info.n_pub);
     if (stt != ZQ4_OK) return stt;
@@ -1331,12 +1345,13 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     int engine, mk, mt;
     zq4_status stt = plan_common(jobs, n_jobs, M, grid, g_static_order, g_static_dep, sc, &engine, &mk, &mt);
     if (stt != ZQ4_OK) return stt;
-    if (engine == kEngineStep && n_jobs > kStaticMaxJobsStep) return ZQ4_ERR_UNSUPPORTED;
+    if (step_like(engine) && n_jobs > kStaticMaxJobsStep) return ZQ4_ERR_UNSUPPORTED;
     if (image_bytes_for(engine, entries_for(engine, jobs, n_jobs, M, g_static_order)) > kStaticPlanBytes ||
         plan_bytes_for(engine, jobs, n_jobs, M, g_static_order) > kStaticDevBytes)
         return ZQ4_ERR_UNSUPPORTED;
     ImageInfo info;
     write_image(engine, jobs, n_jobs, M, g_static_order, g_static_dep, sc, grid, g_static_image, &info);
+    if (!info.ok) return ZQ4_ERR_UNSUPPORTED;
     stt = check_resident(engine, info.entries, M, mk, info.n_pub);
     if (stt != ZQ4_OK) return stt;
     void *dev = nullptr;
@@ -1365,6 +1380,7 @@ zq4_status stack_run(const zq4_stack_plan *plan, cudaStream_t s)
             return ZQ4_ERR_SHAPE;
     }
     if (plan->engine == kEngineStep) return step_run(plan, s);
+    if (plan->engine == kEngineWide) return wide_run(plan, s);
     if (plan->engine != kEngineStack) return ZQ4_ERR_SHAPE;
     const Layout l = layout_for(plan->n_jobs);
     uint8_t *base = static_cast<uint8_t *>(plan->dev);

@@ -63,6 +63,7 @@
 //    copies it issued land before it exits; the plan must then be
 //    initialised again.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -100,6 +101,8 @@ struct Params {
     int fine;                // every work unit is at least `slots` segments long
     int split;               // some job is split into parts
     unsigned long long wait_ns;   // how long a wait on another warp or CTA may last
+    const CUtensorMap *tmaps;     // k_wide: per entry, x[M][K] in boxes of [M][256]
+    int slot_bytes;               // k_wide: one segment and its x
 };
 
 // Finished tiles of split parts, posted by each compute warp to the
@@ -173,6 +176,12 @@ __device__ __forceinline__ int4 lds_s4(uint32_t saddr)
 {
     int4 v;
     asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+__device__ __forceinline__ int2 lds_s2(uint32_t saddr)
+{
+    int2 v;
+    asm volatile("ld.shared.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr));
     return v;
 }
 __device__ __forceinline__ void fence_acq_rel_gpu_() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -299,29 +308,18 @@ __device__ __forceinline__ float *part_record(const Params &p, const StepJob &jb
     return p.work + (size_t(jb.pbase) + size_t(rt)) * size_t(M) * 16 + part_floats(jb, M) * size_t(c);
 }
 
-// A compute warp's finished tile rt of one part of a split job: its sums
-// into the part's record, then (lane 0, once the ring has room) a post to
-// the finisher. False if the finisher never made room (a bounded wait).
-template <int MT>
-__device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &jb, int entry, int rt, int lane, int M,
-                                          const Params &p, uint32_t posted, uint32_t taken, uint32_t posts,
-                                          volatile int *s_abort)
+// Lane 0 posts (entry, tile) to the finisher once the warp's ring of posts
+// has room; false (every lane) if the finisher never made room (a bounded
+// wait). The caller's writes of the part's sums come before (__syncwarp).
+__device__ __forceinline__ bool post_tile(int entry, int rt, int lane, uint32_t posted, uint32_t taken,
+                                          uint32_t posts, volatile int *s_abort, unsigned long long limit)
 {
-    float v0, v1;
-    tile_sums<MT>(acc, v0, v1);
-    const int r = lane >> 2, tok = MT == 1 ? 0 : ((lane & 3) >> 1);
-    float *rec = part_record(p, jb, rt, (jb.flags >> kStepPartShift) & 63, M) + size_t(tok) * 16 + r;
-    if (holder_lane<MT>(lane, M)) {
-        rec[0] = v0;
-        rec[8] = v1;
-    }
-    __syncwarp();
     int ok = 1;
     if (lane == 0) {
         const int n = int(lds_u32(posted));
         const unsigned long long t0 = globaltimer();
         while (n - ld_acquire_cta_s32(taken) >= kPosts) {
-            if (*s_abort || globaltimer() - t0 > p.wait_ns) {
+            if (*s_abort || globaltimer() - t0 > limit) {
                 ok = 0;
                 break;
             }
@@ -336,6 +334,25 @@ __device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// A compute warp's finished tile rt of one part of a split job (one or two
+// tokens): its sums into the part's record, then a post to the finisher.
+template <int MT>
+__device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &jb, int entry, int rt, int lane, int M,
+                                          const Params &p, uint32_t posted, uint32_t taken, uint32_t posts,
+                                          volatile int *s_abort)
+{
+    float v0, v1;
+    tile_sums<MT>(acc, v0, v1);
+    const int r = lane >> 2, tok = MT == 1 ? 0 : ((lane & 3) >> 1);
+    float *rec = part_record(p, jb, rt, (jb.flags >> kStepPartShift) & 63, M) + size_t(tok) * 16 + r;
+    if (holder_lane<MT>(lane, M)) {
+        rec[0] = v0;
+        rec[8] = v1;
+    }
+    __syncwarp();
+    return post_tile(entry, rt, lane, posted, taken, posts, s_abort, p.wait_ns);
+}
+
 // A tile of a split job whose parts have all arrived (the whole warp, after
 // the arrival that completed it and an acquire fence): every part's sums
 // read back and added in part order (the same order whichever part arrived
@@ -343,20 +360,22 @@ __device__ __forceinline__ bool post_part(const float (&acc)[4], const StepJob &
 __device__ __forceinline__ void complete_part(const Params &p, const StepJob &jb, int rt, int lane, int M)
 {
     const int C = ((jb.flags >> kStepSplitShift) & 63) + 1;
-    const int tok = lane >> 4, row = lane & 15;
-    float v = 0.f;
-    if (tok < M) {
-        const float *rec = part_record(p, jb, rt, 0, M) + size_t(tok) * 16 + row;
-        const size_t step = part_floats(jb, M);
-        for (int c = 0; c < C; ++c) v += __ldcg(rec + step * size_t(c));
-    }
-    const int n = rt * 16 + row;
-    if (!(jb.flags & kStepGateUp)) {
-        if (tok < M && n < jb.N) jb.y[size_t(tok) * jb.N + n] = float_to_f16_bits(v);
-    } else {
-        const float u = __shfl_down_sync(0xffffffffu, v, 1);
-        if (tok < M && (row & 1) == 0 && n + 1 < jb.N)
-            jb.y[size_t(tok) * (jb.N >> 1) + (n >> 1)] = float_to_f16_bits(silu_f32(v) * u);
+    const int row = lane & 15, n = rt * 16 + row;
+    const size_t step = part_floats(jb, M);
+    for (int t0 = 0; t0 < M; t0 += 2) {                  // two tokens per pass
+        const int tok = t0 + (lane >> 4);
+        float v = 0.f;
+        if (tok < M) {
+            const float *rec = part_record(p, jb, rt, 0, M) + size_t(tok) * 16 + row;
+            for (int c = 0; c < C; ++c) v += __ldcg(rec + step * size_t(c));
+        }
+        if (!(jb.flags & kStepGateUp)) {
+            if (tok < M && n < jb.N) jb.y[size_t(tok) * jb.N + n] = float_to_f16_bits(v);
+        } else {
+            const float u = __shfl_down_sync(0xffffffffu, v, 1);
+            if (tok < M && (row & 1) == 0 && n + 1 < jb.N)
+                jb.y[size_t(tok) * (jb.N >> 1) + (n >> 1)] = float_to_f16_bits(silu_f32(v) * u);
+        }
     }
 }
 
@@ -365,6 +384,81 @@ __device__ __forceinline__ void fail(const Params &p, volatile int *s_abort)
     atomicOr(&g_step_error, ZQ4_DEVERR_WAIT_TIMEOUT);
     atomicOr(&p.hdr->abort, 1u);
     *s_abort = 1;
+}
+
+// The finisher and publisher warp of a CTA with nw compute warps.
+// Finisher (split jobs): takes the compute warps' posted part tiles (one per
+// warp at a time, lane w for warp w): a GPU-scope fence and an arrival on
+// the tile's counter each; the lane whose arrival completes a tile fences
+// (acquire), and the warp adds the parts and writes the tile. Each taken
+// tile then counts for publishing. Publisher: makes this CTA's finished
+// units of the waited-for jobs visible to every SM: snapshot the shared
+// counters (acquire: the units were counted after their outputs were
+// written), one GPU-scope fence for the whole batch, then one add per
+// changed job. Runs until every compute warp is done (or the CTA aborts).
+template <class JobFn>
+__device__ __forceinline__ void publisher_loop(const Params &p, uint32_t sbase, uint32_t a_posted, uint32_t a_taken,
+                                               uint32_t a_posts, uint32_t a_cta_done, unsigned *cta_pub,
+                                               unsigned *cta_snap, uint32_t s_warps_done, volatile int *s_abort,
+                                               int nw, int n, int M, unsigned done_mul, int lane, JobFn job)
+{
+    (void)sbase;
+    if (p.n_pub == 0 && !p.split) return;
+    int taken_l = 0;                                      // lane w < nw: posts of warp w taken
+    for (;;) {
+        const bool last = __shfl_sync(0xffffffffu, ld_acquire_cta_s32(s_warps_done) == nw || *s_abort, 0);
+        while (p.split) {
+            int have = 0, e = 0, rt = 0, done = 0;
+            if (lane < nw && ld_acquire_cta_s32(a_posted + 4 * lane) != taken_l) {
+                const int2 pr = lds_s2(a_posts + 8 * (lane * kPosts + taken_l % kPosts));
+                have = 1;
+                e = pr.x;
+                rt = pr.y;
+                const StepJob &jb = job(e);
+                fence_acq_rel_gpu_();
+                const unsigned old = atomicAdd(&p.arrive[jb.sbase + rt], 1u);
+                done = reached(old + 1u, done_mul * unsigned(((jb.flags >> kStepSplitShift) & 63) + 1));
+                if (done) fence_acq_rel_gpu_();
+            }
+            if (!__any_sync(0xffffffffu, have)) break;
+            __syncwarp();
+            for (unsigned m = __ballot_sync(0xffffffffu, done); m; m &= m - 1) {
+                const int w = __ffs(m) - 1;
+                const int ew = __shfl_sync(0xffffffffu, e, w), rw = __shfl_sync(0xffffffffu, rt, w);
+                complete_part(p, job(ew), rw, lane, M);
+            }
+            __syncwarp();                                 // the rows written before the units count
+            if (have) {
+                const StepJob &jb = job(e);
+                if (jb.flags & kStepPublish) red_release_cta(a_cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                st_release_cta_s32(a_taken + 4 * lane, ++taken_l);
+            }
+        }
+        bool any = false;
+        for (int i = lane; i < p.n_pub; i += 32) {
+            const unsigned c = unsigned(ld_acquire_cta_s32(a_cta_done + 4 * i));
+            cta_snap[i] = c;
+            any |= c != cta_pub[i];
+        }
+        __syncwarp();                                     // the snapshot before the adds read it
+        if (__any_sync(0xffffffffu, any)) {
+            fence_acq_rel_gpu_();
+            for (int j = lane; j < n; j += 32) {
+                const StepJob &jb = job(j);
+                // every part counts into the job's slot; part 0's entry holds the counter
+                if (!(jb.flags & kStepPublish) || (jb.flags & (63 << kStepPartShift))) continue;
+                const int i = jb.flags >> kStepPubShift;
+                const unsigned c = cta_snap[i];
+                if (c != cta_pub[i]) {
+                    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&p.job_done[j]), "r"(c - cta_pub[i])
+                                 : "memory");
+                    cta_pub[i] = c;
+                }
+            }
+        }
+        if (last) break;
+        __nanosleep(p.split ? 128 : 500);
+    }
 }
 
 template <int MT>
@@ -583,74 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                 if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xtag[c] & 1))) break;
     } else if (warp == kPubWarp) {
         // ---------------- the finisher and publisher ----------------
-        // Finisher (split jobs): takes the compute warps' posted part tiles
-        // (one per warp at a time, lane w for warp w): a GPU-scope fence and
-        // an arrival on the tile's counter each; the lane whose arrival
-        // completes a tile fences (acquire), and the warp adds the parts and
-        // writes the tile. Each taken tile then counts for publishing.
-        // Publisher: makes this CTA's finished units of the waited-for jobs
-        // visible to every SM: snapshot the shared counters (acquire: the
-        // units were counted after their outputs were written), one
-        // GPU-scope fence for the whole batch, then one add per changed job.
-        if (p.n_pub > 0 || p.split) {
-            int taken_l = 0;                              // lane w < kWarps: posts of warp w taken
-            for (;;) {
-                const bool last = __shfl_sync(0xffffffffu, ld_acquire_cta_s32(s_warps_done) == kWarps || *s_abort, 0);
-                while (p.split) {
-                    int have = 0, e = 0, rt = 0, done = 0;
-                    if (lane < kWarps && ld_acquire_cta_s32(sbase + L.posted + 4 * lane) != taken_l) {
-                        const int2 pr = *reinterpret_cast<const int2 *>(smem + L.posts +
-                                                                         8 * (lane * kPosts + taken_l % kPosts));
-                        have = 1;
-                        e = pr.x;
-                        rt = pr.y;
-                        const StepJob &jb = job(e);
-                        fence_acq_rel_gpu_();
-                        const unsigned old = atomicAdd(&p.arrive[jb.sbase + rt], 1u);
-                        done = reached(old + 1u, done_mul * unsigned(((jb.flags >> kStepSplitShift) & 63) + 1));
-                        if (done) fence_acq_rel_gpu_();
-                    }
-                    if (!__any_sync(0xffffffffu, have)) break;
-                    __syncwarp();
-                    for (unsigned m = __ballot_sync(0xffffffffu, done); m; m &= m - 1) {
-                        const int w = __ffs(m) - 1;
-                        const int ew = __shfl_sync(0xffffffffu, e, w), rw = __shfl_sync(0xffffffffu, rt, w);
-                        complete_part(p, job(ew), rw, lane, M);
-                    }
-                    __syncwarp();                         // the rows written before the units count
-                    if (have) {
-                        const StepJob &jb = job(e);
-                        if (jb.flags & kStepPublish) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
-                        st_release_cta_s32(sbase + L.taken + 4 * lane, ++taken_l);
-                    }
-                }
-                bool any = false;
-                for (int i = lane; i < p.n_pub; i += 32) {
-                    const unsigned c = unsigned(ld_acquire_cta_s32(sbase + L.cta_done + 4 * i));
-                    cta_snap[i] = c;
-                    any |= c != cta_pub[i];
-                }
-                __syncwarp();                             // the snapshot before the adds read it
-                if (__any_sync(0xffffffffu, any)) {
-                    fence_acq_rel_gpu_();
-                    for (int j = lane; j < n; j += 32) {
-                        const StepJob &jb = job(j);
-                        // every part counts into the job's slot; part 0's entry holds the counter
-                        if (!(jb.flags & kStepPublish) || (jb.flags & (63 << kStepPartShift))) continue;
-                        const int i = jb.flags >> kStepPubShift;
-                        const unsigned c = cta_snap[i];
-                        if (c != cta_pub[i]) {
-                            asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&p.job_done[j]),
-                                         "r"(c - cta_pub[i])
-                                         : "memory");
-                            cta_pub[i] = c;
-                        }
-                    }
-                }
-                if (last) break;
-                __nanosleep(p.split ? 128 : 500);
-            }
-        }
+        publisher_loop(p, sbase, sbase + L.posted, sbase + L.taken, sbase + L.posts, sbase + L.cta_done, cta_pub,
+                       cta_snap, s_warps_done, s_abort, kWarps, n, M, done_mul, lane, job);
     } else {
         // ---------------- compute warps ----------------
         const int r = lane >> 2, t = lane & 3;
@@ -844,6 +872,379 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Three to sixteen tokens (k_wide)
+// ---------------------------------------------------------------------------
+// Same plan, units, counter, waits, split parts and finisher/publisher warp
+// as k_step; what differs: column n of the m16n8k16 accumulator is token n
+// (a block of 8 tokens; 16 tokens: two blocks from one unpack), the group
+// scales are applied per group (fp32, after the group's two MMAs), and x
+// comes with each segment: every ring slot holds the 2304-byte segment and
+// x[M][256] of its 256 columns, brought by one 2D tensor copy from the job
+// entry's tensor map (no x window). A warp checks the waits of a job when
+// its cursor first reaches it; if they are not met it consumes what it has
+// in flight and waits only once its ring is empty (a unit of an earlier job
+// may still be in its ring).
+template <int MT>
+struct Wide {
+    static constexpr int kWarps = MT <= 8 ? 16 : 10;   // compute warps
+    static constexpr int kThreads = (kWarps + 1) * 32; // + the finisher/publisher warp
+};
+
+struct WSmem {
+    uint32_t ring, bars, desc, posted, taken, posts, misc, cta_done, cta_pub, cta_snap, jobs, total;
+    __host__ __device__ WSmem(int nw, int slots, int slot_bytes, int n_pub, int cached)
+    {
+        ring = 0;
+        bars = ring + uint32_t(nw * slots) * uint32_t(slot_bytes);
+        desc = bars + uint32_t(nw * slots) * 8;
+        posted = desc + uint32_t(nw * slots) * 16;
+        taken = posted + uint32_t(nw) * 4;
+        posts = taken + uint32_t(nw) * 4;
+        misc = posts + uint32_t(nw * kPosts) * 8;
+        cta_done = misc + 64;
+        cta_pub = cta_done + uint32_t(n_pub) * 4;
+        cta_snap = cta_pub + uint32_t(n_pub) * 4;
+        jobs = (cta_snap + uint32_t(n_pub) * 4 + 15) / 16 * 16;
+        total = jobs + uint32_t(cached) * uint32_t(sizeof(StepJob));
+    }
+};
+
+__device__ __forceinline__ float scale_of(const uint4 &s, int g)
+{
+    const uint32_t w = g < 2 ? s.x : g < 4 ? s.y : g < 6 ? s.z : s.w;
+    return (g & 1) ? hi_f32(w) : lo_f32(w);
+}
+
+// One segment into the lane's accumulators: acc[4 b + i] = block b of 8
+// tokens (rows r, r + 8 x tokens 8b + 2t, 8b + 2t + 1). x of the lane's
+// token of block b: 16 bytes at xr[b] + 64 g (columns 32 g + 8 t ..).
+template <int MT>
+__device__ __forceinline__ void segment_wide(uint32_t cb, uint32_t aoff, uint32_t srow, const uint32_t (&xr)[MT / 8],
+                                             float (&acc)[MT / 2])
+{
+    const uint4 c0 = lds_v4(cb + aoff), c1 = lds_v4(cb + aoff + 16);            // row r: groups 0-3, 4-7
+    const uint4 c8 = lds_v4(cb + aoff + 1152), c9 = lds_v4(cb + aoff + 1168);   // row r+8
+    const uint4 s0 = lds_v4(cb + srow), s8 = lds_v4(cb + srow + 1152);          // their 8 group scales
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        uint32_t pa[4], pb[4];
+        unpack_word_f16x2(group_word(c0, c1, g), pa);
+        unpack_word_f16x2(group_word(c8, c9, g), pb);
+        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+        const float sr = scale_of(s0, g), sr8 = scale_of(s8, g);
+#pragma unroll
+        for (int b = 0; b < MT / 8; ++b) {
+            const uint4 xv = lds_v4(xr[b] + 64 * g);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(d, a0, xv.x, xv.y, d);
+            mma16816(d, a1, xv.z, xv.w, d);
+            acc[4 * b + 0] = fmaf(sr, d[0], acc[4 * b + 0]);
+            acc[4 * b + 1] = fmaf(sr, d[1], acc[4 * b + 1]);
+            acc[4 * b + 2] = fmaf(sr8, d[2], acc[4 * b + 2]);
+            acc[4 * b + 3] = fmaf(sr8, d[3], acc[4 * b + 3]);
+        }
+    }
+}
+
+// A finished whole tile: rows row0 + r, row0 + r + 8 of tokens 8b + 2t and
+// 8b + 2t + 1 (gate_up: silu(gate) * up of the row pairs, up from the lane
+// of row r + 1).
+template <int MT>
+__device__ __forceinline__ void finish_wide(const float (&acc)[MT / 2], const StepJob &jb, int row0, int lane, int M)
+{
+    const int r = lane >> 2, t = lane & 3;
+    const bool gu = jb.flags & kStepGateUp;
+    const int ys = gu ? (jb.N >> 1) : jb.N;
+#pragma unroll
+    for (int b = 0; b < MT / 8; ++b) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                    // rows r (h = 0), r + 8 (h = 1)
+            const int row = row0 + r + 8 * h;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {                // tokens 8b + 2t + q
+                const int tok = 8 * b + 2 * t + q;
+                const float v = acc[4 * b + 2 * h + q];
+                if (!gu) {
+                    if (tok < M && row < jb.N) jb.y[size_t(tok) * ys + row] = float_to_f16_bits(v);
+                } else {
+                    const float u = __shfl_down_sync(0xffffffffu, v, 4);
+                    if (tok < M && (r & 1) == 0 && row + 1 < jb.N)
+                        jb.y[size_t(tok) * ys + (row >> 1)] = float_to_f16_bits(silu_f32(v) * u);
+                }
+            }
+        }
+    }
+}
+
+// A finished tile rt of one part of a split job: its sums into the part's
+// record (16 rows per token), then a post to the finisher.
+template <int MT>
+__device__ __forceinline__ bool post_part_wide(const float (&acc)[MT / 2], const StepJob &jb, int entry, int rt,
+                                               int lane, int M, const Params &p, uint32_t posted, uint32_t taken,
+                                               uint32_t posts, volatile int *s_abort)
+{
+    const int r = lane >> 2, t = lane & 3;
+    float *rec = part_record(p, jb, rt, (jb.flags >> kStepPartShift) & 63, M) + r;
+#pragma unroll
+    for (int b = 0; b < MT / 8; ++b)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int tok = 8 * b + 2 * t + q;
+                if (tok < M) rec[size_t(tok) * 16 + 8 * h] = acc[4 * b + 2 * h + q];
+            }
+    __syncwarp();
+    return post_tile(entry, rt, lane, posted, taken, posts, s_abort, p.wait_ns);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
+{
+    constexpr int NW = Wide<MT>::kWarps;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
+    const uint32_t sbase = smem_addr(smem);
+    const int slots = p.slots, slot_bytes = p.slot_bytes;
+    const WSmem L(NW, slots, slot_bytes, p.n_pub, p.cached);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = p.n_jobs, M = p.M;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.misc);
+    const uint32_t s_warps_done = sbase + L.misc + 4;
+    unsigned *cta_done = reinterpret_cast<unsigned *>(smem + L.cta_done);
+    unsigned *cta_pub = reinterpret_cast<unsigned *>(smem + L.cta_pub);
+    unsigned *cta_snap = reinterpret_cast<unsigned *>(smem + L.cta_snap);
+    StepJob *sjobs = reinterpret_cast<StepJob *>(smem + L.jobs);
+    const unsigned launch = *reinterpret_cast<volatile unsigned *>(&p.hdr->epoch);
+
+    for (int i = threadIdx.x; i < p.n_pub; i += blockDim.x) cta_done[i] = cta_pub[i] = 0;
+    for (int i = threadIdx.x; i < NW; i += blockDim.x) {
+        reinterpret_cast<int *>(smem + L.posted)[i] = 0;
+        reinterpret_cast<int *>(smem + L.taken)[i] = 0;
+    }
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        *reinterpret_cast<int *>(smem + L.misc + 4) = 0;
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.jobs);
+        uint4 *dst = reinterpret_cast<uint4 *>(sjobs);
+        const int words = p.cached * int(sizeof(StepJob) / 16);
+        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+    }
+    if (warp < NW && lane == 0) {
+        for (int j = 0; j < slots; ++j) mbar_init(sbase + L.bars + 8 * (warp * slots + j), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto job = [&](int j) -> const StepJob & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
+    const unsigned done_mul = launch + 1u;
+
+    if (warp == NW) {
+        publisher_loop(p, sbase, sbase + L.posted, sbase + L.taken, sbase + L.posts, sbase + L.cta_done, cta_pub,
+                       cta_snap, s_warps_done, s_abort, NW, n, M, done_mul, lane, job);
+    } else {
+        const int r = lane >> 2, t = lane & 3;
+        const bool leader = lane == 0;
+        const uint32_t ring = sbase + L.ring + uint32_t(warp * slots) * uint32_t(slot_bytes);
+        const uint32_t bars = sbase + L.bars + uint32_t(8 * warp * slots);
+        const uint32_t descs = sbase + L.desc + uint32_t(16 * warp * slots);
+        const uint32_t my_posted = sbase + L.posted + 4 * warp, my_taken = sbase + L.taken + 4 * warp;
+        const uint32_t my_posts = sbase + L.posts + uint32_t(8 * kPosts * warp);
+        const uint32_t aoff = segk::lane_code_offset(lane);
+        const uint32_t srow = uint32_t(r * 144 + 128);
+        // x of the lane's token in a slot (tokens past M read token M - 1: their columns are dropped)
+        uint32_t xoff[MT / 8];
+#pragma unroll
+        for (int b = 0; b < MT / 8; ++b) xoff[b] = uint32_t(kSegBytes + min(8 * b + r, M - 1) * 512 + 16 * t);
+        const uint32_t tx = uint32_t(kSegBytes + M * 512);   // bytes one slot receives
+
+        const uint32_t lead = leader ? 1u : 0u;
+        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1, islot = 0, checked = -1;
+        const uint8_t *iptr = nullptr;
+        bool ihave = false, iend = false, reserved = false;
+        unsigned nt = 0;
+        unsigned *const ctr = &p.hdr->next_tile;
+        auto reserve = [&](uint32_t pred) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p atom.global.add.u32 %0, [%2], 1;\n\t}"
+                         : "+r"(nt)
+                         : "r"(pred), "l"(ctr)
+                         : "memory");
+        };
+        auto next_tile = [&]() {
+            if (!reserved) reserve(lead);
+            reserved = false;
+            const unsigned g = __shfl_sync(0xffffffffu, nt, 0);
+            if (g >= unsigned(p.total_tiles)) {
+                iend = true;
+                return;
+            }
+            while (int(g) >= job(fj).tile0 + ((job(fj).N + 15) >> 4)) ++fj;
+            ijob = fj;
+            itile = int(g) - job(fj).tile0;
+            isg = 0;
+            iS = job(fj).K >> 8;
+            iptr = job(fj).seg + size_t(itile) * size_t(job(fj).tstride) * kSegBytes;
+            ihave = true;
+        };
+        // are the waits of entry e met (lane 0's acquire loads, broadcast)
+        auto ready = [&](int e) -> bool {
+            int ok = 1;
+            if (leader) {
+                const StepJob &jk = job(e);
+                const int nw = (jk.flags >> kStepWaitShift) & 3;
+                for (int w = 0; ok && w < nw; ++w) {
+                    const int d = jk.wait[w];
+                    ok = reached(ld_acquire_gpu(&p.job_done[d]), done_mul * unit_count(job(d)));
+                }
+                // the data the waits guard is read by the tensor copies (async proxy)
+                if (ok && nw) asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        // copy the cursor's next segment and its x into slot islot: 1 issued,
+        // 0 no unit left, -1 the cursor's job waits for jobs not done yet
+        auto issue_next = [&]() -> int {
+            if (!ihave) {
+                if (iend) return 0;
+                next_tile();
+                if (iend) return 0;
+            }
+            if (ijob != checked) {
+                if (!ready(ijob)) return -1;
+                checked = ijob;
+            }
+            const bool res = !reserved && isg == (iS >> 1);
+            reserve(res ? lead : 0u);
+            reserved |= res;
+            const uint32_t bar = bars + 8 * islot, dst = ring + uint32_t(islot) * uint32_t(slot_bytes);
+            const CUtensorMap *tm = p.tmaps + ijob;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.u32 p, %0, 0;\n\t"
+                "@p st.shared.v4.s32 [%1], {%2, %3, %4, %5};\n\t"
+                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%6], %7;\n\t"
+                "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%8], [%9], %10, [%6];\n\t"
+                "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%11], [%12, {%13, %14}], [%6];\n\t"
+                "}" ::"r"(lead),
+                "r"(descs + 16 * islot), "r"(ijob), "r"(itile), "r"(isg), "r"(iS), "r"(bar), "r"(tx), "r"(dst),
+                "l"(iptr), "r"(uint32_t(kSegBytes)), "r"(dst + uint32_t(kSegBytes)), "l"(reinterpret_cast<uint64_t>(tm)),
+                "r"(isg * 256), "r"(0)
+                : "memory");
+            iptr += kSegBytes;
+            ihave = ++isg < iS;
+            islot = islot + 1 == slots ? 0 : islot + 1;
+            return 1;
+        };
+
+        int in_flight = 0;
+        bool blocked = false, ok = true;
+        for (;;) {
+            const int rv = issue_next();
+            if (rv <= 0) {
+                blocked = rv < 0;
+                break;
+            }
+            if (++in_flight == slots) break;
+        }
+        float acc[MT / 2];
+#pragma unroll
+        for (int i = 0; i < MT / 2; ++i) acc[i] = 0.f;
+        int cslot = 0;
+        uint32_t cphase = 0;
+        while (in_flight > 0 || blocked) {
+            if (in_flight == 0) {
+                // nothing in flight: every unit this warp took is finished; wait for the job's waits
+                const unsigned long long t0 = globaltimer();
+                int rv = -1;
+                while ((rv = issue_next()) < 0) {
+                    if (*s_abort || *reinterpret_cast<volatile unsigned *>(&p.hdr->abort) ||
+                        globaltimer() - t0 > p.wait_ns) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                if (!ok) break;
+                blocked = false;
+                if (rv == 0) break;
+                ++in_flight;
+                continue;
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * cslot, cphase))) {
+                ok = false;
+                break;
+            }
+            const uint32_t cb = ring + uint32_t(cslot) * uint32_t(slot_bytes);
+            const int4 d = lds_s4(descs + 16 * cslot);
+            if (d.z == 0) {
+#pragma unroll
+                for (int i = 0; i < MT / 2; ++i) acc[i] = 0.f;
+            }
+            uint32_t xr[MT / 8];
+#pragma unroll
+            for (int b = 0; b < MT / 8; ++b) xr[b] = cb + xoff[b];
+            segment_wide<MT>(cb, aoff, srow, xr, acc);
+            // every lane's reads of the slot are done before lane 0's copies refill it
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            --in_flight;
+            if (!blocked) {
+                const int rv = issue_next();
+                if (rv > 0) ++in_flight;
+                blocked = rv < 0;
+            } else if (issue_next() > 0) {
+                ++in_flight;
+                blocked = false;
+            }
+            if (d.z == d.w - 1) {
+                const StepJob &jb = job(d.x);
+                if (!(jb.flags & (63 << kStepSplitShift))) {
+                    finish_wide<MT>(acc, jb, d.y * 16, lane, M);
+                    if (jb.flags & kStepPublish) {
+                        __syncwarp();
+                        if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                    }
+                } else if (!post_part_wide<MT>(acc, jb, d.x, d.y, lane, M, p, my_posted, my_taken, my_posts,
+                                               s_abort)) {
+                    ok = false;
+                }
+            }
+            if (++cslot == slots) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
+            if (!ok) break;
+        }
+        if (!ok && leader) fail(p, s_abort);
+        // after a failed wait: the copies still in flight land before the CTA exits
+        if (!ok && leader)
+            for (int c = 0; c < in_flight; ++c) {
+                const int sl = (cslot + c) % slots;
+                if (!mbar_wait(bars + 8 * sl, cphase ^ (cslot + c >= slots ? 1u : 0u))) break;
+            }
+        __syncwarp();
+        if (leader) red_release_cta(s_warps_done, 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (*s_abort) {
+            atomicOr(&g_step_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+        } else {
+            __threadfence();
+            const unsigned target = (launch + 1u) * gridDim.x;
+            const unsigned dn = atomicAdd(&p.hdr->done, 1u);
+            if (dn == target - 1u) {
+                p.hdr->next_tile = 0;
+                __threadfence();
+                atomicAdd(&p.hdr->epoch, 1u);
+            }
+        }
+    }
+}
+
 }  // namespace sp
 
 // ---------------------------------------------------------------------------
@@ -926,6 +1327,110 @@ zq4_status step_check_resident(int M, int max_k, int n_jobs, int n_pub)
     if (e != cudaSuccess) return cuda_status(e);
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sp::kThreads, sh.smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    return per_sm < 1 ? ZQ4_ERR_UNSUPPORTED : ZQ4_OK;
+}
+
+// ---------------------------------------------------------------------------
+// k_wide host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+namespace {
+
+int wide_smem_set8[kMaxDevices] = {};
+int wide_smem_set16[kMaxDevices] = {};
+
+struct WideShape {
+    int slots, slot_bytes, cached;
+    size_t smem;
+};
+
+// Ring slots (as many as fit, 2 to 4), slot size (one segment and x[M][256])
+// and cached jobs (up to 256, while they leave the slots room).
+bool wide_launch_shape(int M, int n_jobs, int n_pub, WideShape *sh)
+{
+    const size_t cap = size_t(227) * 1024 - 128;
+    const int nw = M <= 8 ? sp::Wide<8>::kWarps : sp::Wide<16>::kWarps;
+    const int slot_bytes = sp::kSegBytes + M * 512;
+    for (int slots = 4; slots >= 2; --slots) {
+        for (int cached = std::min(n_jobs, 256);; cached = cached > 16 ? cached / 2 : 0) {
+            const size_t need = sp::WSmem(nw, slots, slot_bytes, n_pub, cached).total;
+            if (need <= cap && (cached == std::min(n_jobs, 256) || slots == 2)) {
+                sh->slots = slots;
+                sh->slot_bytes = slot_bytes;
+                sh->cached = cached;
+                sh->smem = need + 128;
+                return true;
+            }
+            if (cached == 0 || slots > 2) break;
+        }
+    }
+    return false;
+}
+
+const void *wide_kernel(int M)
+{
+    return M <= 8 ? reinterpret_cast<const void *>(sp::k_wide<8>) : reinterpret_cast<const void *>(sp::k_wide<16>);
+}
+int wide_threads(int M) { return M <= 8 ? sp::Wide<8>::kThreads : sp::Wide<16>::kThreads; }
+
+}  // namespace
+
+bool wide_x_map(void *map128, const uint16_t *x, int M, int K, long long ld)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dim[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t stride[1] = {cuuint64_t(ld) * 2};
+    const cuuint32_t box[2] = {256, cuuint32_t(M)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(static_cast<CUtensorMap *>(map128), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(x), dim,
+               stride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+zq4_status wide_run(const zq4_stack_plan *plan, cudaStream_t s)
+{
+    const StepLayout l(plan->entries, plan->split_tiles, plan->part_records, true);
+    uint8_t *base = static_cast<uint8_t *>(plan->dev);
+    sp::Params p;
+    memset(&p, 0, sizeof(p));
+    p.hdr = reinterpret_cast<StepHeader *>(base + l.hdr);
+    p.jobs = reinterpret_cast<const StepJob *>(base + l.jobs);
+    p.job_done = reinterpret_cast<unsigned *>(base + l.job_done);
+    p.arrive = reinterpret_cast<unsigned *>(base + l.arrive);
+    p.work = reinterpret_cast<float *>(base + l.work);
+    p.tmaps = reinterpret_cast<const CUtensorMap *>(base + l.tmaps);
+    p.n_jobs = plan->entries;
+    p.total_tiles = plan->tiles;
+    p.M = plan->M;
+    p.n_pub = plan->n_pub;
+    WideShape sh;
+    if (!wide_launch_shape(p.M, p.n_jobs, p.n_pub, &sh)) return ZQ4_ERR_UNSUPPORTED;
+    p.slots = sh.slots;
+    p.slot_bytes = sh.slot_bytes;
+    p.cached = sh.cached;
+    p.split = plan->split_tiles > 0 ? 1 : 0;
+    p.wait_ns = plan->wait_ns ? plan->wait_ns : kWaitLimitNs;
+    const void *kern = wide_kernel(p.M);
+    cudaError_t e = ensure_smem(kern, sh.smem, p.M <= 8 ? wide_smem_set8 : wide_smem_set16);
+    if (e != cudaSuccess) return cuda_status(e);
+    void *args[] = {&p};
+    return cuda_status(
+        cudaLaunchCooperativeKernel(kern, dim3(plan->grid), dim3(wide_threads(p.M)), args, sh.smem, s));
+}
+
+zq4_status wide_check_resident(int M, int n_jobs, int n_pub)
+{
+    WideShape sh;
+    if (!wide_launch_shape(M, n_jobs, n_pub, &sh)) return ZQ4_ERR_UNSUPPORTED;
+    if (!tensor_map_encoder()) return ZQ4_ERR_UNSUPPORTED;
+    const void *kern = wide_kernel(M);
+    cudaError_t e = ensure_smem(kern, sh.smem, M <= 8 ? wide_smem_set8 : wide_smem_set16);
+    if (e != cudaSuccess) return cuda_status(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, wide_threads(M), sh.smem);
     if (e != cudaSuccess) return cuda_status(e);
     return per_sm < 1 ? ZQ4_ERR_UNSUPPORTED : ZQ4_OK;
 }

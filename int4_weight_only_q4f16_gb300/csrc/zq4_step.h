@@ -14,6 +14,7 @@
 namespace zq4 {
 
 constexpr int kStepMaxM = 2;          // tokens the step engine handles
+constexpr int kWideMaxM = 16;         // tokens the wide step engine handles (3 ..)
 constexpr int kStepWarps = 16;        // compute warps per CTA
 constexpr int kStepMaxWaits = 3;      // jobs one job may wait for
 
@@ -73,16 +74,19 @@ struct alignas(16) StepJob {
 };
 static_assert(sizeof(StepJob) == 64, "step jobs are 64 bytes");
 
-// Device plan: header, job table, per-entry finished-unit counters, then the
-// split workspace: per split tile an arrival counter, and the parts' sums.
+// Device plan: header, job table, per-entry finished-unit counters, for
+// k_wide a tensor map per entry (x[M][K] in boxes of [M][256], 128 bytes
+// each), then the split workspace: per split tile an arrival counter, and
+// the parts' sums.
 struct StepLayout {
-    size_t hdr, jobs, job_done, arrive, work, total;
-    StepLayout(int n_entries, long long split_tiles, long long part_records)
+    size_t hdr, jobs, job_done, tmaps, arrive, work, total;
+    StepLayout(int n_entries, long long split_tiles, long long part_records, bool wide = false)
     {
         hdr = 0;
         jobs = 128;
         job_done = jobs + size_t(n_entries) * sizeof(StepJob);
-        arrive = (job_done + size_t(n_entries) * 4 + 255) / 256 * 256;
+        tmaps = (job_done + size_t(n_entries) * 4 + 127) / 128 * 128;
+        arrive = (tmaps + (wide ? size_t(n_entries) * 128 : 0) + 255) / 256 * 256;
         work = (arrive + size_t(split_tiles) * 4 + 255) / 256 * 256;
         total = work + size_t(part_records) * 64;
     }
@@ -96,6 +100,10 @@ struct StepShape {
 bool step_launch_shape(int M, int max_k, int n_jobs, int n_pub, StepShape *sh);
 zq4_status step_check_resident(int M, int max_k, int n_jobs, int n_pub);
 zq4_status step_run(const zq4_stack_plan *plan, cudaStream_t s);
+zq4_status wide_check_resident(int M, int n_jobs, int n_pub);
+zq4_status wide_run(const zq4_stack_plan *plan, cudaStream_t s);
+// x[M][K] f16 of an entry (row stride ld elements) as a tensor map of [M][256] boxes
+bool wide_x_map(void *map128, const uint16_t *x, int M, int K, long long ld);
 cudaError_t read_step_error(unsigned *flags, bool clear);
 
 }  // namespace zq4

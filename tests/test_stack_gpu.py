@@ -60,7 +60,7 @@ def test_small_stack_matches_oracle(oracle, M):
             _check_job(oracle, job, what)
 
 
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
 def test_step_engine_split_tiles_match_oracle(oracle, M):
     """Tiles of long-K jobs split along K (K = 9728: 4 parts of 9, 10, 9, 10
     segments; 3328: 6 + 7; 4096 and 4608: 8 + 8 and 9 + 9), a split gate_up
@@ -81,7 +81,7 @@ def test_step_engine_split_tiles_match_oracle(oracle, M):
         jobs.append((seg, x, y, N, K, gu))
         mats.append((wq_h, sc_h))
     plan = zq4.StackPlan(jobs, M)
-    assert plan.plan.engine == 1 and plan.plan.split_tiles > 0
+    assert plan.plan.engine == (1 if M <= 2 else 2) and plan.plan.split_tiles > 0
     first = None
     for run in range(3):
         for j in jobs:
@@ -151,10 +151,10 @@ def test_stack_plan_rejects_bad_jobs():
     s = stk.DecodeStack((("qkv", 64, 512),), 1, None, M=1, mode="calls")
     wq, sc, x, y, N, K, gu = s.jobs()[0]
     seg, _ = zq4.prepare_weight(wq, sc, N, K, zq4.PREP_SEGMENTED)
-    x9 = torch.zeros((9, K), dtype=torch.float16, device="cuda")
-    y9 = torch.empty((9, N), dtype=torch.float16, device="cuda")
+    x9 = torch.zeros((17, K), dtype=torch.float16, device="cuda")
+    y9 = torch.empty((17, N), dtype=torch.float16, device="cuda")
     with pytest.raises(zq4.Zq4Error, match="SHAPE"):
-        zq4.StackPlan([(seg, x9, y9, N, K, gu)], 9)                    # M > 8
+        zq4.StackPlan([(seg, x9, y9, N, K, gu)], 17)                   # M > 16
     with pytest.raises(zq4.Zq4Error, match="SHAPE"):
         zq4.StackPlan([(seg, x, y, N, 480, gu)], 1)                    # K % 256 != 0
     with pytest.raises(zq4.Zq4Error, match="FLAGS"):
@@ -416,3 +416,80 @@ def test_step_wait_runs_out_then_a_new_plan_runs(oracle):
     for i, ((seg, x, y, N_, K_, gu), (wq_h, sc_h)) in enumerate(zip(jobs, mats)):
         y_ref, S = oracle.gemv(wq_h, sc_h, host_f16(x), N_, K_)
         assert_within(host_f16(y), y_ref, S, f"job {i} after the re-initialised plan")
+
+
+@pytest.mark.parametrize("M", [3, 4, 7, 8, 9, 13, 16])
+def test_wide_engine_matches_oracle(oracle, M):
+    """Three to sixteen tokens on the wide step kernel (x brought with every
+    segment by a tensor copy, one MMA column per token): ragged N, K from
+    one to 38 segments (split parts included), gate_up, and a job that reads
+    a gate_up's output; three runs, bit-identical, each matching the oracle."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    rng = synth.rng_for("step_wide", M)
+    spec = [(200, 256, False), (72, 2560, False), (4096, 3072, True), (336, 768, False), (48, 9728, False)] + \
+        [(256, 1024, False)] * 6 + [(120, 2048, False), (333, 512, False)]
+    jobs, mats = [], []
+    for i, (N, K, gu) in enumerate(spec):
+        wq_h, sc_h = synth.weight("step_wide_w", N, K, i)
+        seg = zq4.prepare_weight(dev(wq_h), dev(sc_h), N, K, zq4.PREP_SEGMENTED)[0]
+        x = jobs[2][2] if i == 11 else dev(synth.activations(rng, M, K))   # job 11 reads job 2's output
+        y = torch.full((M, N // 2 if gu else N), float("nan"), dtype=torch.float16, device="cuda")
+        jobs.append((seg, x, y, N, K, gu))
+        mats.append((wq_h, sc_h))
+    plan = zq4.StackPlan(jobs, M)
+    assert plan.plan.engine == 2
+    first = None
+    for run in range(3):
+        for j in jobs:
+            j[2].fill_(float("nan"))
+        plan.run()
+        torch.cuda.synchronize()
+        assert zq4.device_errors(clear=True) == 0
+        bits = [host_f16(j[2]).view(np.uint16).copy() for j in jobs]
+        if first is None:
+            first = bits
+            for i, ((seg, x, y, N, K, gu), (wq_h, sc_h)) in enumerate(zip(jobs, mats)):
+                _check_job(oracle, (dev(wq_h), dev(sc_h), x, y, N, K, gu), f"M={M} wide job {i}")
+        else:
+            for i, (a, b) in enumerate(zip(first, bits)):
+                assert np.array_equal(a, b), f"M={M} run {run} job {i} differs from run 0"
+
+
+@pytest.fixture(scope="module")
+def qwen3_16():
+    """The Qwen3-4B-shaped stack (36 layers of qkv, o, gate_up, down) with
+    16 tokens of seeded input; plans for fewer tokens use its first rows."""
+    s = stk.qwen3_4b_stack(M=16, mode="plan")
+    return s, s.segmented()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_qwen3_full_step_sampled(oracle, qwen3_16, M):
+    """The whole Qwen3-4B-shaped step as one plan at M tokens (the first M
+    rows of the 16-token inputs and outputs; down reads gate_up's output),
+    run twice; sampled rows of every fourth layer match the oracle."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    s, segs = qwen3_16
+    full = s.jobs()
+    views = {}
+
+    def rows(t):
+        if t.data_ptr() not in views:
+            views[t.data_ptr()] = t[:M]
+        return views[t.data_ptr()]
+    pj = [(seg, rows(x), rows(y), N, K, gu) for seg, (wq, sc, x, y, N, K, gu) in zip(segs, full)]
+    plan = zq4.StackPlan(pj, M)
+    assert plan.plan.engine == (1 if M <= 2 else 2)
+    plan.run()
+    plan.run()
+    torch.cuda.synchronize()
+    assert zq4.device_errors(clear=True) == 0
+    per_layer = len(synth.QWEN3_4B_LAYER)
+    rng = np.random.default_rng(7 + M)
+    for l in range(0, synth.QWEN3_4B_LAYERS, 4):
+        for i, (name, N, K) in enumerate(synth.QWEN3_4B_LAYER):
+            wq, sc, x, y, N_, K_, gu = full[l * per_layer + i]
+            r = np.unique(np.concatenate([t * 16 + rng.integers(0, 16, 1) for t in range(0, N // 16, 3)]
+                                         + [[0, N - 1]]))
+            _check_job(oracle, (wq, sc, rows(x), rows(y), N, K, gu), f"qwen3 M={M} layer {l} {name}", rows=r)
