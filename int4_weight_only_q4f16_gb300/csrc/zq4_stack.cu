@@ -1123,7 +1123,9 @@ void write_image(int engine, const zq4_stack_job *jobs, int n, int M, const int 
             if (engine == kEngineWide &&
                 !wide_x_map(host + lay.tmaps + size_t(sc.first[r] + c) * 128, jb.x, M, jb.K, b.K))
                 info->ok = false;
-            tile0 += rows;
+            // work units: tiles, or groups of wide_group(M) tiles for k_wide
+            const int G = engine == kEngineWide ? wide_group(M) : 1;
+            tile0 += (rows + G - 1) / G;
             min_unit = std::min(min_unit, len);
         }
         if (C > 1) {

@@ -887,9 +887,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
 // may still be in its ring).
 template <int MT>
 struct Wide {
-    static constexpr int kWarps = MT <= 8 ? 16 : 10;   // compute warps
+    static constexpr int kGroup = MT <= 8 ? 1 : 2;     // 16-row tiles per unit (they share x)
+    static constexpr int kWarps = MT <= 8 ? 16 : 8;    // compute warps
     static constexpr int kThreads = (kWarps + 1) * 32; // + the finisher/publisher warp
 };
+static_assert(Wide<16>::kGroup == kWideGroup16, "host and kernel agree on the unit size");
 
 struct WSmem {
     uint32_t ring, bars, desc, posted, taken, posts, misc, cta_done, cta_pub, cta_snap, jobs, total;
@@ -916,34 +918,48 @@ __device__ __forceinline__ float scale_of(const uint4 &s, int g)
     return (g & 1) ? hi_f32(w) : lo_f32(w);
 }
 
-// One segment into the lane's accumulators: acc[4 b + i] = block b of 8
-// tokens (rows r, r + 8 x tokens 8b + 2t, 8b + 2t + 1). x of the lane's
-// token of block b: 16 bytes at xr[b] + 64 g (columns 32 g + 8 t ..).
-template <int MT>
+// One segment of G tiles (at cb + 2304 i) into the lane's accumulators:
+// acc[i][4 b + j] = tile i, block b of 8 tokens (rows r, r + 8 x tokens
+// 8b + 2t, 8b + 2t + 1). x of the lane's token of block b: 16 bytes at
+// xr[b] + 64 g (columns 32 g + 8 t ..), shared by the G tiles.
+template <int MT, int G>
 __device__ __forceinline__ void segment_wide(uint32_t cb, uint32_t aoff, uint32_t srow, const uint32_t (&xr)[MT / 8],
-                                             float (&acc)[MT / 2])
+                                             float (&acc)[G][MT / 2])
 {
-    const uint4 c0 = lds_v4(cb + aoff), c1 = lds_v4(cb + aoff + 16);            // row r: groups 0-3, 4-7
-    const uint4 c8 = lds_v4(cb + aoff + 1152), c9 = lds_v4(cb + aoff + 1168);   // row r+8
-    const uint4 s0 = lds_v4(cb + srow), s8 = lds_v4(cb + srow + 1152);          // their 8 group scales
+    uint4 c0[G], c1[G], c8[G], c9[G], s0[G], s8[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+        const uint32_t tb = cb + uint32_t(i * kSegBytes);
+        c0[i] = lds_v4(tb + aoff);                       // row r: groups 0-3, 4-7
+        c1[i] = lds_v4(tb + aoff + 16);
+        c8[i] = lds_v4(tb + aoff + 1152);                // row r+8
+        c9[i] = lds_v4(tb + aoff + 1168);
+        s0[i] = lds_v4(tb + srow);                       // their 8 group scales
+        s8[i] = lds_v4(tb + srow + 1152);
+    }
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-        uint32_t pa[4], pb[4];
-        unpack_word_f16x2(group_word(c0, c1, g), pa);
-        unpack_word_f16x2(group_word(c8, c9, g), pb);
-        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
-        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
-        const float sr = scale_of(s0, g), sr8 = scale_of(s8, g);
+        uint4 xv[MT / 8];
 #pragma unroll
-        for (int b = 0; b < MT / 8; ++b) {
-            const uint4 xv = lds_v4(xr[b] + 64 * g);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            mma16816(d, a0, xv.x, xv.y, d);
-            mma16816(d, a1, xv.z, xv.w, d);
-            acc[4 * b + 0] = fmaf(sr, d[0], acc[4 * b + 0]);
-            acc[4 * b + 1] = fmaf(sr, d[1], acc[4 * b + 1]);
-            acc[4 * b + 2] = fmaf(sr8, d[2], acc[4 * b + 2]);
-            acc[4 * b + 3] = fmaf(sr8, d[3], acc[4 * b + 3]);
+        for (int b = 0; b < MT / 8; ++b) xv[b] = lds_v4(xr[b] + 64 * g);
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            uint32_t pa[4], pb[4];
+            unpack_word_f16x2(group_word(c0[i], c1[i], g), pa);
+            unpack_word_f16x2(group_word(c8[i], c9[i], g), pb);
+            const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+            const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+            const float sr = scale_of(s0[i], g), sr8 = scale_of(s8[i], g);
+#pragma unroll
+            for (int b = 0; b < MT / 8; ++b) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d, a0, xv[b].x, xv[b].y, d);
+                mma16816(d, a1, xv[b].z, xv[b].w, d);
+                acc[i][4 * b + 0] = fmaf(sr, d[0], acc[i][4 * b + 0]);
+                acc[i][4 * b + 1] = fmaf(sr, d[1], acc[i][4 * b + 1]);
+                acc[i][4 * b + 2] = fmaf(sr8, d[2], acc[i][4 * b + 2]);
+                acc[i][4 * b + 3] = fmaf(sr8, d[3], acc[i][4 * b + 3]);
+            }
         }
     }
 }
@@ -1003,7 +1019,7 @@ __device__ __forceinline__ bool post_part_wide(const float (&acc)[MT / 2], const
 template <int MT>
 __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
 {
-    constexpr int NW = Wide<MT>::kWarps;
+    constexpr int NW = Wide<MT>::kWarps, G = Wide<MT>::kGroup;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
     const uint32_t sbase = smem_addr(smem);
@@ -1040,6 +1056,7 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
     }
     __syncthreads();
     auto job = [&](int j) -> const StepJob & { return j < p.cached ? sjobs[j] : p.jobs[j]; };
+    auto units_of = [&](const StepJob &e) { return (((e.N + 15) >> 4) + G - 1) / G; };
     const unsigned done_mul = launch + 1u;
 
     if (warp == NW) {
@@ -1058,12 +1075,12 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
         // x of the lane's token in a slot (tokens past M read token M - 1: their columns are dropped)
         uint32_t xoff[MT / 8];
 #pragma unroll
-        for (int b = 0; b < MT / 8; ++b) xoff[b] = uint32_t(kSegBytes + min(8 * b + r, M - 1) * 512 + 16 * t);
-        const uint32_t tx = uint32_t(kSegBytes + M * 512);   // bytes one slot receives
+        for (int b = 0; b < MT / 8; ++b) xoff[b] = uint32_t(G * kSegBytes + min(8 * b + r, M - 1) * 512 + 16 * t);
 
         const uint32_t lead = leader ? 1u : 0u;
-        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1, islot = 0, checked = -1;
+        int fj = 0, ijob = 0, itile = 0, isg = 0, iS = 1, islot = 0, checked = -1, ivalid = 1;
         const uint8_t *iptr = nullptr;
+        size_t istride = 0;                                   // bytes from one tile's segment to the next tile's
         bool ihave = false, iend = false, reserved = false;
         unsigned nt = 0;
         unsigned *const ctr = &p.hdr->next_tile;
@@ -1081,12 +1098,14 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
                 iend = true;
                 return;
             }
-            while (int(g) >= job(fj).tile0 + ((job(fj).N + 15) >> 4)) ++fj;
+            while (int(g) >= job(fj).tile0 + units_of(job(fj))) ++fj;
             ijob = fj;
-            itile = int(g) - job(fj).tile0;
+            itile = int(g) - job(fj).tile0;                   // unit: tiles G itile ..
             isg = 0;
             iS = job(fj).K >> 8;
-            iptr = job(fj).seg + size_t(itile) * size_t(job(fj).tstride) * kSegBytes;
+            istride = size_t(job(fj).tstride) * kSegBytes;
+            iptr = job(fj).seg + size_t(G * itile) * istride;
+            ivalid = min(G, ((job(fj).N + 15) >> 4) - G * itile);
             ihave = true;
         };
         // are the waits of entry e met (lane 0's acquire loads, broadcast)
@@ -1120,6 +1139,7 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
             reserve(res ? lead : 0u);
             reserved |= res;
             const uint32_t bar = bars + 8 * islot, dst = ring + uint32_t(islot) * uint32_t(slot_bytes);
+            const uint32_t tx = uint32_t(ivalid * kSegBytes + M * 512);   // bytes this slot receives
             const CUtensorMap *tm = p.tmaps + ijob;
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
@@ -1130,9 +1150,19 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
                 "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%11], [%12, {%13, %14}], [%6];\n\t"
                 "}" ::"r"(lead),
                 "r"(descs + 16 * islot), "r"(ijob), "r"(itile), "r"(isg), "r"(iS), "r"(bar), "r"(tx), "r"(dst),
-                "l"(iptr), "r"(uint32_t(kSegBytes)), "r"(dst + uint32_t(kSegBytes)), "l"(reinterpret_cast<uint64_t>(tm)),
-                "r"(isg * 256), "r"(0)
+                "l"(iptr), "r"(uint32_t(kSegBytes)), "r"(dst + uint32_t(G * kSegBytes)),
+                "l"(reinterpret_cast<uint64_t>(tm)), "r"(isg * 256), "r"(0)
                 : "memory");
+#pragma unroll
+            for (int k = 1; k < G; ++k)                       // the unit's other tiles (when they exist)
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\t"
+                    "setp.ne.u32 p, %0, 0;\n\t"
+                    "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%2], %3, [%4];\n\t"
+                    "}" ::"r"(k < ivalid ? lead : 0u),
+                    "r"(dst + uint32_t(k * kSegBytes)), "l"(iptr + size_t(k) * istride), "r"(uint32_t(kSegBytes)),
+                    "r"(bar)
+                    : "memory");
             iptr += kSegBytes;
             ihave = ++isg < iS;
             islot = islot + 1 == slots ? 0 : islot + 1;
@@ -1149,9 +1179,11 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
             }
             if (++in_flight == slots) break;
         }
-        float acc[MT / 2];
+        float acc[G][MT / 2];
 #pragma unroll
-        for (int i = 0; i < MT / 2; ++i) acc[i] = 0.f;
+        for (int k = 0; k < G; ++k)
+#pragma unroll
+            for (int i = 0; i < MT / 2; ++i) acc[k][i] = 0.f;
         int cslot = 0;
         uint32_t cphase = 0;
         while (in_flight > 0 || blocked) {
@@ -1181,12 +1213,14 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
             const int4 d = lds_s4(descs + 16 * cslot);
             if (d.z == 0) {
 #pragma unroll
-                for (int i = 0; i < MT / 2; ++i) acc[i] = 0.f;
+                for (int k = 0; k < G; ++k)
+#pragma unroll
+                    for (int i = 0; i < MT / 2; ++i) acc[k][i] = 0.f;
             }
             uint32_t xr[MT / 8];
 #pragma unroll
             for (int b = 0; b < MT / 8; ++b) xr[b] = cb + xoff[b];
-            segment_wide<MT>(cb, aoff, srow, xr, acc);
+            segment_wide<MT, G>(cb, aoff, srow, xr, acc);
             // every lane's reads of the slot are done before lane 0's copies refill it
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1201,15 +1235,22 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
             }
             if (d.z == d.w - 1) {
                 const StepJob &jb = job(d.x);
-                if (!(jb.flags & (63 << kStepSplitShift))) {
-                    finish_wide<MT>(acc, jb, d.y * 16, lane, M);
-                    if (jb.flags & kStepPublish) {
-                        __syncwarp();
-                        if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                const int tiles = (jb.N + 15) >> 4;
+#pragma unroll
+                for (int k = 0; k < G; ++k) {
+                    const int rt = G * d.y + k;
+                    if (rt >= tiles) break;
+                    if (!(jb.flags & (63 << kStepSplitShift))) {
+                        finish_wide<MT>(acc[k], jb, rt * 16, lane, M);
+                        if (jb.flags & kStepPublish) {
+                            __syncwarp();
+                            if (leader) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                        }
+                    } else if (!post_part_wide<MT>(acc[k], jb, d.x, rt, lane, M, p, my_posted, my_taken, my_posts,
+                                                   s_abort)) {
+                        ok = false;
+                        break;
                     }
-                } else if (!post_part_wide<MT>(acc, jb, d.x, d.y, lane, M, p, my_posted, my_taken, my_posts,
-                                               s_abort)) {
-                    ok = false;
                 }
             }
             if (++cslot == slots) {
@@ -1352,7 +1393,7 @@ bool wide_launch_shape(int M, int n_jobs, int n_pub, WideShape *sh)
 {
     const size_t cap = size_t(227) * 1024 - 128;
     const int nw = M <= 8 ? sp::Wide<8>::kWarps : sp::Wide<16>::kWarps;
-    const int slot_bytes = sp::kSegBytes + M * 512;
+    const int slot_bytes = wide_group(M) * sp::kSegBytes + M * 512;
     for (int slots = 4; slots >= 2; --slots) {
         for (int cached = std::min(n_jobs, 256);; cached = cached > 16 ? cached / 2 : 0) {
             const size_t need = sp::WSmem(nw, slots, slot_bytes, n_pub, cached).total;

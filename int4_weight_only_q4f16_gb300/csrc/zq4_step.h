@@ -15,6 +15,9 @@ namespace zq4 {
 
 constexpr int kStepMaxM = 2;          // tokens the step engine handles
 constexpr int kWideMaxM = 16;         // tokens the wide step engine handles (3 ..)
+constexpr int kWideGroup16 = 2;       // k_wide above 8 tokens: 16-row tiles per work unit
+// 16-row tiles per work unit of the wide step engine at M tokens
+inline int wide_group(int M) { return M > 8 ? kWideGroup16 : 1; }
 constexpr int kStepWarps = 16;        // compute warps per CTA
 constexpr int kStepMaxWaits = 3;      // jobs one job may wait for
 
