@@ -222,11 +222,14 @@ ZQ4_API zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scale
  *
  * wq [N, K/8] u32, scales [N, K/32] f16, x [M, K] f16, resid / res_out / out
  * [M, N] f16, gamma [N] f16; eps >= 0 (finite). work: caller-owned device
- * scratch of zq4_add_rmsnorm_work_bytes(M, N) bytes, 16-byte aligned, whose
- * first 16 bytes must be zero before the first call; every call leaves them
- * zero (the rest is overwritten); calls sharing one work buffer must be
- * ordered on one stream. One launch per block of up to 8 tokens;
- * the last CTA of each normalises all N outputs (fixed reduction order, no
+ * scratch of zq4_add_rmsnorm_work_bytes(M, N) = 16 + 4 M N + 64 ceil(N/16)
+ * bytes, 16-byte aligned, whose first 16 bytes must be zero before the
+ * first call; every call leaves them zero (the rest is overwritten); calls
+ * sharing one work buffer must be ordered on one stream. K % 256 == 0: the
+ * tensor-core decode kernel with the add in its epilogue, one launch per
+ * block of up to 16 tokens, each CTA adding its rows' squares per token;
+ * else the CUDA-core kernel, blocks of up to 8 tokens. The last CTA of each
+ * launch normalises all N outputs (fixed reduction order, no
  * floating-point atomics: repeated calls give identical bits). Outputs and
  * work must not overlap each other or any input. Errors: ZQ4_ERR_NULL,
  * ZQ4_ERR_SHAPE (M, N or K, or eps), ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,

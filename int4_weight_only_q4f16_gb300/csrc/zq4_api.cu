@@ -185,7 +185,9 @@ zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const
 
 size_t zq4_add_rmsnorm_work_bytes(int M, int N)
 {
-    return M > 0 && N > 0 ? 16 + size_t(M) * N * 4 : 0;
+    // counter, fp32 r [M][N], then 16 floats per 16-row tile (the tensor-core
+    // kernel's per-CTA sums of squares)
+    return M > 0 && N > 0 ? 16 + size_t(M) * N * 4 + size_t((N + 15) / 16) * 64 : 0;
 }
 
 zq4_status zq4_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
@@ -200,7 +202,8 @@ zq4_status zq4_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, cons
         (reinterpret_cast<uintptr_t>(gamma) & 1) || (reinterpret_cast<uintptr_t>(res_out) & 1) ||
         (reinterpret_cast<uintptr_t>(out) & 1))
         return ZQ4_ERR_ALIGN;
-    if (size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
+    const bool tc = decode_tc_supported(std::min(M, 16), K);
+    if (!tc && size_t(K) * 2 > decode_max_smem()) return ZQ4_ERR_UNSUPPORTED;
     const size_t mn = size_t(M) * N * 2, wbytes = zq4_add_rmsnorm_work_bytes(M, N);
     const void *ins[5] = {wq, scales, x, resid, gamma};
     const size_t inb[5] = {wq_bytes(N, K), sc_bytes(N, K), size_t(M) * K * 2, mn, size_t(N) * 2};
@@ -212,6 +215,9 @@ zq4_status zq4_gemv_add_rmsnorm(const uint32_t *wq, const uint16_t *scales, cons
         for (int q = o + 1; q < 3; ++q)
             if (overlap(outs[o], outb[o], outs[q], outb[q])) return ZQ4_ERR_OVERLAP;
     }
+    if (tc)   // the tensor-core kernel with the add + RMSNorm epilogue
+        return cuda_status(launch_decode_tc_addnorm(wq, scales, x, resid, gamma, eps, res_out, out, work, M, N, K,
+                                                    static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_add_rmsnorm(wq, scales, x, resid, gamma, eps, res_out, out, work, M, N, K,
                                           static_cast<cudaStream_t>(stream)));
 }

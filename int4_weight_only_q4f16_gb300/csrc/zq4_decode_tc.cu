@@ -46,6 +46,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <atomic>
 
 #include "zq4_async.cuh"
@@ -99,6 +100,9 @@ constexpr int kGpw = (kKC / 32 + kWarps - 1) / kWarps;   // groups of a stage pe
 constexpr uint32_t kSevenEighths = 0x3B003B00u;   // f16x2 (7/8, 7/8)
 constexpr int kUnpack = ZQ4_TC_UNPACK;
 constexpr int kPrefetch = ZQ4_TC_PREFETCH;
+constexpr int kPartLoads = 16;
+__device__ __forceinline__ float lo_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w)); }
+__device__ __forceinline__ float hi_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w >> 16)); }                    // add + RMSNorm: at most 32 x 16 CTAs per launch
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1 KB swizzle alignment");
 
@@ -160,6 +164,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     float *zp = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes());
     uint8_t *xs = smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes() + zp_bytes<NB>(K);
     const int chunks = (K + kKC - 1) / kKC;
+    // add + RMSNorm epilogue: squares of a tile's rows, the CTA's running sums per token
+    __shared__ float s_sq[RU == 4 ? 16 : 1][16];
+    __shared__ float s_ss[RU == 4 ? 16 : 1];
+    if (RU == 4 && threadIdx.x < 16) s_ss[threadIdx.x] = 0.f;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -303,6 +311,11 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        // add + RMSNorm: this thread's residual value of the tile, fetched
+        // now so that its latency hides behind the tile's compute
+        float rres = 0.f;
+        if (RU == 4 && threadIdx.x < 16 * a.M && tile * 16 + (threadIdx.x & 15) < N)
+            rres = f16_bits_to_float(a.resid[size_t(threadIdx.x >> 4) * N + tile * 16 + (threadIdx.x & 15)]);
         float acc[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
@@ -418,6 +431,29 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 }
                 if (i == 0 && o < 16 * a.M) atomicMax(a.amax + m, key);
             }
+        } else if (RU == 4) {
+            // r = resid + x W^T: the new residual (f16 and fp32), and the
+            // CTA's running sum of r^2 per token (rows in order, tiles in order)
+            if (threadIdx.x < 16 * a.M) {                    // 16 M <= 256 outputs: one per thread
+                const int o = threadIdx.x, m = o >> 4, i = o & 15;
+                float v = 0.f;
+                if (row0 + i < N) {
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) v += red[((w * NB + (m >> 3)) * 16 + i) * 8 + (m & 7)];
+                    const size_t at = size_t(m) * N + row0 + i;
+                    v += rres;
+                    a.y[at] = float_to_f16_bits(v);
+                    a.r32[at] = v;
+                }
+                s_sq[m][i] = v * v;
+            }
+            named_barrier_compute();
+            if (threadIdx.x < a.M) {
+                float t = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) t += s_sq[threadIdx.x][i];
+                s_ss[threadIdx.x] += t;
+            }
         } else {
             for (int o = threadIdx.x; o < 8 * a.M; o += kWarps * 32) {
                 const int m = o >> 3, j = o & 7;
@@ -436,6 +472,78 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
         named_barrier_compute();
     }
     if (!ok && lane == 0) atomicOr(&g_device_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+    if (RU == 4) {
+        // The last CTA to finish adds the CTAs' sums of squares (CTA order,
+        // in a fixed pattern: lane l takes CTAs l, l + 32, ..) and writes
+        // every token's normalised rows; it leaves the counter at zero.
+        __shared__ int s_last;
+        __shared__ float s_inv[16];
+        named_barrier_compute();
+        if (threadIdx.x < a.M) a.part[size_t(blockIdx.x) * 16 + threadIdx.x] = s_ss[threadIdx.x];
+        named_barrier_compute();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+        }
+        named_barrier_compute();
+        if (s_last) {
+            __threadfence();
+            // (grid <= 32 kPartLoads CTAs: the launcher caps it; all loads in flight at once)
+            for (int m = warp; m < a.M; m += kWarps) {
+                float v[kPartLoads];
+#pragma unroll
+                for (int j = 0; j < kPartLoads; ++j) {
+                    const int c = lane + 32 * j;
+                    v[j] = c < int(gridDim.x) ? __ldcg(a.part + size_t(c) * 16 + m) : 0.f;
+                }
+                float t = 0.f;
+#pragma unroll
+                for (int j = 0; j < kPartLoads; ++j) t += v[j];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) s_inv[m] = 1.0f / sqrtf(t / float(N) + a.eps);
+            }
+            named_barrier_compute();
+            // every token's rows: four at a time where N allows (16-byte fp32
+            // loads), the loads of a pass issued before its stores
+            for (int m = 0; m < a.M; ++m) {
+                const float inv = s_inv[m];
+                const float *rr = a.r32 + size_t(m) * N;
+                uint16_t *oo = a.out + size_t(m) * N;
+                // (8-byte gamma and out rows: N % 4 == 0 keeps every row at the base's alignment)
+                if ((N & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.gamma) | reinterpret_cast<uintptr_t>(a.out)) & 7) == 0) {
+                    const int n4 = N >> 2;
+                    for (int q0 = threadIdx.x; q0 < n4; q0 += 4 * kWarps * 32) {
+                        float4 rv[4];
+                        uint2 gv[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const int q = q0 + b * kWarps * 32;
+                            if (q < n4) {
+                                rv[b] = __ldcg(reinterpret_cast<const float4 *>(rr) + q);
+                                gv[b] = *reinterpret_cast<const uint2 *>(a.gamma + 4 * q);
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const int q = q0 + b * kWarps * 32;
+                            if (q < n4) {
+                                const uint32_t lo = uint32_t(float_to_f16_bits(rv[b].x * inv * lo_f32(gv[b].x))) |
+                                                    (uint32_t(float_to_f16_bits(rv[b].y * inv * hi_f32(gv[b].x))) << 16);
+                                const uint32_t hi = uint32_t(float_to_f16_bits(rv[b].z * inv * lo_f32(gv[b].y))) |
+                                                    (uint32_t(float_to_f16_bits(rv[b].w * inv * hi_f32(gv[b].y))) << 16);
+                                *reinterpret_cast<uint2 *>(oo + 4 * q) = make_uint2(lo, hi);
+                            }
+                        }
+                    }
+                } else {
+                    for (int n = threadIdx.x; n < N; n += kWarps * 32)
+                        oo[n] = float_to_f16_bits(__ldcg(rr + n) * inv * f16_bits_to_float(a.gamma[n]));
+                }
+            }
+            if (threadIdx.x == 0) *a.counter = 0u;
+        }
+    }
     if (RU == 3) {
         // The last CTA to finish turns the keys into rows and logits and
         // leaves keys and counter at zero for the next call (every CTA
@@ -520,7 +628,8 @@ cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgs 
     if (e != cudaSuccess) return e;
     // CTAs per SM by shared memory (1 KB per CTA is reserved), at most ZQ4_TC_OCC.
     const int occ = std::max(1, std::min(ZQ4_TC_OCC, int(smem_per_sm() / (smem + 1024))));
-    const int grid = std::max(1, std::min(a.tiles, occ * sm_count()));
+    int grid = std::max(1, std::min(a.tiles, occ * sm_count()));
+    if (RU == 4) grid = std::min(grid, 32 * kPartLoads);   // the last CTA reads one sum per CTA
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, mc, ms, a);
 }
 
@@ -593,6 +702,45 @@ cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, 
         a.maxval = maxval ? maxval + m0 : nullptr;
         a.M = mt;
         e = nb == 2 ? tc::launch_t<2, 3>(mc, ms, a, s) : tc::launch_t<1, 3>(mc, ms, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_tc_addnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                                     const uint16_t *resid, const uint16_t *gamma, float eps, uint16_t *res_out,
+                                     uint16_t *out, void *work, int M, int N, int K, cudaStream_t s)
+{
+    CUtensorMap mc, ms;
+    cudaError_t e = tc::make_maps(wq, scales, N, K, &mc, &ms);
+    if (e != cudaSuccess) return e;
+    TcArgs a;
+    memset(&a, 0, sizeof(a));
+    a.wq = wq;
+    a.scales = scales;
+    a.N = N;
+    a.K = K;
+    a.tiles = (N + 15) / 16;
+    a.y_stride = N;
+    a.gamma = gamma;
+    a.eps = eps;
+    a.counter = static_cast<unsigned *>(work);
+    float *r32 = reinterpret_cast<float *>(static_cast<uint8_t *>(work) + 16);
+    a.part = r32 + size_t(M) * N;
+    const bool fit16 = tc::smem_bytes<2>(16, K) <= 220 * 1024;
+    for (int m0 = 0; m0 < M;) {
+        const int rem = M - m0;
+        const int nb = (rem > 8 && fit16) ? 2 : 1;
+        const int mt = std::min(rem, 8 * nb);
+        const size_t o = size_t(m0) * N;
+        a.x = x + size_t(m0) * K;
+        a.resid = resid + o;
+        a.y = res_out + o;
+        a.out = out + o;
+        a.r32 = r32 + o;
+        a.M = mt;
+        e = nb == 2 ? tc::launch_t<2, 4>(mc, ms, a, s) : tc::launch_t<1, 4>(mc, ms, a, s);
         if (e != cudaSuccess) return e;
         m0 += mt;
     }

@@ -83,6 +83,14 @@ struct TcArgs {
     unsigned long long *done;       // CTAs finished (argmax epilogue; zero on entry, left zero)
     int32_t *idx;                   // [M] argmax rows, written by the last CTA
     float *maxval;                  // [M] argmax logits or null, written by the last CTA
+    // residual add + RMSNorm epilogue (y = the new residual, f16)
+    const uint16_t *resid;          // [M][N]
+    const uint16_t *gamma;          // [N]
+    uint16_t *out;                  // [M][N] f16(r / rms * gamma), written by the last CTA
+    float *r32;                     // [M][N] r in fp32
+    float *part;                    // [CTAs][16] each CTA's sum of r^2 per token
+    unsigned *counter;              // CTAs done (zero on entry, left zero)
+    float eps;
 };
 
 size_t smem_per_sm();      // shared memory per SM of the current device (cached)
@@ -94,6 +102,12 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
 // fp32 logits (y32 may be null) and the per-token argmax in the same launch
 // (per block of tokens): work = [M] keys then 8 counters, zero on entry and
 // left zero
+// GEMV + residual add + RMSNorm on the tensor-core kernel: work = 16 bytes
+// of counter (zero on entry, left zero), fp32 r [M][N], then 16 floats per
+// 16-row tile of W (the CTAs' partial sums of squares)
+cudaError_t launch_decode_tc_addnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
+                                     const uint16_t *resid, const uint16_t *gamma, float eps, uint16_t *res_out,
+                                     uint16_t *out, void *work, int M, int N, int K, cudaStream_t s);
 cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
                                     int32_t *idx, float *maxval, unsigned long long *work, int M, int N, int K,
                                     cudaStream_t s);

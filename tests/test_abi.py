@@ -143,7 +143,7 @@ def test_add_rmsnorm_host_checks(lib):
     S, X, R, G, O1, O2, W = (A + (i << 30) for i in range(1, 8))
     f = lib.lib.zq4_gemv_add_rmsnorm
     ok = (P(A), P(S), P(X), P(R), P(G), 1e-5, P(O1), P(O2), P(W), 1, 64, 64, P(0))
-    assert lib.lib.zq4_add_rmsnorm_work_bytes(2, 64) == 16 + 2 * 64 * 4
+    assert lib.lib.zq4_add_rmsnorm_work_bytes(2, 64) == 16 + 2 * 64 * 4 + 4 * 64
     assert lib.lib.zq4_add_rmsnorm_work_bytes(0, 64) == 0
     args = list(ok); args[8] = P(0)
     assert f(*args) == lib.ZQ4_ERR_NULL

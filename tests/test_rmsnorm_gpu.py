@@ -23,7 +23,7 @@ def _case(tag, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 3072, 3072), (1, 3072, 8192), (3, 333, 256), (8, 1000, 512),
-                                   (11, 64, 96)])
+                                   (16, 2000, 1024), (17, 3072, 3072), (11, 64, 96)])
 def test_add_rmsnorm_matches_oracle(oracle, M, N, K):
     from int4_weight_only_q4f16_gb300 import zq4
     wq, sc, x, res, gam = _case("addnorm", M, N, K)
