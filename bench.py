@@ -69,6 +69,10 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the Phi-3 stack (32 is the workload; fewer only for profiling)")
     ap.add_argument("--t", type=int, default=16, help="tokens per step (moe workload)")
+    ap.add_argument("--moe-stages", action="store_true",
+                    help="moe workload: the two per-stage zq4_moe_gemv calls instead of zq4_moe_block")
+    ap.add_argument("--moe-block", action="store_true",
+                    help="moe workload: zq4_moe_block at any T (the default uses it from 16 tokens)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -621,10 +625,22 @@ def run_moe(args, torch, dist, peaks, peak_kind):
         uniq_bytes.append(nu * (N2 * (D // 8) * 4 + N2 * (D // per_scale) * sb + Dn * (I // 8) * 4 +
                                 Dn * (I // per_scale) * sb))
     stream = torch.cuda.Stream()
+    # the q4f16_1 block as one call (each touched expert read once per stage)
+    # where it measured faster than the two per-stage calls (16 tokens: 30% of
+    # HBM against 25%; at 1 and 4 tokens its three launches' fixed cost loses)
+    block = not aff and not args.moe_stages and (T >= 16 or args.moe_block)
+    works = [torch.zeros(zq4.moe_block_work_bytes(T, top_k, D, I), dtype=torch.uint8, device="cuda")
+             for _ in range(banks)] if block else []
+    # the block reads the banks in the segmented layout (same bytes, permuted; made once)
+    gsegs = [zq4.prepare_weight(gq[b], gs[b], E * N2, D, zq4.PREP_SEGMENTED)[0] for b in range(banks)] if block else []
+    dsegs = [zq4.prepare_weight(dq[b], ds[b], E * Dn, I, zq4.PREP_SEGMENTED)[0] for b in range(banks)] if block else []
 
     def chain():
         for b in range(banks):
-            if aff:
+            if block:
+                zq4.moe_block(gsegs[b], dsegs[b], E, xs[b], D, I, ids[b], rs[b], y=ys[b], work=works[b],
+                              stream=stream)
+            elif aff:
                 zq4.moe_gemv_affine(gq[b], gs[b], gbi[b], E, xs[b], N2, D, ids[b], zq4.MOE_GATE_UP_SILU, y=hs[b],
                                     stream=stream)
                 zq4.moe_gemv_affine(dq[b], ds[b], dbi[b], E, hs[b], Dn, I, ids[b], zq4.MOE_DOWN_COMBINE,
@@ -646,7 +662,8 @@ def run_moe(args, torch, dist, peaks, peak_kind):
                       "MoE expert GEMV block (gate_up+SiLU, down+combine) GB/s over unique experts",
             "value": round(ub / per / 1e9, 1), "unit": "GB/s", "T": T, "us_per_block": round(per * 1e6, 3),
             "unique_expert_bytes": ub, "frac_of_measured": round(ub / per / 1e9 / peaks["hbm_gbs"], 4),
-            "config": {"workload": f"MoE 128 experts top-8, T={T}", "banks": banks}}
+            "config": {"workload": f"MoE 128 experts top-8, T={T}", "banks": banks,
+                       "path": "zq4_moe_block" if block else "zq4_moe_gemv stages"}}
 
 
 def run_kernel(args, torch, dist, peaks, peak_kind):

@@ -313,6 +313,44 @@ ZQ4_API zq4_status zq4_moe_gemv(const uint32_t *wq_bank, const uint16_t *scales_
                         const int32_t *expert_ids, const float *route_w, int top_k, int mode,
                         int32_t *dev_status, void *stream);
 
+/*
+ * zq4_moe_block -- the whole MoE block of zq4_moe_gemv's two stages in one
+ * call, each expert touched by the routing read once per stage: the
+ * (token, slot) pairs are grouped by expert on the device (every CTA builds
+ * the same grouping: touched experts in order of their first pair, each
+ * expert's pairs in pair order), a work unit is (expert, block of up to 16
+ * of its pairs, 16 rows of its matrix), and each warp streams its units'
+ * segments through its own ring of bulk copies into the tensor-core
+ * segment loop (the pairs are the MMA columns; x staged once per CTA):
+ * gate_up + SiLU*mul into h, down into fp32 z, then the weighted combine
+ * adds each token's slots in slot order (repeated calls give identical
+ * bits). Source: "Zero-TVM benchmarks", section "MoE chunked prefill";
+ * "Zero TVM Documentation", section "Qwen3.6-35B-A3B MoE".
+ *
+ *   gu_seg: the [E * 2I, D] gate/up bank (rows interleaved per expert, as
+ *   zq4_gate_up_silu) in the segmented layout (zq4_prepare_weight with
+ *   ZQ4_PREP_SEGMENTED over all E * 2I rows); dn_seg: the [E * D, I] down
+ *   bank, segmented; x [T, D] f16; y [T, D] f16:
+ *     y[t] = f16( sum_j route_w[t,j] * W_dn[e](h[t,j]) ),
+ *     h[t,j] = f16( silu/mul epilogue of W_gu[e] x[t] ),  e = expert_ids[t,j],
+ *   fp32 accumulation; an id outside [0, E) contributes nothing and sets
+ *   ZQ4_DEV_BAD_EXPERT_ID in *dev_status (may be NULL).
+ * work: device scratch of zq4_moe_block_work_bytes(T, top_k, D, I) bytes,
+ * 16-byte aligned, caller-owned; it holds, from its start, the grouping as
+ * int32: U (touched experts), V (valid pairs), the V pair indices (t top_k
+ * + j) grouped by expert then P - V of -1, the U expert ids then -1, the
+ * U + 1 start offsets of each expert's pairs then -1 (P = T top_k), padded
+ * to 256 bytes; then h [P, I] f16 (padded to 256 bytes) and z [P, D] fp32.
+ * D and I multiples of 256, P <= 256 (else ZQ4_ERR_UNSUPPORTED: the
+ * per-stage zq4_moe_gemv takes any shape), 1 <= top_k <= 32. Errors:
+ * ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED, ZQ4_ERR_CUDA.
+ */
+ZQ4_API size_t zq4_moe_block_work_bytes(int T, int top_k, int D, int I);
+ZQ4_API zq4_status zq4_moe_block(const void *gu_seg, const void *dn_seg, int num_experts, const uint16_t *x,
+                                 uint16_t *y, int T, int D, int I, const int32_t *expert_ids, const float *route_w,
+                                 int top_k, void *work, size_t work_bytes, int32_t *dev_status, void *stream);
+
 /* Flags of zq4_prepare_weight (ZQ4_PREP_SEGMENTED may be OR-ed with
  * ZQ4_PREP_CONCAT_TO_INTERLEAVED). */
 #define ZQ4_PREP_COPY 0                  /* plain copy of the canonical layout */

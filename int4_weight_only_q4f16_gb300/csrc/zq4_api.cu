@@ -392,6 +392,39 @@ zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *scales_b
                       mode, dev_status, stream);
 }
 
+size_t zq4_moe_block_work_bytes(int T, int top_k, int D, int I)
+{
+    if (T <= 0 || top_k <= 0 || D <= 0 || I <= 0) return 0;
+    return moe_block_work_layout(T, top_k, D, I, nullptr, nullptr);
+}
+
+zq4_status zq4_moe_block(const void *gu_seg, const void *dn_seg, int num_experts, const uint16_t *x, uint16_t *y,
+                         int T, int D, int I, const int32_t *expert_ids, const float *route_w, int top_k, void *work,
+                         size_t work_bytes, int32_t *dev_status, void *stream)
+{
+    if (!gu_seg || !dn_seg || !x || !y || !expert_ids || !route_w || !work) return ZQ4_ERR_NULL;
+    if (num_experts <= 0 || T <= 0 || top_k <= 0 || top_k > 32 || D <= 0 || I <= 0 || D % 256 || I % 256)
+        return ZQ4_ERR_SHAPE;
+    if (!moe_block_supported(T, top_k, D, I)) return ZQ4_ERR_UNSUPPORTED;
+    size_t h_off, z_off;
+    const size_t need = moe_block_work_layout(T, top_k, D, I, &h_off, &z_off);
+    if (work_bytes < need) return ZQ4_ERR_SHAPE;
+    if (!aligned16(gu_seg) || !aligned16(dn_seg) || !aligned16(x) || !aligned16(work) ||
+        (reinterpret_cast<uintptr_t>(y) & 1) || (reinterpret_cast<uintptr_t>(expert_ids) & 3) ||
+        (reinterpret_cast<uintptr_t>(route_w) & 3) || (reinterpret_cast<uintptr_t>(dev_status) & 3))
+        return ZQ4_ERR_ALIGN;
+    const size_t E = size_t(num_experts), P = size_t(T) * top_k;
+    const void *ins[5] = {gu_seg, dn_seg, x, expert_ids, route_w};
+    const size_t inb[5] = {E * segmented_bytes(2 * I, D), E * segmented_bytes(D, I), size_t(T) * D * 2, P * 4, P * 4};
+    const size_t yb = size_t(T) * D * 2;
+    for (int i = 0; i < 5; ++i)
+        if (overlap(y, yb, ins[i], inb[i]) || overlap(work, need, ins[i], inb[i])) return ZQ4_ERR_OVERLAP;
+    if (overlap(y, yb, work, need)) return ZQ4_ERR_OVERLAP;
+    return cuda_status(launch_moe_block(static_cast<const uint8_t *>(gu_seg), static_cast<const uint8_t *>(dn_seg),
+                                        num_experts, x, y, T, D, I, expert_ids, route_w, top_k, work, dev_status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 zq4_status zq4_device_errors(uint32_t *flags, int clear)
 {
     if (!flags) return ZQ4_ERR_NULL;

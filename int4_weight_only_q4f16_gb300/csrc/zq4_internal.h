@@ -108,6 +108,14 @@ cudaError_t launch_decode_tc(const uint32_t *wq, const uint16_t *scales, const u
 cudaError_t launch_decode_tc_addnorm(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
                                      const uint16_t *resid, const uint16_t *gamma, float eps, uint16_t *res_out,
                                      uint16_t *out, void *work, int M, int N, int K, cudaStream_t s);
+// The MoE block on the step kernels' segment loop (zq4_moe_block, zq4_step.cu):
+// gate_up + SiLU*mul of every (token, slot) pair into h, down into fp32 z,
+// then the weighted combine; each touched expert read once per stage.
+bool moe_block_supported(int T, int top_k, int D, int I);
+size_t moe_block_work_layout(int T, int top_k, int D, int I, size_t *h_off, size_t *z_off);
+cudaError_t launch_moe_block(const uint8_t *gu_seg, const uint8_t *dn_seg, int num_experts, const uint16_t *x,
+                             uint16_t *y, int T, int D, int I, const int32_t *ids, const float *route_w, int top_k,
+                             void *work, int32_t *dev_status, cudaStream_t s);
 cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
                                     int32_t *idx, float *maxval, unsigned long long *work, int M, int N, int K,
                                     cudaStream_t s);

@@ -74,6 +74,7 @@
 #include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
+#include "zq4_moe_group.cuh"
 #include "zq4_segment.cuh"
 #include "zq4_step.h"
 
@@ -1286,6 +1287,258 @@ __global__ void __launch_bounds__(Wide<MT>::kThreads, 1) k_wide(Params p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// The MoE block's expert stages (k_moe)
+// ---------------------------------------------------------------------------
+// A stage of zq4_moe_block: MODE 1 gate_up + SiLU*mul (x = the T tokens,
+// output h per (token, slot) pair), MODE 2 down (x = h of the P pairs,
+// output fp32 z per pair). Every CTA stages all of x once and builds the
+// expert grouping; a work unit is (touched expert, block of up to 16 of its
+// pairs, 16-row tile of its matrix), dealt round-robin to the warps of the
+// grid; each warp streams its units' segments (the bank in the segmented
+// layout) through its own ring of bulk copies, the next unit's copies in
+// flight while it finishes the current one. Column m of the accumulator is
+// the block's pair m (two blocks of 8 when it has more than 8 pairs).
+constexpr int kMoeWarps = 12;
+
+struct MoeParams {
+    const uint8_t *seg;       // the bank, segmented ([E * N rows] x K)
+    const uint16_t *x;        // [rows][K]
+    const int32_t *ids;       // [T][top_k]
+    int32_t *dev_status;      // may be null
+    int32_t *group;           // the published grouping (MODE 1), may be null
+    uint16_t *h;              // MODE 1: [P][N / 2]
+    float *z;                 // MODE 2: [P][N]
+    int T, top_k, E, N, K, rows, slots, xpitch;
+};
+
+// MoE shared memory: staged x, the grouping, the rings and their barriers.
+struct MSmem {
+    uint32_t xs, grp, ring, bars, xbar, total;
+    __host__ __device__ MSmem(int rows, int xpitch, int P, int slots)
+    {
+        xs = 0;
+        grp = (uint32_t(rows) * uint32_t(xpitch) + 127) / 128 * 128;
+        ring = (grp + uint32_t(moe_group_smem_ints(P)) * 4 + 127) / 128 * 128;
+        bars = ring + uint32_t(kMoeWarps * slots) * kSegBytes;
+        xbar = bars + uint32_t(kMoeWarps * slots) * 8;
+        total = xbar + 8;
+    }
+};
+
+// One segment into acc[0 .. MT/2) (MT = 8: one block of 8 pair columns, 16:
+// two); x of the lane's column of block b at xr[b] + 64 g.
+template <int MT>
+__device__ __forceinline__ void segment_moe(uint32_t cb, uint32_t aoff, uint32_t srow, const uint32_t (&xr)[2],
+                                            float (&acc)[8])
+{
+    const uint4 c0 = lds_v4(cb + aoff), c1 = lds_v4(cb + aoff + 16);
+    const uint4 c8 = lds_v4(cb + aoff + 1152), c9 = lds_v4(cb + aoff + 1168);
+    const uint4 s0 = lds_v4(cb + srow), s8 = lds_v4(cb + srow + 1152);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        uint32_t pa[4], pb[4];
+        unpack_word_f16x2(group_word(c0, c1, g), pa);
+        unpack_word_f16x2(group_word(c8, c9, g), pb);
+        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+        const float sr = scale_of(s0, g), sr8 = scale_of(s8, g);
+#pragma unroll
+        for (int b = 0; b < MT / 8; ++b) {
+            const uint4 xv = lds_v4(xr[b] + 64 * g);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(d, a0, xv.x, xv.y, d);
+            mma16816(d, a1, xv.z, xv.w, d);
+            acc[4 * b + 0] = fmaf(sr, d[0], acc[4 * b + 0]);
+            acc[4 * b + 1] = fmaf(sr, d[1], acc[4 * b + 1]);
+            acc[4 * b + 2] = fmaf(sr8, d[2], acc[4 * b + 2]);
+            acc[4 * b + 3] = fmaf(sr8, d[3], acc[4 * b + 3]);
+        }
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kMoeWarps * 32, 1) k_moe(MoeParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
+    const uint32_t sbase = smem_addr(smem);
+    const int P = p.T * p.top_k, slots = p.slots, K = p.K, N = p.N, S = K >> 8, tpe = N >> 4;
+    const MSmem L(p.rows, p.xpitch, P, slots);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x, nthr = blockDim.x;
+
+    griddep_wait();                                       // routing and x may come from the previous kernel
+    const uint32_t xbar = sbase + L.xbar;
+    if (lane == 0)
+        for (int j = 0; j < slots; ++j) mbar_init(sbase + L.bars + 8 * (warp * slots + j), 1);
+    if (tid == 0) {
+        mbar_init(xbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(xbar, uint32_t(p.rows) * uint32_t(K * 2));   // every x row, one bulk copy each
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const MoeGroup g = moe_group(p.ids, P, p.E, reinterpret_cast<int *>(smem + L.grp), p.dev_status,
+                                 MODE == 1 && blockIdx.x == 0, tid, nthr);   // ends with a barrier
+    if (blockIdx.x == 0 && MODE == 1) {
+        if (p.group) moe_group_publish(g, P, p.group, tid, nthr);
+        // h rows of a pair with a bad expert id are zero
+        const int half = N >> 1;
+        for (int i = tid; i < P * half; i += nthr) {
+            const int e = p.ids[i / half];
+            if (e < 0 || e >= p.E) p.h[i] = 0;
+        }
+    }
+    griddep_launch_dependents();
+    const int n_units = g.J * tpe, stride = int(gridDim.x) * kMoeWarps;
+    const uint32_t ring = sbase + L.ring + uint32_t(warp * slots) * kSegBytes;
+    const uint32_t bars = sbase + L.bars + uint32_t(8 * warp * slots);
+    const uint32_t aoff = segk::lane_code_offset(lane);
+    const int r = lane >> 2, t = lane & 3;
+    const uint32_t srow = uint32_t(r * 144 + 128);
+    const bool leader = lane == 0;
+
+    // issue cursor: unit iu (of this warp's), segment is
+    int iu = int(blockIdx.x) * kMoeWarps + warp, is = 0, islot = 0;
+    auto unit_seg = [&](int u) -> const uint8_t * {       // first segment of unit u in the bank
+        const int j = u / tpe, tl = u - j * tpe;
+        return p.seg + size_t(g.uexp[g.jt[j] >> 8] * tpe + tl) * size_t(S) * kSegBytes;
+    };
+    const uint8_t *iptr = iu < n_units ? unit_seg(iu) : nullptr;
+    auto issue = [&]() -> bool {
+        if (iu >= n_units) return false;
+        if (leader) {
+            const uint32_t bar = bars + 8 * islot;
+            mbar_arrive_expect_tx(bar, uint32_t(kSegBytes));
+            bulk_load(ring + uint32_t(islot) * kSegBytes, iptr + size_t(is) * kSegBytes, uint32_t(kSegBytes), bar);
+        }
+        if (++is == S) {
+            is = 0;
+            iu += stride;
+            if (iu < n_units) iptr = unit_seg(iu);
+        }
+        islot = islot + 1 == slots ? 0 : islot + 1;
+        return true;
+    };
+    int in_flight = 0;
+    while (in_flight < slots && issue()) ++in_flight;
+    // x rows into shared memory (rows padded to xpitch bytes), behind the weights' first copies
+    for (int m = tid; m < p.rows; m += nthr)
+        bulk_load(sbase + L.xs + uint32_t(m) * uint32_t(p.xpitch), p.x + size_t(m) * K, uint32_t(K * 2), xbar);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(xbar, 0));
+
+    // consume cursor: unit cu, segment cs
+    int cu = int(blockIdx.x) * kMoeWarps + warp, cs = 0, cslot = 0, ucols = 0, ubase = 0, tl = 0;
+    uint32_t cphase = 0;
+    uint32_t xr[2] = {0, 0};
+    float acc[8];
+    while (ok && in_flight > 0) {
+        if (cs == 0) {
+            // a unit starts: its pairs and the x rows its columns read
+            const int j = cu / tpe;
+            tl = cu - j * tpe;
+            const int ue = g.jt[j] >> 8, blk = g.jt[j] & 255;
+            ubase = g.ustart[ue] + 16 * blk;
+            ucols = min(16, g.ustart[ue + 1] - ubase);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int m = min(8 * b + r, ucols - 1);   // columns past the block's pairs repeat its last pair
+                const int q = g.order[ubase + m];
+                const int row = MODE == 1 ? q / p.top_k : q;
+                xr[b] = sbase + L.xs + uint32_t(row * p.xpitch + 16 * t);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * cslot, cphase))) {
+            ok = false;
+            break;
+        }
+        const uint32_t cb = ring + uint32_t(cslot) * kSegBytes;
+        const uint32_t xs_seg[2] = {xr[0] + uint32_t(cs * 512), xr[1] + uint32_t(cs * 512)};
+        if (ucols > 8)
+            segment_moe<16>(cb, aoff, srow, xs_seg, acc);
+        else
+            segment_moe<8>(cb, aoff, srow, xs_seg, acc);
+        __syncwarp();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!issue()) --in_flight;
+        if (++cslot == slots) {
+            cslot = 0;
+            cphase ^= 1u;
+        }
+        if (++cs == S) {
+            // the unit's outputs: rows 16 tl + r + 8 h of the block's pairs
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int qq = 0; qq < 2; ++qq) {
+                        const int m = 8 * b + 2 * t + qq, row = 16 * tl + r + 8 * hh;
+                        const float v = acc[4 * b + 2 * hh + qq];
+                        if (MODE == 1) {
+                            const float u = __shfl_down_sync(0xffffffffu, v, 4);
+                            if (m < ucols && (r & 1) == 0)
+                                p.h[size_t(g.order[ubase + m]) * (N >> 1) + (row >> 1)] =
+                                    float_to_f16_bits(silu_f32(v) * u);
+                        } else if (m < ucols) {
+                            p.z[size_t(g.order[ubase + m]) * N + row] = v;
+                        }
+                    }
+            cs = 0;
+            cu += stride;
+        }
+    }
+    if (!ok && leader) {
+        atomicOr(&g_step_error, ZQ4_DEVERR_WAIT_TIMEOUT);
+        for (int c = 0; c < in_flight; ++c) {
+            const int sl = (cslot + c) % slots;
+            if (!mbar_wait(bars + 8 * sl, cphase ^ (cslot + c >= slots ? 1u : 0u))) break;
+        }
+    }
+}
+
+// The weighted combine of the MoE block: y[t, n] = f16(sum_j w[t, j] z[t top_k + j, n])
+// over the slots with a valid expert id, in slot order; one thread per 4 outputs.
+__global__ void __launch_bounds__(256) k_moe_combine(const float *z, const int32_t *ids, const float *w,
+                                                     uint16_t *y, int T, int D, int top_k, int num_experts)
+{
+    griddep_wait();
+    const int per = D >> 2;
+    const int q = int(blockIdx.x) * 256 + int(threadIdx.x);
+    if (q >= T * per) return;
+    const int t = q / per, n = (q - t * per) * 4;
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    for (int j0 = 0; j0 < top_k; j0 += 8) {            // eight slots' loads in flight, then their sums in order
+        float wj[8];
+        float4 v[8];
+        bool use[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int j = j0 + b;
+            int e = -1;
+            if (j < top_k) e = ids[t * top_k + j];
+            use[b] = e >= 0 && e < num_experts;      // a bad id contributes nothing
+            wj[b] = use[b] ? w[t * top_k + j] : 0.f;
+            v[b] = use[b] ? *reinterpret_cast<const float4 *>(z + (size_t(t) * top_k + j) * D + n)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (!use[b]) continue;
+            r0 = fmaf(wj[b], v[b].x, r0);
+            r1 = fmaf(wj[b], v[b].y, r1);
+            r2 = fmaf(wj[b], v[b].z, r2);
+            r3 = fmaf(wj[b], v[b].w, r3);
+        }
+    }
+    uint16_t *yo = y + size_t(t) * D + n;
+    yo[0] = float_to_f16_bits(r0);
+    yo[1] = float_to_f16_bits(r1);
+    yo[2] = float_to_f16_bits(r2);
+    yo[3] = float_to_f16_bits(r3);
+}
+
 }  // namespace sp
 
 // ---------------------------------------------------------------------------
@@ -1474,6 +1727,104 @@ zq4_status wide_check_resident(int M, int n_jobs, int n_pub)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, wide_threads(M), sh.smem);
     if (e != cudaSuccess) return cuda_status(e);
     return per_sm < 1 ? ZQ4_ERR_UNSUPPORTED : ZQ4_OK;
+}
+
+// ---------------------------------------------------------------------------
+// zq4_moe_block host side
+// ---------------------------------------------------------------------------
+namespace {
+
+int moe_smem_set1[kMaxDevices] = {};
+int moe_smem_set2[kMaxDevices] = {};
+
+// Ring slots (4 down to 2) next to x [rows][K] (rows padded by 16 bytes) and the grouping.
+bool moe_shape(int rows, int K, int P, int *slots, int *xpitch, size_t *smem)
+{
+    const size_t cap = size_t(227) * 1024 - 128;
+    *xpitch = K * 2 + 16;
+    for (int sl = 4; sl >= 2; --sl) {
+        const size_t need = sp::MSmem(rows, *xpitch, P, sl).total;
+        if (need <= cap) {
+            *slots = sl;
+            *smem = need + 128;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int MODE>
+cudaError_t launch_moe_stage(const sp::MoeParams &p, size_t smem, cudaStream_t s)
+{
+    auto kern = sp::k_moe<MODE>;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, MODE == 1 ? moe_smem_set1 : moe_smem_set2);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(sm_count()), dim3(sp::kMoeWarps * 32), smem, s, p);
+}
+
+}  // namespace
+
+size_t moe_block_work_layout(int T, int top_k, int D, int I, size_t *h_off, size_t *z_off)
+{
+    const size_t P = size_t(T) * top_k;
+    const size_t g = (size_t(moe_group_pub_ints(int(P))) * 4 + 255) / 256 * 256;
+    const size_t h = (P * I * 2 + 255) / 256 * 256;
+    if (h_off) *h_off = g;
+    if (z_off) *z_off = g + h;
+    return g + h + P * D * 4;
+}
+
+bool moe_block_supported(int T, int top_k, int D, int I)
+{
+    const int P = T * top_k;
+    int sl, xp;
+    size_t sm;
+    return P <= 256 && D % 256 == 0 && I % 256 == 0 && moe_shape(T, D, P, &sl, &xp, &sm) &&
+           moe_shape(P, I, P, &sl, &xp, &sm);
+}
+
+cudaError_t launch_moe_block(const uint8_t *gu_seg, const uint8_t *dn_seg, int num_experts, const uint16_t *x,
+                             uint16_t *y, int T, int D, int I, const int32_t *ids, const float *route_w, int top_k,
+                             void *work, int32_t *dev_status, cudaStream_t s)
+{
+    size_t h_off, z_off;
+    moe_block_work_layout(T, top_k, D, I, &h_off, &z_off);
+    uint8_t *wb = static_cast<uint8_t *>(work);
+    const int P = T * top_k;
+    sp::MoeParams p;
+    memset(&p, 0, sizeof(p));
+    p.ids = ids;
+    p.T = T;
+    p.top_k = top_k;
+    p.E = num_experts;
+    p.h = reinterpret_cast<uint16_t *>(wb + h_off);
+    p.z = reinterpret_cast<float *>(wb + z_off);
+    size_t smem;
+    // gate_up + SiLU*mul: x [T, D] -> h [P, I]; this stage publishes the grouping and reports bad ids
+    p.seg = gu_seg;
+    p.x = x;
+    p.group = reinterpret_cast<int32_t *>(wb);
+    p.dev_status = dev_status;
+    p.N = 2 * I;
+    p.K = D;
+    p.rows = T;
+    if (!moe_shape(T, D, P, &p.slots, &p.xpitch, &smem)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_moe_stage<1>(p, smem, s);
+    if (e != cudaSuccess) return e;
+    // down: h [P, I] -> z [P, D] fp32
+    p.seg = dn_seg;
+    p.x = p.h;
+    p.group = nullptr;
+    p.dev_status = nullptr;
+    p.N = D;
+    p.K = I;
+    p.rows = P;
+    if (!moe_shape(P, I, P, &p.slots, &p.xpitch, &smem)) return cudaErrorInvalidValue;
+    e = launch_moe_stage<2>(p, smem, s);
+    if (e != cudaSuccess) return e;
+    const int n4 = T * (D / 4);
+    return launch_pdl(sp::k_moe_combine, dim3((n4 + 255) / 256), dim3(256), 0, s, static_cast<const float *>(p.z),
+                      ids, route_w, y, T, D, top_k, num_experts);
 }
 
 cudaError_t read_step_error(unsigned *flags, bool clear)

@@ -37,7 +37,8 @@ PREP_SEGMENTED = 2
 
 EXPORTS = ("zq4_status_string", "zq4_last_cuda_error", "zq4_version", "zq4_device_errors", "zq4_gemv",
            "zq4_gate_up_silu", "zq4_moe_gemv", "zq4_prepare_weight", "zq4_dequant_f32",
-           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_stack_plan_set_wait_limit", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
+           "zq4_dequant_f16", "zq4_stack_plan_bytes", "zq4_stack_plan_waits", "zq4_stack_plan_init", "zq4_stack_run", "zq4_segmented_bytes", "zq4_stack_plan_init_static", "zq4_stack_plan_set_wait_limit", "zq4_moe_block",
+           "zq4_moe_block_work_bytes", "zq4_gemv_seg", "zq4_gate_up_silu_seg",
            "zq4_gemv_argmax", "zq4_gemv_affine", "zq4_gate_up_silu_affine", "zq4_moe_gemv_affine",
            "zq4_add_rmsnorm_work_bytes", "zq4_gemv_add_rmsnorm", "zq4_qkv_rope_append")
 
@@ -75,6 +76,7 @@ def _load():
         "zq4_dequant_f16": [P, P, P, I, I, P],
         "zq4_stack_plan_bytes": [P, I, I, P],
         "zq4_stack_plan_set_wait_limit": [P, ctypes.c_ulonglong],
+        "zq4_moe_block": [P, P, I, P, P, I, I, I, P, P, I, P, ctypes.c_size_t, P, P],
         "zq4_stack_plan_waits": [P, I, I, P, P],
         "zq4_gemv_affine": [P, P, P, P, P, I, I, I, P],
         "zq4_gate_up_silu_affine": [P, P, P, P, P, I, I, I, P],
@@ -292,6 +294,47 @@ def moe_gemv(wq_bank, scales_bank, num_experts, x, N, K, expert_ids, mode, route
         _ptr(route_w, "route_w", T * top_k * 4, 4), top_k, mode,
         _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
     return y
+
+
+def moe_block_work_bytes(T, top_k, D, I):
+    lib.zq4_moe_block_work_bytes.restype = ctypes.c_size_t
+    lib.zq4_moe_block_work_bytes.argtypes = [ctypes.c_int] * 4
+    return int(lib.zq4_moe_block_work_bytes(T, top_k, D, I))
+
+
+def moe_block(gu_seg, dn_seg, num_experts, x, D, I, expert_ids, route_w, y=None, work=None, dev_status=None,
+              stream=None):
+    """The MoE block in one call (zq4_moe_block): gate_up + SiLU*mul and
+    down + weighted combine, each touched expert read once per stage. The
+    banks in the segmented layout (prepare_weight(..., PREP_SEGMENTED) over
+    all of a bank's rows). Returns (y [T, D] f16, work); see include/zq4.h
+    for work's layout (the grouping, then h and z)."""
+    T, top_k = expert_ids.shape
+    E = num_experts
+    wb = moe_block_work_bytes(T, top_k, D, I)
+    if y is None:
+        y = torch.empty((T, D), dtype=torch.float16, device=x.device)
+    if work is None:
+        work = torch.zeros(wb, dtype=torch.uint8, device=x.device)
+    _check("zq4_moe_block", lib.zq4_moe_block(
+        _ptr(gu_seg, "gu_seg", E * segmented_bytes(2 * I, D)), _ptr(dn_seg, "dn_seg", E * segmented_bytes(D, I)),
+        E, _ptr(x, "x", T * D * 2, 2), _ptr(y, "y", T * D * 2, 2), T, D, I,
+        _ptr(expert_ids, "expert_ids", T * top_k * 4, 4), _ptr(route_w, "route_w", T * top_k * 4, 4), top_k,
+        _ptr(work, "work", wb), wb, _ptr(dev_status, "dev_status", 4, 4), _stream(stream)))
+    return y, work
+
+
+def moe_block_views(work, T, top_k, D, I):
+    """(grouping ints, h [T, top_k, I] f16, z [T, top_k, D] fp32) inside a
+    moe_block work buffer."""
+    P = T * top_k
+    g_ints = 3 * P + 3
+    h_off = (g_ints * 4 + 255) // 256 * 256
+    z_off = h_off + (P * I * 2 + 255) // 256 * 256
+    group = work[:g_ints * 4].view(torch.int32)
+    h = work[h_off:h_off + P * I * 2].view(torch.float16).view(T, top_k, I)
+    z = work[z_off:z_off + P * D * 4].view(torch.float32).view(T, top_k, D)
+    return group, h, z
 
 
 def moe_gemv_affine(wq_bank, scales_bank, biases_bank, num_experts, x, N, K, expert_ids, mode, route_w=None,
