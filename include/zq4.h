@@ -588,8 +588,11 @@ ZQ4_API zq4_status zq4_stack_plan_set_wait_limit(zq4_stack_plan *plan, unsigned 
  * Jobs and M as zq4_stack_plan_init. Limit: the job table must fit in the
  * array's first 64 KiB, i.e. at most 961 entries for a plan run by the one-
  * and two-token kernel (64-byte entries; a job split along K takes one per
- * part) and 1257 jobs for the other (48-byte entries); a longer list
- * returns ZQ4_ERR_UNSUPPORTED and changes nothing. The rest of the array
+ * part), 333 for the 3-to-16-token kernel (64-byte entries and a 128-byte
+ * tensor map each; a longer list of up to eight tokens runs on the
+ * eight-token kernel instead) and 1257 jobs for the eight-token kernel
+ * (48-byte entries); a longer list returns ZQ4_ERR_UNSUPPORTED and changes
+ * nothing. The rest of the array
  * (4 MiB and a little more) holds the split parts' sums. What must start at
  * zero (the plan's launch counter, abort flag and per-job and split-tile
  * counters) is cleared by every call. The first call on a device

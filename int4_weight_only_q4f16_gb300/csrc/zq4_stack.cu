@@ -1347,10 +1347,15 @@ zq4_status stack_plan_init_static(const zq4_stack_job *jobs, int n_jobs, int M, 
     int engine, mk, mt;
     zq4_status stt = plan_common(jobs, n_jobs, M, grid, g_static_order, g_static_dep, sc, &engine, &mk, &mt);
     if (stt != ZQ4_OK) return stt;
-    if (step_like(engine) && n_jobs > kStaticMaxJobsStep) return ZQ4_ERR_UNSUPPORTED;
-    if (image_bytes_for(engine, entries_for(engine, jobs, n_jobs, M, g_static_order)) > kStaticPlanBytes ||
-        plan_bytes_for(engine, jobs, n_jobs, M, g_static_order) > kStaticDevBytes)
-        return ZQ4_ERR_UNSUPPORTED;
+    auto fits = [&](int eng) {
+        return !(step_like(eng) && n_jobs > kStaticMaxJobsStep) &&
+               image_bytes_for(eng, entries_for(eng, jobs, n_jobs, M, g_static_order)) <= kStaticPlanBytes &&
+               plan_bytes_for(eng, jobs, n_jobs, M, g_static_order) <= kStaticDevBytes;
+    };
+    // a wide-kernel table (a tensor map per entry) too long for the array: k_stack, up to eight tokens
+    if (engine == kEngineWide && !fits(engine) && M <= st::kTokCols && stack_engine_fits(M, mk) == ZQ4_OK)
+        engine = kEngineStack;
+    if (!fits(engine)) return ZQ4_ERR_UNSUPPORTED;
     ImageInfo info;
     write_image(engine, jobs, n_jobs, M, g_static_order, g_static_dep, sc, grid, g_static_image, &info);
     if (!info.ok) return ZQ4_ERR_UNSUPPORTED;

@@ -387,7 +387,9 @@ __device__ __forceinline__ void fail(const Params &p, volatile int *s_abort)
     *s_abort = 1;
 }
 
-// The finisher and publisher warp of a CTA with nw compute warps.
+// The finisher and publisher warp of a CTA with nw compute warps (k_wide;
+// k_step keeps the same steps written out in its body: measured, the call
+// form cost the one-token step 15 us, 402.8 against 387.2).
 // Finisher (split jobs): takes the compute warps' posted part tiles (one per
 // warp at a time, lane w for warp w): a GPU-scope fence and an arrival on
 // the tile's counter each; the lane whose arrival completes a tile fences
@@ -678,8 +680,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_step(Params p)
                 if (xtag[c] >= 0 && !mbar_wait(sbase + L.xbar + 8 * c, uint32_t(xtag[c] & 1))) break;
     } else if (warp == kPubWarp) {
         // ---------------- the finisher and publisher ----------------
-        publisher_loop(p, sbase, sbase + L.posted, sbase + L.taken, sbase + L.posts, sbase + L.cta_done, cta_pub,
-                       cta_snap, s_warps_done, s_abort, kWarps, n, M, done_mul, lane, job);
+        // Finisher (split jobs): takes the compute warps' posted part tiles
+        // (one per warp at a time, lane w for warp w): a GPU-scope fence and
+        // an arrival on the tile's counter each; the lane whose arrival
+        // completes a tile fences (acquire), and the warp adds the parts and
+        // writes the tile. Each taken tile then counts for publishing.
+        // Publisher: makes this CTA's finished units of the waited-for jobs
+        // visible to every SM: snapshot the shared counters (acquire: the
+        // units were counted after their outputs were written), one
+        // GPU-scope fence for the whole batch, then one add per changed job.
+        if (p.n_pub > 0 || p.split) {
+            int taken_l = 0;                              // lane w < kWarps: posts of warp w taken
+            for (;;) {
+                const bool last = __shfl_sync(0xffffffffu, ld_acquire_cta_s32(s_warps_done) == kWarps || *s_abort, 0);
+                while (p.split) {
+                    int have = 0, e = 0, rt = 0, done = 0;
+                    if (lane < kWarps && ld_acquire_cta_s32(sbase + L.posted + 4 * lane) != taken_l) {
+                        const int2 pr = *reinterpret_cast<const int2 *>(smem + L.posts +
+                                                                         8 * (lane * kPosts + taken_l % kPosts));
+                        have = 1;
+                        e = pr.x;
+                        rt = pr.y;
+                        const StepJob &jb = job(e);
+                        fence_acq_rel_gpu_();
+                        const unsigned old = atomicAdd(&p.arrive[jb.sbase + rt], 1u);
+                        done = reached(old + 1u, done_mul * unsigned(((jb.flags >> kStepSplitShift) & 63) + 1));
+                        if (done) fence_acq_rel_gpu_();
+                    }
+                    if (!__any_sync(0xffffffffu, have)) break;
+                    __syncwarp();
+                    for (unsigned m = __ballot_sync(0xffffffffu, done); m; m &= m - 1) {
+                        const int w = __ffs(m) - 1;
+                        const int ew = __shfl_sync(0xffffffffu, e, w), rw = __shfl_sync(0xffffffffu, rt, w);
+                        complete_part(p, job(ew), rw, lane, M);
+                    }
+                    __syncwarp();                         // the rows written before the units count
+                    if (have) {
+                        const StepJob &jb = job(e);
+                        if (jb.flags & kStepPublish) red_release_cta(sbase + L.cta_done + 4 * (jb.flags >> kStepPubShift), 1u);
+                        st_release_cta_s32(sbase + L.taken + 4 * lane, ++taken_l);
+                    }
+                }
+                bool any = false;
+                for (int i = lane; i < p.n_pub; i += 32) {
+                    const unsigned c = unsigned(ld_acquire_cta_s32(sbase + L.cta_done + 4 * i));
+                    cta_snap[i] = c;
+                    any |= c != cta_pub[i];
+                }
+                __syncwarp();                             // the snapshot before the adds read it
+                if (__any_sync(0xffffffffu, any)) {
+                    fence_acq_rel_gpu_();
+                    for (int j = lane; j < n; j += 32) {
+                        const StepJob &jb = job(j);
+                        // every part counts into the job's slot; part 0's entry holds the counter
+                        if (!(jb.flags & kStepPublish) || (jb.flags & (63 << kStepPartShift))) continue;
+                        const int i = jb.flags >> kStepPubShift;
+                        const unsigned c = cta_snap[i];
+                        if (c != cta_pub[i]) {
+                            asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&p.job_done[j]),
+                                         "r"(c - cta_pub[i])
+                                         : "memory");
+                            cta_pub[i] = c;
+                        }
+                    }
+                }
+                if (last) break;
+                __nanosleep(p.split ? 128 : 500);
+            }
+        }
     } else {
         // ---------------- compute warps ----------------
         const int r = lane >> 2, t = lane & 3;

@@ -64,16 +64,25 @@ def _jobs(M, count):
     return [(seg, x, ys[i], N, K, gu) for i in range(count)]
 
 
-@pytest.mark.parametrize("M,limit", [(1, 961), (3, 1257)])
+@pytest.mark.parametrize("M,limit", [(1, 961), (3, 1257), (12, 333)])
 def test_static_plan_rejects_more_jobs_than_it_holds(M, limit):
     """The 64 KiB array holds 961 job entries of the one- and two-token
-    kernel (64 bytes each) and 1257 of the other (48 bytes each)."""
+    kernel (64 bytes each), 1257 of the eight-token kernel (48 bytes each;
+    three tokens: a list too long for the wide kernel's table runs there)
+    and 333 of the wide kernel (64 bytes and a 128-byte tensor map each)."""
     from int4_weight_only_q4f16_gb300 import zq4
     jobs = _jobs(M, limit + 1)
     with pytest.raises(zq4.Zq4Error, match="UNSUPPORTED"):
         zq4.StaticStackPlan(jobs, M)
     plan = zq4.StaticStackPlan(jobs[:limit], M)     # the documented limit fits
-    assert plan.plan.engine == (1 if M == 1 else 0)
+    assert plan.plan.engine == {1: 1, 3: 0, 12: 2}[M]
+
+
+def test_static_plan_wide_table_falls_back_to_the_eight_token_kernel():
+    from int4_weight_only_q4f16_gb300 import zq4
+    jobs = _jobs(3, 334)
+    assert zq4.StaticStackPlan(jobs[:333], 3).plan.engine == 2
+    assert zq4.StaticStackPlan(jobs, 3).plan.engine == 0
 
 
 def test_static_plan_allocates_no_device_memory():
