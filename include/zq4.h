@@ -198,9 +198,13 @@ ZQ4_API zq4_status zq4_moe_gemv_affine(const uint32_t *wq_bank, const uint16_t *
  *
  * D even (<= 512), H, H_kv, M, n_slots >= 1, K a multiple of 32, rope_base > 0. x
  * 16-byte aligned, outputs 2-byte, pos / slot / dev_status 4-byte aligned;
- * outputs must not overlap each other or the inputs. One launch per block
- * of up to 8 tokens. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
- * ZQ4_ERR_OVERLAP, ZQ4_ERR_UNSUPPORTED (sizes), ZQ4_ERR_CUDA.
+ * outputs must not overlap each other or the inputs. D % 16 == 0 and K %
+ * 256 == 0: the tensor-core decode kernel (a 16-row tile holds pair rows
+ * i..i+7 of both halves of one head, read through a 4-D tensor map; one
+ * launch per block of up to 16 tokens; base^(-2i/D) computed on the host
+ * in fp64); else the CUDA-core kernel (blocks of up to 8 tokens). Errors:
+ * ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED (sizes), ZQ4_ERR_CUDA.
  */
 ZQ4_API zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, int M, int K,
                                        int H, int H_kv, int D, double rope_base, const int32_t *pos,

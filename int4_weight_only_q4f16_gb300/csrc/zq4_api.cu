@@ -180,6 +180,8 @@ zq4_status zq4_qkv_rope_append(const uint32_t *wq, const uint16_t *scales, const
     a.Hkv = H_kv;
     a.D = D;
     a.n_slots = n_slots;
+    if (decode_tc_rope_supported(M, K, D))   // the tensor-core kernel, a RoPE pair in one tile (D % 16 == 0)
+        return cuda_status(launch_decode_tc_rope(a, static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_qkv_rope(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -37,6 +37,7 @@
 
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
+#include "zq4_rope.cuh"
 
 namespace zq4 {
 
@@ -357,10 +358,8 @@ __global__ void __launch_bounds__(kThreads) k_dense_rms(RmsArgs a)
 // thousand per call). Q goes to q_out, rotated K and plain V to the cache
 // rows of the token's slot; a slot outside [0, n_slots) writes nothing and
 // sets ZQ4_DEV_BAD_SLOT.
-// Angles: base^(-2i/D) once per CTA in fp64 (shared memory); per value the
-// fp64 angle pos * f_i is reduced modulo 2 pi (Cody-Waite, 2 pi split into a
-// double and its remainder), and the reduced angle, in [-pi, pi], goes to
-// fp32 sincosf: ~1e-7 rad, far inside the bound the rotation carries.
+// Angles: base^(-2i/D) once per CTA in fp64 (shared memory); the rotation
+// itself is rope_rotate (zq4_rope.cuh).
 // ---------------------------------------------------------------------------
 constexpr int kMaxRopeHalf = 256;                 // D <= 512
 template <int MT, int LPR>
@@ -406,16 +405,7 @@ __global__ void __launch_bounds__(kThreads) k_qkv_rope(QkvArgs a)
         for (int m = 0; m < MT; ++m) {
             if (m >= a.M) continue;
             float oa = part[0][m], ob = part[1][m];
-            if (rot) {
-                const double kTwoPiHi = 6.283185307179586, kTwoPiLo = 2.4492935982947064e-16;
-                const double th = double(s_pos[m]) * inv_freq;
-                const double k = rint(th * (1.0 / kTwoPiHi));
-                const float r = float(fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, th)));
-                float sn, cs;
-                sincosf(r, &sn, &cs);
-                oa = part[0][m] * cs - part[1][m] * sn;
-                ob = part[0][m] * sn + part[1][m] * cs;
-            }
+            if (rot) rope_rotate(s_pos[m], inv_freq, part[0][m], part[1][m], &oa, &ob);
             uint16_t *dst;
             if (hb < a.H) {
                 dst = a.q_out + size_t(m) * a.H * a.D + size_t(hb) * a.D;

@@ -46,18 +46,39 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cmath>
+#include <type_traits>
 #include <cstring>
 #include <atomic>
 
 #include "zq4_async.cuh"
 #include "zq4_common.cuh"
 #include "zq4_internal.h"
+#include "zq4_rope.cuh"
 
 namespace zq4 {
 
 __device__ unsigned g_device_error = 0;
 
 namespace tc {
+
+// 4D tensor-map TMA load / L2 prefetch of one box at (c0, c1, c2, c3)
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
 
 // Tile parameters (compile-time; the defaults are the tuned values).
 #ifndef ZQ4_TC_WARPS
@@ -148,10 +169,18 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int n)
     return (static_cast<unsigned long long>(ord) << 32) | static_cast<unsigned>(~unsigned(n));
 }
 
+// The QKV + RoPE mode's arguments: TcArgs and base^(-2i/D) for i < D/2, in
+// fp64, computed on the host (the kernel reads them from parameter space).
+struct TcRopeArgs : TcArgs {
+    double freq[256];
+};
+template <int RU>
+using TcArgsFor = typename std::conditional<RU == 5, TcRopeArgs, TcArgs>::type;
+
 template <int NB, int RU>
 __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ CUtensorMap tm_codes,
                                                         const __grid_constant__ CUtensorMap tm_scales,
-                                                        TcArgs a)
+                                                        const __grid_constant__ TcArgsFor<RU> a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -168,6 +197,8 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     __shared__ float s_sq[RU == 4 ? 16 : 1][16];
     __shared__ float s_ss[RU == 4 ? 16 : 1];
     if (RU == 4 && threadIdx.x < 16) s_ss[threadIdx.x] = 0.f;
+    // QKV + RoPE epilogue: the tokens' positions and slots
+    __shared__ int s_pos[RU == 5 ? 16 : 1], s_slot[RU == 5 ? 16 : 1];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -182,10 +213,17 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
         // ---------------- producer warp ----------------
         // Stage j of this CTA is chunk j % chunks of tile blockIdx + (j / chunks) * grid.
         const int nstage = ((a.tiles - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x)) * chunks;
+        const int tpp = RU == 5 ? a.D >> 4 : 1;          // RoPE: tiles per head
         auto prefetch_stage = [&](int j) {
             if (j >= nstage) return;
             const int tile = blockIdx.x + (j / chunks) * gridDim.x, k0 = (j % chunks) * kKC;
             const int nseg = min(kKC, K - k0) / 256;
+            if (RU == 5) {
+                const int hb = tile / tpp, i0 = (tile - hb * tpp) * 8;
+                for (int g = 0; g < nseg; ++g) tma_prefetch_4d(&tm_codes, (k0 >> 3) + 32 * g, i0, 0, hb);
+                tma_prefetch_4d(&tm_scales, k0 >> 5, i0, 0, hb);
+                return;
+            }
             for (int g = 0; g < nseg; ++g) tma_prefetch_2d(&tm_codes, (k0 >> 3) + 32 * g, tile * 16);
             tma_prefetch_2d(&tm_scales, k0 >> 5, tile * 16);
         };
@@ -212,9 +250,16 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     const int k0 = c * kKC, nseg = min(kKC, K - k0) / 256;
                     const uint32_t full = full0 + 8 * s, st = ring + s * kStageBytes;
                     mbar_arrive_expect_tx(full, uint32_t(nseg * kSegBytes + kScaleBytes));
-                    for (int g = 0; g < nseg; ++g)
-                        tma_load_2d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, tile * 16, full);
-                    tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                    if (RU == 5) {
+                        const int hb = tile / tpp, i0 = (tile - hb * tpp) * 8;
+                        for (int g = 0; g < nseg; ++g)
+                            tma_load_4d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, i0, 0, hb, full);
+                        tma_load_4d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, i0, 0, hb, full);
+                    } else {
+                        for (int g = 0; g < nseg; ++g)
+                            tma_load_2d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, tile * 16, full);
+                        tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                    }
                     if (it >= kStages) prefetch_stage(it + kPrefetch);   // keep the window moving
                 }
                 __syncwarp();
@@ -233,6 +278,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
 
     // ---------------- compute warps ----------------
     griddep_wait();
+    if (RU == 5 && threadIdx.x < a.M) {                  // positions and slots of the launch's tokens
+        s_pos[threadIdx.x] = a.pos[threadIdx.x];
+        s_slot[threadIdx.x] = a.slot[threadIdx.x];
+    }
     const uint32_t xrow = uint32_t(xs_row_bytes(K));
     {
         // Stage x[0..M): the 8 values of word chunk cw of token m are stored
@@ -431,6 +480,38 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 }
                 if (i == 0 && o < 16 * a.M) atomicMax(a.amax + m, key);
             }
+        } else if (RU == 5) {
+            // QKV + RoPE + KV append: tile row i < 8 is pair index i0 + i of head
+            // hb (first half), row i + 8 its partner i0 + i + D/2; Q and K heads
+            // rotated, Q to q_out, K and V to the cache rows of the token's slot
+            const int tpp = a.D >> 4, hb = tile / tpp, i0 = (tile - hb * tpp) * 8, half = a.D >> 1;
+            const bool rot = hb < a.H + a.Hkv;
+            for (int o = threadIdx.x; o < 8 * a.M; o += kWarps * 32) {
+                const int m = o >> 3, i = o & 7;
+                float va = 0.f, vb = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    va += red[((w * NB + (m >> 3)) * 16 + i) * 8 + (m & 7)];
+                    vb += red[((w * NB + (m >> 3)) * 16 + i + 8) * 8 + (m & 7)];
+                }
+                float oa = va, ob = vb;
+                if constexpr (RU == 5)
+                    if (rot) rope_rotate(s_pos[m], a.freq[i0 + i], va, vb, &oa, &ob);
+                uint16_t *dst;
+                if (hb < a.H) {
+                    dst = a.q_out + size_t(m) * a.H * a.D + size_t(hb) * a.D;
+                } else {
+                    const int sl = s_slot[m];
+                    if (sl < 0 || sl >= a.n_slots) {
+                        if (a.dev_status) atomicOr(reinterpret_cast<unsigned *>(a.dev_status), ZQ4_DEV_BAD_SLOT);
+                        continue;
+                    }
+                    dst = (rot ? a.k_cache : a.v_cache) + size_t(sl) * a.Hkv * a.D +
+                          size_t(rot ? hb - a.H : hb - a.H - a.Hkv) * a.D;
+                }
+                dst[i0 + i] = float_to_f16_bits(oa);
+                dst[i0 + i + half] = float_to_f16_bits(ob);
+            }
         } else if (RU == 4) {
             // r = resid + x W^T: the new residual (f16 and fp32), and the
             // CTA's running sum of r^2 per token (rows in order, tiles in order)
@@ -619,7 +700,7 @@ cudaError_t make_maps(const uint32_t *wq, const uint16_t *scales, int N, int K, 
 }
 
 template <int NB, int RU>
-cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgs &a, cudaStream_t s)
+cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgsFor<RU> &a, cudaStream_t s)
 {
     static int smem_set[kMaxDevices] = {};
     auto kern = k_decode_tc<NB, RU>;
@@ -741,6 +822,71 @@ cudaError_t launch_decode_tc_addnorm(const uint32_t *wq, const uint16_t *scales,
         a.r32 = r32 + o;
         a.M = mt;
         e = nb == 2 ? tc::launch_t<2, 4>(mc, ms, a, s) : tc::launch_t<1, 4>(mc, ms, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
+}
+
+bool decode_tc_rope_supported(int M, int K, int D)
+{
+    return decode_tc_supported(std::min(M, 16), K) && D > 0 && D % 16 == 0 && D / 2 <= 256;
+}
+
+cudaError_t launch_decode_tc_rope(const QkvArgs &q, cudaStream_t s)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tc::encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int K = q.K, D = q.D, heads = q.H + 2 * q.Hkv;
+    // W viewed as [heads][2 halves][D/2 rows][K]: one box = pair rows i0..i0+7 of both halves
+    CUtensorMap mc, ms;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    {
+        const cuuint64_t dim[4] = {cuuint64_t(K / 8), cuuint64_t(D / 2), 2, cuuint64_t(heads)};
+        const cuuint64_t stride[3] = {cuuint64_t(K / 2), cuuint64_t(D / 2) * (K / 2), cuuint64_t(D) * (K / 2)};
+        const cuuint32_t box[4] = {32, 8, 2, 1};
+        if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<uint32_t *>(q.wq), dim, stride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dim[4] = {cuuint64_t(K / 32), cuuint64_t(D / 2), 2, cuuint64_t(heads)};
+        const cuuint64_t stride[3] = {cuuint64_t(K / 16), cuuint64_t(D / 2) * (K / 16), cuuint64_t(D) * (K / 16)};
+        const cuuint32_t box[4] = {cuuint32_t(tc::kScaleCols), 8, 2, 1};
+        if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<uint16_t *>(q.scales), dim, stride, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    tc::TcRopeArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int i = 0; i < D / 2; ++i) a.freq[i] = std::pow(q.base, -2.0 * double(i) / double(D));
+    a.wq = q.wq;
+    a.scales = q.scales;
+    a.N = heads * D;
+    a.K = K;
+    a.tiles = heads * (D / 16);
+    a.k_cache = q.k_cache;
+    a.v_cache = q.v_cache;
+    a.dev_status = q.dev_status;
+    a.base = q.base;
+    a.H = q.H;
+    a.Hkv = q.Hkv;
+    a.D = D;
+    a.n_slots = q.n_slots;
+    const bool fit16 = tc::smem_bytes<2>(16, K) <= 220 * 1024;
+    cudaError_t e = cudaSuccess;
+    for (int m0 = 0; m0 < q.M;) {
+        const int rem = q.M - m0;
+        const int nb = (rem > 8 && fit16) ? 2 : 1;
+        const int mt = std::min(rem, 8 * nb);
+        a.x = q.x + size_t(m0) * K;
+        a.pos = q.pos + m0;
+        a.slot = q.slot + m0;
+        a.q_out = q.q_out + size_t(m0) * q.H * D;
+        a.M = mt;
+        e = nb == 2 ? tc::launch_t<2, 5>(mc, ms, a, s) : tc::launch_t<1, 5>(mc, ms, a, s);
         if (e != cudaSuccess) return e;
         m0 += mt;
     }

@@ -91,6 +91,13 @@ struct TcArgs {
     float *part;                    // [CTAs][16] each CTA's sum of r^2 per token
     unsigned *counter;              // CTAs done (zero on entry, left zero)
     float eps;
+    // QKV + RoPE + KV append epilogue: the maps view W as [heads][2][D/2][K]
+    // (a tile = pair rows i0..i0+7 of both halves of one head)
+    const int32_t *pos, *slot;      // [M]
+    uint16_t *q_out, *k_cache, *v_cache;
+    int32_t *dev_status;
+    double base;
+    int H, Hkv, D, n_slots;
 };
 
 size_t smem_per_sm();      // shared memory per SM of the current device (cached)
@@ -116,6 +123,9 @@ size_t moe_block_work_layout(int T, int top_k, int D, int I, size_t *h_off, size
 cudaError_t launch_moe_block(const uint8_t *gu_seg, const uint8_t *dn_seg, int num_experts, const uint16_t *x,
                              uint16_t *y, int T, int D, int I, const int32_t *ids, const float *route_w, int top_k,
                              void *work, int32_t *dev_status, cudaStream_t s);
+// QKV + RoPE + KV append on the tensor-core kernel (zq4_qkv_rope_append)
+bool decode_tc_rope_supported(int M, int K, int D);
+cudaError_t launch_decode_tc_rope(const QkvArgs &q, cudaStream_t s);
 cudaError_t launch_decode_tc_argmax(const uint32_t *wq, const uint16_t *scales, const uint16_t *x, float *y32,
                                     int32_t *idx, float *maxval, unsigned long long *work, int M, int N, int K,
                                     cudaStream_t s);

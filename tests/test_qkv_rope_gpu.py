@@ -22,7 +22,7 @@ def _case(H, Hkv, D, K, M, seed):
 
 
 @pytest.mark.parametrize("H,Hkv,D,K,M", [(32, 32, 96, 3072, 1), (8, 2, 64, 512, 3), (2, 1, 8, 64, 9),
-                                         (4, 4, 128, 2560, 2)])
+                                         (4, 4, 128, 2560, 2), (8, 2, 64, 1024, 16), (4, 2, 96, 768, 17)])
 def test_qkv_rope_append_matches_oracle(oracle, H, Hkv, D, K, M):
     from int4_weight_only_q4f16_gb300 import zq4
     rng, wq, sc, x = _case(H, Hkv, D, K, M, 0)
@@ -44,9 +44,10 @@ def test_qkv_rope_append_matches_oracle(oracle, H, Hkv, D, K, M):
     assert int(status.item()) == 0
 
 
-def test_qkv_rope_bad_slot_is_reported_and_skipped(oracle):
+@pytest.mark.parametrize("D,K", [(16, 128), (32, 256)])      # CUDA-core and tensor-core kernels
+def test_qkv_rope_bad_slot_is_reported_and_skipped(oracle, D, K):
     from int4_weight_only_q4f16_gb300 import zq4
-    H, Hkv, D, K, M = 4, 2, 16, 128, 3
+    H, Hkv, M = 4, 2, 3
     rng, wq, sc, x = _case(H, Hkv, D, K, M, 1)
     n_slots = 4
     pos = np.array([1, 2, 3], np.int32)
