@@ -121,9 +121,9 @@ constexpr int kGpw = (kKC / 32 + kWarps - 1) / kWarps;   // groups of a stage pe
 constexpr uint32_t kSevenEighths = 0x3B003B00u;   // f16x2 (7/8, 7/8)
 constexpr int kUnpack = ZQ4_TC_UNPACK;
 constexpr int kPrefetch = ZQ4_TC_PREFETCH;
-constexpr int kPartLoads = 16;
+constexpr int kPartLoads = 16;                    // add + RMSNorm: at most 32 x 16 CTAs per launch
 __device__ __forceinline__ float lo_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w)); }
-__device__ __forceinline__ float hi_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w >> 16)); }                    // add + RMSNorm: at most 32 x 16 CTAs per launch
+__device__ __forceinline__ float hi_f32(uint32_t w) { return f16_bits_to_float(uint16_t(w >> 16)); }
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1 KB swizzle alignment");
 
@@ -174,13 +174,35 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int n)
 struct TcRopeArgs : TcArgs {
     double freq[256];
 };
-template <int RU>
-using TcArgsFor = typename std::conditional<RU == 5, TcRopeArgs, TcArgs>::type;
+// The MLX affine format's arguments: TcArgs and the biases' tensor map (the
+// scales' map then holds one scale per 64 weights too).
+struct TcAffArgs : TcArgs {
+    CUtensorMap tm_bias;
+};
+template <int RU, bool AFF>
+using TcArgsFor = typename std::conditional<AFF, TcAffArgs,
+                                            typename std::conditional<RU == 5, TcRopeArgs, TcArgs>::type>::type;
 
-template <int NB, int RU>
+// Affine unpack: four f16x2 values holding q exactly (no zero point), the
+// element pairs of unpack_word_f16x2 (magic-number OR, then the bias removed).
+__device__ __forceinline__ void unpack_word_q_f16x2(uint32_t w, uint32_t p[4])
+{
+    const uint32_t kMagic = 0x64006400u;       // (1024, 1024)
+    const uint32_t kSixteenth = 0x2C002C00u;   // (1/16, 1/16)
+    const uint32_t kNeg64 = 0xD400D400u;       // (-64, -64): 1024/16
+    uint32_t w8 = w >> 8;
+    p[0] = hsub2(and_or<0x000F000Fu>(w, kMagic), kMagic);
+    p[1] = hfma2(and_or<0x00F000F0u>(w, kMagic), kSixteenth, kNeg64);
+    p[2] = hsub2(and_or<0x000F000Fu>(w8, kMagic), kMagic);
+    p[3] = hfma2(and_or<0x00F000F0u>(w8, kMagic), kSixteenth, kNeg64);
+}
+// affine: per-warp bias scratch and the x sums of every 32-column group ([K/32][16] floats)
+__host__ __device__ inline size_t aff_bytes(int K) { return scale_bytes() + size_t(K / 32) * 16 * 4; }
+
+template <int NB, int RU, bool AFF = false>
 __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ CUtensorMap tm_codes,
                                                         const __grid_constant__ CUtensorMap tm_scales,
-                                                        const __grid_constant__ TcArgsFor<RU> a)
+                                                        const __grid_constant__ TcArgsFor<RU, AFF> a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -192,6 +214,9 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     const int K = a.K, N = a.N;
     float *zp = reinterpret_cast<float *>(smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes());
     uint8_t *xs = smem + kRingBytes + kMbarBytes + red_bytes<NB>() + scale_bytes() + zp_bytes<NB>(K);
+    // affine: per-warp bias scratch (as sscr) and the x sums of the 32-column groups, after x
+    float2 *sbias = reinterpret_cast<float2 *>(xs + size_t(a.M) * xs_row_bytes(K));
+    float *xsum = reinterpret_cast<float *>(xs + size_t(a.M) * xs_row_bytes(K) + scale_bytes());
     const int chunks = (K + kKC - 1) / kKC;
     // add + RMSNorm epilogue: squares of a tile's rows, the CTA's running sums per token
     __shared__ float s_sq[RU == 4 ? 16 : 1][16];
@@ -225,7 +250,12 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 return;
             }
             for (int g = 0; g < nseg; ++g) tma_prefetch_2d(&tm_codes, (k0 >> 3) + 32 * g, tile * 16);
-            tma_prefetch_2d(&tm_scales, k0 >> 5, tile * 16);
+            if (AFF) {
+                tma_prefetch_2d(&tm_scales, k0 >> 6, tile * 16);
+                if constexpr (AFF) tma_prefetch_2d(&a.tm_bias, k0 >> 6, tile * 16);
+            } else {
+                tma_prefetch_2d(&tm_scales, k0 >> 5, tile * 16);
+            }
         };
         // L2 look-ahead: the stages after the ring's first fill are requested
         // from DRAM now (before the grid-dependency wait), so ring refills
@@ -258,7 +288,13 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     } else {
                         for (int g = 0; g < nseg; ++g)
                             tma_load_2d(st + g * kSegBytes, &tm_codes, (k0 >> 3) + 32 * g, tile * 16, full);
-                        tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                        if (AFF) {                        // scales, then biases: one per 64 columns, 512 B each
+                            tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 6, tile * 16, full);
+                            if constexpr (AFF)
+                                tma_load_2d(st + kSegs * kSegBytes + kScaleBytes / 2, &a.tm_bias, k0 >> 6, tile * 16, full);
+                        } else {
+                            tma_load_2d(st + kSegs * kSegBytes, &tm_scales, k0 >> 5, tile * 16, full);
+                        }
                     }
                     if (it >= kStages) prefetch_stage(it + kPrefetch);   // keep the window moving
                 }
@@ -323,6 +359,29 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
         }
     }
     named_barrier_compute();
+    if (AFF) {
+        // the x sums of every 32-column group and token (tokens past M: 0), fp32, from the
+        // staged x (a group's 32 values, in the staging's pair order); groups spread over the threads
+        const int G = K >> 5;
+        for (int i = threadIdx.x; i < a.M * G; i += kWarps * 32) {
+            const int m = i / G, g = i - m * G;
+            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + size_t(m) * xrow + size_t(g) * 64);
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = xp[q];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) sum += lo_f32(w[h]) + hi_f32(w[h]);
+            }
+            xsum[size_t(g) * 16 + m] = sum;
+        }
+        for (int i = threadIdx.x; i < (16 - a.M) * G; i += kWarps * 32) {
+            const int m = a.M + i / G, g = i % G;
+            xsum[size_t(g) * 16 + m] = 0.f;
+        }
+        named_barrier_compute();
+    }
     griddep_launch_dependents();
     const int r = lane >> 2, t = lane & 3;
     {
@@ -381,12 +440,25 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 const uint8_t *st = smem + s * kStageBytes;
                 // this warp's scales of the stage, as fp32 pairs 8*(s[r], s[r+8])
                 const uint16_t *scl = reinterpret_cast<const uint16_t *>(st + kSegs * kSegBytes);
-                for (int i = lane; i < ng * 8; i += 32) {
-                    const int gi = i >> 3, rp = i & 7;
-                    const float s0 = f16_bits_to_float(scl[rp * kScaleCols + g_lo + gi]);
-                    const float s1 = f16_bits_to_float(scl[(rp + 8) * kScaleCols + g_lo + gi]);
-                    const float f = kUnpack == 0 ? 1.f : 8.f;
-                    sp[gi * 8 + rp] = make_float2(f * s0, f * s1);
+                if (AFF) {
+                    // a scale and a bias per 64 columns: rows of kScaleCols / 2
+                    const uint16_t *bia = scl + 16 * (kScaleCols / 2);
+                    for (int i = lane; i < ng * 8; i += 32) {
+                        const int gi = i >> 3, rp = i & 7, col = (g_lo + gi) >> 1;
+                        sp[gi * 8 + rp] = make_float2(f16_bits_to_float(scl[rp * (kScaleCols / 2) + col]),
+                                                      f16_bits_to_float(scl[(rp + 8) * (kScaleCols / 2) + col]));
+                        sbias[warp * kGpw * 8 + gi * 8 + rp] =
+                            make_float2(f16_bits_to_float(bia[rp * (kScaleCols / 2) + col]),
+                                        f16_bits_to_float(bia[(rp + 8) * (kScaleCols / 2) + col]));
+                    }
+                } else {
+                    for (int i = lane; i < ng * 8; i += 32) {
+                        const int gi = i >> 3, rp = i & 7;
+                        const float s0 = f16_bits_to_float(scl[rp * kScaleCols + g_lo + gi]);
+                        const float s1 = f16_bits_to_float(scl[(rp + 8) * kScaleCols + g_lo + gi]);
+                        const float f = kUnpack == 0 ? 1.f : 8.f;
+                        sp[gi * 8 + rp] = make_float2(f * s0, f * s1);
+                    }
                 }
                 __syncwarp();
                 const int kg0 = (k0 >> 5) + g_lo;           // global index of the warp's first group
@@ -401,7 +473,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p + 8 * 128);
                     const float2 sc = sp[gi * 8 + r];
                     uint32_t pa[4], pb[4];
-                    if (kUnpack == 0) {
+                    if (AFF) {
+                        unpack_word_q_f16x2(w0, pa);
+                        unpack_word_q_f16x2(w1, pb);
+                    } else if (kUnpack == 0) {
                         unpack_word_f16x2(w0, pa);
                         unpack_word_f16x2(w1, pb);
                     } else {
@@ -428,10 +503,20 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                             e[0] = e[2] = ev.x;
                             e[1] = e[3] = ev.y;
                         }
-                        acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
-                        acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
-                        acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
-                        acc[nb][3] = fmaf(sc.y, d[3] - e[3], acc[nb][3]);
+                        if (AFF) {
+                            // s sum(x q) + b sum(x) over the group's 32 columns
+                            const float2 bv = sbias[warp * kGpw * 8 + gi * 8 + r];
+                            const float2 xs2 = *reinterpret_cast<const float2 *>(xsum + size_t(kg0 + gi) * 16 + 8 * nb + 2 * t);
+                            acc[nb][0] = fmaf(bv.x, xs2.x, fmaf(sc.x, d[0], acc[nb][0]));
+                            acc[nb][1] = fmaf(bv.x, xs2.y, fmaf(sc.x, d[1], acc[nb][1]));
+                            acc[nb][2] = fmaf(bv.y, xs2.x, fmaf(sc.y, d[2], acc[nb][2]));
+                            acc[nb][3] = fmaf(bv.y, xs2.y, fmaf(sc.y, d[3], acc[nb][3]));
+                        } else {
+                            acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
+                            acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
+                            acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
+                            acc[nb][3] = fmaf(sc.y, d[3] - e[3], acc[nb][3]);
+                        }
                     }
                 }
             }
@@ -699,12 +784,12 @@ cudaError_t make_maps(const uint32_t *wq, const uint16_t *scales, int N, int K, 
     return cudaSuccess;
 }
 
-template <int NB, int RU>
-cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgsFor<RU> &a, cudaStream_t s)
+template <int NB, int RU, bool AFF = false>
+cudaError_t launch_t(const CUtensorMap &mc, const CUtensorMap &ms, const TcArgsFor<RU, AFF> &a, cudaStream_t s)
 {
     static int smem_set[kMaxDevices] = {};
-    auto kern = k_decode_tc<NB, RU>;
-    const size_t smem = smem_bytes<NB>(a.M, a.K);
+    auto kern = k_decode_tc<NB, RU, AFF>;
+    const size_t smem = smem_bytes<NB>(a.M, a.K) + (AFF ? aff_bytes(a.K) : 0);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
     // CTAs per SM by shared memory (1 KB per CTA is reserved), at most ZQ4_TC_OCC.
@@ -822,6 +907,58 @@ cudaError_t launch_decode_tc_addnorm(const uint32_t *wq, const uint16_t *scales,
         a.r32 = r32 + o;
         a.M = mt;
         e = nb == 2 ? tc::launch_t<2, 4>(mc, ms, a, s) : tc::launch_t<1, 4>(mc, ms, a, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
+}
+
+bool decode_tc_affine_supported(int M, int K)
+{
+    // scale rows of K/64 f16 must be 16-byte multiples for their tensor maps
+    return K % 512 == 0 && decode_tc_supported(std::min(M, 16), K) &&
+           tc::smem_bytes<2>(std::min(M, 16), K) + tc::aff_bytes(K) <= 220 * 1024;
+}
+
+cudaError_t launch_decode_tc_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                    const uint16_t *x, uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tc::encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap mc, ms;
+    cudaError_t e = tc::make_maps(wq, scales, N, K, &mc, &ms);    // codes (the scales map is replaced)
+    if (e != cudaSuccess) return e;
+    tc::TcAffArgs a;
+    memset(&a, 0, sizeof(a));
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dim[2] = {cuuint64_t(K / 64), cuuint64_t(N)};
+    const cuuint64_t stride[1] = {cuuint64_t(K / 32)};
+    const cuuint32_t box[2] = {cuuint32_t(tc::kScaleCols / 2), 16};
+    if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(scales), dim, stride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&a.tm_bias, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(biases), dim, stride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int out_cols = gate_up ? N / 2 : N;
+    a.wq = wq;
+    a.scales = scales;
+    a.N = N;
+    a.K = K;
+    a.tiles = (N + 15) / 16;
+    a.y_stride = out_cols;
+    for (int m0 = 0; m0 < M;) {
+        const int rem = M - m0;
+        const int nb = rem > 8 ? 2 : 1;
+        const int mt = std::min(rem, 8 * nb);
+        a.x = x + size_t(m0) * K;
+        a.y = y + size_t(m0) * out_cols;
+        a.M = mt;
+        if (nb == 2)
+            e = gate_up ? tc::launch_t<2, 2, true>(mc, ms, a, s) : tc::launch_t<2, 1, true>(mc, ms, a, s);
+        else
+            e = gate_up ? tc::launch_t<1, 2, true>(mc, ms, a, s) : tc::launch_t<1, 1, true>(mc, ms, a, s);
         if (e != cudaSuccess) return e;
         m0 += mt;
     }

@@ -123,6 +123,10 @@ size_t moe_block_work_layout(int T, int top_k, int D, int I, size_t *h_off, size
 cudaError_t launch_moe_block(const uint8_t *gu_seg, const uint8_t *dn_seg, int num_experts, const uint16_t *x,
                              uint16_t *y, int T, int D, int I, const int32_t *ids, const float *route_w, int top_k,
                              void *work, int32_t *dev_status, cudaStream_t s);
+// The MLX affine format on the tensor-core kernel (zq4_gemv_affine / _gate_up_silu_affine)
+bool decode_tc_affine_supported(int M, int K);
+cudaError_t launch_decode_tc_affine(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
+                                    const uint16_t *x, uint16_t *y, int M, int N, int K, bool gate_up, cudaStream_t s);
 // QKV + RoPE + KV append on the tensor-core kernel (zq4_qkv_rope_append)
 bool decode_tc_rope_supported(int M, int K, int D);
 cudaError_t launch_decode_tc_rope(const QkvArgs &q, cudaStream_t s);

@@ -23,7 +23,7 @@ def _affine_weight(tag, N, K, i=0):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 3072, 2560), (3, 333, 192), (8, 1000, 9728), (16, 256, 640),
-                                   (5, 64, 64), (1, 2560, 9728)])
+                                   (5, 64, 64), (1, 2560, 9728), (16, 1000, 1536), (13, 77, 3072)])
 def test_affine_gemv_matches_oracle(oracle, M, N, K):
     from int4_weight_only_q4f16_gb300 import zq4
     wq, sc, bi = _affine_weight("aff_gemv", N, K)
