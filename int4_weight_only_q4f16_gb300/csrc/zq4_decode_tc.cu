@@ -196,8 +196,8 @@ __device__ __forceinline__ void unpack_word_q_f16x2(uint32_t w, uint32_t p[4])
     p[2] = hsub2(and_or<0x000F000Fu>(w8, kMagic), kMagic);
     p[3] = hfma2(and_or<0x00F000F0u>(w8, kMagic), kSixteenth, kNeg64);
 }
-// affine: per-warp bias scratch and the x sums of every 32-column group ([K/32][16] floats)
-__host__ __device__ inline size_t aff_bytes(int K) { return scale_bytes() + size_t(K / 32) * 16 * 4; }
+// affine: per-warp bias scratch and the x sums of every 64-column group ([K/64][16] floats)
+__host__ __device__ inline size_t aff_bytes(int K) { return scale_bytes() + size_t(K / 64) * 16 * 4; }
 
 template <int NB, int RU, bool AFF = false>
 __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ CUtensorMap tm_codes,
@@ -360,15 +360,16 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
     }
     named_barrier_compute();
     if (AFF) {
-        // the x sums of every 32-column group and token (tokens past M: 0), fp32, from the
-        // staged x (a group's 32 values, in the staging's pair order); groups spread over the threads
-        const int G = K >> 5;
+        // the x sums of every 64-column group (one scale and bias) and token (tokens past
+        // M: 0), fp32, from the staged x (a 32-column chunk's values are 64 consecutive
+        // bytes in the staging's pair order); groups spread over the threads
+        const int G = K >> 6;
         for (int i = threadIdx.x; i < a.M * G; i += kWarps * 32) {
             const int m = i / G, g = i - m * G;
-            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + size_t(m) * xrow + size_t(g) * 64);
+            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + size_t(m) * xrow + size_t(g) * 128);
             float sum = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 const uint4 v = xp[q];
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -441,10 +442,11 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 // this warp's scales of the stage, as fp32 pairs 8*(s[r], s[r+8])
                 const uint16_t *scl = reinterpret_cast<const uint16_t *>(st + kSegs * kSegBytes);
                 if (AFF) {
-                    // a scale and a bias per 64 columns: rows of kScaleCols / 2
+                    // a scale and a bias per 64 columns (a pair of 32-column chunks; the
+                    // warp's share starts on a pair and holds whole pairs): rows of kScaleCols / 2
                     const uint16_t *bia = scl + 16 * (kScaleCols / 2);
-                    for (int i = lane; i < ng * 8; i += 32) {
-                        const int gi = i >> 3, rp = i & 7, col = (g_lo + gi) >> 1;
+                    for (int i = lane; i < (ng >> 1) * 8; i += 32) {
+                        const int gi = i >> 3, rp = i & 7, col = (g_lo >> 1) + gi;
                         sp[gi * 8 + rp] = make_float2(f16_bits_to_float(scl[rp * (kScaleCols / 2) + col]),
                                                       f16_bits_to_float(scl[(rp + 8) * (kScaleCols / 2) + col]));
                         sbias[warp * kGpw * 8 + gi * 8 + rp] =
@@ -465,6 +467,55 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                 const uint8_t *xg = xs + size_t(kg0) * 64 + 16 * t;
                 const float *zg = zp + size_t(kg0) * NB * 8 + 2 * t;
                 const uint8_t *rowr = st + r * 128 + 4 * t;  // row r; row r+8 is 1 KB further
+                if constexpr (AFF) {
+                    // one 64-column group per trip: the MMA chain sums both chunks' x.q, then
+                    // s * sum(x q) + b * sum(x) once per group
+                    static_assert(!AFF || 16 % (2 * kWarps) == 0, "a warp's share of 16 or 32 chunks is whole pairs");
+                    const float2 *sbw = sbias + warp * kGpw * 8;
+                    const float *xsg = xsum + size_t(kg0 >> 1) * 16 + 2 * t;
+#pragma unroll(kUnrollG / 2)
+                    for (int gp = 0; gp < (ng >> 1); ++gp) {
+                        const int gl = g_lo + 2 * gp;        // first chunk of the pair, within the stage
+                        const uint8_t *p0 = rowr + (gl >> 3) * kSegBytes + (((gl & 7) ^ r) << 4);
+                        const uint8_t *p1 = rowr + ((gl + 1) >> 3) * kSegBytes + ((((gl + 1) & 7) ^ r) << 4);
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(p0);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p0 + 8 * 128);
+                        const uint32_t w2 = *reinterpret_cast<const uint32_t *>(p1);
+                        const uint32_t w3 = *reinterpret_cast<const uint32_t *>(p1 + 8 * 128);
+                        const float2 sc = sp[gp * 8 + r];
+                        const float2 bv = sbw[gp * 8 + r];
+                        uint32_t pa[4], pb[4], pc[4], pd[4];
+                        unpack_word_q_f16x2(w0, pa);
+                        unpack_word_q_f16x2(w1, pb);
+                        unpack_word_q_f16x2(w2, pc);
+                        unpack_word_q_f16x2(w3, pd);
+                        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+                        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+                        const uint32_t a2[4] = {pc[0], pd[0], pc[1], pd[1]};
+                        const uint32_t a3[4] = {pc[2], pd[2], pc[3], pd[3]};
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb) {
+                            const int m = r + 8 * nb;
+                            uint4 xv = make_uint4(0, 0, 0, 0), xw = make_uint4(0, 0, 0, 0);
+                            if (m < a.M) {
+                                const uint8_t *xq = xg + size_t(m) * xrow + 128 * gp;
+                                xv = *reinterpret_cast<const uint4 *>(xq);
+                                xw = *reinterpret_cast<const uint4 *>(xq + 64);
+                            }
+                            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                            float d[4];
+                            mma16816(d, a0, xv.x, xv.y, z);
+                            mma16816(d, a1, xv.z, xv.w, d);
+                            mma16816(d, a2, xw.x, xw.y, d);
+                            mma16816(d, a3, xw.z, xw.w, d);
+                            const float2 xs2 = *reinterpret_cast<const float2 *>(xsg + size_t(gp) * 16 + 8 * nb);
+                            acc[nb][0] = fmaf(bv.x, xs2.x, fmaf(sc.x, d[0], acc[nb][0]));
+                            acc[nb][1] = fmaf(bv.x, xs2.y, fmaf(sc.x, d[1], acc[nb][1]));
+                            acc[nb][2] = fmaf(bv.y, xs2.x, fmaf(sc.y, d[2], acc[nb][2]));
+                            acc[nb][3] = fmaf(bv.y, xs2.y, fmaf(sc.y, d[3], acc[nb][3]));
+                        }
+                    }
+                } else {
 #pragma unroll(kUnrollG)
                 for (int gi = 0; gi < ng; ++gi) {
                     const int gl = g_lo + gi;                // group within the stage
@@ -473,10 +524,7 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                     const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p + 8 * 128);
                     const float2 sc = sp[gi * 8 + r];
                     uint32_t pa[4], pb[4];
-                    if (AFF) {
-                        unpack_word_q_f16x2(w0, pa);
-                        unpack_word_q_f16x2(w1, pb);
-                    } else if (kUnpack == 0) {
+                    if (kUnpack == 0) {
                         unpack_word_f16x2(w0, pa);
                         unpack_word_f16x2(w1, pb);
                     } else {
@@ -503,21 +551,12 @@ __global__ void __launch_bounds__(kThreads) k_decode_tc(const __grid_constant__ 
                             e[0] = e[2] = ev.x;
                             e[1] = e[3] = ev.y;
                         }
-                        if (AFF) {
-                            // s sum(x q) + b sum(x) over the group's 32 columns
-                            const float2 bv = sbias[warp * kGpw * 8 + gi * 8 + r];
-                            const float2 xs2 = *reinterpret_cast<const float2 *>(xsum + size_t(kg0 + gi) * 16 + 8 * nb + 2 * t);
-                            acc[nb][0] = fmaf(bv.x, xs2.x, fmaf(sc.x, d[0], acc[nb][0]));
-                            acc[nb][1] = fmaf(bv.x, xs2.y, fmaf(sc.x, d[1], acc[nb][1]));
-                            acc[nb][2] = fmaf(bv.y, xs2.x, fmaf(sc.y, d[2], acc[nb][2]));
-                            acc[nb][3] = fmaf(bv.y, xs2.y, fmaf(sc.y, d[3], acc[nb][3]));
-                        } else {
-                            acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
-                            acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
-                            acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
-                            acc[nb][3] = fmaf(sc.y, d[3] - e[3], acc[nb][3]);
-                        }
+                        acc[nb][0] = fmaf(sc.x, d[0] - e[0], acc[nb][0]);
+                        acc[nb][1] = fmaf(sc.x, d[1] - e[1], acc[nb][1]);
+                        acc[nb][2] = fmaf(sc.y, d[2] - e[2], acc[nb][2]);
+                        acc[nb][3] = fmaf(sc.y, d[3] - e[3], acc[nb][3]);
                     }
+                }
                 }
             }
             __syncwarp();
