@@ -43,17 +43,20 @@ def test_affine_gate_up_matches_oracle(oracle, M, N2, K):
     assert_within(host_f16(h), h_ref, Sh, f"affine gate_up M={M} N2={N2} K={K}")
 
 
-def test_affine_one_hot_bit_exact(oracle):
+@pytest.mark.parametrize("K", [256, 1024])
+def test_affine_one_hot_bit_exact(oracle, K):
     """x = e_k returns f16(s q + b) exactly: scales and biases are multiples
-    of 2^-8 below 1, so s q + b is exact in fp32 and f16 rounds it once."""
-    N, K = 96, 256
-    rng = synth.rng_for("aff_onehot")
+    of 2^-8 below 1, so s q + b is exact in fp32 and f16 rounds it once
+    (K = 256: the CUDA-core kernel; K = 1024: the tensor-core kernel, whose
+    64-column group sums x q and x exactly when x is one-hot)."""
+    N = 96
+    rng = synth.rng_for("aff_onehot", K)
     wq = synth.packed_codes(rng, N, K)
     sc = (rng.integers(1, 64, (N, K // 64)) / 256.0).astype(np.float16)
     bi = (rng.integers(-255, 256, (N, K // 64)) / 256.0).astype(np.float16)
     w = oracle.dequant_affine(wq, sc, bi, N, K)
     from int4_weight_only_q4f16_gb300 import zq4
-    for k in (0, 7, 63, 64, 130, 255):
+    for k in (0, 7, 63, 64, 130, 255, K - 1):
         x = np.zeros((1, K), np.float16)
         x[0, k] = 1.0
         y = host_f16(zq4.gemv_affine(dev(wq), dev(sc), dev(bi), dev(x), N, K))
