@@ -302,7 +302,8 @@ zq4_status zq4_gemv_affine(const uint32_t *wq, const uint16_t *scales, const uin
 {
     const zq4_status st = affine_common(wq, scales, biases, x, y, M, N, K, size_t(M > 0 ? M : 0) * (N > 0 ? N : 0) * 2);
     if (st != ZQ4_OK) return st;
-    if (decode_tc_affine_supported(M, K))
+    // the tensor-core kernel reads scales and biases through tensor maps (16-byte bases)
+    if (aligned16(scales) && aligned16(biases) && decode_tc_affine_supported(M, K))
         return cuda_status(launch_decode_tc_affine(wq, scales, biases, x, y, M, N, K, false,
                                                    static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_decode(wq, scales, biases, x, y, M, N, K, false, static_cast<cudaStream_t>(stream)));
@@ -315,7 +316,7 @@ zq4_status zq4_gate_up_silu_affine(const uint32_t *wq, const uint16_t *scales, c
     const zq4_status st =
         affine_common(wq, scales, biases, x, h, M, N2, K, size_t(M > 0 ? M : 0) * (N2 > 0 ? N2 / 2 : 0) * 2);
     if (st != ZQ4_OK) return st;
-    if (decode_tc_affine_supported(M, K))
+    if (aligned16(scales) && aligned16(biases) && decode_tc_affine_supported(M, K))
         return cuda_status(launch_decode_tc_affine(wq, scales, biases, x, h, M, N2, K, true,
                                                    static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_decode(wq, scales, biases, x, h, M, N2, K, true, static_cast<cudaStream_t>(stream)));

@@ -43,6 +43,35 @@ def test_affine_gate_up_matches_oracle(oracle, M, N2, K):
     assert_within(host_f16(h), h_ref, Sh, f"affine gate_up M={M} N2={N2} K={K}")
 
 
+def _offset_by_one(a):
+    """a copy of f16 array a on the device whose first element sits 2 bytes
+    past an allocation's (16-byte aligned) start"""
+    buf = torch.zeros(a.size + 1, dtype=torch.float16, device="cuda")
+    buf[1:] = torch.from_numpy(np.ascontiguousarray(a).reshape(-1)).cuda()
+    return buf[1:]
+
+
+@pytest.mark.parametrize("gate_up", [False, True])
+def test_affine_scales_on_2_byte_boundaries(oracle, gate_up):
+    """Scales and biases need only 2-byte alignment: at K = 1024 (a shape the
+    tensor-core kernel takes when they are 16-byte aligned) the call runs the
+    CUDA-core kernel and still matches the oracle."""
+    from int4_weight_only_q4f16_gb300 import zq4
+    M, N, K = 3, 160, 1024
+    wq, sc, bi = _affine_weight("aff_odd", N, K)
+    x = synth.activations(synth.rng_for("aff_oddx", M, K), M, K)
+    s2, b2 = _offset_by_one(sc), _offset_by_one(bi)
+    assert s2.data_ptr() % 16 == 2 and b2.data_ptr() % 16 == 2
+    if gate_up:
+        out = zq4.gate_up_silu_affine(dev(wq), s2, b2, dev(x), N, K)
+        ref, S = oracle.gate_up_silu_affine(wq, sc, bi, x, N, K)
+    else:
+        out = zq4.gemv_affine(dev(wq), s2, b2, dev(x), N, K)
+        ref, S = oracle.gemv_affine(wq, sc, bi, x, N, K)
+    assert_within(host_f16(out), ref, S, f"affine, 2-byte aligned scales, gate_up={gate_up}")
+    assert zq4.device_errors(clear=True) == 0
+
+
 @pytest.mark.parametrize("K", [256, 1024])
 def test_affine_one_hot_bit_exact(oracle, K):
     """x = e_k returns f16(s q + b) exactly: scales and biases are multiples
