@@ -147,12 +147,12 @@ ZQ4_API zq4_status zq4_gate_up_silu(const uint32_t *wq, const uint16_t *scales, 
  *   x [M, K] f16         y [M, N] f16 (h [M, N2/2] for gate_up, rows
  *                        interleaved as in zq4_gate_up_silu)
  * Per 64-weight group the product is s * sum(x q) + b * sum(x), fp32.
- * M >= 1 (blocks of up to 8 tokens per launch), N >= 1 (N2 even), K a
- * multiple of 64. The tensor-core kernel runs when K is a multiple of 512
- * and scales and biases start on 16-byte boundaries (blocks of up to 16
- * tokens); other calls run the CUDA-core kernel, with the same results
- * up to fp32 summation order. wq and x 16-byte aligned, scales, biases and the output
- * 2-byte aligned; the output must not overlap any input. Device pointers,
+ * M >= 1, N >= 1 (N2 even), K a multiple of 64. The tensor-core kernel
+ * runs when K is a multiple of 512 and scales and biases start on 16-byte
+ * boundaries (blocks of up to 16 tokens per launch); other calls run the
+ * CUDA-core kernel (blocks of up to 8 tokens), with the same results up to
+ * fp32 summation order. wq and x 16-byte aligned, scales, biases and the
+ * output 2-byte aligned; the output must not overlap any input. Device pointers,
  * caller-owned. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
  * ZQ4_ERR_OVERLAP, ZQ4_ERR_UNSUPPORTED (x of K does not fit in shared
  * memory), ZQ4_ERR_CUDA.
