@@ -102,9 +102,11 @@ ZQ4_API zq4_status zq4_device_errors(uint32_t *flags, int clear);
  *
  * M >= 1 (1..16 run the decode GEMV kernels; M >= 64 the tensor-core GEMM
  * that dequantizes tiles into shared memory; 17..63 the decode kernels in
- * blocks of 16 rows), N >= 1, K a multiple of 32. y must not overlap wq,
- * scales or x. Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN,
- * ZQ4_ERR_OVERLAP, ZQ4_ERR_CUDA.
+ * blocks of 16 rows), N >= 1, K a multiple of 32. wq, scales and x
+ * 16-byte aligned, y 2-byte aligned; y must not overlap wq, scales or x.
+ * Errors: ZQ4_ERR_NULL, ZQ4_ERR_SHAPE, ZQ4_ERR_ALIGN, ZQ4_ERR_OVERLAP,
+ * ZQ4_ERR_UNSUPPORTED (M < 64 and a row of x, 2K bytes, larger than the
+ * decode kernels can stage in shared memory), ZQ4_ERR_CUDA.
  */
 ZQ4_API zq4_status zq4_gemv(const uint32_t *wq, const uint16_t *scales, const uint16_t *x,
                     uint16_t *y, int M, int N, int K, void *stream);
