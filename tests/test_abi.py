@@ -178,6 +178,49 @@ def test_qkv_rope_host_checks(lib):
     assert f(*args) == lib.ZQ4_ERR_OVERLAP        # k and v caches the same
 
 
+def test_moe_block_work_bytes_follow_the_documented_layout(lib):
+    """The header's layout: 3 P + 3 int32 of grouping padded to 256 bytes,
+    h [P, I] f16 padded to 256 bytes, z [P, D] fp32 (P = T top_k)."""
+    def pad(n):
+        return (n + 255) // 256 * 256
+    for T, top_k, D, I in ((1, 8, 2048, 512), (16, 8, 2048, 512), (3, 5, 256, 768), (32, 8, 4096, 1536)):
+        P = T * top_k
+        assert lib.moe_block_work_bytes(T, top_k, D, I) == pad(4 * (3 * P + 3)) + pad(2 * P * I) + 4 * P * D
+    for bad in ((0, 8, 256, 256), (1, 0, 256, 256), (1, 8, 0, 256), (1, 8, 256, -1)):
+        assert lib.moe_block_work_bytes(*bad) == 0
+
+
+@host_checks_only
+def test_moe_block_host_checks(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000
+    Dn, X, Y, ids, r, W = (A + (i << 30) for i in range(1, 7))
+    T, top_k, D, I = 2, 8, 256, 512
+    wb = lib.moe_block_work_bytes(T, top_k, D, I)
+    f = lib.lib.zq4_moe_block
+    ok = [P(A), P(Dn), 16, P(X), P(Y), T, D, I, P(ids), P(r), top_k, P(W), wb, P(0), P(0)]
+
+    def call(**change):
+        args = list(ok)
+        for i, v in change.items():
+            args[int(i[1:])] = v
+        return f(*args)
+    for i in (0, 1, 3, 4, 8, 9, 11):
+        assert call(**{f"a{i}": P(0)}) == lib.ZQ4_ERR_NULL, i
+    assert call(a2=0) == lib.ZQ4_ERR_SHAPE                       # no experts
+    assert call(a5=0) == lib.ZQ4_ERR_SHAPE                       # no tokens
+    assert call(a10=33) == lib.ZQ4_ERR_SHAPE                     # top_k above 32
+    assert call(a6=320) == lib.ZQ4_ERR_SHAPE                     # D not a multiple of 256
+    assert call(a7=192) == lib.ZQ4_ERR_SHAPE                     # I not a multiple of 256
+    assert call(a5=33) == lib.ZQ4_ERR_UNSUPPORTED                # 264 pairs
+    assert call(a12=wb - 1) == lib.ZQ4_ERR_SHAPE                 # scratch too small
+    assert call(a0=P(A + 4)) == lib.ZQ4_ERR_ALIGN
+    assert call(a11=P(W + 8)) == lib.ZQ4_ERR_ALIGN               # work 16-byte aligned
+    assert call(a8=P(ids + 2)) == lib.ZQ4_ERR_ALIGN
+    assert call(a4=P(X + 32)) == lib.ZQ4_ERR_OVERLAP             # y over x
+    assert call(a11=P(r)) == lib.ZQ4_ERR_OVERLAP                 # work over the router weights
+
+
 def test_header_is_plain_c_and_a_c_program_links(lib):
     """include/zq4.h compiles as strict C99 (no C++ in the boundary), every
     declared entry point resolves when a C program links libzq4.so, and the
