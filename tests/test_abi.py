@@ -268,6 +268,99 @@ int main(void)
     assert r.stdout.split() == [str(len(syms)), "0"]
 
 
+def test_binding_structs_match_the_header_layout(lib):
+    """The binding's ctypes mirrors of zq4_stack_job and zq4_stack_plan have
+    the C compiler's size and field offsets for include/zq4.h."""
+    import ctypes
+    import shutil
+    import subprocess
+    from int4_weight_only_q4f16_gb300 import build
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    mirrors = {"zq4_stack_job": lib.StackJob, "zq4_stack_plan": lib.StackPlanC}
+    lines = []
+    for cname, py in mirrors.items():
+        lines.append(f'    printf("{cname} size %lu\\n", (unsigned long)sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'    printf("{cname} {field} %lu\\n", (unsigned long)offsetof({cname}, {field}));')
+    out_dir = os.path.join(build.BUILD, "c_abi_check")
+    os.makedirs(out_dir, exist_ok=True)
+    src, exe = os.path.join(out_dir, "c_layout.c"), os.path.join(out_dir, "c_layout")
+    with open(src, "w") as f:
+        f.write("#include <stddef.h>\n#include <stdio.h>\n#include \"zq4.h\"\n\nint main(void)\n{\n" +
+                "\n".join(lines) + "\n    return 0;\n}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0
+    got = {}
+    for line in r.stdout.split("\n"):
+        if line:
+            cname, field, v = line.split()
+            got[(cname, field)] = int(v)
+    for cname, py in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert got[(cname, field)] == getattr(py, field).offset, (cname, field)
+
+
+def test_host_only_calls(lib):
+    """Calls that never touch a device: the segmented layout's size (one
+    2304-byte segment per 16-row tile and 256-column block) and the plan's
+    wait limit (0 restores the 2 s default)."""
+    import ctypes
+    sb = lib.lib.zq4_segmented_bytes
+    for N, K in ((1, 256), (16, 256), (17, 512), (3072, 3072), (32064, 3072)):
+        assert sb(N, K) == (N + 15) // 16 * (K // 256) * 2304, (N, K)
+    for N, K in ((0, 256), (16, 128), (16, 0), (-1, 256)):
+        assert sb(N, K) == 0, (N, K)
+    plan = lib.StackPlanC()
+    f = lib.lib.zq4_stack_plan_set_wait_limit
+    assert f(None, 5) == lib.ZQ4_ERR_NULL
+    assert f(ctypes.byref(plan), 5_000_000) == lib.ZQ4_OK and plan.wait_ns == 5_000_000
+    assert f(ctypes.byref(plan), 0) == lib.ZQ4_OK and plan.wait_ns == 2_000_000_000
+    nbytes = ctypes.c_size_t(0)
+    job = lib.StackJob()
+    assert lib.lib.zq4_stack_plan_bytes(ctypes.byref(job), 1, 1, None) == lib.ZQ4_ERR_NULL
+    assert lib.lib.zq4_stack_plan_bytes(None, 1, 1, ctypes.byref(nbytes)) == lib.ZQ4_ERR_NULL
+    assert lib.lib.zq4_stack_plan_bytes(ctypes.byref(job), 0, 1, ctypes.byref(nbytes)) == lib.ZQ4_ERR_SHAPE
+
+
+@host_checks_only
+def test_argmax_and_segmented_host_checks(lib):
+    P = ctypes.c_void_p
+    A = 0x7F0000000000
+    S, X, Y32, Ix, Mx, W = (A + (i << 30) for i in range(1, 7))
+    am = lib.lib.zq4_gemv_argmax
+    ok = [P(A), P(S), P(X), P(Y32), P(Ix), P(Mx), P(W), 1, 64, 256, P(0)]
+
+    def call(f, base, **change):
+        args = list(base)
+        for i, v in change.items():
+            args[int(i[1:])] = v
+        return f(*args)
+    for i in (2, 4, 6):
+        assert call(am, ok, **{f"a{i}": P(0)}) == lib.ZQ4_ERR_NULL, i
+    assert call(am, ok, a7=0) == lib.ZQ4_ERR_SHAPE
+    assert call(am, ok, a7=65) == lib.ZQ4_ERR_SHAPE              # at most 64 tokens
+    assert call(am, ok, a2=P(X + 2)) == lib.ZQ4_ERR_ALIGN
+    assert call(am, ok, a4=P(Ix + 2)) == lib.ZQ4_ERR_ALIGN
+    assert call(am, ok, a6=P(W + 4)) == lib.ZQ4_ERR_ALIGN          # keys 8-byte aligned
+    for f, gate_up in ((lib.lib.zq4_gemv_seg, False), (lib.lib.zq4_gate_up_silu_seg, True)):
+        base = [P(A), P(X), P(Y32), 1, 64, 256, P(0)]
+        assert call(f, base, a0=P(0)) == lib.ZQ4_ERR_NULL
+        assert call(f, base, a2=P(0)) == lib.ZQ4_ERR_NULL
+        assert call(f, base, a5=128) == lib.ZQ4_ERR_SHAPE          # K % 256
+        assert call(f, base, a3=0) == lib.ZQ4_ERR_SHAPE
+        assert call(f, base, a0=P(A + 4)) == lib.ZQ4_ERR_ALIGN
+        assert call(f, base, a1=P(X + 2)) == lib.ZQ4_ERR_ALIGN
+        assert call(f, base, a2=P(Y32 + 1)) == lib.ZQ4_ERR_ALIGN
+        if gate_up:
+            assert call(f, base, a4=63) == lib.ZQ4_ERR_SHAPE
+
+
 def test_binding_fails_loudly_without_the_library():
     """No CPU fallback: with libzq4.so absent, importing the binding (and the
     decode-stack driver that uses it) raises ImportError."""
